@@ -1,0 +1,168 @@
+"""ORACLE — test infrastructure only.
+
+A plain, slow fp64 CPU statement of the MSA forward path (``msa_oracle.c``),
+loaded through ctypes.  Only the tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the product library
+never does, and the two share no code.  Inputs are bf16 bit patterns
+(``uint16`` numpy arrays); outputs are float64 / int32 numpy arrays.
+
+Every function states the passage it follows in ``msa_oracle.c``.  All parts
+are pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_pins.py``
+(brute-force token scoring, an independent sort, the textbook dense attention
+and masked attention of ``torch``, a stable argsort, hand-worked cases and
+invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SO = os.path.join(_HERE, "libmsa_oracle.so")
+_lib = None
+
+
+def build():
+    """Compile the oracle with gcc (plain C, no GPU)."""
+    src = os.path.join(_HERE, "msa_oracle.c")
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c99", "-o", _SO, src, "-lm"]
+    p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+    if p.returncode != 0:
+        raise RuntimeError("oracle build failed:\n" + p.stdout.decode())
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_SO):
+            build()
+        lib = ctypes.CDLL(_SO)
+        P, I64, I, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        lib.msa_ref_block_scores.argtypes = [P, P, P, I64, I64, I, I, I, P, I]
+        lib.msa_ref_select_blocks.argtypes = [P, P, P, I64, I64, I, I, I, I, P, P, I]
+        lib.msa_ref_invert_blocks.argtypes = [P, I64, I, I, I, P, P, P]
+        lib.msa_ref_sparse_attn.argtypes = [P, P, P, P, P, I64, I64, I, I, I, I, I, D, P, P, I]
+        lib.msa_ref_dense_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, D, P, P, I]
+        lib.msa_ref_decode.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, I, I, D, P, P, P, P, I]
+        for f in ("msa_ref_block_scores", "msa_ref_select_blocks", "msa_ref_invert_blocks",
+                  "msa_ref_sparse_attn", "msa_ref_dense_attn", "msa_ref_decode"):
+            getattr(lib, f).restype = I
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else None
+
+
+def _u16(a):
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def _i64(a):
+    return np.ascontiguousarray(a, dtype=np.int64)
+
+
+def threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise RuntimeError("%s failed with status %d" % (name, rc))
+
+
+def block_scores(q_idx_rows, k_idx, rows, N, Bk, n_threads=None):
+    """S[r, g, b] = max_{j in b, j <= t_r} q^I.k^I_j / sqrt(d_I) (-inf past local(t)).
+
+    "MSA" study note, 2-3 "Fixed attention budget" (equations for s and S)."""
+    q_idx_rows, k_idx, rows = _u16(q_idx_rows), _u16(k_idx), _i64(rows)
+    n_rows, G, d_I = q_idx_rows.shape
+    nb = (N + Bk - 1) // Bk
+    S = np.empty((n_rows, G, nb), np.float64)
+    _check(_load().msa_ref_block_scores(_p(q_idx_rows), _p(k_idx), _p(rows), n_rows, N, G, d_I, Bk, _p(S),
+                                        n_threads or threads()), "msa_ref_block_scores")
+    return S
+
+
+def select_blocks(q_idx_rows, k_idx, rows, N, Bk, k, n_threads=None):
+    """block_idx[g, r, :] (slot 0 local, then descending score, -1 padding) and
+    kth[g, r, :] = (last taken, first left out) non-local block scores.
+
+    "MSA" study note 2-3 / 3-4 / 3-5; chipsbuilder "Che cos'é MSA"; Flash-MSA
+    "プロキシアテンション" (local block pinned to +inf)."""
+    q_idx_rows, k_idx, rows = _u16(q_idx_rows), _u16(k_idx), _i64(rows)
+    n_rows, G, d_I = q_idx_rows.shape
+    blk = np.empty((G, n_rows, k), np.int32)
+    kth = np.empty((G, n_rows, 2), np.float64)
+    _check(_load().msa_ref_select_blocks(_p(q_idx_rows), _p(k_idx), _p(rows), n_rows, N, G, d_I, Bk, k, _p(blk),
+                                         _p(kth), n_threads or threads()), "msa_ref_select_blocks")
+    return blk, kth
+
+
+def invert_blocks(block_idx, Bk):
+    """CSR B* per group: row_ptr [G, nb+1], entries [G, N*k] (t*k+slot, ascending t), n_entries [G].
+
+    Flash-MSA "バックワードパス" (B -> B*)."""
+    block_idx = np.ascontiguousarray(block_idx, np.int32)
+    G, N, k = block_idx.shape
+    nb = (N + Bk - 1) // Bk
+    row_ptr = np.empty((G, nb + 1), np.int32)
+    entries = np.full((G, N * k), -1, np.int32)
+    n_entries = np.empty(G, np.int32)
+    _check(_load().msa_ref_invert_blocks(_p(block_idx), N, G, Bk, k, _p(row_ptr), _p(entries), _p(n_entries)),
+           "msa_ref_invert_blocks")
+    return row_ptr, entries, n_entries
+
+
+def sparse_attn(q_rows, K, V, block_idx_rows, rows, Bk, scale, n_threads=None):
+    """out [n_rows, H_q, d] and lse [n_rows, H_q] over each row's selected blocks' tokens j <= t.
+
+    "MSA" study note 2-3 (Attn over K_{g,B}, V_{g,B}) and 3-3 "Main Branch"."""
+    q_rows, K, V, rows = _u16(q_rows), _u16(K), _u16(V), _i64(rows)
+    block_idx_rows = np.ascontiguousarray(block_idx_rows, np.int32)
+    n_rows, H_q, d = q_rows.shape
+    N, H_kv, _ = K.shape
+    k = block_idx_rows.shape[2]
+    out = np.empty((n_rows, H_q, d), np.float64)
+    lse = np.empty((n_rows, H_q), np.float64)
+    _check(_load().msa_ref_sparse_attn(_p(q_rows), _p(K), _p(V), _p(block_idx_rows), _p(rows), n_rows, N, H_q,
+                                       H_kv, d, Bk, k, float(scale), _p(out), _p(lse), n_threads or threads()),
+           "msa_ref_sparse_attn")
+    return out, lse
+
+
+def dense_attn(q_rows, K, V, rows, scale, n_threads=None):
+    """Dense causal GQA attention ("MSA" study note 1-1)."""
+    q_rows, K, V, rows = _u16(q_rows), _u16(K), _u16(V), _i64(rows)
+    n_rows, H_q, d = q_rows.shape
+    N, H_kv, _ = K.shape
+    out = np.empty((n_rows, H_q, d), np.float64)
+    lse = np.empty((n_rows, H_q), np.float64)
+    _check(_load().msa_ref_dense_attn(_p(q_rows), _p(K), _p(V), _p(rows), n_rows, N, H_q, H_kv, d, float(scale),
+                                      _p(out), _p(lse), n_threads or threads()), "msa_ref_dense_attn")
+    return out, lse
+
+
+def decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, Bk, k, scale, n_threads=None):
+    """One decode step: out [B,H_q,d], lse [B,H_q], block_idx [B,G,k], kth [B,G,2].
+
+    velog llama.cpp analysis, section 2 (scan the whole index-key cache, read
+    only the selected K/V blocks)."""
+    q_t, q_idx_t, k_idx_cache = _u16(q_t), _u16(q_idx_t), _u16(k_idx_cache)
+    k_cache, v_cache, ctx_len = _u16(k_cache), _u16(v_cache), _i64(ctx_len)
+    B, H_q, d = q_t.shape
+    _, G, d_I = q_idx_t.shape
+    ctx_max = k_idx_cache.shape[1]
+    H_kv = k_cache.shape[2]
+    out = np.empty((B, H_q, d), np.float64)
+    lse = np.empty((B, H_q), np.float64)
+    blk = np.empty((B, G, k), np.int32)
+    kth = np.empty((B, G, 2), np.float64)
+    _check(_load().msa_ref_decode(_p(q_t), _p(q_idx_t), _p(k_idx_cache), _p(k_cache), _p(v_cache), _p(ctx_len), B,
+                                  ctx_max, H_q, H_kv, d, d_I, Bk, k, float(scale), _p(out), _p(lse), _p(blk),
+                                  _p(kth), n_threads or threads()), "msa_ref_decode")
+    return out, lse, blk, kth

@@ -1,0 +1,467 @@
+/*
+ * ORACLE — test infrastructure only.  Plain, slow fp64 CPU statement of the
+ * MiniMax Sparse Attention (MSA) forward path.  Only the tests, the smoke
+ * check and the benchmark's CPU-baseline leg may load this library; the
+ * product path never does.  It shares no code with the CUDA library.
+ *
+ * Sources (page titles and sections):
+ *   [P1] "MSA" study note (dimensionstp.github.io), 1-1 "Full attention의 병목"
+ *        (dense causal GQA softmax, scale 1/sqrt(d_h)); 2-1 "Two-branch sparse
+ *        attention" (the four steps); 2-3 "Fixed attention budget" (equations
+ *        for s, S and the selected set; Bk = 128, k = 16 including the local
+ *        block -> at most 2048 keys); 3-2 "Index Branch" (max-pooling of the
+ *        causally visible token scores); 3-3 "Main Branch" (exact softmax over
+ *        the selected support, per-head weights, group-shared selection); 3-4
+ *        "Forced local block"; 3-5 "GPU kernel co-design" (exp-free top-k;
+ *        LSE saved).
+ *   [P2] "MSA: un nuovo approccio all'attenzione sparsa" (chipsbuilder.com),
+ *        "Che cos'é MSA" (k = 16 blocks incl. the query's block, kBk = 2048)
+ *        and "Funzionamento Delle Due Branch" (one index query head per GQA
+ *        group, one shared index key head; causally visible tokens).
+ *   [P3] "MiniMax M3의 Sparse Attention 구조 및 llama.cpp 구현 제약 분석"
+ *        (velog.io), section 2 (decode: the whole index-key cache is scanned,
+ *        only the selected K/V blocks are read).
+ *   [P4] "Flash-MSA" (hackernews.jp translation), "フォワードパス" / "プロキシ
+ *        アテンション" (top-k on raw scores while streaming keys; the local
+ *        block's score set to +inf; main LSE saved) and "バックワードパス"
+ *        (the block->query inversion B -> B*).
+ *
+ * Readings where the pages leave a step open:
+ *   - k counts the local block: the set is {local(t)} plus the (k-1)
+ *     highest-scoring blocks b < local(t) ([P1] 2-3, [P2], [P4] +inf pin);
+ *   - fewer than k-1 earlier blocks: all of them are taken (set size
+ *     min(k, local(t)+1)); unused slots hold -1;
+ *   - equal block scores: the lower block index wins;
+ *   - slot 0 = local(t), then descending score (ties by ascending block);
+ *   - lse is the natural-log log-sum-exp of the scaled main scores;
+ *   - decode: the query sits at position ctx_len-1 and its keys are already
+ *     in the caches.
+ *
+ * Arithmetic: bf16 inputs widened exactly to double; every dot product,
+ * maximum, exponential and sum in double.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+#define ORACLE_NO_MEM 2
+
+/* ------------------------------------------------------------------ helpers */
+static double bf16_to_double(uint16_t h) {
+  union { uint32_t u; float f; } c;
+  c.u = (uint32_t)h << 16;
+  return (double)c.f;
+}
+
+static double dot_bf16(const uint16_t* a, const uint16_t* b, int n) {
+  double s = 0.0;
+  for (int i = 0; i < n; ++i) s += bf16_to_double(a[i]) * bf16_to_double(b[i]);
+  return s;
+}
+
+typedef struct {
+  int64_t lo, hi;
+  void* ctx;
+  void (*fn)(int64_t, void*);
+} range_t;
+
+static void* range_main(void* p) {
+  range_t* r = (range_t*)p;
+  for (int64_t i = r->lo; i < r->hi; ++i) r->fn(i, r->ctx);
+  return NULL;
+}
+
+/* Runs fn(i) for i in [0, n) over n_threads threads (interleaved chunks). */
+static void parallel_for(int64_t n, int n_threads, void (*fn)(int64_t, void*), void* ctx) {
+  if (n_threads < 1) n_threads = 1;
+  if (n_threads > 512) n_threads = 512;
+  if ((int64_t)n_threads > n) n_threads = (int)(n > 0 ? n : 1);
+  pthread_t th[512];
+  range_t rg[512];
+  for (int i = 0; i < n_threads; ++i) {
+    rg[i].lo = n * i / n_threads;
+    rg[i].hi = n * (i + 1) / n_threads;
+    rg[i].ctx = ctx;
+    rg[i].fn = fn;
+  }
+  for (int i = 1; i < n_threads; ++i) pthread_create(&th[i], NULL, range_main, &rg[i]);
+  range_main(&rg[0]);
+  for (int i = 1; i < n_threads; ++i) pthread_join(th[i], NULL);
+}
+
+/* ------------------------------------------------- step 1: block scores S */
+/*
+ * [P1] 2-3: s_{t,g,j} = q^I_{t,g} . k^I_j / sqrt(d_I) and
+ * S_{t,g,b} = max over j in block b with j <= t of s_{t,g,j}.
+ * Blocks past local(t) have no visible token: S = -inf there.
+ */
+static void block_scores_row(const uint16_t* qrow /*[d_I]*/, const uint16_t* k_idx, int64_t t,
+                             int d_I, int Bk, int64_t nb, double* S /*[nb]*/) {
+  double inv = 1.0 / sqrt((double)d_I);
+  double q[512];
+  for (int c = 0; c < d_I; ++c) q[c] = bf16_to_double(qrow[c]);
+  for (int64_t b = 0; b < nb; ++b) S[b] = -INFINITY;
+  /* four keys at a time: four independent dot products, each summed in order */
+  int64_t j = 0;
+  for (; j + 3 <= t; j += 4) {
+    const uint16_t *k0 = k_idx + j * d_I, *k1 = k0 + d_I, *k2 = k1 + d_I, *k3 = k2 + d_I;
+    double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+    for (int c = 0; c < d_I; ++c) {
+      s0 += q[c] * bf16_to_double(k0[c]);
+      s1 += q[c] * bf16_to_double(k1[c]);
+      s2 += q[c] * bf16_to_double(k2[c]);
+      s3 += q[c] * bf16_to_double(k3[c]);
+    }
+    double s[4] = {s0 * inv, s1 * inv, s2 * inv, s3 * inv};
+    for (int i = 0; i < 4; ++i) {
+      int64_t b = (j + i) / Bk;
+      if (s[i] > S[b]) S[b] = s[i];
+    }
+  }
+  for (; j <= t; ++j) {
+    double s = dot_bf16(qrow, k_idx + j * d_I, d_I) * inv;
+    int64_t b = j / Bk;
+    if (s > S[b]) S[b] = s;
+  }
+}
+
+/*
+ * Step 2 ([P1] 2-3, 3-4, 3-5; [P4] +inf pin): slot 0 = local(t); then the
+ * k-1 largest S over b < local(t), ties to the lower b, in descending order;
+ * then -1.  kth[0], kth[1] = the (k-1)-th and k-th largest non-local scores
+ * (the last taken and the first left out), +inf/-inf when no block is left
+ * out.
+ */
+static void topk_row(const double* S, int64_t t, int Bk, int k, int32_t* out /*[k]*/,
+                     double* kth /*[2] or NULL*/, unsigned char* taken /*[nb] scratch*/) {
+  int64_t local = t / Bk;
+  for (int i = 0; i < k; ++i) out[i] = -1;
+  out[0] = (int32_t)local;
+  for (int64_t b = 0; b < local; ++b) taken[b] = 0;
+  double last = INFINITY;
+  int n_take = (int)((local < (int64_t)(k - 1)) ? local : (int64_t)(k - 1));
+  for (int i = 0; i < n_take; ++i) {
+    int64_t best = -1;
+    for (int64_t b = 0; b < local; ++b) {
+      if (taken[b]) continue;
+      if (best < 0 || S[b] > S[best]) best = b; /* strict: the lower b keeps a tie */
+    }
+    taken[best] = 1;
+    out[1 + i] = (int32_t)best;
+    last = S[best];
+  }
+  if (kth) {
+    double next = -INFINITY;
+    for (int64_t b = 0; b < local; ++b)
+      if (!taken[b] && S[b] > next) next = S[b];
+    kth[0] = (n_take > 0) ? last : INFINITY;
+    kth[1] = next;
+  }
+}
+
+typedef struct {
+  const uint16_t* q_idx_rows; /* [n_rows, G, d_I] */
+  const uint16_t* k_idx;      /* [N, d_I] */
+  const int64_t* rows;
+  int64_t n_rows, N, nb;
+  int G, d_I, Bk, k;
+  double* S;        /* [n_rows, G, nb] or NULL */
+  int32_t* blk;     /* [G, n_rows, k] or NULL */
+  double* kth;      /* [G, n_rows, 2] or NULL */
+  int status;
+} select_ctx;
+
+static void select_item(int64_t it, void* p) {
+  select_ctx* c = (select_ctx*)p;
+  int64_t r = it / c->G;
+  int g = (int)(it % c->G);
+  int64_t t = c->rows[r];
+  double* S = c->S ? c->S + (r * c->G + g) * c->nb : (double*)malloc(sizeof(double) * (size_t)c->nb);
+  unsigned char* taken = (unsigned char*)malloc((size_t)c->nb + 1);
+  if (!S || !taken) {
+    c->status = ORACLE_NO_MEM;
+    if (!c->S) free(S);
+    free(taken);
+    return;
+  }
+  block_scores_row(c->q_idx_rows + (r * c->G + g) * c->d_I, c->k_idx, t, c->d_I, c->Bk, c->nb, S);
+  if (c->blk)
+    topk_row(S, t, c->Bk, c->k, c->blk + ((int64_t)g * c->n_rows + r) * c->k,
+             c->kth ? c->kth + ((int64_t)g * c->n_rows + r) * 2 : NULL, taken);
+  if (!c->S) free(S);
+  free(taken);
+}
+
+/*
+ * Block scores S for the listed query positions (rows[r] = t).
+ * q_idx_rows holds the index-query rows of those positions only.
+ */
+int msa_ref_block_scores(const uint16_t* q_idx_rows, const uint16_t* k_idx, const int64_t* rows,
+                         int64_t n_rows, int64_t N, int G, int d_I, int Bk, double* S, int n_threads) {
+  if (!q_idx_rows || !k_idx || !rows || !S || N <= 0 || G <= 0 || d_I <= 0 || d_I > 512 || Bk <= 0)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  select_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, 0, S, NULL, NULL, 0};
+  parallel_for(n_rows * G, n_threads, select_item, &c);
+  return c.status;
+}
+
+/* Selected block sets block_idx[g, r, :] for the listed positions. */
+int msa_ref_select_blocks(const uint16_t* q_idx_rows, const uint16_t* k_idx, const int64_t* rows,
+                          int64_t n_rows, int64_t N, int G, int d_I, int Bk, int k, int32_t* block_idx,
+                          double* kth, int n_threads) {
+  if (!q_idx_rows || !k_idx || !rows || !block_idx || N <= 0 || G <= 0 || d_I <= 0 || d_I > 512 || Bk <= 0 ||
+      k < 1)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  select_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, k, NULL, block_idx, kth, 0};
+  parallel_for(n_rows * G, n_threads, select_item, &c);
+  return c.status;
+}
+
+/* ----------------------------------------------- step 3: B -> B* inversion */
+/*
+ * [P4] "バックワードパス": B[g, t, slot] -> block becomes B*[g, block] -> the
+ * (t, slot) pairs that chose it.  CSR per group: entries of block b are
+ * entries[g*N*k + row_ptr[g*(nb+1) + b] ...], each t*k + slot, ascending t.
+ * Ids outside [0, nb) and -1 are not listed.
+ */
+int msa_ref_invert_blocks(const int32_t* block_idx, int64_t N, int G, int Bk, int k, int32_t* row_ptr,
+                          int32_t* entries, int32_t* n_entries) {
+  if (!block_idx || !row_ptr || !entries || !n_entries || N <= 0 || G <= 0 || Bk <= 0 || k < 1)
+    return ORACLE_BAD_ARG;
+  int64_t nb = (N + Bk - 1) / Bk;
+  for (int g = 0; g < G; ++g) {
+    const int32_t* B = block_idx + (int64_t)g * N * k;
+    int32_t* rp = row_ptr + (int64_t)g * (nb + 1);
+    int32_t* E = entries + (int64_t)g * N * k;
+    for (int64_t b = 0; b <= nb; ++b) rp[b] = 0;
+    for (int64_t e = 0; e < N * k; ++e)
+      if (B[e] >= 0 && B[e] < nb) rp[B[e] + 1] += 1;
+    for (int64_t b = 0; b < nb; ++b) rp[b + 1] += rp[b];
+    n_entries[g] = rp[nb];
+    /* fill each block's list by scanning (t, slot) in increasing order */
+    int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * (size_t)(nb + 1));
+    if (!cursor) return ORACLE_NO_MEM;
+    for (int64_t b = 0; b < nb; ++b) cursor[b] = rp[b];
+    for (int64_t e = 0; e < N * k; ++e) {
+      int32_t b = B[e];
+      if (b >= 0 && b < nb) E[cursor[b]++] = (int32_t)e;
+    }
+    free(cursor);
+  }
+  return ORACLE_OK;
+}
+
+/* --------------------------------------- step 4: attention over a key set */
+/*
+ * [P1] 1-1 and 3-3: out = softmax(scale * q K_J^T) V_J over the key set J,
+ * lse = log sum_j exp(scale q.k_j) ([P1] 3-5 item 4, [P4] main LSE).
+ * An empty J gives out = 0 and lse = -inf.
+ */
+static void attend_set(const uint16_t* q /*[d]*/, const uint16_t* K, const uint16_t* V, int64_t kv_stride,
+                       const int64_t* J, int64_t nJ, int d, double scale, double* out, double* lse,
+                       double* z /*[nJ] scratch*/) {
+  for (int c = 0; c < d; ++c) out[c] = 0.0;
+  if (nJ == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int64_t i = 0; i < nJ; ++i) {
+    z[i] = scale * dot_bf16(q, K + J[i] * kv_stride, d);
+    if (z[i] > m) m = z[i];
+  }
+  double l = 0.0;
+  for (int64_t i = 0; i < nJ; ++i) {
+    double p = exp(z[i] - m);
+    l += p;
+    const uint16_t* vr = V + J[i] * kv_stride;
+    for (int c = 0; c < d; ++c) out[c] += p * bf16_to_double(vr[c]);
+  }
+  for (int c = 0; c < d; ++c) out[c] /= l;
+  *lse = m + log(l);
+}
+
+/*
+ * J(t, set) = { j : floor(j / Bk) is an id of the set, j <= t } in slot order,
+ * ascending j within a block ([P1] 2-3 and 3-3; [P2] "causally visible").
+ * A repeated id counts once.
+ */
+static int64_t key_set(const int32_t* sel, int k, int64_t t, int Bk, int64_t nb, int64_t* J) {
+  int64_t n = 0;
+  for (int s = 0; s < k; ++s) {
+    int32_t b = sel[s];
+    if (b < 0 || b >= nb) continue;
+    int dup = 0;
+    for (int s2 = 0; s2 < s; ++s2)
+      if (sel[s2] == b) dup = 1;
+    if (dup) continue;
+    for (int64_t j = (int64_t)b * Bk; j < (int64_t)(b + 1) * Bk && j <= t; ++j) J[n++] = j;
+  }
+  return n;
+}
+
+typedef struct {
+  const uint16_t *q_rows, *K, *V;
+  const int32_t* blk; /* [G, n_rows, k] or NULL for dense */
+  const int64_t* rows;
+  int64_t n_rows, N, nb;
+  int H_q, H_kv, d, Bk, k;
+  double scale;
+  double *out, *lse;
+  int status;
+} attn_ctx;
+
+static void attn_item(int64_t it, void* p) {
+  attn_ctx* c = (attn_ctx*)p;
+  int64_t r = it / c->H_q;
+  int h = (int)(it % c->H_q);
+  int g = h / (c->H_q / c->H_kv); /* [P1] 1-1: head h reads the K/V of its GQA group */
+  int64_t t = c->rows[r];
+  int64_t cap = c->blk ? (int64_t)c->k * c->Bk : t + 1;
+  int64_t* J = (int64_t*)malloc(sizeof(int64_t) * (size_t)(cap + 1));
+  double* z = (double*)malloc(sizeof(double) * (size_t)(cap + 1));
+  if (!J || !z) {
+    c->status = ORACLE_NO_MEM;
+    free(J);
+    free(z);
+    return;
+  }
+  int64_t nJ;
+  if (c->blk) {
+    nJ = key_set(c->blk + ((int64_t)g * c->n_rows + r) * c->k, c->k, t, c->Bk, c->nb, J);
+  } else {
+    nJ = t + 1; /* dense causal: every j <= t */
+    for (int64_t j = 0; j <= t; ++j) J[j] = j;
+  }
+  int64_t kv_stride = (int64_t)c->H_kv * c->d;
+  attend_set(c->q_rows + (r * c->H_q + h) * c->d, c->K + (int64_t)g * c->d, c->V + (int64_t)g * c->d,
+             kv_stride, J, nJ, c->d, c->scale, c->out + (r * c->H_q + h) * c->d, c->lse + r * c->H_q + h, z);
+  free(J);
+  free(z);
+}
+
+/*
+ * Block-sparse attention of the listed positions over a given selection
+ * (block_idx_rows[g, r, :] is the set of row r).  q_rows: [n_rows, H_q, d];
+ * K, V: [N, H_kv, d].  out: [n_rows, H_q, d], lse: [n_rows, H_q].
+ */
+int msa_ref_sparse_attn(const uint16_t* q_rows, const uint16_t* K, const uint16_t* V,
+                        const int32_t* block_idx_rows, const int64_t* rows, int64_t n_rows, int64_t N,
+                        int H_q, int H_kv, int d, int Bk, int k, double scale, double* out, double* lse,
+                        int n_threads) {
+  if (!q_rows || !K || !V || !block_idx_rows || !rows || !out || !lse || N <= 0 || H_kv <= 0 ||
+      H_q % H_kv != 0 || d <= 0 || Bk <= 0 || k < 1)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  attn_ctx c = {q_rows, K, V, block_idx_rows, rows, n_rows, N, (N + Bk - 1) / Bk, H_q, H_kv, d, Bk, k,
+                scale, out, lse, 0};
+  parallel_for(n_rows * H_q, n_threads, attn_item, &c);
+  return c.status;
+}
+
+/* Dense causal GQA attention ([P1] 1-1) of the listed positions. */
+int msa_ref_dense_attn(const uint16_t* q_rows, const uint16_t* K, const uint16_t* V, const int64_t* rows,
+                       int64_t n_rows, int64_t N, int H_q, int H_kv, int d, double scale, double* out,
+                       double* lse, int n_threads) {
+  if (!q_rows || !K || !V || !rows || !out || !lse || N <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  attn_ctx c = {q_rows, K, V, NULL, rows, n_rows, N, 1, H_q, H_kv, d, 1, 1, scale, out, lse, 0};
+  parallel_for(n_rows * H_q, n_threads, attn_item, &c);
+  return c.status;
+}
+
+/* ------------------------------------------------------- step 6: decode */
+typedef struct {
+  const uint16_t *q_t, *q_idx_t, *k_idx_cache, *k_cache, *v_cache;
+  const int64_t* ctx_len;
+  int64_t ctx_max, nb_max;
+  int B, H_q, H_kv, d, d_I, Bk, k;
+  double scale;
+  double *out, *lse, *kth;
+  int32_t* blk; /* [B, G, k] */
+  int status;
+} decode_ctx;
+
+static void decode_select_item(int64_t it, void* p) {
+  decode_ctx* c = (decode_ctx*)p;
+  int G = c->H_kv;
+  int64_t b = it / G;
+  int g = (int)(it % G);
+  int64_t t = c->ctx_len[b] - 1;
+  int64_t nb = t / c->Bk + 1;
+  double* S = (double*)malloc(sizeof(double) * (size_t)nb);
+  unsigned char* taken = (unsigned char*)malloc((size_t)nb + 1);
+  if (!S || !taken) {
+    c->status = ORACLE_NO_MEM;
+    free(S);
+    free(taken);
+    return;
+  }
+  block_scores_row(c->q_idx_t + (b * G + g) * c->d_I, c->k_idx_cache + b * c->ctx_max * c->d_I, t, c->d_I,
+                   c->Bk, nb, S);
+  topk_row(S, t, c->Bk, c->k, c->blk + (b * G + g) * c->k, c->kth ? c->kth + (b * G + g) * 2 : NULL, taken);
+  free(S);
+  free(taken);
+}
+
+static void decode_attn_item(int64_t it, void* p) {
+  decode_ctx* c = (decode_ctx*)p;
+  int64_t b = it / c->H_q;
+  int h = (int)(it % c->H_q);
+  int G = c->H_kv;
+  int g = h / (c->H_q / G);
+  int64_t t = c->ctx_len[b] - 1;
+  int64_t* J = (int64_t*)malloc(sizeof(int64_t) * (size_t)c->k * c->Bk);
+  double* z = (double*)malloc(sizeof(double) * (size_t)c->k * c->Bk);
+  if (!J || !z) {
+    c->status = ORACLE_NO_MEM;
+    free(J);
+    free(z);
+    return;
+  }
+  int64_t nJ = key_set(c->blk + (b * G + g) * c->k, c->k, t, c->Bk, c->nb_max, J);
+  int64_t kv_stride = (int64_t)G * c->d;
+  const uint16_t* K = c->k_cache + b * c->ctx_max * kv_stride + (int64_t)g * c->d;
+  const uint16_t* V = c->v_cache + b * c->ctx_max * kv_stride + (int64_t)g * c->d;
+  attend_set(c->q_t + (b * c->H_q + h) * c->d, K, V, kv_stride, J, nJ, c->d, c->scale,
+             c->out + (b * c->H_q + h) * c->d, c->lse + b * c->H_q + h, z);
+  free(J);
+  free(z);
+}
+
+/*
+ * One decode step ([P3] section 2): per sequence b the query at
+ * t = ctx_len[b] - 1 scores the whole index-key cache, keeps its block set
+ * (steps 1-2) and attends over the selected blocks' tokens j <= t (step 4).
+ * q_t [B,H_q,d], q_idx_t [B,G,d_I], k_idx_cache [B,ctx_max,d_I],
+ * k_cache / v_cache [B,ctx_max,H_kv,d].  Outputs out [B,H_q,d], lse [B,H_q],
+ * block_idx [B,G,k], kth [B,G,2] (nullable).
+ */
+int msa_ref_decode(const uint16_t* q_t, const uint16_t* q_idx_t, const uint16_t* k_idx_cache,
+                   const uint16_t* k_cache, const uint16_t* v_cache, const int64_t* ctx_len, int B,
+                   int64_t ctx_max, int H_q, int H_kv, int d, int d_I, int Bk, int k, double scale,
+                   double* out, double* lse, int32_t* block_idx, double* kth, int n_threads) {
+  if (!q_t || !q_idx_t || !k_idx_cache || !k_cache || !v_cache || !ctx_len || !out || !lse || !block_idx ||
+      B <= 0 || ctx_max <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 || d_I <= 0 || d_I > 512 || Bk <= 0 ||
+      k < 1)
+    return ORACLE_BAD_ARG;
+  for (int b = 0; b < B; ++b)
+    if (ctx_len[b] < 1 || ctx_len[b] > ctx_max) return ORACLE_BAD_ARG;
+  decode_ctx c = {q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, ctx_max, (ctx_max + Bk - 1) / Bk,
+                  B, H_q, H_kv, d, d_I, Bk, k, scale, out, lse, kth, block_idx, 0};
+  parallel_for((int64_t)B * H_kv, n_threads, decode_select_item, &c);
+  if (c.status) return c.status;
+  parallel_for((int64_t)B * H_q, n_threads, decode_attn_item, &c);
+  return c.status;
+}
