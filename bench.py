@@ -1,0 +1,457 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA forward path on GB300.
+
+Default (N=1): one JSON line for the 128K prefill step (select -> invert ->
+KV-outer attention -> combine) on device-resident synthetic inputs, with a
+"decode" object for the 1M-context decode step, the roofline of the dominant
+kernel, sampled SM clocks, an end-to-end number through host buffers and the
+fp64 oracle timed on the host cores.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 (torchrun) every rank runs an independent replica of the step (the
+path needs no exchange between GPUs); value = tokens of all ranks / max time.
+--impl reference times the fp64 CPU oracle on the same workload instead.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA prefill tokens/s at 128K, decode tokens/s at 1M ctx; % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="prefill_128k")
+    ap.add_argument("--decode-config", default="decode_1m")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="oracle rows timed for cpu_baseline")
+    ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode"],
+                    help="time one stage alone on --config (small-memory cases for profiler captures)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Dist:
+    def __init__(self, use_cuda):
+        import torch
+        import torch.distributed as dist
+        self.ws, self.rank, self.local = dist_setup()
+        self.dist = dist
+        self.on = self.ws > 1
+        if self.on:
+            dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+
+    def barrier(self):
+        if self.on:
+            self.dist.barrier()
+
+    def max(self, x):
+        if not self.on:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.on:
+            self.dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while running; summarised for the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for i, n in enumerate(names):
+                    if r[5 + i].lower().startswith("active"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- traffic from a committed ncu summary
+def traffic_for(kernel_key, src_file):
+    """Per-launch DRAM bytes recorded in profiles/traffic.json for the given kernel source hash, else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f).get(kernel_key)
+        with open(os.path.join(ROOT, src_file), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+        if d and d.get("source_sha") == h:
+            return d.get("bytes_per_launch")
+    except (OSError, ValueError):
+        return None
+    return None
+
+
+# --------------------------------------------------------------------------- the GPU arm
+def prefill_launches(cfg):
+    """Kernels libmsa launches for one prefill step: select 1, invert 4, per query slab 4."""
+    per_pos = cfg.k * cfg.H_q * (2.0 * cfg.d + 4.0)
+    cap = int(36.0e9 / per_pos)
+    cap = max(1024, min(131072, cap))
+    slab = min(cfg.N, cap)
+    n_slabs = (cfg.N + slab - 1) // slab
+    return 1 + 4 + 4 * n_slabs
+
+
+def bench_prefill(args, dist, torch, peaks):
+    import datagen
+    from block_sparse_long_index_gb300 import MsaPrefill
+    cfg = datagen.CONFIGS[args.config]
+    inp = datagen.prefill_device(cfg)
+    run = MsaPrefill(cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    q, k, v, qi, ki = inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"]
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        run(q, k, v, qi, ki)
+    torch.cuda.synchronize()
+    if run.device_status() != 0:
+        raise RuntimeError("device error during warm-up")
+    K = args.steps
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(E(), E(), E()) for _ in range(K)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = E(), E()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        run.select(qi, ki)
+        ev[i][1].record(stream)
+        run.attend(q, k, v)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    sel_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / K
+    att_ms = sum(b.elapsed_time(c) for _, b, c in ev) / K
+    assert run.device_status() == 0
+    res = dict(cfg=cfg, total_ms=total_ms, sel_ms=sel_ms, att_ms=att_ms, clocks=clk)
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    if not args.no_e2e:
+        host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in
+                (("q", q), ("k", k), ("v", v), ("q_idx", qi), ("k_idx", ki))}
+        for n, t in (("q", q), ("k", k), ("v", v), ("q_idx", qi), ("k_idx", ki)):
+            host[n].copy_(t)
+        hout = {"out": torch.empty(run.out.shape, dtype=run.out.dtype, pin_memory=True),
+                "lse": torch.empty(run.lse.shape, dtype=run.lse.dtype, pin_memory=True)}
+        from block_sparse_long_index_gb300.api import prefill_from_host
+        devbufs = {"q": q, "k": k, "v": v, "q_idx": qi, "k_idx": ki}
+        prefill_from_host(run, host, devbufs, hout)
+        torch.cuda.synchronize()
+        Ke = max(1, min(K, 5))
+        dist.barrier()
+        torch.cuda.synchronize()
+        a, b = E(), E()
+        a.record(stream)
+        for _ in range(Ke):
+            prefill_from_host(run, host, devbufs, hout)
+        b.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        e2e_ms = a.elapsed_time(b) / Ke
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in hout.values())
+        res["e2e"] = dict(ms=e2e_ms, h2d=h2d, d2h=d2h)
+    del inp, run
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_decode(args, dist, torch):
+    import datagen
+    from block_sparse_long_index_gb300 import MsaDecode
+    cfg = datagen.CONFIGS[args.decode_config]
+    inp = datagen.decode_device(cfg)
+    run = MsaDecode(cfg.B, cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # 4x L2, rewritten between steps
+    args_ = (inp["q_t"], inp["q_idx_t"], inp["k_idx_cache"], inp["k_cache"], inp["v_cache"], inp["ctx_len"])
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        run(*args_)
+    torch.cuda.synchronize()
+    K = max(args.steps, 20)
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(E(), E()) for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        run(*args_)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    assert run.device_status() == 0
+    times = sorted(a.elapsed_time(b) for a, b in ev)
+    mean_ms = sum(times) / K
+    res = dict(cfg=cfg, mean_ms=mean_ms, median_ms=times[K // 2], steps=K)
+    del inp, run, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------------- the oracle (CPU) leg
+def oracle_prefill_sample(cfg, n_rows, seed=7):
+    """Times the fp64 oracle (select + attention over every head) on n_rows sampled positions.
+    Returns (seconds, rows, threads)."""
+    import numpy as np
+
+    import datagen
+    import oracle
+    rows = datagen.sample_rows(cfg.N, n_rows, seed)
+    host = datagen.prefill_host(cfg, rows=rows)
+    th = oracle.threads()
+    t0 = time.perf_counter()
+    blk, _ = oracle.select_blocks(host["q_idx"], host["k_idx"], rows, cfg.N, cfg.Bk, cfg.k, n_threads=th)
+    oracle.sparse_attn(host["q"], host["k"], host["v"], blk, rows, cfg.Bk, 1.0 / math.sqrt(cfg.d), n_threads=th)
+    dt = time.perf_counter() - t0
+    return dt, len(rows), th
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle on the host cores, same metric and workload."""
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    import datagen
+    cfg = datagen.CONFIGS[args.config]
+    rows_per_step = 96
+    for i in range(args.warmup):
+        oracle_prefill_sample(cfg, rows_per_step // 4, seed=100 + i)
+    total_s, total_rows, th = 0.0, 0, 1
+    for i in range(args.steps):
+        dt, n, th = oracle_prefill_sample(cfg, rows_per_step, seed=200 + i)
+        total_s += dt
+        total_rows += n
+    value = total_rows / total_s
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "sample": "%d seeded query rows per step" % rows_per_step},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                             "sample": "%d rows x %d steps of the %s workload (select over all groups + "
+                                       "attention over all heads per row)" % (rows_per_step, args.steps, cfg.name)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_name(cfg):
+    if cfg.kind == "prefill":
+        return ("%s: prefill N=%d H_q=%d H_kv=%d d=%d d_I=%d Bk=%d k=%d, %d needle blocks/group"
+                % (cfg.name, cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k, cfg.needles))
+    return ("%s: decode B=%d ctx=%d H_q=%d H_kv=%d d=%d d_I=%d Bk=%d k=%d, %d needle blocks/group"
+            % (cfg.name, cfg.B, cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k, cfg.needles))
+
+
+def run_stage(args):
+    """One stage alone on --config, for profiler captures: prints {"stage", "ms", ...}."""
+    import torch
+
+    import datagen
+    from block_sparse_long_index_gb300 import msa
+    cfg = datagen.CONFIGS[args.config]
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    if args.stage == "decode":
+        from block_sparse_long_index_gb300 import MsaDecode
+        inp = datagen.decode_device(cfg)
+        run = MsaDecode(cfg.B, cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+        call = lambda: run(inp["q_t"], inp["q_idx_t"], inp["k_idx_cache"], inp["k_cache"], inp["v_cache"],  # noqa
+                           inp["ctx_len"])
+    else:
+        want = ("q_idx", "k_idx") if args.stage == "select" else ("q", "k", "v", "q_idx", "k_idx")
+        inp = datagen.prefill_device(cfg, want=want)
+        blk = torch.empty((cfg.G, cfg.N, cfg.k), dtype=torch.int32, device="cuda")
+        ws_sel = torch.empty(msa.msa_select_blocks_workspace(cfg.N, cfg.G, cfg.d_I, cfg.Bk, cfg.k),
+                             dtype=torch.uint8, device="cuda")
+        select = lambda: msa.msa_select_blocks(inp["q_idx"], inp["k_idx"], cfg.N, cfg.G, cfg.d_I, cfg.Bk,  # noqa
+                                               cfg.k, blk, ws_sel)
+        if args.stage == "select":
+            call = select
+        else:
+            select()
+            shp = msa.shape(cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+            ws = torch.empty(msa.msa_sparse_attn_fwd_workspace(shp), dtype=torch.uint8, device="cuda")
+            out = torch.empty((cfg.N, cfg.H_q, cfg.d), dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty((cfg.H_q, cfg.N), dtype=torch.float32, device="cuda")
+            call = lambda: msa.msa_sparse_attn_fwd(inp["q"], inp["k"], inp["v"], blk, shp,  # noqa
+                                                   1.0 / math.sqrt(cfg.d), out, lse, ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    a, b = E(), E()
+    a.record()
+    for _ in range(args.steps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"stage": args.stage, "config": workload_name(cfg), "steps": args.steps,
+                      "ms": a.elapsed_time(b) / args.steps}), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.stage != "all":
+        return run_stage(args)
+    import torch
+    ws, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist = Dist(True)
+    peaks, peak_src = load_peaks()
+
+    pre = bench_prefill(args, dist, torch, peaks)
+    cfg = pre["cfg"]
+    total_ms = dist.max(pre["total_ms"])
+    K = args.steps
+    value = ws * cfg.N * K / (total_ms / 1000.0)
+    flops_index = (cfg.N ** 2 / 2.0) * cfg.G * cfg.d_I * 2.0
+    flops_main = cfg.N * cfg.H_q * cfg.k * cfg.Bk * cfg.d * 4.0
+    step_s = total_ms / K / 1000.0
+    sel_s, att_s = pre["sel_ms"] / 1000.0, pre["att_ms"] / 1000.0
+    peak_t = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    sel_tf = flops_index / sel_s / 1e12
+    roofline = {"kernel": "msa_select_blocks (index scoring + pooling + top-k, one launch)", "bound": "tensor",
+                "achieved": sel_tf, "peak": peak_t, "unit": "TFLOP/s", "frac": sel_tf / peak_t,
+                "traffic": traffic_for("select_prefill_128k", "block_sparse_long_index_gb300/csrc/msa_select.cu"),
+                "algorithmic": "(N^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index,
+                "peak_source": "%s bf16_tflops_sustained" % peak_src}
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(cfg), "parallelism": "replicas" if ws > 1 else "single",
+                       "l2": "inputs larger than L2 (q alone is %.2f GB)" % (cfg.N * cfg.H_q * cfg.d * 2 / 1e9)},
+            "clocks": pre["clocks"],
+            "gpu_launches": prefill_launches(cfg) * K,
+            "roofline": roofline,
+            "stages_ms": {"select": pre["sel_ms"], "attend": pre["att_ms"]},
+            "step_frac_of_tensor_peak": (flops_index + flops_main) / step_s / 1e12 / peak_t,
+            "step_tflops": (flops_index + flops_main) / step_s / 1e12}
+    if "e2e" in pre:
+        e = pre["e2e"]
+        e_ms = dist.max(e["ms"])
+        line["e2e"] = {"value": ws * cfg.N / (e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": e["h2d"],
+                       "d2h_bytes_per_step": e["d2h"]}
+    if not args.no_decode:
+        dec = bench_decode(args, dist, torch)
+        dcfg = dec["cfg"]
+        d_ms = dist.max(dec["mean_ms"])
+        bytes_step = dcfg.B * (dcfg.ctx * dcfg.d_I * 2 + dcfg.k * dcfg.Bk * 2 * dcfg.H_kv * dcfg.d * 2)
+        bw = bytes_step / (d_ms / 1000.0) / 1e9
+        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        line["decode"] = {"metric": "decode tokens/s at 1M ctx", "value": ws * dcfg.B / (d_ms / 1000.0),
+                          "unit": "tokens/s", "ms_per_step": d_ms, "median_ms": dec["median_ms"],
+                          "steps": dec["steps"], "workload": workload_name(dcfg), "l2": "512 MB buffer rewritten "
+                          "between steps (outside the timed events)",
+                          "roofline": {"bound": "hbm", "achieved": bw, "peak": hbm, "unit": "GB/s",
+                                       "frac": bw / hbm, "traffic": None,
+                                       "algorithmic": "B*(ctx*d_I*2 + k*Bk*2*H_kv*d*2) = %d bytes per step"
+                                                      % bytes_step,
+                                       "peak_source": "%s hbm_gbs" % peak_src},
+                          "gpu_launches": 4 * dec["steps"]}
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        dt, n, th = oracle_prefill_sample(cfg, args.cpu_rows)
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",
+                                "sample": "%d seeded query rows of the %s workload (select over all %d groups + "
+                                          "attention over all %d heads), %.1f s" % (n, cfg.name, cfg.G, cfg.H_q, dt)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

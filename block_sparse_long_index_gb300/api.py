@@ -1,0 +1,110 @@
+"""Tensor-level entry points over the C ABI (allocation of outputs and workspaces with torch).
+
+``MsaPrefill`` / ``MsaDecode`` own their outputs and workspace so repeated steps
+allocate nothing; ``prefill`` / ``decode`` are one-shot conveniences.  All
+compute is in libmsa.so.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import msa as _c
+
+
+def _check_bf16(name, t, shape):
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA bfloat16 tensor" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+class MsaPrefill:
+    """One prefill layer step: select -> (invert + KV-outer attention + combine)."""
+
+    def __init__(self, N, H_q, H_kv, d, d_I, Bk, k, device="cuda"):
+        self.N, self.H_q, self.H_kv, self.d, self.d_I, self.Bk, self.k = N, H_q, H_kv, d, d_I, Bk, k
+        self.G = H_kv
+        self.shape = _c.shape(N, H_q, H_kv, d, d_I, Bk, k)
+        ws = max(_c.msa_select_blocks_workspace(N, self.G, d_I, Bk, k), _c.msa_sparse_attn_fwd_workspace(self.shape))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.block_idx = torch.empty((self.G, N, k), dtype=torch.int32, device=device)
+        self.out = torch.empty((N, H_q, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((H_q, N), dtype=torch.float32, device=device)
+
+    def select(self, q_idx, k_idx, stream=None):
+        _c.msa_select_blocks(q_idx, k_idx, self.N, self.G, self.d_I, self.Bk, self.k, self.block_idx,
+                             self.workspace, stream=stream)
+        return self.block_idx
+
+    def attend(self, q, k, v, block_idx=None, scale=None, stream=None):
+        scale = 1.0 / math.sqrt(self.d) if scale is None else scale
+        _c.msa_sparse_attn_fwd(q, k, v, self.block_idx if block_idx is None else block_idx, self.shape, scale,
+                               self.out, self.lse, self.workspace, stream=stream)
+        return self.out, self.lse
+
+    def __call__(self, q, k, v, q_idx, k_idx, scale=None, stream=None):
+        N, G = self.N, self.G
+        _check_bf16("q", q, (N, self.H_q, self.d))
+        _check_bf16("k", k, (N, self.H_kv, self.d))
+        _check_bf16("v", v, (N, self.H_kv, self.d))
+        _check_bf16("q_idx", q_idx, (N, G, self.d_I))
+        _check_bf16("k_idx", k_idx, (N, self.d_I))
+        self.select(q_idx, k_idx, stream)
+        self.attend(q, k, v, None, scale, stream)
+        return self.out, self.lse, self.block_idx
+
+    def device_status(self, stream=None):
+        return _c.msa_check_device_error(self.workspace, stream)
+
+
+class MsaDecode:
+    """One decode step for B sequences over caches of capacity ctx_max."""
+
+    def __init__(self, B, ctx_max, H_q, H_kv, d, d_I, Bk, k, device="cuda"):
+        self.B, self.ctx_max = B, ctx_max
+        self.H_q, self.H_kv, self.d, self.d_I, self.Bk, self.k = H_q, H_kv, d, d_I, Bk, k
+        self.shape = _c.shape(ctx_max, H_q, H_kv, d, d_I, Bk, k)
+        self.workspace = torch.empty(_c.msa_decode_workspace(B, self.shape), dtype=torch.uint8, device=device)
+        self.out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((B, H_q), dtype=torch.float32, device=device)
+        self.block_idx = torch.empty((B, H_kv, k), dtype=torch.int32, device=device)
+
+    def __call__(self, q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, scale=None, stream=None):
+        scale = 1.0 / math.sqrt(self.d) if scale is None else scale
+        _c.msa_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, self.B, self.shape, scale, self.out,
+                      self.lse, self.block_idx, self.workspace, stream=stream)
+        return self.out, self.lse, self.block_idx
+
+    def device_status(self, stream=None):
+        return _c.msa_check_device_error(self.workspace, stream)
+
+
+def prefill(q, k, v, q_idx, k_idx, Bk=128, k_blocks=16, scale=None):
+    """One-shot prefill: returns (out [N,H_q,d] bf16, lse [H_q,N] fp32, block_idx [G,N,k] int32)."""
+    N, H_q, d = q.shape
+    H_kv = k.shape[1]
+    run = MsaPrefill(N, H_q, H_kv, d, q_idx.shape[2], Bk, k_blocks, device=q.device)
+    out, lse, blk = run(q, k, v, q_idx, k_idx, scale)
+    return out, lse, blk
+
+
+def decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, Bk=128, k_blocks=16, scale=None):
+    """One-shot decode step: returns (out [B,H_q,d], lse [B,H_q], block_idx [B,G,k])."""
+    B, H_q, d = q_t.shape
+    _, ctx_max, H_kv, _ = k_cache.shape
+    run = MsaDecode(B, ctx_max, H_q, H_kv, d, q_idx_t.shape[2], Bk, k_blocks, device=q_t.device)
+    return run(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, scale)
+
+
+def prefill_from_host(run: MsaPrefill, host_inputs, dev_inputs, host_out, stream=None):
+    """End-to-end step through the public API with host buffers: pinned host -> device copies,
+    the prefill step, device -> pinned host copies of out and lse, all on one stream."""
+    for name in ("q", "k", "v", "q_idx", "k_idx"):
+        dev_inputs[name].copy_(host_inputs[name], non_blocking=True)
+    out, lse, blk = run(dev_inputs["q"], dev_inputs["k"], dev_inputs["v"], dev_inputs["q_idx"], dev_inputs["k_idx"],
+                        stream=stream)
+    host_out["out"].copy_(out, non_blocking=True)
+    host_out["lse"].copy_(lse, non_blocking=True)
+    return host_out

@@ -1,0 +1,188 @@
+// C ABI of libmsa.so: argument validation, workspace sizing and layout,
+// device error word, dispatch to the kernel translation units.
+// The declarations and their contracts are in include/msa.h.
+#include <stdint.h>
+
+#include "../../include/msa.h"
+#include "msa_common.cuh"
+
+namespace msa {
+
+int num_sms() {
+  static int cached_dev = -1;
+  static int cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+}  // namespace msa
+
+using msa::align_up;
+
+namespace {
+
+constexpr size_t kHeader = sizeof(msa::DeviceStatus);  // 256 bytes at the start of every workspace
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool pow2_upto8(int x) { return x == 1 || x == 2 || x == 4 || x == 8; }
+
+msa_status_t check_common(int64_t N, int G, int d_I, int Bk, int k) {
+  if (N < 1 || G < 1 || d_I < 1 || Bk < 1 || k < 1) return MSA_ERR_INVALID_ARGUMENT;
+  if (G > 64 || (d_I != 32 && d_I != 64 && d_I != 128) || (Bk != 64 && Bk != 128) || k > 32)
+    return MSA_ERR_UNSUPPORTED;
+  const int64_t nb = (N + Bk - 1) / Bk;
+  if (nb > 32768 || N * (int64_t)k >= ((int64_t)1 << 31)) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+msa_status_t check_shape(const msa_shape_t* s) {
+  if (!s) return MSA_ERR_INVALID_ARGUMENT;
+  if (s->H_q < 1 || s->H_kv < 1 || s->d < 1) return MSA_ERR_INVALID_ARGUMENT;
+  if (s->H_q % s->H_kv != 0) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_common(s->N, s->H_kv, s->d_I, s->Bk, s->k);
+  if (st != MSA_OK) return st;
+  if (!pow2_upto8(s->H_q / s->H_kv) || (s->d != 64 && s->d != 128)) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+msa_status_t begin(void* ws, size_t ws_bytes, size_t need, cudaStream_t s) {
+  if (!ws) return MSA_ERR_INVALID_ARGUMENT;
+  if (((uintptr_t)ws & 255u) != 0) return MSA_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < need) return MSA_ERR_WORKSPACE_TOO_SMALL;
+  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return MSA_ERR_CUDA;
+  return MSA_OK;
+}
+
+msa_status_t finish(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t msa_select_blocks_workspace(int64_t N, int G, int d_I, int Bk, int k) {
+  (void)N;
+  (void)G;
+  (void)d_I;
+  (void)Bk;
+  (void)k;
+  return kHeader;
+}
+
+msa_status_t msa_select_blocks(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
+                               int32_t* block_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  if (!q_idx || !k_idx || !block_idx) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_common(N, G, d_I, Bk, k);
+  if (st != MSA_OK) return st;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || ((uintptr_t)block_idx & 3u)) return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_select_blocks_workspace(N, G, d_I, Bk, k), s);
+  if (st != MSA_OK) return st;
+  return finish(msa::launch_select(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, (msa::DeviceStatus*)workspace, s));
+}
+
+size_t msa_invert_blocks_workspace(int64_t N, int G, int Bk, int k) {
+  if (N < 1 || G < 1 || Bk < 1 || k < 1) return kHeader;
+  return kHeader + msa::invert_scratch_bytes(N, G, Bk, k);
+}
+
+msa_status_t msa_invert_blocks(const int32_t* block_idx, int64_t N, int G, int Bk, int k, int32_t* row_ptr,
+                               int32_t* entries, int32_t* n_entries, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream) {
+  if (!block_idx || !row_ptr || !entries || !n_entries) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_common(N, G, 32, Bk, k);
+  if (st != MSA_OK) return st;
+  if (((uintptr_t)block_idx | (uintptr_t)row_ptr | (uintptr_t)entries | (uintptr_t)n_entries) & 3u)
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_invert_blocks_workspace(N, G, Bk, k), s);
+  if (st != MSA_OK) return st;
+  msa::InvertScratch sc = msa::invert_scratch_carve((char*)workspace + kHeader, N, G, Bk, k);
+  return finish(msa::launch_invert(block_idx, N, G, Bk, k, row_ptr, entries, n_entries, sc,
+                                   (msa::DeviceStatus*)workspace, s));
+}
+
+size_t msa_sparse_attn_fwd_workspace(const msa_shape_t* shape) {
+  if (check_shape(shape) != MSA_OK) return kHeader;
+  msa::AttnPlan p = msa::attn_plan(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
+  return kHeader + msa::attn_scratch_bytes(p);
+}
+
+msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* block_idx,
+                                 const msa_shape_t* shape, float scale, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream) {
+  if (!q || !k || !v || !block_idx || !out || !lse) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || ((uintptr_t)block_idx & 3u) ||
+      ((uintptr_t)lse & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_sparse_attn_fwd_workspace(shape), s);
+  if (st != MSA_OK) return st;
+  msa::AttnPlan p = msa::attn_plan(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
+  return finish(msa::launch_attn(q, k, v, block_idx, p, scale, out, lse, (char*)workspace + kHeader,
+                                 (msa::DeviceStatus*)workspace, s));
+}
+
+size_t msa_decode_workspace(int B, const msa_shape_t* shape) {
+  if (B < 1 || check_shape(shape) != MSA_OK) return kHeader;
+  msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,
+                                       shape->k);
+  return kHeader + msa::decode_scratch_bytes(p);
+}
+
+msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                        const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                        void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                        msa_stream_t stream) {
+  if (!q_t || !q_idx_t || !k_idx_cache || !k_cache || !v_cache || !ctx_len || !out) return MSA_ERR_INVALID_ARGUMENT;
+  if (B < 1) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (shape->H_kv > 8) return MSA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q_t) || !aligned16(q_idx_t) || !aligned16(k_idx_cache) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || ((uintptr_t)ctx_len & 3u) || ((uintptr_t)out & 1u) || ((uintptr_t)lse & 3u) ||
+      ((uintptr_t)block_idx & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_decode_workspace(B, shape), s);
+  if (st != MSA_OK) return st;
+  msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,
+                                       shape->k);
+  return finish(msa::launch_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, p, scale, out, lse,
+                                   block_idx, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
+}
+
+msa_status_t msa_check_device_error(void* workspace, msa_stream_t stream) {
+  if (!workspace) return MSA_ERR_INVALID_ARGUMENT;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MSA_ERR_CUDA;
+  unsigned int flags = 0;
+  if (cudaMemcpy(&flags, workspace, sizeof(flags), cudaMemcpyDeviceToHost) != cudaSuccess) return MSA_ERR_CUDA;
+  if (flags & msa::kErrBadIndex) return MSA_ERR_BAD_INDEX;
+  if (flags & msa::kErrTimeout) return MSA_ERR_TIMEOUT;
+  return MSA_OK;
+}
+
+const char* msa_status_string(msa_status_t status) {
+  switch (status) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARGUMENT: return "invalid argument (null or misaligned pointer, bad size or shape)";
+    case MSA_ERR_UNSUPPORTED: return "unsupported shape (see include/msa.h for the supported set)";
+    case MSA_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than the *_workspace() size";
+    case MSA_ERR_CUDA: return "CUDA launch or runtime error";
+    case MSA_ERR_BAD_INDEX: return "bad index found on the device (entry skipped)";
+    case MSA_ERR_TIMEOUT: return "a bounded device wait gave up";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

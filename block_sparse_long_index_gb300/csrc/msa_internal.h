@@ -1,0 +1,60 @@
+// Internal launch interface between the C-ABI layer (msa_capi.cu) and the
+// kernel translation units.  Not part of the public header.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace msa {
+
+struct DeviceStatus;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int num_sms();  // cached cudaDevAttrMultiProcessorCount of the current device
+
+// ---- select (msa_select.cu)
+cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
+                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s);
+
+// ---- invert (msa_invert.cu)
+struct InvertScratch {
+  int32_t* counts;  // [G, n_chunks, nb]
+  int chunk;        // positions per chunk
+  int n_chunks;
+};
+size_t invert_scratch_bytes(int64_t N, int G, int Bk, int k);
+InvertScratch invert_scratch_carve(void* base, int64_t N, int G, int Bk, int k);
+cudaError_t launch_invert(const int32_t* block_idx, int64_t N, int G, int Bk, int k, int32_t* row_ptr,
+                          int32_t* entries, int32_t* n_entries, const InvertScratch& sc, DeviceStatus* st,
+                          cudaStream_t s);
+
+// ---- attention (msa_attn.cu)
+struct AttnPlan {
+  int64_t N;
+  int H_q, H_kv, d, Bk, k, gs;
+  int64_t nb;
+  int64_t slab;  // query positions per slab
+  int P;         // query positions per tile
+};
+AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k);
+size_t attn_scratch_bytes(const AttnPlan& p);
+cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
+                        float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);
+
+// ---- decode (msa_decode.cu)
+struct DecodePlan {
+  int B;
+  int64_t ctx_max;
+  int H_q, H_kv, d, d_I, Bk, k, gs;
+  int splits;  // CTAs per sequence in the index-key scan
+};
+DecodePlan decode_plan(int B, int64_t ctx_max, int H_q, int H_kv, int d, int d_I, int Bk, int k);
+size_t decode_scratch_bytes(const DecodePlan& p);
+cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                          const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
+                          float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s);
+
+}  // namespace msa

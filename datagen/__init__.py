@@ -87,6 +87,9 @@ CONFIGS = {
                            k=16, needles=8, index=2),
     "decode_1m": Config("decode_1m", "decode", B=4, ctx=1 << 20, H_q=64, H_kv=8, d=128, d_I=128, Bk=128,
                         k=16, needles=4, index=3),
+    # a smaller decode case (same shapes, 256K context) for profiler captures of a few GB
+    "decode_256k": Config("decode_256k", "decode", B=4, ctx=1 << 18, H_q=64, H_kv=8, d=128, d_I=128, Bk=128,
+                          k=16, needles=4, index=5),
     "prefill_1m": Config("prefill_1m", "prefill", N=1 << 20, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
                          needles=16, index=4),
 }
@@ -349,31 +352,36 @@ def _u16_to_bf16_tensor(a):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
 
-def prefill_device(cfg: Config, device="cuda"):
+def prefill_device(cfg: Config, device="cuda", want=("q", "k", "v", "q_idx", "k_idx")):
     """Device bf16 prefill inputs (q, k, v, q_idx, k_idx) filled in place on the GPU."""
     import torch
     N, H_q, H_kv, d, d_I, G = cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.G
     nd = make_needles(cfg)
     bf = torch.bfloat16
-    q = device_normal_(torch.empty((N, H_q, d), dtype=bf, device=device), cfg.seed, TID["q"])
-    k = device_normal_(torch.empty((N, H_kv, d), dtype=bf, device=device), cfg.seed, TID["k"])
-    v = device_normal_(torch.empty((N, H_kv, d), dtype=bf, device=device), cfg.seed, TID["v"])
-    k_idx = device_normal_(torch.empty((N, d_I), dtype=bf, device=device), cfg.seed, TID["k_idx"])
-    krows, valid = needle_key_rows(nd)
-    toks = nd.tokens(cfg.Bk)
-    if valid.any():
-        idx = torch.from_numpy(toks[valid]).to(device)
-        k_idx[idx] = _u16_to_bf16_tensor(krows[valid]).to(device)
-    q_idx = torch.empty((N, G, d_I), dtype=bf, device=device)
-    nb_dev = torch.from_numpy(np.ascontiguousarray(nd.blocks[0].reshape(-1), np.int32)).to(device)
-    u_dev = torch.from_numpy(nd.u).to(device) if nd.u.size else torch.zeros(1, device=device)
-    rc = _cuda().dg_cuda_q_idx(ctypes.c_void_p(q_idx.data_ptr()), N, None, cfg.seed, TID["q_idx"], TID["pick"],
-                               G, d_I, cfg.Bk, nd.m, nd.cap, ctypes.c_void_p(nb_dev.data_ptr()),
-                               ctypes.c_void_p(u_dev.data_ptr()), ctypes.c_float(nd.beta),
-                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
-    if rc != 0:
-        raise RuntimeError("dg_cuda_q_idx failed: %d" % rc)
-    return dict(q=q, k=k, v=v, q_idx=q_idx, k_idx=k_idx, needles=nd)
+    out = dict(needles=nd)
+    for name, shp in (("q", (N, H_q, d)), ("k", (N, H_kv, d)), ("v", (N, H_kv, d))):
+        if name in want:
+            out[name] = device_normal_(torch.empty(shp, dtype=bf, device=device), cfg.seed, TID[name])
+    if "k_idx" in want:
+        k_idx = device_normal_(torch.empty((N, d_I), dtype=bf, device=device), cfg.seed, TID["k_idx"])
+        krows, valid = needle_key_rows(nd)
+        toks = nd.tokens(cfg.Bk)
+        if valid.any():
+            idx = torch.from_numpy(toks[valid]).to(device)
+            k_idx[idx] = _u16_to_bf16_tensor(krows[valid]).to(device)
+        out["k_idx"] = k_idx
+    if "q_idx" in want:
+        q_idx = torch.empty((N, G, d_I), dtype=bf, device=device)
+        nb_dev = torch.from_numpy(np.ascontiguousarray(nd.blocks[0].reshape(-1), np.int32)).to(device)
+        u_dev = torch.from_numpy(nd.u).to(device) if nd.u.size else torch.zeros(1, device=device)
+        rc = _cuda().dg_cuda_q_idx(ctypes.c_void_p(q_idx.data_ptr()), N, None, cfg.seed, TID["q_idx"], TID["pick"],
+                                   G, d_I, cfg.Bk, nd.m, nd.cap, ctypes.c_void_p(nb_dev.data_ptr()),
+                                   ctypes.c_void_p(u_dev.data_ptr()), ctypes.c_float(nd.beta),
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        if rc != 0:
+            raise RuntimeError("dg_cuda_q_idx failed: %d" % rc)
+        out["q_idx"] = q_idx
+    return out
 
 
 def decode_device(cfg: Config, ctx_len=None, device="cuda"):

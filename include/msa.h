@@ -1,0 +1,180 @@
+/*
+ * msa.h — C ABI of libmsa.so, the GB300 (sm_103a) forward path of MiniMax
+ * Sparse Attention (MSA).
+ *
+ * The method (pages: the "MSA" study note, sections 2-1 "Two-branch sparse
+ * attention" and 2-3 "Fixed attention budget"; the chipsbuilder.com article,
+ * "Funzionamento Delle Due Branch"):
+ *   index scores  s[t,g,j] = q^I[t,g] . k^I[j] / sqrt(d_I)      (j <= t)
+ *   block scores  S[t,g,b] = max over j in block b, j <= t, of s[t,g,j]
+ *   block set     B[t,g]   = {local(t)} + the k-1 best S[t,g,b], b < local(t)
+ *   output        O[t,h]   = softmax(scale * q[t,h] K_J^T) V_J,
+ *                 J = tokens j <= t of the blocks in B[t, g(h)], g(h) = h / (H_q/H_kv)
+ *
+ * Conventions for every call:
+ *   - Returns a status; work is enqueued asynchronously on `stream`.
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller; the
+ *     library neither frees nor keeps it after the call returns.
+ *   - The library allocates nothing.  Scratch comes from a caller-owned device
+ *     workspace whose minimum size the matching *_workspace() call returns.
+ *     The workspace must stay alive and untouched until the enqueued work has
+ *     finished; two calls in flight at once need two workspaces.
+ *   - Tensors are dense, row-major, contiguous; bf16 is stored as 16-bit
+ *     words; shapes are given beside each argument.
+ *   - Indices are 0-based.  local(t) = t / Bk.  nb = ceil(N / Bk).
+ *   - Host-side validation happens before any launch and returns
+ *     MSA_ERR_INVALID_ARGUMENT (bad pointer, size or shape),
+ *     MSA_ERR_UNSUPPORTED (a valid shape outside the supported set) or
+ *     MSA_ERR_WORKSPACE_TOO_SMALL.  A failed launch returns MSA_ERR_CUDA.
+ *   - Bad data found on the device (a block id outside [0, nb) other than -1)
+ *     does not trap: the entry is skipped and an error word at the start of
+ *     the workspace is set.  msa_check_device_error() reads that word; each
+ *     call clears it when it starts.
+ *
+ * Supported shapes: d in {64, 128}; d_I in {32, 64, 128}; Bk in {64, 128};
+ * 1 <= k <= 32; H_q / H_kv in {1, 2, 4, 8}; 1 <= H_kv <= 64; N >= 1.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* msa_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARGUMENT = 1,
+  MSA_ERR_UNSUPPORTED = 2,
+  MSA_ERR_WORKSPACE_TOO_SMALL = 3,
+  MSA_ERR_CUDA = 4,
+  MSA_ERR_BAD_INDEX = 5,
+  MSA_ERR_TIMEOUT = 6
+} msa_status_t;
+
+/* Problem shape.  G = H_kv GQA groups (one index-query head per group);
+ * gs = H_q / H_kv query heads per group; k counts the local block. */
+typedef struct {
+  int64_t N; /* tokens (prefill) or cache capacity per sequence (decode) */
+  int H_q;   /* query heads */
+  int H_kv;  /* key/value heads = GQA groups = index-query heads */
+  int d;     /* head dim of q, k, v */
+  int d_I;   /* index head dim of q^I, k^I */
+  int Bk;    /* tokens per KV block */
+  int k;     /* blocks per (query, group), local block included */
+} msa_shape_t;
+
+/* ---------------------------------------------------------------- select
+ * Index branch: scoring, block max-pooling and the local-pinned top-k.
+ * Pages: "MSA" study note 2-3 (equations for s, S and the block set), 3-2
+ * "Index Branch", 3-4 "Forced local block", 3-5 "GPU kernel co-design"
+ * (exp-free top-k on raw scores); Flash-MSA "プロキシアテンション" (streaming
+ * top-k while sweeping key tiles; local block pinned to +inf).
+ *
+ *   q_idx     [N, G, d_I] bf16: index queries (one head per group)
+ *   k_idx     [N, d_I]    bf16: index keys (one head shared by all groups)
+ *   block_idx [G, N, k]   int32 out: slot 0 = local(t); slots 1.. = the
+ *             min(k-1, local(t)) blocks b < local(t) of largest S, in
+ *             descending S, equal S ordered by ascending b (the lower block
+ *             wins a tie at the cut); remaining slots = -1.
+ * Ranking uses the fp32 tensor-core dot products q^I . k^I (a positive
+ * scale does not change the order).
+ */
+size_t msa_select_blocks_workspace(int64_t N, int G, int d_I, int Bk, int k);
+msa_status_t msa_select_blocks(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk,
+                               int k, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream);
+
+/* ---------------------------------------------------------------- invert
+ * B -> B*: for every group g and block b, the (t, slot) pairs whose set
+ * holds b.  Pages: Flash-MSA "バックワードパス" (B[batch, head, query,
+ * slot] -> block inverted to B*[batch, head, block] -> queries) and the
+ * "MSA" study note 3-5 (reverse sparse index feeding KV-outer attention).
+ *
+ *   block_idx [G, N, k] int32 (ids in [0, nb) or -1)
+ *   row_ptr   [G, nb+1] int32 out: offsets into the group's entry region
+ *   entries   [G, N*k]  int32 out: group g's list of block b is
+ *             entries[g*N*k + row_ptr[g][b] .. g*N*k + row_ptr[g][b+1]),
+ *             each entry t*k + slot, in ascending t (deterministic).
+ *             Entries past n_entries[g] are left untouched.
+ *   n_entries [G]       int32 out: entries listed for group g.
+ * An id outside [0, nb) other than -1 sets the device error word and is not
+ * listed.
+ */
+size_t msa_invert_blocks_workspace(int64_t N, int G, int Bk, int k);
+msa_status_t msa_invert_blocks(const int32_t* block_idx, int64_t N, int G, int Bk, int k, int32_t* row_ptr,
+                               int32_t* entries, int32_t* n_entries, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream);
+
+/* ---------------------------------------------------------------- attend
+ * Main branch: exact softmax attention over the selected blocks' causally
+ * visible tokens, every head of group g reading group g's set, computed
+ * KV-outer (each K/V block once per tile of the queries that chose it) with
+ * per-(t, h, slot) partial results merged by their log-sum-exp.
+ * Pages: "MSA" study note 2-3 (Attn over K_{g,B}, V_{g,B}), 3-3 "Main
+ * Branch", 3-5 (KV-outer execution, pre-scheduled tile chunking, two-phase
+ * combine, LSE kept); chipsbuilder "Funzionamento Delle Due Branch" (tokens
+ * causally visible in the selected blocks); Flash-MSA "フォワードパス" (main
+ * LSE saved).
+ *
+ *   q         [N, H_q, d]  bf16
+ *   k, v      [N, H_kv, d] bf16
+ *   block_idx [G, N, k]    int32: each row's set (-1 = empty slot; a repeated
+ *             id counts once; ids past local(t) hold no visible token and add
+ *             nothing)
+ *   scale     softmax scale (1/sqrt(d) in the pages)
+ *   out       [N, H_q, d]  bf16 out: O[t, h]
+ *   lse       [H_q, N]     fp32 out: natural-log log-sum-exp of the scaled
+ *             scores over J; -inf (with out = 0) when J is empty.
+ */
+size_t msa_sparse_attn_fwd_workspace(const msa_shape_t* shape);
+msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* block_idx,
+                                 const msa_shape_t* shape, float scale, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* ---------------------------------------------------------------- decode
+ * One decode step for B sequences.  The query of sequence s sits at position
+ * t = ctx_len[s] - 1 and its k, v and k^I are already in the caches.  The
+ * whole index-key cache is scanned (the only part that grows with the
+ * context), the block set is chosen as in msa_select_blocks, and only the
+ * selected K/V blocks are read.  Pages: velog llama.cpp analysis, section 2
+ * (256 B/token index-key scan, fixed K/V read per step) and section 4 (block
+ * scores, max-pooling, forced local block, top-k, then attention over the
+ * gathered blocks).
+ *
+ *   q_t          [B, H_q, d] bf16
+ *   q_idx_t      [B, G, d_I] bf16
+ *   k_idx_cache  [B, shape->N, d_I] bf16  (shape->N = cache capacity)
+ *   k_cache      [B, shape->N, H_kv, d] bf16, v_cache likewise
+ *   ctx_len      [B] int32 (device): 1 <= ctx_len[s] <= shape->N
+ *   out          [B, H_q, d] bf16 out
+ *   lse          [B, H_q] fp32 out (nullable)
+ *   block_idx    [B, G, k] int32 out (nullable): the sets chosen
+ * ctx_len values outside [1, N] set the device error word; that sequence's
+ * outputs are zero.
+ */
+size_t msa_decode_workspace(int B, const msa_shape_t* shape);
+msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                        const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                        void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                        msa_stream_t stream);
+
+/* ---------------------------------------------------------------- status
+ * msa_check_device_error: waits for `stream`, then returns MSA_ERR_BAD_INDEX
+ * if the last call that used `workspace` met bad data on the device,
+ * MSA_ERR_TIMEOUT if one of its kernels gave up a bounded wait, MSA_OK
+ * otherwise (or MSA_ERR_CUDA if the wait itself failed).
+ * msa_status_string: a static, readable description of a status.
+ */
+msa_status_t msa_check_device_error(void* workspace, msa_stream_t stream);
+const char* msa_status_string(msa_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

@@ -1,0 +1,95 @@
+"""The C-ABI library loads and exports every declared symbol; host-side validation (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    so = os.path.join(ROOT, "block_sparse_long_index_gb300", "libmsa.so")
+    if not os.path.exists(so):
+        import __graft_entry__
+        __graft_entry__.build()
+    from block_sparse_long_index_gb300 import msa
+    return msa
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "msa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    raw = lib.raw()
+    for n in names:
+        assert hasattr(raw, n), n
+    assert sorted(lib.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.msa_status_string(s)
+    assert "unknown" in lib.msa_status_string(99)
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+
+
+def test_select_validation(lib):
+    raw = lib.raw()
+    big = 1 << 30
+    assert raw.msa_select_blocks(None, FAKE, 1024, 1, 32, 64, 4, FAKE, FAKE, big, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_select_blocks(FAKE, FAKE, 0, 1, 32, 64, 4, FAKE, FAKE, big, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_select_blocks(FAKE, FAKE, 1024, 1, 48, 64, 4, FAKE, FAKE, big, None) == lib.MSA_ERR_UNSUPPORTED
+    assert raw.msa_select_blocks(FAKE, FAKE, 1024, 1, 32, 96, 4, FAKE, FAKE, big, None) == lib.MSA_ERR_UNSUPPORTED
+    assert raw.msa_select_blocks(FAKE, FAKE, 1024, 1, 32, 64, 33, FAKE, FAKE, big, None) == lib.MSA_ERR_UNSUPPORTED
+    assert raw.msa_select_blocks(FAKE, FAKE, 1024, 65, 32, 64, 4, FAKE, FAKE, big, None) == lib.MSA_ERR_UNSUPPORTED
+    mis = ctypes.c_void_p((1 << 20) + 2)
+    assert raw.msa_select_blocks(mis, FAKE, 1024, 1, 32, 64, 4, FAKE, FAKE, big, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    need = lib.msa_select_blocks_workspace(1024, 1, 32, 64, 4)
+    assert raw.msa_select_blocks(FAKE, FAKE, 1024, 1, 32, 64, 4, FAKE, FAKE, need - 1,
+                                 None) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    assert raw.msa_select_blocks(FAKE, FAKE, 1024, 1, 32, 64, 4, FAKE, None, need, None) == lib.MSA_ERR_INVALID_ARGUMENT
+
+
+def test_attention_and_decode_validation(lib):
+    raw = lib.raw()
+    s = lib.shape(4096, 8, 3, 128, 128, 128, 16)  # gs not an integer
+    assert raw.msa_sparse_attn_fwd(FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, 1 << 40,
+                                   None) == lib.MSA_ERR_INVALID_ARGUMENT
+    s = lib.shape(4096, 48, 3, 128, 128, 128, 16)  # gs = 16 unsupported
+    assert raw.msa_sparse_attn_fwd(FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, 1 << 40,
+                                   None) == lib.MSA_ERR_UNSUPPORTED
+    s = lib.shape(4096, 16, 2, 96, 128, 128, 16)  # d = 96 unsupported
+    assert raw.msa_sparse_attn_fwd(FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, 1 << 40,
+                                   None) == lib.MSA_ERR_UNSUPPORTED
+    s = lib.shape(4096, 16, 2, 128, 128, 128, 16)
+    assert raw.msa_sparse_attn_fwd(FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), -1.0, FAKE, FAKE, FAKE, 1 << 40,
+                                   None) == lib.MSA_ERR_INVALID_ARGUMENT
+    need = lib.msa_sparse_attn_fwd_workspace(s)
+    assert need > 256
+    assert raw.msa_sparse_attn_fwd(FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, need - 256,
+                                   None) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    d = lib.shape(1 << 20, 64, 16, 128, 128, 128, 16)  # decode supports at most 8 groups
+    assert raw.msa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, ctypes.byref(d), 0.1, FAKE, None, None, FAKE,
+                          1 << 40, None) == lib.MSA_ERR_UNSUPPORTED
+    d = lib.shape(1 << 20, 64, 8, 128, 128, 128, 16)
+    assert raw.msa_decode(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.byref(d), 0.1, FAKE, None, None, FAKE,
+                          1 << 40, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert lib.msa_decode_workspace(4, d) > 256
+
+
+def test_invert_validation(lib):
+    raw = lib.raw()
+    assert raw.msa_invert_blocks(None, 100, 1, 64, 4, FAKE, FAKE, FAKE, FAKE, 1 << 30, None) == \
+        lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_invert_blocks(FAKE, 100, 1, 64, 4, FAKE, FAKE, FAKE, FAKE, 1, None) == \
+        lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    assert lib.msa_invert_blocks_workspace(1 << 20, 8, 128, 16) > 256

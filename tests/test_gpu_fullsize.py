@@ -1,0 +1,123 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py times.
+
+The oracle checks 512 seeded query rows per head on the prefill configs (always
+including t = 0, Bk-1, Bk, N-1) and every sequence of the 1M decode config."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+from parity import bf16_tensor_to_f64, check_set_invariants, compare_attn, compare_sets, compare_sets_lazy
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _prefill_sampled(name, n_rows=512):
+    from block_sparse_long_index_gb300 import MsaPrefill
+    cfg = datagen.CONFIGS[name]
+    dev = datagen.prefill_device(cfg)
+    run = MsaPrefill(cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    out, lse, blk = run(dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"])
+    assert run.device_status() == 0
+    rows = datagen.sample_rows(cfg.N, n_rows, cfg.seed, must=(0, cfg.Bk - 1, cfg.Bk, cfg.N - 1))
+    rows_d = torch.from_numpy(rows).cuda()
+    gpu_blk = blk[:, rows_d].cpu().numpy()
+    out_pipe = bf16_tensor_to_f64(out[rows_d])
+    lse_pipe = lse[:, rows_d].T.cpu().numpy().astype(np.float64)
+    host = datagen.prefill_host(cfg, rows=rows)
+    check_set_invariants(gpu_blk, rows, cfg.Bk, cfg.k)
+    ora, kth = oracle.select_blocks(host["q_idx"], host["k_idx"], rows, cfg.N, cfg.Bk, cfg.k)
+    rep = compare_sets_lazy(gpu_blk, ora, kth, host["q_idx"], host["k_idx"], rows, cfg.N, cfg.Bk)
+    print(name, "sets", rep)
+    # needles picked by the sampled rows are selected
+    nd = host["needles"]
+    masks = datagen.pick_masks(cfg, nd, rows, rows, datagen.TID["pick"])
+    for i in range(len(rows)):
+        for g in range(cfg.G):
+            for n in range(nd.m):
+                if masks[i, g] >> n & 1:
+                    assert int(nd.blocks[0, g, n]) in set(gpu_blk[g, i].tolist())
+    scale = 1.0 / math.sqrt(cfg.d)
+    ref, ref_lse = oracle.sparse_attn(host["q"], host["k"], host["v"], ora, rows, cfg.Bk, scale)
+    # (1) the attention kernel on the oracle's sets at the sampled rows
+    blk2 = blk.clone()
+    blk2[:, rows_d] = torch.from_numpy(ora).cuda()
+    out2, lse2 = run.attend(dev["q"], dev["k"], dev["v"], blk2)
+    assert run.device_status() == 0
+    rep2 = compare_attn(bf16_tensor_to_f64(out2[rows_d]), lse2[:, rows_d].T.cpu().numpy().astype(np.float64), ref,
+                        ref_lse)
+    print(name, "attention on oracle sets", rep2)
+    # (2) the full pipeline on rows whose GPU set equals the oracle's
+    same = np.all(np.sort(gpu_blk, 2) == np.sort(ora, 2), axis=2)  # [G, R]
+    for g in range(cfg.G):
+        hs = slice(g * cfg.gs, (g + 1) * cfg.gs)
+        m = same[g]
+        compare_attn(out_pipe[m][:, hs], lse_pipe[m][:, hs], ref[m][:, hs], ref_lse[m][:, hs])
+    assert same.mean() > 0.95
+
+
+def test_prefill_32k_sampled():
+    _prefill_sampled("prefill_32k", n_rows=1024)
+
+
+def test_prefill_128k_sampled():
+    _prefill_sampled("prefill_128k")
+
+
+def test_prefill_1m_sampled():
+    _prefill_sampled("prefill_1m")
+
+
+def test_decode_1m_full():
+    from block_sparse_long_index_gb300 import MsaDecode
+    cfg = datagen.CONFIGS["decode_1m"]
+    dev = datagen.decode_device(cfg)
+    run = MsaDecode(cfg.B, cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    scale = 1.0 / math.sqrt(cfg.d)
+    out, lse, blk = run(dev["q_t"], dev["q_idx_t"], dev["k_idx_cache"], dev["k_cache"], dev["v_cache"],
+                        dev["ctx_len"], scale)
+    assert run.device_status() == 0
+    gpu_blk = blk.cpu().numpy()
+    ctx_len = dev["ctx_len_host"]
+    host = datagen.decode_host(cfg, ctx_len, want=("q_t", "q_idx_t", "k_idx_cache"))
+    check_set_invariants(gpu_blk.transpose(1, 0, 2), ctx_len - 1, cfg.Bk, cfg.k)
+    # the K/V rows the oracle reads: blocks chosen by either side (zero pages elsewhere are never touched)
+    kc = np.zeros((cfg.B, cfg.ctx, cfg.H_kv, cfg.d), np.uint16)
+    vc = np.zeros((cfg.B, cfg.ctx, cfg.H_kv, cfg.d), np.uint16)
+    sel_o = []
+    for b in range(cfg.B):
+        t = int(ctx_len[b]) - 1
+        o_b, kth_b = oracle.select_blocks(host["q_idx_t"][b:b + 1], host["k_idx_cache"][b, :t + 1], [t], t + 1,
+                                          cfg.Bk, cfg.k)
+        sel_o.append((o_b, kth_b))
+        blocks = set(o_b.reshape(-1).tolist()) | set(gpu_blk[b].reshape(-1).tolist())
+        toks = np.concatenate([np.arange(x * cfg.Bk, min((x + 1) * cfg.Bk, cfg.ctx)) for x in sorted(blocks) if x >= 0])
+        ids = b * cfg.ctx + toks
+        kc[b, toks] = datagen.host_normal_rows(ids, cfg.H_kv * cfg.d, cfg.seed, datagen.TID["k_cache"]).reshape(
+            -1, cfg.H_kv, cfg.d)
+        vc[b, toks] = datagen.host_normal_rows(ids, cfg.H_kv * cfg.d, cfg.seed, datagen.TID["v_cache"]).reshape(
+            -1, cfg.H_kv, cfg.d)
+    ref, ref_lse, ora_blk, kth = oracle.decode(host["q_t"], host["q_idx_t"], host["k_idx_cache"], kc, vc, ctx_len,
+                                               cfg.Bk, cfg.k, scale)
+    for b in range(cfg.B):
+        np.testing.assert_array_equal(sel_o[b][0][:, 0, :], ora_blk[b])
+    rep = compare_sets(gpu_blk.transpose(1, 0, 2), ora_blk.transpose(1, 0, 2), kth.transpose(1, 0, 2))
+    print("decode_1m sets", rep)
+    nd = host["needles"]
+    for b in range(cfg.B):
+        mk = datagen.pick_masks(cfg, nd, [b], [ctx_len[b] - 1], datagen.TID["pick_t"], s=b)[0]
+        for g in range(cfg.G):
+            for n in range(nd.m):
+                if mk[g] >> n & 1:
+                    assert int(nd.blocks[b, g, n]) in set(gpu_blk[b, g].tolist())
+    same = np.all(np.sort(gpu_blk, 2) == np.sort(ora_blk, 2), axis=2)
+    o, l = bf16_tensor_to_f64(out), lse.cpu().numpy().astype(np.float64)
+    for b in range(cfg.B):
+        for g in range(cfg.G):
+            if same[b, g]:
+                hs = slice(g * cfg.gs, (g + 1) * cfg.gs)
+                compare_attn(o[b:b + 1, hs], l[b:b + 1, hs], ref[b:b + 1, hs], ref_lse[b:b + 1, hs])
+    assert same.mean() >= 0.75

@@ -1,0 +1,267 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, at sizes the oracle
+finishes in seconds: several tiles, ragged tails, edge cases."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+from datagen import bf16_to_f64
+from parity import (bf16_tensor_to_f64, check_set_invariants, compare_attn, compare_sets, gamma_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def dev_bf16(a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+@pytest.fixture(scope="module")
+def msa():
+    from block_sparse_long_index_gb300 import msa as m
+    return m
+
+
+def run_select(msa, q_idx, k_idx, N, G, d_I, Bk, k):
+    blk = torch.full((G, N, k), -7, dtype=torch.int32, device="cuda")  # poisoned
+    ws = torch.empty(msa.msa_select_blocks_workspace(N, G, d_I, Bk, k), dtype=torch.uint8, device="cuda")
+    msa.msa_select_blocks(dev_bf16(q_idx), dev_bf16(k_idx), N, G, d_I, Bk, k, blk, ws)
+    assert msa.msa_check_device_error(ws) == 0
+    return blk.cpu().numpy()
+
+
+def run_attn(msa, q, kk, vv, blk, N, H_q, H_kv, d, d_I, Bk, k, scale):
+    shp = msa.shape(N, H_q, H_kv, d, d_I, Bk, k)
+    ws = torch.empty(msa.msa_sparse_attn_fwd_workspace(shp), dtype=torch.uint8, device="cuda")
+    out = torch.full((N, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((H_q, N), float("nan"), dtype=torch.float32, device="cuda")
+    b = blk if isinstance(blk, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(blk, np.int32)).cuda()
+    msa.msa_sparse_attn_fwd(dev_bf16(q) if not isinstance(q, torch.Tensor) else q,
+                            dev_bf16(kk) if not isinstance(kk, torch.Tensor) else kk,
+                            dev_bf16(vv) if not isinstance(vv, torch.Tensor) else vv, b, shp, scale, out, lse, ws)
+    status = msa.msa_check_device_error(ws)
+    return out, lse, status
+
+
+PREFILL_CASES = [
+    # name, N, H_q, H_kv, d, d_I, Bk, k, needles
+    ("tiny", None, None, None, None, None, None, None, None),
+    ("ragged_bk64", 1000, 8, 4, 64, 64, 64, 5, 2),
+    ("ragged_bk128_gs8", 2100, 16, 2, 128, 128, 128, 4, 3),
+    ("short_under_one_block", 50, 2, 1, 64, 32, 64, 4, 0),
+    ("k1_local_only", 777, 4, 2, 128, 32, 128, 1, 0),
+    ("k32_wide", 4096, 8, 8, 64, 128, 64, 32, 4),
+    ("gs1_bk128", 1536, 4, 4, 128, 64, 128, 6, 2),
+]
+
+
+def make_cfg(case):
+    name, N, H_q, H_kv, d, d_I, Bk, k, m = case
+    if name == "tiny":
+        return datagen.CONFIGS["tiny"]
+    return datagen.make_config(name, N=N, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k, needles=m)
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_select_parity_full_rows(msa, case):
+    cfg = make_cfg(case)
+    inp = datagen.prefill_host(cfg, want=("q_idx", "k_idx"))
+    rows = np.arange(cfg.N)
+    gpu = run_select(msa, inp["q_idx"], inp["k_idx"], cfg.N, cfg.G, cfg.d_I, cfg.Bk, cfg.k)
+    check_set_invariants(gpu, rows, cfg.Bk, cfg.k)
+    ora, kth = oracle.select_blocks(inp["q_idx"], inp["k_idx"], rows, cfg.N, cfg.Bk, cfg.k)
+    S = oracle.block_scores(inp["q_idx"], inp["k_idx"], rows, cfg.N, cfg.Bk)
+    gam = gamma_rows(bf16_to_f64(inp["q_idx"]), bf16_to_f64(inp["k_idx"]), rows, cfg.d_I)
+    rep = compare_sets(gpu, ora, kth, S=S, gamma=gam, rows=rows, Bk=cfg.Bk)
+    print(cfg.name, rep)
+    # planted needles are always selected
+    nd = inp["needles"]
+    if nd.m:
+        masks = datagen.pick_masks(cfg, nd, rows, rows, datagen.TID["pick"])
+        for t in range(cfg.N):
+            for g in range(cfg.G):
+                for n in range(nd.m):
+                    if masks[t, g] >> n & 1:
+                        assert int(nd.blocks[0, g, n]) in set(gpu[g, t].tolist())
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_attention_parity_on_oracle_sets(msa, case):
+    cfg = make_cfg(case)
+    inp = datagen.prefill_host(cfg)
+    rows = np.arange(cfg.N)
+    ora, _ = oracle.select_blocks(inp["q_idx"], inp["k_idx"], rows, cfg.N, cfg.Bk, cfg.k)
+    scale = 1.0 / math.sqrt(cfg.d)
+    out, lse, status = run_attn(msa, inp["q"], inp["k"], inp["v"], ora, cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I,
+                                cfg.Bk, cfg.k, scale)
+    assert status == 0
+    ref, ref_lse = oracle.sparse_attn(inp["q"], inp["k"], inp["v"], ora, rows, cfg.Bk, scale)
+    rep = compare_attn(bf16_tensor_to_f64(out), lse.T.cpu().numpy().astype(np.float64), ref, ref_lse)
+    print(cfg.name, rep)
+
+
+def test_pipeline_select_then_attend(msa):
+    """select -> attend on the GPU; outputs compared on rows whose set equals the oracle's."""
+    cfg = datagen.make_config("pipe", N=3000, H_q=16, H_kv=4, d=128, d_I=128, Bk=128, k=6, needles=3)
+    inp = datagen.prefill_host(cfg)
+    from block_sparse_long_index_gb300 import MsaPrefill
+    run = MsaPrefill(cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    out, lse, blk = run(dev_bf16(inp["q"]), dev_bf16(inp["k"]), dev_bf16(inp["v"]), dev_bf16(inp["q_idx"]),
+                        dev_bf16(inp["k_idx"]))
+    assert run.device_status() == 0
+    gpu_blk = blk.cpu().numpy()
+    rows = np.arange(cfg.N)
+    ora, _ = oracle.select_blocks(inp["q_idx"], inp["k_idx"], rows, cfg.N, cfg.Bk, cfg.k)
+    same = np.all(np.sort(gpu_blk, 2) == np.sort(ora, 2), axis=2)  # [G, N]
+    ref, ref_lse = oracle.sparse_attn(inp["q"], inp["k"], inp["v"], ora, rows, cfg.Bk, 1 / math.sqrt(cfg.d))
+    gs = cfg.gs
+    o, l = bf16_tensor_to_f64(out), lse.T.cpu().numpy().astype(np.float64)
+    for g in range(cfg.G):
+        m = same[g]
+        assert m.mean() > 0.9
+        heads = slice(g * gs, (g + 1) * gs)
+        compare_attn(o[:, heads][m], l[:, heads][m], ref[:, heads][m], ref_lse[:, heads][m])
+
+
+def test_attention_dense_special_case(msa):
+    """k >= number of blocks: MSA equals dense causal GQA attention."""
+    N, H_q, H_kv, d, Bk = 1100, 8, 2, 64, 64
+    k = (N + Bk - 1) // Bk
+    q = datagen.host_normal(N * H_q * d, 5, 1).reshape(N, H_q, d)
+    kk = datagen.host_normal(N * H_kv * d, 5, 2).reshape(N, H_kv, d)
+    vv = datagen.host_normal(N * H_kv * d, 5, 3).reshape(N, H_kv, d)
+    blk = np.full((H_kv, N, k), -1, np.int32)
+    for t in range(N):
+        loc = t // Bk
+        blk[:, t, 0] = loc
+        blk[:, t, 1:loc + 1] = np.arange(loc)
+    k_lim = min(k, 32)
+    blk = blk[:, :, :k_lim] if k > 32 else blk
+    if k > 32:
+        pytest.skip("k > 32 unsupported")
+    scale = 1 / math.sqrt(d)
+    out, lse, status = run_attn(msa, q, kk, vv, blk, N, H_q, H_kv, d, 32, Bk, k, scale)
+    assert status == 0
+    ref, ref_lse = oracle.dense_attn(q, kk, vv, np.arange(N), scale)
+    compare_attn(bf16_tensor_to_f64(out), lse.T.cpu().numpy().astype(np.float64), ref, ref_lse)
+
+
+def test_attention_empty_sets_and_future_blocks(msa):
+    """Rows whose set holds only -1 give out = 0, lse = -inf; ids past local(t) add nothing."""
+    N, H_q, H_kv, d, Bk, k = 640, 4, 2, 64, 64, 3
+    q = datagen.host_normal(N * H_q * d, 6, 1).reshape(N, H_q, d)
+    kk = datagen.host_normal(N * H_kv * d, 6, 2).reshape(N, H_kv, d)
+    vv = datagen.host_normal(N * H_kv * d, 6, 3).reshape(N, H_kv, d)
+    blk = np.full((H_kv, N, k), -1, np.int32)
+    rng = np.random.default_rng(0)
+    nb = N // Bk
+    for t in range(N):
+        if t % 5 == 0:
+            continue  # empty row
+        loc = t // Bk
+        blk[:, t, 0] = loc
+        blk[:, t, 1] = (loc + 1 + rng.integers(0, nb - 1)) % nb  # any other block, possibly a future one
+        if t % 11 == 0:
+            blk[:, t, 2] = loc  # a repeated id counts once
+    scale = 0.2
+    out, lse, status = run_attn(msa, q, kk, vv, blk, N, H_q, H_kv, d, 32, Bk, k, scale)
+    assert status == 0
+    ref, ref_lse = oracle.sparse_attn(q, kk, vv, blk, np.arange(N), Bk, scale)
+    compare_attn(bf16_tensor_to_f64(out), lse.T.cpu().numpy().astype(np.float64), ref, ref_lse)
+
+
+@pytest.mark.parametrize("N,G,Bk,k", [(1024, 1, 64, 4), (3001, 3, 128, 7), (5000, 8, 64, 16)])
+def test_invert_parity_bit_exact(msa, N, G, Bk, k):
+    """GPU B* equals the oracle's CSR bit for bit, on seeded random sets with holes."""
+    rng = np.random.default_rng(N + G)
+    blk = np.full((G, N, k), -1, np.int32)
+    for g in range(G):
+        for t in range(N):
+            loc = t // Bk
+            n = min(k, loc + 1)
+            ids = [loc] + list(rng.permutation(loc)[: n - 1]) if loc else [loc]
+            if t % 7 == 3 and n > 1:
+                ids = ids[:-1]
+            blk[g, t, : len(ids)] = ids
+    nb = (N + Bk - 1) // Bk
+    d_blk = torch.from_numpy(blk).cuda()
+    row_ptr = torch.full((G, nb + 1), -9, dtype=torch.int32, device="cuda")
+    entries = torch.full((G, N * k), -9, dtype=torch.int32, device="cuda")
+    n_ent = torch.full((G,), -9, dtype=torch.int32, device="cuda")
+    ws = torch.empty(msa.msa_invert_blocks_workspace(N, G, Bk, k), dtype=torch.uint8, device="cuda")
+    msa.msa_invert_blocks(d_blk, N, G, Bk, k, row_ptr, entries, n_ent, ws)
+    assert msa.msa_check_device_error(ws) == 0
+    rp, en, ne = oracle.invert_blocks(blk, Bk)
+    np.testing.assert_array_equal(row_ptr.cpu().numpy(), rp)
+    np.testing.assert_array_equal(n_ent.cpu().numpy(), ne)
+    e = entries.cpu().numpy()
+    for g in range(G):
+        np.testing.assert_array_equal(e[g, : ne[g]], en[g, : ne[g]])
+
+
+def test_bad_block_ids_raise_device_error_and_are_skipped(msa):
+    N, H_q, H_kv, d, Bk, k = 512, 2, 1, 64, 64, 3
+    q = datagen.host_normal(N * H_q * d, 8, 1).reshape(N, H_q, d)
+    kk = datagen.host_normal(N * H_kv * d, 8, 2).reshape(N, H_kv, d)
+    vv = datagen.host_normal(N * H_kv * d, 8, 3).reshape(N, H_kv, d)
+    blk = np.full((1, N, k), -1, np.int32)
+    blk[0, :, 0] = np.arange(N) // Bk
+    blk[0, 100, 1] = 10 ** 6    # out of range
+    blk[0, 200, 2] = -5         # negative, not -1
+    out, lse, status = run_attn(msa, q, kk, vv, blk, N, H_q, H_kv, d, 32, Bk, k, 0.125)
+    assert status == msa.MSA_ERR_BAD_INDEX
+    clean = blk.copy()
+    clean[0, 100, 1] = -1
+    clean[0, 200, 2] = -1
+    ref, ref_lse = oracle.sparse_attn(q, kk, vv, clean, np.arange(N), Bk, 0.125)
+    compare_attn(bf16_tensor_to_f64(out), lse.T.cpu().numpy().astype(np.float64), ref, ref_lse)
+
+
+DECODE_CASES = [
+    ("dec_small", 3, 5000, 8, 4, 128, 64, 64, 5, 2, [5000, 4097, 70]),
+    ("dec_bk128", 2, 20000, 16, 8, 128, 128, 128, 16, 4, [20000, 13000]),
+    ("dec_tiny_ctx", 2, 300, 4, 1, 64, 32, 64, 4, 1, [1, 300]),
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=[c[0] for c in DECODE_CASES])
+def test_decode_parity(msa, case):
+    name, B, C, H_q, H_kv, d, d_I, Bk, k, m, ctx_len = case
+    cfg = datagen.make_config(name, kind="decode", B=B, ctx=C, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k,
+                              needles=m)
+    ctx_len = np.asarray(ctx_len, np.int64)
+    inp = datagen.decode_host(cfg, ctx_len)
+    from block_sparse_long_index_gb300 import MsaDecode
+    run = MsaDecode(B, C, H_q, H_kv, d, d_I, Bk, k)
+    scale = 1 / math.sqrt(d)
+    out, lse, blk = run(dev_bf16(inp["q_t"]), dev_bf16(inp["q_idx_t"]), dev_bf16(inp["k_idx_cache"]),
+                        dev_bf16(inp["k_cache"]), dev_bf16(inp["v_cache"]),
+                        torch.from_numpy(ctx_len.astype(np.int32)).cuda(), scale)
+    assert run.device_status() == 0
+    ref, ref_lse, ora_blk, kth = oracle.decode(inp["q_t"], inp["q_idx_t"], inp["k_idx_cache"], inp["k_cache"],
+                                               inp["v_cache"], ctx_len, Bk, k, scale)
+    gpu_blk = blk.cpu().numpy()
+    check_set_invariants(gpu_blk.transpose(1, 0, 2), ctx_len - 1, Bk, k)
+    rep = compare_sets(gpu_blk.transpose(1, 0, 2), ora_blk.transpose(1, 0, 2), kth.transpose(1, 0, 2))
+    print(name, rep)
+    same = np.all(np.sort(gpu_blk, 2) == np.sort(ora_blk, 2), axis=2)  # [B, G]
+    o, l = bf16_tensor_to_f64(out), lse.cpu().numpy().astype(np.float64)
+    gs = H_q // H_kv
+    for b in range(B):
+        for g in range(H_kv):
+            if same[b, g]:
+                hs = slice(g * gs, (g + 1) * gs)
+                compare_attn(o[b:b + 1, hs], l[b:b + 1, hs], ref[b:b + 1, hs], ref_lse[b:b + 1, hs])
+    assert same.mean() >= 0.75
+
+
+def test_datagen_device_matches_host():
+    """The in-place device generator reproduces the host generator bit for bit."""
+    cfg = datagen.make_config("dgchk", N=4096, H_q=8, H_kv=2, d=64, d_I=128, Bk=128, k=8, needles=3)
+    host = datagen.prefill_host(cfg)
+    devi = datagen.prefill_device(cfg)
+    for name in ("q", "k", "v", "q_idx", "k_idx"):
+        a = devi[name].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(a, host[name]), name
