@@ -117,8 +117,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tile_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t n_gb = (int64_t)H_kv * nb;
   const int32_t total = tile_off[n_gb];
+  // a contiguous range of tiles per CTA: consecutive tiles mostly share (g, b), so K_b, V_b stay staged
+  const int32_t t_begin = (int32_t)((int64_t)total * blockIdx.x / gridDim.x);
+  const int32_t t_end = (int32_t)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  int64_t staged_gb = -1;
 
-  for (int32_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+  for (int32_t tile = t_begin; tile < t_end; ++tile) {
     // locate (g, b) of this tile: largest gb with tile_off[gb] <= tile
     int64_t l = 0, h = n_gb;
     while (h - l > 1) {
@@ -152,13 +156,16 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tile_kernel(
       const uint16_t* src = q + ((t < 0 ? 0 : t) * H_q + g * gs + hh) * D + c8 * 8;
       cp_async_16(Qs + r * LDS + c8 * 8, src, t < 0 ? 0 : 16);
     }
-    for (int i = tid; i < BK * (D / 8); i += kAttnThreads) {
-      int r = i / (D / 8), c8 = i % (D / 8);
-      int64_t key = b * BK + r;
-      bool ok = key < N;
-      int64_t kc = ok ? key : 0;
-      cp_async_16(Ks + r * LDS + c8 * 8, kk + (kc * H_kv + g) * D + c8 * 8, ok ? 16 : 0);
-      cp_async_16(Vs + r * LDS + c8 * 8, vv + (kc * H_kv + g) * D + c8 * 8, ok ? 16 : 0);
+    if (gb != staged_gb) {
+      for (int i = tid; i < BK * (D / 8); i += kAttnThreads) {
+        int r = i / (D / 8), c8 = i % (D / 8);
+        int64_t key = b * BK + r;
+        bool ok = key < N;
+        int64_t kc = ok ? key : 0;
+        cp_async_16(Ks + r * LDS + c8 * 8, kk + (kc * H_kv + g) * D + c8 * 8, ok ? 16 : 0);
+        cp_async_16(Vs + r * LDS + c8 * 8, vv + (kc * H_kv + g) * D + c8 * 8, ok ? 16 : 0);
+      }
+      staged_gb = gb;
     }
     cp_async_commit();
     cp_async_wait<0>();
@@ -277,66 +284,87 @@ __global__ void __launch_bounds__(kAttnThreads) attn_tile_kernel(
 }
 
 // ---------------------------------------------------------------- combine
+// One CTA per query position t: the position's partials (k slots x H_q heads x
+// d, contiguous) are read once, coalesced.  Slot s of group g contributes iff
+// its id is in [0, nb) and not repeated by an earlier slot (the set counts
+// each block once).  out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max),
+// lse = max + log(sum_s w_s); no contribution gives out = 0, lse = -inf.
 template <int D>
-__global__ void combine_kernel(const int32_t* __restrict__ block_idx, const uint16_t* __restrict__ part_o,
-                               const float* __restrict__ part_lse, int64_t N, int H_q, int gs, int k, int64_t nb,
-                               int64_t T0, int64_t slab_len, uint16_t* __restrict__ out, float* __restrict__ lse) {
-  constexpr int PER = D / 32;  // elements per lane
-  const int lane = threadIdx.x & 31;
-  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (w >= slab_len * H_q) return;
-  const int64_t tr = w / H_q;
-  const int h = (int)(w % H_q);
+__global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ block_idx,
+                                                      const uint16_t* __restrict__ part_o,
+                                                      const float* __restrict__ part_lse, int64_t N, int H_q, int G,
+                                                      int gs, int k, int64_t nb, int64_t T0,
+                                                      uint16_t* __restrict__ out, float* __restrict__ lse) {
+  extern __shared__ float cw[];          // [k][H_q] weights, then [H_q] 1/L
+  __shared__ uint32_t use_mask[64];      // per group: bit s set if slot s contributes
+  float* inv_l = cw + k * H_q;
+  const int tid = threadIdx.x;
+  const int64_t tr = blockIdx.x;
   const int64_t t = T0 + tr;
-  const int g = h / gs;
-  const int32_t* sel = block_idx + ((int64_t)g * N + t) * k;
-  // slot s contributes iff its id is in range and not repeated by an earlier slot (the set counts once)
-  uint32_t use = 0;
-  for (int s = 0; s < k; ++s) {
-    int32_t b = sel[s];
-    bool ok = b >= 0 && (int64_t)b < nb;
-    for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != b;
-    use |= (ok ? 1u : 0u) << s;
-  }
-  float m = __int_as_float(0xff800000);
-  for (int s = 0; s < k; ++s)
-    if (use >> s & 1u) m = fmaxf(m, part_lse[(tr * k + s) * H_q + h]);
-  float acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float L = 0.f;
-  if (m != __int_as_float(0xff800000)) {
+  for (int g = tid; g < G; g += blockDim.x) {
+    const int32_t* sel = block_idx + ((int64_t)g * N + t) * k;
+    uint32_t use = 0;
     for (int s = 0; s < k; ++s) {
-      if (!(use >> s & 1u)) continue;
-      float ls = part_lse[(tr * k + s) * H_q + h];
-      if (ls == __int_as_float(0xff800000)) continue;
-      float wgt = __expf(ls - m);
-      L += wgt;
-      const uint16_t* src = part_o + ((tr * k + s) * H_q + h) * D + lane * PER;
-      if (PER == 4) {
-        uint2 v = *reinterpret_cast<const uint2*>(src);
-        acc[0] += wgt * bf16_lo(v.x);
-        acc[1] += wgt * bf16_hi(v.x);
-        acc[2 % PER] += wgt * bf16_lo(v.y);
-        acc[3 % PER] += wgt * bf16_hi(v.y);
-      } else {
-        uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-        acc[0] += wgt * bf16_lo(v);
-        acc[1 % PER] += wgt * bf16_hi(v);
-      }
+      int32_t b = sel[s];
+      bool ok = b >= 0 && (int64_t)b < nb;
+      for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != b;
+      use |= (ok ? 1u : 0u) << s;
     }
+    use_mask[g] = use;
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  uint16_t* dst = out + (t * H_q + h) * D + lane * PER;
-  if (PER == 4) {
-    uint2 v;
-    v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16x2(acc[2 % PER] * inv, acc[3 % PER] * inv);
-    *reinterpret_cast<uint2*>(dst) = v;
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1 % PER] * inv);
+  __syncthreads();
+  const float* pl = part_lse + tr * k * H_q;
+  for (int i = tid; i < k * H_q; i += blockDim.x) {
+    const int s = i / H_q, h = i % H_q;
+    cw[i] = (use_mask[h / gs] >> s & 1u) ? pl[i] : __int_as_float(0xff800000);
   }
-  if (lane == 0) lse[(int64_t)h * N + t] = (L > 0.f) ? m + logf(L) : __int_as_float(0xff800000);
+  __syncthreads();
+  for (int h = tid; h < H_q; h += blockDim.x) {
+    float m = __int_as_float(0xff800000);
+    for (int s = 0; s < k; ++s) m = fmaxf(m, cw[s * H_q + h]);
+    float L = 0.f;
+    if (m != __int_as_float(0xff800000)) {
+      for (int s = 0; s < k; ++s) {
+        float w = __expf(cw[s * H_q + h] - m);  // exp(-inf) = 0 for unused slots
+        cw[s * H_q + h] = w;
+        L += w;
+      }
+    } else {
+      for (int s = 0; s < k; ++s) cw[s * H_q + h] = 0.f;
+    }
+    inv_l[h] = L > 0.f ? 1.f / L : 0.f;
+    lse[(int64_t)h * N + t] = L > 0.f ? m + logf(L) : __int_as_float(0xff800000);
+  }
+  __syncthreads();
+  constexpr int C8 = D / 8;
+  const uint16_t* po = part_o + tr * k * H_q * D;
+  for (int i = tid; i < H_q * C8; i += blockDim.x) {
+    const int h = i / C8, c8 = i % C8;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < k; ++s) {
+      const float w = cw[s * H_q + h];
+      if (w == 0.f) continue;
+      const uint4 v = *reinterpret_cast<const uint4*>(po + ((int64_t)s * H_q + h) * D + c8 * 8);
+      acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
+      acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
+      acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
+      acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
+      acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
+      acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
+      acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
+      acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+    }
+    const float il = inv_l[h];
+    uint4 o;
+    o.x = pack_bf16x2(acc[0] * il, acc[1] * il);
+    o.y = pack_bf16x2(acc[2] * il, acc[3] * il);
+    o.z = pack_bf16x2(acc[4] * il, acc[5] * il);
+    o.w = pack_bf16x2(acc[6] * il, acc[7] * il);
+    *reinterpret_cast<uint4*>(out + (t * H_q + h) * D + c8 * 8) = o;
+  }
 }
 
 // ---------------------------------------------------------------- scratch layout
@@ -431,14 +459,14 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
     else if (p.Bk == 64) e = launch_tiles<128, 64>(q, k, v, sc, p, T0, scale, s);
     else e = launch_tiles<128, 128>(q, k, v, sc, p, T0, scale, s);
     if (e != cudaSuccess) return e;
-    const int64_t warps = (T1 - T0) * p.H_q;
-    const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-    if (p.d == 64)
-      combine_kernel<64><<<blocks, 256, 0, s>>>(block_idx, sc.part_o, sc.part_lse, p.N, p.H_q, p.gs, p.k, p.nb, T0,
-                                                T1 - T0, (uint16_t*)out, lse);
-    else
-      combine_kernel<128><<<blocks, 256, 0, s>>>(block_idx, sc.part_o, sc.part_lse, p.N, p.H_q, p.gs, p.k, p.nb,
-                                                 T0, T1 - T0, (uint16_t*)out, lse);
+    const size_t cs = ((size_t)p.k * p.H_q + p.H_q) * sizeof(float);
+    auto ck = p.d == 64 ? combine_kernel<64> : combine_kernel<128>;
+    if (cs > 48 * 1024) {
+      e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cs);
+      if (e != cudaSuccess) return e;
+    }
+    ck<<<(unsigned)(T1 - T0), 256, cs, s>>>(block_idx, sc.part_o, sc.part_lse, p.N, p.H_q, G, p.gs, p.k, p.nb, T0,
+                                            (uint16_t*)out, lse);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -136,28 +136,55 @@ __global__ void __launch_bounds__(kScanThreads) decode_scan_kernel(
   }
 }
 
+// One warp per (sequence, group): each lane merges a strided subset of the
+// scan CTAs' candidate lists, then lane 0 merges the 32 lane lists.
 template <int CAP>
-__global__ void decode_merge_kernel(const float* __restrict__ cand_s, const int32_t* __restrict__ cand_b,
-                                    const int32_t* __restrict__ ctx_len, int64_t ctx_max, int Bk, int G, int k,
-                                    int splits, int32_t* __restrict__ block_idx) {
-  const int seq = blockIdx.x;
-  const int g = threadIdx.x;
-  if (g >= G) return;
+__global__ void __launch_bounds__(32) decode_merge_kernel(const float* __restrict__ cand_s,
+                                                          const int32_t* __restrict__ cand_b,
+                                                          const int32_t* __restrict__ ctx_len, int64_t ctx_max,
+                                                          int Bk, int G, int k, int splits,
+                                                          int32_t* __restrict__ block_idx) {
+  __shared__ float ls[32][CAP];
+  __shared__ int32_t lb[32][CAP];
+  const int seq = blockIdx.x, g = blockIdx.y, lane = threadIdx.x;
   const int64_t len = ctx_len[seq];
   int32_t* out = block_idx + ((int64_t)seq * G + g) * k;
   if (len < 1 || len > ctx_max) {
-    for (int i = 0; i < k; ++i) out[i] = -1;
+    for (int i = lane; i < k; i += 32) out[i] = -1;
     return;
   }
   TopK<CAP> m;
   m.init(k - 1);
-  for (int sp = 0; sp < splits; ++sp) {
+  for (int sp = lane; sp < splits; sp += 32) {
     const int64_t base = (((int64_t)seq * splits + sp) * G + g) * CAP;
+    float sv[CAP];
+    int32_t bv[CAP];
+#pragma unroll
+    for (int i = 0; i < CAP; ++i) {
+      sv[i] = cand_s[base + i];
+      bv[i] = cand_b[base + i];
+    }
+#pragma unroll
     for (int i = 0; i < CAP; ++i)
-      if (cand_b[base + i] >= 0) m.insert(cand_s[base + i], cand_b[base + i]);
+      if (bv[i] >= 0) m.insert(sv[i], bv[i]);
   }
-  out[0] = (int32_t)((len - 1) / Bk);
-  if (k > 1) m.emit(k - 1, out + 1);
+  int32_t ids[CAP];
+  float scs[CAP];
+  const int n = m.emit(CAP, ids, scs);
+  for (int i = 0; i < CAP; ++i) {
+    ls[lane][i] = i < n ? scs[i] : 0.f;
+    lb[lane][i] = i < n ? ids[i] : -1;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    TopK<CAP> f;
+    f.init(k - 1);
+    for (int l = 0; l < 32; ++l)
+      for (int i = 0; i < CAP; ++i)
+        if (lb[l][i] >= 0) f.insert(ls[l][i], lb[l][i]);
+    out[0] = (int32_t)((len - 1) / Bk);
+    if (k > 1) f.emit(k - 1, out + 1);
+  }
 }
 
 // One CTA per (slot, group, sequence): 128 threads.
@@ -317,8 +344,9 @@ cudaError_t launch_scan_merge(const void* q_idx_t, const void* k_idx_cache, cons
   decode_scan_kernel<DI, BK, CAP><<<grid, kScanThreads, 0, s>>>((const uint16_t*)q_idx_t,
                                                                 (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max,
                                                                 p.H_kv, p.k, p.splits, sc.cand_s, sc.cand_b, st);
-  decode_merge_kernel<CAP><<<p.B, 32, 0, s>>>(sc.cand_s, sc.cand_b, ctx_len, p.ctx_max, p.Bk, p.H_kv, p.k, p.splits,
-                                              blk);
+  decode_merge_kernel<CAP><<<dim3((unsigned)p.B, (unsigned)p.H_kv), 32, 0, s>>>(sc.cand_s, sc.cand_b, ctx_len,
+                                                                             p.ctx_max, p.Bk, p.H_kv, p.k,
+                                                                             p.splits, blk);
   return cudaGetLastError();
 }
 

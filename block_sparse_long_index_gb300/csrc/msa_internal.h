@@ -15,6 +15,12 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int num_sms();  // cached cudaDevAttrMultiProcessorCount of the current device
 
+// 2-D tiled TMA descriptor over a row-major bf16 matrix [rows, inner] with the
+// given row stride, box {box_inner, box_rows} and swizzle (0, 32, 64 or 128
+// bytes); out-of-bounds elements read as zero.  False if the driver refuses.
+bool encode_tmap_2d(void* tmap /* CUtensorMap */, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
+
 // ---- select (msa_select.cu)
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
                           int32_t* block_idx, DeviceStatus* st, cudaStream_t s);

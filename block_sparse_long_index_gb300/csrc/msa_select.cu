@@ -1,193 +1,337 @@
-// msa_select_blocks: index scoring + block max-pooling + local-pinned top-k.
+// msa_select_blocks: index scoring + block max-pooling + local-pinned top-k
+// on the 5th-generation tensor cores (tcgen05, TMEM accumulators, TMA).
 //
 // "MSA" study note 2-3 (s = q^I.k^I / sqrt(d_I); S = max over the block's
 // tokens j <= t; set = local block + top-k), 3-2 (max-pooling), 3-5
 // (exp-free top-k on raw scores) and Flash-MSA "プロキシアテンション"
-// (per-tile maxima inserted into a register top-k while sweeping keys; local
-// block pinned).
+// (per-tile maxima inserted into a register top-k while sweeping key tiles;
+// local block pinned).
 //
-// One CTA owns 128 consecutive query rows of one group.  Their index queries
-// stay in registers as MMA fragments; index-key tiles of 64 keys stream
-// through a double-buffered shared-memory ring.  A tile's 128x64 raw scores
-// live only in accumulator registers: each row takes its maximum over the
-// tile, folds it into the running block maximum and, at the end of a block,
-// offers (max, block) to a per-row top-(k-1) list held in registers.  No score
-// is ever written to memory.  Only blocks b < local(t) are candidates: for
-// every such block all its tokens satisfy j <= t, so no causal mask is
-// needed, and the local block is emitted directly as slot 0.
-#include "msa_common.cuh"
+// Work item = (query tile of 128 rows, quad of up to 4 GQA groups).  The
+// index key is shared by all groups, so one 64-key tile of k^I staged in
+// shared memory feeds GPC (<= 4) MMAs of 128 x 64 x d_I, one per group:
+//   warp 0      TMA producer: the item's q^I tiles (A, resident for the
+//               item) and a 4-stage ring of k^I tiles (B), 128B-swizzled;
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma into one of two
+//               accumulator buffers (GPC x 64 fp32 columns each) and commits
+//               completion to mbarriers;
+//   warps 2..9  epilogue: each thread owns one query row (a TMEM lane) for two
+//               of the groups, loads its 64 scores per group with tcgen05.ld,
+//               reduces them with 3-input max into the running block maximum
+//               and, when a block is complete, offers (max, block) to its
+//               register top-(k-1) list.  Scores never leave the SM.
+// Only blocks b < local(t) are candidates: every token of such a block is
+// visible (j <= t), so no causal mask is applied; the local block is written
+// directly as slot 0.  Items are visited longest-first in a snake order over
+// the persistent CTAs so the causal triangle balances.  Every wait is bounded
+// (about 2 s); on expiry the kernel raises the timeout flag, drains its own
+// asynchronous work and exits.
+#include "msa_sm100.cuh"
 
 namespace msa {
 
 namespace {
 
-constexpr int kRows = 128;   // query rows per CTA
-constexpr int kKeys = 64;    // keys per streamed tile
-constexpr int kThreads = 128;
+using namespace sm100;
 
-template <int DI, int BK, int CAP>
-__global__ void __launch_bounds__(kThreads) select_kernel(const uint16_t* __restrict__ q_idx,
-                                                          const uint16_t* __restrict__ k_idx, int64_t N, int G,
-                                                          int k, int32_t* __restrict__ block_idx) {
-  constexpr int LDS = DI + 8;  // padded row (elements): ldmatrix rows hit distinct banks
-  constexpr int KS = DI / 16;  // MMA k-steps
-  extern __shared__ __align__(16) uint16_t smem[];
-  uint16_t* Qs = smem;                  // [kRows][LDS]
-  uint16_t* Ks = smem + kRows * LDS;    // [2][kKeys][LDS]
+constexpr int kRows = 128;    // query rows per tile = MMA M
+constexpr int kKeys = 64;     // keys per tile = MMA N
+constexpr int kStages = 4;    // k^I ring depth
+constexpr int kMaxGpc = 4;    // groups per work item
+constexpr int kThreads = 320; // 10 warps
+constexpr int kEpiWarps = 8;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = blockIdx.y;
-  const int64_t n_tiles = (N + kRows - 1) / kRows;
-  const int64_t r0 = (n_tiles - 1 - (int64_t)blockIdx.x) * kRows;  // longest rows first
-  const int64_t t_last = min(r0 + kRows - 1, N - 1);
-  const int64_t n_kt = (t_last / BK) * BK / kKeys;  // key tiles before the last row's block
+template <int DI>
+struct SelectLayout {
+  static constexpr int CH_E = DI >= 64 ? 64 : DI;  // elements per swizzled row chunk
+  static constexpr int CH_B = CH_E * 2;             // 128 or 64 bytes
+  static constexpr int NCH = DI / CH_E;
+  static constexpr int A_CHUNK = kRows * CH_B;
+  static constexpr int B_CHUNK = kKeys * CH_B;
+  static constexpr int A_BYTES = kMaxGpc * NCH * A_CHUNK;
+  static constexpr int STAGE_BYTES = NCH * B_CHUNK;
+  static constexpr int KSTEPS = CH_E / 16;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = 1024 + A_BYTES + kStages * STAGE_BYTES + BAR_BYTES;
+};
 
-  // ---- index queries of the CTA's rows (zero rows past N)
-  for (int i = tid; i < kRows * (DI / 8); i += kThreads) {
-    int r = i / (DI / 8), c8 = i % (DI / 8);
-    int64_t t = r0 + r;
-    int64_t tc = t < N ? t : N - 1;
-    cp_async_16(Qs + r * LDS + c8 * 8, q_idx + (tc * G + g) * DI + c8 * 8, t < N ? 16 : 0);
+__device__ __forceinline__ bool next_item(int64_t& r, int64_t n_items, int64_t& j) {
+  // snake order over the persistent CTAs: round r visits items [r*grid, (r+1)*grid)
+  while (true) {
+    const int64_t base = r * gridDim.x;
+    if (base >= n_items) return false;
+    const int64_t c = (r & 1) ? (int64_t)gridDim.x - 1 - blockIdx.x : (int64_t)blockIdx.x;
+    ++r;
+    j = base + c;
+    if (j < n_items) return true;
   }
-  cp_async_commit();
+}
 
-  auto load_keys = [&](int64_t kt, int buf) {
-    uint16_t* dst = Ks + buf * kKeys * LDS;
-    for (int i = tid; i < kKeys * (DI / 8); i += kThreads) {
-      int r = i / (DI / 8), c8 = i % (DI / 8);
-      cp_async_16(dst + r * LDS + c8 * 8, k_idx + (kt * kKeys + r) * DI + c8 * 8, 16);
+template <int DI, int CAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     int64_t N, int G, int gpc, int Bk, int k, int32_t* __restrict__ block_idx, DeviceStatus* st) {
+  using L = SelectLayout<DI>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + L::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * L::STAGE_BYTES);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t a_full = bar0 + 8u * (2 * kStages);
+  const uint32_t a_empty = a_full + 8u;
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * kStages + 4 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 6);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int acc_cols = kMaxGpc * kKeys;  // columns per accumulator buffer
+  const uint32_t tmem_cols = 2 * acc_cols;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
     }
-    cp_async_commit();
-  };
-  if (n_kt > 0) load_keys(0, 0);
+    mbar_init(a_full, 1);
+    mbar_init(a_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_q);
+    prefetch_tmap(&tmap_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), tmem_cols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
 
-  // owner row of this thread: quad lane c owns (m-tile c>>1, half c&1)
-  const int c = lane & 3;
-  const int64_t t_own = r0 + warp * 32 + 16 * (c >> 1) + 8 * (c & 1) + (lane >> 2);
-  const int64_t local_own = t_own / BK;
+  const int64_t n_qt = (N + kRows - 1) / kRows;
+  const int n_gq = G / gpc;
+  const int64_t n_items = n_qt * n_gq;
+  auto n_kt_of = [&](int64_t qb) -> int64_t { return Bk == 128 ? 2 * qb : 2 * qb + 1; };
 
-  TopK<CAP> top;
-  top.init(k - 1);
-  float run = __int_as_float(0xff800000);
-
-  if (n_kt > 0) {
-    cp_async_wait<1>();
-    __syncthreads();
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t kt_glob = 0, a_glob = 0;
+      int last_phase[kStages];
+      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+      int a_last = -1;
+      int64_t r = 0, j;
+      bool ok = true;
+      while (ok && next_item(r, n_items, j)) {
+        const int64_t qb = n_qt - 1 - j / n_gq;
+        const int gq = (int)(j % n_gq);
+        const int64_t nkt = n_kt_of(qb);
+        if (nkt == 0) continue;
+        if (!(ok = mbar_wait(a_empty, (a_glob & 1) ^ 1, abort, st, 0x101))) break;
+        mbar_arrive_expect_tx(a_full, (uint32_t)(gpc * L::NCH * L::A_CHUNK));
+        for (int gi = 0; gi < gpc; ++gi)
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(smem_u32(sA + (gi * L::NCH + c) * L::A_CHUNK), &tmap_q,
+                        (gq * gpc + gi) * DI + c * L::CH_E, (int32_t)(qb * kRows), a_full);
+        a_last = a_glob & 1;
+        ++a_glob;
+        for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
+          const int s = kt_glob % kStages;
+          const uint32_t ph = (kt_glob / kStages) & 1;
+          if (!(ok = mbar_wait(empty_bar(s), ph ^ 1, abort, st, 0x102))) break;
+          mbar_arrive_expect_tx(full_bar(s), (uint32_t)L::STAGE_BYTES);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_2d(smem_u32(sB + s * L::STAGE_BYTES + c * L::B_CHUNK), &tmap_k, c * L::CH_E,
+                        (int32_t)(kt * kKeys), full_bar(s));
+          last_phase[s] = (int)ph;
+        }
+      }
+      if (!ok) {  // let our own copies land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (last_phase[s] >= 0) mbar_wait(full_bar(s), (uint32_t)last_phase[s], nullptr, st, 0x1F1);
+        if (a_last >= 0) mbar_wait(a_full, (uint32_t)a_last, nullptr, st, 0x1F2);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(kRows, kKeys);
+      uint32_t kt_glob = 0, a_glob = 0, acc_glob = 0;
+      int64_t r = 0, j;
+      bool ok = true;
+      while (ok && next_item(r, n_items, j)) {
+        const int64_t qb = n_qt - 1 - j / n_gq;
+        const int64_t nkt = n_kt_of(qb);
+        if (nkt == 0) continue;
+        if (!(ok = mbar_wait(a_full, a_glob & 1, abort, st, 0x201))) break;
+        tc_fence_after();
+        for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob, ++acc_glob) {
+          const int s = kt_glob % kStages;
+          if (!(ok = mbar_wait(full_bar(s), (kt_glob / kStages) & 1, abort, st, 0x202))) break;
+          const int buf = acc_glob & 1;
+          if (!(ok = mbar_wait(acc_empty(buf), ((acc_glob >> 1) & 1) ^ 1, abort, st, 0x203))) break;
+          tc_fence_after();
+          for (int gi = 0; gi < gpc; ++gi) {
+            const uint32_t d = tmem + (uint32_t)(buf * acc_cols + gi * kKeys);
+#pragma unroll
+            for (int c = 0; c < L::NCH; ++c)
+#pragma unroll
+              for (int kk = 0; kk < L::KSTEPS; ++kk) {
+                const uint64_t ad = umma_desc_kmajor(smem_u32(sA + (gi * L::NCH + c) * L::A_CHUNK + kk * 32), L::CH_B);
+                const uint64_t bd =
+                    umma_desc_kmajor(smem_u32(sB + s * L::STAGE_BYTES + c * L::B_CHUNK + kk * 32), L::CH_B);
+                mma_bf16_ss(d, ad, bd, IDESC, (c | kk) != 0);
+              }
+          }
+          umma_commit(empty_bar(s));
+          umma_commit(acc_full(buf));
+        }
+        if (!ok) break;
+        umma_commit(a_empty);
+        ++a_glob;
+      }
+      if (!ok) {  // wait for the MMAs already issued before TMEM is released
+        umma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, nullptr, st, 0x2F1);
+      }
+    }
   } else {
-    cp_async_wait<0>();
-    __syncthreads();
-  }
-  uint32_t qf[2][KS][4];
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+    const int half = (warp - 2) >> 2;         // which pair of groups
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    uint32_t acc_glob = 0;
+    int64_t r = 0, j;
+    bool ok = true;
+    TopK<CAP> top0, top1;
+    while (ok && next_item(r, n_items, j)) {
+      const int64_t qb = n_qt - 1 - j / n_gq;
+      const int gq = (int)(j % n_gq);
+      const int64_t nkt = n_kt_of(qb);
+      const int64_t t = qb * kRows + row;
+      const int64_t local = t / Bk;
+      const int gi0 = half * 2, gi1 = half * 2 + 1;
+      const bool has0 = gi0 < gpc, has1 = gi1 < gpc;
+      top0.init(k - 1);
+      top1.init(k - 1);
+      float run0 = __int_as_float(0xff800000), run1 = run0;
+      for (int64_t kt = 0; kt < nkt; ++kt, ++acc_glob) {
+        const int buf = acc_glob & 1;
+        if (!(ok = mbar_wait(acc_full(buf), (acc_glob >> 1) & 1, abort, st, 0x301))) break;
+        tc_fence_after();
+        const uint32_t col = (uint32_t)(buf * acc_cols);
+        if (has0) {
+          uint32_t x[32], y[32];
+          tmem_ld_x32(tmem + lane_base + col + gi0 * kKeys, x);
+          tmem_ld_x32(tmem + lane_base + col + gi0 * kKeys + 32, y);
+          tmem_ld_wait();
+          float m = run0;
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
+          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const uint16_t* p = Qs + (warp * 32 + mt * 16 + (lane & 15)) * LDS + ks * 16 + 8 * (lane >> 4);
-      ldmatrix_x4(qf[mt][ks][0], qf[mt][ks][1], qf[mt][ks][2], qf[mt][ks][3], p);
-    }
-
-  for (int64_t kt = 0; kt < n_kt; ++kt) {
-    if (kt + 1 < n_kt) {
-      load_keys(kt + 1, (int)((kt + 1) & 1));
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const uint16_t* Kb = Ks + (int)(kt & 1) * kKeys * LDS;
-
-    float acc[2][kKeys / 8][4];
+          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+          run0 = m;
+        }
+        if (has1) {
+          uint32_t x[32], y[32];
+          tmem_ld_x32(tmem + lane_base + col + gi1 * kKeys, x);
+          tmem_ld_x32(tmem + lane_base + col + gi1 * kKeys + 32, y);
+          tmem_ld_wait();
+          float m = run1;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
 #pragma unroll
-      for (int nt = 0; nt < kKeys / 8; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
-
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-      for (int np = 0; np < kKeys / 16; ++np) {
-        uint32_t b0[2], b1[2];
-        const uint16_t* p = Kb + (np * 16 + (lane & 7) + 8 * (lane >> 4)) * LDS + ks * 16 + 8 * ((lane >> 3) & 1);
-        ldmatrix_x4(b0[0], b0[1], b1[0], b1[1], p);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          mma_bf16_16816(acc[mt][2 * np], qf[mt][ks], b0);
-          mma_bf16_16816(acc[mt][2 * np + 1], qf[mt][ks], b1);
+          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+          run1 = m;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(buf));
+        if (Bk == kKeys || (kt & 1)) {  // block (kt for Bk=64, kt/2 for Bk=128) complete
+          const int b = (int)(Bk == kKeys ? kt : kt >> 1);
+          if (b < local) {
+            if (has0) top0.insert(run0, b);
+            if (has1) top1.insert(run1, b);
+          }
+          run0 = __int_as_float(0xff800000);
+          run1 = run0;
+        }
+      }
+      if (!ok) break;
+      if (t < N) {
+        if (has0) {
+          int32_t* out = block_idx + ((int64_t)(gq * gpc + gi0) * N + t) * k;
+          out[0] = (int32_t)local;
+          if (k > 1) top0.emit(k - 1, out + 1);
+        }
+        if (has1) {
+          int32_t* out = block_idx + ((int64_t)(gq * gpc + gi1) * N + t) * k;
+          out[0] = (int32_t)local;
+          if (k > 1) top1.emit(k - 1, out + 1);
         }
       }
     }
-    __syncthreads();  // the buffer just read is refilled by the next prefetch
-
-    // row maxima of the tile: quad-local max over the thread's columns, then across the quad
-    float rm[2][2];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float m = fmaxf(acc[mt][0][2 * h], acc[mt][0][2 * h + 1]);
-#pragma unroll
-        for (int nt = 1; nt < kKeys / 8; ++nt) m = fmaxf(m, fmaxf(acc[mt][nt][2 * h], acc[mt][nt][2 * h + 1]));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        rm[mt][h] = m;
-      }
-    float mine = (c == 0) ? rm[0][0] : (c == 1) ? rm[0][1] : (c == 2) ? rm[1][0] : rm[1][1];
-    run = fmaxf(run, mine);
-    const int64_t key_end = (kt + 1) * kKeys;
-    if (key_end % BK == 0) {  // a block is complete
-      int b = (int)(key_end / BK) - 1;
-      if (b < local_own) top.insert(run, b);
-      run = __int_as_float(0xff800000);
-    }
   }
 
-  if (t_own < N) {
-    int32_t* out = block_idx + ((int64_t)g * N + t_own) * k;
-    out[0] = (int32_t)local_own;
-    if (k > 1) top.emit(k - 1, out + 1);
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
-template <int DI, int BK, int CAP>
-cudaError_t launch_t(const void* q_idx, const void* k_idx, int64_t N, int G, int k, int32_t* block_idx,
-                     cudaStream_t s) {
-  constexpr int LDS = DI + 8;
-  const size_t smem = (size_t)(kRows + 2 * kKeys) * LDS * sizeof(uint16_t);
-  auto kern = select_kernel<DI, BK, CAP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+template <int DI, int CAP>
+cudaError_t launch_t(const void* q_idx, const void* k_idx, int64_t N, int G, int gpc, int Bk, int k,
+                     int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
+  using L = SelectLayout<DI>;
+  CUtensorMap tq, tk;
+  if (!encode_tmap_2d(&tq, q_idx, (uint64_t)G * DI, (uint64_t)N, (uint64_t)G * DI * 2, L::CH_E, kRows, L::CH_B))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tk, k_idx, (uint64_t)DI, (uint64_t)N, (uint64_t)DI * 2, L::CH_E, kKeys, L::CH_B))
+    return cudaErrorInvalidValue;
+  auto kern = select_tc_kernel<DI, CAP>;
+  // more than half of an SM's shared memory: one CTA per SM, so the 512 TMEM columns are always free
+  const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((N + kRows - 1) / kRows), (unsigned)G);
-  kern<<<grid, kThreads, smem, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, N, G, k, block_idx);
+  const int64_t n_items = ((N + kRows - 1) / kRows) * (G / gpc);
+  const int grid = (int)(n_items < num_sms() ? n_items : num_sms());
+  kern<<<grid, kThreads, smem, s>>>(tq, tk, N, G, gpc, Bk, k, block_idx, st);
   return cudaGetLastError();
 }
 
-template <int DI, int BK>
-cudaError_t launch_cap(const void* q_idx, const void* k_idx, int64_t N, int G, int k, int32_t* block_idx,
-                       cudaStream_t s) {
-  int km1 = k - 1;
-  if (km1 <= 4) return launch_t<DI, BK, 4>(q_idx, k_idx, N, G, k, block_idx, s);
-  if (km1 <= 8) return launch_t<DI, BK, 8>(q_idx, k_idx, N, G, k, block_idx, s);
-  if (km1 <= 16) return launch_t<DI, BK, 16>(q_idx, k_idx, N, G, k, block_idx, s);
-  return launch_t<DI, BK, 32>(q_idx, k_idx, N, G, k, block_idx, s);
-}
-
 template <int DI>
-cudaError_t launch_bk(const void* q_idx, const void* k_idx, int64_t N, int G, int Bk, int k, int32_t* block_idx,
-                      cudaStream_t s) {
-  if (Bk == 64) return launch_cap<DI, 64>(q_idx, k_idx, N, G, k, block_idx, s);
-  return launch_cap<DI, 128>(q_idx, k_idx, N, G, k, block_idx, s);
+cudaError_t launch_cap(const void* q_idx, const void* k_idx, int64_t N, int G, int gpc, int Bk, int k,
+                       int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
+  const int km1 = k - 1;
+  if (km1 <= 4) return launch_t<DI, 4>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (km1 <= 8) return launch_t<DI, 8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (km1 <= 16) return launch_t<DI, 16>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  return launch_t<DI, 32>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
 }
 
 }  // namespace
 
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
                           int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
-  (void)st;
-  if (d_I == 32) return launch_bk<32>(q_idx, k_idx, N, G, Bk, k, block_idx, s);
-  if (d_I == 64) return launch_bk<64>(q_idx, k_idx, N, G, Bk, k, block_idx, s);
-  return launch_bk<128>(q_idx, k_idx, N, G, Bk, k, block_idx, s);
+  const int gpc = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+  if (d_I == 32) return launch_cap<32>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (d_I == 64) return launch_cap<64>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  return launch_cap<128>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
 }
 
 }  // namespace msa
