@@ -190,6 +190,33 @@ msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_
                                    block_idx, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
 }
 
+// The decode step without a caller workspace: its scratch is the library's
+// fixed device array (see msa_decode.cu), so this call allocates nothing.
+msa_status_t msa_decode_noalloc(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                                const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape,
+                                float scale, void* out, float* lse, int32_t* block_idx, msa_stream_t stream) {
+  if (!q_t || !q_idx_t || !k_idx_cache || !k_cache || !v_cache || !ctx_len || !out) return MSA_ERR_INVALID_ARGUMENT;
+  if (B < 1) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (shape->H_kv > 8) return MSA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q_t) || !aligned16(q_idx_t) || !aligned16(k_idx_cache) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || ((uintptr_t)ctx_len & 3u) || ((uintptr_t)out & 1u) || ((uintptr_t)lse & 3u) ||
+      ((uintptr_t)block_idx & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  const msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,
+                                             shape->k);
+  const size_t need = kHeader + msa::decode_scratch_bytes(p);
+  if (need > msa::kNoAllocScratchBytes) return MSA_ERR_WORKSPACE_TOO_SMALL;  // beyond the fixed array
+  void* scratch = nullptr;
+  if (msa::noalloc_scratch(need, &scratch) != cudaSuccess || !scratch) return MSA_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(scratch, 0, kHeader, s) != cudaSuccess) return MSA_ERR_CUDA;  // the status word starts clear
+  return finish(msa::launch_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, p, scale, out, lse,
+                                   block_idx, (char*)scratch + kHeader, (msa::DeviceStatus*)scratch, s));
+}
+
 msa_status_t msa_check_device_error(void* workspace, msa_stream_t stream) {
   if (!workspace) return MSA_ERR_INVALID_ARGUMENT;
   if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MSA_ERR_CUDA;

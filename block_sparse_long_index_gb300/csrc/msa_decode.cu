@@ -17,6 +17,8 @@
 //   4. combine: per (sequence, head) the partials are merged by their lse.
 #include <math.h>
 
+#include <mutex>
+
 #include "msa_common.cuh"
 
 namespace msa {
@@ -426,6 +428,35 @@ cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_id
   else
     decode_combine_kernel<128><<<p.B * p.H_q, 128, 0, s>>>(sc.part_o, sc.part_lse, p.H_q, p.k, (uint16_t*)out, lse);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- fixed scratch for msa_decode_noalloc
+// Scratch of the decode step for callers that cannot allocate device memory:
+// a file-scope device array, resident on every GPU that loads the library
+// until the process exits.  In host code `g_noalloc_scratch` names a host-side
+// shadow, not device memory, so kernels only ever receive the address looked
+// up below with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t noalloc_scratch(size_t need, void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  *out = nullptr;
+  if (need > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {  // once per device, with that device current
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace msa

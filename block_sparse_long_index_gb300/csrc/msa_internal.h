@@ -63,4 +63,10 @@ cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_id
                           const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
                           float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s);
 
+// Fixed device scratch of msa_decode_noalloc (8 MiB, shared by all calls on a
+// device).  Returns its device address for the current device (looked up on
+// the first call per device), or an error if `need` exceeds it.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+cudaError_t noalloc_scratch(size_t need, void** out);
+
 }  // namespace msa

@@ -45,6 +45,7 @@ _SIGS = {
     "msa_sparse_attn_fwd": (_I, [_P, _P, _P, _P, _SP, _F, _P, _P, _P, _SZ, _P]),
     "msa_decode_workspace": (_SZ, [_I, _SP]),
     "msa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
+    "msa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P]),
     "msa_check_device_error": (_I, [_P, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -135,6 +136,15 @@ def msa_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shp, sca
     return _check(_lib.msa_decode(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_cache), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(ctx_len), B, ctypes.byref(shp), float(scale), _ptr(out), _ptr(lse),
                                   _ptr(block_idx), _ptr(workspace), wb, _stream(stream)), "msa_decode")
+
+
+def msa_decode_noalloc(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shp, scale, out, lse, block_idx,
+                       stream=None):
+    """msa_decode without a workspace, for callers that may not allocate device memory (the library's
+    fixed 8 MiB device array is the scratch; calls on one device must not overlap)."""
+    return _check(_lib.msa_decode_noalloc(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_cache), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(ctx_len), B, ctypes.byref(shp), float(scale), _ptr(out), _ptr(lse),
+                                          _ptr(block_idx), _stream(stream)), "msa_decode_noalloc")
 
 
 def msa_check_device_error(workspace, stream=None):

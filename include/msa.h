@@ -163,6 +163,36 @@ msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_
                         void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
                         msa_stream_t stream);
 
+/* ---------------------------------------------------------------- decode without allocation
+ * The same decode step as msa_decode, for callers that cannot allocate device
+ * memory: for instance a plugin whose host application owns every byte of the
+ * GPU, or a serving loop that must not call cudaMalloc because it can block
+ * and synchronize the device mid-step.  The pages have no counterpart of this
+ * call; it exists only for such callers.
+ *
+ * No workspace argument: the scratch is a fixed 8 MiB array that the library
+ * keeps in device memory on every GPU that loads it, until the process exits.
+ * The call makes no allocation of any kind (no cudaMalloc/cudaFree, no
+ * allocating library routine).  Arguments, layouts and outputs are those of
+ * msa_decode.
+ *   - The first call on a device looks up the array's device address for that
+ *     device (cudaGetSymbolAddress, with the device current); make that first
+ *     call before any stream capture.
+ *   - Shapes whose scratch (what msa_decode_workspace() reports for them)
+ *     exceeds 8 MiB are rejected with MSA_ERR_WORKSPACE_TOO_SMALL before any
+ *     launch.  B = 4, H_q = 64, H_kv = 8, d = 128, k = 16 needs about 2.4 MiB.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents; each call clears what must start at zero.  Two calls
+ *     that can overlap on the GPU (different streams, or different host
+ *     threads) race on it: order them on one stream.
+ *   - Device-side bad data (ctx_len outside [1, N]) still zeroes that
+ *     sequence's outputs, but the error word lives in the shared array and is
+ *     not reported by this call.
+ */
+msa_status_t msa_decode_noalloc(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                                const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape,
+                                float scale, void* out, float* lse, int32_t* block_idx, msa_stream_t stream);
+
 /* ---------------------------------------------------------------- status
  * msa_check_device_error: waits for `stream`, then returns MSA_ERR_BAD_INDEX
  * if the last call that used `workspace` met bad data on the device,
