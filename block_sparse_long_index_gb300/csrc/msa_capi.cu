@@ -24,8 +24,7 @@ int num_sms() {
   return cached;
 }
 
-bool encode_tmap_2d(void* tmap, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
-                    uint32_t box_inner, uint32_t box_rows, int swizzle_bytes) {
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -33,20 +32,46 @@ bool encode_tmap_2d(void* tmap, const void* base, uint64_t inner, uint64_t rows,
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess || !fn)
-      return false;
+      return nullptr;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  CUtensorMapSwizzle sw = swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
-                          : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                          : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                                : CU_TENSOR_MAP_SWIZZLE_NONE;
+  return encode;
+}
+
+static CUtensorMapSwizzle swizzle_of(int swizzle_bytes) {
+  return swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+         : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+         : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                               : CU_TENSOR_MAP_SWIZZLE_NONE;
+}
+
+bool encode_tmap_2d(void* tmap, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                    uint32_t box_inner, uint32_t box_rows, int swizzle_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle_of(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                    uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      swizzle_of(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

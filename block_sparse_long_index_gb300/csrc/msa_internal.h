@@ -20,6 +20,9 @@ int num_sms();  // cached cudaDevAttrMultiProcessorCount of the current device
 // bytes); out-of-bounds elements read as zero.  False if the driver refuses.
 bool encode_tmap_2d(void* tmap /* CUtensorMap */, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
+// 3-D variant: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1 and 2, box {b0, b1, b2}.
+bool encode_tmap_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                    uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes);
 
 // ---- select (msa_select.cu)
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
@@ -47,6 +50,11 @@ struct AttnPlan {
 };
 AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k);
 size_t attn_scratch_bytes(const AttnPlan& p);
+// The tcgen05 tile kernel of one query slab (msa_attn_tile.cu).
+cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const int32_t* entries, const int32_t* lo,
+                              const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d,
+                              int Bk, int k_blocks, int64_t nb, int gs, int P, int64_t T0, float scale,
+                              uint16_t* part_o, float* part_lse, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);
 
