@@ -11,7 +11,8 @@
 //               shared-memory staging is needed) and scores all groups at once
 //               (16 keys x 8 groups x d_I per mma chain); block maxima feed a
 //               per-group top-(k-1) list per warp, merged per CTA.
-//   2. merge:   per (sequence, group) the CTAs' candidates -> block set.
+//   2. merge:   per (sequence, group) a tournament over the CTAs' candidate
+//               lists -> block set.
 //   3. attend:  per (sequence, group, slot) one CTA reads that block's K/V
 //               rows and produces each group head's partial (O, lse).
 //   4. combine: per (sequence, head) the partials are merged by their lse.
@@ -19,7 +20,7 @@
 
 #include <mutex>
 
-#include "msa_common.cuh"
+#include "msa_sm100.cuh"
 
 namespace msa {
 
@@ -138,54 +139,71 @@ __global__ void __launch_bounds__(kScanThreads) decode_scan_kernel(
   }
 }
 
-// One warp per (sequence, group): each lane merges a strided subset of the
-// scan CTAs' candidate lists, then lane 0 merges the 32 lane lists.
+// One CTA per (sequence, group): a tournament over the scan CTAs' candidate
+// lists (each sorted best-first).  Thread i holds the head of list i (and of
+// lists i + blockDim, ...); each of the k-1 rounds takes the best head in the
+// CTA (larger score, then smaller block id) and advances the winner's list.
+__device__ __forceinline__ uint64_t rank_key(float s, int32_t b) {
+  // larger key = better pair: scores ordered as unsigned integers, ties to the smaller block
+  uint32_t u = __float_as_uint(s);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)b);
+}
+
 template <int CAP>
-__global__ void __launch_bounds__(32) decode_merge_kernel(const float* __restrict__ cand_s,
-                                                          const int32_t* __restrict__ cand_b,
-                                                          const int32_t* __restrict__ ctx_len, int64_t ctx_max,
-                                                          int Bk, int G, int k, int splits,
-                                                          int32_t* __restrict__ block_idx) {
-  __shared__ float ls[32][CAP];
-  __shared__ int32_t lb[32][CAP];
-  const int seq = blockIdx.x, g = blockIdx.y, lane = threadIdx.x;
+__global__ void __launch_bounds__(1024) decode_merge_kernel(const float* __restrict__ cand_s,
+                                                            const int32_t* __restrict__ cand_b,
+                                                            const int32_t* __restrict__ ctx_len, int64_t ctx_max,
+                                                            int Bk, int G, int k, int splits,
+                                                            int32_t* __restrict__ block_idx) {
+  __shared__ uint64_t warp_best[32];
+  const int seq = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
   const int64_t len = ctx_len[seq];
   int32_t* out = block_idx + ((int64_t)seq * G + g) * k;
   if (len < 1 || len > ctx_max) {
-    for (int i = lane; i < k; i += 32) out[i] = -1;
+    for (int i = tid; i < k; i += blockDim.x) out[i] = -1;
     return;
   }
-  TopK<CAP> m;
-  m.init(k - 1);
-  for (int sp = lane; sp < splits; sp += 32) {
-    const int64_t base = (((int64_t)seq * splits + sp) * G + g) * CAP;
-    float sv[CAP];
-    int32_t bv[CAP];
+  // this thread's lists: tid, tid + blockDim, ...; pos[] = next unread entry of each
+  auto list_base = [&](int sp) { return (((int64_t)seq * splits + sp) * G + g) * CAP; };
+  auto head_key = [&](int sp, int p) -> uint64_t {
+    if (p >= CAP) return 0;
+    const int32_t b = cand_b[list_base(sp) + p];
+    return b < 0 ? 0 : rank_key(cand_s[list_base(sp) + p], b);
+  };
+  constexpr int kMaxLists = 4;  // lists per thread (splits <= 4 * 1024)
+  int pos[kMaxLists];
+  uint64_t key[kMaxLists];
 #pragma unroll
-    for (int i = 0; i < CAP; ++i) {
-      sv[i] = cand_s[base + i];
-      bv[i] = cand_b[base + i];
+  for (int i = 0; i < kMaxLists; ++i) {
+    const int sp = tid + i * blockDim.x;
+    pos[i] = 0;
+    key[i] = sp < splits ? head_key(sp, 0) : 0;
+  }
+  if (tid == 0) out[0] = (int32_t)((len - 1) / Bk);
+  for (int r = 0; r < k - 1; ++r) {
+    uint64_t best = 0;
+#pragma unroll
+    for (int i = 0; i < kMaxLists; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+      best = other > best ? other : best;
     }
+    if (lane == 0) warp_best[warp] = best;
+    __syncthreads();
+    uint64_t all = 0;
+    for (int w = 0; w < nwarps; ++w) all = warp_best[w] > all ? warp_best[w] : all;
+    __syncthreads();  // warp_best is rewritten next round
+    if (tid == 0) out[1 + r] = all == 0 ? -1 : (int32_t)(0xFFFFFFFFu - (uint32_t)(all & 0xFFFFFFFFu));
+    if (all == 0) continue;
 #pragma unroll
-    for (int i = 0; i < CAP; ++i)
-      if (bv[i] >= 0) m.insert(sv[i], bv[i]);
-  }
-  int32_t ids[CAP];
-  float scs[CAP];
-  const int n = m.emit(CAP, ids, scs);
-  for (int i = 0; i < CAP; ++i) {
-    ls[lane][i] = i < n ? scs[i] : 0.f;
-    lb[lane][i] = i < n ? ids[i] : -1;
-  }
-  __syncwarp();
-  if (lane == 0) {
-    TopK<CAP> f;
-    f.init(k - 1);
-    for (int l = 0; l < 32; ++l)
-      for (int i = 0; i < CAP; ++i)
-        if (lb[l][i] >= 0) f.insert(ls[l][i], lb[l][i]);
-    out[0] = (int32_t)((len - 1) / Bk);
-    if (k > 1) f.emit(k - 1, out + 1);
+    for (int i = 0; i < kMaxLists; ++i)
+      if (key[i] == all) {  // keys are unique: block ids differ across lists
+        const int sp = tid + i * blockDim.x;
+        key[i] = head_key(sp, ++pos[i]);
+      }
   }
 }
 
@@ -346,9 +364,9 @@ cudaError_t launch_scan_merge(const void* q_idx_t, const void* k_idx_cache, cons
   decode_scan_kernel<DI, BK, CAP><<<grid, kScanThreads, 0, s>>>((const uint16_t*)q_idx_t,
                                                                 (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max,
                                                                 p.H_kv, p.k, p.splits, sc.cand_s, sc.cand_b, st);
-  decode_merge_kernel<CAP><<<dim3((unsigned)p.B, (unsigned)p.H_kv), 32, 0, s>>>(sc.cand_s, sc.cand_b, ctx_len,
-                                                                             p.ctx_max, p.Bk, p.H_kv, p.k,
-                                                                             p.splits, blk);
+  const int mthreads = p.splits >= 1024 ? 1024 : (p.splits + 31) / 32 * 32;
+  decode_merge_kernel<CAP><<<dim3((unsigned)p.B, (unsigned)p.H_kv), mthreads, 0, s>>>(
+      sc.cand_s, sc.cand_b, ctx_len, p.ctx_max, p.Bk, p.H_kv, p.k, p.splits, blk);
   return cudaGetLastError();
 }
 

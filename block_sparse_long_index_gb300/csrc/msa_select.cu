@@ -15,8 +15,8 @@
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma into one of two
 //               accumulator buffers (GPC x 64 fp32 columns each) and commits
 //               completion to mbarriers;
-//   warps 2..9  epilogue: each thread owns one query row (a TMEM lane) for two
-//               of the groups, loads its 64 scores per group with tcgen05.ld,
+//   warps 2..17 epilogue: each thread owns one query row (a TMEM lane) of one
+//               group, loads its 64 scores with tcgen05.ld,
 //               reduces them with 3-input max into the running block maximum
 //               and, when a block is complete, offers (max, block) to its
 //               register top-(k-1) list.  Scores never leave the SM.
@@ -38,8 +38,8 @@ constexpr int kRows = 128;    // query rows per tile = MMA M
 constexpr int kKeys = 64;     // keys per tile = MMA N
 constexpr int kStages = 4;    // k^I ring depth
 constexpr int kMaxGpc = 4;    // groups per work item
-constexpr int kThreads = 320; // 10 warps
-constexpr int kEpiWarps = 8;
+constexpr int kThreads = 576; // 18 warps: producer, MMA, 16 epilogue
+constexpr int kEpiWarps = 16;
 
 template <int DI>
 struct SelectLayout {
@@ -210,79 +210,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-    const int half = (warp - 2) >> 2;         // which pair of groups
+    const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
+    const int gi = (warp - 2) >> 2;        // the group (of the item's quad) this warp reduces
+    const bool has = gi < gpc;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     uint32_t acc_glob = 0;
     int64_t r = 0, j;
     bool ok = true;
-    TopK<CAP> top0, top1;
+    TopK<CAP> top;
     while (ok && next_item(r, n_items, j)) {
       const int64_t qb = n_qt - 1 - j / n_gq;
       const int gq = (int)(j % n_gq);
       const int64_t nkt = n_kt_of(qb);
       const int64_t t = qb * kRows + row;
       const int64_t local = t / Bk;
-      const int gi0 = half * 2, gi1 = half * 2 + 1;
-      const bool has0 = gi0 < gpc, has1 = gi1 < gpc;
-      top0.init(k - 1);
-      top1.init(k - 1);
-      float run0 = __int_as_float(0xff800000), run1 = run0;
+      top.init(k - 1);
+      float run = __int_as_float(0xff800000);
       for (int64_t kt = 0; kt < nkt; ++kt, ++acc_glob) {
         const int buf = acc_glob & 1;
         if (!(ok = mbar_wait(acc_full(buf), (acc_glob >> 1) & 1, abort, st, 0x301))) break;
         tc_fence_after();
-        const uint32_t col = (uint32_t)(buf * acc_cols);
-        if (has0) {
+        if (has) {
+          const uint32_t col = (uint32_t)(buf * acc_cols + gi * kKeys);
           uint32_t x[32], y[32];
-          tmem_ld_x32(tmem + lane_base + col + gi0 * kKeys, x);
-          tmem_ld_x32(tmem + lane_base + col + gi0 * kKeys + 32, y);
+          tmem_ld_x32(tmem + lane_base + col, x);
+          tmem_ld_x32(tmem + lane_base + col + 32, y);
           tmem_ld_wait();
-          float m = run0;
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(buf));  // the scores are in registers: release TMEM early
+          float m = run;
 #pragma unroll
           for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
 #pragma unroll
           for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
-          run0 = m;
+          run = m;
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(buf));
         }
-        if (has1) {
-          uint32_t x[32], y[32];
-          tmem_ld_x32(tmem + lane_base + col + gi1 * kKeys, x);
-          tmem_ld_x32(tmem + lane_base + col + gi1 * kKeys + 32, y);
-          tmem_ld_wait();
-          float m = run1;
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
-          run1 = m;
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty(buf));
         if (Bk == kKeys || (kt & 1)) {  // block (kt for Bk=64, kt/2 for Bk=128) complete
           const int b = (int)(Bk == kKeys ? kt : kt >> 1);
-          if (b < local) {
-            if (has0) top0.insert(run0, b);
-            if (has1) top1.insert(run1, b);
-          }
-          run0 = __int_as_float(0xff800000);
-          run1 = run0;
+          if (has && b < local) top.insert(run, b);
+          run = __int_as_float(0xff800000);
         }
       }
       if (!ok) break;
-      if (t < N) {
-        if (has0) {
-          int32_t* out = block_idx + ((int64_t)(gq * gpc + gi0) * N + t) * k;
-          out[0] = (int32_t)local;
-          if (k > 1) top0.emit(k - 1, out + 1);
-        }
-        if (has1) {
-          int32_t* out = block_idx + ((int64_t)(gq * gpc + gi1) * N + t) * k;
-          out[0] = (int32_t)local;
-          if (k > 1) top1.emit(k - 1, out + 1);
-        }
+      if (has && t < N) {
+        int32_t* out = block_idx + ((int64_t)(gq * gpc + gi) * N + t) * k;
+        out[0] = (int32_t)local;
+        if (k > 1) top.emit(k - 1, out + 1);
       }
     }
   }
