@@ -7,19 +7,20 @@
 // (per-tile maxima inserted into a register top-k while sweeping key tiles;
 // local block pinned).
 //
-// Work item = (query tile of 128 rows, quad of up to 4 GQA groups).  The
-// index key is shared by all groups, so one 64-key tile of k^I staged in
-// shared memory feeds GPC (<= 4) MMAs of 128 x 64 x d_I, one per group:
+// Work item = (query tile of 128 rows, pair of GQA groups).  The index key
+// is shared by all groups, so one 128-key tile of k^I staged in shared memory
+// feeds GPC (<= 2) MMAs of 128 x 128 x d_I, one per group (128-wide B tiles
+// keep the operand traffic within what shared memory delivers per cycle):
 //   warp 0      TMA producer: the item's q^I tiles (A, resident for the
-//               item) and a 4-stage ring of k^I tiles (B), 128B-swizzled;
+//               item) and a 4-stage ring of k^I tiles (B), swizzled;
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma into one of two
-//               accumulator buffers (GPC x 64 fp32 columns each) and commits
+//               accumulator buffers (GPC x 128 fp32 columns each) and commits
 //               completion to mbarriers;
-//   warps 2..17 epilogue: each thread owns one query row (a TMEM lane) of one
-//               group, loads its 64 scores with tcgen05.ld,
-//               reduces them with 3-input max into the running block maximum
-//               and, when a block is complete, offers (max, block) to its
-//               register top-(k-1) list.  Scores never leave the SM.
+//   warps 2..9  epilogue: each thread owns one query row (a TMEM lane) of one
+//               group, loads its 128 scores with tcgen05.ld, reduces them with
+//               3-input max into block maxima (one per Bk-block of the tile)
+//               and offers (max, block) to its register top-(k-1) list.
+//               Scores never leave the SM.
 // Only blocks b < local(t) are candidates: every token of such a block is
 // visible (j <= t), so no causal mask is applied; the local block is written
 // directly as slot 0.  Items are visited longest-first in a snake order over
@@ -34,12 +35,12 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kRows = 128;    // query rows per tile = MMA M
-constexpr int kKeys = 64;     // keys per tile = MMA N
-constexpr int kStages = 4;    // k^I ring depth
-constexpr int kMaxGpc = 4;    // groups per work item
-constexpr int kThreads = 576; // 18 warps: producer, MMA, 16 epilogue
-constexpr int kEpiWarps = 16;
+constexpr int kRows = 128;     // query rows per tile = MMA M
+constexpr int kKeys = 128;     // keys per tile = MMA N
+constexpr int kStages = 4;     // k^I ring depth
+constexpr int kMaxGpc = 2;     // groups per work item
+constexpr int kEpiWarps = 4 * kMaxGpc;
+constexpr int kThreads = (2 + kEpiWarps) * 32;
 
 template <int DI>
 struct SelectLayout {
@@ -67,6 +68,11 @@ __device__ __forceinline__ bool next_item(int64_t& r, int64_t n_items, int64_t& 
   }
 }
 
+// Key tiles a query tile needs: all 128-key tiles holding blocks before the
+// last row's local block (for Bk = 64 the second half of the query tile also
+// takes block 2qb).
+__device__ __forceinline__ int64_t key_tiles(int64_t qb, int Bk) { return Bk == 128 ? qb : qb + 1; }
+
 template <int DI, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -90,8 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 6);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int acc_cols = kMaxGpc * kKeys;  // columns per accumulator buffer
-  const uint32_t tmem_cols = 2 * acc_cols;
+  constexpr int acc_cols = kMaxGpc * kKeys;  // columns per accumulator buffer
+  constexpr uint32_t tmem_cols = 2 * acc_cols;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -124,7 +130,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n_qt = (N + kRows - 1) / kRows;
   const int n_gq = G / gpc;
   const int64_t n_items = n_qt * n_gq;
-  auto n_kt_of = [&](int64_t qb) -> int64_t { return Bk == 128 ? 2 * qb : 2 * qb + 1; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && next_item(r, n_items, j)) {
         const int64_t qb = n_qt - 1 - j / n_gq;
         const int gq = (int)(j % n_gq);
-        const int64_t nkt = n_kt_of(qb);
+        const int64_t nkt = key_tiles(qb, Bk);
         if (nkt == 0) continue;
         if (!(ok = mbar_wait(a_empty, (a_glob & 1) ^ 1, abort, st, 0x101))) break;
         mbar_arrive_expect_tx(a_full, (uint32_t)(gpc * L::NCH * L::A_CHUNK));
@@ -174,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && next_item(r, n_items, j)) {
         const int64_t qb = n_qt - 1 - j / n_gq;
-        const int64_t nkt = n_kt_of(qb);
+        const int64_t nkt = key_tiles(qb, Bk);
         if (nkt == 0) continue;
         if (!(ok = mbar_wait(a_full, a_glob & 1, abort, st, 0x201))) break;
         tc_fence_after();
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
-    const int gi = (warp - 2) >> 2;        // the group (of the item's quad) this warp reduces
+    const int gi = (warp - 2) >> 2;        // the group (of the item's pair) this warp reduces
     const bool has = gi < gpc;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -222,38 +227,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && next_item(r, n_items, j)) {
       const int64_t qb = n_qt - 1 - j / n_gq;
       const int gq = (int)(j % n_gq);
-      const int64_t nkt = n_kt_of(qb);
+      const int64_t nkt = key_tiles(qb, Bk);
       const int64_t t = qb * kRows + row;
       const int64_t local = t / Bk;
       top.init(k - 1);
-      float run = __int_as_float(0xff800000);
       for (int64_t kt = 0; kt < nkt; ++kt, ++acc_glob) {
         const int buf = acc_glob & 1;
         if (!(ok = mbar_wait(acc_full(buf), (acc_glob >> 1) & 1, abort, st, 0x301))) break;
         tc_fence_after();
+        float m0 = __int_as_float(0xff800000), m1 = m0;  // maxima of columns 0..63 and 64..127
         if (has) {
-          const uint32_t col = (uint32_t)(buf * acc_cols + gi * kKeys);
-          uint32_t x[32], y[32];
-          tmem_ld_x32(tmem + lane_base + col, x);
-          tmem_ld_x32(tmem + lane_base + col + 32, y);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty(buf));  // the scores are in registers: release TMEM early
-          float m = run;
+          const uint32_t col = tmem + lane_base + (uint32_t)(buf * acc_cols + gi * kKeys);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+          for (int h = 0; h < 2; ++h) {
+            uint32_t x[32], y[32];
+            tmem_ld_x32(col + 64 * h, x);
+            tmem_ld_x32(col + 64 * h + 32, y);
+            tmem_ld_wait();
+            float m = __int_as_float(0xff800000);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
-          run = m;
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty(buf));
+            for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+            if (h == 0) m0 = m; else m1 = m;
+          }
         }
-        if (Bk == kKeys || (kt & 1)) {  // block (kt for Bk=64, kt/2 for Bk=128) complete
-          const int b = (int)(Bk == kKeys ? kt : kt >> 1);
-          if (has && b < local) top.insert(run, b);
-          run = __int_as_float(0xff800000);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(buf));  // the maxima are in registers: release TMEM
+        if (has) {
+          if (Bk == kKeys) {
+            const int b = (int)kt;
+            if (b < local) top.insert(fmaxf(m0, m1), b);
+          } else {  // two 64-token blocks per key tile
+            const int b = (int)(2 * kt);
+            if (b < local) top.insert(m0, b);
+            if (b + 1 < local) top.insert(m1, b + 1);
+          }
         }
       }
       if (!ok) break;
@@ -306,7 +316,7 @@ cudaError_t launch_cap(const void* q_idx, const void* k_idx, int64_t N, int G, i
 
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
                           int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
-  const int gpc = (G % 4 == 0) ? 4 : (G % 2 == 0) ? 2 : 1;
+  const int gpc = (G % 2 == 0) ? 2 : 1;
   if (d_I == 32) return launch_cap<32>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
   if (d_I == 64) return launch_cap<64>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
   return launch_cap<128>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
