@@ -11,16 +11,16 @@
 //      entries t*k + slot.
 //   2. Per query slab [T0, T1): for every (group, block) the sub-list of
 //      entries with t in the slab (two binary searches, the list is sorted),
-//      cut into tiles of P = 128 / gs positions; an exclusive scan turns the
-//      tile counts into a flat work list (hot blocks simply yield more tiles).
+//      cut into tiles of 16 positions; an exclusive scan turns the tile
+//      counts into a flat work list (hot blocks simply yield more tiles).
 //   3. Tile kernel (msa_attn_tile.cu, persistent, tcgen05): K_b and V_b are
 //      staged in shared memory once per run of tiles of the same block and
-//      shared by each tile's P positions x gs heads = 128 query rows;
-//      S = Q K_b^T and O = P V_b on tensor cores; the causal mask applies only
-//      where b == local(t).  Each row writes its normalised partial O (bf16)
-//      and partial lse (fp32) for its (t, slot).
-//   4. Combine: per (t, h) the partials of the row's slots are merged by their
-//      lse into out and lse.
+//      shared by each tile's 16 positions x 8 head slots = 128 query rows
+//      (gs of every 8 used); S = Q K_b^T and O = P V_b on tensor cores; the
+//      causal mask applies only where b == local(t).  Each row writes its
+//      un-normalised partial O (bf16) and its (m, l) (fp32) for its (t, slot).
+//   4. Combine: per (t, h) the partials of the row's slots are merged:
+//      M = max m_s, L = sum l_s 2^(m_s - M), out = sum O_s 2^(m_s - M) / L.
 #include <math.h>
 
 #include "msa_common.cuh"
@@ -29,7 +29,7 @@ namespace msa {
 
 namespace {
 
-constexpr int kTileRows = 128;  // query rows per attention tile (positions x heads of a group)
+constexpr int kTilePos = 16;  // query positions per attention tile (x 8 head slots = 128 MMA rows)
 
 // ---------------------------------------------------------------- schedule
 // For each (g, b): [lo, hi) of the group's entry list with t in [T0, T1).
@@ -103,17 +103,20 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(const int32_t* __restr
 // One CTA per query position t: the position's partials (k slots x H_q heads x
 // d, contiguous) are read once, coalesced.  Slot s of group g contributes iff
 // its id is in [0, nb) and not repeated by an earlier slot (the set counts
-// each block once).  out = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max),
-// lse = max + log(sum_s w_s); no contribution gives out = 0, lse = -inf.
+// each block once).  Partial s of head h holds O_s = sum_j p_j v_j with
+// p_j = 2^(s_j - m_s) (s_j in log2 units) and l_s = sum_j p_j; then
+// M = max m_s, w_s = 2^(m_s - M) / sum_s l_s 2^(m_s - M), out = sum_s w_s O_s,
+// lse = ln 2 (M + log2 sum_s l_s 2^(m_s - M)); no contribution gives out = 0,
+// lse = -inf.
 template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ block_idx,
                                                       const uint16_t* __restrict__ part_o,
-                                                      const float* __restrict__ part_lse, int64_t N, int H_q, int G,
+                                                      const float2* __restrict__ part_ml, int64_t N, int H_q, int G,
                                                       int gs, int k, int64_t nb, int64_t T0,
                                                       uint16_t* __restrict__ out, float* __restrict__ lse) {
-  extern __shared__ float cw[];          // [k][H_q] weights, then [H_q] 1/L
+  extern __shared__ float cw[];          // [k][H_q] m, then weights; then [k][H_q] l
   __shared__ uint32_t use_mask[64];      // per group: bit s set if slot s contributes
-  float* inv_l = cw + k * H_q;
+  float* cl = cw + k * H_q;
   const int tid = threadIdx.x;
   const int64_t tr = blockIdx.x;
   const int64_t t = T0 + tr;
@@ -129,27 +132,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     use_mask[g] = use;
   }
   __syncthreads();
-  const float* pl = part_lse + tr * k * H_q;
+  const float2* pm = part_ml + tr * k * H_q;
   for (int i = tid; i < k * H_q; i += blockDim.x) {
     const int s = i / H_q, h = i % H_q;
-    cw[i] = (use_mask[h / gs] >> s & 1u) ? pl[i] : __int_as_float(0xff800000);
+    const float2 ml = pm[i];
+    const bool use = (use_mask[h / gs] >> s) & 1u;
+    cw[i] = use ? ml.x : __int_as_float(0xff800000);
+    cl[i] = use ? ml.y : 0.f;
   }
   __syncthreads();
   for (int h = tid; h < H_q; h += blockDim.x) {
-    float m = __int_as_float(0xff800000);
-    for (int s = 0; s < k; ++s) m = fmaxf(m, cw[s * H_q + h]);
+    float M = __int_as_float(0xff800000);
+    for (int s = 0; s < k; ++s) M = fmaxf(M, cw[s * H_q + h]);
     float L = 0.f;
-    if (m != __int_as_float(0xff800000)) {
+    if (M != __int_as_float(0xff800000)) {
       for (int s = 0; s < k; ++s) {
-        float w = __expf(cw[s * H_q + h] - m);  // exp(-inf) = 0 for unused slots
-        cw[s * H_q + h] = w;
-        L += w;
+        const float e = exp2f(cw[s * H_q + h] - M);  // 2^-inf = 0 for unused slots
+        cw[s * H_q + h] = e;
+        L += e * cl[s * H_q + h];
       }
     } else {
       for (int s = 0; s < k; ++s) cw[s * H_q + h] = 0.f;
     }
-    inv_l[h] = L > 0.f ? 1.f / L : 0.f;
-    lse[(int64_t)h * N + t] = L > 0.f ? m + logf(L) : __int_as_float(0xff800000);
+    const float il = L > 0.f ? 1.f / L : 0.f;
+    for (int s = 0; s < k; ++s) cw[s * H_q + h] *= il;
+    lse[(int64_t)h * N + t] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : __int_as_float(0xff800000);
   }
   __syncthreads();
   constexpr int C8 = D / 8;
@@ -173,12 +180,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
       acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
       acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
     }
-    const float il = inv_l[h];
     uint4 o;
-    o.x = pack_bf16x2(acc[0] * il, acc[1] * il);
-    o.y = pack_bf16x2(acc[2] * il, acc[3] * il);
-    o.z = pack_bf16x2(acc[4] * il, acc[5] * il);
-    o.w = pack_bf16x2(acc[6] * il, acc[7] * il);
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
     *reinterpret_cast<uint4*>(out + (t * H_q + h) * D + c8 * 8) = o;
   }
 }
@@ -189,7 +195,7 @@ struct AttnScratch {
   InvertScratch inv;
   int32_t *lo, *cnt, *tiles, *tile_off;
   uint16_t* part_o;
-  float* part_lse;
+  float2* part_ml;
 };
 
 static size_t carve(const AttnPlan& p, void* base, AttnScratch* out) {
@@ -213,7 +219,7 @@ static size_t carve(const AttnPlan& p, void* base, AttnScratch* out) {
   s.tiles = (int32_t*)take((size_t)G * p.nb * 4);
   s.tile_off = (int32_t*)take(((size_t)G * p.nb + 1) * 4);
   s.part_o = (uint16_t*)take((size_t)p.slab * p.k * p.H_q * p.d * 2);
-  s.part_lse = (float*)take((size_t)p.slab * p.k * p.H_q * 4);
+  s.part_ml = (float2*)take((size_t)p.slab * p.k * p.H_q * 8);
   if (out) *out = s;
   return off;
 }
@@ -230,9 +236,9 @@ AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k) {
   p.k = k;
   p.gs = H_q / H_kv;
   p.nb = (N + Bk - 1) / Bk;
-  p.P = kTileRows / p.gs;
-  // partial results of one slab: slab * k * H_q * (2d + 4) bytes, at most ~36 GB
-  const double per_pos = (double)k * H_q * (2.0 * d + 4.0);
+  p.P = kTilePos;
+  // partial results of one slab: slab * k * H_q * (2d + 8) bytes, at most ~36 GB
+  const double per_pos = (double)k * H_q * (2.0 * d + 8.0);
   int64_t cap = (int64_t)(36.0e9 / per_pos);
   if (cap > 131072) cap = 131072;
   if (cap < 1024) cap = 1024;
@@ -256,15 +262,15 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
                                                                       T1, p.P, sc.lo, sc.cnt, sc.tiles);
     sched_scan_kernel<<<1, 1024, 0, s>>>(sc.tiles, n_gb, sc.tile_off);
     e = launch_attn_tiles(q, k, v, sc.entries, sc.lo, sc.cnt, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb,
-                          p.gs, p.P, T0, scale, sc.part_o, sc.part_lse, st, s);
+                          p.gs, T0, p.slab * p.k, scale, sc.part_o, sc.part_ml, st, s);
     if (e != cudaSuccess) return e;
-    const size_t cs = ((size_t)p.k * p.H_q + p.H_q) * sizeof(float);
+    const size_t cs = (size_t)2 * p.k * p.H_q * sizeof(float);
     auto ck = p.d == 64 ? combine_kernel<64> : combine_kernel<128>;
     if (cs > 48 * 1024) {
       e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cs);
       if (e != cudaSuccess) return e;
     }
-    ck<<<(unsigned)(T1 - T0), 256, cs, s>>>(block_idx, sc.part_o, sc.part_lse, p.N, p.H_q, G, p.gs, p.k, p.nb, T0,
+    ck<<<(unsigned)(T1 - T0), 256, cs, s>>>(block_idx, sc.part_o, sc.part_ml, p.N, p.H_q, G, p.gs, p.k, p.nb, T0,
                                             (uint16_t*)out, lse);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

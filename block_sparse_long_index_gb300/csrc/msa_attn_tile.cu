@@ -1,30 +1,39 @@
 // KV-outer attention tiles on the 5th-generation tensor cores.
 //
 // "MSA" study note 3-3 "Main Branch" (exact softmax over the selected
-// support, per-head weights, group-shared blocks) and 3-5 (KV-outer:
-// the queries that chose a KV block are concatenated into one large MMA that
+// support, per-head weights, group-shared blocks) and 3-5 (KV-outer: the
+// queries that chose a KV block are concatenated into one large MMA that
 // reuses the block from on-chip memory; hot blocks pre-chunked into tiles).
 //
-// A tile is (group g, block b, up to P = 128/gs query positions that chose b)
-// and its 128 rows are (position, head of g).  Per tile:
-//   S = Q K_b^T (128 x Bk fp32 in TMEM), causal mask j <= t, row softmax,
-//   P (bf16, written back into S's TMEM columns), O = P V_b (128 x d fp32 in
-//   TMEM, P read from TMEM as the A operand), then the normalised partial O
-//   (bf16) and partial lse of every (t, slot, h) row.
-// Roles (448 threads):
-//   warps 0..3   Q loaders: loader w gathers the Q rows of tiles i = w mod 4
-//                into Q buffer w with cp.async (128B-swizzled K-major layout),
-//                so four tiles' gathers are in flight;
-//   warp 4       TMEM owner; lane 0 issues tcgen05.mma: S(i+1) then PV(i)
-//                (PV(i) first when tile i+1 needs another K/V block);
-//   warps 5..12  two softmax warpgroups, one per tile parity, each with its own
-//                S/P and O columns in TMEM: softmax(i) then epilogue(i);
-//   warp 13      K/V loader: one TMA load of K_b and V_b per run of tiles of
-//                the same block, released by the MMA issuer after the run's
-//                last P V.
-// K_b and Q feed the tensor cores as K-major shared-memory operands, V_b as an
-// MN-major one (d contiguous), P from TMEM.  Every wait is bounded; on expiry
-// the kernel flags a timeout, drains its own async work and exits.
+// A tile is (group g, block b, up to 16 query positions that chose b).  Its
+// 128 MMA rows are (position pp, head slot hh) -> row 8 pp + hh; head slots
+// hh >= gs are padding (never loaded, never stored).  Per tile:
+//   S = Q K_b^T (128 x Bk fp32 in TMEM), causal mask j <= t, row max m and
+//   P = 2^(s log2e / sqrt(d) - m) (bf16, written back over S's TMEM columns),
+//   O = P V_b (128 x d fp32 in TMEM, P read from TMEM as the A operand); the
+//   row's un-normalised O goes out in bf16 and its (m, l = sum P) in fp32, so
+//   the combine divides once per (t, h) by the merged sum.
+// Roles (512 threads):
+//   warp 0        Q loader: publishes each tile's metadata (query positions,
+//                 slots) to a shared ring and gathers its Q rows with one TMA
+//                 box {64 dims, gs heads} per position into one of four
+//                 128B-swizzled K-major Q buffers;
+//   warp 1        TMEM owner; lane 0 issues tcgen05.mma.  S/P has three TMEM
+//                 buffers and O one, so S runs up to two tiles ahead of P V:
+//                 per tile i it issues every S(j), j <= i+2, of i's K/V block,
+//                 then PV(i);
+//   warp 2        K/V loader: one TMA load of K_b and V_b per run of tiles of
+//                 the same block, released after the run's last P V;
+//   warps 4..11   two softmax warpgroups (tiles of each parity);
+//   warps 12..15  epilogue warpgroup: O -> bf16 in a swizzled shared tile,
+//                 written out by TMA stores of one box per position.
+// Buffer reuse needs no extra waits: S(j) is issued after PV(j-3) (tensor
+// core operations run in issue order), and each barrier phase a role waits
+// for cannot be overtaken by the next one (the next use of a buffer depends,
+// through the issue order, on the consumer having passed it).  K_b, Q feed
+// the tensor cores as K-major shared-memory operands, V_b as an MN-major one
+// (d contiguous), P from TMEM.  Every wait is bounded; on expiry the kernel
+// flags a timeout, drains its own async work and exits.
 #include <math.h>
 
 #include "msa_sm100.cuh"
@@ -35,27 +44,44 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kRowsT = 128;
-constexpr int kQLoaders = 4;
-constexpr int kWarpMma = 4;
-constexpr int kWarpSoft0 = 5;
-constexpr int kWarpKv = 13;
-constexpr int kThreadsT = 14 * 32;
+constexpr int kRowsT = 128;   // MMA rows per tile
+constexpr int kPosT = 16;     // query positions per tile
+constexpr int kQBufs = 4;     // Q buffers in shared memory
+constexpr int kSBufs = 3;     // S/P buffers in TMEM
+constexpr int kMeta = 8;      // tile metadata slots
+constexpr int kWarpLoad = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpKv = 2;
+constexpr int kWarpSoft0 = 4;
+constexpr int kWarpEpi0 = 12;
+constexpr int kThreadsT = 16 * 32;
 constexpr int kSoftWarps = 4;  // per warpgroup
+constexpr int kEpiWarps = 4;
+constexpr int kMetaReaders = 1 + kSoftWarps + 1;  // MMA issuer, one softmax warpgroup, epilogue store issuer
+
+// What the Q loader publishes per tile, so that no other role walks the
+// schedule in global memory.
+struct TileMeta {
+  int32_t gb, g, b, count;
+  int32_t t[kPosT];     // query position (valid for pp < count)
+  int32_t slot[kPosT];  // its slot in the position's block set
+};
 
 template <int D, int BK>
 struct AttnLayout {
-  static constexpr int NCD = D / 64;  // 64-column chunks of d
-  static constexpr int Q_CHUNK = kRowsT * 128;
-  static constexpr int Q_BYTES = NCD * Q_CHUNK;
+  static constexpr int NCD = D / 64;                // 64-column chunks of d
+  static constexpr int ROWS_CHUNK = kRowsT * 128;   // one chunk of 128 rows x 128 bytes
+  static constexpr int Q_BYTES = NCD * ROWS_CHUNK;
   static constexpr int KV_CHUNK = BK * 128;
   static constexpr int K_BYTES = NCD * KV_CHUNK;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + kQLoaders * Q_BYTES;
+  static constexpr int OFF_K = OFF_Q + kQBufs * Q_BYTES;
   static constexpr int OFF_V = OFF_K + K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + K_BYTES;
-  static constexpr int SMEM = 1024 + OFF_BAR + 256;
-  // TMEM: per parity p, S (and P over it) at p*256, O at p*256 + 128
+  static constexpr int OFF_STG = OFF_V + K_BYTES;   // bf16 O of one tile, same layout as Q
+  static constexpr int OFF_BAR = OFF_STG + Q_BYTES;
+  static constexpr int SMEM = 1024 + OFF_BAR + 512;
+  // TMEM: S/P buffer j at 128 j (j < 3), O at 384
+  static constexpr uint32_t TMEM_O = 384;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -74,7 +100,6 @@ struct TileIter {
   const int32_t* __restrict__ lo;
   const int32_t* __restrict__ cnt;
   int64_t n_gb, nb;
-  int P;
   int64_t gb;
 
   __device__ __forceinline__ void seek(int32_t tile) {
@@ -93,8 +118,8 @@ struct TileIter {
     r.g = (int)(gb / nb);
     r.b = gb % nb;
     const int32_t base = lo[gb];
-    r.first = base + (tile - tile_off[gb]) * P;
-    r.count = min(P, base + cnt[gb] - r.first);
+    r.first = base + (tile - tile_off[gb]) * kPosT;
+    r.count = min(kPosT, base + cnt[gb] - r.first);
     return r;
   }
 };
@@ -107,11 +132,30 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ void epi_bar_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiWarps * 32) : "memory"); }
+// Named barrier of the epilogue warpgroup that also ANDs a flag over its threads.
+__device__ __forceinline__ bool epi_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kEpiWarps * 32)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Descriptor of an MN-major operand: 64-element (128 B) rows along N, 8-row
 // groups along K at 1024 B, successive 64-element N chunks `lbo` bytes apart.
@@ -145,54 +189,87 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
+// Packed pairs of fp32 (one 64-bit register): two lanes per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int D, int BK>
 __global__ void __launch_bounds__(kThreadsT, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                   const uint16_t* __restrict__ q, const int32_t* __restrict__ entries,
-                   const int32_t* __restrict__ lo_arr, const int32_t* __restrict__ cnt_arr,
-                   const int32_t* __restrict__ tile_off, int64_t N, int H_q, int H_kv, int k, int64_t nb, int gs, int P,
-                   int64_t T0, float scale_log2, uint16_t* __restrict__ part_o, float* __restrict__ part_lse,
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_po,
+                   const int32_t* __restrict__ entries, const int32_t* __restrict__ lo_arr,
+                   const int32_t* __restrict__ cnt_arr, const int32_t* __restrict__ tile_off, int64_t N, int H_q,
+                   int H_kv, int k, int64_t nb, int gs, int64_t T0, float scale_log2, float2* __restrict__ part_ml,
                    DeviceStatus* st) {
   using L = AttnLayout<D, BK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int32_t ld_t[kQLoaders][kRowsT];  // per Q loader: query position of each tile position
+  __shared__ TileMeta meta[kMeta];
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto q_full = [&](int i) { return bar0 + 8u * (0 + i); };
   auto q_empty = [&](int i) { return bar0 + 8u * (4 + i); };
   auto s_full = [&](int i) { return bar0 + 8u * (8 + i); };
-  auto p_full = [&](int i) { return bar0 + 8u * (10 + i); };
-  auto o_full = [&](int i) { return bar0 + 8u * (12 + i); };
-  auto o_empty = [&](int i) { return bar0 + 8u * (14 + i); };
+  auto p_full = [&](int i) { return bar0 + 8u * (11 + i); };
+  const uint32_t o_full = bar0 + 8u * 14;
+  const uint32_t o_empty = bar0 + 8u * 15;
   const uint32_t kv_full = bar0 + 8u * 16;
   const uint32_t kv_empty = bar0 + 8u * 17;
   const uint32_t drain_bar = bar0 + 8u * 18;
+  auto meta_full = [&](int i) { return bar0 + 8u * (19 + i); };
+  auto meta_empty = [&](int i) { return bar0 + 8u * (19 + kMeta + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Head slots >= gs of the Q buffers are never loaded: zero them (and the
+  // rest) once so that the padding rows of S stay finite.
+  for (int i = tid; i < kQBufs * L::Q_BYTES / 16; i += kThreadsT)
+    reinterpret_cast<uint4*>(smem + L::OFF_Q)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (tid == 0) {
-    for (int i = 0; i < kQLoaders; ++i) {
-      mbar_init(q_full(i), 32);
+    for (int i = 0; i < kQBufs; ++i) {
+      mbar_init(q_full(i), 1);
       mbar_init(q_empty(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(s_full(i), 1);
       mbar_init(p_full(i), kSoftWarps);
-      mbar_init(o_full(i), 1);
-      mbar_init(o_empty(i), kSoftWarps);
     }
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, kEpiWarps);
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     mbar_init(drain_bar, 1);
+    for (int i = 0; i < kMeta; ++i) {
+      mbar_init(meta_full(i), 1);
+      mbar_init(meta_empty(i), kMetaReaders);
+    }
     fence_mbar_init();
     abort_flag = 0;
   }
-  if (warp == kWarpKv && lane == 0) {
+  if (warp == kWarpLoad && lane == 0) {
+    prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
+    prefetch_tmap(&tmap_po);
   }
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&tmem_slot), L::TMEM_COLS);
@@ -208,44 +285,54 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int32_t t_begin = (int32_t)((int64_t)total * blockIdx.x / gridDim.x);
   const int32_t t_end = (int32_t)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
   const int n = t_end - t_begin;
-  TileIter it{tile_off, lo_arr, cnt_arr, n_gb, nb, P, 0};
+  TileIter it{tile_off, lo_arr, cnt_arr, n_gb, nb, 0};
   if (n > 0) it.seek(t_begin);
 
-  if (warp < kQLoaders) {
-    // ------------------------------------------------------------ Q loader `warp`
-    const int w = warp;
-    int32_t* my_t = ld_t[w];
+  if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ Q loader + tile metadata
     bool ok = true;
-    constexpr int CPR = D / 8;  // 16-byte chunks per Q row
-    constexpr int ROWS_PER_PASS = 32 / CPR;
-    const int sub_row = lane / CPR, cc = lane % CPR;
-    const int ch = cc >> 3, jj = cc & 7;
-    const uint32_t qdst = sbase + L::OFF_Q + w * L::Q_BYTES;
-    for (int i = w; i < n && ok; i += kQLoaders) {
+    int issued = 0;
+    for (int i = 0; i < n && ok; ++i) {
+      const int ms_ = i % kMeta;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(meta_empty(ms_), ((i / kMeta) & 1) ^ 1, abort, st, 0x400) ? 1 : 0;
+      if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       const Tile tl = it.at(t_begin + i);
       const int32_t* E = entries + (int64_t)tl.g * N * k;
-      for (int pp = lane; pp < P; pp += 32) my_t[pp] = pp < tl.count ? E[tl.first + pp] / k : -1;
-      __syncwarp();
-      int okq = 1;
-      if (lane == 0) okq = mbar_wait(q_empty(w), ((i / kQLoaders) & 1) ^ 1, abort, st, 0x401) ? 1 : 0;
-      if (!(ok = __shfl_sync(0xffffffffu, okq, 0) != 0)) break;
-#pragma unroll 4
-      for (int r0 = 0; r0 < kRowsT; r0 += ROWS_PER_PASS) {
-        const int r = r0 + sub_row;
-        const int pp = r / gs, hh = r % gs;
-        const int32_t t = my_t[pp];
-        const bool valid = t >= 0;
-        const uint16_t* src = q + (((int64_t)(valid ? t : 0) * H_q + (int64_t)tl.g * gs + hh) * D + cc * 8);
-        const uint32_t dst = qdst + ch * L::Q_CHUNK + r * 128 + ((jj ^ (r & 7)) << 4);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                     : "memory");
+      TileMeta& mt = meta[ms_];
+      int32_t t = -1;
+      if (lane < kPosT && lane < tl.count) {
+        const int32_t e = E[tl.first + lane];
+        t = e / k;
+        mt.t[lane] = t;
+        mt.slot[lane] = e - t * k;
       }
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();  // my_t is rewritten for the next tile only after every lane used it
-      mbar_arrive(q_full(w));
+      if (lane == 0) {
+        mt.gb = (int32_t)tl.gb;
+        mt.g = tl.g;
+        mt.b = (int32_t)tl.b;
+        mt.count = tl.count;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(meta_full(ms_));
+      const int qb = i % kQBufs;
+      if (lane == 0) {
+        w = mbar_wait(q_empty(qb), ((i / kQBufs) & 1) ^ 1, abort, st, 0x401) ? 1 : 0;
+        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(tl.count * L::NCD * gs * 128));
+      }
+      if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
+      if (t >= 0) {
+        const uint32_t dst = sbase + L::OFF_Q + qb * L::Q_BYTES + lane * 1024;
+#pragma unroll
+        for (int c = 0; c < L::NCD; ++c)
+          tma_load_3d(dst + c * L::ROWS_CHUNK, &tmap_q, c * 64, tl.g * gs, t, q_full(qb));
+      }
+      issued = i + 1;
     }
-    cp_async_wait_all();
+    // after an abort: wait for the Q loads still in flight before the CTA exits
+    if (!ok && lane == 0)
+      for (int i = max(0, issued - kQBufs); i < issued; ++i)
+        mbar_wait(q_full(i % kQBufs), (i / kQBufs) & 1, nullptr, st, 0x4F2);
   } else if (warp == kWarpKv) {
     // ------------------------------------------------------------ K/V loader
     if (lane == 0 && n > 0) {
@@ -276,174 +363,249 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint32_t kv_cnt = 0;
       bool ok = true;
       int64_t gb_staged = -1;
+      // (g, b) of tile j, read once per tile from the metadata ring in tile order
+      int32_t gbq[8];
+      int fetched = 0;
+      auto gb_of = [&](int j, int32_t& out) -> bool {
+        while (fetched <= j) {
+          const int ms_ = fetched % kMeta;
+          if (!mbar_wait(meta_full(ms_), (fetched / kMeta) & 1, abort, st, 0x500)) return false;
+          gbq[fetched & 7] = meta[ms_].gb;
+          mbar_arrive(meta_empty(ms_));
+          ++fetched;
+        }
+        out = gbq[j & 7];
+        return true;
+      };
+      int s_next = 0;  // next tile whose S is not issued
+      int32_t gb_s_next = 0, gb_cur = 0;
+      ok = gb_of(0, gb_s_next);
       auto issue_S = [&](int j, int64_t gb_j) -> bool {
-        const int qb = j % kQLoaders;
-        if (!mbar_wait(q_full(qb), (j / kQLoaders) & 1, abort, st, 0x501)) return false;
+        const int qb = j % kQBufs;
+        if (!mbar_wait(q_full(qb), (j / kQBufs) & 1, abort, st, 0x501)) return false;
         if (gb_j != gb_staged) {
           if (!mbar_wait(kv_full, kv_cnt & 1, abort, st, 0x502)) return false;
           ++kv_cnt;
           gb_staged = gb_j;
         }
         tc_fence_after();
-        // S(j) reuses the columns of S/P(j-2), whose P V was issued earlier (MMAs run in issue order)
-        const uint32_t d = tmem + (uint32_t)((j & 1) * 256);
+        // buffer j % 3 last held P(j-3), whose P V was issued before this S
+        const uint32_t d = tmem + (uint32_t)((j % kSBufs) * 128);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int c = ks >> 2, kk = ks & 3;
-          const uint64_t ad = umma_desc_kmajor(sbase + L::OFF_Q + qb * L::Q_BYTES + c * L::Q_CHUNK + kk * 32, 128);
+          const uint64_t ad =
+              umma_desc_kmajor(sbase + L::OFF_Q + qb * L::Q_BYTES + c * L::ROWS_CHUNK + kk * 32, 128);
           const uint64_t bd = umma_desc_kmajor(sbase + L::OFF_K + c * L::KV_CHUNK + kk * 32, 128);
           mma_bf16_ss(d, ad, bd, IDESC_S, ks > 0);
         }
-        umma_commit(s_full(j & 1));
+        umma_commit(s_full(j % kSBufs));
         umma_commit(q_empty(qb));
         return true;
       };
-      auto issue_PV = [&](int i, bool last_of_block) -> bool {
-        const int pb = i & 1;
-        if (!mbar_wait(p_full(pb), (i >> 1) & 1, abort, st, 0x503)) return false;
-        if (!mbar_wait(o_empty(pb), ((i >> 1) & 1) ^ 1, abort, st, 0x504)) return false;
+      for (int i = 0; i < n && ok; ++i) {
+        if (!(ok = gb_of(i, gb_cur))) break;
+        // S ahead: every tile j <= i+2 of tile i's K/V block
+        while (ok && s_next < n && s_next <= i + 2 && gb_s_next == gb_cur) {
+          ok = issue_S(s_next, gb_s_next);
+          ++s_next;
+          if (ok && s_next < n) ok = gb_of(s_next, gb_s_next);
+        }
+        if (!ok) break;
+        // PV(i)
+        const int sb = i % kSBufs;
+        if (!(ok = mbar_wait(p_full(sb), (i / kSBufs) & 1, abort, st, 0x503))) break;
+        if (!(ok = mbar_wait(o_empty, (i & 1) ^ 1, abort, st, 0x504))) break;
         tc_fence_after();
-        const uint32_t pcol = tmem + (uint32_t)(pb * 256);
-        const uint32_t d = pcol + 128;
+        const uint32_t pcol = tmem + (uint32_t)(sb * 128);
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks) {
           const uint64_t bd = umma_desc_mnmajor_sw128(sbase + L::OFF_V + ks * 16 * 128, L::KV_CHUNK);
-          mma_bf16_ts(d, pcol + 8 * ks, bd, IDESC_PV, ks > 0);
+          mma_bf16_ts(tmem + L::TMEM_O, pcol + 8 * ks, bd, IDESC_PV, ks > 0);
         }
-        umma_commit(o_full(pb));
+        umma_commit(o_full);
+        const bool last_of_block = (i + 1 == n) || (s_next > i + 1 ? false : gb_s_next != gb_cur);
         if (last_of_block) umma_commit(kv_empty);
-        return true;
-      };
-      int64_t gb_cur = it.at(t_begin).gb;
-      ok = issue_S(0, gb_cur);
-      for (int i = 0; i < n && ok; ++i) {
-        const bool has_next = i + 1 < n;
-        const int64_t gb_next = has_next ? it.at(t_begin + i + 1).gb : -1;
-        const bool same = has_next && gb_next == gb_cur;
-        if (same && !(ok = issue_S(i + 1, gb_next))) break;
-        if (!(ok = issue_PV(i, !same))) break;
-        if (has_next && !same && !(ok = issue_S(i + 1, gb_next))) break;
-        gb_cur = gb_next;
       }
       if (!ok) {
         umma_commit(drain_bar);
         mbar_wait(drain_bar, 0, nullptr, st, 0x5F1);
       }
     }
-  } else {
+  } else if (warp >= kWarpSoft0 && warp < kWarpEpi0) {
     // ------------------------------------------------------------ softmax warpgroup `par`
     const int par = (warp - kWarpSoft0) / kSoftWarps;  // tiles of this parity
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint32_t scol = tmem + lane_base + (uint32_t)(par * 256);
-    const uint32_t ocol = scol + 128;
-    const int pos = row / gs, hh = row % gs;
+    const int pos = row >> 3, hh = row & 7;
+    const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     bool ok = true;
     for (int j = par; j < n && ok; j += 2) {
-      const Tile tl = it.at(t_begin + j);
-      int64_t t = -1;
-      int slot = 0;
-      if (pos < tl.count) {
-        const int32_t e = entries[(int64_t)tl.g * N * k + tl.first + pos];
-        t = e / k;
-        slot = e % k;
-      }
-      const uint32_t ph = (j >> 1) & 1;
-      if (!(ok = mbar_wait(s_full(par), ph, abort, st, 0x601))) break;
+      const int ms_ = j % kMeta;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(meta_full(ms_), (j / kMeta) & 1, abort, st, 0x600)))) break;
+      const int64_t t = (hh < gs && pos < meta[ms_].count) ? meta[ms_].t[pos] : -1;
+      const int slot = meta[ms_].slot[pos];
+      const int tg = meta[ms_].g;
+      const int64_t tb = meta[ms_].b;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(meta_empty(ms_));
+      const int sb = j % kSBufs;
+      const uint32_t scol = tmem + lane_base + (uint32_t)(sb * 128);
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full(sb), (j / kSBufs) & 1, abort, st, 0x601)))) break;
       tc_fence_after();
-      // ---- softmax: max pass, then exp pass writing bf16 P over the S columns already read.
-      // Columns move in pairs of 32 per TMEM wait; rows that see the whole block skip the mask.
-      const int64_t key0 = tl.b * BK;
-      const int lim = (int)max((int64_t)-1, min((int64_t)BK - 1, t - key0));  // last visible column
-      const bool full = lim == BK - 1;
+      // Last visible column of the row; rows without output count as unmasked
+      // so that a warp takes the masked path only where a real row needs it
+      // (TMEM loads are warp-collective).
+      const int64_t key0 = tb * BK;
+      const int lim = t < 0 ? BK - 1 : (int)max((int64_t)-1, min((int64_t)BK - 1, t - key0));
+      const bool full = __all_sync(0xffffffffu, lim == BK - 1);
       float m = __int_as_float(0xff800000);
+      uint64_t lsum2 = 0;  // two fp32 zeros
+      if (full) {
 #pragma unroll
-      for (int c = 0; c < BK / 32; c += 2) {
-        uint32_t x[32], y[32];
-        tmem_ld_x32(scol + c * 32, x);
-        tmem_ld_x32(scol + c * 32 + 32, y);
-        tmem_ld_wait();
-        if (full) {
+        for (int c = 0; c < BK / 32; c += 2) {
+          uint32_t x[32], y[32];
+          tmem_ld_x32(scol + c * 32, x);
+          tmem_ld_x32(scol + c * 32 + 32, y);
+          tmem_ld_wait();
 #pragma unroll
           for (int e2 = 0; e2 < 32; e2 += 2) {
             m = max3(m, __uint_as_float(x[e2]), __uint_as_float(x[e2 + 1]));
             m = max3(m, __uint_as_float(y[e2]), __uint_as_float(y[e2 + 1]));
           }
-        } else {
-#pragma unroll
-          for (int e2 = 0; e2 < 32; ++e2) {
-            if (c * 32 + e2 <= lim) m = fmaxf(m, __uint_as_float(x[e2]));
-            if (c * 32 + 32 + e2 <= lim) m = fmaxf(m, __uint_as_float(y[e2]));
-          }
         }
-      }
-      const bool empty = m == __int_as_float(0xff800000);
-      const float ms = empty ? 0.f : m * scale_log2;
-      float l = 0.f;
+        const float ms = m * scale_log2;
+        const uint64_t nms2 = f2_pack(-ms, -ms);
 #pragma unroll
-      for (int c = 0; c < BK / 32; c += 2) {
-        uint32_t x[32], y[32];
-        tmem_ld_x32(scol + c * 32, x);
-        tmem_ld_x32(scol + c * 32 + 32, y);
-        tmem_ld_wait();
-        uint32_t px[16], py[16];
+        for (int c = 0; c < BK / 32; c += 2) {
+          uint32_t x[32], y[32];
+          tmem_ld_x32(scol + c * 32, x);
+          tmem_ld_x32(scol + c * 32 + 32, y);
+          tmem_ld_wait();
+          uint32_t px[16], py[16];
 #pragma unroll
-        for (int e2 = 0; e2 < 32; e2 += 2) {
-          float a0 = ex2_approx(fmaf(__uint_as_float(x[e2]), scale_log2, -ms));
-          float a1 = ex2_approx(fmaf(__uint_as_float(x[e2 + 1]), scale_log2, -ms));
-          float b0 = ex2_approx(fmaf(__uint_as_float(y[e2]), scale_log2, -ms));
-          float b1 = ex2_approx(fmaf(__uint_as_float(y[e2 + 1]), scale_log2, -ms));
-          if (!full) {
-            a0 = (c * 32 + e2 <= lim) ? a0 : 0.f;
-            a1 = (c * 32 + e2 + 1 <= lim) ? a1 : 0.f;
-            b0 = (c * 32 + 32 + e2 <= lim) ? b0 : 0.f;
-            b1 = (c * 32 + 33 + e2 <= lim) ? b1 : 0.f;
+          for (int e2 = 0; e2 < 32; e2 += 2) {
+            float a0, a1, b0, b1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[e2]), __uint_as_float(x[e2 + 1])), scale2, nms2), a0, a1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(y[e2]), __uint_as_float(y[e2 + 1])), scale2, nms2), b0, b1);
+            a0 = ex2_approx(a0);
+            a1 = ex2_approx(a1);
+            b0 = ex2_approx(b0);
+            b1 = ex2_approx(b1);
+            lsum2 = f2_add(lsum2, f2_add(f2_pack(a0, a1), f2_pack(b0, b1)));
+            px[e2 >> 1] = pack_bf16x2(a0, a1);
+            py[e2 >> 1] = pack_bf16x2(b0, b1);
           }
-          l += (a0 + a1) + (b0 + b1);
-          px[e2 >> 1] = pack_bf16x2(a0, a1);
-          py[e2 >> 1] = pack_bf16x2(b0, b1);
+          tmem_st_x16(scol + c * 16, px);  // keys 32c..32c+31 -> packed columns 16c..16c+15
+          tmem_st_x16(scol + c * 16 + 16, py);
         }
-        tmem_st_x16(scol + c * 16, px);  // keys 32c..32c+31 -> packed columns 16c..16c+15
-        tmem_st_x16(scol + c * 16 + 16, py);
+        m = ms;
+      } else {
+        // diagonal tiles (and rows of blocks past t): one 32-column chunk at a time
+#pragma unroll 1
+        for (int c = 0; c < BK / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld_x32(scol + c * 32, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e <= lim) m = fmaxf(m, __uint_as_float(x[e]));
+        }
+        const bool none = m == __int_as_float(0xff800000);
+        const float ms = none ? 0.f : m * scale_log2;
+#pragma unroll 1
+        for (int c = 0; c < BK / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld_x32(scol + c * 32, x);
+          tmem_ld_wait();
+          uint32_t px[16];
+          float l = 0.f;
+#pragma unroll
+          for (int e2 = 0; e2 < 32; e2 += 2) {
+            float a0 = ex2_approx(fmaf(__uint_as_float(x[e2]), scale_log2, -ms));
+            float a1 = ex2_approx(fmaf(__uint_as_float(x[e2 + 1]), scale_log2, -ms));
+            a0 = c * 32 + e2 <= lim ? a0 : 0.f;
+            a1 = c * 32 + e2 + 1 <= lim ? a1 : 0.f;
+            l += a0 + a1;
+            px[e2 >> 1] = pack_bf16x2(a0, a1);
+          }
+          lsum2 = f2_add(lsum2, f2_pack(l, 0.f));
+          tmem_st_x16(scol + c * 16, px);
+        }
+        m = none ? __int_as_float(0xff800000) : ms;
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(par));
-      // ---- epilogue: normalised partial O and partial lse
-      if (!(ok = mbar_wait(o_full(par), ph, abort, st, 0x602))) break;
+      if (lane == 0) mbar_arrive(p_full(sb));
+      // (m, l) of the row for the combine; m = -inf marks a row without keys
+      if (t >= 0) {
+        float l0, l1;
+        f2_unpack(lsum2, l0, l1);
+        const int64_t prow = ((t - T0) * k + slot) * H_q + (int64_t)tg * gs + hh;
+        part_ml[prow] = make_float2(m, l0 + l1);
+      }
+    }
+  } else if (warp >= kWarpEpi0) {
+    // ------------------------------------------------------------ epilogue warpgroup
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t ocol = tmem + ((uint32_t)(quarter * 32) << 16) + L::TMEM_O;
+    const bool leader = warp == kWarpEpi0;
+    const uint32_t stg = sbase + L::OFF_STG;
+    bool lead_ok = true;  // the store issuer's own waits
+    for (int i = 0; i < n; ++i) {
+      const bool w = mbar_wait(o_full, i & 1, abort, st, 0x701);
+      // the staging tile is free once the previous tile's stores have read it
+      if (leader) bulk_wait_read_all();
+      // all four warps leave together (the named barriers have no time limit)
+      if (!epi_bar_and(w && lead_ok)) break;
       tc_fence_after();
-      const float inv = (!empty && l > 0.f) ? 1.f / l : 0.f;
-      const int64_t prow = t >= 0 ? ((t - T0) * k + slot) * H_q + (int64_t)tl.g * gs + hh : 0;
-      uint16_t* dst = part_o + prow * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; c += 2) {
+      for (int c = 0; c < L::NCD; ++c) {
         uint32_t x[2][32];
-        tmem_ld_x32(ocol + c * 32, x[0]);
-        tmem_ld_x32(ocol + c * 32 + 32, x[1]);
+        tmem_ld_x32(ocol + c * 64, x[0]);
+        tmem_ld_x32(ocol + c * 64 + 32, x[1]);
         tmem_ld_wait();
-        if (t >= 0) {
+        if (c == L::NCD - 1) {  // the whole row has left TMEM: hand O back to the tensor core
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_empty);
+        }
+        // columns 64c + 8jj .. +7 -> 16-byte unit jj of the row, 128B-swizzled
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2)
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const uint32_t* z = x[h2] + 8 * q4;
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(z[0]) * inv, __uint_as_float(z[1]) * inv);
-              v.y = pack_bf16x2(__uint_as_float(z[2]) * inv, __uint_as_float(z[3]) * inv);
-              v.z = pack_bf16x2(__uint_as_float(z[4]) * inv, __uint_as_float(z[5]) * inv);
-              v.w = pack_bf16x2(__uint_as_float(z[6]) * inv, __uint_as_float(z[7]) * inv);
-              *reinterpret_cast<uint4*>(dst + (c + h2) * 32 + q4 * 8) = v;
-            }
+        for (int jj = 0; jj < 8; ++jj) {
+          const uint32_t* z = x[jj >> 2] + (jj & 3) * 8;
+          const uint32_t a = stg + c * L::ROWS_CHUNK + row * 128 + ((jj ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a),
+                       "r"(pack_bf16x2(__uint_as_float(z[0]), __uint_as_float(z[1]))),
+                       "r"(pack_bf16x2(__uint_as_float(z[2]), __uint_as_float(z[3]))),
+                       "r"(pack_bf16x2(__uint_as_float(z[4]), __uint_as_float(z[5]))),
+                       "r"(pack_bf16x2(__uint_as_float(z[6]), __uint_as_float(z[7])))
+                       : "memory");
         }
       }
-      if (t >= 0)
-        part_lse[prow] = (!empty && l > 0.f) ? (ms + log2f(l)) * 0.69314718055994530942f : __int_as_float(0xff800000);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_empty(par));
+      fence_proxy_async_smem();
+      epi_bar_sync();
+      if (leader) {
+        const int ms_ = i % kMeta;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x702) ? 1 : 0;
+        lead_ok = __shfl_sync(0xffffffffu, w, 0) != 0;
+        const TileMeta& mt = meta[ms_];
+        if (lead_ok && lane < mt.count) {
+          const int32_t z = (int32_t)((mt.t[lane] - T0) * k + mt.slot[lane]);
+#pragma unroll
+          for (int c = 0; c < L::NCD; ++c)
+            tma_store_3d(&tmap_po, stg + c * L::ROWS_CHUNK + lane * 1024, c * 64, mt.g * gs, z);
+          bulk_commit();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(meta_empty(ms_));
+      }
     }
+    if (leader) bulk_wait_all();
   }
 
   __syncthreads();
@@ -456,23 +618,28 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 template <int D, int BK>
 cudaError_t launch_t(const void* q, const void* kk, const void* vv, const int32_t* entries, const int32_t* lo,
                      const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int k, int64_t nb,
-                     int gs, int P, int64_t T0, float scale, uint16_t* part_o, float* part_lse, DeviceStatus* st,
-                     cudaStream_t s) {
+                     int gs, int64_t T0, int64_t rows, float scale, uint16_t* part_o, float2* part_ml,
+                     DeviceStatus* st, cudaStream_t s) {
   using L = AttnLayout<D, BK>;
-  alignas(64) unsigned char tk[128], tv[128];
-  if (!encode_tmap_3d(tk, kk, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, (uint64_t)D * 2, (uint64_t)H_kv * D * 2, 64,
+  alignas(64) unsigned char tq[128], tk[128], tv[128], tpo[128];
+  const uint64_t row_bytes = (uint64_t)D * 2;
+  if (!encode_tmap_3d(tq, q, (uint64_t)D, (uint64_t)H_q, (uint64_t)N, row_bytes, (uint64_t)H_q * row_bytes, 64,
+                      (uint32_t)gs, 1, 128) ||
+      !encode_tmap_3d(tk, kk, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, row_bytes, (uint64_t)H_kv * row_bytes, 64,
                       1, BK, 128) ||
-      !encode_tmap_3d(tv, vv, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, (uint64_t)D * 2, (uint64_t)H_kv * D * 2, 64,
-                      1, BK, 128))
+      !encode_tmap_3d(tv, vv, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, row_bytes, (uint64_t)H_kv * row_bytes, 64,
+                      1, BK, 128) ||
+      !encode_tmap_3d(tpo, part_o, (uint64_t)D, (uint64_t)H_q, (uint64_t)rows, row_bytes,
+                      (uint64_t)H_q * row_bytes, 64, (uint32_t)gs, 1, 128))
     return cudaErrorInvalidValue;
   auto kern = attn_tc_kernel<D, BK>;
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;  // one CTA per SM: TMEM is never contended
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms(), kThreadsT, smem, s>>>(*reinterpret_cast<const CUtensorMap*>(tk),
-                                          *reinterpret_cast<const CUtensorMap*>(tv), (const uint16_t*)q, entries, lo,
-                                          cnt, tile_off, N, H_q, H_kv, k, nb, gs, P, T0,
-                                          scale * 1.4426950408889634f, part_o, part_lse, st);
+  kern<<<num_sms(), kThreadsT, smem, s>>>(
+      *reinterpret_cast<const CUtensorMap*>(tq), *reinterpret_cast<const CUtensorMap*>(tk),
+      *reinterpret_cast<const CUtensorMap*>(tv), *reinterpret_cast<const CUtensorMap*>(tpo), entries, lo, cnt,
+      tile_off, N, H_q, H_kv, k, nb, gs, T0, scale * 1.4426950408889634f, part_ml, st);
   return cudaGetLastError();
 }
 
@@ -480,19 +647,19 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const int32_
 
 cudaError_t launch_attn_tiles(const void* q, const void* kk, const void* vv, const int32_t* entries, const int32_t* lo,
                               const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d,
-                              int Bk, int k, int64_t nb, int gs, int P, int64_t T0, float scale, uint16_t* part_o,
-                              float* part_lse, DeviceStatus* st, cudaStream_t s) {
+                              int Bk, int k, int64_t nb, int gs, int64_t T0, int64_t rows, float scale,
+                              uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s) {
   if (d == 64 && Bk == 64)
-    return launch_t<64, 64>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, P, T0, scale, part_o,
-                            part_lse, st, s);
+    return launch_t<64, 64>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale, part_o,
+                            part_ml, st, s);
   if (d == 64)
-    return launch_t<64, 128>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, P, T0, scale, part_o,
-                             part_lse, st, s);
+    return launch_t<64, 128>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale,
+                             part_o, part_ml, st, s);
   if (Bk == 64)
-    return launch_t<128, 64>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, P, T0, scale, part_o,
-                             part_lse, st, s);
-  return launch_t<128, 128>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, P, T0, scale, part_o,
-                            part_lse, st, s);
+    return launch_t<128, 64>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale,
+                             part_o, part_ml, st, s);
+  return launch_t<128, 128>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale, part_o,
+                            part_ml, st, s);
 }
 
 }  // namespace msa

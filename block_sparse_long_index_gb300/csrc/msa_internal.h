@@ -53,8 +53,8 @@ size_t attn_scratch_bytes(const AttnPlan& p);
 // The tcgen05 tile kernel of one query slab (msa_attn_tile.cu).
 cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const int32_t* entries, const int32_t* lo,
                               const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d,
-                              int Bk, int k_blocks, int64_t nb, int gs, int P, int64_t T0, float scale,
-                              uint16_t* part_o, float* part_lse, DeviceStatus* st, cudaStream_t s);
+                              int Bk, int k_blocks, int64_t nb, int gs, int64_t T0, int64_t rows, float scale,
+                              uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);
 

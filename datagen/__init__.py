@@ -90,6 +90,9 @@ CONFIGS = {
     # a smaller decode case (same shapes, 256K context) for profiler captures of a few GB
     "decode_256k": Config("decode_256k", "decode", B=4, ctx=1 << 18, H_q=64, H_kv=8, d=128, d_I=128, Bk=128,
                           k=16, needles=4, index=5),
+    # a smaller prefill case (same shapes, N = 8K) for profiler captures of a few GB
+    "prefill_8k": Config("prefill_8k", "prefill", N=8192, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
+                         needles=4, index=6),
     "prefill_1m": Config("prefill_1m", "prefill", N=1 << 20, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
                          needles=16, index=4),
 }
