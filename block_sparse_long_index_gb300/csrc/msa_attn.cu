@@ -12,7 +12,8 @@
 //   2. Per query slab [T0, T1): for every (group, block) the sub-list of
 //      entries with t in the slab (two binary searches, the list is sorted),
 //      cut into tiles of 16 positions; an exclusive scan turns the tile
-//      counts into a flat work list (hot blocks simply yield more tiles).
+//      counts into a flat work list (hot blocks simply yield more tiles),
+//      and one 128-byte record per tile lists its positions and slots.
 //   3. Tile kernel (msa_attn_tile.cu, persistent, tcgen05): K_b and V_b are
 //      staged in shared memory once per run of tiles of the same block and
 //      shared by each tile's 16 positions x 8 head slots = 128 query rows
@@ -29,7 +30,7 @@ namespace msa {
 
 namespace {
 
-constexpr int kTilePos = 16;  // query positions per attention tile (x 8 head slots = 128 MMA rows)
+constexpr int kTilePos = kTilePositions;  // query positions per tile (x 8 head slots = 128 MMA rows)
 
 // ---------------------------------------------------------------- schedule
 // For each (g, b): [lo, hi) of the group's entry list with t in [T0, T1).
@@ -97,6 +98,45 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(const int32_t* __restr
     run += x;
   }
   if (tid == blockDim.x - 1) off[n] = run;
+}
+
+// Record of every tile: 16 threads per tile, thread pp fills position pp.
+__global__ void __launch_bounds__(256) tile_records_kernel(const int32_t* __restrict__ tile_off,
+                                                           const int32_t* __restrict__ lo,
+                                                           const int32_t* __restrict__ cnt,
+                                                           const int32_t* __restrict__ entries, int64_t N, int k,
+                                                           int64_t nb, int64_t n_gb, int64_t max_tiles,
+                                                           TileRecord* __restrict__ rec) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t tile = gt / kTilePos;
+  const int pp = (int)(gt % kTilePos);
+  const int32_t total = tile_off[n_gb];
+  if (tile >= total || tile >= max_tiles) return;
+  // the last (g, b) whose first tile is <= tile: its list is not empty
+  int64_t l = 0, h = n_gb;
+  while (h - l > 1) {
+    const int64_t m = (l + h) >> 1;
+    if (tile_off[m] <= tile) l = m; else h = m;
+  }
+  const int64_t gb = l;
+  const int g = (int)(gb / nb);
+  const int32_t first = lo[gb] + (int32_t)(tile - tile_off[gb]) * kTilePos;
+  const int count = min(kTilePos, lo[gb] + cnt[gb] - first);
+  TileRecord& r = rec[tile];
+  if (pp == 0) {
+    r.gb = (int32_t)gb;
+    r.g = g;
+    r.b = (int32_t)(gb % nb);
+    r.count = count;
+  }
+  int32_t t = -1, slot = 0;
+  if (pp < count) {
+    const int32_t e = entries[(int64_t)g * N * k + first + pp];
+    t = e / k;
+    slot = e - t * k;
+  }
+  r.t[pp] = t;
+  r.slot[pp] = (uint8_t)slot;
 }
 
 // ---------------------------------------------------------------- combine
@@ -194,6 +234,7 @@ struct AttnScratch {
   int32_t *row_ptr, *entries, *n_entries;
   InvertScratch inv;
   int32_t *lo, *cnt, *tiles, *tile_off;
+  TileRecord* rec;
   uint16_t* part_o;
   float2* part_ml;
 };
@@ -218,6 +259,7 @@ static size_t carve(const AttnPlan& p, void* base, AttnScratch* out) {
   s.cnt = (int32_t*)take((size_t)G * p.nb * 4);
   s.tiles = (int32_t*)take((size_t)G * p.nb * 4);
   s.tile_off = (int32_t*)take(((size_t)G * p.nb + 1) * 4);
+  s.rec = (TileRecord*)take((size_t)p.max_tiles * sizeof(TileRecord));
   s.part_o = (uint16_t*)take((size_t)p.slab * p.k * p.H_q * p.d * 2);
   s.part_ml = (float2*)take((size_t)p.slab * p.k * p.H_q * 8);
   if (out) *out = s;
@@ -236,13 +278,14 @@ AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k) {
   p.k = k;
   p.gs = H_q / H_kv;
   p.nb = (N + Bk - 1) / Bk;
-  p.P = kTilePos;
   // partial results of one slab: slab * k * H_q * (2d + 8) bytes, at most ~36 GB
   const double per_pos = (double)k * H_q * (2.0 * d + 8.0);
   int64_t cap = (int64_t)(36.0e9 / per_pos);
   if (cap > 131072) cap = 131072;
   if (cap < 1024) cap = 1024;
   p.slab = N < cap ? N : cap;
+  // sum over (g, b) of ceil(cnt / 16) <= entries / 16 + lists
+  p.max_tiles = (int64_t)H_kv * ceil_div(p.slab * k, kTilePos) + (int64_t)H_kv * p.nb;
   return p;
 }
 
@@ -259,10 +302,12 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
   for (int64_t T0 = 0; T0 < p.N; T0 += p.slab) {
     const int64_t T1 = T0 + p.slab < p.N ? T0 + p.slab : p.N;
     sched_count_kernel<<<(unsigned)((n_gb + 255) / 256), 256, 0, s>>>(sc.row_ptr, sc.entries, p.N, G, p.k, p.nb, T0,
-                                                                      T1, p.P, sc.lo, sc.cnt, sc.tiles);
+                                                                      T1, kTilePos, sc.lo, sc.cnt, sc.tiles);
     sched_scan_kernel<<<1, 1024, 0, s>>>(sc.tiles, n_gb, sc.tile_off);
-    e = launch_attn_tiles(q, k, v, sc.entries, sc.lo, sc.cnt, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb,
-                          p.gs, T0, p.slab * p.k, scale, sc.part_o, sc.part_ml, st, s);
+    tile_records_kernel<<<(unsigned)ceil_div(p.max_tiles * kTilePos, 256), 256, 0, s>>>(
+        sc.tile_off, sc.lo, sc.cnt, sc.entries, p.N, p.k, p.nb, n_gb, p.max_tiles, sc.rec);
+    e = launch_attn_tiles(q, k, v, sc.rec, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb, p.gs, T0,
+                          p.slab * p.k, p.max_tiles, scale, sc.part_o, sc.part_ml, st, s);
     if (e != cudaSuccess) return e;
     const size_t cs = (size_t)2 * p.k * p.H_q * sizeof(float);
     auto ck = p.d == 64 ? combine_kernel<64> : combine_kernel<128>;

@@ -14,9 +14,10 @@
 //   row's un-normalised O goes out in bf16 and its (m, l = sum P) in fp32, so
 //   the combine divides once per (t, h) by the merged sum.
 // Roles (512 threads):
-//   warp 0        Q loader: publishes each tile's metadata (query positions,
-//                 slots) to a shared ring and gathers its Q rows with one TMA
-//                 box {64 dims, gs heads} per position into one of four
+//   warp 3        copies each tile's 128-byte record (query positions, slots)
+//                 from the schedule into an 8-slot shared ring;
+//   warp 0        Q loader: gathers a tile's Q rows with one TMA box
+//                 {64 dims, gs heads} per position into one of four
 //                 128B-swizzled K-major Q buffers;
 //   warp 1        TMEM owner; lane 0 issues tcgen05.mma.  S/P has three TMEM
 //                 buffers and O one, so S runs up to two tiles ahead of P V:
@@ -52,20 +53,15 @@ constexpr int kMeta = 8;      // tile metadata slots
 constexpr int kWarpLoad = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpKv = 2;
+constexpr int kWarpMeta = 3;
 constexpr int kWarpSoft0 = 4;
 constexpr int kWarpEpi0 = 12;
 constexpr int kThreadsT = 16 * 32;
 constexpr int kSoftWarps = 4;  // per warpgroup
 constexpr int kEpiWarps = 4;
-constexpr int kMetaReaders = 1 + kSoftWarps + 1;  // MMA issuer, one softmax warpgroup, epilogue store issuer
-
-// What the Q loader publishes per tile, so that no other role walks the
-// schedule in global memory.
-struct TileMeta {
-  int32_t gb, g, b, count;
-  int32_t t[kPosT];     // query position (valid for pp < count)
-  int32_t slot[kPosT];  // its slot in the position's block set
-};
+// Q loader, K/V loader, MMA issuer, one softmax warpgroup, epilogue store issuer
+constexpr int kMetaReaders = 1 + 1 + 1 + kSoftWarps + 1;
+static_assert(kPosT == kTilePositions, "tile records hold 16 positions");
 
 template <int D, int BK>
 struct AttnLayout {
@@ -85,45 +81,6 @@ struct AttnLayout {
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
-struct Tile {
-  int64_t gb;
-  int g;
-  int64_t b;
-  int32_t first;
-  int count;
-};
-
-// Walks a CTA's contiguous tile range: one binary search for the first tile,
-// then (g, b) advances past empty lists as the tile index grows.
-struct TileIter {
-  const int32_t* __restrict__ tile_off;
-  const int32_t* __restrict__ lo;
-  const int32_t* __restrict__ cnt;
-  int64_t n_gb, nb;
-  int64_t gb;
-
-  __device__ __forceinline__ void seek(int32_t tile) {
-    int64_t l = 0, h = n_gb;
-    while (h - l > 1) {
-      const int64_t m = (l + h) >> 1;
-      if (tile_off[m] <= tile) l = m; else h = m;
-    }
-    gb = l;
-  }
-  // tiles must be visited in nondecreasing order
-  __device__ __forceinline__ Tile at(int32_t tile) {
-    while (gb + 1 < n_gb && tile_off[gb + 1] <= tile) ++gb;
-    Tile r;
-    r.gb = gb;
-    r.g = (int)(gb / nb);
-    r.b = gb % nb;
-    const int32_t base = lo[gb];
-    r.first = base + (tile - tile_off[gb]) * kPosT;
-    r.count = min(kPosT, base + cnt[gb] - r.first);
-    return r;
-  }
-};
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar) {
   asm volatile(
@@ -131,6 +88,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "[%5];\n" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
+}
+// Plain bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                   dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
@@ -213,16 +177,15 @@ template <int D, int BK>
 __global__ void __launch_bounds__(kThreadsT, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_po,
-                   const int32_t* __restrict__ entries, const int32_t* __restrict__ lo_arr,
-                   const int32_t* __restrict__ cnt_arr, const int32_t* __restrict__ tile_off, int64_t N, int H_q,
-                   int H_kv, int k, int64_t nb, int gs, int64_t T0, float scale_log2, float2* __restrict__ part_ml,
-                   DeviceStatus* st) {
+                   const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t max_tiles,
+                   int H_q, int H_kv, int k, int64_t nb, int gs, int64_t T0, float scale_log2,
+                   float2* __restrict__ part_ml, DeviceStatus* st) {
   using L = AttnLayout<D, BK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ TileMeta meta[kMeta];
+  __shared__ TileRecord meta[kMeta];
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
@@ -281,51 +244,50 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   volatile int* abort = &abort_flag;
 
   const int64_t n_gb = (int64_t)H_kv * nb;
-  const int32_t total = tile_off[n_gb];
-  const int32_t t_begin = (int32_t)((int64_t)total * blockIdx.x / gridDim.x);
-  const int32_t t_end = (int32_t)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-  const int n = t_end - t_begin;
-  TileIter it{tile_off, lo_arr, cnt_arr, n_gb, nb, 0};
-  if (n > 0) it.seek(t_begin);
+  const int64_t total = min((int64_t)tile_off[n_gb], max_tiles);
+  const int64_t t_begin = total * blockIdx.x / gridDim.x;
+  const int n = (int)(total * (blockIdx.x + 1) / gridDim.x - t_begin);
 
-  if (warp == kWarpLoad) {
-    // ------------------------------------------------------------ Q loader + tile metadata
+  if (warp == kWarpMeta) {
+    // ------------------------------------------------------------ tile records -> shared ring
+    if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
+      for (int i = 0; i < n && ok; ++i) {
+        const int ms_ = i % kMeta;
+        if (!(ok = mbar_wait(meta_empty(ms_), ((i / kMeta) & 1) ^ 1, abort, st, 0x300))) break;
+        mbar_arrive_expect_tx(meta_full(ms_), (uint32_t)sizeof(TileRecord));
+        bulk_load(smem_u32(&meta[ms_]), rec + t_begin + i, (uint32_t)sizeof(TileRecord), meta_full(ms_));
+        issued = i + 1;
+      }
+      // after an abort: wait for the copies still in flight before the CTA exits
+      if (!ok)
+        for (int i = max(0, issued - kMeta); i < issued; ++i)
+          mbar_wait(meta_full(i % kMeta), (i / kMeta) & 1, nullptr, st, 0x3F1);
+    }
+  } else if (warp == kWarpLoad) {
+    // ------------------------------------------------------------ Q loader
     bool ok = true;
     int issued = 0;
     for (int i = 0; i < n && ok; ++i) {
       const int ms_ = i % kMeta;
-      int w = 1;
-      if (lane == 0) w = mbar_wait(meta_empty(ms_), ((i / kMeta) & 1) ^ 1, abort, st, 0x400) ? 1 : 0;
-      if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
-      const Tile tl = it.at(t_begin + i);
-      const int32_t* E = entries + (int64_t)tl.g * N * k;
-      TileMeta& mt = meta[ms_];
-      int32_t t = -1;
-      if (lane < kPosT && lane < tl.count) {
-        const int32_t e = E[tl.first + lane];
-        t = e / k;
-        mt.t[lane] = t;
-        mt.slot[lane] = e - t * k;
-      }
-      if (lane == 0) {
-        mt.gb = (int32_t)tl.gb;
-        mt.g = tl.g;
-        mt.b = (int32_t)tl.b;
-        mt.count = tl.count;
-      }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x400)))) break;
+      const int count = meta[ms_].count, g = meta[ms_].g;
+      const int32_t t = lane < count ? meta[ms_].t[lane] : -1;
       __syncwarp();
-      if (lane == 0) mbar_arrive(meta_full(ms_));
+      if (lane == 0) mbar_arrive(meta_empty(ms_));
       const int qb = i % kQBufs;
+      int w = 1;
       if (lane == 0) {
         w = mbar_wait(q_empty(qb), ((i / kQBufs) & 1) ^ 1, abort, st, 0x401) ? 1 : 0;
-        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(tl.count * L::NCD * gs * 128));
+        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(count * L::NCD * gs * 128));
       }
       if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
       if (t >= 0) {
         const uint32_t dst = sbase + L::OFF_Q + qb * L::Q_BYTES + lane * 1024;
 #pragma unroll
         for (int c = 0; c < L::NCD; ++c)
-          tma_load_3d(dst + c * L::ROWS_CHUNK, &tmap_q, c * 64, tl.g * gs, t, q_full(qb));
+          tma_load_3d(dst + c * L::ROWS_CHUNK, &tmap_q, c * 64, g * gs, t, q_full(qb));
       }
       issued = i + 1;
     }
@@ -341,14 +303,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       int last = -1;
       bool ok = true;
       for (int i = 0; i < n && ok; ++i) {
-        const Tile tl = it.at(t_begin + i);
-        if (tl.gb == prev) continue;
-        prev = tl.gb;
+        const int ms_ = i % kMeta;
+        if (!(ok = mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x403))) break;
+        const int64_t gb = meta[ms_].gb;
+        const int g = meta[ms_].g;
+        const int32_t b = meta[ms_].b;
+        mbar_arrive(meta_empty(ms_));
+        if (gb == prev) continue;
+        prev = gb;
         if (!(ok = mbar_wait(kv_empty, (runs & 1) ^ 1, abort, st, 0x402))) break;
         mbar_arrive_expect_tx(kv_full, (uint32_t)(2 * L::K_BYTES));
         for (int c = 0; c < L::NCD; ++c) {
-          tma_load_3d(sbase + L::OFF_K + c * L::KV_CHUNK, &tmap_k, c * 64, tl.g, (int32_t)(tl.b * BK), kv_full);
-          tma_load_3d(sbase + L::OFF_V + c * L::KV_CHUNK, &tmap_v, c * 64, tl.g, (int32_t)(tl.b * BK), kv_full);
+          tma_load_3d(sbase + L::OFF_K + c * L::KV_CHUNK, &tmap_k, c * 64, g, b * BK, kv_full);
+          tma_load_3d(sbase + L::OFF_V + c * L::KV_CHUNK, &tmap_v, c * 64, g, b * BK, kv_full);
         }
         last = runs & 1;
         ++runs;
@@ -363,18 +330,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       uint32_t kv_cnt = 0;
       bool ok = true;
       int64_t gb_staged = -1;
-      // (g, b) of tile j, read once per tile from the metadata ring in tile order
-      int32_t gbq[8];
+      // (g, b) of tile j from the record ring; the issuer holds a tile's slot
+      // from its first look until that tile's P V has been issued
       int fetched = 0;
       auto gb_of = [&](int j, int32_t& out) -> bool {
-        while (fetched <= j) {
-          const int ms_ = fetched % kMeta;
-          if (!mbar_wait(meta_full(ms_), (fetched / kMeta) & 1, abort, st, 0x500)) return false;
-          gbq[fetched & 7] = meta[ms_].gb;
-          mbar_arrive(meta_empty(ms_));
-          ++fetched;
-        }
-        out = gbq[j & 7];
+        for (; fetched <= j; ++fetched)
+          if (!mbar_wait(meta_full(fetched % kMeta), (fetched / kMeta) & 1, abort, st, 0x500)) return false;
+        out = meta[j % kMeta].gb;
         return true;
       };
       int s_next = 0;  // next tile whose S is not issued
@@ -424,6 +386,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           mma_bf16_ts(tmem + L::TMEM_O, pcol + 8 * ks, bd, IDESC_PV, ks > 0);
         }
         umma_commit(o_full);
+        mbar_arrive(meta_empty(i % kMeta));
         const bool last_of_block = (i + 1 == n) || (s_next > i + 1 ? false : gb_s_next != gb_cur);
         if (last_of_block) umma_commit(kv_empty);
       }
@@ -593,7 +556,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         int w = 1;
         if (lane == 0) w = mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x702) ? 1 : 0;
         lead_ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        const TileMeta& mt = meta[ms_];
+        const TileRecord& mt = meta[ms_];
         if (lead_ok && lane < mt.count) {
           const int32_t z = (int32_t)((mt.t[lane] - T0) * k + mt.slot[lane]);
 #pragma unroll
@@ -616,10 +579,10 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 }
 
 template <int D, int BK>
-cudaError_t launch_t(const void* q, const void* kk, const void* vv, const int32_t* entries, const int32_t* lo,
-                     const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int k, int64_t nb,
-                     int gs, int64_t T0, int64_t rows, float scale, uint16_t* part_o, float2* part_ml,
-                     DeviceStatus* st, cudaStream_t s) {
+cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRecord* rec, const int32_t* tile_off,
+                     int64_t N, int H_q, int H_kv, int k, int64_t nb, int gs, int64_t T0, int64_t rows,
+                     int64_t max_tiles, float scale, uint16_t* part_o, float2* part_ml, DeviceStatus* st,
+                     cudaStream_t s) {
   using L = AttnLayout<D, BK>;
   alignas(64) unsigned char tq[128], tk[128], tv[128], tpo[128];
   const uint64_t row_bytes = (uint64_t)D * 2;
@@ -638,28 +601,21 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const int32_
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kThreadsT, smem, s>>>(
       *reinterpret_cast<const CUtensorMap*>(tq), *reinterpret_cast<const CUtensorMap*>(tk),
-      *reinterpret_cast<const CUtensorMap*>(tv), *reinterpret_cast<const CUtensorMap*>(tpo), entries, lo, cnt,
-      tile_off, N, H_q, H_kv, k, nb, gs, T0, scale * 1.4426950408889634f, part_ml, st);
+      *reinterpret_cast<const CUtensorMap*>(tv), *reinterpret_cast<const CUtensorMap*>(tpo), rec, tile_off,
+      max_tiles, H_q, H_kv, k, nb, gs, T0, scale * 1.4426950408889634f, part_ml, st);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_tiles(const void* q, const void* kk, const void* vv, const int32_t* entries, const int32_t* lo,
-                              const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d,
-                              int Bk, int k, int64_t nb, int gs, int64_t T0, int64_t rows, float scale,
-                              uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s) {
-  if (d == 64 && Bk == 64)
-    return launch_t<64, 64>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale, part_o,
-                            part_ml, st, s);
-  if (d == 64)
-    return launch_t<64, 128>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale,
-                             part_o, part_ml, st, s);
-  if (Bk == 64)
-    return launch_t<128, 64>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale,
-                             part_o, part_ml, st, s);
-  return launch_t<128, 128>(q, kk, vv, entries, lo, cnt, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, scale, part_o,
-                            part_ml, st, s);
+cudaError_t launch_attn_tiles(const void* q, const void* kk, const void* vv, const TileRecord* rec,
+                              const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k, int64_t nb,
+                              int gs, int64_t T0, int64_t rows, int64_t max_tiles, float scale, uint16_t* part_o,
+                              float2* part_ml, DeviceStatus* st, cudaStream_t s) {
+  auto launch = d == 64 ? (Bk == 64 ? launch_t<64, 64> : launch_t<64, 128>)
+                        : (Bk == 64 ? launch_t<128, 64> : launch_t<128, 128>);
+  return launch(q, kk, vv, rec, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, max_tiles, scale, part_o, part_ml, st,
+                s);
 }
 
 }  // namespace msa

@@ -41,19 +41,34 @@ cudaError_t launch_invert(const int32_t* block_idx, int64_t N, int G, int Bk, in
                           cudaStream_t s);
 
 // ---- attention (msa_attn.cu)
+// One attention tile of a slab's flat work list: (group g, block b) and up to
+// kTilePositions query positions that chose b, with each position's slot in
+// its block set.  Written by the schedule, copied whole into shared memory by
+// the tile kernel (128 bytes, 16-byte aligned).
+constexpr int kTilePositions = 16;
+struct alignas(16) TileRecord {
+  int32_t gb;     // g * nb + b
+  int32_t g, b;
+  int32_t count;  // positions in the tile, 1..16
+  int32_t t[kTilePositions];
+  uint8_t slot[kTilePositions];
+  int32_t pad[4 + 4];
+};
+static_assert(sizeof(TileRecord) == 128, "tile record is one 128-byte line");
+
 struct AttnPlan {
   int64_t N;
   int H_q, H_kv, d, Bk, k, gs;
   int64_t nb;
-  int64_t slab;  // query positions per slab
-  int P;         // query positions per tile
+  int64_t slab;       // query positions per slab
+  int64_t max_tiles;  // bound on the tiles of one slab
 };
 AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k);
 size_t attn_scratch_bytes(const AttnPlan& p);
 // The tcgen05 tile kernel of one query slab (msa_attn_tile.cu).
-cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const int32_t* entries, const int32_t* lo,
-                              const int32_t* cnt, const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d,
-                              int Bk, int k_blocks, int64_t nb, int gs, int64_t T0, int64_t rows, float scale,
+cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const TileRecord* rec,
+                              const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k_blocks,
+                              int64_t nb, int gs, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
                               uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);
