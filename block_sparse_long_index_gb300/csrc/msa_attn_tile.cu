@@ -16,9 +16,9 @@
 // Roles (512 threads):
 //   warp 3        copies each tile's 128-byte record (query positions, slots)
 //                 from the schedule into an 8-slot shared ring;
-//   warp 0        Q loader: gathers a tile's Q rows with one TMA box
-//                 {64 dims, gs heads} per position into one of four
-//                 128B-swizzled K-major Q buffers;
+//   warp 0        Q loader: gathers a tile's Q rows with one TMA box per
+//                 position (8 heads x d, as d/64 swizzled 1 KB atoms) into one
+//                 of four position-major, 128B-swizzled K-major Q buffers;
 //   warp 1        TMEM owner; lane 0 issues tcgen05.mma.  S/P has three TMEM
 //                 buffers and O one, so S runs up to two tiles ahead of P V:
 //                 per tile i it issues every S(j), j <= i+2, of i's K/V block,
@@ -26,8 +26,9 @@
 //   warp 2        K/V loader: one TMA load of K_b and V_b per run of tiles of
 //                 the same block, released after the run's last P V;
 //   warps 4..11   two softmax warpgroups (tiles of each parity);
-//   warps 12..15  epilogue warpgroup: O -> bf16 in a swizzled shared tile,
-//                 written out by TMA stores of one box per position.
+//   warps 12..15  epilogue warpgroup: O -> bf16 in a swizzled shared tile of
+//                 the same layout, written out by TMA stores (one box per
+//                 position when gs = 8, one per 64 dims otherwise).
 // Buffer reuse needs no extra waits: S(j) is issued after PV(j-3) (tensor
 // core operations run in issue order), and each barrier phase a role waits
 // for cannot be overtaken by the next one (the next use of a buffer depends,
@@ -63,11 +64,14 @@ constexpr int kEpiWarps = 4;
 constexpr int kMetaReaders = 1 + 1 + 1 + kSoftWarps + 1;
 static_assert(kPosT == kTilePositions, "tile records hold 16 positions");
 
+// Q and O tiles in shared memory are position-major: position pp holds its
+// d/64 chunks of 8 rows x 128 bytes (one 128B-swizzle atom each) in
+// POS_BYTES, so rows 8pp..8pp+7 of K-chunk c sit at pp * POS_BYTES + c * 1024.
 template <int D, int BK>
 struct AttnLayout {
   static constexpr int NCD = D / 64;                // 64-column chunks of d
-  static constexpr int ROWS_CHUNK = kRowsT * 128;   // one chunk of 128 rows x 128 bytes
-  static constexpr int Q_BYTES = NCD * ROWS_CHUNK;
+  static constexpr int POS_BYTES = NCD * 1024;
+  static constexpr int Q_BYTES = kPosT * POS_BYTES;
   static constexpr int KV_CHUNK = BK * 128;
   static constexpr int K_BYTES = NCD * KV_CHUNK;
   static constexpr int OFF_Q = 0;
@@ -96,11 +100,30 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                : "memory");
 }
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            int32_t w, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                             int32_t w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(x), "r"(y), "r"(z)
+               "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
+}
+// K-major, 128B-swizzled operand whose 8-row atoms are `sbo` bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_sbo(uint32_t saddr, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1u << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1u << 46;
+  d |= (uint64_t)2u << 61;
+  return d;
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
@@ -178,7 +201,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_po,
                    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t max_tiles,
-                   int H_q, int H_kv, int k, int64_t nb, int gs, int64_t T0, float scale_log2,
+                   int H_q, int H_kv, int k, int64_t nb, int gs, int q_box_heads, int64_t T0, float scale_log2,
                    float2* __restrict__ part_ml, DeviceStatus* st) {
   using L = AttnLayout<D, BK>;
   extern __shared__ uint8_t smem_raw[];
@@ -280,14 +303,17 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       int w = 1;
       if (lane == 0) {
         w = mbar_wait(q_empty(qb), ((i / kQBufs) & 1) ^ 1, abort, st, 0x401) ? 1 : 0;
-        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(count * L::NCD * gs * 128));
+        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(count * L::NCD * q_box_heads * 128));
       }
       if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
-      if (t >= 0) {
-        const uint32_t dst = sbase + L::OFF_Q + qb * L::Q_BYTES + lane * 1024;
+      if (t >= 0) {  // heads g*gs .. g*gs + q_box_heads - 1 (past H_q: zero fill)
+        const uint32_t dst = sbase + L::OFF_Q + qb * L::Q_BYTES + lane * L::POS_BYTES;
+        if (q_box_heads == 8) {  // all d/64 atoms in one box
+          tma_load_4d(dst, &tmap_q, 0, g * gs, 0, t, q_full(qb));
+        } else {                 // fewer than 8 heads: one box per atom
 #pragma unroll
-        for (int c = 0; c < L::NCD; ++c)
-          tma_load_3d(dst + c * L::ROWS_CHUNK, &tmap_q, c * 64, g * gs, t, q_full(qb));
+          for (int c = 0; c < L::NCD; ++c) tma_load_4d(dst + c * 1024, &tmap_q, 0, g * gs, c, t, q_full(qb));
+        }
       }
       issued = i + 1;
     }
@@ -357,7 +383,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         for (int ks = 0; ks < D / 16; ++ks) {
           const int c = ks >> 2, kk = ks & 3;
           const uint64_t ad =
-              umma_desc_kmajor(sbase + L::OFF_Q + qb * L::Q_BYTES + c * L::ROWS_CHUNK + kk * 32, 128);
+              umma_desc_kmajor_sbo(sbase + L::OFF_Q + qb * L::Q_BYTES + c * 1024 + kk * 32, L::POS_BYTES);
           const uint64_t bd = umma_desc_kmajor(sbase + L::OFF_K + c * L::KV_CHUNK + kk * 32, 128);
           mma_bf16_ss(d, ad, bd, IDESC_S, ks > 0);
         }
@@ -517,6 +543,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t ocol = tmem + ((uint32_t)(quarter * 32) << 16) + L::TMEM_O;
     const bool leader = warp == kWarpEpi0;
     const uint32_t stg = sbase + L::OFF_STG;
+    const uint32_t my_row = stg + (row >> 3) * L::POS_BYTES + (row & 7) * 128;
     bool lead_ok = true;  // the store issuer's own waits
     for (int i = 0; i < n; ++i) {
       const bool w = mbar_wait(o_full, i & 1, abort, st, 0x701);
@@ -540,7 +567,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           const uint32_t* z = x[jj >> 2] + (jj & 3) * 8;
-          const uint32_t a = stg + c * L::ROWS_CHUNK + row * 128 + ((jj ^ (row & 7)) << 4);
+          const uint32_t a = my_row + c * 1024 + ((jj ^ (row & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a),
                        "r"(pack_bf16x2(__uint_as_float(z[0]), __uint_as_float(z[1]))),
                        "r"(pack_bf16x2(__uint_as_float(z[2]), __uint_as_float(z[3]))),
@@ -559,9 +586,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         const TileRecord& mt = meta[ms_];
         if (lead_ok && lane < mt.count) {
           const int32_t z = (int32_t)((mt.t[lane] - T0) * k + mt.slot[lane]);
+          const uint32_t src = stg + lane * L::POS_BYTES;
+          if (gs == 8) {  // the position's 8 heads x d in one box
+            tma_store_4d(&tmap_po, src, 0, mt.g * 8, 0, z);
+          } else {        // gs heads of each 64-dim chunk
 #pragma unroll
-          for (int c = 0; c < L::NCD; ++c)
-            tma_store_3d(&tmap_po, stg + c * L::ROWS_CHUNK + lane * 1024, c * 64, mt.g * gs, z);
+            for (int c = 0; c < L::NCD; ++c) tma_store_4d(&tmap_po, src + c * 1024, 0, mt.g * gs, c, z);
+          }
           bulk_commit();
         }
         __syncwarp();
@@ -586,14 +617,20 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
   using L = AttnLayout<D, BK>;
   alignas(64) unsigned char tq[128], tk[128], tv[128], tpo[128];
   const uint64_t row_bytes = (uint64_t)D * 2;
-  if (!encode_tmap_3d(tq, q, (uint64_t)D, (uint64_t)H_q, (uint64_t)N, row_bytes, (uint64_t)H_q * row_bytes, 64,
-                      (uint32_t)gs, 1, 128) ||
+  // Q and partial O as [rows][H_q][d/64][64] viewed in the order {64, H_q, d/64, rows}: a box
+  // {64, heads, d/64, 1} lands as d/64 atoms of `heads` x 128 bytes, i.e. the tiles' layout.
+  const int q_box_heads = H_q < 8 ? H_q : 8;
+  const uint64_t q_dims[4] = {64, (uint64_t)H_q, (uint64_t)L::NCD, (uint64_t)N};
+  const uint64_t po_dims[4] = {64, (uint64_t)H_q, (uint64_t)L::NCD, (uint64_t)rows};
+  const uint64_t qo_strides[3] = {row_bytes, 128, (uint64_t)H_q * row_bytes};
+  const uint32_t q_box[4] = {64, (uint32_t)q_box_heads, q_box_heads == 8 ? (uint32_t)L::NCD : 1u, 1};
+  const uint32_t po_box[4] = {64, (uint32_t)gs, gs == 8 ? (uint32_t)L::NCD : 1u, 1};
+  if (!encode_tmap_4d(tq, q, q_dims, qo_strides, q_box, 128) ||
       !encode_tmap_3d(tk, kk, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, row_bytes, (uint64_t)H_kv * row_bytes, 64,
                       1, BK, 128) ||
       !encode_tmap_3d(tv, vv, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, row_bytes, (uint64_t)H_kv * row_bytes, 64,
                       1, BK, 128) ||
-      !encode_tmap_3d(tpo, part_o, (uint64_t)D, (uint64_t)H_q, (uint64_t)rows, row_bytes,
-                      (uint64_t)H_q * row_bytes, 64, (uint32_t)gs, 1, 128))
+      !encode_tmap_4d(tpo, part_o, po_dims, qo_strides, po_box, 128))
     return cudaErrorInvalidValue;
   auto kern = attn_tc_kernel<D, BK>;
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;  // one CTA per SM: TMEM is never contended
@@ -602,7 +639,7 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
   kern<<<num_sms(), kThreadsT, smem, s>>>(
       *reinterpret_cast<const CUtensorMap*>(tq), *reinterpret_cast<const CUtensorMap*>(tk),
       *reinterpret_cast<const CUtensorMap*>(tv), *reinterpret_cast<const CUtensorMap*>(tpo), rec, tile_off,
-      max_tiles, H_q, H_kv, k, nb, gs, T0, scale * 1.4426950408889634f, part_ml, st);
+      max_tiles, H_q, H_kv, k, nb, gs, q_box_heads, T0, scale * 1.4426950408889634f, part_ml, st);
   return cudaGetLastError();
 }
 

@@ -75,6 +75,20 @@ bool encode_tmap_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_4d(void* tmap, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                    const uint32_t box[4], int swizzle_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode) return false;
+  cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t s[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                      const_cast<void*>(base), d, s, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(swizzle_bytes),
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace msa
 
 using msa::align_up;

@@ -23,6 +23,9 @@ bool encode_tmap_2d(void* tmap /* CUtensorMap */, const void* base, uint64_t inn
 // 3-D variant: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1 and 2, box {b0, b1, b2}.
 bool encode_tmap_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
                     uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes);
+// 4-D variant: byte strides of dims 1..3 in any order (a permuted view is allowed).
+bool encode_tmap_4d(void* tmap, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                    const uint32_t box[4], int swizzle_bytes);
 
 // ---- select (msa_select.cu)
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
