@@ -86,53 +86,52 @@ __device__ __forceinline__ uint4 ldg_stream_16(const void* p) {
 }
 
 // ------------------------------------------------------------------ top-k list
-// Keeps the best K (<= CAP) (score, block) pairs seen so far, best = larger
-// score, then smaller block id.  Slots are kept in ascending order of
-// goodness: slot 0 is the worst kept pair (the eviction candidate).  Slots
-// K..CAP-1 are locked with (+inf, INT_MIN), which outrank every real pair and
-// stay at the top; unfilled real slots hold (-inf, INT_MAX).  All indexing is
-// static so the list lives in registers.
-__device__ __forceinline__ bool worse(float s1, int b1, float s2, int b2) {
-  return s1 < s2 || (s1 == s2 && b1 > b2);
+// (score, block) pairs ranked by one unsigned 64-bit key: larger key = better
+// pair = larger score, then smaller block id.  The high word orders fp32
+// scores as unsigned integers (-0 is first made +0, so that equal scores tie
+// and fall to the block id); the low word is the complement of the id.
+__device__ __forceinline__ uint64_t rank_key(float s, int32_t b) {
+  uint32_t u = __float_as_uint(s + 0.0f);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)b);
+}
+__device__ __forceinline__ float rank_key_score(uint64_t key) {
+  const uint32_t u = (uint32_t)(key >> 32);
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+__device__ __forceinline__ int32_t rank_key_block(uint64_t key) {
+  return (int32_t)(0xFFFFFFFFu - (uint32_t)key);
 }
 
+// Keeps the best K (<= CAP) pairs seen so far as keys in ascending order:
+// slot 0 is the worst kept pair (the eviction candidate).  Slots K..CAP-1 are
+// locked with the largest key and stay on top; unfilled real slots hold key 0,
+// which every real pair beats.  All indexing is static so the list lives in
+// registers; an insertion is one compare and two selects per slot.
 template <int CAP>
 struct TopK {
-  float sc[CAP];
-  int ix[CAP];
+  uint64_t key[CAP];
 
   __device__ __forceinline__ void init(int K) {
 #pragma unroll
-    for (int i = 0; i < CAP; ++i) {
-      bool locked = i >= K;
-      sc[i] = locked ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
-      ix[i] = locked ? INT_MIN : INT_MAX;
-    }
+    for (int i = 0; i < CAP; ++i) key[i] = i >= K ? ~0ull : 0ull;
   }
 
-  // Cheap test for the common case: does (s, b) beat the worst kept pair?
-  __device__ __forceinline__ bool admits(float s, int b) const { return worse(sc[0], ix[0], s, b); }
+  __device__ __forceinline__ bool admits(float s, int b) const { return rank_key(s, b) > key[0]; }
 
-  __device__ __forceinline__ void insert(float s, int b) {
-    if (!admits(s, b)) return;
+  __device__ __forceinline__ void insert(float s, int b) { insert_key(rank_key(s, b)); }
+
+  __device__ __forceinline__ void insert_key(uint64_t x) {
+    if (x <= key[0]) return;
+    // below[i]: slot i holds a worse pair than x (true for a prefix of the slots)
+    bool below[CAP];
+#pragma unroll
+    for (int i = 0; i < CAP; ++i) below[i] = key[i] < x;
+    // the prefix shifts down one slot and x takes the last place of the prefix
 #pragma unroll
     for (int i = 0; i < CAP; ++i) {
-      float o_s = sc[i];
-      int o_b = ix[i];
-      if (i + 1 < CAP) {
-        float n_s = sc[i + 1];
-        int n_b = ix[i + 1];
-        if (worse(n_s, n_b, s, b)) {  // the next pair moves down one slot
-          sc[i] = n_s;
-          ix[i] = n_b;
-        } else if (i == 0 || worse(o_s, o_b, s, b)) {
-          sc[i] = s;
-          ix[i] = b;
-        }
-      } else if (i == 0 || worse(o_s, o_b, s, b)) {
-        sc[i] = s;
-        ix[i] = b;
-      }
+      const bool next_below = i + 1 < CAP && below[i + 1];
+      key[i] = next_below ? key[i + 1 < CAP ? i + 1 : i] : (below[i] ? x : key[i]);
     }
   }
 
@@ -142,9 +141,9 @@ struct TopK {
     int n = 0;
 #pragma unroll
     for (int i = CAP - 1; i >= 0; --i) {
-      if (ix[i] != INT_MIN && ix[i] != INT_MAX) {
-        out[n] = ix[i];
-        if (out_s) out_s[n] = sc[i];
+      if (key[i] != 0ull && key[i] != ~0ull) {
+        out[n] = rank_key_block(key[i]);
+        if (out_s) out_s[n] = rank_key_score(key[i]);
         ++n;
       }
     }

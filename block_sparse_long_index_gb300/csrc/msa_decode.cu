@@ -143,13 +143,6 @@ __global__ void __launch_bounds__(kScanThreads) decode_scan_kernel(
 // lists (each sorted best-first).  Thread i holds the head of list i (and of
 // lists i + blockDim, ...); each of the k-1 rounds takes the best head in the
 // CTA (larger score, then smaller block id) and advances the winner's list.
-__device__ __forceinline__ uint64_t rank_key(float s, int32_t b) {
-  // larger key = better pair: scores ordered as unsigned integers, ties to the smaller block
-  uint32_t u = __float_as_uint(s);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)b);
-}
-
 template <int CAP>
 __global__ void __launch_bounds__(1024) decode_merge_kernel(const float* __restrict__ cand_s,
                                                             const int32_t* __restrict__ cand_b,
