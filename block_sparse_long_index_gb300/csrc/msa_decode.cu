@@ -209,9 +209,12 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ block_idx, int64_t ctx_max,
                                                           int H_q, int G, int k, float scale,
                                                           float* __restrict__ part_o, float* __restrict__ part_lse) {
+  // the block's K rows [BK][D] (16-byte chunk c of row j stored at chunk c ^ (j mod C8)), then its V rows
+  extern __shared__ __align__(16) uint16_t kv_s[];
   __shared__ float qs[8][D];
-  __shared__ float ps[8][BK];
+  __shared__ __align__(16) float ps[BK][8];  // scores, then probabilities, key-major
   __shared__ float red[8][2];
+  constexpr int C8 = D / 8;  // 16-byte chunks per row
   const int slot = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gs = H_q / G;
@@ -228,26 +231,40 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     for (int hh = tid; hh < gs; hh += blockDim.x) pl[(int64_t)hh * k] = __int_as_float(0xff800000);
     return;
   }
+  // stage the visible K and V rows with every copy in flight at once (rows past nvis read as zero)
+  const int64_t kv_row = (int64_t)G * D;
+  const uint16_t* Kb = k_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
+  const uint16_t* Vb = v_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
+  uint16_t* Ks = kv_s;
+  uint16_t* Vs = kv_s + BK * D;
+  for (int i = tid; i < BK * C8; i += blockDim.x) {
+    const int j = i / C8, c8 = i % C8;
+    const bool in = j < nvis;
+    const int64_t off = (int64_t)(in ? j : 0) * kv_row + c8 * 8;
+    cp_async_16(Ks + j * D + (c8 ^ (j & (C8 - 1))) * 8, Kb + off, in ? 16 : 0);
+    cp_async_16(Vs + j * D + c8 * 8, Vb + off, in ? 16 : 0);
+  }
+  cp_async_commit();
   for (int i = tid; i < gs * D; i += blockDim.x) {
     int hh = i / D, cc = i % D;
     uint16_t w = q_t[((int64_t)seq * H_q + g * gs + hh) * D + cc];
     qs[hh][cc] = __uint_as_float((uint32_t)w << 16);
   }
+  cp_async_wait<0>();
   __syncthreads();
-  const int64_t kv_row = (int64_t)G * D;
-  const uint16_t* Kb = k_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
-  const uint16_t* Vb = v_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
-  // scores: thread j owns key j
+  // scores: thread j owns key j; all lanes take the same chunk c8 (q is a
+  // broadcast), which the swizzle spreads over distinct banks of the K rows
   for (int j = tid; j < BK; j += blockDim.x) {
     float sc[8];
 #pragma unroll
     for (int hh = 0; hh < 8; ++hh) sc[hh] = 0.f;
     if (j < nvis) {
-      const uint16_t* kr = Kb + (int64_t)j * kv_row;
-      for (int c8 = 0; c8 < D / 8; ++c8) {
-        uint4 v = *reinterpret_cast<const uint4*>(kr + c8 * 8);
-        float kv[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                       bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+      const uint16_t* kr = Ks + j * D;
+#pragma unroll 4
+      for (int c8 = 0; c8 < C8; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(kr + (c8 ^ (j & (C8 - 1))) * 8);
+        const float kv[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
+                             bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
 #pragma unroll
         for (int hh = 0; hh < 8; ++hh) {
           if (hh < gs) {
@@ -259,19 +276,19 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     }
 #pragma unroll
     for (int hh = 0; hh < 8; ++hh)
-      if (hh < gs) ps[hh][j] = (j < nvis) ? sc[hh] * scale : __int_as_float(0xff800000);
+      if (hh < gs) ps[j][hh] = (j < nvis) ? sc[hh] * scale : __int_as_float(0xff800000);
   }
   __syncthreads();
   // softmax statistics per head: warp w handles heads w, w+4
   for (int hh = warp; hh < gs; hh += 4) {
     float m = __int_as_float(0xff800000);
-    for (int j = lane; j < BK; j += 32) m = fmaxf(m, ps[hh][j]);
+    for (int j = lane; j < BK; j += 32) m = fmaxf(m, ps[j][hh]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f;
     for (int j = lane; j < BK; j += 32) {
-      float p = __expf(ps[hh][j] - m);
-      ps[hh][j] = p;
+      float p = __expf(ps[j][hh] - m);
+      ps[j][hh] = p;
       l += p;
     }
 #pragma unroll
@@ -282,16 +299,20 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     }
   }
   __syncthreads();
-  // O = P V: thread owns columns cc
+  // O = P V from shared memory: thread owns column cc
   for (int cc = tid; cc < D; cc += blockDim.x) {
     float o[8];
 #pragma unroll
     for (int hh = 0; hh < 8; ++hh) o[hh] = 0.f;
+#pragma unroll 4
     for (int j = 0; j < nvis; ++j) {
-      float vj = __uint_as_float((uint32_t)Vb[(int64_t)j * kv_row + cc] << 16);
+      const float vj = __uint_as_float((uint32_t)Vs[j * D + cc] << 16);
+      const float4 p0 = *reinterpret_cast<const float4*>(&ps[j][0]);
+      const float4 p1 = *reinterpret_cast<const float4*>(&ps[j][4]);
+      const float pj[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
       for (int hh = 0; hh < 8; ++hh)
-        if (hh < gs) o[hh] = fmaf(ps[hh][j], vj, o[hh]);
+        if (hh < gs) o[hh] = fmaf(pj[hh], vj, o[hh]);
     }
 #pragma unroll
     for (int hh = 0; hh < 8; ++hh)
@@ -416,20 +437,26 @@ cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_id
   }
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)p.k, (unsigned)p.H_kv, (unsigned)p.B);
+  auto attn_smem = [](int D, int BK) { return 2 * BK * D * 2; };  // K and V rows of one block
+  if (p.d == 128 && p.Bk == 128) {
+    e = cudaFuncSetAttribute(decode_attn_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             attn_smem(128, 128));
+    if (e != cudaSuccess) return e;
+  }
   if (p.d == 64 && p.Bk == 64)
-    decode_attn_kernel<64, 64><<<grid, 128, 0, s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
+    decode_attn_kernel<64, 64><<<grid, 128, attn_smem(64, 64), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
                                                     (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q, p.H_kv,
                                                     p.k, scale, sc.part_o, sc.part_lse);
   else if (p.d == 64)
-    decode_attn_kernel<64, 128><<<grid, 128, 0, s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
+    decode_attn_kernel<64, 128><<<grid, 128, attn_smem(64, 128), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
                                                      (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q,
                                                      p.H_kv, p.k, scale, sc.part_o, sc.part_lse);
   else if (p.Bk == 64)
-    decode_attn_kernel<128, 64><<<grid, 128, 0, s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
+    decode_attn_kernel<128, 64><<<grid, 128, attn_smem(128, 64), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
                                                      (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q,
                                                      p.H_kv, p.k, scale, sc.part_o, sc.part_lse);
   else
-    decode_attn_kernel<128, 128><<<grid, 128, 0, s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
+    decode_attn_kernel<128, 128><<<grid, 128, attn_smem(128, 128), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
                                                       (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q,
                                                       p.H_kv, p.k, scale, sc.part_o, sc.part_lse);
   e = cudaGetLastError();
