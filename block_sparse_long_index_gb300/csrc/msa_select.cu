@@ -8,16 +8,17 @@
 // local block pinned).
 //
 // Work item = (query tile of 128 rows, pair of GQA groups).  The index key
-// is shared by all groups, so one 128-key tile of k^I staged in shared memory
-// feeds GPC (<= 2) MMAs of 128 x 128 x d_I, one per group (128-wide B tiles
-// keep the operand traffic within what shared memory delivers per cycle):
+// is shared by all groups, so one 256-key tile of k^I staged in shared memory
+// feeds GPC (<= 2) MMAs of 128 x 256 x d_I, one per group (256-wide B tiles
+// run the tensor core closer to its peak than 128-wide ones):
 //   warp 0      TMA producer: the item's q^I tiles (A, resident for the
-//               item) and a 4-stage ring of k^I tiles (B), swizzled;
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma into one of two
-//               accumulator buffers (GPC x 128 fp32 columns each) and commits
-//               completion to mbarriers;
+//               item) and a ring of k^I tiles (B, 2 to 4 stages), swizzled;
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma into one 256-column
+//               fp32 accumulator per group (with one group, two buffers
+//               alternate), so one group's MMAs run while the other's scores
+//               are reduced, and commits completion to mbarriers;
 //   warps 2..9  epilogue: each thread owns one query row (a TMEM lane) of one
-//               group, loads its 128 scores with tcgen05.ld, reduces them with
+//               group, loads its 256 scores with tcgen05.ld, reduces them with
 //               3-input max into block maxima (one per Bk-block of the tile)
 //               and offers (max, block) to its register top-(k-1) list.
 //               Scores never leave the SM.
@@ -36,8 +37,7 @@ namespace {
 using namespace sm100;
 
 constexpr int kRows = 128;     // query rows per tile = MMA M
-constexpr int kKeys = 128;     // keys per tile = MMA N
-constexpr int kStages = 4;     // k^I ring depth
+constexpr int kKeys = 256;     // keys per tile = MMA N
 constexpr int kMaxGpc = 2;     // groups per work item
 constexpr int kEpiWarps = 4 * kMaxGpc;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
@@ -51,9 +51,12 @@ struct SelectLayout {
   static constexpr int B_CHUNK = kKeys * CH_B;
   static constexpr int A_BYTES = kMaxGpc * NCH * A_CHUNK;
   static constexpr int STAGE_BYTES = NCH * B_CHUNK;
+  static constexpr int STAGES_FIT = (200 * 1024 - A_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;  // k^I ring depth
   static constexpr int KSTEPS = CH_E / 16;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = 1024 + A_BYTES + kStages * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM = 1024 + A_BYTES + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(STAGES >= 2, "k^I ring needs two stages");
 };
 
 __device__ __forceinline__ bool next_item(int64_t& r, int64_t n_items, int64_t& j) {
@@ -68,10 +71,14 @@ __device__ __forceinline__ bool next_item(int64_t& r, int64_t n_items, int64_t& 
   }
 }
 
-// Key tiles a query tile needs: all 128-key tiles holding blocks before the
+// Key tiles a query tile needs: the 256-key tiles holding blocks before the
 // last row's local block (for Bk = 64 the second half of the query tile also
-// takes block 2qb).
-__device__ __forceinline__ int64_t key_tiles(int64_t qb, int Bk) { return Bk == 128 ? qb : qb + 1; }
+// takes block 2qb).  Keys past that (a local block, or past N: zero fill) are
+// scored but never offered.
+__device__ __forceinline__ int64_t key_tiles(int64_t qb, int Bk) {
+  const int64_t key_limit = qb * kRows + (Bk == 128 ? 0 : 64);
+  return (key_limit + kKeys - 1) / kKeys;
+}
 
 template <int DI, int CAP>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -82,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + L::A_BYTES;
+  constexpr int kStages = L::STAGES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * L::STAGE_BYTES);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -96,8 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 6);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int acc_cols = kMaxGpc * kKeys;  // columns per accumulator buffer
-  constexpr uint32_t tmem_cols = 2 * acc_cols;
+  constexpr uint32_t tmem_cols = 2 * kKeys;  // accumulator buffer b at columns kKeys * b
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -108,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(a_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), kEpiWarps);
+      mbar_init(acc_empty(b), 4);  // the four warps of the group that drains it
     }
     mbar_init(drain_bar, 1);
     fence_mbar_init();
@@ -174,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC = idesc_bf16_f32(kRows, kKeys);
-      uint32_t kt_glob = 0, a_glob = 0, acc_glob = 0;
+      uint32_t kt_glob = 0, a_glob = 0;
+      uint32_t uses0 = 0, uses1 = 0;  // fills of accumulator buffers 0 and 1 so far
       int64_t r = 0, j;
       bool ok = true;
       while (ok && next_item(r, n_items, j)) {
@@ -183,14 +191,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nkt == 0) continue;
         if (!(ok = mbar_wait(a_full, a_glob & 1, abort, st, 0x201))) break;
         tc_fence_after();
-        for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob, ++acc_glob) {
+        for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
           const int s = kt_glob % kStages;
           if (!(ok = mbar_wait(full_bar(s), (kt_glob / kStages) & 1, abort, st, 0x202))) break;
-          const int buf = acc_glob & 1;
-          if (!(ok = mbar_wait(acc_empty(buf), ((acc_glob >> 1) & 1) ^ 1, abort, st, 0x203))) break;
-          tc_fence_after();
-          for (int gi = 0; gi < gpc; ++gi) {
-            const uint32_t d = tmem + (uint32_t)(buf * acc_cols + gi * kKeys);
+          for (int gi = 0; gi < gpc && ok; ++gi) {
+            const int buf = gpc == 2 ? gi : (int)(kt_glob & 1);
+            const uint32_t use = buf ? uses1 : uses0;
+            if (!(ok = mbar_wait(acc_empty(buf), (use & 1) ^ 1, abort, st, 0x203))) break;
+            tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)(buf * kKeys);
 #pragma unroll
             for (int c = 0; c < L::NCH; ++c)
 #pragma unroll
@@ -200,9 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_desc_kmajor(smem_u32(sB + s * L::STAGE_BYTES + c * L::B_CHUNK + kk * 32), L::CH_B);
                 mma_bf16_ss(d, ad, bd, IDESC, (c | kk) != 0);
               }
+            umma_commit(acc_full(buf));
+            if (buf) ++uses1; else ++uses0;
           }
+          if (!ok) break;
           umma_commit(empty_bar(s));
-          umma_commit(acc_full(buf));
         }
         if (!ok) break;
         umma_commit(a_empty);
@@ -217,12 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int quarter = warp & 3;          // TMEM lanes 32*quarter .. +31
     const int gi = (warp - 2) >> 2;        // the group (of the item's pair) this warp reduces
-    const bool has = gi < gpc;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    uint32_t acc_glob = 0;
+    uint32_t kt_glob = 0;
+    uint32_t uses0 = 0, uses1 = 0;
     int64_t r = 0, j;
-    bool ok = true;
+    bool ok = gi < gpc;  // with one group per item, the second group's warps have nothing to do
     TopK<CAP> top;
     while (ok && next_item(r, n_items, j)) {
       const int64_t qb = n_qt - 1 - j / n_gq;
@@ -231,43 +242,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t t = qb * kRows + row;
       const int64_t local = t / Bk;
       top.init(k - 1);
-      for (int64_t kt = 0; kt < nkt; ++kt, ++acc_glob) {
-        const int buf = acc_glob & 1;
-        if (!(ok = mbar_wait(acc_full(buf), (acc_glob >> 1) & 1, abort, st, 0x301))) break;
+      for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
+        const int buf = gpc == 2 ? gi : (int)(kt_glob & 1);
+        const uint32_t use = buf ? uses1 : uses0;
+        if (!(ok = mbar_wait(acc_full(buf), use & 1, abort, st, 0x301))) break;
+        if (buf) ++uses1; else ++uses0;
         tc_fence_after();
-        float m0 = __int_as_float(0xff800000), m1 = m0;  // maxima of columns 0..63 and 64..127
-        if (has) {
-          const uint32_t col = tmem + lane_base + (uint32_t)(buf * acc_cols + gi * kKeys);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t x[32], y[32];
-            tmem_ld_x32(col + 64 * h, x);
-            tmem_ld_x32(col + 64 * h + 32, y);
-            tmem_ld_wait();
-            float m = __int_as_float(0xff800000);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) m = max3(m, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
-            if (h == 0) m0 = m; else m1 = m;
+        // the tile's four 64-key quarters in turn; a block's maximum is offered
+        // as soon as its quarters are done (Bk = 128: two, Bk = 64: one)
+        const uint32_t col = tmem + lane_base + (uint32_t)(buf * kKeys);
+        float mb = __int_as_float(0xff800000);
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+          uint32_t x[32], y[32];
+          tmem_ld_x32(col + 64 * h, x);
+          tmem_ld_x32(col + 64 * h + 32, y);
+          tmem_ld_wait();
+          if (h == 3) {  // the whole tile is in registers or reduced: release TMEM
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(buf));
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(acc_empty(buf));  // the maxima are in registers: release TMEM
-        if (has) {
-          if (Bk == kKeys) {
-            const int b = (int)kt;
-            if (b < local) top.insert(fmaxf(m0, m1), b);
-          } else {  // two 64-token blocks per key tile
-            const int b = (int)(2 * kt);
-            if (b < local) top.insert(m0, b);
-            if (b + 1 < local) top.insert(m1, b + 1);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) mb = max3(mb, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) mb = max3(mb, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+          if (Bk == 64 || (h & 1)) {
+            const int b = Bk == 128 ? (int)(2 * kt) + (h >> 1) : (int)(4 * kt) + h;
+            if (b < local) top.insert(mb, b);
+            mb = __int_as_float(0xff800000);
           }
         }
       }
       if (!ok) break;
-      if (has && t < N) {
+      if (t < N) {
         int32_t* out = block_idx + ((int64_t)(gq * gpc + gi) * N + t) * k;
         out[0] = (int32_t)local;
         if (k > 1) top.emit(k - 1, out + 1);
