@@ -9,7 +9,8 @@
 // 128 MMA rows are (position pp, head slot hh) -> row 8 pp + hh; head slots
 // hh >= gs are padding (never loaded, never stored).  Per tile:
 //   S = Q K_b^T (128 x Bk fp32 in TMEM), causal mask j <= t, row max m and
-//   P = 2^(s log2e / sqrt(d) - m) (bf16, written back over S's TMEM columns),
+//   P = 2^(s log2e / sqrt(d) - m) (bf16, each half of the keys written back
+//   over the first columns of that half of S),
 //   O = P V_b (128 x d fp32 in TMEM, P read from TMEM as the A operand); the
 //   row's un-normalised O goes out in bf16 and its (m, l = sum P) in fp32, so
 //   the combine divides once per (t, h) by the merged sum.
@@ -18,18 +19,19 @@
 //                 from the schedule into an 8-slot shared ring;
 //   warp 0        Q loader: gathers a tile's Q rows with one TMA box per
 //                 position (8 heads x d, as d/64 swizzled 1 KB atoms) into one
-//                 of four position-major, 128B-swizzled K-major Q buffers;
-//   warp 1        TMEM owner; lane 0 issues tcgen05.mma.  S/P has three TMEM
-//                 buffers and O one, so S runs up to two tiles ahead of P V:
-//                 per tile i it issues every S(j), j <= i+2, of i's K/V block,
-//                 then PV(i);
+//                 of three position-major, 128B-swizzled K-major Q buffers;
+//   warp 1        TMEM owner; lane 0 issues tcgen05.mma.  S/P and O have two
+//                 TMEM buffers each, so S runs one tile ahead of P V and the
+//                 epilogue drains O(i-1) while PV(i) runs: per tile i it issues
+//                 S(i+1) if it uses i's K/V block, then PV(i);
 //   warp 2        K/V loader: one TMA load of K_b and V_b per run of tiles of
 //                 the same block, released after the run's last P V;
-//   warps 4..11   two softmax warpgroups (tiles of each parity);
+//   warps 4..11   two softmax warpgroups, both on every tile: each takes one
+//                 half of the key columns and writes its P over that half;
 //   warps 12..15  epilogue warpgroup: O -> bf16 in a swizzled shared tile of
 //                 the same layout, written out by TMA stores (one box per
 //                 position when gs = 8, one per 64 dims otherwise).
-// Buffer reuse needs no extra waits: S(j) is issued after PV(j-3) (tensor
+// Buffer reuse needs no extra waits: S(j) is issued after PV(j-2) (tensor
 // core operations run in issue order), and each barrier phase a role waits
 // for cannot be overtaken by the next one (the next use of a buffer depends,
 // through the issue order, on the consumer having passed it).  K_b, Q feed
@@ -48,8 +50,9 @@ using namespace sm100;
 
 constexpr int kRowsT = 128;   // MMA rows per tile
 constexpr int kPosT = 16;     // query positions per tile
-constexpr int kQBufs = 4;     // Q buffers in shared memory
-constexpr int kSBufs = 3;     // S/P buffers in TMEM
+constexpr int kQBufs = 3;     // Q buffers in shared memory
+constexpr int kSBufs = 2;     // S/P buffers in TMEM (one per softmax warpgroup)
+constexpr int kOBufs = 2;     // O buffers in TMEM
 constexpr int kMeta = 8;      // tile metadata slots
 constexpr int kWarpLoad = 0;
 constexpr int kWarpMma = 1;
@@ -60,8 +63,8 @@ constexpr int kWarpEpi0 = 12;
 constexpr int kThreadsT = 16 * 32;
 constexpr int kSoftWarps = 4;  // per warpgroup
 constexpr int kEpiWarps = 4;
-// Q loader, K/V loader, MMA issuer, one softmax warpgroup, epilogue store issuer
-constexpr int kMetaReaders = 1 + 1 + 1 + kSoftWarps + 1;
+// Q loader, K/V loader, MMA issuer, the eight softmax warps, epilogue store issuer
+constexpr int kMetaReaders = 1 + 1 + 1 + 2 * kSoftWarps + 1;
 static_assert(kPosT == kTilePositions, "tile records hold 16 positions");
 
 // Q and O tiles in shared memory are position-major: position pp holds its
@@ -80,8 +83,8 @@ struct AttnLayout {
   static constexpr int OFF_STG = OFF_V + K_BYTES;   // bf16 O of one tile, same layout as Q
   static constexpr int OFF_BAR = OFF_STG + Q_BYTES;
   static constexpr int SMEM = 1024 + OFF_BAR + 512;
-  // TMEM: S/P buffer j at 128 j (j < 3), O at 384
-  static constexpr uint32_t TMEM_O = 384;
+  // TMEM: S/P buffer j at 128 j, O buffer j at 256 + 128 j
+  static constexpr uint32_t TMEM_O = 256;
   static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -140,6 +143,18 @@ __device__ __forceinline__ bool epi_bar_and(bool v) {
   return r != 0;
 }
 
+// Named barrier of the two softmax warpgroups (id 2), plain and ANDing a flag.
+__device__ __forceinline__ void soft_bar_sync() { asm volatile("bar.sync 2, %0;\n" ::"n"(2 * kSoftWarps * 32) : "memory"); }
+__device__ __forceinline__ bool soft_bar_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 2, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(2 * kSoftWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
@@ -176,6 +191,17 @@ __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the
+// same one).  512 threads launch with 128 registers each; the budgets after
+// the split add up to the same 65536: producers 64, softmax 2 x 168, epilogue 112.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
+constexpr uint32_t kRegsProducers = 64, kRegsSoftmax = 168, kRegsEpilogue = 112;
+static_assert(4 * 32 * kRegsProducers + 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsEpilogue == 512 * 128,
+              "register split must add up to the launch's registers");
+
 // Packed pairs of fp32 (one 64-bit register): two lanes per instruction.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   uint64_t r;
@@ -209,15 +235,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ TileRecord meta[kMeta];
+  __shared__ float ex_m[2][kRowsT], ex_l[2][kRowsT];  // softmax halves: row maxima and partial sums
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
   auto q_full = [&](int i) { return bar0 + 8u * (0 + i); };
   auto q_empty = [&](int i) { return bar0 + 8u * (4 + i); };
   auto s_full = [&](int i) { return bar0 + 8u * (8 + i); };
-  auto p_full = [&](int i) { return bar0 + 8u * (11 + i); };
-  const uint32_t o_full = bar0 + 8u * 14;
-  const uint32_t o_empty = bar0 + 8u * 15;
+  auto p_full = [&](int i) { return bar0 + 8u * (10 + i); };
+  auto o_full = [&](int i) { return bar0 + 8u * (12 + i); };
+  auto o_empty = [&](int i) { return bar0 + 8u * (14 + i); };
   const uint32_t kv_full = bar0 + 8u * 16;
   const uint32_t kv_empty = bar0 + 8u * 17;
   const uint32_t drain_bar = bar0 + 8u * 18;
@@ -237,10 +264,12 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     }
     for (int i = 0; i < kSBufs; ++i) {
       mbar_init(s_full(i), 1);
-      mbar_init(p_full(i), kSoftWarps);
+      mbar_init(p_full(i), 2 * kSoftWarps);
     }
-    mbar_init(o_full, 1);
-    mbar_init(o_empty, kEpiWarps);
+    for (int i = 0; i < kOBufs; ++i) {
+      mbar_init(o_full(i), 1);
+      mbar_init(o_empty(i), kEpiWarps);
+    }
     mbar_init(kv_full, 1);
     mbar_init(kv_empty, 1);
     mbar_init(drain_bar, 1);
@@ -271,6 +300,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const int64_t t_begin = total * blockIdx.x / gridDim.x;
   const int n = (int)(total * (blockIdx.x + 1) / gridDim.x - t_begin);
 
+  if (warp < kWarpSoft0) {
+  regs_dec<kRegsProducers>();  // warps 0..3: the producers' warpgroup
   if (warp == kWarpMeta) {
     // ------------------------------------------------------------ tile records -> shared ring
     if (lane == 0) {
@@ -377,7 +408,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           gb_staged = gb_j;
         }
         tc_fence_after();
-        // buffer j % 3 last held P(j-3), whose P V was issued before this S
+        // buffer j % 2 last held P(j-2), whose P V was issued before this S
         const uint32_t d = tmem + (uint32_t)((j % kSBufs) * 128);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -393,8 +424,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       };
       for (int i = 0; i < n && ok; ++i) {
         if (!(ok = gb_of(i, gb_cur))) break;
-        // S ahead: every tile j <= i+2 of tile i's K/V block
-        while (ok && s_next < n && s_next <= i + 2 && gb_s_next == gb_cur) {
+        // S ahead: tile i+1 if it uses tile i's K/V block
+        while (ok && s_next < n && s_next <= i + 1 && gb_s_next == gb_cur) {
           ok = issue_S(s_next, gb_s_next);
           ++s_next;
           if (ok && s_next < n) ok = gb_of(s_next, gb_s_next);
@@ -403,15 +434,20 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         // PV(i)
         const int sb = i % kSBufs;
         if (!(ok = mbar_wait(p_full(sb), (i / kSBufs) & 1, abort, st, 0x503))) break;
-        if (!(ok = mbar_wait(o_empty, (i & 1) ^ 1, abort, st, 0x504))) break;
+        const int ob = i % kOBufs;
+        if (!(ok = mbar_wait(o_empty(ob), ((i / kOBufs) & 1) ^ 1, abort, st, 0x504))) break;
         tc_fence_after();
         const uint32_t pcol = tmem + (uint32_t)(sb * 128);
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks) {
+          // keys 16ks.. of half h = 16ks / (BK/2) sit packed at column h*BK/2 + (16ks - h*BK/2)/2
+          constexpr int HW = BK / 2;
+          const int h = (16 * ks) / HW;
+          const uint32_t acol = pcol + (uint32_t)(h * HW + (16 * ks - h * HW) / 2);
           const uint64_t bd = umma_desc_mnmajor_sw128(sbase + L::OFF_V + ks * 16 * 128, L::KV_CHUNK);
-          mma_bf16_ts(tmem + L::TMEM_O, pcol + 8 * ks, bd, IDESC_PV, ks > 0);
+          mma_bf16_ts(tmem + L::TMEM_O + (uint32_t)(ob * 128), acol, bd, IDESC_PV, ks > 0);
         }
-        umma_commit(o_full);
+        umma_commit(o_full(ob));
         mbar_arrive(meta_empty(i % kMeta));
         const bool last_of_block = (i + 1 == n) || (s_next > i + 1 ? false : gb_s_next != gb_cur);
         if (last_of_block) umma_commit(kv_empty);
@@ -421,99 +457,112 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         mbar_wait(drain_bar, 0, nullptr, st, 0x5F1);
       }
     }
-  } else if (warp >= kWarpSoft0 && warp < kWarpEpi0) {
-    // ------------------------------------------------------------ softmax warpgroup `par`
-    const int par = (warp - kWarpSoft0) / kSoftWarps;  // tiles of this parity
+  }
+  } else if (warp < kWarpEpi0) {
+    regs_inc<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax: both warpgroups on every tile
+    // Warpgroup `half` owns key columns [half*HW, half*HW + HW) of every row
+    // and writes its P (bf16, packed) over the first HW/2 of those columns.
+    // The two halves exchange row maxima and partial sums through shared
+    // memory at a named barrier of the eight warps.
+    constexpr int HW = BK / 2;
+    const int half = (warp - kWarpSoft0) / kSoftWarps;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int pos = row >> 3, hh = row & 7;
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-    bool ok = true;
-    for (int j = par; j < n && ok; j += 2) {
+    for (int j = 0; j < n; ++j) {
       const int ms_ = j % kMeta;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(meta_full(ms_), (j / kMeta) & 1, abort, st, 0x600)))) break;
-      const int64_t t = (hh < gs && pos < meta[ms_].count) ? meta[ms_].t[pos] : -1;
+      const bool w1 = mbar_wait(meta_full(ms_), (j / kMeta) & 1, abort, st, 0x600);
+      const int64_t t = (w1 && hh < gs && pos < meta[ms_].count) ? meta[ms_].t[pos] : -1;
       const int slot = meta[ms_].slot[pos];
       const int tg = meta[ms_].g;
       const int64_t tb = meta[ms_].b;
       __syncwarp();
-      if (lane == 0) mbar_arrive(meta_empty(ms_));
+      if (lane == 0 && w1) mbar_arrive(meta_empty(ms_));
       const int sb = j % kSBufs;
-      const uint32_t scol = tmem + lane_base + (uint32_t)(sb * 128);
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full(sb), (j / kSBufs) & 1, abort, st, 0x601)))) break;
+      const uint32_t scol = tmem + lane_base + (uint32_t)(sb * 128 + half * HW);
+      // Everything that does not need S is settled before waiting for it: the
+      // row's partial (m, l) slot, and the last visible column of this half
+      // (rows without output count as unmasked so that a warp takes the
+      // masked path only where a real row needs it; TMEM loads are
+      // warp-collective).
+      const int64_t prow = t >= 0 ? ((t - T0) * k + slot) * H_q + (int64_t)tg * gs + hh : 0;
+      const int64_t key0 = tb * BK + half * HW;
+      const int lim = t < 0 ? HW - 1 : (int)max((int64_t)-1, min((int64_t)HW - 1, t - key0));
+      const bool full = __all_sync(0xffffffffu, lim == HW - 1);
+      const bool w2 = w1 && mbar_wait(s_full(sb), (j / kSBufs) & 1, abort, st, 0x601);
+      // all eight warps leave together (the exchanges below are named barriers)
+      if (!soft_bar_and(w2)) break;
       tc_fence_after();
-      // Last visible column of the row; rows without output count as unmasked
-      // so that a warp takes the masked path only where a real row needs it
-      // (TMEM loads are warp-collective).
-      const int64_t key0 = tb * BK;
-      const int lim = t < 0 ? BK - 1 : (int)max((int64_t)-1, min((int64_t)BK - 1, t - key0));
-      const bool full = __all_sync(0xffffffffu, lim == BK - 1);
       float m = __int_as_float(0xff800000);
-      uint64_t lsum2 = 0;  // two fp32 zeros
+      uint32_t x[HW / 32][32];
       if (full) {
 #pragma unroll
-        for (int c = 0; c < BK / 32; c += 2) {
-          uint32_t x[32], y[32];
-          tmem_ld_x32(scol + c * 32, x);
-          tmem_ld_x32(scol + c * 32 + 32, y);
+        for (int c = 0; c < HW / 32; ++c) tmem_ld_x32(scol + c * 32, x[c]);
+        tmem_ld_wait();
+        float mc[HW / 32];
+#pragma unroll
+        for (int c = 0; c < HW / 32; ++c) {
+          mc[c] = __int_as_float(0xff800000);
+#pragma unroll
+          for (int e2 = 0; e2 < 32; e2 += 2) mc[c] = max3(mc[c], __uint_as_float(x[c][e2]), __uint_as_float(x[c][e2 + 1]));
+        }
+#pragma unroll
+        for (int c = 0; c < HW / 32; ++c) m = fmaxf(m, mc[c]);
+      } else {
+        // diagonal tiles (and rows of blocks past t): masked, one chunk at a time
+#pragma unroll 1
+        for (int c = 0; c < HW / 32; ++c) {
+          uint32_t y[32];
+          tmem_ld_x32(scol + c * 32, y);
           tmem_ld_wait();
 #pragma unroll
-          for (int e2 = 0; e2 < 32; e2 += 2) {
-            m = max3(m, __uint_as_float(x[e2]), __uint_as_float(x[e2 + 1]));
-            m = max3(m, __uint_as_float(y[e2]), __uint_as_float(y[e2 + 1]));
-          }
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e <= lim) m = fmaxf(m, __uint_as_float(y[e]));
         }
-        const float ms = m * scale_log2;
+      }
+      ex_m[half][row] = m;
+      soft_bar_sync();
+      m = fmaxf(ex_m[0][row], ex_m[1][row]);
+      const bool none = m == __int_as_float(0xff800000);
+      const float ms = none ? 0.f : m * scale_log2;
+      uint64_t lsum2 = 0;  // two fp32 zeros
+      if (full) {
         const uint64_t nms2 = f2_pack(-ms, -ms);
 #pragma unroll
-        for (int c = 0; c < BK / 32; c += 2) {
-          uint32_t x[32], y[32];
-          tmem_ld_x32(scol + c * 32, x);
-          tmem_ld_x32(scol + c * 32 + 32, y);
-          tmem_ld_wait();
-          uint32_t px[16], py[16];
+        for (int c = 0; c < HW / 32; ++c) {
+          uint32_t px[16];
 #pragma unroll
-          for (int e2 = 0; e2 < 32; e2 += 2) {
+          for (int e2 = 0; e2 < 32; e2 += 4) {
             float a0, a1, b0, b1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[e2]), __uint_as_float(x[e2 + 1])), scale2, nms2), a0, a1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(y[e2]), __uint_as_float(y[e2 + 1])), scale2, nms2), b0, b1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c][e2]), __uint_as_float(x[c][e2 + 1])), scale2, nms2), a0,
+                      a1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c][e2 + 2]), __uint_as_float(x[c][e2 + 3])), scale2, nms2),
+                      b0, b1);
             a0 = ex2_approx(a0);
             a1 = ex2_approx(a1);
             b0 = ex2_approx(b0);
             b1 = ex2_approx(b1);
             lsum2 = f2_add(lsum2, f2_add(f2_pack(a0, a1), f2_pack(b0, b1)));
             px[e2 >> 1] = pack_bf16x2(a0, a1);
-            py[e2 >> 1] = pack_bf16x2(b0, b1);
+            px[(e2 >> 1) + 1] = pack_bf16x2(b0, b1);
           }
-          tmem_st_x16(scol + c * 16, px);  // keys 32c..32c+31 -> packed columns 16c..16c+15
-          tmem_st_x16(scol + c * 16 + 16, py);
+          tmem_st_x16(scol + c * 16, px);  // keys 32c..32c+31 of the half -> packed columns 16c..16c+15
         }
-        m = ms;
       } else {
-        // diagonal tiles (and rows of blocks past t): one 32-column chunk at a time
 #pragma unroll 1
-        for (int c = 0; c < BK / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld_x32(scol + c * 32, x);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= lim) m = fmaxf(m, __uint_as_float(x[e]));
-        }
-        const bool none = m == __int_as_float(0xff800000);
-        const float ms = none ? 0.f : m * scale_log2;
-#pragma unroll 1
-        for (int c = 0; c < BK / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld_x32(scol + c * 32, x);
+        for (int c = 0; c < HW / 32; ++c) {
+          uint32_t y[32];
+          tmem_ld_x32(scol + c * 32, y);
           tmem_ld_wait();
           uint32_t px[16];
           float l = 0.f;
 #pragma unroll
           for (int e2 = 0; e2 < 32; e2 += 2) {
-            float a0 = ex2_approx(fmaf(__uint_as_float(x[e2]), scale_log2, -ms));
-            float a1 = ex2_approx(fmaf(__uint_as_float(x[e2 + 1]), scale_log2, -ms));
+            float a0 = ex2_approx(fmaf(__uint_as_float(y[e2]), scale_log2, -ms));
+            float a1 = ex2_approx(fmaf(__uint_as_float(y[e2 + 1]), scale_log2, -ms));
             a0 = c * 32 + e2 <= lim ? a0 : 0.f;
             a1 = c * 32 + e2 + 1 <= lim ? a1 : 0.f;
             l += a0 + a1;
@@ -522,21 +571,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
           lsum2 = f2_add(lsum2, f2_pack(l, 0.f));
           tmem_st_x16(scol + c * 16, px);
         }
-        m = none ? __int_as_float(0xff800000) : ms;
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(sb));
+      float l0, l1;
+      f2_unpack(lsum2, l0, l1);
+      ex_l[half][row] = l0 + l1;
+      soft_bar_sync();
       // (m, l) of the row for the combine; m = -inf marks a row without keys
-      if (t >= 0) {
-        float l0, l1;
-        f2_unpack(lsum2, l0, l1);
-        const int64_t prow = ((t - T0) * k + slot) * H_q + (int64_t)tg * gs + hh;
-        part_ml[prow] = make_float2(m, l0 + l1);
-      }
+      if (half == 0 && t >= 0)
+        part_ml[prow] = make_float2(none ? __int_as_float(0xff800000) : ms, ex_l[0][row] + ex_l[1][row]);
     }
-  } else if (warp >= kWarpEpi0) {
+  } else {
+    regs_dec<kRegsEpilogue>();
     // ------------------------------------------------------------ epilogue warpgroup
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -546,7 +595,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t my_row = stg + (row >> 3) * L::POS_BYTES + (row & 7) * 128;
     bool lead_ok = true;  // the store issuer's own waits
     for (int i = 0; i < n; ++i) {
-      const bool w = mbar_wait(o_full, i & 1, abort, st, 0x701);
+      const int ob = i % kOBufs;
+      const bool w = mbar_wait(o_full(ob), (i / kOBufs) & 1, abort, st, 0x701);
       // the staging tile is free once the previous tile's stores have read it
       if (leader) bulk_wait_read_all();
       // all four warps leave together (the named barriers have no time limit)
@@ -555,13 +605,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 #pragma unroll
       for (int c = 0; c < L::NCD; ++c) {
         uint32_t x[2][32];
-        tmem_ld_x32(ocol + c * 64, x[0]);
-        tmem_ld_x32(ocol + c * 64 + 32, x[1]);
+        tmem_ld_x32(ocol + (uint32_t)(ob * 128) + c * 64, x[0]);
+        tmem_ld_x32(ocol + (uint32_t)(ob * 128) + c * 64 + 32, x[1]);
         tmem_ld_wait();
         if (c == L::NCD - 1) {  // the whole row has left TMEM: hand O back to the tensor core
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(o_empty);
+          if (lane == 0) mbar_arrive(o_empty(ob));
         }
         // columns 64c + 8jj .. +7 -> 16-byte unit jj of the row, 128B-swizzled
 #pragma unroll
