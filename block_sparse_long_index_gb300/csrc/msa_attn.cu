@@ -147,9 +147,12 @@ __global__ void __launch_bounds__(256) tile_records_kernel(const int32_t* __rest
 // p_j = 2^(s_j - m_s) (s_j in log2 units) and l_s = sum_j p_j; then
 // M = max m_s, w_s = 2^(m_s - M) / sum_s l_s 2^(m_s - M), out = sum_s w_s O_s,
 // lse = ln 2 (M + log2 sum_s l_s 2^(m_s - M)); no contribution gives out = 0,
-// lse = -inf.
+// lse = -inf.  128 threads with two loads in flight each was the fastest
+// shape measured for this HBM-bound pass.
+constexpr int kCombineThreads = 128;
+
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict__ block_idx,
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t* __restrict__ block_idx,
                                                       const uint16_t* __restrict__ part_o,
                                                       const float2* __restrict__ part_ml, int64_t N, int H_q, int G,
                                                       int gs, int k, int64_t nb, int64_t T0,
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const int32_t* __restrict_
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 4
+#pragma unroll 2
     for (int s = 0; s < k; ++s) {
       const float w = cw[s * H_q + h];
       if (w == 0.f) continue;
@@ -315,7 +318,7 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
       e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cs);
       if (e != cudaSuccess) return e;
     }
-    ck<<<(unsigned)(T1 - T0), 256, cs, s>>>(block_idx, sc.part_o, sc.part_ml, p.N, p.H_q, G, p.gs, p.k, p.nb, T0,
+    ck<<<(unsigned)(T1 - T0), kCombineThreads, cs, s>>>(block_idx, sc.part_o, sc.part_ml, p.N, p.H_q, G, p.gs, p.k, p.nb, T0,
                                             (uint16_t*)out, lse);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
