@@ -404,11 +404,32 @@ def main():
     sel_s, att_s = pre["sel_ms"] / 1000.0, pre["att_ms"] / 1000.0
     peak_t = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     sel_tf = flops_index / sel_s / 1e12
-    roofline = {"kernel": "msa_select_blocks (index scoring + pooling + top-k, one launch)", "bound": "tensor",
-                "achieved": sel_tf, "peak": peak_t, "unit": "TFLOP/s", "frac": sel_tf / peak_t,
-                "traffic": traffic_for("select_prefill_128k", "block_sparse_long_index_gb300/csrc/msa_select.cu"),
-                "algorithmic": "(N^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index,
-                "peak_source": "%s bf16_tflops_sustained" % peak_src}
+    roofline_select = {"kernel": "msa_select_blocks (index scoring + pooling + top-k, one launch)",
+                       "bound": "tensor", "achieved": sel_tf, "peak": peak_t, "unit": "TFLOP/s",
+                       "frac": sel_tf / peak_t,
+                       "traffic": traffic_for("select_prefill_128k",
+                                              "block_sparse_long_index_gb300/csrc/msa_select.cu"),
+                       "algorithmic": "(N^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index,
+                       "peak_source": "%s bf16_tflops_sustained" % peak_src}
+    # The attention call (inversion, schedule, KV-outer tiles, combine) is the larger share of the
+    # step and is bound by HBM: each (t, group, slot) entry gathers its gs query rows once and
+    # writes gs partial rows once; the combine reads the partials back; K/V of every (group, block)
+    # once; block_idx, out and lse once.
+    entries = cfg.N * cfg.G * cfg.k
+    row = cfg.gs * cfg.d * 2
+    attn_bytes = (entries * row * 3                      # Q gather, partial O write, partial O read
+                  + entries * cfg.gs * 8 * 2             # (m, l) per partial row, written and read
+                  + cfg.G * cfg.nb * cfg.Bk * cfg.d * 2 * 2  # K and V
+                  + cfg.G * cfg.N * cfg.k * 4 * 3        # block_idx read twice, B* entries written
+                  + cfg.N * cfg.H_q * (cfg.d * 2 + 4))   # out, lse
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    att_bw = attn_bytes / att_s / 1e9
+    roofline = {"kernel": "msa_sparse_attn_fwd (B->B*, schedule, KV-outer tcgen05 tiles, LSE combine)",
+                "bound": "hbm", "achieved": att_bw, "peak": hbm, "unit": "GB/s", "frac": att_bw / hbm,
+                "traffic": None,
+                "algorithmic": "N*G*k*gs*d*2*3 + N*G*k*gs*16 + G*nb*Bk*d*4 + G*N*k*12 + N*H_q*(2d+4)"
+                               " = %d bytes per call" % attn_bytes,
+                "peak_source": "%s hbm_gbs" % peak_src}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
             "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
@@ -417,6 +438,7 @@ def main():
             "clocks": pre["clocks"],
             "gpu_launches": prefill_launches(cfg) * K,
             "roofline": roofline,
+            "roofline_select": roofline_select,
             "stages_ms": {"select": pre["sel_ms"], "attend": pre["att_ms"]},
             "step_frac_of_tensor_peak": (flops_index + flops_main) / step_s / 1e12 / peak_t,
             "step_tflops": (flops_index + flops_main) / step_s / 1e12}
