@@ -597,35 +597,38 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     for (int i = 0; i < n; ++i) {
       const int ob = i % kOBufs;
       const bool w = mbar_wait(o_full(ob), (i / kOBufs) & 1, abort, st, 0x701);
-      // the staging tile is free once the previous tile's stores have read it
-      if (leader) bulk_wait_read_all();
       // all four warps leave together (the named barriers have no time limit)
       if (!epi_bar_and(w && lead_ok)) break;
       tc_fence_after();
+      // the whole row into registers as bf16 pairs, then O goes straight back to the tensor core
+      uint32_t pk[D / 2];
 #pragma unroll
       for (int c = 0; c < L::NCD; ++c) {
         uint32_t x[2][32];
         tmem_ld_x32(ocol + (uint32_t)(ob * 128) + c * 64, x[0]);
         tmem_ld_x32(ocol + (uint32_t)(ob * 128) + c * 64 + 32, x[1]);
         tmem_ld_wait();
-        if (c == L::NCD - 1) {  // the whole row has left TMEM: hand O back to the tensor core
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(o_empty(ob));
-        }
-        // columns 64c + 8jj .. +7 -> 16-byte unit jj of the row, 128B-swizzled
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          pk[c * 32 + e] = pack_bf16x2(__uint_as_float(x[e >> 4][(e & 15) * 2]),
+                                       __uint_as_float(x[e >> 4][(e & 15) * 2 + 1]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty(ob));
+      // the staging tile is free once the previous tile's stores have read it
+      if (leader) bulk_wait_read_all();
+      epi_bar_sync();
+      // 16-byte unit jj of 64-column chunk c -> its 128B-swizzled place in the row
+#pragma unroll
+      for (int c = 0; c < L::NCD; ++c)
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          const uint32_t* z = x[jj >> 2] + (jj & 3) * 8;
           const uint32_t a = my_row + c * 1024 + ((jj ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a),
-                       "r"(pack_bf16x2(__uint_as_float(z[0]), __uint_as_float(z[1]))),
-                       "r"(pack_bf16x2(__uint_as_float(z[2]), __uint_as_float(z[3]))),
-                       "r"(pack_bf16x2(__uint_as_float(z[4]), __uint_as_float(z[5]))),
-                       "r"(pack_bf16x2(__uint_as_float(z[6]), __uint_as_float(z[7])))
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(pk[c * 32 + jj * 4]),
+                       "r"(pk[c * 32 + jj * 4 + 1]), "r"(pk[c * 32 + jj * 4 + 2]), "r"(pk[c * 32 + jj * 4 + 3])
                        : "memory");
         }
-      }
       fence_proxy_async_smem();
       epi_bar_sync();
       if (leader) {
