@@ -201,6 +201,14 @@ __global__ void __launch_bounds__(1024) decode_merge_kernel(const float* __restr
 }
 
 // One CTA per (slot, group, sequence): 128 threads.
+// One CTA (4 warps) per (slot, group, sequence): the block's K/V rows are
+// staged in shared memory (16-byte chunk c of row j stored at chunk
+// c ^ (j mod d/8), so ldmatrix rows fall in distinct banks).  The group's
+// heads are the rows of m16n8k16 tensor-core tiles (rows >= gs are zero):
+// warp w scores keys [w BK/4, (w+1) BK/4), the softmax statistics are merged
+// across warps in shared memory, P stays in registers as the A operand of
+// P V (V read transposed by ldmatrix), and the warps' partial O are summed in
+// shared memory before the head's partial (O, lse) is written.
 template <int D, int BK>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __restrict__ q_t,
                                                           const uint16_t* __restrict__ k_cache,
@@ -209,14 +217,16 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ block_idx, int64_t ctx_max,
                                                           int H_q, int G, int k, float scale,
                                                           float* __restrict__ part_o, float* __restrict__ part_lse) {
-  // the block's K rows [BK][D] (16-byte chunk c of row j stored at chunk c ^ (j mod C8)), then its V rows
-  extern __shared__ __align__(16) uint16_t kv_s[];
-  __shared__ float qs[8][D];
-  __shared__ __align__(16) float ps[BK][8];  // scores, then probabilities, key-major
-  __shared__ float red[8][2];
-  constexpr int C8 = D / 8;  // 16-byte chunks per row
+  extern __shared__ __align__(16) uint16_t kv_s[];  // K rows [BK][D], then V rows [BK][D]
+  __shared__ float red_m[4][8], red_l[4][8];
+  constexpr int C8 = D / 8;     // 16-byte chunks per row
+  constexpr int KPW = BK / 4;   // keys per warp
+  constexpr int NT = KPW / 8;   // 8-key n-tiles per warp
+  constexpr int KS = D / 16;    // k-steps over d
+  static_assert(NT % 2 == 0, "two n-tiles per ldmatrix");
   const int slot = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row (head) and column pair
   const int gs = H_q / G;
   const int64_t len = ctx_len[seq];
   const int32_t b = block_idx[((int64_t)seq * G + g) * k + slot];
@@ -241,84 +251,109 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     const int j = i / C8, c8 = i % C8;
     const bool in = j < nvis;
     const int64_t off = (int64_t)(in ? j : 0) * kv_row + c8 * 8;
-    cp_async_16(Ks + j * D + (c8 ^ (j & (C8 - 1))) * 8, Kb + off, in ? 16 : 0);
-    cp_async_16(Vs + j * D + c8 * 8, Vb + off, in ? 16 : 0);
+    const int sw = (c8 ^ (j & (C8 - 1))) * 8;
+    cp_async_16(Ks + j * D + sw, Kb + off, in ? 16 : 0);
+    cp_async_16(Vs + j * D + sw, Vb + off, in ? 16 : 0);
   }
   cp_async_commit();
-  for (int i = tid; i < gs * D; i += blockDim.x) {
-    int hh = i / D, cc = i % D;
-    uint16_t w = q_t[((int64_t)seq * H_q + g * gs + hh) * D + cc];
-    qs[hh][cc] = __uint_as_float((uint32_t)w << 16);
+  // q as A fragments: row gq = head gq of the group (zero past gs), rows 8..15 zero
+  uint32_t qa[KS][2];
+  {
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q_t + ((int64_t)seq * H_q + g * gs + gq) * D);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = gq < gs ? qrow[(16 * ks + 2 * tq) >> 1] : 0u;
+      qa[ks][1] = gq < gs ? qrow[(16 * ks + 8 + 2 * tq) >> 1] : 0u;
+    }
   }
   cp_async_wait<0>();
   __syncthreads();
-  // scores: thread j owns key j; all lanes take the same chunk c8 (q is a
-  // broadcast), which the swizzle spreads over distinct banks of the K rows
-  for (int j = tid; j < BK; j += blockDim.x) {
-    float sc[8];
+  // S = q K^T for this warp's keys
+  float sacc[NT][4];
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh) sc[hh] = 0.f;
-    if (j < nvis) {
-      const uint16_t* kr = Ks + j * D;
-#pragma unroll 4
-      for (int c8 = 0; c8 < C8; ++c8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(kr + (c8 ^ (j & (C8 - 1))) * 8);
-        const float kv[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                             bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+  for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
-        for (int hh = 0; hh < 8; ++hh) {
-          if (hh < gs) {
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) sc[hh] = fmaf(qs[hh][c8 * 8 + e], kv[e], sc[hh]);
-          }
-        }
-      }
+    for (int np = 0; np < NT; np += 2) {
+      // matrices: (n-tile np, dims +0..7), (np, +8..15), (np+1, +0..7), (np+1, +8..15)
+      const int key = warp * KPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
+      const int chunk = 2 * ks + ((lane >> 3) & 1);
+      uint32_t r0, r1, r2, r3;
+      ldmatrix_x4(r0, r1, r2, r3, Ks + key * D + ((chunk ^ (key & (C8 - 1))) * 8));
+      const uint32_t b0[2] = {r0, r1}, b1[2] = {r2, r3};
+      mma_bf16_16816(sacc[np], a, b0);
+      mma_bf16_16816(sacc[np + 1], a, b1);
     }
+  }
+  // scale, mask past nvis, row (head) maxima across the warp's keys and then across warps
+  float mx = __int_as_float(0xff800000);
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh)
-      if (hh < gs) ps[j][hh] = (j < nvis) ? sc[hh] * scale : __int_as_float(0xff800000);
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int j = warp * KPW + nt * 8 + 2 * tq + e;
+      const float v = j < nvis ? sacc[nt][e] * scale : __int_as_float(0xff800000);
+      sacc[nt][e] = v;
+      mx = fmaxf(mx, v);
+    }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  if (tq == 0) red_m[warp][gq] = mx;
+  __syncthreads();
+  const float m = fmaxf(fmaxf(red_m[0][gq], red_m[1][gq]), fmaxf(red_m[2][gq], red_m[3][gq]));
+  float ls = 0.f;
+  uint32_t pa[NT / 2][2];  // P as A fragments of the P V k-steps (16 keys each)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const float p0 = __expf(sacc[nt][0] - m), p1 = __expf(sacc[nt][1] - m);  // e^-inf = 0
+    ls += p0 + p1;
+    pa[nt >> 1][nt & 1] = pack_bf16x2(p0, p1);
+  }
+  ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+  ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+  if (tq == 0) red_l[warp][gq] = ls;
+  // O = P V over this warp's keys
+  float oacc[D / 8][4];
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
+#pragma unroll
+  for (int ks2 = 0; ks2 < NT / 2; ++ks2) {
+    const uint32_t a[4] = {pa[ks2][0], 0u, pa[ks2][1], 0u};
+#pragma unroll
+    for (int nd = 0; nd < D / 8; nd += 2) {
+      // transposed matrices: (keys +0..7, d n-tile nd), (keys +8..15, nd), (+0..7, nd+1), (+8..15, nd+1)
+      const int key = warp * KPW + 16 * ks2 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      const int chunk = nd + (lane >> 4);
+      uint32_t r0, r1, r2, r3;
+      ldmatrix_x4_trans(r0, r1, r2, r3, Vs + key * D + ((chunk ^ (key & (C8 - 1))) * 8));
+      const uint32_t b0[2] = {r0, r1}, b1[2] = {r2, r3};
+      mma_bf16_16816(oacc[nd], a, b0);
+      mma_bf16_16816(oacc[nd + 1], a, b1);
+    }
+  }
+  // sum the warps' partial O in shared memory (over the K rows, which are no longer read)
+  __syncthreads();
+  float* red_o = reinterpret_cast<float*>(kv_s);  // [4 warps][8 rows][D]
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) {
+    red_o[(warp * 8 + gq) * D + nd * 8 + 2 * tq] = oacc[nd][0];
+    red_o[(warp * 8 + gq) * D + nd * 8 + 2 * tq + 1] = oacc[nd][1];
   }
   __syncthreads();
-  // softmax statistics per head: warp w handles heads w, w+4
-  for (int hh = warp; hh < gs; hh += 4) {
-    float m = __int_as_float(0xff800000);
-    for (int j = lane; j < BK; j += 32) m = fmaxf(m, ps[j][hh]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float l = 0.f;
-    for (int j = lane; j < BK; j += 32) {
-      float p = __expf(ps[j][hh] - m);
-      ps[j][hh] = p;
-      l += p;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) {
-      red[hh][0] = m;
-      red[hh][1] = l;
-    }
+  for (int i = tid; i < gs * D; i += blockDim.x) {
+    const int hh = i / D, dc = i % D;
+    const float L = red_l[0][hh] + red_l[1][hh] + red_l[2][hh] + red_l[3][hh];
+    const float o = red_o[(0 * 8 + hh) * D + dc] + red_o[(1 * 8 + hh) * D + dc] + red_o[(2 * 8 + hh) * D + dc] +
+                    red_o[(3 * 8 + hh) * D + dc];
+    po[(int64_t)hh * k * D + dc] = o / L;
   }
-  __syncthreads();
-  // O = P V from shared memory: thread owns column cc
-  for (int cc = tid; cc < D; cc += blockDim.x) {
-    float o[8];
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh) o[hh] = 0.f;
-#pragma unroll 4
-    for (int j = 0; j < nvis; ++j) {
-      const float vj = __uint_as_float((uint32_t)Vs[j * D + cc] << 16);
-      const float4 p0 = *reinterpret_cast<const float4*>(&ps[j][0]);
-      const float4 p1 = *reinterpret_cast<const float4*>(&ps[j][4]);
-      const float pj[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-      for (int hh = 0; hh < 8; ++hh)
-        if (hh < gs) o[hh] = fmaf(pj[hh], vj, o[hh]);
-    }
-#pragma unroll
-    for (int hh = 0; hh < 8; ++hh)
-      if (hh < gs) po[(int64_t)hh * k * D + cc] = o[hh] / red[hh][1];
+  if (tid < gs) {
+    const float M = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]), fmaxf(red_m[2][tid], red_m[3][tid]));
+    const float L = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
+    pl[(int64_t)tid * k] = M + logf(L);
   }
-  if (tid < gs) pl[(int64_t)tid * k] = red[tid][0] + logf(red[tid][1]);
 }
 
 template <int D>
