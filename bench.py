@@ -463,7 +463,7 @@ def main():
                                        "algorithmic": "B*(ctx*d_I*2 + k*Bk*2*H_kv*d*2) = %d bytes per step"
                                                       % bytes_step,
                                        "peak_source": "%s hbm_gbs" % peak_src},
-                          "gpu_launches": 4 * dec["steps"]}
+                          "gpu_launches": 2 * dec["steps"]}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         dt, n, th = oracle_prefill_sample(cfg, args.cpu_rows)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",

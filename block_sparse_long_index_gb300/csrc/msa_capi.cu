@@ -119,11 +119,13 @@ msa_status_t check_shape(const msa_shape_t* s) {
   return MSA_OK;
 }
 
-msa_status_t begin(void* ws, size_t ws_bytes, size_t need, cudaStream_t s) {
+// Validates the workspace and clears its first `clear` bytes (the status header
+// and, for calls that keep completion counters there, those counters).
+msa_status_t begin(void* ws, size_t ws_bytes, size_t need, cudaStream_t s, size_t clear = kHeader) {
   if (!ws) return MSA_ERR_INVALID_ARGUMENT;
   if (((uintptr_t)ws & 255u) != 0) return MSA_ERR_INVALID_ARGUMENT;
   if (ws_bytes < need) return MSA_ERR_WORKSPACE_TOO_SMALL;
-  if (cudaMemsetAsync(ws, 0, kHeader, s) != cudaSuccess) return MSA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, clear, s) != cudaSuccess) return MSA_ERR_CUDA;
   return MSA_OK;
 }
 
@@ -221,10 +223,10 @@ msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_
       ((uintptr_t)block_idx & 3u))
     return MSA_ERR_INVALID_ARGUMENT;
   cudaStream_t s = (cudaStream_t)stream;
-  st = begin(workspace, workspace_bytes, msa_decode_workspace(B, shape), s);
-  if (st != MSA_OK) return st;
   msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,
                                        shape->k);
+  st = begin(workspace, workspace_bytes, msa_decode_workspace(B, shape), s, kHeader + msa::decode_clear_bytes(p));
+  if (st != MSA_OK) return st;
   return finish(msa::launch_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, p, scale, out, lse,
                                    block_idx, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
 }
@@ -251,7 +253,8 @@ msa_status_t msa_decode_noalloc(const void* q_t, const void* q_idx_t, const void
   void* scratch = nullptr;
   if (msa::noalloc_scratch(need, &scratch) != cudaSuccess || !scratch) return MSA_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemsetAsync(scratch, 0, kHeader, s) != cudaSuccess) return MSA_ERR_CUDA;  // the status word starts clear
+  // the status word and the completion counters start clear
+  if (cudaMemsetAsync(scratch, 0, kHeader + msa::decode_clear_bytes(p), s) != cudaSuccess) return MSA_ERR_CUDA;
   return finish(msa::launch_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, p, scale, out, lse,
                                    block_idx, (char*)scratch + kHeader, (msa::DeviceStatus*)scratch, s));
 }

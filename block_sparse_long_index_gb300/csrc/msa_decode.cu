@@ -5,17 +5,22 @@
 // (block scores -> max-pooling -> forced local block + top-k -> attention over
 // the selected blocks); "MSA" study note 2-3 for the equations.
 //
-//   1. scan:    split-K over the cache.  Each warp streams 16 index keys at a
-//               time straight from HBM into MMA A-fragments (16-byte loads,
-//               dims permuted consistently in the query fragments, so no
-//               shared-memory staging is needed) and scores all groups at once
-//               (16 keys x 8 groups x d_I per mma chain); block maxima feed a
-//               per-group top-(k-1) list per warp, merged per CTA.
-//   2. merge:   per (sequence, group) a tournament over the CTAs' candidate
-//               lists -> block set.
-//   3. attend:  per (sequence, group, slot) one CTA reads that block's K/V
-//               rows and produces each group head's partial (O, lse).
-//   4. combine: per (sequence, head) the partials are merged by their lse.
+// Two launches per step:
+//   1. scan (+ merge): split-K over the cache, two 8-warp CTAs per SM.  Each
+//      warp streams an equal share of 16-key chunks straight from HBM into
+//      mma.sync A fragments (16-byte loads, one chunk in flight ahead of the
+//      one being scored; dims permuted consistently in the query fragments, so
+//      no shared-memory staging is needed) and scores all groups at once
+//      (16 keys x 8 groups x d_I per mma chain).  Block maxima meet in shared
+//      memory (an atomic max on order-preserving integers joins the two parts
+//      of a block split between warps); each CTA then keeps its top-(k-1)
+//      blocks per group, and the last CTA of a sequence to finish merges the
+//      CTAs' lists into that sequence's block sets.
+//   2. attend (+ combine): per (sequence, group, slot) one CTA reads that
+//      block's K/V rows and produces each group head's partial (O, lse); the
+//      last CTA of a (sequence, group) merges the k partials by their lse.
+//      It is launched as a programmatic dependent of the scan, so its launch
+//      overlaps the scan's tail.
 #include <math.h>
 
 #include <mutex>
@@ -26,8 +31,11 @@ namespace msa {
 
 namespace {
 
-constexpr int kScanThreads = 256;  // 8 warps
-constexpr int kGroupsPerMma = 8;   // mma n = 8 groups
+constexpr int kScanThreads = 256;  // 8 warps, two CTAs per SM
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kGroupsPerMma = 8;    // mma n = 8 groups
+constexpr int kMergeListsPerLane = 16;  // last-CTA merge: splits <= 32 * 16
+constexpr int kMaxCtaBlocks = 2048;     // block maxima kept in shared memory per scan CTA
 
 // dims of fragment column kf (0..15) in k-step ks: see the load pattern below
 __device__ __forceinline__ int frag_dim(int ks, int kf) {
@@ -36,23 +44,47 @@ __device__ __forceinline__ int frag_dim(int ks, int kf) {
   return 32 * p + 8 * c + 4 * half + 2 * hi + e;
 }
 
-template <int DI, int BK, int CAP>
-__global__ void __launch_bounds__(kScanThreads) decode_scan_kernel(
+// fp32 -> unsigned with the same order (-0 folded to +0); 0 is below every value
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int DI>
+__device__ __forceinline__ void load_keys16(uint4 (&v)[DI / 32][2], const uint16_t* p) {
+#pragma unroll
+  for (int q = 0; q < DI / 32; ++q) {
+    v[q][0] = ldg_stream_16(p + 32 * q);
+    v[q][1] = ldg_stream_16(p + 8 * DI + 32 * q);
+  }
+}
+
+// Scan CTA (split, seq): candidate blocks [b_lo, b_hi) of sequence seq, where
+// the candidates are the blocks before the query's local block.  The CTA's
+// 16-key chunks are divided evenly among its warps; a block whose chunks fall
+// to two warps gets its maximum from both through the shared-memory atomic.
+template <int DI, int BK>
+__global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     const uint16_t* __restrict__ q_idx_t, const uint16_t* __restrict__ k_idx_cache,
-    const int32_t* __restrict__ ctx_len, int64_t ctx_max, int G, int k, int splits, float* __restrict__ cand_s,
-    int32_t* __restrict__ cand_b, DeviceStatus* st) {
+    const int32_t* __restrict__ ctx_len, int64_t ctx_max, int G, int k, int splits, uint64_t* __restrict__ cand,
+    unsigned int* __restrict__ tickets, int32_t* __restrict__ block_idx, DeviceStatus* st) {
   constexpr int KS = DI / 16;
-  __shared__ float sm_s[kScanThreads / 32][kGroupsPerMma][CAP];
-  __shared__ int32_t sm_b[kScanThreads / 32][kGroupsPerMma][CAP];
+  constexpr int CPB = BK / 16;  // chunks per block
+  extern __shared__ uint32_t bmax_s[];  // [blocks of this CTA][8 groups], ordered_bits of the block maxima
+  __shared__ int s_last;
+  griddep_launch_dependents();  // the attention grid may be scheduled once every scan CTA is resident
   const int seq = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, row = lane >> 2;
+  const int km1 = k - 1;
   const int64_t len = ctx_len[seq];
   const bool ok = len >= 1 && len <= ctx_max;
   if (!ok && split == 0 && tid == 0) raise_error(st, kErrBadIndex, 2u);
   const int64_t t = ok ? len - 1 : 0;
   const int64_t local = t / BK;  // candidates: blocks [0, local)
-  const int64_t b_lo = ok ? local * split / splits : 0, b_hi = ok ? local * (split + 1) / splits : 0;
+  const int64_t b_lo = local * split / splits, b_hi = local * (split + 1) / splits;
+  const int nblk = (int)(b_hi - b_lo);
+  for (int i = tid; i < nblk * kGroupsPerMma; i += kScanThreads) bmax_s[i] = 0u;
 
   // query fragments (B operand): column n = group, k rows follow frag_dim
   uint32_t qf[KS][2];
@@ -71,136 +103,118 @@ __global__ void __launch_bounds__(kScanThreads) decode_scan_kernel(
         qf[ks][r] = w;
       }
   }
+  __syncthreads();
 
-  TopK<CAP> top;
-  top.init(lane < G ? k - 1 : 0);
-  const uint16_t* cache = k_idx_cache + (int64_t)seq * ctx_max * DI;
-
-  for (int64_t b = b_lo + warp; b < b_hi; b += kScanThreads / 32) {
-    float bm0 = __int_as_float(0xff800000), bm1 = bm0;
-#pragma unroll 2
-    for (int it = 0; it < BK / 16; ++it) {
-      const int64_t key = b * BK + it * 16 + row;
-      const uint16_t* pa = cache + key * DI + 8 * c;
-      const uint16_t* pb = pa + 8 * DI;
-      uint4 va[DI / 32], vb[DI / 32];
+  // this warp's chunks [c0, c1) of the CTA's nblk * CPB
+  const int64_t nch = (int64_t)nblk * CPB;
+  const int64_t c0 = nch * warp / kScanWarps, c1 = nch * (warp + 1) / kScanWarps;
+  const uint16_t* base = k_idx_cache + ((int64_t)seq * ctx_max + b_lo * BK + row) * DI + 8 * c;
+  float bm0 = __int_as_float(0xff800000), bm1 = bm0;
+  auto score = [&](const uint4 (&v)[DI / 32][2], int64_t cc) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int p = 0; p < DI / 32; ++p) {
-        va[p] = ldg_stream_16(pa + 32 * p);
-        vb[p] = ldg_stream_16(pb + 32 * p);
-      }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int p = 0; p < DI / 32; ++p) {
-        uint32_t a0[4] = {va[p].x, vb[p].x, va[p].y, vb[p].y};  // k-step 2p: dims +0..3 of each 8
-        uint32_t a1[4] = {va[p].z, vb[p].z, va[p].w, vb[p].w};  // k-step 2p+1: dims +4..7
-        mma_bf16_16816(acc, a0, qf[2 * p]);
-        mma_bf16_16816(acc, a1, qf[2 * p + 1]);
-      }
-      bm0 = fmaxf(bm0, fmaxf(acc[0], acc[2]));  // group 2c, keys row and row+8
-      bm1 = fmaxf(bm1, fmaxf(acc[1], acc[3]));  // group 2c+1
+    for (int q = 0; q < DI / 32; ++q) {
+      const uint32_t a0[4] = {v[q][0].x, v[q][1].x, v[q][0].y, v[q][1].y};  // k-step 2q: dims +0..3 of each 8
+      const uint32_t a1[4] = {v[q][0].z, v[q][1].z, v[q][0].w, v[q][1].w};  // k-step 2q+1: dims +4..7
+      mma_bf16_16816(acc, a0, qf[2 * q]);
+      mma_bf16_16816(acc, a1, qf[2 * q + 1]);
     }
+    bm0 = fmaxf(bm0, fmaxf(acc[0], acc[2]));  // group 2c, keys row and row+8
+    bm1 = fmaxf(bm1, fmaxf(acc[1], acc[3]));  // group 2c+1
+    if ((cc % CPB) == CPB - 1 || cc == c1 - 1) {  // end of this warp's part of a block
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
-      bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
+      for (int o = 4; o < 32; o <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o));
+      }
+      // group g's maximum sits in lane g/2 (value g&1)
+      const float x0 = __shfl_sync(0xffffffffu, bm0, (lane & 7) >> 1);
+      const float x1 = __shfl_sync(0xffffffffu, bm1, (lane & 7) >> 1);
+      if (lane < G) atomicMax(&bmax_s[(int)(cc / CPB) * kGroupsPerMma + lane], ordered_bits((lane & 1) ? x1 : x0));
+      bm0 = bm1 = __int_as_float(0xff800000);
     }
-    // group g's maximum sits in lane g/2 (value g&1)
-    float x0 = __shfl_sync(0xffffffffu, bm0, (lane & 7) >> 1);
-    float x1 = __shfl_sync(0xffffffffu, bm1, (lane & 7) >> 1);
-    if (lane < G) top.insert((lane & 1) ? x1 : x0, (int)b);
-  }
-
-  // merge the warps' lists: lane g of warp 0 collects group g
-  if (lane < kGroupsPerMma) {
-    int32_t ids[CAP];
-    float scs[CAP];
-    int n = top.emit(CAP, ids, scs);
-    for (int i = 0; i < CAP; ++i) {
-      sm_s[warp][lane][i] = i < n ? scs[i] : __int_as_float(0xff800000);
-      sm_b[warp][lane][i] = i < n ? ids[i] : -1;
+  };
+  uint4 va[DI / 32][2], vb[DI / 32][2];
+  if (c0 < c1) load_keys16<DI>(va, base + c0 * 16 * DI);
+  for (int64_t ci = c0; ci < c1; ci += 2) {  // one chunk in flight ahead of the one being scored
+    if (ci + 1 < c1) load_keys16<DI>(vb, base + (ci + 1) * 16 * DI);
+    score(va, ci);
+    if (ci + 1 < c1) {
+      if (ci + 2 < c1) load_keys16<DI>(va, base + (ci + 2) * 16 * DI);
+      score(vb, ci + 1);
     }
   }
   __syncthreads();
-  if (warp == 0 && lane < G) {
-    TopK<CAP> m;
-    m.init(k - 1);
-    for (int w = 0; w < kScanThreads / 32; ++w)
-      for (int i = 0; i < CAP; ++i)
-        if (sm_b[w][lane][i] >= 0) m.insert(sm_s[w][lane][i], sm_b[w][lane][i]);
-    int32_t ids[CAP];
-    float scs[CAP];
-    int n = m.emit(CAP, ids, scs);
-    const int64_t base = (((int64_t)seq * splits + split) * G + lane) * CAP;
-    for (int i = 0; i < CAP; ++i) {
-      cand_s[base + i] = i < n ? scs[i] : __int_as_float(0xff800000);
-      cand_b[base + i] = i < n ? ids[i] : -1;
-    }
-  }
-}
 
-// One CTA per (sequence, group): a tournament over the scan CTAs' candidate
-// lists (each sorted best-first).  Thread i holds the head of list i (and of
-// lists i + blockDim, ...); each of the k-1 rounds takes the best head in the
-// CTA (larger score, then smaller block id) and advances the winner's list.
-template <int CAP>
-__global__ void __launch_bounds__(1024) decode_merge_kernel(const float* __restrict__ cand_s,
-                                                            const int32_t* __restrict__ cand_b,
-                                                            const int32_t* __restrict__ ctx_len, int64_t ctx_max,
-                                                            int Bk, int G, int k, int splits,
-                                                            int32_t* __restrict__ block_idx) {
-  __shared__ uint64_t warp_best[32];
-  const int seq = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const int64_t len = ctx_len[seq];
-  int32_t* out = block_idx + ((int64_t)seq * G + g) * k;
-  if (len < 1 || len > ctx_max) {
-    for (int i = tid; i < k; i += blockDim.x) out[i] = -1;
-    return;
-  }
-  // this thread's lists: tid, tid + blockDim, ...; pos[] = next unread entry of each
-  auto list_base = [&](int sp) { return (((int64_t)seq * splits + sp) * G + g) * CAP; };
-  auto head_key = [&](int sp, int p) -> uint64_t {
-    if (p >= CAP) return 0;
-    const int32_t b = cand_b[list_base(sp) + p];
-    return b < 0 ? 0 : rank_key(cand_s[list_base(sp) + p], b);
-  };
-  constexpr int kMaxLists = 4;  // lists per thread (splits <= 4 * 1024)
-  int pos[kMaxLists];
-  uint64_t key[kMaxLists];
-#pragma unroll
-  for (int i = 0; i < kMaxLists; ++i) {
-    const int sp = tid + i * blockDim.x;
-    pos[i] = 0;
-    key[i] = sp < splits ? head_key(sp, 0) : 0;
-  }
-  if (tid == 0) out[0] = (int32_t)((len - 1) / Bk);
-  for (int r = 0; r < k - 1; ++r) {
-    uint64_t best = 0;
-#pragma unroll
-    for (int i = 0; i < kMaxLists; ++i) best = key[i] > best ? key[i] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    if (lane == 0) warp_best[warp] = best;
-    __syncthreads();
-    uint64_t all = 0;
-    for (int w = 0; w < nwarps; ++w) all = warp_best[w] > all ? warp_best[w] : all;
-    __syncthreads();  // warp_best is rewritten next round
-    if (tid == 0) out[1 + r] = all == 0 ? -1 : (int32_t)(0xFFFFFFFFu - (uint32_t)(all & 0xFFFFFFFFu));
-    if (all == 0) continue;
-#pragma unroll
-    for (int i = 0; i < kMaxLists; ++i)
-      if (key[i] == all) {  // keys are unique: block ids differ across lists
-        const int sp = tid + i * blockDim.x;
-        key[i] = head_key(sp, ++pos[i]);
+  // this CTA's top-(k-1) blocks of group g (warp g): k-1 rounds of a warp-wide
+  // maximum over (score, lower block id first) keys; the winner is cleared
+  if (warp < G) {
+    const int g = warp;
+    uint64_t* out = cand + (((int64_t)seq * splits + split) * G + g) * km1;
+    for (int r = 0; r < km1; ++r) {
+      uint64_t best = 0;
+      for (int b = lane; b < nblk; b += 32) {
+        const uint32_t o = bmax_s[b * kGroupsPerMma + g];
+        const uint64_t key = o ? (((uint64_t)o << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(b_lo + b))) : 0ull;
+        best = key > best ? key : best;
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      if (best != 0) {
+        const int b = (int)((0xFFFFFFFFu - (uint32_t)best) - (uint32_t)b_lo);
+        if ((b & 31) == lane) bmax_s[b * kGroupsPerMma + g] = 0u;
+      }
+      __syncwarp();
+      if (lane == 0) out[r] = best;  // 0 = no candidate
+    }
   }
+
+  // the last CTA of this sequence to get here merges every CTA's lists
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&tickets[seq], 1u) == (unsigned)(splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (warp < G) {
+    // a tournament: lane l holds the heads of lists l, l + 32, ... (each sorted best-first)
+    const int g = warp;
+    auto list = [&](int sp) { return cand + (((int64_t)seq * splits + sp) * G + g) * km1; };
+    int pos[kMergeListsPerLane];
+    uint64_t head[kMergeListsPerLane];
+#pragma unroll
+    for (int i = 0; i < kMergeListsPerLane; ++i) {
+      const int sp = lane + 32 * i;
+      pos[i] = 0;
+      head[i] = (sp < splits && km1 > 0) ? __ldcg(list(sp)) : 0ull;
+    }
+    int32_t* outb = block_idx + ((int64_t)seq * G + g) * k;
+    if (lane == 0) outb[0] = ok ? (int32_t)local : -1;
+    for (int r = 0; r < km1; ++r) {
+      uint64_t best = 0;
+#pragma unroll
+      for (int i = 0; i < kMergeListsPerLane; ++i) best = head[i] > best ? head[i] : best;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
+        best = other > best ? other : best;
+      }
+      if (lane == 0) outb[1 + r] = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
+      if (best == 0) continue;
+#pragma unroll
+      for (int i = 0; i < kMergeListsPerLane; ++i)
+        if (head[i] == best) {  // keys are unique: block ids differ across lists
+          ++pos[i];
+          head[i] = pos[i] < km1 ? __ldcg(list(lane + 32 * i) + pos[i]) : 0ull;
+        }
+    }
+  }
+  if (tid == 0) tickets[seq] = 0u;  // ready for the next call
 }
 
-// One CTA per (slot, group, sequence): 128 threads.
 // One CTA (4 warps) per (slot, group, sequence): the block's K/V rows are
 // staged in shared memory (16-byte chunk c of row j stored at chunk
 // c ^ (j mod d/8), so ldmatrix rows fall in distinct banks).  The group's
@@ -208,7 +222,10 @@ __global__ void __launch_bounds__(1024) decode_merge_kernel(const float* __restr
 // warp w scores keys [w BK/4, (w+1) BK/4), the softmax statistics are merged
 // across warps in shared memory, P stays in registers as the A operand of
 // P V (V read transposed by ldmatrix), and the warps' partial O are summed in
-// shared memory before the head's partial (O, lse) is written.
+// shared memory before the head's partial (O, lse) is written.  The last CTA
+// of a (sequence, group) to finish merges the group's k partials per head:
+// M = max lse_s, w_s = e^(lse_s - M) / sum e^(lse_s - M), out = sum w_s O_s,
+// lse = M + ln sum e^(lse_s - M).
 template <int D, int BK>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __restrict__ q_t,
                                                           const uint16_t* __restrict__ k_cache,
@@ -216,9 +233,13 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
                                                           const int32_t* __restrict__ ctx_len,
                                                           const int32_t* __restrict__ block_idx, int64_t ctx_max,
                                                           int H_q, int G, int k, float scale,
-                                                          float* __restrict__ part_o, float* __restrict__ part_lse) {
+                                                          float* __restrict__ part_o, float* __restrict__ part_lse,
+                                                          unsigned int* __restrict__ tickets,
+                                                          uint16_t* __restrict__ out, float* __restrict__ lse) {
   extern __shared__ __align__(16) uint16_t kv_s[];  // K rows [BK][D], then V rows [BK][D]
   __shared__ float red_m[4][8], red_l[4][8];
+  __shared__ float w_s[8][32];  // combine weights [head][slot]
+  __shared__ int s_last;
   constexpr int C8 = D / 8;     // 16-byte chunks per row
   constexpr int KPW = BK / 4;   // keys per warp
   constexpr int NT = KPW / 8;   // 8-key n-tiles per warp
@@ -229,6 +250,7 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   const int gq = lane >> 2, tq = lane & 3;  // fragment row (head) and column pair
   const int gs = H_q / G;
   const int64_t len = ctx_len[seq];
+  griddep_wait();  // block_idx comes from the scan grid
   const int32_t b = block_idx[((int64_t)seq * G + g) * k + slot];
   const int64_t nb = (ctx_max + BK - 1) / BK;
   const bool valid = len >= 1 && len <= ctx_max && b >= 0 && (int64_t)b < nb;
@@ -239,8 +261,7 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   float* pl = part_lse + ((int64_t)seq * H_q + g * gs) * k + slot;
   if (nvis == 0) {
     for (int hh = tid; hh < gs; hh += blockDim.x) pl[(int64_t)hh * k] = __int_as_float(0xff800000);
-    return;
-  }
+  } else {
   // stage the visible K and V rows with every copy in flight at once (rows past nvis read as zero)
   const int64_t kv_row = (int64_t)G * D;
   const uint16_t* Kb = k_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
@@ -354,37 +375,65 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     const float L = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
     pl[(int64_t)tid * k] = M + logf(L);
   }
-}
+  }  // nvis > 0
 
-template <int D>
-__global__ void decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int H_q,
-                                      int k, uint16_t* __restrict__ out, float* __restrict__ lse) {
-  const int64_t sh = blockIdx.x;  // seq * H_q + h
-  const float* pl = part_lse + sh * k;
-  float m = __int_as_float(0xff800000);
-  for (int s = 0; s < k; ++s) m = fmaxf(m, pl[s]);
-  for (int cc = threadIdx.x; cc < D; cc += blockDim.x) {
-    float acc = 0.f, L = 0.f;
-    if (m != __int_as_float(0xff800000)) {
+  // the last of the group's k CTAs merges the partials
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&tickets[(int64_t)seq * G + g], 1u) == (unsigned)(k - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* gl = part_lse + ((int64_t)seq * H_q + g * gs) * k;  // [gs][k]
+  for (int i = tid; i < gs * k; i += blockDim.x) w_s[i / k][i % k] = __ldcg(gl + i);
+  __syncthreads();
+  if (tid < gs) {
+    float M = __int_as_float(0xff800000);
+    for (int s = 0; s < k; ++s) M = fmaxf(M, w_s[tid][s]);
+    float L = 0.f;
+    if (M != __int_as_float(0xff800000))
       for (int s = 0; s < k; ++s) {
-        if (pl[s] == __int_as_float(0xff800000)) continue;
-        float w = __expf(pl[s] - m);
+        const float w = w_s[tid][s] == __int_as_float(0xff800000) ? 0.f : __expf(w_s[tid][s] - M);
+        w_s[tid][s] = w;
         L += w;
-        acc += w * part_o[(sh * k + s) * D + cc];
+      }
+    else
+      for (int s = 0; s < k; ++s) w_s[tid][s] = 0.f;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int s = 0; s < k; ++s) w_s[tid][s] *= inv;
+    if (lse) lse[(int64_t)seq * H_q + g * gs + tid] = L > 0.f ? M + logf(L) : __int_as_float(0xff800000);
+  }
+  __syncthreads();
+  const float* go = part_o + ((int64_t)seq * H_q + g * gs) * k * D;  // [gs][k][D]
+  for (int i = tid; i < gs * (D / 2); i += blockDim.x) {
+    const int hh = i / (D / 2), dc = 2 * (i % (D / 2));
+    float a0 = 0.f, a1 = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const float w = w_s[hh][s];
+      if (w != 0.f) {
+        const float2 o = __ldcg(reinterpret_cast<const float2*>(go + ((int64_t)hh * k + s) * D + dc));
+        a0 += w * o.x;
+        a1 += w * o.y;
       }
     }
-    out[sh * D + cc] = (uint16_t)(pack_bf16x2(L > 0.f ? acc / L : 0.f, 0.f) & 0xFFFFu);
-    if (cc == 0 && lse) lse[sh] = L > 0.f ? m + logf(L) : __int_as_float(0xff800000);
+    const uint32_t pr = pack_bf16x2(a0, a1);
+    uint16_t* o = out + ((int64_t)seq * H_q + g * gs + hh) * D + dc;  // out needs only 2-byte alignment
+    o[0] = (uint16_t)(pr & 0xFFFFu);
+    o[1] = (uint16_t)(pr >> 16);
   }
+  if (tid == 0) tickets[(int64_t)seq * G + g] = 0u;  // ready for the next call
 }
 
+
 struct DecodeScratch {
-  float* cand_s;
-  int32_t* cand_b;
+  unsigned int* tickets;  // [B] scan + [B * G] attention; cleared before every call
+  uint64_t* cand;         // [B, splits, G, k-1] per-CTA candidate keys
   int32_t* blk;
   float* part_o;
   float* part_lse;
 };
+
+static size_t ticket_bytes(const DecodePlan& p) { return align_up((size_t)p.B * (1 + p.H_kv) * 4, 256); }
 
 static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   char* c = (char*)base;
@@ -394,10 +443,9 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
     off += align_up(bytes, 256);
     return r;
   };
-  const int cap = topk_cap(p.k - 1);
   DecodeScratch s;
-  s.cand_s = (float*)take((size_t)p.B * p.splits * p.H_kv * cap * 4);
-  s.cand_b = (int32_t*)take((size_t)p.B * p.splits * p.H_kv * cap * 4);
+  s.tickets = (unsigned int*)take(ticket_bytes(p));
+  s.cand = (uint64_t*)take((size_t)p.B * p.splits * p.H_kv * (p.k > 1 ? p.k - 1 : 1) * 8);
   s.blk = (int32_t*)take((size_t)p.B * p.H_kv * p.k * 4);
   s.part_o = (float*)take((size_t)p.B * p.H_q * p.k * p.d * 4);
   s.part_lse = (float*)take((size_t)p.B * p.H_q * p.k * 4);
@@ -405,28 +453,41 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   return off;
 }
 
-template <int DI, int BK, int CAP>
-cudaError_t launch_scan_merge(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len,
-                              const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
-                              cudaStream_t s) {
-  dim3 grid((unsigned)p.splits, (unsigned)p.B);
-  decode_scan_kernel<DI, BK, CAP><<<grid, kScanThreads, 0, s>>>((const uint16_t*)q_idx_t,
-                                                                (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max,
-                                                                p.H_kv, p.k, p.splits, sc.cand_s, sc.cand_b, st);
-  const int mthreads = p.splits >= 1024 ? 1024 : (p.splits + 31) / 32 * 32;
-  decode_merge_kernel<CAP><<<dim3((unsigned)p.B, (unsigned)p.H_kv), mthreads, 0, s>>>(
-      sc.cand_s, sc.cand_b, ctx_len, p.ctx_max, p.Bk, p.H_kv, p.k, p.splits, blk);
+template <int DI, int BK>
+cudaError_t launch_scan(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const DecodePlan& p,
+                        const DecodeScratch& sc, int32_t* blk, DeviceStatus* st, cudaStream_t s) {
+  const size_t smem = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
+  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel<DI, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_scan_kernel<DI, BK><<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
+      (const uint16_t*)q_idx_t, (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max, p.H_kv, p.k, p.splits, sc.cand,
+      sc.tickets, blk, st);
   return cudaGetLastError();
 }
 
-template <int DI, int BK>
-cudaError_t scan_cap(const void* a, const void* b, const int32_t* c, const DecodePlan& p, const DecodeScratch& sc,
-                     int32_t* blk, DeviceStatus* st, cudaStream_t s) {
-  int km1 = p.k - 1;
-  if (km1 <= 4) return launch_scan_merge<DI, BK, 4>(a, b, c, p, sc, blk, st, s);
-  if (km1 <= 8) return launch_scan_merge<DI, BK, 8>(a, b, c, p, sc, blk, st, s);
-  if (km1 <= 16) return launch_scan_merge<DI, BK, 16>(a, b, c, p, sc, blk, st, s);
-  return launch_scan_merge<DI, BK, 32>(a, b, c, p, sc, blk, st, s);
+// The attention grid as a programmatic dependent of the scan: its CTAs may be
+// scheduled while the scan drains and wait (griddepcontrol.wait) for its results.
+template <int D, int BK>
+cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
+                            const int32_t* blk, const DecodePlan& p, float scale, const DecodeScratch& sc, void* out,
+                            float* lse, cudaStream_t s) {
+  const int smem = 2 * BK * D * 2;  // K and V rows of one block
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.k, (unsigned)p.H_kv, (unsigned)p.B);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, BK>, (const uint16_t*)q_t, (const uint16_t*)k_cache,
+                            (const uint16_t*)v_cache, ctx_len, (const int32_t*)blk, p.ctx_max, p.H_q, p.H_kv, p.k,
+                            scale, sc.part_o, sc.part_lse, sc.tickets + p.B, (uint16_t*)out, lse);
 }
 
 }  // namespace
@@ -442,16 +503,23 @@ DecodePlan decode_plan(int B, int64_t ctx_max, int H_q, int H_kv, int d, int d_I
   p.Bk = Bk;
   p.k = k;
   p.gs = H_q / H_kv;
-  const int64_t nb = (ctx_max + Bk - 1) / Bk;
-  int64_t splits = ((int64_t)num_sms() * 4 + B - 1) / B;  // ~4 CTAs of 8 warps per SM
-  int64_t max_splits = nb / 8 > 1 ? nb / 8 : 1;             // at least 8 blocks per CTA
-  if (splits > max_splits) splits = max_splits;
+  const int64_t cand_max = ctx_max >= 1 ? (ctx_max - 1) / Bk : 0;  // candidate blocks of the longest sequence
+  int64_t splits = ((int64_t)num_sms() * 2 + B - 1) / B;           // two scan CTAs per SM
+  const int64_t few = cand_max / 8 > 1 ? cand_max / 8 : 1;          // at least ~8 blocks per CTA
+  if (splits > few) splits = few;
+  const int64_t need = (cand_max + kMaxCtaBlocks - 1) / kMaxCtaBlocks;  // shared-memory bound per CTA
+  if (splits < need) splits = need;
+  if (splits > 32 * kMergeListsPerLane) splits = 32 * kMergeListsPerLane;
   if (splits < 1) splits = 1;
   p.splits = (int)splits;
+  p.max_cta_blocks = (int)((cand_max + splits - 1) / splits);
+  if (p.max_cta_blocks < 1) p.max_cta_blocks = 1;
   return p;
 }
 
 size_t decode_scratch_bytes(const DecodePlan& p) { return carve(p, nullptr, nullptr); }
+
+size_t decode_clear_bytes(const DecodePlan& p) { return ticket_bytes(p); }
 
 cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
                           const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
@@ -461,46 +529,21 @@ cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_id
   int32_t* blk = block_idx ? block_idx : sc.blk;
   cudaError_t e;
   if (p.d_I == 32) {
-    e = p.Bk == 64 ? scan_cap<32, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
-                   : scan_cap<32, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<32, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
+                   : launch_scan<32, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
   } else if (p.d_I == 64) {
-    e = p.Bk == 64 ? scan_cap<64, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
-                   : scan_cap<64, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<64, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
+                   : launch_scan<64, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
   } else {
-    e = p.Bk == 64 ? scan_cap<128, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
-                   : scan_cap<128, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<128, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
+                   : launch_scan<128, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
   }
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)p.k, (unsigned)p.H_kv, (unsigned)p.B);
-  auto attn_smem = [](int D, int BK) { return 2 * BK * D * 2; };  // K and V rows of one block
-  if (p.d == 128 && p.Bk == 128) {
-    e = cudaFuncSetAttribute(decode_attn_kernel<128, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             attn_smem(128, 128));
-    if (e != cudaSuccess) return e;
-  }
-  if (p.d == 64 && p.Bk == 64)
-    decode_attn_kernel<64, 64><<<grid, 128, attn_smem(64, 64), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
-                                                    (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q, p.H_kv,
-                                                    p.k, scale, sc.part_o, sc.part_lse);
-  else if (p.d == 64)
-    decode_attn_kernel<64, 128><<<grid, 128, attn_smem(64, 128), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
-                                                     (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q,
-                                                     p.H_kv, p.k, scale, sc.part_o, sc.part_lse);
-  else if (p.Bk == 64)
-    decode_attn_kernel<128, 64><<<grid, 128, attn_smem(128, 64), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
-                                                     (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q,
-                                                     p.H_kv, p.k, scale, sc.part_o, sc.part_lse);
-  else
-    decode_attn_kernel<128, 128><<<grid, 128, attn_smem(128, 128), s>>>((const uint16_t*)q_t, (const uint16_t*)k_cache,
-                                                      (const uint16_t*)v_cache, ctx_len, blk, p.ctx_max, p.H_q,
-                                                      p.H_kv, p.k, scale, sc.part_o, sc.part_lse);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.d == 64)
-    decode_combine_kernel<64><<<p.B * p.H_q, 64, 0, s>>>(sc.part_o, sc.part_lse, p.H_q, p.k, (uint16_t*)out, lse);
-  else
-    decode_combine_kernel<128><<<p.B * p.H_q, 128, 0, s>>>(sc.part_o, sc.part_lse, p.H_q, p.k, (uint16_t*)out, lse);
-  return cudaGetLastError();
+    return p.Bk == 64 ? launch_attn_dep<64, 64>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s)
+                      : launch_attn_dep<64, 128>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s);
+  return p.Bk == 64 ? launch_attn_dep<128, 64>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s)
+                    : launch_attn_dep<128, 128>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s);
 }
 
 // ---------------------------------------------------------------- fixed scratch for msa_decode_noalloc

@@ -81,10 +81,14 @@ struct DecodePlan {
   int B;
   int64_t ctx_max;
   int H_q, H_kv, d, d_I, Bk, k, gs;
-  int splits;  // CTAs per sequence in the index-key scan
+  int splits;          // CTAs per sequence in the index-key scan
+  int max_cta_blocks;  // candidate blocks of one scan CTA, at most
 };
 DecodePlan decode_plan(int B, int64_t ctx_max, int H_q, int H_kv, int d, int d_I, int Bk, int k);
 size_t decode_scratch_bytes(const DecodePlan& p);
+// Bytes at the start of the decode scratch that must be zero when a call starts
+// (the completion tickets of the scan and attention CTAs).
+size_t decode_clear_bytes(const DecodePlan& p);
 cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
                           const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
                           float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s);
