@@ -215,17 +215,21 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   if (tid == 0) tickets[seq] = 0u;  // ready for the next call
 }
 
-// One CTA (4 warps) per (slot, group, sequence): the block's K/V rows are
-// staged in shared memory (16-byte chunk c of row j stored at chunk
-// c ^ (j mod d/8), so ldmatrix rows fall in distinct banks).  The group's
-// heads are the rows of m16n8k16 tensor-core tiles (rows >= gs are zero):
-// warp w scores keys [w BK/4, (w+1) BK/4), the softmax statistics are merged
-// across warps in shared memory, P stays in registers as the A operand of
-// P V (V read transposed by ldmatrix), and the warps' partial O are summed in
-// shared memory before the head's partial (O, lse) is written.  The last CTA
-// of a (sequence, group) to finish merges the group's k partials per head:
-// M = max lse_s, w_s = e^(lse_s - M) / sum e^(lse_s - M), out = sum w_s O_s,
-// lse = M + ln sum e^(lse_s - M).
+// One CTA (4 warps) per (slot, group, sequence).  The group's heads are the
+// rows of m16n8k16 tensor-core tiles (rows >= gs are zero) and warp w takes
+// keys [w BK/4, (w+1) BK/4):
+//   - K rows go straight from HBM into B fragments (16-byte loads; the head
+//     dims are permuted the same way in the query's A fragments, as in the
+//     scan), so only V is staged in shared memory (16-byte chunk c of row j
+//     stored at chunk c ^ (j mod d/8), so ldmatrix rows fall in distinct
+//     banks), which keeps every CTA of the grid resident at once;
+//   - the softmax statistics are merged across warps in shared memory, P stays
+//     in registers as the A operand of P V (V read transposed by ldmatrix),
+//     and the warps' partial O are summed in shared memory before the head's
+//     partial (O, lse) is written.
+// The last CTA of a (sequence, group) to finish merges the group's k partials
+// per head: M = max lse_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
+// out = sum w_s O_s, lse = M + ln sum e^(lse_s - M).
 template <int D, int BK>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __restrict__ q_t,
                                                           const uint16_t* __restrict__ k_cache,
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
                                                           float* __restrict__ part_o, float* __restrict__ part_lse,
                                                           unsigned int* __restrict__ tickets,
                                                           uint16_t* __restrict__ out, float* __restrict__ lse) {
-  extern __shared__ __align__(16) uint16_t kv_s[];  // K rows [BK][D], then V rows [BK][D]
+  extern __shared__ __align__(16) uint16_t v_s[];  // V rows [BK][D]; later the warps' partial O
   __shared__ float red_m[4][8], red_l[4][8];
   __shared__ float w_s[8][32];  // combine weights [head][slot]
   __shared__ int s_last;
@@ -244,12 +248,22 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   constexpr int KPW = BK / 4;   // keys per warp
   constexpr int NT = KPW / 8;   // 8-key n-tiles per warp
   constexpr int KS = D / 16;    // k-steps over d
-  static_assert(NT % 2 == 0, "two n-tiles per ldmatrix");
+  constexpr int NP = D / 32;    // 16-byte pieces of a row per lane
+  static_assert(NT % 2 == 0, "P V k-steps take two n-tiles");
+  static_assert(4 * 8 * D * 4 <= BK * D * 2, "partial O sums fit over V");
   const int slot = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = lane >> 2, tq = lane & 3;  // fragment row (head) and column pair
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row (head; key of a B column) and column pair
   const int gs = H_q / G;
   const int64_t len = ctx_len[seq];
+  // q as A fragments: row gq = head gq of the group (zero past gs), rows 8..15 zero; piece p holds dims
+  // 32p + 8tq .. +7: words x, y feed k-step 2p and z, w k-step 2p+1 (the order of the K fragments below)
+  uint4 qv[NP];
+  {
+    const uint16_t* qrow = q_t + ((int64_t)seq * H_q + g * gs + gq) * D + 8 * tq;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) qv[p] = gq < gs ? ldg_stream_16(qrow + 32 * p) : make_uint4(0u, 0u, 0u, 0u);
+  }
   griddep_wait();  // block_idx comes from the scan grid
   const int32_t b = block_idx[((int64_t)seq * G + g) * k + slot];
   const int64_t nb = (ctx_max + BK - 1) / BK;
@@ -262,119 +276,110 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   if (nvis == 0) {
     for (int hh = tid; hh < gs; hh += blockDim.x) pl[(int64_t)hh * k] = __int_as_float(0xff800000);
   } else {
-  // stage the visible K and V rows with every copy in flight at once (rows past nvis read as zero)
-  const int64_t kv_row = (int64_t)G * D;
-  const uint16_t* Kb = k_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
-  const uint16_t* Vb = v_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
-  uint16_t* Ks = kv_s;
-  uint16_t* Vs = kv_s + BK * D;
-  for (int i = tid; i < BK * C8; i += blockDim.x) {
-    const int j = i / C8, c8 = i % C8;
-    const bool in = j < nvis;
-    const int64_t off = (int64_t)(in ? j : 0) * kv_row + c8 * 8;
-    const int sw = (c8 ^ (j & (C8 - 1))) * 8;
-    cp_async_16(Ks + j * D + sw, Kb + off, in ? 16 : 0);
-    cp_async_16(Vs + j * D + sw, Vb + off, in ? 16 : 0);
-  }
-  cp_async_commit();
-  // q as A fragments: row gq = head gq of the group (zero past gs), rows 8..15 zero
-  uint32_t qa[KS][2];
-  {
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(q_t + ((int64_t)seq * H_q + g * gs + gq) * D);
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = gq < gs ? qrow[(16 * ks + 2 * tq) >> 1] : 0u;
-      qa[ks][1] = gq < gs ? qrow[(16 * ks + 8 + 2 * tq) >> 1] : 0u;
+    const int64_t kv_row = (int64_t)G * D;
+    const uint16_t* Kb = k_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
+    const uint16_t* Vb = v_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
+    // V rows into shared memory (rows past nvis read as zero), every copy in flight at once
+    for (int i = tid; i < BK * C8; i += blockDim.x) {
+      const int j = i / C8, c8 = i % C8;
+      const bool in = j < nvis;
+      cp_async_16(v_s + j * D + (c8 ^ (j & (C8 - 1))) * 8, Vb + (int64_t)(in ? j : 0) * kv_row + c8 * 8, in ? 16 : 0);
     }
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-  // S = q K^T for this warp's keys
-  float sacc[NT][4];
+    cp_async_commit();
+    // K rows of this warp's keys as B fragments (key = column gq of n-tile nt); rows past nvis repeat a
+    // visible row and are masked below
+    uint4 kf[NT][NP];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int j = min(warp * KPW + nt * 8 + gq, nvis - 1);
+      const uint16_t* kr = Kb + (int64_t)j * kv_row + 8 * tq;
 #pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-    const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-#pragma unroll
-    for (int np = 0; np < NT; np += 2) {
-      // matrices: (n-tile np, dims +0..7), (np, +8..15), (np+1, +0..7), (np+1, +8..15)
-      const int key = warp * KPW + np * 8 + (lane & 7) + ((lane >> 4) << 3);
-      const int chunk = 2 * ks + ((lane >> 3) & 1);
-      uint32_t r0, r1, r2, r3;
-      ldmatrix_x4(r0, r1, r2, r3, Ks + key * D + ((chunk ^ (key & (C8 - 1))) * 8));
-      const uint32_t b0[2] = {r0, r1}, b1[2] = {r2, r3};
-      mma_bf16_16816(sacc[np], a, b0);
-      mma_bf16_16816(sacc[np + 1], a, b1);
+      for (int p = 0; p < NP; ++p) kf[nt][p] = ldg_stream_16(kr + 32 * p);
     }
-  }
-  // scale, mask past nvis, row (head) maxima across the warp's keys and then across warps
-  float mx = __int_as_float(0xff800000);
+    // S = q K^T for this warp's keys
+    float sacc[NT][4];
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+    for (int nt = 0; nt < NT; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int j = warp * KPW + nt * 8 + 2 * tq + e;
-      const float v = j < nvis ? sacc[nt][e] * scale : __int_as_float(0xff800000);
-      sacc[nt][e] = v;
-      mx = fmaxf(mx, v);
+    for (int p = 0; p < NP; ++p) {
+      const uint32_t a0[4] = {qv[p].x, 0u, qv[p].y, 0u};
+      const uint32_t a1[4] = {qv[p].z, 0u, qv[p].w, 0u};
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint32_t b0[2] = {kf[nt][p].x, kf[nt][p].y}, b1[2] = {kf[nt][p].z, kf[nt][p].w};
+        mma_bf16_16816(sacc[nt], a0, b0);
+        mma_bf16_16816(sacc[nt], a1, b1);
+      }
     }
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-  if (tq == 0) red_m[warp][gq] = mx;
-  __syncthreads();
-  const float m = fmaxf(fmaxf(red_m[0][gq], red_m[1][gq]), fmaxf(red_m[2][gq], red_m[3][gq]));
-  float ls = 0.f;
-  uint32_t pa[NT / 2][2];  // P as A fragments of the P V k-steps (16 keys each)
+    // scale, mask past nvis, row (head) maxima across the warp's keys and then across warps
+    float mx = __int_as_float(0xff800000);
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const float p0 = __expf(sacc[nt][0] - m), p1 = __expf(sacc[nt][1] - m);  // e^-inf = 0
-    ls += p0 + p1;
-    pa[nt >> 1][nt & 1] = pack_bf16x2(p0, p1);
-  }
-  ls += __shfl_xor_sync(0xffffffffu, ls, 1);
-  ls += __shfl_xor_sync(0xffffffffu, ls, 2);
-  if (tq == 0) red_l[warp][gq] = ls;
-  // O = P V over this warp's keys
-  float oacc[D / 8][4];
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
+      for (int e = 0; e < 2; ++e) {
+        const int j = warp * KPW + nt * 8 + 2 * tq + e;
+        const float v = j < nvis ? sacc[nt][e] * scale : __int_as_float(0xff800000);
+        sacc[nt][e] = v;
+        mx = fmaxf(mx, v);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (tq == 0) red_m[warp][gq] = mx;
+    __syncthreads();
+    const float m = fmaxf(fmaxf(red_m[0][gq], red_m[1][gq]), fmaxf(red_m[2][gq], red_m[3][gq]));
+    float ls = 0.f;
+    uint32_t pa[NT / 2][2];  // P as A fragments of the P V k-steps (16 keys each)
 #pragma unroll
-  for (int ks2 = 0; ks2 < NT / 2; ++ks2) {
-    const uint32_t a[4] = {pa[ks2][0], 0u, pa[ks2][1], 0u};
-#pragma unroll
-    for (int nd = 0; nd < D / 8; nd += 2) {
-      // transposed matrices: (keys +0..7, d n-tile nd), (keys +8..15, nd), (+0..7, nd+1), (+8..15, nd+1)
-      const int key = warp * KPW + 16 * ks2 + (lane & 7) + (((lane >> 3) & 1) << 3);
-      const int chunk = nd + (lane >> 4);
-      uint32_t r0, r1, r2, r3;
-      ldmatrix_x4_trans(r0, r1, r2, r3, Vs + key * D + ((chunk ^ (key & (C8 - 1))) * 8));
-      const uint32_t b0[2] = {r0, r1}, b1[2] = {r2, r3};
-      mma_bf16_16816(oacc[nd], a, b0);
-      mma_bf16_16816(oacc[nd + 1], a, b1);
+    for (int nt = 0; nt < NT; ++nt) {
+      const float p0 = __expf(sacc[nt][0] - m), p1 = __expf(sacc[nt][1] - m);  // e^-inf = 0
+      ls += p0 + p1;
+      pa[nt >> 1][nt & 1] = pack_bf16x2(p0, p1);
     }
-  }
-  // sum the warps' partial O in shared memory (over the K rows, which are no longer read)
-  __syncthreads();
-  float* red_o = reinterpret_cast<float*>(kv_s);  // [4 warps][8 rows][D]
+    ls += __shfl_xor_sync(0xffffffffu, ls, 1);
+    ls += __shfl_xor_sync(0xffffffffu, ls, 2);
+    if (tq == 0) red_l[warp][gq] = ls;
+    cp_async_wait<0>();
+    __syncthreads();
+    // O = P V over this warp's keys
+    float oacc[D / 8][4];
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) {
-    red_o[(warp * 8 + gq) * D + nd * 8 + 2 * tq] = oacc[nd][0];
-    red_o[(warp * 8 + gq) * D + nd * 8 + 2 * tq + 1] = oacc[nd][1];
-  }
-  __syncthreads();
-  for (int i = tid; i < gs * D; i += blockDim.x) {
-    const int hh = i / D, dc = i % D;
-    const float L = red_l[0][hh] + red_l[1][hh] + red_l[2][hh] + red_l[3][hh];
-    const float o = red_o[(0 * 8 + hh) * D + dc] + red_o[(1 * 8 + hh) * D + dc] + red_o[(2 * 8 + hh) * D + dc] +
-                    red_o[(3 * 8 + hh) * D + dc];
-    po[(int64_t)hh * k * D + dc] = o / L;
-  }
-  if (tid < gs) {
-    const float M = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]), fmaxf(red_m[2][tid], red_m[3][tid]));
-    const float L = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
-    pl[(int64_t)tid * k] = M + logf(L);
-  }
+    for (int nd = 0; nd < D / 8; ++nd) oacc[nd][0] = oacc[nd][1] = oacc[nd][2] = oacc[nd][3] = 0.f;
+#pragma unroll
+    for (int ks2 = 0; ks2 < NT / 2; ++ks2) {
+      const uint32_t a[4] = {pa[ks2][0], 0u, pa[ks2][1], 0u};
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 2) {
+        // transposed matrices: (keys +0..7, d n-tile nd), (keys +8..15, nd), (+0..7, nd+1), (+8..15, nd+1)
+        const int key = warp * KPW + 16 * ks2 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int chunk = nd + (lane >> 4);
+        uint32_t r0, r1, r2, r3;
+        ldmatrix_x4_trans(r0, r1, r2, r3, v_s + key * D + ((chunk ^ (key & (C8 - 1))) * 8));
+        const uint32_t b0[2] = {r0, r1}, b1[2] = {r2, r3};
+        mma_bf16_16816(oacc[nd], a, b0);
+        mma_bf16_16816(oacc[nd + 1], a, b1);
+      }
+    }
+    // sum the warps' partial O in shared memory (over the V rows, which are no longer read)
+    __syncthreads();
+    float* red_o = reinterpret_cast<float*>(v_s);  // [4 warps][8 rows][D]
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      red_o[(warp * 8 + gq) * D + nd * 8 + 2 * tq] = oacc[nd][0];
+      red_o[(warp * 8 + gq) * D + nd * 8 + 2 * tq + 1] = oacc[nd][1];
+    }
+    __syncthreads();
+    for (int i = tid; i < gs * D; i += blockDim.x) {
+      const int hh = i / D, dc = i % D;
+      const float L = red_l[0][hh] + red_l[1][hh] + red_l[2][hh] + red_l[3][hh];
+      const float o = red_o[(0 * 8 + hh) * D + dc] + red_o[(1 * 8 + hh) * D + dc] + red_o[(2 * 8 + hh) * D + dc] +
+                      red_o[(3 * 8 + hh) * D + dc];
+      po[(int64_t)hh * k * D + dc] = o / L;
+    }
+    if (tid < gs) {
+      const float M = fmaxf(fmaxf(red_m[0][tid], red_m[1][tid]), fmaxf(red_m[2][tid], red_m[3][tid]));
+      const float L = red_l[0][tid] + red_l[1][tid] + red_l[2][tid] + red_l[3][tid];
+      pl[(int64_t)tid * k] = M + logf(L);
+    }
   }  // nvis > 0
 
   // the last of the group's k CTAs merges the partials
@@ -391,35 +396,48 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     float M = __int_as_float(0xff800000);
     for (int s = 0; s < k; ++s) M = fmaxf(M, w_s[tid][s]);
     float L = 0.f;
-    if (M != __int_as_float(0xff800000))
-      for (int s = 0; s < k; ++s) {
-        const float w = w_s[tid][s] == __int_as_float(0xff800000) ? 0.f : __expf(w_s[tid][s] - M);
-        w_s[tid][s] = w;
-        L += w;
-      }
-    else
-      for (int s = 0; s < k; ++s) w_s[tid][s] = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const float w = M == __int_as_float(0xff800000) || w_s[tid][s] == __int_as_float(0xff800000)
+                          ? 0.f
+                          : __expf(w_s[tid][s] - M);
+      w_s[tid][s] = w;
+      L += w;
+    }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int s = 0; s < k; ++s) w_s[tid][s] *= inv;
     if (lse) lse[(int64_t)seq * H_q + g * gs + tid] = L > 0.f ? M + logf(L) : __int_as_float(0xff800000);
   }
   __syncthreads();
+  // thread -> (head, 4 columns); the partial loads of 16 slots are all in flight before the sums
   const float* go = part_o + ((int64_t)seq * H_q + g * gs) * k * D;  // [gs][k][D]
-  for (int i = tid; i < gs * (D / 2); i += blockDim.x) {
-    const int hh = i / (D / 2), dc = 2 * (i % (D / 2));
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < k; ++s) {
-      const float w = w_s[hh][s];
-      if (w != 0.f) {
-        const float2 o = __ldcg(reinterpret_cast<const float2*>(go + ((int64_t)hh * k + s) * D + dc));
-        a0 += w * o.x;
-        a1 += w * o.y;
+  for (int i = tid; i < gs * (D / 4); i += blockDim.x) {
+    const int hh = i / (D / 4), dc = 4 * (i % (D / 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < k; s0 += 16) {
+      float4 o[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int s = s0 + j;
+        const bool use = s < k && w_s[hh][s < k ? s : 0] != 0.f;
+        o[j] = use ? __ldcg(reinterpret_cast<const float4*>(go + ((int64_t)hh * k + s) * D + dc))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int s = s0 + j;
+        const float w = s < k ? w_s[hh][s] : 0.f;
+        acc.x += w * o[j].x;
+        acc.y += w * o[j].y;
+        acc.z += w * o[j].z;
+        acc.w += w * o[j].w;
       }
     }
-    const uint32_t pr = pack_bf16x2(a0, a1);
+    const uint32_t lo = pack_bf16x2(acc.x, acc.y), hi = pack_bf16x2(acc.z, acc.w);
     uint16_t* o = out + ((int64_t)seq * H_q + g * gs + hh) * D + dc;  // out needs only 2-byte alignment
-    o[0] = (uint16_t)(pr & 0xFFFFu);
-    o[1] = (uint16_t)(pr >> 16);
+    o[0] = (uint16_t)(lo & 0xFFFFu);
+    o[1] = (uint16_t)(lo >> 16);
+    o[2] = (uint16_t)(hi & 0xFFFFu);
+    o[3] = (uint16_t)(hi >> 16);
   }
   if (tid == 0) tickets[(int64_t)seq * G + g] = 0u;  // ready for the next call
 }
@@ -472,7 +490,7 @@ template <int D, int BK>
 cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
                             const int32_t* blk, const DecodePlan& p, float scale, const DecodeScratch& sc, void* out,
                             float* lse, cudaStream_t s) {
-  const int smem = 2 * BK * D * 2;  // K and V rows of one block
+  const int smem = BK * D * 2;  // V rows of one block
   cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
