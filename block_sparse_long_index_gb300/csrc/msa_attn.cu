@@ -24,6 +24,8 @@
 //      M = max m_s, L = sum l_s 2^(m_s - M), out = sum O_s 2^(m_s - M) / L.
 #include <math.h>
 
+#include <algorithm>
+
 #include "msa_common.cuh"
 
 namespace msa {
@@ -140,96 +142,146 @@ __global__ void __launch_bounds__(256) tile_records_kernel(const int32_t* __rest
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per query position t: the position's partials (k slots x H_q heads x
-// d, contiguous) are read once, coalesced.  Slot s of group g contributes iff
-// its id is in [0, nb) and not repeated by an earlier slot (the set counts
-// each block once).  Partial s of head h holds O_s = sum_j p_j v_j with
-// p_j = 2^(s_j - m_s) (s_j in log2 units) and l_s = sum_j p_j; then
+// Persistent CTAs of 256 threads, two per SM, each walking the slab's query
+// positions t with a stride of the grid.  Per position the partials (k slots x
+// H_q heads x d, contiguous) are read once, coalesced, with all k slot loads of
+// a thread's (head, 8-column) item in flight together; the next position's
+// (m, l) pairs and block ids are copied into the other half of a shared-memory
+// double buffer (cp.async) while this position streams.  Slot s of group g
+// contributes iff its id is in [0, nb) and not repeated by an earlier slot (the
+// set counts each block once).  Partial s of head h holds O_s = sum_j p_j v_j
+// with p_j = 2^(s_j - m_s) (s_j in log2 units) and l_s = sum_j p_j; then
 // M = max m_s, w_s = 2^(m_s - M) / sum_s l_s 2^(m_s - M), out = sum_s w_s O_s,
 // lse = ln 2 (M + log2 sum_s l_s 2^(m_s - M)); no contribution gives out = 0,
-// lse = -inf.  128 threads with two loads in flight each was the fastest
-// shape measured for this HBM-bound pass.
-constexpr int kCombineThreads = 128;
+// lse = -inf.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineSlots = 16;  // slot loads in flight per item
+
+struct CombineSmem {
+  size_t ml, bidx, cw, use, total;  // byte offsets of one buffer's parts and the total
+  int nbuf;
+};
+inline CombineSmem combine_smem(int k, int H_q, int G) {
+  CombineSmem c;
+  const size_t ml = align_up((size_t)k * H_q * 8, 16), bi = align_up((size_t)G * k * 4, 16);
+  const size_t cw = align_up((size_t)k * H_q * 4, 16), use = align_up((size_t)G * k, 16);
+  c.nbuf = 2 * (ml + bi) + cw + use <= 160 * 1024 ? 2 : 1;
+  c.ml = 0;
+  c.bidx = c.nbuf * ml;
+  c.cw = c.bidx + c.nbuf * bi;
+  c.use = c.cw + cw;
+  c.total = c.use + use;
+  return c;
+}
+
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_8(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
 
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const int32_t* __restrict__ block_idx,
-                                                      const uint16_t* __restrict__ part_o,
-                                                      const float2* __restrict__ part_ml, int64_t N, int H_q, int G,
-                                                      int gs, int k, int64_t nb, int64_t T0,
-                                                      uint16_t* __restrict__ out, float* __restrict__ lse) {
-  extern __shared__ float cw[];          // [k][H_q] m, then weights; then [k][H_q] l
-  __shared__ uint32_t use_mask[64];      // per group: bit s set if slot s contributes
-  float* cl = cw + k * H_q;
-  const int tid = threadIdx.x;
-  const int64_t tr = blockIdx.x;
-  const int64_t t = T0 + tr;
-  for (int g = tid; g < G; g += blockDim.x) {
-    const int32_t* sel = block_idx + ((int64_t)g * N + t) * k;
-    uint32_t use = 0;
-    for (int s = 0; s < k; ++s) {
-      int32_t b = sel[s];
-      bool ok = b >= 0 && (int64_t)b < nb;
-      for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != b;
-      use |= (ok ? 1u : 0u) << s;
-    }
-    use_mask[g] = use;
-  }
-  __syncthreads();
-  const float2* pm = part_ml + tr * k * H_q;
-  for (int i = tid; i < k * H_q; i += blockDim.x) {
-    const int s = i / H_q, h = i % H_q;
-    const float2 ml = pm[i];
-    const bool use = (use_mask[h / gs] >> s) & 1u;
-    cw[i] = use ? ml.x : __int_as_float(0xff800000);
-    cl[i] = use ? ml.y : 0.f;
-  }
-  __syncthreads();
-  for (int h = tid; h < H_q; h += blockDim.x) {
-    float M = __int_as_float(0xff800000);
-    for (int s = 0; s < k; ++s) M = fmaxf(M, cw[s * H_q + h]);
-    float L = 0.f;
-    if (M != __int_as_float(0xff800000)) {
-      for (int s = 0; s < k; ++s) {
-        const float e = exp2f(cw[s * H_q + h] - M);  // 2^-inf = 0 for unused slots
-        cw[s * H_q + h] = e;
-        L += e * cl[s * H_q + h];
-      }
-    } else {
-      for (int s = 0; s < k; ++s) cw[s * H_q + h] = 0.f;
-    }
-    const float il = L > 0.f ? 1.f / L : 0.f;
-    for (int s = 0; s < k; ++s) cw[s * H_q + h] *= il;
-    lse[(int64_t)h * N + t] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : __int_as_float(0xff800000);
-  }
-  __syncthreads();
+__global__ void __launch_bounds__(kCombineThreads, 2) combine_kernel(
+    const int32_t* __restrict__ block_idx, const uint16_t* __restrict__ part_o, const float2* __restrict__ part_ml,
+    int64_t N, int H_q, int G, int gs, int k, int64_t nb, int64_t T0, int64_t rows, CombineSmem lay,
+    uint16_t* __restrict__ out, float* __restrict__ lse) {
+  extern __shared__ __align__(16) unsigned char cmb_s[];
   constexpr int C8 = D / 8;
-  const uint16_t* po = part_o + tr * k * H_q * D;
-  for (int i = tid; i < H_q * C8; i += blockDim.x) {
-    const int h = i / C8, c8 = i % C8;
-    float acc[8];
+  const int tid = threadIdx.x;
+  const int kh = k * H_q, gk = G * k;
+  float2* ml_s = reinterpret_cast<float2*>(cmb_s + lay.ml);      // [nbuf][k][H_q]
+  int32_t* bidx_s = reinterpret_cast<int32_t*>(cmb_s + lay.bidx);  // [nbuf][G][k]
+  float* cw = reinterpret_cast<float*>(cmb_s + lay.cw);            // [k][H_q] weights
+  uint8_t* use_s = cmb_s + lay.use;                                // [G][k]
+  const size_t ml_stride = (lay.bidx - lay.ml) / lay.nbuf / 8, bi_stride = (lay.cw - lay.bidx) / lay.nbuf / 4;
+  auto fetch = [&](int64_t tr, int buf) {  // (m, l) and block ids of position T0 + tr into buffer buf
+    const float2* pm = part_ml + tr * kh;
+    for (int i = tid; i < kh; i += kCombineThreads) cp_async_8(ml_s + buf * ml_stride + i, pm + i);
+    const int64_t t = T0 + tr;
+    for (int i = tid; i < gk; i += kCombineThreads)
+      cp_async_4(bidx_s + buf * bi_stride + i, block_idx + ((int64_t)(i / k) * N + t) * k + (i % k));
+    cp_async_commit();
+  };
+  const int64_t stride = gridDim.x;
+  int64_t tr = blockIdx.x;
+  if (lay.nbuf == 2 && tr < rows) fetch(tr, 0);
+  for (int it = 0; tr < rows; ++it, tr += stride) {
+    const int buf = lay.nbuf == 2 ? (it & 1) : 0;
+    const int64_t t = T0 + tr;
+    const uint16_t* po = part_o + tr * kh * D;
+    // the partial loads of this thread's first item do not need the weights: issue them first
+    uint4 v[kCombineSlots];
+    auto load_item = [&](int item, int s0) {
+      const int h = item / C8, c8 = item % C8;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll 2
-    for (int s = 0; s < k; ++s) {
-      const float w = cw[s * H_q + h];
-      if (w == 0.f) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(po + ((int64_t)s * H_q + h) * D + c8 * 8);
-      acc[0] = fmaf(w, bf16_lo(v.x), acc[0]);
-      acc[1] = fmaf(w, bf16_hi(v.x), acc[1]);
-      acc[2] = fmaf(w, bf16_lo(v.y), acc[2]);
-      acc[3] = fmaf(w, bf16_hi(v.y), acc[3]);
-      acc[4] = fmaf(w, bf16_lo(v.z), acc[4]);
-      acc[5] = fmaf(w, bf16_hi(v.z), acc[5]);
-      acc[6] = fmaf(w, bf16_lo(v.w), acc[6]);
-      acc[7] = fmaf(w, bf16_hi(v.w), acc[7]);
+      for (int j = 0; j < kCombineSlots; ++j)
+        if (s0 + j < k) v[j] = ldg_stream_16(po + ((int64_t)(s0 + j) * H_q + h) * D + c8 * 8);
+    };
+    if (tid < H_q * C8) load_item(tid, 0);
+    if (lay.nbuf == 1) fetch(tr, 0);
+    cp_async_wait<0>();
+    __syncthreads();
+    const float2* ml = ml_s + buf * ml_stride;
+    const int32_t* bi = bidx_s + buf * bi_stride;
+    for (int i = tid; i < gk; i += kCombineThreads) {  // slot s of group g counts iff valid and first of its id
+      const int g = i / k, sl = i % k;
+      const int32_t b = bi[i];
+      bool ok = b >= 0 && (int64_t)b < nb;
+      for (int s2 = 0; s2 < sl && ok; ++s2) ok = bi[g * k + s2] != b;
+      use_s[i] = ok ? 1 : 0;
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4*>(out + (t * H_q + h) * D + c8 * 8) = o;
+    __syncthreads();
+    if (lay.nbuf == 2 && tr + stride < rows) fetch(tr + stride, buf ^ 1);  // lands while this position streams
+    for (int h = tid; h < H_q; h += kCombineThreads) {
+      const uint8_t* use = use_s + (h / gs) * k;
+      float M = __int_as_float(0xff800000);
+      for (int sl = 0; sl < k; ++sl)
+        if (use[sl]) M = fmaxf(M, ml[sl * H_q + h].x);
+      float L = 0.f;
+      for (int sl = 0; sl < k; ++sl) {
+        const float e = use[sl] && M != __int_as_float(0xff800000) ? exp2f(ml[sl * H_q + h].x - M) : 0.f;
+        cw[sl * H_q + h] = e;
+        L += e * (use[sl] ? ml[sl * H_q + h].y : 0.f);
+      }
+      const float il = L > 0.f ? 1.f / L : 0.f;
+      for (int sl = 0; sl < k; ++sl) cw[sl * H_q + h] *= il;
+      lse[(int64_t)h * N + t] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : __int_as_float(0xff800000);
+    }
+    __syncthreads();
+    for (int item = tid; item < H_q * C8; item += kCombineThreads) {
+      const int h = item / C8, c8 = item % C8;
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int s0 = 0; s0 < k; s0 += kCombineSlots) {
+        if (item != tid || s0 != 0) load_item(item, s0);
+#pragma unroll
+        for (int j = 0; j < kCombineSlots; ++j) {
+          if (s0 + j >= k) break;
+          const float w = cw[(s0 + j) * H_q + h];
+          // unused slots may hold stale bits: zero them instead of multiplying by w = 0
+          const uint4 x = w != 0.f ? v[j] : make_uint4(0u, 0u, 0u, 0u);
+          acc[0] = fmaf(w, bf16_lo(x.x), acc[0]);
+          acc[1] = fmaf(w, bf16_hi(x.x), acc[1]);
+          acc[2] = fmaf(w, bf16_lo(x.y), acc[2]);
+          acc[3] = fmaf(w, bf16_hi(x.y), acc[3]);
+          acc[4] = fmaf(w, bf16_lo(x.z), acc[4]);
+          acc[5] = fmaf(w, bf16_hi(x.z), acc[5]);
+          acc[6] = fmaf(w, bf16_lo(x.w), acc[6]);
+          acc[7] = fmaf(w, bf16_hi(x.w), acc[7]);
+        }
+      }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(out + (t * H_q + h) * D + c8 * 8) = o;
+    }
+    __syncthreads();  // cw, use_s and this buffer are rewritten for the next position
   }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- scratch layout
@@ -312,14 +364,13 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
     e = launch_attn_tiles(q, k, v, sc.rec, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb, p.gs, T0,
                           p.slab * p.k, p.max_tiles, scale, sc.part_o, sc.part_ml, st, s);
     if (e != cudaSuccess) return e;
-    const size_t cs = (size_t)2 * p.k * p.H_q * sizeof(float);
+    const CombineSmem lay = combine_smem(p.k, p.H_q, G);
     auto ck = p.d == 64 ? combine_kernel<64> : combine_kernel<128>;
-    if (cs > 48 * 1024) {
-      e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cs);
-      if (e != cudaSuccess) return e;
-    }
-    ck<<<(unsigned)(T1 - T0), kCombineThreads, cs, s>>>(block_idx, sc.part_o, sc.part_ml, p.N, p.H_q, G, p.gs, p.k, p.nb, T0,
-                                            (uint16_t*)out, lse);
+    e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.total);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(T1 - T0, (int64_t)num_sms() * 2);
+    ck<<<(unsigned)grid, kCombineThreads, lay.total, s>>>(block_idx, sc.part_o, sc.part_ml, p.N, p.H_q, G, p.gs, p.k,
+                                                           p.nb, T0, T1 - T0, lay, (uint16_t*)out, lse);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
