@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-rows", type=int, default=512, help="oracle rows timed for cpu_baseline")
+    ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
     ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode"],
                     help="time one stage alone on --config (small-memory cases for profiler captures)")
     return ap.parse_args()
