@@ -21,13 +21,17 @@ def _check_bf16(name, t, shape):
 
 
 class MsaPrefill:
-    """One prefill layer step: select -> (invert + KV-outer attention + combine)."""
+    """One prefill layer step: select -> (invert + KV-outer attention + combine).
+
+    Calling the object runs msa_prefill (both stages in one call); ``select``
+    and ``attend`` run the two stages as separate calls."""
 
     def __init__(self, N, H_q, H_kv, d, d_I, Bk, k, device="cuda"):
         self.N, self.H_q, self.H_kv, self.d, self.d_I, self.Bk, self.k = N, H_q, H_kv, d, d_I, Bk, k
         self.G = H_kv
         self.shape = _c.shape(N, H_q, H_kv, d, d_I, Bk, k)
-        ws = max(_c.msa_select_blocks_workspace(N, self.G, d_I, Bk, k), _c.msa_sparse_attn_fwd_workspace(self.shape))
+        ws = max(_c.msa_select_blocks_workspace(N, self.G, d_I, Bk, k), _c.msa_sparse_attn_fwd_workspace(self.shape),
+                 _c.msa_prefill_workspace(self.shape))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
         self.block_idx = torch.empty((self.G, N, k), dtype=torch.int32, device=device)
         self.out = torch.empty((N, H_q, d), dtype=torch.bfloat16, device=device)
@@ -51,8 +55,9 @@ class MsaPrefill:
         _check_bf16("v", v, (N, self.H_kv, self.d))
         _check_bf16("q_idx", q_idx, (N, G, self.d_I))
         _check_bf16("k_idx", k_idx, (N, self.d_I))
-        self.select(q_idx, k_idx, stream)
-        self.attend(q, k, v, None, scale, stream)
+        scale = 1.0 / math.sqrt(self.d) if scale is None else scale
+        _c.msa_prefill(q, k, v, q_idx, k_idx, self.shape, scale, self.block_idx, self.out, self.lse, self.workspace,
+                       stream=stream)
         return self.out, self.lse, self.block_idx
 
     def device_status(self, stream=None):

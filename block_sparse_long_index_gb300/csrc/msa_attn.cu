@@ -346,6 +346,14 @@ AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k) {
 
 size_t attn_scratch_bytes(const AttnPlan& p) { return carve(p, nullptr, nullptr); }
 
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                           int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
+                           void* scratch, DeviceStatus* st, cudaStream_t s) {
+  cudaError_t e = launch_select(q_idx, k_idx, p.N, p.H_kv, d_I, p.Bk, p.k, block_idx, st, s);
+  if (e != cudaSuccess) return e;
+  return launch_attn(q, k, v, block_idx, p, scale, out, lse, scratch, st, s);
+}
+
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s) {
   AttnScratch sc;

@@ -201,6 +201,30 @@ msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
                                  (msa::DeviceStatus*)workspace, s));
 }
 
+size_t msa_prefill_workspace(const msa_shape_t* shape) {
+  if (check_shape(shape) != MSA_OK) return kHeader;
+  msa::AttnPlan p = msa::attn_plan(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
+  return kHeader + msa::attn_scratch_bytes(p);
+}
+
+msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                         const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  if (!q || !k || !v || !q_idx || !k_idx || !block_idx || !out || !lse) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      !aligned16(out) || ((uintptr_t)block_idx & 3u) || ((uintptr_t)lse & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_prefill_workspace(shape), s);
+  if (st != MSA_OK) return st;
+  msa::AttnPlan p = msa::attn_plan(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
+  return finish(msa::launch_prefill(q, k, v, q_idx, k_idx, shape->d_I, p, scale, block_idx, out, lse,
+                                    (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
+}
+
 size_t msa_decode_workspace(int B, const msa_shape_t* shape) {
   if (B < 1 || check_shape(shape) != MSA_OK) return kHeader;
   msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,

@@ -75,6 +75,10 @@ cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const
                               uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);
+// The select kernel followed by the attention call, on one stream.
+cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                           int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
+                           void* scratch, DeviceStatus* st, cudaStream_t s);
 
 // ---- decode (msa_decode.cu)
 struct DecodePlan {

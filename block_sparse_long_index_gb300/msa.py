@@ -43,6 +43,8 @@ _SIGS = {
     "msa_invert_blocks": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "msa_sparse_attn_fwd_workspace": (_SZ, [_SP]),
     "msa_sparse_attn_fwd": (_I, [_P, _P, _P, _P, _SP, _F, _P, _P, _P, _SZ, _P]),
+    "msa_prefill_workspace": (_SZ, [_SP]),
+    "msa_prefill": (_I, [_P, _P, _P, _P, _P, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_workspace": (_SZ, [_I, _SP]),
     "msa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P]),
@@ -124,6 +126,18 @@ def msa_sparse_attn_fwd(q, k, v, block_idx, shp, scale, out, lse, workspace, wor
     return _check(_lib.msa_sparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), ctypes.byref(shp),
                                            float(scale), _ptr(out), _ptr(lse), _ptr(workspace), wb,
                                            _stream(stream)), "msa_sparse_attn_fwd")
+
+
+def msa_prefill_workspace(shp):
+    return int(_lib.msa_prefill_workspace(ctypes.byref(shp)))
+
+
+def msa_prefill(q, k, v, q_idx, k_idx, shp, scale, block_idx, out, lse, workspace, workspace_bytes=None,
+                stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), ctypes.byref(shp),
+                                   float(scale), _ptr(block_idx), _ptr(out), _ptr(lse), _ptr(workspace), wb,
+                                   _stream(stream)), "msa_prefill")
 
 
 def msa_decode_workspace(B, shp):

@@ -136,6 +136,24 @@ msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
                                  const msa_shape_t* shape, float scale, void* out, float* lse,
                                  void* workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/* ---------------------------------------------------------------- prefill
+ * The whole forward pass in one call: msa_select_blocks followed by
+ * msa_sparse_attn_fwd on the same shapes and stream, with the same results.
+ * Pages: "MSA" study note 3-5 (the index and main branches as separate
+ * kernels feeding KV-outer attention and the two-phase combine); the pages
+ * give no fused entry point.
+ *
+ *   q, k, v, q_idx, k_idx, scale, out, lse: as msa_select_blocks and
+ *             msa_sparse_attn_fwd
+ *   block_idx [G, N, k] int32 out: the sets, as msa_select_blocks
+ *   workspace msa_prefill_workspace(shape) bytes, 256-byte aligned (one
+ *             workspace serves both stages)
+ */
+size_t msa_prefill_workspace(const msa_shape_t* shape);
+msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                         const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, msa_stream_t stream);
+
 /* ---------------------------------------------------------------- decode
  * One decode step for B sequences.  The query of sequence s sits at position
  * t = ctx_len[s] - 1 and its k, v and k^I are already in the caches.  The

@@ -125,6 +125,33 @@ def test_pipeline_select_then_attend(msa):
         compare_attn(o[:, heads][m], l[:, heads][m], ref[:, heads][m], ref_lse[:, heads][m])
 
 
+@pytest.mark.parametrize("N,H_q,H_kv,d,d_I,Bk,k", [(16384, 16, 4, 128, 128, 128, 8), (20000, 8, 2, 64, 64, 64, 5)])
+def test_prefill_call_equals_separate_calls(msa, N, H_q, H_kv, d, d_I, Bk, k):
+    """msa_prefill (both stages in one call) gives the same block sets, out and lse as
+    msa_select_blocks followed by msa_sparse_attn_fwd, also on a ragged N with a partial last block."""
+    cfg = datagen.make_config("slabs", N=N, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k, needles=2)
+    dev = datagen.prefill_device(cfg)
+    shp = msa.shape(N, H_q, H_kv, d, d_I, Bk, k)
+    scale = 1.0 / math.sqrt(d)
+    G = H_kv
+    ws_sel = torch.empty(msa.msa_select_blocks_workspace(N, G, d_I, Bk, k), dtype=torch.uint8, device="cuda")
+    blk_ref = torch.full((G, N, k), -7, dtype=torch.int32, device="cuda")
+    msa.msa_select_blocks(dev["q_idx"], dev["k_idx"], N, G, d_I, Bk, k, blk_ref, ws_sel)
+    out_ref, lse_ref, status = run_attn(msa, dev["q"], dev["k"], dev["v"], blk_ref, N, H_q, H_kv, d, d_I, Bk, k,
+                                        scale)
+    assert status == 0
+    ws = torch.empty(msa.msa_prefill_workspace(shp), dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace
+        blk = torch.full((G, N, k), -7, dtype=torch.int32, device="cuda")
+        out = torch.full((N, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((H_q, N), float("nan"), dtype=torch.float32, device="cuda")
+        msa.msa_prefill(dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"], shp, scale, blk, out, lse, ws)
+        assert msa.msa_check_device_error(ws) == 0
+        assert torch.equal(blk, blk_ref)
+        assert torch.equal(out, out_ref)
+        assert torch.equal(lse, lse_ref)
+
+
 def test_attention_dense_special_case(msa):
     """k >= number of blocks: MSA equals dense causal GQA attention."""
     N, H_q, H_kv, d, Bk = 1100, 8, 2, 64, 64
