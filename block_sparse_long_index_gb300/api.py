@@ -113,3 +113,66 @@ def prefill_from_host(run: MsaPrefill, host_inputs, dev_inputs, host_out, stream
     host_out["out"].copy_(out, non_blocking=True)
     host_out["lse"].copy_(lse, non_blocking=True)
     return host_out
+
+
+class PrefillHostPipeline:
+    """Prefill steps from pinned host buffers to pinned host buffers, with the copies overlapped.
+
+    Three streams: host->device copies, compute, device->host copies.  Step i's
+    inputs land in one of two device input sets while step i-1 computes on the
+    other; its index inputs (q_idx, k_idx) are copied first so that the select
+    can start while q, k and v are still in flight; out and lse of step i are
+    copied back while step i+1 runs.  Every step still copies all of its inputs
+    in and all of its outputs (out, lse) out."""
+
+    NAMES = ("q_idx", "k_idx", "q", "k", "v")
+
+    def __init__(self, run: MsaPrefill, device="cuda"):
+        self.run = run
+        self.dev = [{n: torch.empty(_input_shape(run, n), dtype=torch.bfloat16, device=device) for n in self.NAMES}
+                    for _ in range(2)]
+        self.h2d, self.d2h = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+
+    def __call__(self, host_inputs, host_outputs, stream=None):
+        """host_inputs: list of dicts of pinned bf16 tensors (q, k, v, q_idx, k_idx), one per step;
+        host_outputs: list of dicts of pinned tensors (out, lse), one per step.  Returns once the
+        work is queued; it is ordered before later work on `stream` (default: the current stream)."""
+        comp = torch.cuda.current_stream() if stream is None else stream
+        E = torch.cuda.Event
+        self.h2d.wait_stream(comp)
+        self.d2h.wait_stream(comp)
+        attn_done, d2h_done = {}, {}
+        for i, (hin, hout) in enumerate(zip(host_inputs, host_outputs)):
+            dev = self.dev[i % 2]
+            idx_in, qkv_in = E(), E()
+            with torch.cuda.stream(self.h2d):
+                if i - 2 in attn_done:  # the attention of step i-2 has finished reading this input set
+                    self.h2d.wait_event(attn_done[i - 2])
+                for n in ("q_idx", "k_idx"):
+                    dev[n].copy_(hin[n], non_blocking=True)
+                idx_in.record(self.h2d)
+                for n in ("q", "k", "v"):
+                    dev[n].copy_(hin[n], non_blocking=True)
+                qkv_in.record(self.h2d)
+            comp.wait_event(idx_in)
+            self.run.select(dev["q_idx"], dev["k_idx"], stream=comp)
+            comp.wait_event(qkv_in)
+            if i - 1 in d2h_done:  # out and lse of step i-1 are on the host before they are rewritten
+                comp.wait_event(d2h_done[i - 1])
+            self.run.attend(dev["q"], dev["k"], dev["v"], stream=comp)
+            attn_done[i] = E()
+            attn_done[i].record(comp)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(attn_done[i])
+                hout["out"].copy_(self.run.out, non_blocking=True)
+                hout["lse"].copy_(self.run.lse, non_blocking=True)
+                d2h_done[i] = E()
+                d2h_done[i].record(self.d2h)
+        comp.wait_stream(self.h2d)
+        comp.wait_stream(self.d2h)
+        return host_outputs
+
+
+def _input_shape(run: MsaPrefill, name):
+    return {"q": (run.N, run.H_q, run.d), "k": (run.N, run.H_kv, run.d), "v": (run.N, run.H_kv, run.d),
+            "q_idx": (run.N, run.G, run.d_I), "k_idx": (run.N, run.d_I)}[name]

@@ -152,6 +152,32 @@ def test_prefill_call_equals_separate_calls(msa, N, H_q, H_kv, d, d_I, Bk, k):
         assert torch.equal(lse, lse_ref)
 
 
+def test_host_pipeline_matches_device_calls():
+    """PrefillHostPipeline (copies overlapped with compute across steps, two device input sets) returns,
+    for each of three steps with different inputs, exactly the device-path outputs of that step."""
+    from block_sparse_long_index_gb300 import MsaPrefill
+    from block_sparse_long_index_gb300.api import PrefillHostPipeline
+    names = ("q", "k", "v", "q_idx", "k_idx")
+    cfgs = [datagen.make_config("hostpipe%d" % i, index=200 + i, N=2048, H_q=8, H_kv=2, d=64, d_I=64, Bk=64, k=6,
+                                needles=2)
+            for i in range(3)]
+    run = MsaPrefill(2048, 8, 2, 64, 64, 64, 6)
+    hosts, refs = [], []
+    for cfg in cfgs:
+        dev = datagen.prefill_device(cfg, want=names)
+        out, lse, _ = run(dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"])
+        refs.append((out.cpu(), lse.cpu()))
+        hosts.append({n: dev[n].cpu().pin_memory() for n in names})
+    houts = [{"out": torch.empty(run.out.shape, dtype=run.out.dtype).pin_memory(),
+              "lse": torch.empty(run.lse.shape, dtype=run.lse.dtype).pin_memory()} for _ in range(3)]
+    PrefillHostPipeline(run)(hosts, houts)
+    torch.cuda.synchronize()
+    assert run.device_status() == 0
+    for (ro, rl), h in zip(refs, houts):
+        assert torch.equal(h["out"], ro)
+        assert torch.equal(h["lse"], rl)
+
+
 def test_attention_dense_special_case(msa):
     """k >= number of blocks: MSA equals dense causal GQA attention."""
     N, H_q, H_kv, d, Bk = 1100, 8, 2, 64, 64
