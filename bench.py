@@ -268,6 +268,8 @@ def bench_prefill(args, dist, torch, peaks):
 
 
 def bench_decode(args, dist, torch):
+    import numpy as np
+
     import datagen
     from block_sparse_long_index_gb300 import MsaDecode
     cfg = datagen.CONFIGS[args.decode_config]
@@ -295,6 +297,32 @@ def bench_decode(args, dist, torch):
     times = sorted(a.elapsed_time(b) for a, b in ev)
     mean_ms = sum(times) / K
     res = dict(cfg=cfg, mean_ms=mean_ms, median_ms=times[K // 2], steps=K)
+    # the same step over paged caches: the caches viewed as a pool of 128-token pages, each sequence's
+    # pages scattered by a random page table (the bytes read are the same, in page order)
+    from block_sparse_long_index_gb300 import msa
+    page = 128
+    mp = cfg.ctx // page
+    n_pages = cfg.B * mp
+    perm = torch.from_numpy(np.random.default_rng(11).permutation(n_pages).astype(np.int32)).view(cfg.B, mp).cuda()
+    pools = (inp["k_idx_cache"].view(n_pages, page, cfg.d_I), inp["k_cache"].view(n_pages, page, cfg.H_kv, cfg.d),
+             inp["v_cache"].view(n_pages, page, cfg.H_kv, cfg.d))
+    scale = 1.0 / math.sqrt(cfg.d)
+    paged = lambda: msa.msa_decode_paged(inp["q_t"], inp["q_idx_t"], pools[0], pools[1], pools[2], perm, mp,  # noqa
+                                         n_pages, page, inp["ctx_len"], cfg.B, run.shape, scale, run.out, run.lse,
+                                         run.block_idx, run.workspace)
+    for _ in range(args.warmup):
+        paged()
+    torch.cuda.synchronize()
+    evp = [(E(), E()) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        evp[i][0].record(stream)
+        paged()
+        evp[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert run.device_status() == 0
+    tp = sorted(a.elapsed_time(b) for a, b in evp)
+    res["paged"] = dict(mean_ms=sum(tp) / K, median_ms=tp[K // 2], page=page)
     del inp, run, flush
     torch.cuda.empty_cache()
     return res
@@ -490,6 +518,17 @@ def main():
                                                       % bytes_step,
                                        "peak_source": "%s hbm_gbs" % peak_src},
                           "gpu_launches": 2 * dec["steps"]}
+        pg = dec["paged"]
+        pg_ms = dist.max(pg["mean_ms"])
+        pbw = bytes_step / (pg_ms / 1000.0) / 1e9
+        line["decode_paged"] = {"metric": "decode tokens/s at 1M ctx, paged caches (msa_decode_paged)",
+                                "value": ws * dcfg.B / (pg_ms / 1000.0), "unit": "tokens/s", "ms_per_step": pg_ms,
+                                "median_ms": pg["median_ms"], "page_tokens": pg["page"],
+                                "workload": workload_name(dcfg) + ", pages scattered by a random page table",
+                                "roofline": {"bound": "hbm", "achieved": pbw, "peak": hbm, "unit": "GB/s",
+                                             "frac": pbw / hbm, "traffic": None,
+                                             "peak_source": "%s hbm_gbs" % peak_src},
+                                "gpu_launches": 2 * dec["steps"]}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         dt, n, th = oracle_prefill_sample(cfg, args.cpu_rows)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",

@@ -255,6 +255,38 @@ msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_
                                    block_idx, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
 }
 
+msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* k_idx_pool, const void* k_pool,
+                              const void* v_pool, const int32_t* page_table, int64_t max_pages, int64_t n_pages,
+                              int page_size, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                              void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                              msa_stream_t stream) {
+  if (!q_t || !q_idx_t || !k_idx_pool || !k_pool || !v_pool || !page_table || !ctx_len || !out)
+    return MSA_ERR_INVALID_ARGUMENT;
+  if (B < 1 || max_pages < 1 || n_pages < 1 || page_size < 16 || page_size % 16 != 0) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (shape->N != max_pages * (int64_t)page_size) return MSA_ERR_INVALID_ARGUMENT;  // capacity of a sequence
+  if (shape->H_kv > 8) return MSA_ERR_UNSUPPORTED;
+  if (n_pages > (int64_t)1 << 31) return MSA_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q_t) || !aligned16(q_idx_t) || !aligned16(k_idx_pool) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      ((uintptr_t)page_table & 3u) || ((uintptr_t)ctx_len & 3u) || ((uintptr_t)out & 1u) || ((uintptr_t)lse & 3u) ||
+      ((uintptr_t)block_idx & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,
+                                       shape->k);
+  st = begin(workspace, workspace_bytes, msa_decode_workspace(B, shape), s, kHeader + msa::decode_clear_bytes(p));
+  if (st != MSA_OK) return st;
+  msa::CacheMap map;
+  map.table = page_table;
+  map.max_pages = max_pages;
+  map.n_pages = n_pages;
+  map.page = page_size;
+  return finish(msa::launch_decode(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, ctx_len, p, scale, out, lse, block_idx,
+                                   (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s, &map));
+}
+
 // The decode step without a caller workspace: its scratch is the library's
 // fixed device array (see msa_decode.cu), so this call allocates nothing.
 msa_status_t msa_decode_noalloc(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,

@@ -29,6 +29,16 @@ __device__ __forceinline__ void raise_error(DeviceStatus* st, unsigned int flag,
   if (old == 0) atomicExch(&st->first_code, code);
 }
 
+__device__ __forceinline__ int64_t CacheMap::row(int64_t seq, int64_t key, DeviceStatus* st) const {
+  const int64_t lp = key / page;
+  int32_t pp = __ldg(table + seq * max_pages + lp);
+  if (pp < 0 || (int64_t)pp >= n_pages) {
+    raise_error(st, kErrBadIndex, 3u);
+    pp = 0;
+  }
+  return (int64_t)pp * page + (key - lp * page);
+}
+
 // ------------------------------------------------------------------ bf16
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

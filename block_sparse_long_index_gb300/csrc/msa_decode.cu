@@ -63,11 +63,12 @@ __device__ __forceinline__ void load_keys16(uint4 (&v)[DI / 32][2], const uint16
 // the candidates are the blocks before the query's local block.  The CTA's
 // 16-key chunks are divided evenly among its warps; a block whose chunks fall
 // to two warps gets its maximum from both through the shared-memory atomic.
-template <int DI, int BK>
+template <int DI, int BK, bool PAGED>
 __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     const uint16_t* __restrict__ q_idx_t, const uint16_t* __restrict__ k_idx_cache,
-    const int32_t* __restrict__ ctx_len, int64_t ctx_max, int G, int k, int splits, uint64_t* __restrict__ cand,
-    unsigned int* __restrict__ tickets, int32_t* __restrict__ block_idx, DeviceStatus* st) {
+    const int32_t* __restrict__ ctx_len, int64_t ctx_max, CacheMap map, int G, int k, int splits,
+    uint64_t* __restrict__ cand, unsigned int* __restrict__ tickets, int32_t* __restrict__ block_idx,
+    DeviceStatus* st) {
   constexpr int KS = DI / 16;
   constexpr int CPB = BK / 16;  // chunks per block
   extern __shared__ uint32_t bmax_s[];  // [blocks of this CTA][8 groups], ordered_bits of the block maxima
@@ -109,6 +110,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   const int64_t nch = (int64_t)nblk * CPB;
   const int64_t c0 = nch * warp / kScanWarps, c1 = nch * (warp + 1) / kScanWarps;
   const uint16_t* base = k_idx_cache + ((int64_t)seq * ctx_max + b_lo * BK + row) * DI + 8 * c;
+  // first key row of chunk cc (+ row): contiguous, or through the page table (a page holds whole chunks)
+  auto chunk_ptr = [&](int64_t cc) -> const uint16_t* {
+    if (!PAGED) return base + cc * 16 * DI;
+    const int64_t key = b_lo * BK + cc * 16;
+    const int64_t r = map.row(seq, key, st);
+    return k_idx_cache + (r + row) * DI + 8 * c;
+  };
   float bm0 = __int_as_float(0xff800000), bm1 = bm0;
   auto score = [&](const uint4 (&v)[DI / 32][2], int64_t cc) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -135,12 +143,12 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     }
   };
   uint4 va[DI / 32][2], vb[DI / 32][2];
-  if (c0 < c1) load_keys16<DI>(va, base + c0 * 16 * DI);
+  if (c0 < c1) load_keys16<DI>(va, chunk_ptr(c0));
   for (int64_t ci = c0; ci < c1; ci += 2) {  // one chunk in flight ahead of the one being scored
-    if (ci + 1 < c1) load_keys16<DI>(vb, base + (ci + 1) * 16 * DI);
+    if (ci + 1 < c1) load_keys16<DI>(vb, chunk_ptr(ci + 1));
     score(va, ci);
     if (ci + 1 < c1) {
-      if (ci + 2 < c1) load_keys16<DI>(va, base + (ci + 2) * 16 * DI);
+      if (ci + 2 < c1) load_keys16<DI>(va, chunk_ptr(ci + 2));
       score(vb, ci + 1);
     }
   }
@@ -230,20 +238,22 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
 // The last CTA of a (sequence, group) to finish merges the group's k partials
 // per head: M = max lse_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
 // out = sum w_s O_s, lse = M + ln sum e^(lse_s - M).
-template <int D, int BK>
+template <int D, int BK, bool PAGED>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __restrict__ q_t,
                                                           const uint16_t* __restrict__ k_cache,
                                                           const uint16_t* __restrict__ v_cache,
                                                           const int32_t* __restrict__ ctx_len,
                                                           const int32_t* __restrict__ block_idx, int64_t ctx_max,
-                                                          int H_q, int G, int k, float scale,
+                                                          CacheMap map, int H_q, int G, int k, float scale,
                                                           float* __restrict__ part_o, float* __restrict__ part_lse,
                                                           unsigned int* __restrict__ tickets,
-                                                          uint16_t* __restrict__ out, float* __restrict__ lse) {
+                                                          uint16_t* __restrict__ out, float* __restrict__ lse,
+                                                          DeviceStatus* st) {
   extern __shared__ __align__(16) uint16_t v_s[];  // V rows [BK][D]; later the warps' partial O
   __shared__ float red_m[4][8], red_l[4][8];
   __shared__ float w_s[8][32];  // combine weights [head][slot]
   __shared__ int s_last;
+  __shared__ int64_t krow_s[PAGED ? BK : 1];  // cache row of each key of the block (paged caches)
   constexpr int C8 = D / 8;     // 16-byte chunks per row
   constexpr int KPW = BK / 4;   // keys per warp
   constexpr int NT = KPW / 8;   // 8-key n-tiles per warp
@@ -277,13 +287,20 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     for (int hh = tid; hh < gs; hh += blockDim.x) pl[(int64_t)hh * k] = __int_as_float(0xff800000);
   } else {
     const int64_t kv_row = (int64_t)G * D;
-    const uint16_t* Kb = k_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
-    const uint16_t* Vb = v_cache + ((int64_t)seq * ctx_max + key0) * kv_row + (int64_t)g * D;
+    // key j of the block: row key0 + j of this sequence's cache, or row krow_s[j] of the page pool
+    const int64_t first = PAGED ? 0 : (int64_t)seq * ctx_max + key0;
+    const uint16_t* Kb = k_cache + first * kv_row + (int64_t)g * D;
+    const uint16_t* Vb = v_cache + first * kv_row + (int64_t)g * D;
+    if (PAGED) {
+      for (int j = tid; j < BK; j += blockDim.x) krow_s[j] = j < nvis ? map.row(seq, key0 + j, st) : 0;
+      __syncthreads();
+    }
+    auto row_off = [&](int j) -> int64_t { return (PAGED ? krow_s[PAGED ? j : 0] : (int64_t)j) * kv_row; };
     // V rows into shared memory (rows past nvis read as zero), every copy in flight at once
     for (int i = tid; i < BK * C8; i += blockDim.x) {
       const int j = i / C8, c8 = i % C8;
       const bool in = j < nvis;
-      cp_async_16(v_s + j * D + (c8 ^ (j & (C8 - 1))) * 8, Vb + (int64_t)(in ? j : 0) * kv_row + c8 * 8, in ? 16 : 0);
+      cp_async_16(v_s + j * D + (c8 ^ (j & (C8 - 1))) * 8, Vb + row_off(in ? j : 0) + c8 * 8, in ? 16 : 0);
     }
     cp_async_commit();
     // K rows of this warp's keys as B fragments (key = column gq of n-tile nt); rows past nvis repeat a
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int j = min(warp * KPW + nt * 8 + gq, nvis - 1);
-      const uint16_t* kr = Kb + (int64_t)j * kv_row + 8 * tq;
+      const uint16_t* kr = Kb + row_off(j) + 8 * tq;
 #pragma unroll
       for (int p = 0; p < NP; ++p) kf[nt][p] = ldg_stream_16(kr + 32 * p);
     }
@@ -471,27 +488,36 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   return off;
 }
 
-template <int DI, int BK>
-cudaError_t launch_scan(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const DecodePlan& p,
-                        const DecodeScratch& sc, int32_t* blk, DeviceStatus* st, cudaStream_t s) {
+template <int DI, int BK, bool PAGED>
+cudaError_t launch_scan_t(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
+                          const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
+                          cudaStream_t s) {
   const size_t smem = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
-  cudaError_t e = cudaFuncSetAttribute(decode_scan_kernel<DI, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  auto kern = decode_scan_kernel<DI, BK, PAGED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_scan_kernel<DI, BK><<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
-      (const uint16_t*)q_idx_t, (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max, p.H_kv, p.k, p.splits, sc.cand,
-      sc.tickets, blk, st);
+  kern<<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
+      (const uint16_t*)q_idx_t, (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits,
+      sc.cand, sc.tickets, blk, st);
   return cudaGetLastError();
+}
+
+template <int DI, int BK>
+cudaError_t launch_scan(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
+                        const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st, cudaStream_t s) {
+  return map.table ? launch_scan_t<DI, BK, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                   : launch_scan_t<DI, BK, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
 }
 
 // The attention grid as a programmatic dependent of the scan: its CTAs may be
 // scheduled while the scan drains and wait (griddepcontrol.wait) for its results.
-template <int D, int BK>
-cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
-                            const int32_t* blk, const DecodePlan& p, float scale, const DecodeScratch& sc, void* out,
-                            float* lse, cudaStream_t s) {
+template <int D, int BK, bool PAGED>
+cudaError_t launch_attn_dep_t(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
+                              const int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
+                              const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
   const int smem = BK * D * 2;  // V rows of one block
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = decode_attn_kernel<D, BK, PAGED>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.k, (unsigned)p.H_kv, (unsigned)p.B);
@@ -503,9 +529,19 @@ cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<D, BK>, (const uint16_t*)q_t, (const uint16_t*)k_cache,
-                            (const uint16_t*)v_cache, ctx_len, (const int32_t*)blk, p.ctx_max, p.H_q, p.H_kv, p.k,
-                            scale, sc.part_o, sc.part_lse, sc.tickets + p.B, (uint16_t*)out, lse);
+  return cudaLaunchKernelEx(&cfg, kern, (const uint16_t*)q_t, (const uint16_t*)k_cache, (const uint16_t*)v_cache,
+                            ctx_len, (const int32_t*)blk, p.ctx_max, map, p.H_q, p.H_kv, p.k, scale, sc.part_o,
+                            sc.part_lse, sc.tickets + p.B, (uint16_t*)out, lse, st);
+}
+
+template <int D, int BK>
+cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
+                            const int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
+                            const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
+  return map.table ? launch_attn_dep_t<D, BK, true>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse,
+                                                     st, s)
+                   : launch_attn_dep_t<D, BK, false>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out,
+                                                      lse, st, s);
 }
 
 }  // namespace
@@ -541,27 +577,29 @@ size_t decode_clear_bytes(const DecodePlan& p) { return ticket_bytes(p); }
 
 cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
                           const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
-                          float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s) {
+                          float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s,
+                          const CacheMap* paged) {
+  const CacheMap map = paged ? *paged : CacheMap{};
   DecodeScratch sc;
   carve(p, scratch, &sc);
   int32_t* blk = block_idx ? block_idx : sc.blk;
   cudaError_t e;
   if (p.d_I == 32) {
-    e = p.Bk == 64 ? launch_scan<32, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
-                   : launch_scan<32, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<32, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                   : launch_scan<32, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
   } else if (p.d_I == 64) {
-    e = p.Bk == 64 ? launch_scan<64, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
-                   : launch_scan<64, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<64, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                   : launch_scan<64, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
   } else {
-    e = p.Bk == 64 ? launch_scan<128, 64>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s)
-                   : launch_scan<128, 128>(q_idx_t, k_idx_cache, ctx_len, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<128, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                   : launch_scan<128, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
   }
   if (e != cudaSuccess) return e;
   if (p.d == 64)
-    return p.Bk == 64 ? launch_attn_dep<64, 64>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s)
-                      : launch_attn_dep<64, 128>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s);
-  return p.Bk == 64 ? launch_attn_dep<128, 64>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s)
-                    : launch_attn_dep<128, 128>(q_t, k_cache, v_cache, ctx_len, blk, p, scale, sc, out, lse, s);
+    return p.Bk == 64 ? launch_attn_dep<64, 64>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s)
+                      : launch_attn_dep<64, 128>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s);
+  return p.Bk == 64 ? launch_attn_dep<128, 64>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s)
+                    : launch_attn_dep<128, 128>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s);
 }
 
 // ---------------------------------------------------------------- fixed scratch for msa_decode_noalloc

@@ -81,6 +81,19 @@ cudaError_t launch_prefill(const void* q, const void* k, const void* v, const vo
                            void* scratch, DeviceStatus* st, cudaStream_t s);
 
 // ---- decode (msa_decode.cu)
+// Where token `key` of sequence `seq` sits in a decode cache: contiguous (no
+// table: row seq * ctx_max + key) or paged (row table[seq][key / page] * page +
+// key % page of a pool of n_pages pages; page a multiple of 16 tokens).
+struct CacheMap {
+  const int32_t* table = nullptr;  // [B, max_pages] physical page of each logical page
+  int64_t max_pages = 0;
+  int64_t n_pages = 0;
+  int page = 0;
+#ifdef __CUDACC__
+  // a page id outside [0, n_pages) sets the device error word and reads page 0
+  __device__ __forceinline__ int64_t row(int64_t seq, int64_t key, DeviceStatus* st) const;
+#endif
+};
 struct DecodePlan {
   int B;
   int64_t ctx_max;
@@ -95,7 +108,8 @@ size_t decode_scratch_bytes(const DecodePlan& p);
 size_t decode_clear_bytes(const DecodePlan& p);
 cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
                           const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
-                          float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s);
+                          float* lse, int32_t* block_idx, void* scratch, DeviceStatus* st, cudaStream_t s,
+                          const CacheMap* paged = nullptr);
 
 // Fixed device scratch of msa_decode_noalloc (8 MiB, shared by all calls on a
 // device).  Returns its device address for the current device (looked up on

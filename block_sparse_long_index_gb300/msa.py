@@ -47,6 +47,7 @@ _SIGS = {
     "msa_prefill": (_I, [_P, _P, _P, _P, _P, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_workspace": (_SZ, [_I, _SP]),
     "msa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
+    "msa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P]),
     "msa_check_device_error": (_I, [_P, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I]),
@@ -150,6 +151,15 @@ def msa_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shp, sca
     return _check(_lib.msa_decode(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_cache), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(ctx_len), B, ctypes.byref(shp), float(scale), _ptr(out), _ptr(lse),
                                   _ptr(block_idx), _ptr(workspace), wb, _stream(stream)), "msa_decode")
+
+
+def msa_decode_paged(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, page_table, max_pages, n_pages, page_size, ctx_len,
+                     B, shp, scale, out, lse, block_idx, workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_decode_paged(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_pool), _ptr(k_pool), _ptr(v_pool),
+                                        _ptr(page_table), int(max_pages), int(n_pages), int(page_size), _ptr(ctx_len),
+                                        B, ctypes.byref(shp), float(scale), _ptr(out), _ptr(lse), _ptr(block_idx),
+                                        _ptr(workspace), wb, _stream(stream)), "msa_decode_paged")
 
 
 def msa_decode_noalloc(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shp, scale, out, lse, block_idx,

@@ -181,6 +181,33 @@ msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_
                         void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
                         msa_stream_t stream);
 
+/* ---------------------------------------------------------------- paged decode
+ * msa_decode over caches kept in pages: sequence s's token j is row
+ * page_table[s][j / page_size] * page_size + j % page_size of the page pools,
+ * so sequences of different lengths share one pool without a dense
+ * [B, capacity] layout.  Same selection, attention and outputs as msa_decode
+ * on the caches the pages spell out.  Pages: velog llama.cpp analysis, section
+ * 4 (a per-sequence position -> cache cell -> block map is what lets a decode
+ * kernel serve several sequences of different lengths, where the analysed
+ * port falls back to one dense unified cache).
+ *
+ *   k_idx_pool  [n_pages, page_size, d_I] bf16
+ *   k_pool      [n_pages, page_size, H_kv, d] bf16, v_pool likewise
+ *   page_table  [B, max_pages] int32 (device): physical page of each logical
+ *               page; entries past a sequence's ctx_len are not read
+ *   page_size   tokens per page, a positive multiple of 16
+ *   shape->N    = max_pages * page_size (a sequence's capacity)
+ *   workspace   msa_decode_workspace(B, shape) bytes
+ *   the rest as msa_decode.
+ * A page id read outside [0, n_pages) sets the device error word (reported as
+ * MSA_ERR_BAD_INDEX) and page 0 is read in its place.
+ */
+msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* k_idx_pool, const void* k_pool,
+                              const void* v_pool, const int32_t* page_table, int64_t max_pages, int64_t n_pages,
+                              int page_size, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                              void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                              msa_stream_t stream);
+
 /* ---------------------------------------------------------------- decode without allocation
  * The same decode step as msa_decode, for callers that cannot allocate device
  * memory: for instance a plugin whose host application owns every byte of the

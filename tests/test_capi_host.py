@@ -93,3 +93,26 @@ def test_invert_validation(lib):
     assert raw.msa_invert_blocks(FAKE, 100, 1, 64, 4, FAKE, FAKE, FAKE, FAKE, 1, None) == \
         lib.MSA_ERR_WORKSPACE_TOO_SMALL
     assert lib.msa_invert_blocks_workspace(1 << 20, 8, 128, 16) > 256
+
+
+def test_prefill_and_paged_decode_validation(lib):
+    raw = lib.raw()
+    s = lib.shape(4096, 16, 2, 128, 128, 128, 16)
+    need = lib.msa_prefill_workspace(s)
+    assert need >= lib.msa_sparse_attn_fwd_workspace(s)
+    assert raw.msa_prefill(FAKE, FAKE, FAKE, None, FAKE, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, FAKE, need,
+                           None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, FAKE, need - 256,
+                           None) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    # paged decode: capacity = max_pages * page_size, page_size a multiple of 16
+    d = lib.shape(64 * 128, 16, 2, 128, 128, 128, 8)
+    ws = lib.msa_decode_workspace(2, d)
+    args = lambda mp, npg, ps, wsb: (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, mp, npg, ps, FAKE, 2, ctypes.byref(d), 0.1,  # noqa
+                                     FAKE, None, None, FAKE, wsb, None)
+    assert raw.msa_decode_paged(*args(64, 200, 120, ws)) == lib.MSA_ERR_INVALID_ARGUMENT  # 120 % 16 != 0
+    assert raw.msa_decode_paged(*args(32, 200, 128, ws)) == lib.MSA_ERR_INVALID_ARGUMENT  # 32 * 128 != N
+    assert raw.msa_decode_paged(*args(64, 0, 128, ws)) == lib.MSA_ERR_INVALID_ARGUMENT    # empty pool
+    assert raw.msa_decode_paged(*args(64, 200, 128, ws - 256)) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    big = lib.shape(64 * 128, 64, 16, 128, 128, 128, 8)  # more than 8 groups
+    assert raw.msa_decode_paged(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 200, 128, FAKE, 2, ctypes.byref(big), 0.1,
+                                FAKE, None, None, FAKE, 1 << 40, None) == lib.MSA_ERR_UNSUPPORTED

@@ -310,6 +310,77 @@ def test_decode_parity(msa, case):
     assert same.mean() >= 0.75
 
 
+def _paged(cache, page, n_extra, rng):
+    """Scatter a contiguous [B, C, ...] cache into a page pool with a random page table (plus unused pages)."""
+    B, C = cache.shape[:2]
+    mp = C // page
+    n_pages = B * mp + n_extra
+    perm = torch.from_numpy(rng.permutation(n_pages)[:B * mp].astype(np.int64)).view(B, mp)
+    pool = torch.zeros((n_pages, page) + tuple(cache.shape[2:]), dtype=cache.dtype, device=cache.device)
+    pool[perm.to(cache.device)] = cache.view((B, mp, page) + tuple(cache.shape[2:]))
+    return pool, perm.to(torch.int32).cuda(), mp, n_pages
+
+
+@pytest.mark.parametrize("page", [16, 64, 128, 512])
+def test_decode_paged_equals_contiguous(msa, page):
+    """msa_decode_paged on pools scattered by a random page table gives exactly msa_decode's results on the
+    contiguous caches (same sets, out and lse), with ragged lengths that end inside a page and a block."""
+    B, C, H_q, H_kv, d, d_I, Bk, k = 3, 4096, 16, 4, 128, 128, 128, 8
+    cfg = datagen.make_config("paged", kind="decode", B=B, ctx=C, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k,
+                              needles=2)
+    ctx_len = np.array([4096, 3001, 77], np.int64)
+    inp = datagen.decode_host(cfg, ctx_len)
+    q_t, q_idx_t = dev_bf16(inp["q_t"]), dev_bf16(inp["q_idx_t"])
+    kic, kc, vc = dev_bf16(inp["k_idx_cache"]), dev_bf16(inp["k_cache"]), dev_bf16(inp["v_cache"])
+    lens = torch.from_numpy(ctx_len.astype(np.int32)).cuda()
+    shp = msa.shape(C, H_q, H_kv, d, d_I, Bk, k)
+    scale = 1 / math.sqrt(d)
+    ws = torch.empty(msa.msa_decode_workspace(B, shp), dtype=torch.uint8, device="cuda")
+    outs = []
+    for paged in (False, True):
+        out = torch.full((B, H_q, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((B, H_q), float("nan"), dtype=torch.float32, device="cuda")
+        blk = torch.full((B, H_kv, k), -7, dtype=torch.int32, device="cuda")
+        if paged:
+            rng = np.random.default_rng(page)
+            kip, table, mp, n_pages = _paged(kic, page, 5, rng)
+            rng = np.random.default_rng(page)  # the same table for the K/V pools
+            kp, _, _, _ = _paged(kc, page, 5, rng)
+            rng = np.random.default_rng(page)
+            vp, _, _, _ = _paged(vc, page, 5, rng)
+            msa.msa_decode_paged(q_t, q_idx_t, kip, kp, vp, table, mp, n_pages, page, lens, B, shp, scale, out, lse,
+                                 blk, ws)
+        else:
+            msa.msa_decode(q_t, q_idx_t, kic, kc, vc, lens, B, shp, scale, out, lse, blk, ws)
+        assert msa.msa_check_device_error(ws) == 0
+        outs.append((out, lse, blk))
+    (o0, l0, b0), (o1, l1, b1) = outs
+    assert torch.equal(b0, b1)
+    assert torch.equal(o0, o1)
+    assert torch.equal(l0, l1)
+
+
+def test_decode_paged_bad_page_id_is_flagged(msa):
+    """A page id outside the pool sets MSA_ERR_BAD_INDEX (page 0 is read instead; nothing faults)."""
+    B, C, H_q, H_kv, d, d_I, Bk, k, page = 1, 1024, 8, 2, 64, 64, 64, 4, 64
+    cfg = datagen.make_config("paged_bad", kind="decode", B=B, ctx=C, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k,
+                              needles=0)
+    dev = datagen.decode_device(cfg)
+    mp = C // page
+    table = torch.arange(mp, dtype=torch.int32, device="cuda").view(1, mp).clone()
+    table[0, 3] = mp + 100  # beyond the pool of mp pages
+    shp = msa.shape(C, H_q, H_kv, d, d_I, Bk, k)
+    ws = torch.empty(msa.msa_decode_workspace(B, shp), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, H_q, d), dtype=torch.bfloat16, device="cuda")
+    lens = torch.full((B,), C, dtype=torch.int32, device="cuda")
+    kip = dev["k_idx_cache"].view(mp, page, d_I)
+    kp = dev["k_cache"].view(mp, page, H_kv, d)
+    vp = dev["v_cache"].view(mp, page, H_kv, d)
+    msa.msa_decode_paged(dev["q_t"], dev["q_idx_t"], kip, kp, vp, table, mp, mp, page, lens, B, shp, 0.125, out, None,
+                         None, ws)
+    assert msa.msa_check_device_error(ws) == msa.MSA_ERR_BAD_INDEX
+
+
 def test_datagen_device_matches_host():
     """The in-place device generator reproduces the host generator bit for bit."""
     cfg = datagen.make_config("dgchk", N=4096, H_q=8, H_kv=2, d=64, d_I=128, Bk=128, k=8, needles=3)
