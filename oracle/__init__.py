@@ -1,6 +1,6 @@
 """ORACLE — test infrastructure only.
 
-A plain, slow fp64 CPU statement of the MSA forward path (``msa_oracle.c``),
+A plain, slow fp64 CPU statement of the MSA forward path and its backward (``msa_oracle.c``),
 loaded through ctypes.  Only the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package; the product library
 never does, and the two share no code.  Inputs are bf16 bit patterns
@@ -47,8 +47,10 @@ def _load():
         lib.msa_ref_sparse_attn.argtypes = [P, P, P, P, P, I64, I64, I, I, I, I, I, D, P, P, I]
         lib.msa_ref_dense_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, D, P, P, I]
         lib.msa_ref_decode.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, I, I, D, P, P, P, P, I]
+        lib.msa_ref_sparse_attn_bwd.argtypes = [P, P, P, P, P, P, P, I64, I, I, I, I, I, I, D, D, P, P, P, P, P, P,
+                                                I]
         for f in ("msa_ref_block_scores", "msa_ref_select_blocks", "msa_ref_invert_blocks",
-                  "msa_ref_sparse_attn", "msa_ref_dense_attn", "msa_ref_decode"):
+                  "msa_ref_sparse_attn", "msa_ref_dense_attn", "msa_ref_decode", "msa_ref_sparse_attn_bwd"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -166,3 +168,25 @@ def decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, Bk, k, scale, n
                                   ctx_max, H_q, H_kv, d, d_I, Bk, k, float(scale), _p(out), _p(lse), _p(blk),
                                   _p(kth), n_threads or threads()), "msa_ref_decode")
     return out, lse, blk, kth
+
+
+def sparse_attn_bwd(q, k, v, q_idx, k_idx, block_idx, dout, Bk, scale, kl_weight=1.0, n_threads=None):
+    """Backward of the main branch (upstream dout) and of the index branch's KL loss over all N rows
+    (msa_oracle.c: msa_ref_sparse_attn_bwd; study note 4-2 / 4-3, Flash-MSA KL section).  Inputs are
+    bf16 bit patterns: q, dout [N, H_q, d]; k, v [N, H_kv, d]; q_idx [N, G, d_I]; k_idx [N, d_I];
+    block_idx [G, N, k] int32.  Returns a dict of float64 arrays dq, dk, dv, dq_idx, dk_idx and kl [G, N]."""
+    lib = _load()
+    q, k, v, q_idx, k_idx, dout = (_u16(a) for a in (q, k, v, q_idx, k_idx, dout))
+    blk = np.ascontiguousarray(block_idx, dtype=np.int32)
+    N, H_q, d = q.shape
+    H_kv = k.shape[1]
+    d_I = q_idx.shape[2]
+    kk = blk.shape[2]
+    out = {"dq": np.zeros((N, H_q, d)), "dk": np.zeros((N, H_kv, d)), "dv": np.zeros((N, H_kv, d)),
+           "dq_idx": np.zeros((N, H_kv, d_I)), "dk_idx": np.zeros((N, d_I)), "kl": np.zeros((H_kv, N))}
+    rc = lib.msa_ref_sparse_attn_bwd(_p(q), _p(k), _p(v), _p(q_idx), _p(k_idx), _p(blk), _p(dout), N, H_q, H_kv, d,
+                                     d_I, Bk, kk, float(scale), float(kl_weight), _p(out["dq"]), _p(out["dk"]),
+                                     _p(out["dv"]), _p(out["dq_idx"]), _p(out["dk_idx"]), _p(out["kl"]),
+                                     n_threads or threads())
+    _check(rc, "msa_ref_sparse_attn_bwd")
+    return out

@@ -1,6 +1,6 @@
 /*
  * ORACLE — test infrastructure only.  Plain, slow fp64 CPU statement of the
- * MiniMax Sparse Attention (MSA) forward path.  Only the tests, the smoke
+ * MiniMax Sparse Attention (MSA) forward path and of its backward.  Only the tests, the smoke
  * check and the benchmark's CPU-baseline leg may load this library; the
  * product path never does.  It shares no code with the CUDA library.
  *
@@ -36,6 +36,21 @@
  *   - lse is the natural-log log-sum-exp of the scaled main scores;
  *   - decode: the query sits at position ctx_len-1 and its keys are already
  *     in the caches.
+ *
+ * Backward (msa_ref_sparse_attn_bwd, at the end of this file):
+ *   [P1] 4-2 "Why LM loss alone is insufficient" (the index branch learns from
+ *        an auxiliary KL loss whose teacher is the mean over the GQA group's
+ *        query heads of the main-branch attention probabilities), 4-3
+ *        "Gradient detach" (the teacher is detached and the index input gets a
+ *        stop-gradient: the KL updates only the index query and key);
+ *   [P4] "バックワードパス" (main and proxy gradients over the cached sparse
+ *        blocks; proxy LSE recomputed over the selected blocks) and "KL
+ *        ダイバージェンス損失" (the KL gradient on the proxy logits is the proxy
+ *        probability minus the main probability).
+ *   Readings: the KL of row (t, g) is taken over the same support J(t, g) as
+ *   the main attention (the selected blocks' visible tokens) with the index
+ *   logits q^I.k^I / sqrt(d_I); the loss is kl_weight * sum over (t, g) of
+ *   KL(teacher || index); the main branch receives dO only.
  *
  * Arithmetic: bf16 inputs widened exactly to double; every dot product,
  * maximum, exponential and sum in double.
@@ -463,5 +478,180 @@ int msa_ref_decode(const uint16_t* q_t, const uint16_t* q_idx_t, const uint16_t*
   parallel_for((int64_t)B * H_kv, n_threads, decode_select_item, &c);
   if (c.status) return c.status;
   parallel_for((int64_t)B * H_q, n_threads, decode_attn_item, &c);
+  return c.status;
+}
+
+
+/* ------------------------------------------------------------- backward */
+/*
+ * One row (t, g) of the backward, for every head h of group g:
+ *   forward, recomputed: z_j = scale q_{t,h}.k_{j,g}, P_j = exp(z_j - lse),
+ *   O = sum_j P_j v_{j,g} ([P1] 3-3);
+ *   main gradient of a softmax attention with upstream dO:
+ *     D = dO.O, dP_j = dO.v_j, dZ_j = P_j (dP_j - D),
+ *     dq_{t,h} = scale sum_j dZ_j k_j, dk_j += scale dZ_j q_{t,h}, dv_j += P_j dO;
+ *   index branch ([P1] 4-2, 4-3; [P4] KL section): teacher pbar_j = mean_h P_j
+ *   (detached), index logits zI_j = q^I.k^I_j / sqrt(d_I), pI = softmax_J(zI),
+ *     KL = sum_j pbar_j (log pbar_j - log pI_j),
+ *     dL/dzI_j = w (pI_j - pbar_j),
+ *     dq^I_{t,g} = sum_j dL/dzI_j k^I_j / sqrt(d_I), dk^I_j += dL/dzI_j q^I_{t,g} / sqrt(d_I).
+ * Sums over (t, h) into dk, dv and dk^I go to the work item's private
+ * accumulators (dk_acc/dv_acc [N][d] of group g, dkI_acc [N][d_I]).
+ */
+typedef struct {
+  const uint16_t *q, *K, *V, *q_idx, *k_idx, *dO;
+  const int32_t* blk;
+  int64_t N, nb;
+  int H_q, H_kv, d, d_I, Bk, k, chunks;
+  double scale, kl_weight;
+  double *dq, *dq_idx, *kl;          /* row-local outputs */
+  double *dk_acc, *dv_acc, *dkI_acc; /* [items][N][d], [items][N][d], [items][N][d_I] */
+  int status;
+} bwd_ctx;
+
+static void bwd_item(int64_t it, void* p) {
+  bwd_ctx* c = (bwd_ctx*)p;
+  const int g = (int)(it / c->chunks), ch = (int)(it % c->chunks);
+  const int gs = c->H_q / c->H_kv, d = c->d, dI = c->d_I;
+  const int64_t r0 = c->N * ch / c->chunks, r1 = c->N * (ch + 1) / c->chunks;
+  const int64_t cap = (int64_t)c->k * c->Bk;
+  const int64_t kv_stride = (int64_t)c->H_kv * d;
+  double* dk_acc = c->dk_acc + it * c->N * d;
+  double* dv_acc = c->dv_acc + it * c->N * d;
+  double* dkI_acc = c->dkI_acc + it * c->N * dI;
+  int64_t* J = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);
+  double* P = (double*)malloc(sizeof(double) * (size_t)(cap * gs));
+  double* pbar = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* zI = (double*)malloc(sizeof(double) * (size_t)cap);
+  double* O = (double*)malloc(sizeof(double) * (size_t)d);
+  if (!J || !P || !pbar || !zI || !O) {
+    c->status = ORACLE_NO_MEM;
+    free(J), free(P), free(pbar), free(zI), free(O);
+    return;
+  }
+  for (int64_t t = r0; t < r1; ++t) {
+    const int64_t nJ = key_set(c->blk + ((int64_t)g * c->N + t) * c->k, c->k, t, c->Bk, c->nb, J);
+    for (int64_t i = 0; i < nJ; ++i) pbar[i] = 0.0;
+    for (int hh = 0; hh < gs; ++hh) {
+      const int h = g * gs + hh;
+      const uint16_t* qr = c->q + (t * c->H_q + h) * d;
+      const uint16_t* dOr = c->dO + (t * c->H_q + h) * d;
+      double* Ph = P + (int64_t)hh * cap;
+      double* dq = c->dq + (t * c->H_q + h) * d;
+      for (int x = 0; x < d; ++x) dq[x] = 0.0;
+      if (nJ == 0) continue;
+      double m = -INFINITY;
+      for (int64_t i = 0; i < nJ; ++i) {
+        Ph[i] = c->scale * dot_bf16(qr, c->K + J[i] * kv_stride + (int64_t)g * d, d);
+        if (Ph[i] > m) m = Ph[i];
+      }
+      double l = 0.0;
+      for (int64_t i = 0; i < nJ; ++i) l += exp(Ph[i] - m);
+      const double lse = m + log(l);
+      for (int x = 0; x < d; ++x) O[x] = 0.0;
+      for (int64_t i = 0; i < nJ; ++i) {
+        Ph[i] = exp(Ph[i] - lse);
+        const uint16_t* vr = c->V + J[i] * kv_stride + (int64_t)g * d;
+        for (int x = 0; x < d; ++x) O[x] += Ph[i] * bf16_to_double(vr[x]);
+      }
+      double D = 0.0;
+      for (int x = 0; x < d; ++x) D += bf16_to_double(dOr[x]) * O[x];
+      for (int64_t i = 0; i < nJ; ++i) {
+        const uint16_t* kr = c->K + J[i] * kv_stride + (int64_t)g * d;
+        const uint16_t* vr = c->V + J[i] * kv_stride + (int64_t)g * d;
+        const double dZ = Ph[i] * (dot_bf16(dOr, vr, d) - D);
+        double* dkr = dk_acc + J[i] * d;
+        double* dvr = dv_acc + J[i] * d;
+        for (int x = 0; x < d; ++x) {
+          dq[x] += c->scale * dZ * bf16_to_double(kr[x]);
+          dkr[x] += c->scale * dZ * bf16_to_double(qr[x]);
+          dvr[x] += Ph[i] * bf16_to_double(dOr[x]);
+        }
+        pbar[i] += Ph[i] / gs;
+      }
+    }
+    /* index branch */
+    const uint16_t* qIr = c->q_idx + (t * c->H_kv + g) * dI;
+    double* dqI = c->dq_idx + (t * c->H_kv + g) * dI;
+    for (int x = 0; x < dI; ++x) dqI[x] = 0.0;
+    double* klr = c->kl + (int64_t)g * c->N + t;
+    *klr = 0.0;
+    if (nJ == 0) continue;
+    const double sI = 1.0 / sqrt((double)dI);
+    double mI = -INFINITY;
+    for (int64_t i = 0; i < nJ; ++i) {
+      zI[i] = sI * dot_bf16(qIr, c->k_idx + J[i] * dI, dI);
+      if (zI[i] > mI) mI = zI[i];
+    }
+    double lI = 0.0;
+    for (int64_t i = 0; i < nJ; ++i) lI += exp(zI[i] - mI);
+    const double lseI = mI + log(lI);
+    double kl = 0.0;
+    for (int64_t i = 0; i < nJ; ++i) {
+      const double logpI = zI[i] - lseI;
+      const double pI = exp(logpI);
+      if (pbar[i] > 0.0) kl += pbar[i] * (log(pbar[i]) - logpI);
+      const double dz = c->kl_weight * (pI - pbar[i]);
+      const uint16_t* kIr = c->k_idx + J[i] * dI;
+      double* dkIr = dkI_acc + J[i] * dI;
+      for (int x = 0; x < dI; ++x) {
+        dqI[x] += sI * dz * bf16_to_double(kIr[x]);
+        dkIr[x] += sI * dz * bf16_to_double(qIr[x]);
+      }
+    }
+    *klr = kl;
+  }
+  free(J), free(P), free(pbar), free(zI), free(O);
+}
+
+/*
+ * Backward of block-sparse attention and of the index branch's KL loss for
+ * all N positions.  q, dO: [N, H_q, d]; K, V: [N, H_kv, d]; q_idx: [N, G,
+ * d_I]; k_idx: [N, d_I]; block_idx: [G, N, k].  Outputs (double): dq [N,
+ * H_q, d], dk and dv [N, H_kv, d], dq_idx [N, G, d_I], dk_idx [N, d_I], kl
+ * [G, N] (each row's KL(teacher || index)).
+ */
+int msa_ref_sparse_attn_bwd(const uint16_t* q, const uint16_t* K, const uint16_t* V, const uint16_t* q_idx,
+                            const uint16_t* k_idx, const int32_t* block_idx, const uint16_t* dO, int64_t N, int H_q,
+                            int H_kv, int d, int d_I, int Bk, int k, double scale, double kl_weight, double* dq,
+                            double* dk, double* dv, double* dq_idx, double* dk_idx, double* kl, int n_threads) {
+  if (!q || !K || !V || !q_idx || !k_idx || !block_idx || !dO || !dq || !dk || !dv || !dq_idx || !dk_idx || !kl ||
+      N <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 || d_I <= 0 || Bk <= 0 || k < 1)
+    return ORACLE_BAD_ARG;
+  int chunks = n_threads / H_kv;
+  if (chunks < 1) chunks = 1;
+  const double acc_bytes = (double)N * (2 * d + d_I) * 8.0;
+  while (chunks > 1 && acc_bytes * chunks * H_kv > 2.0e9) --chunks;
+  const int64_t items = (int64_t)H_kv * chunks;
+  double* dk_acc = (double*)calloc((size_t)(items * N * d), sizeof(double));
+  double* dv_acc = (double*)calloc((size_t)(items * N * d), sizeof(double));
+  double* dkI_acc = (double*)calloc((size_t)(items * N * d_I), sizeof(double));
+  if (!dk_acc || !dv_acc || !dkI_acc) {
+    free(dk_acc), free(dv_acc), free(dkI_acc);
+    return ORACLE_NO_MEM;
+  }
+  bwd_ctx c = {q, K, V, q_idx, k_idx, dO, block_idx, N, (N + Bk - 1) / Bk, H_q, H_kv, d, d_I, Bk, k, chunks,
+               scale, kl_weight, dq, dq_idx, kl, dk_acc, dv_acc, dkI_acc, 0};
+  parallel_for(items, n_threads, bwd_item, &c);
+  /* sum the items' accumulators */
+  for (int64_t j = 0; j < N; ++j) {
+    for (int g = 0; g < H_kv; ++g)
+      for (int x = 0; x < d; ++x) {
+        double a = 0.0, b = 0.0;
+        for (int ch = 0; ch < chunks; ++ch) {
+          const int64_t itm = (int64_t)g * chunks + ch;
+          a += dk_acc[(itm * N + j) * d + x];
+          b += dv_acc[(itm * N + j) * d + x];
+        }
+        dk[(j * H_kv + g) * d + x] = a;
+        dv[(j * H_kv + g) * d + x] = b;
+      }
+    for (int x = 0; x < d_I; ++x) {
+      double a = 0.0;
+      for (int64_t itm = 0; itm < items; ++itm) a += dkI_acc[(itm * N + j) * d_I + x];
+      dk_idx[j * d_I + x] = a;
+    }
+  }
+  free(dk_acc), free(dv_acc), free(dkI_acc);
   return c.status;
 }
