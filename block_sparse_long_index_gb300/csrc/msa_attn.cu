@@ -346,6 +346,18 @@ AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k) {
 
 size_t attn_scratch_bytes(const AttnPlan& p) { return carve(p, nullptr, nullptr); }
 
+cudaError_t launch_tile_schedule(const int32_t* row_ptr, const int32_t* entries, int64_t N, int G, int k, int64_t nb,
+                                 int64_t T0, int64_t T1, int64_t max_tiles, int32_t* lo, int32_t* cnt,
+                                 int32_t* tiles, int32_t* tile_off, TileRecord* rec, cudaStream_t s) {
+  const int64_t n_gb = (int64_t)G * nb;
+  sched_count_kernel<<<(unsigned)((n_gb + 255) / 256), 256, 0, s>>>(row_ptr, entries, N, G, k, nb, T0, T1, kTilePos,
+                                                                    lo, cnt, tiles);
+  sched_scan_kernel<<<1, 1024, 0, s>>>(tiles, n_gb, tile_off);
+  tile_records_kernel<<<(unsigned)ceil_div(max_tiles * kTilePos, 256), 256, 0, s>>>(tile_off, lo, cnt, entries, N, k,
+                                                                                    nb, n_gb, max_tiles, rec);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
                            int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
                            void* scratch, DeviceStatus* st, cudaStream_t s) {

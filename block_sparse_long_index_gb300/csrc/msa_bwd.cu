@@ -1,0 +1,822 @@
+// msa_sparse_attn_bwd: gradients of block-sparse attention (main branch) and
+// of the index branch's KL alignment loss.
+//
+// "MSA" study note 4-2 (the index branch is trained by a KL loss whose teacher
+// is the mean of the GQA group's main-branch attention probabilities) and 4-3
+// (the teacher is detached and the index input gets a stop-gradient, so the KL
+// reaches only q^I and k^I); Flash-MSA "バックワードパス" (both backward passes
+// run over the cached sparse blocks, scheduled through the inverted map B*,
+// with the proxy LSE recomputed over the selected blocks) and "KLダイバージェ
+// ンス損失" (the gradient on the proxy logits is the proxy probability minus the
+// main probability).
+//
+// Per row (t, h), g = h / gs, J = the selected blocks' tokens j <= t:
+//   P_j = exp(scale q.k_j - lse), D = dO.O, dZ_j = P_j (dO.v_j - D),
+//   dq = scale sum_j dZ_j k_j, dk_j += scale dZ_j q, dv_j += P_j dO;
+// per row (t, g): teacher pbar_j = mean_h P_j, index logits zI_j = q^I.k^I_j /
+// sqrt(d_I), pI = softmax_J(zI), KL = sum_j pbar_j (log pbar_j - log pI_j),
+//   dzI_j = w (pI_j - pbar_j), dq^I = sum_j dzI_j k^I_j / sqrt(d_I),
+//   dk^I_j += dzI_j q^I / sqrt(d_I).
+//
+// Kernels, all over the forward's KV-outer tile list (B -> B*, tiles of 16
+// positions x 8 head slots = 128 rows, one (group, block) per tile):
+//   rowdot:     D[h, t] = dO.O;
+//   index lse:  per tile the masked index logits of its 16 positions -> one
+//               (max, sum) per (t, slot); a combine per (t, g) -> lse^I;
+//   main:       warps own 16-key slices: S^T, P^T, dP^T, dZ^T for their keys
+//               and the tile's rows, dV and dK accumulated in registers over
+//               the tiles of a (group, block) and flushed with fp32 reductions;
+//               dZ staged in shared memory, then warps own rows for dQ, added
+//               to dq with fp32 reductions;
+//   index:      the same shape for the index branch: S^T recomputed for the
+//               teacher, the index logits, dzI, dk^I per key slice in
+//               registers, dq^I through shared memory; KL per row.
+// A block id repeated in a row's set contributes once (its first slot).
+#include <math.h>
+
+#include "msa_common.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kRowsT = 128;            // tile rows: kPosT positions x 8 head slots
+constexpr int kPosT = kTilePositions;  // 16
+constexpr int kThreadsB = 256;
+
+// ------------------------------------------------------------------ shared-memory tiles
+// A bf16 tile with `cols` elements per row keeps 16-byte chunk c of row r at
+// chunk swz(r, c): the 8 row addresses of an ldmatrix at one chunk then fall
+// in distinct banks (rows of >= 8 chunks: XOR with r mod 8; rows of 4 chunks:
+// XOR with (r / 2) mod 4).
+__device__ __forceinline__ int swz(int r, int c, int cpr) { return cpr >= 8 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3)); }
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int r, int col, int cols) {
+  return base + (uint32_t)(r * cols * 2 + swz(r, col >> 3, cols >> 3) * 16 + (col & 7) * 2);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// A fragment (16 x 16) of rows r0.. and columns k0.. of a row-major tile
+__device__ __forceinline__ void lds_a(uint32_t (&a)[4], uint32_t base, int r0, int k0, int cols) {
+  const int lane = threadIdx.x & 31, m = lane >> 3;
+  ldsm_x4(a, tile_addr(base, r0 + ((m & 1) << 3) + (lane & 7), k0 + ((m >> 1) << 3), cols));
+}
+// B fragments of n-tiles n0 and n0+8 (k0..k0+15) from a tile stored [n][k]
+__device__ __forceinline__ void lds_b_nk(uint32_t (&b)[4], uint32_t base, int n0, int k0, int cols) {
+  const int lane = threadIdx.x & 31;
+  ldsm_x4(b, tile_addr(base, n0 + (lane & 7) + ((lane >> 4) << 3), k0 + (((lane >> 3) & 1) << 3), cols));
+}
+// B fragments of n-tiles n0 and n0+8 (k0..k0+15) from a tile stored [k][n]
+__device__ __forceinline__ void lds_b_kn(uint32_t (&b)[4], uint32_t base, int k0, int n0, int cols) {
+  const int lane = threadIdx.x & 31;
+  ldsm_x4_t(b, tile_addr(base, k0 + (lane & 7) + (((lane >> 3) & 1) << 3), n0 + ((lane >> 4) << 3), cols));
+}
+__device__ __forceinline__ void mma2(float (&c0)[4], float (&c1)[4], const uint32_t (&a)[4], const uint32_t (&b)[4]) {
+  const uint32_t b0[2] = {b[0], b[1]}, b1[2] = {b[2], b[3]};
+  mma_bf16_16816(c0, a, b0);
+  mma_bf16_16816(c1, a, b1);
+}
+// A fragment (16 rows x 16 k) from two m16n8 accumulator tiles (columns k 0-7 and 8-15)
+__device__ __forceinline__ void c_to_a(uint32_t (&a)[4], const float (&c0)[4], const float (&c1)[4]) {
+  a[0] = pack_bf16x2(c0[0], c0[1]);
+  a[1] = pack_bf16x2(c0[2], c0[3]);
+  a[2] = pack_bf16x2(c1[0], c1[1]);
+  a[3] = pack_bf16x2(c1[2], c1[3]);
+}
+__device__ __forceinline__ void red_add2(float* p, float x, float y) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};\n" ::"l"(p), "f"(x), "f"(y) : "memory");
+}
+__device__ __forceinline__ void st_bf16(uint16_t* base, int r, int col, int cols, float v) {
+  uint16_t* p = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(base) + r * cols * 2 +
+                                            swz(r, col >> 3, cols >> 3) * 16 + (col & 7) * 2);
+  *p = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
+}
+
+// Rows [0, nrows) of a tile with `cols` bf16 per row: row r from src(r), or
+// zeros where src(r) is null (`any` is a valid global address for those copies).
+template <typename F>
+__device__ __forceinline__ void load_rows(uint16_t* dst, int nrows, int cols, const uint16_t* any, F src) {
+  const int cpr = cols >> 3;
+  for (int i = threadIdx.x; i < nrows * cpr; i += blockDim.x) {
+    const int r = i / cpr, c = i % cpr;
+    const uint16_t* gp = src(r);
+    cp_async_16(reinterpret_cast<char*>(dst) + r * cols * 2 + swz(r, c, cpr) * 16, gp ? gp + c * 8 : any,
+                gp ? 16 : 0);
+  }
+}
+
+// The contiguous range of the flat tile list this CTA walks.
+__device__ __forceinline__ void tile_range(const int32_t* tile_off, int64_t n_gb, int64_t& lo, int64_t& hi) {
+  const int64_t total = tile_off[n_gb];
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  lo = min(total, per * (int64_t)blockIdx.x);
+  hi = min(total, lo + per);
+}
+
+// Position t of row r of the tile (p = r / 8, head slot r % 8) or -1: past the
+// tile's count, past gs, or a slot whose block id already appeared earlier in
+// the row's set (the set counts each block once).
+__device__ __forceinline__ int32_t row_position(const TileRecord& rc, int r, int gs, const int32_t* block_idx,
+                                                int64_t N, int k) {
+  const int p = r >> 3, hh = r & 7;
+  if (p >= rc.count || hh >= gs) return -1;
+  const int32_t t = rc.t[p];
+  const int32_t* sel = block_idx + ((int64_t)rc.g * N + t) * k;
+  for (int s2 = 0; s2 < rc.slot[p]; ++s2)
+    if (sel[s2] == rc.b) return -1;
+  return t;
+}
+
+__device__ __forceinline__ void copy_record(TileRecord* dst, const TileRecord* src) {
+  if (threadIdx.x < 8)
+    reinterpret_cast<uint4*>(dst)[threadIdx.x] = __ldg(reinterpret_cast<const uint4*>(src) + threadIdx.x);
+}
+
+// ------------------------------------------------------------------ D = dO . O
+__global__ void bwd_rowdot_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ out, int64_t N,
+                                  int H_q, int D, float* __restrict__ Dr) {
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // t * H_q + h
+  const int lane = threadIdx.x & 31;
+  if (row >= N * H_q) return;
+  const uint16_t* a = dout + row * D;
+  const uint16_t* b = out + row * D;
+  float s = 0.f;
+  for (int c = 2 * lane; c < D; c += 64) {
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(a + c), y = *reinterpret_cast<const uint32_t*>(b + c);
+    s = fmaf(bf16_lo(x), bf16_lo(y), s);
+    s = fmaf(bf16_hi(x), bf16_hi(y), s);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if (lane == 0) {
+    const int64_t t = row / H_q;
+    const int h = (int)(row % H_q);
+    Dr[(int64_t)h * N + t] = s;
+  }
+}
+
+// ------------------------------------------------------------------ index-branch lse
+// Per tile: zI = q^I.k^I_j / sqrt(d_I) of its positions over the block's keys
+// j <= t; one (max, sum of exp) per (t, slot) into part[g, t, slot].
+template <int BK, int DI>
+__global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
+    const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const TileRecord* __restrict__ rec,
+    const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int G, int k, float sI,
+    float2* __restrict__ part) {
+  __shared__ __align__(128) uint16_t kIs[BK * DI];
+  __shared__ __align__(128) uint16_t qIs[kPosT * DI];
+  __shared__ float red_m[8][kPosT], red_l[8][kPosT];
+  __shared__ __align__(16) TileRecord rc;
+  constexpr int KSL = BK / 16;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
+  const uint32_t kIs_a = smem_u32(kIs), qIs_a = smem_u32(qIs);
+  int64_t lo, hi;
+  tile_range(tile_off, n_gb, lo, hi);
+  int cur_gb = -1;
+  for (int64_t ti = lo; ti < hi; ++ti) {
+    __syncthreads();
+    copy_record(&rc, rec + ti);
+    __syncthreads();
+    if (rc.gb != cur_gb) {
+      cur_gb = rc.gb;
+      load_rows(kIs, BK, DI, k_idx, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)rc.b * BK + r;
+        return j < N ? k_idx + j * DI : nullptr;
+      });
+    }
+    load_rows(qIs, kPosT, DI, q_idx, [&](int p) -> const uint16_t* {
+      return p < rc.count ? q_idx + ((int64_t)rc.t[p] * G + rc.g) * DI : nullptr;
+    });
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    float zi[2][4] = {};
+    if (warp < KSL) {
+#pragma unroll
+      for (int kk = 0; kk < DI; kk += 16) {
+        uint32_t a[4], b[4];
+        lds_a(a, kIs_a, warp * 16, kk, DI);
+        lds_b_nk(b, qIs_a, 0, kk, DI);
+        mma2(zi[0], zi[1], a, b);
+      }
+    }
+    // element (key row g8 + 8 half, position nt * 8 + 2 c4 + e)
+    float mx[2][2];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int p = nt * 8 + 2 * c4 + e;
+        const int64_t t = p < rc.count ? rc.t[p] : -1;
+        float m = __int_as_float(0xff800000);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int64_t j = (int64_t)rc.b * BK + warp * 16 + g8 + 8 * half;
+          const bool ok = warp < KSL && j <= t;
+          zi[nt][2 * half + e] = ok ? zi[nt][2 * half + e] * sI : __int_as_float(0xff800000);
+          m = fmaxf(m, zi[nt][2 * half + e]);
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        mx[nt][e] = m;
+      }
+    if (g8 == 0)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) red_m[warp][nt * 8 + 2 * c4 + e] = mx[nt][e];
+    __syncthreads();
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int p = nt * 8 + 2 * c4 + e;
+        float M = __int_as_float(0xff800000);
+        for (int w = 0; w < KSL; ++w) M = fmaxf(M, red_m[w][p]);
+        float l = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const float z = zi[nt][2 * half + e];
+          l += z == __int_as_float(0xff800000) ? 0.f : __expf(z - M);
+        }
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        mx[nt][e] = l;
+      }
+    if (g8 == 0)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) red_l[warp][nt * 8 + 2 * c4 + e] = mx[nt][e];
+    __syncthreads();
+    if (tid < rc.count) {
+      float M = __int_as_float(0xff800000), L = 0.f;
+      for (int w = 0; w < KSL; ++w) M = fmaxf(M, red_m[w][tid]);
+      for (int w = 0; w < KSL; ++w) L += red_l[w][tid];
+      part[((int64_t)rc.g * N + rc.t[tid]) * k + rc.slot[tid]] = make_float2(M, L);
+    }
+  }
+}
+
+// lse^I[g, t] from the (max, sum) of the row's slots; a slot counts iff its id
+// is in [0, nb) and first of its kind in the row.
+__global__ void bwd_index_lse_combine_kernel(const float2* __restrict__ part, const int32_t* __restrict__ block_idx,
+                                             int64_t N, int G, int k, int64_t nb, float* __restrict__ lseI) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // g * N + t
+  if (i >= (int64_t)G * N) return;
+  const int32_t* sel = block_idx + i * k;
+  const float2* pp = part + i * k;
+  float M = __int_as_float(0xff800000);
+  for (int s = 0; s < k; ++s) {
+    bool ok = sel[s] >= 0 && (int64_t)sel[s] < nb;
+    for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != sel[s];
+    if (ok) M = fmaxf(M, pp[s].x);
+  }
+  float L = 0.f;
+  if (M != __int_as_float(0xff800000))
+    for (int s = 0; s < k; ++s) {
+      bool ok = sel[s] >= 0 && (int64_t)sel[s] < nb;
+      for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != sel[s];
+      if (ok && pp[s].x != __int_as_float(0xff800000)) L += pp[s].y * __expf(pp[s].x - M);
+    }
+  lseI[i] = L > 0.f ? M + logf(L) : __int_as_float(0x7f800000);  // +inf: no index logit (no gradient)
+}
+
+// ------------------------------------------------------------------ main branch
+template <int D, int BK>
+struct MainSmem {
+  static constexpr int K = 0, V = BK * D * 2, Q = 2 * BK * D * 2, DO = Q + kRowsT * D * 2, DZ = DO + kRowsT * D * 2;
+  static constexpr int BYTES = DZ + kRowsT * BK * 2;
+};
+
+template <int D, int BK>
+__global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
+    const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
+    const int32_t* __restrict__ block_idx, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
+    int64_t n_gb, int64_t N, int H_q, int H_kv, int gs, int k, float scale, float* __restrict__ dq,
+    float* __restrict__ dk, float* __restrict__ dv) {
+  using L = MainSmem<D, BK>;
+  extern __shared__ __align__(128) uint8_t smb[];
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smb + L::K);
+  uint16_t* Vs = reinterpret_cast<uint16_t*>(smb + L::V);
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smb + L::Q);
+  uint16_t* dOs = reinterpret_cast<uint16_t*>(smb + L::DO);
+  uint16_t* dZs = reinterpret_cast<uint16_t*>(smb + L::DZ);
+  __shared__ float lse_s[kRowsT], D_s[kRowsT];
+  __shared__ int32_t t_s[kRowsT];
+  __shared__ __align__(16) TileRecord rc;
+  constexpr int KSL = BK / 16;   // key slices of 16
+  constexpr int RG = 8 / KSL;    // row groups (1 or 2)
+  constexpr int RPW = kRowsT / RG;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
+  const int ksl = warp % KSL, rg = warp / KSL;
+  const uint32_t Ks_a = smem_u32(Ks), Vs_a = smem_u32(Vs), Qs_a = smem_u32(Qs), dOs_a = smem_u32(dOs),
+                 dZs_a = smem_u32(dZs);
+  float accK[D / 8][4], accV[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) accK[i][e] = accV[i][e] = 0.f;
+  int cur_gb = -1, cur_g = 0, cur_b = 0;
+  // dK and dV of this warp's 16 keys of the current block into dk, dv
+  auto flush = [&]() {
+    if (cur_gb < 0) return;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int64_t j = (int64_t)cur_b * BK + ksl * 16 + g8 + 8 * half;
+      if (j < N) {
+        float* pk = dk + (j * H_kv + cur_g) * D + 2 * c4;
+        float* pv = dv + (j * H_kv + cur_g) * D + 2 * c4;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          red_add2(pk + nd * 8, scale * accK[nd][2 * half], scale * accK[nd][2 * half + 1]);
+          red_add2(pv + nd * 8, accV[nd][2 * half], accV[nd][2 * half + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) accK[i][e] = accV[i][e] = 0.f;
+  };
+  int64_t lo, hi;
+  tile_range(tile_off, n_gb, lo, hi);
+  for (int64_t ti = lo; ti < hi; ++ti) {
+    __syncthreads();  // the previous tile is done with every buffer
+    copy_record(&rc, rec + ti);
+    __syncthreads();
+    if (rc.gb != cur_gb) {
+      flush();
+      cur_gb = rc.gb;
+      cur_g = rc.g;
+      cur_b = rc.b;
+      const int64_t kv_row = (int64_t)H_kv * D;
+      load_rows(Ks, BK, D, kc, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)cur_b * BK + r;
+        return j < N ? kc + j * kv_row + (int64_t)cur_g * D : nullptr;
+      });
+      load_rows(Vs, BK, D, vc, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)cur_b * BK + r;
+        return j < N ? vc + j * kv_row + (int64_t)cur_g * D : nullptr;
+      });
+    }
+    for (int r = tid; r < kRowsT; r += blockDim.x) {
+      const int32_t t = row_position(rc, r, gs, block_idx, N, k);
+      t_s[r] = t;
+      const int h = cur_g * gs + (r & 7);
+      lse_s[r] = t >= 0 ? lse[(int64_t)h * N + t] : __int_as_float(0x7f800000);
+      D_s[r] = t >= 0 ? Dr[(int64_t)h * N + t] : 0.f;
+    }
+    __syncthreads();
+    load_rows(Qs, kRowsT, D, q, [&](int r) -> const uint16_t* {
+      const int32_t t = t_s[r];
+      return t >= 0 ? q + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D : nullptr;
+    });
+    load_rows(dOs, kRowsT, D, dout, [&](int r) -> const uint16_t* {
+      const int32_t t = t_s[r];
+      return t >= 0 ? dout + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D : nullptr;
+    });
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- phase A: this warp's 16 keys against its rows, 16 rows at a time
+    const int key0 = ksl * 16;
+    for (int rc0 = 0; rc0 < RPW; rc0 += 16) {
+      const int row0 = rg * RPW + rc0;
+      float s[2][4] = {}, dp[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < D; kk += 16) {
+        uint32_t a[4], b[4];
+        lds_a(a, Ks_a, key0, kk, D);
+        lds_b_nk(b, Qs_a, row0, kk, D);
+        mma2(s[0], s[1], a, b);
+        lds_a(a, Vs_a, key0, kk, D);
+        lds_b_nk(b, dOs_a, row0, kk, D);
+        mma2(dp[0], dp[1], a, b);
+      }
+      // element (key g8 + 8 half, row row0 + 8 nt + 2 c4 + e): P^T and dZ^T
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = row0 + nt * 8 + 2 * c4 + e;
+          const int32_t t = t_s[r];
+          const float ls = lse_s[r], dd = D_s[r];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int64_t j = (int64_t)cur_b * BK + key0 + g8 + 8 * half;
+            float pv = 0.f, zv = 0.f;
+            if (t >= 0 && j <= t) {
+              pv = __expf(s[nt][2 * half + e] * scale - ls);
+              zv = pv * (dp[nt][2 * half + e] - dd);
+            }
+            s[nt][2 * half + e] = pv;
+            dp[nt][2 * half + e] = zv;
+            st_bf16(dZs, r, key0 + g8 + 8 * half, BK, zv);
+          }
+        }
+      uint32_t pa[4], za[4];
+      c_to_a(pa, s[0], s[1]);
+      c_to_a(za, dp[0], dp[1]);
+#pragma unroll
+      for (int nd = 0; nd < D / 8; nd += 2) {
+        uint32_t b[4];
+        lds_b_kn(b, dOs_a, row0, nd * 8, D);
+        mma2(accV[nd], accV[nd + 1], pa, b);
+        lds_b_kn(b, Qs_a, row0, nd * 8, D);
+        mma2(accK[nd], accK[nd + 1], za, b);
+      }
+    }
+    __syncthreads();  // dZ complete
+
+    // ---- phase B: dQ of rows [16 warp, 16 warp + 16) = scale dZ K
+    {
+      const int r0 = warp * 16;
+      float acc[D / 8][4];
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < BK; kk += 16) {
+        uint32_t a[4];
+        lds_a(a, dZs_a, r0, kk, BK);
+#pragma unroll
+        for (int nd = 0; nd < D / 8; nd += 2) {
+          uint32_t b[4];
+          lds_b_kn(b, Ks_a, kk, nd * 8, D);
+          mma2(acc[nd], acc[nd + 1], a, b);
+        }
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int r = r0 + g8 + 8 * half;
+        const int32_t t = t_s[r];
+        if (t >= 0) {
+          float* p = dq + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D + 2 * c4;
+#pragma unroll
+          for (int nd = 0; nd < D / 8; ++nd)
+            red_add2(p + nd * 8, scale * acc[nd][2 * half], scale * acc[nd][2 * half + 1]);
+        }
+      }
+    }
+  }
+  flush();
+}
+
+// ------------------------------------------------------------------ index branch
+template <int D, int BK, int DI>
+struct IndexSmem {
+  static constexpr int K = 0, Q = BK * D * 2, KI = Q + kRowsT * D * 2, QI = KI + BK * DI * 2, DZ = QI + kPosT * DI * 2,
+                       PB = DZ + kPosT * BK * 2;
+  static constexpr int BYTES = PB + kPosT * BK * 4;
+};
+
+template <int D, int BK, int DI>
+__global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ q_idx,
+    const uint16_t* __restrict__ k_idx, const float* __restrict__ lse, const float* __restrict__ lseI,
+    const int32_t* __restrict__ block_idx, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
+    int64_t n_gb, int64_t N, int H_q, int H_kv, int gs, int k, float scale, float sI, float w,
+    float* __restrict__ dq_idx, float* __restrict__ dk_idx, float* __restrict__ kl) {
+  using L = IndexSmem<D, BK, DI>;
+  extern __shared__ __align__(128) uint8_t smb[];
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smb + L::K);
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smb + L::Q);
+  uint16_t* kIs = reinterpret_cast<uint16_t*>(smb + L::KI);
+  uint16_t* qIs = reinterpret_cast<uint16_t*>(smb + L::QI);
+  uint16_t* dzs = reinterpret_cast<uint16_t*>(smb + L::DZ);
+  float* pbar_s = reinterpret_cast<float*>(smb + L::PB);  // [position][key]
+  __shared__ float lse_s[kRowsT];
+  __shared__ int32_t t_s[kRowsT];
+  __shared__ float lseI_s[kPosT];
+  __shared__ int32_t tp_s[kPosT];  // position of tile position p, or -1
+  __shared__ __align__(16) TileRecord rc;
+  constexpr int KSL = BK / 16;
+  constexpr int RG = 8 / KSL;
+  constexpr int RPW = kRowsT / RG;
+  const int G = H_kv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
+  const int ksl = warp % KSL, rg = warp / KSL;
+  const uint32_t Ks_a = smem_u32(Ks), Qs_a = smem_u32(Qs), kIs_a = smem_u32(kIs), qIs_a = smem_u32(qIs),
+                 dzs_a = smem_u32(dzs);
+  const float inv_gs = 1.f / (float)gs;
+  float accI[DI / 8][4];
+#pragma unroll
+  for (int i = 0; i < DI / 8; ++i) accI[i][0] = accI[i][1] = accI[i][2] = accI[i][3] = 0.f;
+  int cur_gb = -1, cur_g = 0, cur_b = 0;
+  auto flush = [&]() {
+    if (cur_gb < 0) return;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int64_t j = (int64_t)cur_b * BK + ksl * 16 + g8 + 8 * half;
+      if (j < N) {
+        float* p = dk_idx + j * DI + 2 * c4;
+#pragma unroll
+        for (int nd = 0; nd < DI / 8; ++nd) red_add2(p + nd * 8, sI * accI[nd][2 * half], sI * accI[nd][2 * half + 1]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < DI / 8; ++i) accI[i][0] = accI[i][1] = accI[i][2] = accI[i][3] = 0.f;
+  };
+  int64_t lo, hi;
+  tile_range(tile_off, n_gb, lo, hi);
+  for (int64_t ti = lo; ti < hi; ++ti) {
+    __syncthreads();
+    copy_record(&rc, rec + ti);
+    __syncthreads();
+    if (rc.gb != cur_gb) {
+      flush();
+      cur_gb = rc.gb;
+      cur_g = rc.g;
+      cur_b = rc.b;
+      const int64_t kv_row = (int64_t)H_kv * D;
+      load_rows(Ks, BK, D, kc, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)cur_b * BK + r;
+        return j < N ? kc + j * kv_row + (int64_t)cur_g * D : nullptr;
+      });
+      load_rows(kIs, BK, DI, k_idx, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)cur_b * BK + r;
+        return j < N ? k_idx + j * DI : nullptr;
+      });
+    }
+    for (int r = tid; r < kRowsT; r += blockDim.x) {
+      const int32_t t = row_position(rc, r, gs, block_idx, N, k);
+      t_s[r] = t;
+      lse_s[r] = t >= 0 ? lse[(int64_t)(cur_g * gs + (r & 7)) * N + t] : __int_as_float(0x7f800000);
+    }
+    __syncthreads();
+    if (tid < kPosT) {  // head slot 0 of a position is a real head whenever the position is
+      const int32_t t = t_s[tid * 8];
+      tp_s[tid] = t;
+      lseI_s[tid] = t >= 0 ? lseI[(int64_t)cur_g * N + t] : __int_as_float(0x7f800000);
+    }
+    load_rows(Qs, kRowsT, D, q, [&](int r) -> const uint16_t* {
+      const int32_t t = t_s[r];
+      return t >= 0 ? q + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D : nullptr;
+    });
+    load_rows(qIs, kPosT, DI, q_idx, [&](int p) -> const uint16_t* {
+      const int32_t t = t_s[p * 8];
+      return t >= 0 ? q_idx + ((int64_t)t * G + cur_g) * DI : nullptr;
+    });
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- teacher: pbar[p][key] = mean over the position's heads of P, for this warp's keys and rows
+    const int key0 = ksl * 16;
+    for (int rc0 = 0; rc0 < RPW; rc0 += 16) {
+      const int row0 = rg * RPW + rc0;
+      float s[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < D; kk += 16) {
+        uint32_t a[4], b[4];
+        lds_a(a, Ks_a, key0, kk, D);
+        lds_b_nk(b, Qs_a, row0, kk, D);
+        mma2(s[0], s[1], a, b);
+      }
+      // n-tile nt holds the 8 head slots of position row0 / 8 + nt
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        float sum[2] = {0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = row0 + nt * 8 + 2 * c4 + e;
+          const int32_t t = t_s[r];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int64_t j = (int64_t)cur_b * BK + key0 + g8 + 8 * half;
+            if (t >= 0 && j <= t) sum[half] += __expf(s[nt][2 * half + e] * scale - lse_s[r]);
+          }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          sum[half] += __shfl_xor_sync(0xffffffffu, sum[half], 1);
+          sum[half] += __shfl_xor_sync(0xffffffffu, sum[half], 2);
+        }
+        if (c4 == 0) {
+          const int p = row0 / 8 + nt;
+          pbar_s[p * BK + key0 + g8] = sum[0] * inv_gs;
+          pbar_s[p * BK + key0 + g8 + 8] = sum[1] * inv_gs;
+        }
+      }
+    }
+    __syncthreads();
+
+    // ---- index logits of this warp's keys for all 16 positions, dzI and the KL terms
+    if (rg == 0) {
+      float zi[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < DI; kk += 16) {
+        uint32_t a[4], b[4];
+        lds_a(a, kIs_a, key0, kk, DI);
+        lds_b_nk(b, qIs_a, 0, kk, DI);
+        mma2(zi[0], zi[1], a, b);
+      }
+      float klp[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int p = nt * 8 + 2 * c4 + e;
+          const int32_t t = tp_s[p];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int key = key0 + g8 + 8 * half;
+            const int64_t j = (int64_t)cur_b * BK + key;
+            float dz = 0.f;
+            if (t >= 0 && j <= t) {
+              const float logp = zi[nt][2 * half + e] * sI - lseI_s[p];
+              const float pb = pbar_s[p * BK + key];
+              dz = w * (__expf(logp) - pb);
+              if (pb > 0.f) klp[nt][e] += pb * (__logf(pb) - logp);
+            }
+            zi[nt][2 * half + e] = dz;
+            st_bf16(dzs, p, key, BK, dz);
+          }
+        }
+      if (kl) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float x = klp[nt][e];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            const int p = nt * 8 + 2 * c4 + e;
+            if (g8 == 0 && tp_s[p] >= 0) atomicAdd(kl + (int64_t)cur_g * N + tp_s[p], x);
+          }
+      }
+      // dk^I of these keys += dzI^T q^I (k = the 16 positions)
+      uint32_t za[4];
+      c_to_a(za, zi[0], zi[1]);
+#pragma unroll
+      for (int nd = 0; nd < DI / 8; nd += 2) {
+        uint32_t b[4];
+        lds_b_kn(b, qIs_a, 0, nd * 8, DI);
+        mma2(accI[nd], accI[nd + 1], za, b);
+      }
+    }
+    __syncthreads();  // dzI complete
+
+    // ---- dq^I (16 positions x d_I) = sI dzI kI: warp w takes columns [16 w, 16 w + 16)
+    if (warp * 16 < DI) {
+      float acc[2][4] = {};
+#pragma unroll
+      for (int kk = 0; kk < BK; kk += 16) {
+        uint32_t a[4], b[4];
+        lds_a(a, dzs_a, 0, kk, BK);
+        lds_b_kn(b, kIs_a, kk, warp * 16, DI);
+        mma2(acc[0], acc[1], a, b);
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int p = g8 + 8 * half;
+        const int32_t t = tp_s[p];
+        if (t >= 0) {
+          float* pp = dq_idx + ((int64_t)t * G + cur_g) * DI + warp * 16 + 2 * c4;
+          red_add2(pp, sI * acc[0][2 * half], sI * acc[0][2 * half + 1]);
+          red_add2(pp + 8, sI * acc[1][2 * half], sI * acc[1][2 * half + 1]);
+        }
+      }
+    }
+  }
+  flush();
+}
+
+// ------------------------------------------------------------------ scratch and launch
+struct BwdScratch {
+  int32_t *row_ptr, *entries, *n_entries;
+  InvertScratch inv;
+  int32_t *lo, *cnt, *tiles, *tile_off;
+  TileRecord* rec;
+  float *Dr, *lseI;
+  float2* partI;
+  int64_t max_tiles, nb;
+};
+
+size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* out) {
+  char* c = (char*)base;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* r = c ? c + off : nullptr;
+    off += align_up(bytes, 256);
+    return r;
+  };
+  BwdScratch s;
+  s.nb = ceil_div(N, Bk);
+  s.max_tiles = (int64_t)G * ceil_div(N * k, kPosT) + (int64_t)G * s.nb;
+  s.row_ptr = (int32_t*)take((size_t)G * (s.nb + 1) * 4);
+  s.entries = (int32_t*)take((size_t)G * N * k * 4);
+  s.n_entries = (int32_t*)take((size_t)G * 4);
+  char* inv_base = take(invert_scratch_bytes(N, G, Bk, k));
+  s.inv = invert_scratch_carve(inv_base, N, G, Bk, k);
+  s.lo = (int32_t*)take((size_t)G * s.nb * 4);
+  s.cnt = (int32_t*)take((size_t)G * s.nb * 4);
+  s.tiles = (int32_t*)take((size_t)G * s.nb * 4);
+  s.tile_off = (int32_t*)take(((size_t)G * s.nb + 1) * 4);
+  s.rec = (TileRecord*)take((size_t)s.max_tiles * sizeof(TileRecord));
+  s.Dr = (float*)take((size_t)H_q * N * 4);
+  s.lseI = (float*)take((size_t)G * N * 4);
+  s.partI = (float2*)take((size_t)G * N * k * 8);
+  if (out) *out = s;
+  return off;
+}
+
+template <int D, int BK, int DI>
+cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
+                         const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc,
+                         int64_t N, int H_q, int H_kv, int k, float scale, float kl_weight, float* dq, float* dk,
+                         float* dv, float* dq_idx, float* dk_idx, float* kl, cudaStream_t s) {
+  const int G = H_kv, gs = H_q / H_kv;
+  const int64_t n_gb = (int64_t)G * sc.nb;
+  const float sI = 1.f / sqrtf((float)DI);
+  const int grid = num_sms();
+  bwd_index_lse_kernel<BK, DI><<<grid, kThreadsB, 0, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec,
+                                                          sc.tile_off, n_gb, N, G, k, sI, sc.partI);
+  bwd_index_lse_combine_kernel<<<(unsigned)ceil_div((int64_t)G * N, 256), 256, 0, s>>>(sc.partI, block_idx, N, G, k,
+                                                                                      sc.nb, sc.lseI);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto km = bwd_main_kernel<D, BK>;
+  e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, MainSmem<D, BK>::BYTES);
+  if (e != cudaSuccess) return e;
+  km<<<grid, kThreadsB, MainSmem<D, BK>::BYTES, s>>>((const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v,
+                                                    (const uint16_t*)dout, lse, sc.Dr, block_idx, sc.rec,
+                                                    sc.tile_off, n_gb, N, H_q, H_kv, gs, k, scale, dq, dk, dv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto ki = bwd_index_kernel<D, BK, DI>;
+  e = cudaFuncSetAttribute(ki, cudaFuncAttributeMaxDynamicSharedMemorySize, IndexSmem<D, BK, DI>::BYTES);
+  if (e != cudaSuccess) return e;
+  ki<<<grid, kThreadsB, IndexSmem<D, BK, DI>::BYTES, s>>>(
+      (const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)q_idx, (const uint16_t*)k_idx, lse, sc.lseI,
+      block_idx, sc.rec, sc.tile_off, n_gb, N, H_q, H_kv, gs, k, scale, sI, kl_weight, dq_idx, dk_idx, kl);
+  return cudaGetLastError();
+}
+
+template <int D, int BK>
+cudaError_t launch_di(int d_I, const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
+                      const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc, int64_t N,
+                      int H_q, int H_kv, int k, float scale, float w, float* dq, float* dk, float* dv, float* dq_idx,
+                      float* dk_idx, float* kl, cudaStream_t s) {
+  if (d_I == 32)
+    return launch_tiles<D, BK, 32>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
+                                   dk, dv, dq_idx, dk_idx, kl, s);
+  if (d_I == 64)
+    return launch_tiles<D, BK, 64>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
+                                   dk, dv, dq_idx, dk_idx, kl, s);
+  return launch_tiles<D, BK, 128>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
+                                  dk, dv, dq_idx, dk_idx, kl, s);
+}
+
+}  // namespace
+
+size_t bwd_scratch_bytes(int64_t N, int H_q, int H_kv, int d, int Bk, int k) {
+  (void)d;
+  return carve(N, H_q, H_kv, Bk, k, nullptr, nullptr);
+}
+
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                       const int32_t* block_idx, const void* out, const float* lse, const void* dout, int64_t N,
+                       int H_q, int H_kv, int d, int d_I, int Bk, int kb, float scale, float kl_weight, float* dq,
+                       float* dk, float* dv, float* dq_idx, float* dk_idx, float* kl, void* scratch, DeviceStatus* st,
+                       cudaStream_t s) {
+  const int G = H_kv;
+  BwdScratch sc;
+  carve(N, H_q, G, Bk, kb, scratch, &sc);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(dq, 0, (size_t)N * H_q * d * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dk, 0, (size_t)N * H_kv * d * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dv, 0, (size_t)N * H_kv * d * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dq_idx, 0, (size_t)N * G * d_I * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dk_idx, 0, (size_t)N * d_I * 4, s)) != cudaSuccess) return e;
+  if (kl && (e = cudaMemsetAsync(kl, 0, (size_t)G * N * 4, s)) != cudaSuccess) return e;
+  if ((e = launch_invert(block_idx, N, G, Bk, kb, sc.row_ptr, sc.entries, sc.n_entries, sc.inv, st, s)) != cudaSuccess)
+    return e;
+  if ((e = launch_tile_schedule(sc.row_ptr, sc.entries, N, G, kb, sc.nb, 0, N, sc.max_tiles, sc.lo, sc.cnt, sc.tiles,
+                                sc.tile_off, sc.rec, s)) != cudaSuccess)
+    return e;
+  bwd_rowdot_kernel<<<(unsigned)ceil_div(N * H_q * 32, 256), 256, 0, s>>>((const uint16_t*)dout,
+                                                                        (const uint16_t*)out, N, H_q, d, sc.Dr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (d == 64)
+    return Bk == 64 ? launch_di<64, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
+                                        kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s)
+                    : launch_di<64, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
+                                         scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s);
+  return Bk == 64 ? launch_di<128, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
+                                       kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s)
+                  : launch_di<128, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
+                                        scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s);
+}
+
+}  // namespace msa

@@ -225,6 +225,34 @@ msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void
                                     (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
 }
 
+size_t msa_sparse_attn_bwd_workspace(const msa_shape_t* shape) {
+  if (check_shape(shape) != MSA_OK) return kHeader;
+  return kHeader + msa::bwd_scratch_bytes(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
+}
+
+msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                 const int32_t* block_idx, const void* out, const float* lse, const void* dout,
+                                 const msa_shape_t* shape, float scale, float kl_weight, float* dq, float* dk,
+                                 float* dv, float* dq_idx, float* dk_idx, float* kl, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream) {
+  if (!q || !k || !v || !q_idx || !k_idx || !block_idx || !out || !lse || !dout || !dq || !dk || !dv || !dq_idx ||
+      !dk_idx)
+    return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (!(scale > 0.f) || scale != scale || kl_weight != kl_weight) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_idx) || !aligned16(k_idx) || !aligned16(out) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dq_idx) ||
+      !aligned16(dk_idx) || ((uintptr_t)block_idx & 3u) || ((uintptr_t)lse & 3u) || ((uintptr_t)kl & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_sparse_attn_bwd_workspace(shape), s);
+  if (st != MSA_OK) return st;
+  return finish(msa::launch_bwd(q, k, v, q_idx, k_idx, block_idx, out, lse, dout, shape->N, shape->H_q, shape->H_kv,
+                                shape->d, shape->d_I, shape->Bk, shape->k, scale, kl_weight, dq, dk, dv, dq_idx,
+                                dk_idx, kl, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
+}
+
 size_t msa_decode_workspace(int B, const msa_shape_t* shape) {
   if (B < 1 || check_shape(shape) != MSA_OK) return kHeader;
   msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,

@@ -73,12 +73,26 @@ cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const
                               const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k_blocks,
                               int64_t nb, int gs, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
                               uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s);
+// The flat tile list of positions [T0, T1) from the CSR (row_ptr, entries): per (g, b)
+// the list's positions cut into tiles of kTilePositions, tile_off[G*nb] = total.
+cudaError_t launch_tile_schedule(const int32_t* row_ptr, const int32_t* entries, int64_t N, int G, int k, int64_t nb,
+                                 int64_t T0, int64_t T1, int64_t max_tiles, int32_t* lo, int32_t* cnt,
+                                 int32_t* tiles, int32_t* tile_off, TileRecord* rec, cudaStream_t s);
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);
 // The select kernel followed by the attention call, on one stream.
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
                            int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
                            void* scratch, DeviceStatus* st, cudaStream_t s);
+
+// ---- backward (msa_bwd.cu)
+size_t bwd_scratch_bytes(int64_t N, int H_q, int H_kv, int d, int Bk, int k);
+// Gradients are fp32 and accumulated in place (the launcher clears them first).
+cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                       const int32_t* block_idx, const void* out, const float* lse, const void* dout, int64_t N,
+                       int H_q, int H_kv, int d, int d_I, int Bk, int kb, float scale, float kl_weight, float* dq,
+                       float* dk, float* dv, float* dq_idx, float* dk_idx, float* kl, void* scratch, DeviceStatus* st,
+                       cudaStream_t s);
 
 // ---- decode (msa_decode.cu)
 // Where token `key` of sequence `seq` sits in a decode cache: contiguous (no

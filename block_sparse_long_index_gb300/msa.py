@@ -43,6 +43,9 @@ _SIGS = {
     "msa_invert_blocks": (_I, [_P, _I64, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "msa_sparse_attn_fwd_workspace": (_SZ, [_SP]),
     "msa_sparse_attn_fwd": (_I, [_P, _P, _P, _P, _SP, _F, _P, _P, _P, _SZ, _P]),
+    "msa_sparse_attn_bwd_workspace": (_SZ, [_SP]),
+    "msa_sparse_attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _SP, _F, _F, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                 _P]),
     "msa_prefill_workspace": (_SZ, [_SP]),
     "msa_prefill": (_I, [_P, _P, _P, _P, _P, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_workspace": (_SZ, [_I, _SP]),
@@ -127,6 +130,19 @@ def msa_sparse_attn_fwd(q, k, v, block_idx, shp, scale, out, lse, workspace, wor
     return _check(_lib.msa_sparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(block_idx), ctypes.byref(shp),
                                            float(scale), _ptr(out), _ptr(lse), _ptr(workspace), wb,
                                            _stream(stream)), "msa_sparse_attn_fwd")
+
+
+def msa_sparse_attn_bwd_workspace(shp):
+    return int(_lib.msa_sparse_attn_bwd_workspace(ctypes.byref(shp)))
+
+
+def msa_sparse_attn_bwd(q, k, v, q_idx, k_idx, block_idx, out, lse, dout, shp, scale, kl_weight, dq, dk, dv, dq_idx,
+                        dk_idx, kl, workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_sparse_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx),
+                                           _ptr(out), _ptr(lse), _ptr(dout), ctypes.byref(shp), float(scale),
+                                           float(kl_weight), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dq_idx), _ptr(dk_idx),
+                                           _ptr(kl), _ptr(workspace), wb, _stream(stream)), "msa_sparse_attn_bwd")
 
 
 def msa_prefill_workspace(shp):

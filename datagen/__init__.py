@@ -39,7 +39,8 @@ _CUDA_SO = os.path.join(_HERE, "libdg_cuda.so")
 
 # tensor ids of the counter-based streams
 TID = dict(q=1, k=2, v=3, q_idx=4, k_idx=5, pick=6,
-           q_t=11, k_cache=12, v_cache=13, q_idx_t=14, k_idx_cache=15, pick_t=16)
+           q_t=11, k_cache=12, v_cache=13, q_idx_t=14, k_idx_cache=15, pick_t=16,
+           dout=21)
 
 SEED_BASE = 0x4D5341
 

@@ -136,6 +136,41 @@ msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
                                  const msa_shape_t* shape, float scale, void* out, float* lse,
                                  void* workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/* ---------------------------------------------------------------- backward
+ * Gradients of msa_sparse_attn_fwd (main branch) and of the index branch's KL
+ * alignment loss, over the same block sets.  Pages: "MSA" study note 4-2 (the
+ * index branch learns from a KL loss against the mean of the GQA group's
+ * main-branch attention probabilities) and 4-3 (the teacher is detached and the
+ * index input gets a stop-gradient: the KL reaches only q^I and k^I);
+ * Flash-MSA "バックワードパス" (both backward passes over the cached sparse
+ * blocks, scheduled through the inverted map B*) and "KLダイバージェンス損失"
+ * (the gradient on the index logits is index probability minus teacher).
+ *
+ * Per row (t, h), group g = h / gs, J = the selected blocks' tokens j <= t:
+ *   P_j = exp(scale q.k_j - lse), D = dout.out, dZ_j = P_j (dout.v_j - D),
+ *   dq = scale sum_j dZ_j k_j, dk_j += scale dZ_j q, dv_j += P_j dout.
+ * Per row (t, g): teacher pbar_j = mean over the group's heads of P_j; index
+ * logits z_j = q^I.k^I_j / sqrt(d_I); p_j = softmax over J of z;
+ *   kl[g, t] = sum_j pbar_j (log pbar_j - log p_j)
+ *   (loss = kl_weight * sum over (t, g) of kl), dL/dz_j = kl_weight (p_j - pbar_j),
+ *   dq_idx = sum_j dL/dz_j k^I_j / sqrt(d_I), dk_idx_j += dL/dz_j q^I / sqrt(d_I).
+ *
+ *   q, k, v, q_idx, k_idx, block_idx, scale: as the forward calls
+ *   out, lse  the forward's outputs for the same inputs
+ *   dout      [N, H_q, d] bf16: gradient of the loss with respect to out
+ *   dq        [N, H_q, d] fp32 out;  dk, dv [N, H_kv, d] fp32 out
+ *   dq_idx    [N, G, d_I] fp32 out;  dk_idx [N, d_I] fp32 out
+ *   kl        [G, N] fp32 out (nullable): each row's KL
+ *   workspace msa_sparse_attn_bwd_workspace(shape) bytes, 256-byte aligned
+ * The gradient outputs are cleared and then accumulated in place on `stream`.
+ */
+size_t msa_sparse_attn_bwd_workspace(const msa_shape_t* shape);
+msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                 const int32_t* block_idx, const void* out, const float* lse, const void* dout,
+                                 const msa_shape_t* shape, float scale, float kl_weight, float* dq, float* dk,
+                                 float* dv, float* dq_idx, float* dk_idx, float* kl, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream);
+
 /* ---------------------------------------------------------------- prefill
  * The whole forward pass in one call: msa_select_blocks followed by
  * msa_sparse_attn_fwd on the same shapes and stream, with the same results.

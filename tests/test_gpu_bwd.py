@@ -1,0 +1,86 @@
+"""Parity of msa_sparse_attn_bwd (through the C ABI) with the fp64 oracle's backward.
+
+The GPU's own select and forward give the block sets, out and lse; the oracle
+recomputes the forward in fp64 on the same sets and writes the gradients out.
+Tolerance: the kernels round P and dZ (and the index branch's dz) to bf16 for
+the tensor-core products (2^-9 relative each), take D = dout.out from the bf16
+forward output, and sum in fp32.  Each row's dZ sums to zero, so dq and dk
+are differences of much larger terms whose rounding errors do not cancel:
+elements can be off by a few percent of the tensor's RMS while the tensor as
+a whole is off by ~0.2 %.  The checks: relative L2 error <= 1e-2 and cosine
+>= 0.999 per tensor (the pages' bf16 correctness sweep uses a cosine
+tolerance of 0.01), cosine >= 0.99 for every row, and every element within
+0.1 rms(ref) + 2e-2 |ref|.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, N, H_q, H_kv, d, d_I, Bk, k, needles
+    ("tiny", 1024, 4, 1, 64, 32, 64, 4, 2),
+    ("ragged_bk64", 1000, 8, 4, 64, 64, 64, 5, 2),
+    ("ragged_bk128_gs8", 2100, 16, 2, 128, 128, 128, 4, 3),
+    ("gs1_bk128", 1536, 4, 4, 128, 64, 128, 6, 2),
+    ("k1_local_only", 777, 4, 2, 128, 32, 128, 1, 0),
+    ("gs2_k8", 3000, 8, 4, 64, 128, 64, 8, 2),
+]
+
+
+def rel_report(gpu, ref):
+    rms = float(np.sqrt(np.mean(ref * ref))) + 1e-30
+    err = np.abs(gpu - ref)
+    l2 = float(np.linalg.norm(gpu - ref) / (np.linalg.norm(ref) + 1e-30))
+    cos = float((gpu * ref).sum() / (np.linalg.norm(gpu) * np.linalg.norm(ref) + 1e-30))
+    g2, r2 = gpu.reshape(gpu.shape[0], -1), ref.reshape(ref.shape[0], -1)
+    rn = np.linalg.norm(r2, axis=1)
+    live = rn > 1e-6 * rn.max()
+    row_cos = (g2 * r2).sum(axis=1)[live] / (np.linalg.norm(g2, axis=1)[live] * rn[live])
+    min_row_cos = float(row_cos.min()) if live.any() else 1.0
+    elem = bool(np.all(err <= 0.1 * rms + 2e-2 * np.abs(ref)))
+    ok = l2 <= 1e-2 and cos >= 0.999 and min_row_cos >= 0.99 and elem
+    return dict(l2=l2, cos=cos, min_row_cos=min_row_cos, max_err_over_rms=float(err.max() / rms), ok=ok)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_bwd_parity(case):
+    from block_sparse_long_index_gb300 import msa
+    name, N, H_q, H_kv, d, d_I, Bk, k, m = case
+    cfg = datagen.make_config(name, N=N, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k, needles=m)
+    h = datagen.prefill_host(cfg)
+    dout = datagen.host_normal(N * H_q * d, cfg.seed, datagen.TID["dout"]).reshape(N, H_q, d)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()  # noqa
+    q, kk, v, qi, ki, do = dev(h["q"]), dev(h["k"]), dev(h["v"]), dev(h["q_idx"]), dev(h["k_idx"]), dev(dout)
+    shp = msa.shape(N, H_q, H_kv, d, d_I, Bk, k)
+    scale, w = 1.0 / math.sqrt(d), 0.7
+    G = H_kv
+    blk = torch.empty((G, N, k), dtype=torch.int32, device="cuda")
+    out = torch.empty((N, H_q, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((H_q, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(msa.msa_prefill_workspace(shp), msa.msa_sparse_attn_bwd_workspace(shp)), dtype=torch.uint8,
+                     device="cuda")
+    msa.msa_prefill(q, kk, v, qi, ki, shp, scale, blk, out, lse, ws)
+    assert msa.msa_check_device_error(ws) == 0
+    f32 = lambda *s: torch.full(s, float("nan"), dtype=torch.float32, device="cuda")  # noqa
+    g = dict(dq=f32(N, H_q, d), dk=f32(N, H_kv, d), dv=f32(N, H_kv, d), dq_idx=f32(N, G, d_I), dk_idx=f32(N, d_I),
+             kl=f32(G, N))
+    for _ in range(2):  # a second call on dirty outputs and workspace gives the same result
+        msa.msa_sparse_attn_bwd(q, kk, v, qi, ki, blk, out, lse, do, shp, scale, w, g["dq"], g["dk"], g["dv"],
+                                g["dq_idx"], g["dk_idx"], g["kl"], ws)
+        assert msa.msa_check_device_error(ws) == 0
+    ref = oracle.sparse_attn_bwd(h["q"], h["k"], h["v"], h["q_idx"], h["k_idx"], blk.cpu().numpy(), dout, Bk, scale, w)
+    reports = {}
+    for nm in ("dq", "dk", "dv", "dq_idx", "dk_idx", "kl"):
+        gpu = g[nm].cpu().numpy().astype(np.float64)
+        assert np.isfinite(gpu).all(), nm
+        reports[nm] = rel_report(gpu, ref[nm])
+    print(name, reports)
+    for nm, r in reports.items():
+        assert r["ok"], (nm, r)
