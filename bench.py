@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
     ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode"],
                     help="time one stage alone on --config (small-memory cases for profiler captures)")
@@ -229,6 +230,33 @@ def bench_prefill(args, dist, torch, peaks):
     att_ms = sum(b.elapsed_time(c) for _, b, c in ev) / K
     assert run.device_status() == 0
     res = dict(cfg=cfg, total_ms=total_ms, sel_ms=sel_ms, att_ms=att_ms, clocks=clk)
+
+    # ---- backward of the same step: main-branch gradients and the index branch's KL gradient
+    if not args.no_backward:
+        from block_sparse_long_index_gb300 import msa
+        N, G = cfg.N, cfg.G
+        dout = datagen.device_normal_(torch.empty((N, cfg.H_q, cfg.d), dtype=torch.bfloat16, device="cuda"),
+                                      cfg.seed, datagen.TID["dout"])
+        f32 = lambda *shp: torch.empty(shp, dtype=torch.float32, device="cuda")  # noqa: E731
+        grads = (f32(N, cfg.H_q, cfg.d), f32(N, cfg.H_kv, cfg.d), f32(N, cfg.H_kv, cfg.d), f32(N, G, cfg.d_I),
+                 f32(N, cfg.d_I), f32(G, N))
+        wsb = torch.empty(msa.msa_sparse_attn_bwd_workspace(run.shape), dtype=torch.uint8, device="cuda")
+        run(q, k, v, qi, ki)
+        scale = 1.0 / math.sqrt(cfg.d)
+        bwd = lambda: msa.msa_sparse_attn_bwd(q, k, v, qi, ki, run.block_idx, run.out, run.lse, dout, run.shape,  # noqa
+                                              scale, 1.0, *grads, wsb)
+        for _ in range(args.warmup):
+            bwd()
+        torch.cuda.synchronize()
+        a, b = E(), E()
+        a.record(stream)
+        for _ in range(K):
+            bwd()
+        b.record(stream)
+        torch.cuda.synchronize()
+        assert msa.msa_check_device_error(wsb) == 0
+        res["bwd_ms"] = a.elapsed_time(b) / K
+        del dout, grads, wsb
 
     # ---- end to end through host buffers (pinned), copies inside the timed region: every step copies
     # its five inputs in and out, lse back; PrefillHostPipeline overlaps those copies with compute
@@ -493,6 +521,19 @@ def main():
                                   "the step runs them as one msa_prefill call"},
             "step_frac_of_tensor_peak": (flops_index + flops_main) / step_s / 1e12 / peak_t,
             "step_tflops": (flops_index + flops_main) / step_s / 1e12}
+    if "bwd_ms" in pre:
+        bms = dist.max(pre["bwd_ms"])
+        bflops = cfg.N * cfg.H_q * cfg.k * cfg.Bk * cfg.d * 10.0 + cfg.N * cfg.G * cfg.k * cfg.Bk * cfg.d_I * 6.0
+        btf = bflops / (bms / 1000.0) / 1e12
+        line["backward"] = {"metric": "prefill backward tokens/s at 128K (main-branch gradients + index KL gradient, "
+                                      "msa_sparse_attn_bwd)", "value": ws * cfg.N / (bms / 1000.0),
+                            "unit": "tokens/s", "ms_per_step": bms,
+                            "roofline": {"bound": "tensor", "achieved": btf, "peak": peak_t, "unit": "TFLOP/s",
+                                         "frac": btf / peak_t, "traffic": None,
+                                         "algorithmic": "N*H_q*k*Bk*d*10 (S, dP, dV, dK, dQ) + N*G*k*Bk*d_I*6 "
+                                                        "(index logits, dk_idx, dq_idx) = %.4g FLOP per call" % bflops,
+                                         "peak_source": "%s bf16_tflops_sustained" % peak_src},
+                            "gpu_launches": 10 * K}
     if "e2e" in pre:
         e = pre["e2e"]
         e_ms = dist.max(e["ms"])

@@ -49,8 +49,11 @@ def _load():
         lib.msa_ref_decode.argtypes = [P, P, P, P, P, P, I, I64, I, I, I, I, I, I, D, P, P, P, P, I]
         lib.msa_ref_sparse_attn_bwd.argtypes = [P, P, P, P, P, P, P, I64, I, I, I, I, I, I, D, D, P, P, P, P, P, P,
                                                 I]
+        lib.msa_ref_sparse_attn_bwd_rows.argtypes = [P, P, P, P, P, P, P, P, I64, I64, I, I, I, I, I, I, D, D, P, P,
+                                                     P, I]
         for f in ("msa_ref_block_scores", "msa_ref_select_blocks", "msa_ref_invert_blocks",
-                  "msa_ref_sparse_attn", "msa_ref_dense_attn", "msa_ref_decode", "msa_ref_sparse_attn_bwd"):
+                  "msa_ref_sparse_attn", "msa_ref_dense_attn", "msa_ref_decode", "msa_ref_sparse_attn_bwd",
+                  "msa_ref_sparse_attn_bwd_rows"):
             getattr(lib, f).restype = I
         _lib = lib
     return _lib
@@ -190,3 +193,22 @@ def sparse_attn_bwd(q, k, v, q_idx, k_idx, block_idx, dout, Bk, scale, kl_weight
                                      n_threads or threads())
     _check(rc, "msa_ref_sparse_attn_bwd")
     return out
+
+
+def sparse_attn_bwd_rows(q, k, v, q_idx, k_idx, block_idx, dout, rows, Bk, scale, kl_weight=1.0, n_threads=None):
+    """The row-local backward outputs (dq [R, H_q, d], dq_idx [R, G, d_I], kl [G, R]) of the listed positions
+    over full-size inputs (msa_oracle.c: msa_ref_sparse_attn_bwd_rows; same arithmetic as sparse_attn_bwd)."""
+    lib = _load()
+    q, k, v, q_idx, k_idx, dout = (_u16(a) for a in (q, k, v, q_idx, k_idx, dout))
+    blk = np.ascontiguousarray(block_idx, dtype=np.int32)
+    rows = _i64(rows)
+    N, H_q, d = q.shape
+    H_kv = k.shape[1]
+    d_I = q_idx.shape[2]
+    R = len(rows)
+    dq, dqi, kl = np.zeros((R, H_q, d)), np.zeros((R, H_kv, d_I)), np.zeros((H_kv, R))
+    rc = lib.msa_ref_sparse_attn_bwd_rows(_p(q), _p(k), _p(v), _p(q_idx), _p(k_idx), _p(blk), _p(dout), _p(rows), R,
+                                          N, H_q, H_kv, d, d_I, Bk, blk.shape[2], float(scale), float(kl_weight),
+                                          _p(dq), _p(dqi), _p(kl), n_threads or threads())
+    _check(rc, "msa_ref_sparse_attn_bwd_rows")
+    return {"dq": dq, "dq_idx": dqi, "kl": kl}

@@ -501,6 +501,8 @@ int msa_ref_decode(const uint16_t* q_t, const uint16_t* q_idx_t, const uint16_t*
 typedef struct {
   const uint16_t *q, *K, *V, *q_idx, *k_idx, *dO;
   const int32_t* blk;
+  const int64_t* rows; /* NULL: every position; else only these (dq, dq_idx and kl rows only) */
+  int64_t n_rows;
   int64_t N, nb;
   int H_q, H_kv, d, d_I, Bk, k, chunks;
   double scale, kl_weight;
@@ -513,12 +515,12 @@ static void bwd_item(int64_t it, void* p) {
   bwd_ctx* c = (bwd_ctx*)p;
   const int g = (int)(it / c->chunks), ch = (int)(it % c->chunks);
   const int gs = c->H_q / c->H_kv, d = c->d, dI = c->d_I;
-  const int64_t r0 = c->N * ch / c->chunks, r1 = c->N * (ch + 1) / c->chunks;
+  const int64_t r0 = c->n_rows * ch / c->chunks, r1 = c->n_rows * (ch + 1) / c->chunks;
   const int64_t cap = (int64_t)c->k * c->Bk;
   const int64_t kv_stride = (int64_t)c->H_kv * d;
-  double* dk_acc = c->dk_acc + it * c->N * d;
-  double* dv_acc = c->dv_acc + it * c->N * d;
-  double* dkI_acc = c->dkI_acc + it * c->N * dI;
+  double* dk_acc = c->dk_acc ? c->dk_acc + it * c->N * d : NULL;
+  double* dv_acc = c->dv_acc ? c->dv_acc + it * c->N * d : NULL;
+  double* dkI_acc = c->dkI_acc ? c->dkI_acc + it * c->N * dI : NULL;
   int64_t* J = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);
   double* P = (double*)malloc(sizeof(double) * (size_t)(cap * gs));
   double* pbar = (double*)malloc(sizeof(double) * (size_t)cap);
@@ -529,7 +531,8 @@ static void bwd_item(int64_t it, void* p) {
     free(J), free(P), free(pbar), free(zI), free(O);
     return;
   }
-  for (int64_t t = r0; t < r1; ++t) {
+  for (int64_t ri = r0; ri < r1; ++ri) {
+    const int64_t t = c->rows ? c->rows[ri] : ri;
     const int64_t nJ = key_set(c->blk + ((int64_t)g * c->N + t) * c->k, c->k, t, c->Bk, c->nb, J);
     for (int64_t i = 0; i < nJ; ++i) pbar[i] = 0.0;
     for (int hh = 0; hh < gs; ++hh) {
@@ -560,12 +563,14 @@ static void bwd_item(int64_t it, void* p) {
         const uint16_t* kr = c->K + J[i] * kv_stride + (int64_t)g * d;
         const uint16_t* vr = c->V + J[i] * kv_stride + (int64_t)g * d;
         const double dZ = Ph[i] * (dot_bf16(dOr, vr, d) - D);
-        double* dkr = dk_acc + J[i] * d;
-        double* dvr = dv_acc + J[i] * d;
-        for (int x = 0; x < d; ++x) {
-          dq[x] += c->scale * dZ * bf16_to_double(kr[x]);
-          dkr[x] += c->scale * dZ * bf16_to_double(qr[x]);
-          dvr[x] += Ph[i] * bf16_to_double(dOr[x]);
+        for (int x = 0; x < d; ++x) dq[x] += c->scale * dZ * bf16_to_double(kr[x]);
+        if (dk_acc) {
+          double* dkr = dk_acc + J[i] * d;
+          double* dvr = dv_acc + J[i] * d;
+          for (int x = 0; x < d; ++x) {
+            dkr[x] += c->scale * dZ * bf16_to_double(qr[x]);
+            dvr[x] += Ph[i] * bf16_to_double(dOr[x]);
+          }
         }
         pbar[i] += Ph[i] / gs;
       }
@@ -593,10 +598,10 @@ static void bwd_item(int64_t it, void* p) {
       if (pbar[i] > 0.0) kl += pbar[i] * (log(pbar[i]) - logpI);
       const double dz = c->kl_weight * (pI - pbar[i]);
       const uint16_t* kIr = c->k_idx + J[i] * dI;
-      double* dkIr = dkI_acc + J[i] * dI;
-      for (int x = 0; x < dI; ++x) {
-        dqI[x] += sI * dz * bf16_to_double(kIr[x]);
-        dkIr[x] += sI * dz * bf16_to_double(qIr[x]);
+      for (int x = 0; x < dI; ++x) dqI[x] += sI * dz * bf16_to_double(kIr[x]);
+      if (dkI_acc) {
+        double* dkIr = dkI_acc + J[i] * dI;
+        for (int x = 0; x < dI; ++x) dkIr[x] += sI * dz * bf16_to_double(qIr[x]);
       }
     }
     *klr = kl;
@@ -630,8 +635,8 @@ int msa_ref_sparse_attn_bwd(const uint16_t* q, const uint16_t* K, const uint16_t
     free(dk_acc), free(dv_acc), free(dkI_acc);
     return ORACLE_NO_MEM;
   }
-  bwd_ctx c = {q, K, V, q_idx, k_idx, dO, block_idx, N, (N + Bk - 1) / Bk, H_q, H_kv, d, d_I, Bk, k, chunks,
-               scale, kl_weight, dq, dq_idx, kl, dk_acc, dv_acc, dkI_acc, 0};
+  bwd_ctx c = {q, K, V, q_idx, k_idx, dO, block_idx, NULL, N, N, (N + Bk - 1) / Bk, H_q, H_kv, d, d_I, Bk, k,
+               chunks, scale, kl_weight, dq, dq_idx, kl, dk_acc, dv_acc, dkI_acc, 0};
   parallel_for(items, n_threads, bwd_item, &c);
   /* sum the items' accumulators */
   for (int64_t j = 0; j < N; ++j) {
@@ -653,5 +658,44 @@ int msa_ref_sparse_attn_bwd(const uint16_t* q, const uint16_t* K, const uint16_t
     }
   }
   free(dk_acc), free(dv_acc), free(dkI_acc);
+  return c.status;
+}
+
+/*
+ * The row-local part of the backward (dq, dq_idx and kl) for the listed
+ * positions only, over the full-size inputs: dq [n_rows, H_q, d], dq_idx
+ * [n_rows, G, d_I], kl [G, n_rows] in list order.  Same arithmetic as
+ * msa_ref_sparse_attn_bwd for those rows.
+ */
+int msa_ref_sparse_attn_bwd_rows(const uint16_t* q, const uint16_t* K, const uint16_t* V, const uint16_t* q_idx,
+                                 const uint16_t* k_idx, const int32_t* block_idx, const uint16_t* dO,
+                                 const int64_t* rows, int64_t n_rows, int64_t N, int H_q, int H_kv, int d, int d_I,
+                                 int Bk, int k, double scale, double kl_weight, double* dq_rows, double* dq_idx_rows,
+                                 double* kl_rows, int n_threads) {
+  if (!q || !K || !V || !q_idx || !k_idx || !block_idx || !dO || !rows || !dq_rows || !dq_idx_rows || !kl_rows ||
+      n_rows <= 0 || N <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 || d_I <= 0 || Bk <= 0 || k < 1)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  /* full-size row outputs, only the listed rows written; copied out in list order */
+  double* dq = (double*)calloc((size_t)(N * H_q * d), sizeof(double));
+  double* dqI = (double*)calloc((size_t)(N * H_kv * d_I), sizeof(double));
+  double* kl = (double*)calloc((size_t)(H_kv * N), sizeof(double));
+  if (!dq || !dqI || !kl) {
+    free(dq), free(dqI), free(kl);
+    return ORACLE_NO_MEM;
+  }
+  int chunks = n_threads / H_kv;
+  if (chunks < 1) chunks = 1;
+  bwd_ctx c = {q, K, V, q_idx, k_idx, dO, block_idx, rows, n_rows, N, (N + Bk - 1) / Bk, H_q, H_kv, d, d_I, Bk, k,
+               chunks, scale, kl_weight, dq, dqI, kl, NULL, NULL, NULL, 0};
+  parallel_for((int64_t)H_kv * chunks, n_threads, bwd_item, &c);
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int64_t t = rows[r];
+    memcpy(dq_rows + r * H_q * d, dq + t * H_q * d, sizeof(double) * (size_t)(H_q * d));
+    memcpy(dq_idx_rows + r * H_kv * d_I, dqI + t * H_kv * d_I, sizeof(double) * (size_t)(H_kv * d_I));
+    for (int g = 0; g < H_kv; ++g) kl_rows[(int64_t)g * n_rows + r] = kl[(int64_t)g * N + t];
+  }
+  free(dq), free(dqI), free(kl);
   return c.status;
 }

@@ -121,3 +121,70 @@ def test_decode_1m_full():
                 hs = slice(g * cfg.gs, (g + 1) * cfg.gs)
                 compare_attn(o[b:b + 1, hs], l[b:b + 1, hs], ref[b:b + 1, hs], ref_lse[b:b + 1, hs])
     assert same.mean() >= 0.75
+
+
+def _bwd_sampled(name, n_rows):
+    """The backward at full size: dq, dq_idx and kl of sampled rows against the oracle (on the GPU's own sets,
+    rules of test_gpu_bwd.py), and over every row the identities sum_j dk_j = 0, sum_j dk_idx_j = 0 and
+    sum_j dv_{j,g} = the sum of the group's dout rows (each row's probabilities sum to 1)."""
+    from test_gpu_bwd import rel_report
+    from block_sparse_long_index_gb300 import msa
+    cfg = datagen.CONFIGS[name]
+    N, G, d, d_I = cfg.N, cfg.G, cfg.d, cfg.d_I
+    dev = datagen.prefill_device(cfg)
+    dout = datagen.device_normal_(torch.empty((N, cfg.H_q, d), dtype=torch.bfloat16, device="cuda"), cfg.seed,
+                                  datagen.TID["dout"])
+    shp = msa.shape(N, cfg.H_q, cfg.H_kv, d, d_I, cfg.Bk, cfg.k)
+    scale, w = 1.0 / math.sqrt(d), 1.0
+    blk = torch.empty((G, N, cfg.k), dtype=torch.int32, device="cuda")
+    out = torch.empty((N, cfg.H_q, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((cfg.H_q, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(msa.msa_prefill_workspace(shp), msa.msa_sparse_attn_bwd_workspace(shp)), dtype=torch.uint8,
+                     device="cuda")
+    msa.msa_prefill(dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"], shp, scale, blk, out, lse, ws)
+    f32 = lambda *s_: torch.empty(s_, dtype=torch.float32, device="cuda")  # noqa: E731
+    g = dict(dq=f32(N, cfg.H_q, d), dk=f32(N, cfg.H_kv, d), dv=f32(N, cfg.H_kv, d), dq_idx=f32(N, G, d_I),
+             dk_idx=f32(N, d_I), kl=f32(G, N))
+    msa.msa_sparse_attn_bwd(dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"], blk, out, lse, dout, shp, scale,
+                            w, g["dq"], g["dk"], g["dv"], g["dq_idx"], g["dk_idx"], g["kl"], ws)
+    assert msa.msa_check_device_error(ws) == 0
+    # identities over every row (fp64 sums of the fp32 gradients)
+    for nm, axis_shape in (("dk", (G, d)), ("dk_idx", (d_I,))):
+        x = g[nm].double()
+        tot = x.sum(dim=0).abs()
+        norm = x.pow(2).sum(dim=0).sqrt()
+        assert float((tot / norm).max()) < 2e-2, nm
+    dv_sum = g["dv"].double().sum(dim=0)                                        # [G, d]
+    do_sum = dout.double().view(N, G, cfg.gs, d).sum(dim=(0, 2))
+    assert float(((dv_sum - do_sum).norm() / do_sum.norm())) < 1e-2
+    # sampled rows against the oracle
+    rows = datagen.sample_rows(N, n_rows, cfg.seed + 17, must=(0, cfg.Bk - 1, cfg.Bk, N - 1))
+    rows_d = torch.from_numpy(rows).cuda()
+    host = datagen.prefill_host(cfg, rows=rows, want=("q", "q_idx", "k", "v", "k_idx"))
+    full = lambda part, shape: _scatter_rows(part, rows, shape)  # noqa: E731
+    q_full = full(host["q"], (N, cfg.H_q, d))
+    qi_full = full(host["q_idx"], (N, G, d_I))
+    do_full = full(datagen.host_normal_rows(rows, cfg.H_q * d, cfg.seed, datagen.TID["dout"]).reshape(-1, cfg.H_q, d),
+                   (N, cfg.H_q, d))
+    ref = oracle.sparse_attn_bwd_rows(q_full, host["k"], host["v"], qi_full, host["k_idx"], blk.cpu().numpy(), do_full,
+                                      rows, cfg.Bk, scale, w)
+    reps = {}
+    for nm, gpu in (("dq", g["dq"][rows_d]), ("dq_idx", g["dq_idx"][rows_d]), ("kl", g["kl"][:, rows_d])):
+        reps[nm] = rel_report(gpu.cpu().numpy().astype(np.float64), ref[nm])
+    print(name, "backward", reps)
+    for nm, r in reps.items():
+        assert r["ok"], (nm, r)
+
+
+def _scatter_rows(part, rows, shape):
+    full = np.zeros(shape, dtype=np.uint16)
+    full[rows] = part
+    return full
+
+
+def test_bwd_32k_sampled():
+    _bwd_sampled("prefill_32k", 256)
+
+
+def test_bwd_128k_sampled():
+    _bwd_sampled("prefill_128k", 64)

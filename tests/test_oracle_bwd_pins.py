@@ -117,3 +117,15 @@ def test_bwd_row_chunking_does_not_change_the_result():
     b = oracle.sparse_attn_bwd(q, kk, v, q_idx, k_idx, blk, dout, Bk, 0.3, 1.0, n_threads=16)
     for name in a:
         np.testing.assert_allclose(a[name], b[name], rtol=1e-12, atol=1e-13, err_msg=name)
+
+
+def test_bwd_rows_mode_equals_full():
+    """The row-local mode (dq, dq_idx, kl of listed positions) reproduces the full backward's rows exactly."""
+    N, H_q, H_kv, d, d_I, Bk, k = 200, 4, 2, 8, 8, 8, 5
+    q, kk, v, q_idx, k_idx, dout, blk = make_case(N, H_q, H_kv, d, d_I, Bk, k, seed=5)
+    a = oracle.sparse_attn_bwd(q, kk, v, q_idx, k_idx, blk, dout, Bk, 0.3, 0.8, n_threads=4)
+    rows = np.array([0, 7, 8, 150, 199, 42, 42])
+    b = oracle.sparse_attn_bwd_rows(q, kk, v, q_idx, k_idx, blk, dout, rows, Bk, 0.3, 0.8, n_threads=3)
+    np.testing.assert_array_equal(b["dq"], a["dq"][rows])
+    np.testing.assert_array_equal(b["dq_idx"], a["dq_idx"][rows])
+    np.testing.assert_array_equal(b["kl"], a["kl"][:, rows])
