@@ -28,9 +28,12 @@
 //               the tiles of a (group, block) and flushed with fp32 reductions;
 //               dZ staged in shared memory, then warps own rows for dQ, added
 //               to dq with fp32 reductions;
-//   index:      the same shape for the index branch: S^T recomputed for the
-//               teacher, the index logits, dzI, dk^I per key slice in
-//               registers, dq^I through shared memory; KL per row.
+//   index:      the same shape for the index branch, with the teacher rows
+//               the main kernel wrote per tile: the index logits, dzI, dk^I
+//               per key slice in registers, dq^I through shared memory; KL
+//               per row.
+// The tile kernels prefetch: while one tile computes, the next tile's rows
+// (and the record after it) arrive by cp.async into a second set of buffers.
 // A block id repeated in a row's set contributes once (its first slot).
 #include <math.h>
 
@@ -121,18 +124,39 @@ __device__ __forceinline__ void tile_range(const int32_t* tile_off, int64_t n_gb
   hi = min(total, lo + per);
 }
 
-// Position t of row r of the tile (p = r / 8, head slot r % 8) or -1: past the
-// tile's count, past gs, or a slot whose block id already appeared earlier in
-// the row's set (the set counts each block once).
-__device__ __forceinline__ int32_t row_position(const TileRecord& rc, int r, int gs, const int32_t* block_idx,
-                                                int64_t N, int k) {
+__device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+// Position t of row r of a tile (p = r / 8, head slot r % 8), or -1 past the
+// tile's count or past gs (and for slots marked as repeats, see mark_repeats).
+__device__ __forceinline__ int32_t row_t(const TileRecord& rc, int r, int gs) {
   const int p = r >> 3, hh = r & 7;
-  if (p >= rc.count || hh >= gs) return -1;
-  const int32_t t = rc.t[p];
-  const int32_t* sel = block_idx + ((int64_t)rc.g * N + t) * k;
-  for (int s2 = 0; s2 < rc.slot[p]; ++s2)
-    if (sel[s2] == rc.b) return -1;
-  return t;
+  return (p < rc.count && hh < gs) ? rc.t[p] : -1;
+}
+
+// Record ti of the list into a shared slot (eight 16-byte copies).
+__device__ __forceinline__ void issue_record(TileRecord* slot, const TileRecord* rec, int64_t ti) {
+  if (threadIdx.x < 8) cp_async_16(reinterpret_cast<char*>(slot) + 16 * threadIdx.x,
+                                   reinterpret_cast<const char*>(rec + ti) + 16 * threadIdx.x, 16);
+}
+
+// A block id repeated in a row's set counts once: its later slots are marked
+// t = -1 in the tile records, so the backward kernels skip them.
+__global__ void mark_repeats_kernel(TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb,
+                                    const int32_t* __restrict__ block_idx, int64_t N, int k) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t tile = i / kPosT;
+  const int p = (int)(i % kPosT);
+  if (tile >= tile_off[n_gb]) return;
+  TileRecord& r = rec[tile];
+  if (p >= r.count) return;
+  const int32_t* sel = block_idx + ((int64_t)r.g * N + r.t[p]) * k;
+  for (int s2 = 0; s2 < r.slot[p]; ++s2)
+    if (sel[s2] == r.b) {
+      r.t[p] = -1;
+      return;
+    }
 }
 
 __device__ __forceinline__ void copy_record(TileRecord* dst, const TileRecord* src) {
@@ -193,7 +217,7 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
       });
     }
     load_rows(qIs, kPosT, DI, q_idx, [&](int p) -> const uint16_t* {
-      return p < rc.count ? q_idx + ((int64_t)rc.t[p] * G + rc.g) * DI : nullptr;
+      return p < rc.count && rc.t[p] >= 0 ? q_idx + ((int64_t)rc.t[p] * G + rc.g) * DI : nullptr;
     });
     cp_async_commit();
     cp_async_wait<0>();
@@ -215,7 +239,7 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int p = nt * 8 + 2 * c4 + e;
-        const int64_t t = p < rc.count ? rc.t[p] : -1;
+        const int64_t t = p < rc.count ? rc.t[p] : -1;  // -1: no position, or a repeated block
         float m = __int_as_float(0xff800000);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -257,7 +281,7 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
 #pragma unroll
         for (int e = 0; e < 2; ++e) red_l[warp][nt * 8 + 2 * c4 + e] = mx[nt][e];
     __syncthreads();
-    if (tid < rc.count) {
+    if (tid < rc.count && rc.t[tid] >= 0) {
       float M = __int_as_float(0xff800000), L = 0.f;
       for (int w = 0; w < KSL; ++w) M = fmaxf(M, red_m[w][tid]);
       for (int w = 0; w < KSL; ++w) L += red_l[w][tid];
@@ -291,9 +315,12 @@ __global__ void bwd_index_lse_combine_kernel(const float2* __restrict__ part, co
 }
 
 // ------------------------------------------------------------------ main branch
+// Shared memory: K and V rows of the current (group, block); two sets of the
+// tile's Q and dO rows (the next tile's land while this one computes); dZ.
 template <int D, int BK>
 struct MainSmem {
-  static constexpr int K = 0, V = BK * D * 2, Q = 2 * BK * D * 2, DO = Q + kRowsT * D * 2, DZ = DO + kRowsT * D * 2;
+  static constexpr int K = 0, V = BK * D * 2, Q = 2 * BK * D * 2, DO = Q + 2 * kRowsT * D * 2,
+                       DZ = DO + 2 * kRowsT * D * 2;
   static constexpr int BYTES = DZ + kRowsT * BK * 2;
 };
 
@@ -301,26 +328,26 @@ template <int D, int BK>
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
     const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
-    const int32_t* __restrict__ block_idx, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
-    int64_t n_gb, int64_t N, int H_q, int H_kv, int gs, int k, float scale, float* __restrict__ dq,
-    float* __restrict__ dk, float* __restrict__ dv) {
+    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int H_q,
+    int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+    float* __restrict__ pbar_g) {
   using L = MainSmem<D, BK>;
   extern __shared__ __align__(128) uint8_t smb[];
   uint16_t* Ks = reinterpret_cast<uint16_t*>(smb + L::K);
   uint16_t* Vs = reinterpret_cast<uint16_t*>(smb + L::V);
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smb + L::Q);
-  uint16_t* dOs = reinterpret_cast<uint16_t*>(smb + L::DO);
   uint16_t* dZs = reinterpret_cast<uint16_t*>(smb + L::DZ);
-  __shared__ float lse_s[kRowsT], D_s[kRowsT];
-  __shared__ int32_t t_s[kRowsT];
-  __shared__ __align__(16) TileRecord rc;
+  __shared__ float lse_s[2][kRowsT], D_s[2][kRowsT];
+  __shared__ int32_t tpos_s[2][kPosT];  // position of each of the tile's 16 positions (-1: none)
+  __shared__ __align__(16) TileRecord rc_s[3];
   constexpr int KSL = BK / 16;   // key slices of 16
   constexpr int RG = 8 / KSL;    // row groups (1 or 2)
   constexpr int RPW = kRowsT / RG;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
   const int ksl = warp % KSL, rg = warp / KSL;
-  const uint32_t Ks_a = smem_u32(Ks), Vs_a = smem_u32(Vs), Qs_a = smem_u32(Qs), dOs_a = smem_u32(dOs),
-                 dZs_a = smem_u32(dZs);
+  const float inv_gs = 1.f / (float)gs;
+  const uint32_t Ks_a = smem_u32(Ks), Vs_a = smem_u32(Vs), dZs_a = smem_u32(dZs);
+  auto Qs = [&](int b) { return reinterpret_cast<uint16_t*>(smb + L::Q + b * kRowsT * D * 2); };
+  auto dOs = [&](int b) { return reinterpret_cast<uint16_t*>(smb + L::DO + b * kRowsT * D * 2); };
   float accK[D / 8][4], accV[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i)
@@ -348,12 +375,47 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
 #pragma unroll
       for (int e = 0; e < 4; ++e) accK[i][e] = accV[i][e] = 0.f;
   };
+  // the rows of tile ti (record in slot ti % 3) into buffer b: positions, lse, D, Q and dO, all asynchronous
+  auto issue_rows = [&](int64_t ti, int b) {
+    const TileRecord& rc = rc_s[ti % 3];
+    const int g = rc.g;
+    if (tid < kPosT) tpos_s[b][tid] = tid < rc.count ? rc.t[tid] : -1;
+    for (int r = tid; r < kRowsT; r += blockDim.x) {
+      const int32_t t = row_t(rc, r, gs);
+      if (t >= 0) {
+        const int64_t h = g * gs + (r & 7);
+        cp_async_4(&lse_s[b][r], lse + h * N + t);
+        cp_async_4(&D_s[b][r], Dr + h * N + t);
+      } else {
+        lse_s[b][r] = __int_as_float(0x7f800000);
+        D_s[b][r] = 0.f;
+      }
+    }
+    load_rows(Qs(b), kRowsT, D, q, [&](int r) -> const uint16_t* {
+      const int32_t t = row_t(rc, r, gs);
+      return t >= 0 ? q + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
+    });
+    load_rows(dOs(b), kRowsT, D, dout, [&](int r) -> const uint16_t* {
+      const int32_t t = row_t(rc, r, gs);
+      return t >= 0 ? dout + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
+    });
+  };
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
-  for (int64_t ti = lo; ti < hi; ++ti) {
-    __syncthreads();  // the previous tile is done with every buffer
-    copy_record(&rc, rec + ti);
+  if (lo < hi) {
+    issue_record(&rc_s[lo % 3], rec, lo);
+    if (lo + 1 < hi) issue_record(&rc_s[(lo + 1) % 3], rec, lo + 1);
+    cp_async_commit();
+    cp_async_wait<0>();
     __syncthreads();
+    issue_rows(lo, 0);
+    cp_async_commit();
+  }
+  for (int64_t ti = lo; ti < hi; ++ti) {
+    const int buf = (int)((ti - lo) & 1);
+    cp_async_wait<0>();  // this tile's rows and the next record
+    __syncthreads();
+    const TileRecord& rc = rc_s[ti % 3];
     if (rc.gb != cur_gb) {
       flush();
       cur_gb = rc.gb;
@@ -368,28 +430,19 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
         const int64_t j = (int64_t)cur_b * BK + r;
         return j < N ? vc + j * kv_row + (int64_t)cur_g * D : nullptr;
       });
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
     }
-    for (int r = tid; r < kRowsT; r += blockDim.x) {
-      const int32_t t = row_position(rc, r, gs, block_idx, N, k);
-      t_s[r] = t;
-      const int h = cur_g * gs + (r & 7);
-      lse_s[r] = t >= 0 ? lse[(int64_t)h * N + t] : __int_as_float(0x7f800000);
-      D_s[r] = t >= 0 ? Dr[(int64_t)h * N + t] : 0.f;
-    }
-    __syncthreads();
-    load_rows(Qs, kRowsT, D, q, [&](int r) -> const uint16_t* {
-      const int32_t t = t_s[r];
-      return t >= 0 ? q + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D : nullptr;
-    });
-    load_rows(dOs, kRowsT, D, dout, [&](int r) -> const uint16_t* {
-      const int32_t t = t_s[r];
-      return t >= 0 ? dout + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D : nullptr;
-    });
+    // the next tile's rows and the record after it, while this tile computes
+    if (ti + 2 < hi) issue_record(&rc_s[(ti + 2) % 3], rec, ti + 2);
+    if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
     cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
+    const uint32_t Qs_a = smem_u32(Qs(buf)), dOs_a = smem_u32(dOs(buf));
+    // position of row r, or -1 (no position, a repeated block, or a head slot past gs)
+    auto row_pos = [&](int r) -> int32_t { return (r & 7) < gs ? tpos_s[buf][r >> 3] : -1; };
 
-    // ---- phase A: this warp's 16 keys against its rows, 16 rows at a time
+    // ---- phase A: this warp's 16 keys against its rows, 16 rows (two positions) at a time
     const int key0 = ksl * 16;
     for (int rc0 = 0; rc0 < RPW; rc0 += 16) {
       const int row0 = rg * RPW + rc0;
@@ -404,14 +457,15 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
         lds_b_nk(b, dOs_a, row0, kk, D);
         mma2(dp[0], dp[1], a, b);
       }
-      // element (key g8 + 8 half, row row0 + 8 nt + 2 c4 + e): P^T and dZ^T
+      // element (key g8 + 8 half, row row0 + 8 nt + 2 c4 + e): P^T and dZ^T; n-tile nt = one position
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt) {
+        float tsum[2] = {0.f, 0.f};  // teacher: sum of P over the position's head slots
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int r = row0 + nt * 8 + 2 * c4 + e;
-          const int32_t t = t_s[r];
-          const float ls = lse_s[r], dd = D_s[r];
+          const int32_t t = row_pos(r);
+          const float ls = lse_s[buf][r], dd = D_s[buf][r];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int64_t j = (int64_t)cur_b * BK + key0 + g8 + 8 * half;
@@ -422,9 +476,23 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
             }
             s[nt][2 * half + e] = pv;
             dp[nt][2 * half + e] = zv;
+            tsum[half] += pv;
             st_bf16(dZs, r, key0 + g8 + 8 * half, BK, zv);
           }
         }
+        if (pbar_g) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            tsum[half] += __shfl_xor_sync(0xffffffffu, tsum[half], 1);
+            tsum[half] += __shfl_xor_sync(0xffffffffu, tsum[half], 2);
+          }
+          if (c4 == 0) {
+            float* pb = pbar_g + (ti * kPosT + row0 / 8 + nt) * BK + key0 + g8;
+            pb[0] = tsum[0] * inv_gs;
+            pb[8] = tsum[1] * inv_gs;
+          }
+        }
+      }
       uint32_t pa[4], za[4];
       c_to_a(pa, s[0], s[1]);
       c_to_a(za, dp[0], dp[1]);
@@ -459,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int r = r0 + g8 + 8 * half;
-        const int32_t t = t_s[r];
+        const int32_t t = row_pos(r);
         if (t >= 0) {
           float* p = dq + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D + 2 * c4;
 #pragma unroll
@@ -473,51 +541,41 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
 }
 
 // ------------------------------------------------------------------ index branch
-template <int D, int BK, int DI>
+// Shared memory: the block's index keys; two sets of the tile's index queries
+// and teacher rows (from the main kernel); dzI.
+template <int BK, int DI>
 struct IndexSmem {
-  static constexpr int K = 0, Q = BK * D * 2, KI = Q + kRowsT * D * 2, QI = KI + BK * DI * 2, DZ = QI + kPosT * DI * 2,
-                       PB = DZ + kPosT * BK * 2;
-  static constexpr int BYTES = PB + kPosT * BK * 4;
+  static constexpr int KI = 0, QI = BK * DI * 2, PB = QI + 2 * kPosT * DI * 2, DZ = PB + 2 * kPosT * BK * 4;
+  static constexpr int BYTES = DZ + kPosT * BK * 2;
 };
 
-template <int D, int BK, int DI>
+template <int BK, int DI>
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
-    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ q_idx,
-    const uint16_t* __restrict__ k_idx, const float* __restrict__ lse, const float* __restrict__ lseI,
-    const int32_t* __restrict__ block_idx, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
-    int64_t n_gb, int64_t N, int H_q, int H_kv, int gs, int k, float scale, float sI, float w,
-    float* __restrict__ dq_idx, float* __restrict__ dk_idx, float* __restrict__ kl) {
-  using L = IndexSmem<D, BK, DI>;
+    const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const float* __restrict__ lseI,
+    const float* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
+    int64_t n_gb, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
+    float* __restrict__ kl) {
+  using L = IndexSmem<BK, DI>;
   extern __shared__ __align__(128) uint8_t smb[];
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(smb + L::K);
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smb + L::Q);
   uint16_t* kIs = reinterpret_cast<uint16_t*>(smb + L::KI);
-  uint16_t* qIs = reinterpret_cast<uint16_t*>(smb + L::QI);
   uint16_t* dzs = reinterpret_cast<uint16_t*>(smb + L::DZ);
-  float* pbar_s = reinterpret_cast<float*>(smb + L::PB);  // [position][key]
-  __shared__ float lse_s[kRowsT];
-  __shared__ int32_t t_s[kRowsT];
-  __shared__ float lseI_s[kPosT];
-  __shared__ int32_t tp_s[kPosT];  // position of tile position p, or -1
-  __shared__ __align__(16) TileRecord rc;
+  __shared__ float lseI_s[2][kPosT];
+  __shared__ int32_t tp_s[2][kPosT];
+  __shared__ __align__(16) TileRecord rc_s[3];
   constexpr int KSL = BK / 16;
-  constexpr int RG = 8 / KSL;
-  constexpr int RPW = kRowsT / RG;
-  const int G = H_kv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
-  const int ksl = warp % KSL, rg = warp / KSL;
-  const uint32_t Ks_a = smem_u32(Ks), Qs_a = smem_u32(Qs), kIs_a = smem_u32(kIs), qIs_a = smem_u32(qIs),
-                 dzs_a = smem_u32(dzs);
-  const float inv_gs = 1.f / (float)gs;
+  const uint32_t kIs_a = smem_u32(kIs), dzs_a = smem_u32(dzs);
+  auto qIs = [&](int b) { return reinterpret_cast<uint16_t*>(smb + L::QI + b * kPosT * DI * 2); };
+  auto pbs = [&](int b) { return reinterpret_cast<float*>(smb + L::PB + b * kPosT * BK * 4); };
   float accI[DI / 8][4];
 #pragma unroll
   for (int i = 0; i < DI / 8; ++i) accI[i][0] = accI[i][1] = accI[i][2] = accI[i][3] = 0.f;
   int cur_gb = -1, cur_g = 0, cur_b = 0;
   auto flush = [&]() {
-    if (cur_gb < 0) return;
+    if (cur_gb < 0 || warp >= KSL) return;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      const int64_t j = (int64_t)cur_b * BK + ksl * 16 + g8 + 8 * half;
+      const int64_t j = (int64_t)cur_b * BK + warp * 16 + g8 + 8 * half;
       if (j < N) {
         float* p = dk_idx + j * DI + 2 * c4;
 #pragma unroll
@@ -527,92 +585,60 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
 #pragma unroll
     for (int i = 0; i < DI / 8; ++i) accI[i][0] = accI[i][1] = accI[i][2] = accI[i][3] = 0.f;
   };
+  auto issue_rows = [&](int64_t ti, int b) {
+    const TileRecord& rc = rc_s[ti % 3];
+    if (tid < kPosT) {
+      const int32_t t = tid < rc.count ? rc.t[tid] : -1;
+      tp_s[b][tid] = t;
+      if (t >= 0) cp_async_4(&lseI_s[b][tid], lseI + (int64_t)rc.g * N + t);
+      else lseI_s[b][tid] = __int_as_float(0x7f800000);
+    }
+    load_rows(qIs(b), kPosT, DI, q_idx, [&](int p) -> const uint16_t* {
+      const int32_t t = p < rc.count ? rc.t[p] : -1;
+      return t >= 0 ? q_idx + ((int64_t)t * G + rc.g) * DI : nullptr;
+    });
+    const float* src = pbar_g + ti * kPosT * BK;  // the teacher rows the main kernel wrote for this tile
+    float* dst = pbs(b);
+    for (int i = tid; i < kPosT * BK / 4; i += blockDim.x) cp_async_16(dst + 4 * i, src + 4 * i, 16);
+  };
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
+  if (lo < hi) {
+    issue_record(&rc_s[lo % 3], rec, lo);
+    if (lo + 1 < hi) issue_record(&rc_s[(lo + 1) % 3], rec, lo + 1);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    issue_rows(lo, 0);
+    cp_async_commit();
+  }
   for (int64_t ti = lo; ti < hi; ++ti) {
+    const int buf = (int)((ti - lo) & 1);
+    cp_async_wait<0>();
     __syncthreads();
-    copy_record(&rc, rec + ti);
-    __syncthreads();
+    const TileRecord& rc = rc_s[ti % 3];
     if (rc.gb != cur_gb) {
       flush();
       cur_gb = rc.gb;
       cur_g = rc.g;
       cur_b = rc.b;
-      const int64_t kv_row = (int64_t)H_kv * D;
-      load_rows(Ks, BK, D, kc, [&](int r) -> const uint16_t* {
-        const int64_t j = (int64_t)cur_b * BK + r;
-        return j < N ? kc + j * kv_row + (int64_t)cur_g * D : nullptr;
-      });
       load_rows(kIs, BK, DI, k_idx, [&](int r) -> const uint16_t* {
         const int64_t j = (int64_t)cur_b * BK + r;
         return j < N ? k_idx + j * DI : nullptr;
       });
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncthreads();
     }
-    for (int r = tid; r < kRowsT; r += blockDim.x) {
-      const int32_t t = row_position(rc, r, gs, block_idx, N, k);
-      t_s[r] = t;
-      lse_s[r] = t >= 0 ? lse[(int64_t)(cur_g * gs + (r & 7)) * N + t] : __int_as_float(0x7f800000);
-    }
-    __syncthreads();
-    if (tid < kPosT) {  // head slot 0 of a position is a real head whenever the position is
-      const int32_t t = t_s[tid * 8];
-      tp_s[tid] = t;
-      lseI_s[tid] = t >= 0 ? lseI[(int64_t)cur_g * N + t] : __int_as_float(0x7f800000);
-    }
-    load_rows(Qs, kRowsT, D, q, [&](int r) -> const uint16_t* {
-      const int32_t t = t_s[r];
-      return t >= 0 ? q + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D : nullptr;
-    });
-    load_rows(qIs, kPosT, DI, q_idx, [&](int p) -> const uint16_t* {
-      const int32_t t = t_s[p * 8];
-      return t >= 0 ? q_idx + ((int64_t)t * G + cur_g) * DI : nullptr;
-    });
+    if (ti + 2 < hi) issue_record(&rc_s[(ti + 2) % 3], rec, ti + 2);
+    if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
     cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
+    const uint32_t qIs_a = smem_u32(qIs(buf));
+    const float* pb_s = pbs(buf);
 
-    // ---- teacher: pbar[p][key] = mean over the position's heads of P, for this warp's keys and rows
-    const int key0 = ksl * 16;
-    for (int rc0 = 0; rc0 < RPW; rc0 += 16) {
-      const int row0 = rg * RPW + rc0;
-      float s[2][4] = {};
-#pragma unroll
-      for (int kk = 0; kk < D; kk += 16) {
-        uint32_t a[4], b[4];
-        lds_a(a, Ks_a, key0, kk, D);
-        lds_b_nk(b, Qs_a, row0, kk, D);
-        mma2(s[0], s[1], a, b);
-      }
-      // n-tile nt holds the 8 head slots of position row0 / 8 + nt
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float sum[2] = {0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int r = row0 + nt * 8 + 2 * c4 + e;
-          const int32_t t = t_s[r];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int64_t j = (int64_t)cur_b * BK + key0 + g8 + 8 * half;
-            if (t >= 0 && j <= t) sum[half] += __expf(s[nt][2 * half + e] * scale - lse_s[r]);
-          }
-        }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          sum[half] += __shfl_xor_sync(0xffffffffu, sum[half], 1);
-          sum[half] += __shfl_xor_sync(0xffffffffu, sum[half], 2);
-        }
-        if (c4 == 0) {
-          const int p = row0 / 8 + nt;
-          pbar_s[p * BK + key0 + g8] = sum[0] * inv_gs;
-          pbar_s[p * BK + key0 + g8 + 8] = sum[1] * inv_gs;
-        }
-      }
-    }
-    __syncthreads();
-
-    // ---- index logits of this warp's keys for all 16 positions, dzI and the KL terms
-    if (rg == 0) {
+    // ---- index logits of this warp's 16 keys for the 16 positions, dzI and the KL terms
+    if (warp < KSL) {
+      const int key0 = warp * 16;
       float zi[2][4] = {};
 #pragma unroll
       for (int kk = 0; kk < DI; kk += 16) {
@@ -627,15 +653,15 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int p = nt * 8 + 2 * c4 + e;
-          const int32_t t = tp_s[p];
+          const int32_t t = tp_s[buf][p];
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int key = key0 + g8 + 8 * half;
             const int64_t j = (int64_t)cur_b * BK + key;
             float dz = 0.f;
             if (t >= 0 && j <= t) {
-              const float logp = zi[nt][2 * half + e] * sI - lseI_s[p];
-              const float pb = pbar_s[p * BK + key];
+              const float logp = zi[nt][2 * half + e] * sI - lseI_s[buf][p];
+              const float pb = pb_s[p * BK + key];
               dz = w * (__expf(logp) - pb);
               if (pb > 0.f) klp[nt][e] += pb * (__logf(pb) - logp);
             }
@@ -652,7 +678,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
 #pragma unroll
             for (int o = 4; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
             const int p = nt * 8 + 2 * c4 + e;
-            if (g8 == 0 && tp_s[p] >= 0) atomicAdd(kl + (int64_t)cur_g * N + tp_s[p], x);
+            if (g8 == 0 && tp_s[buf][p] >= 0) atomicAdd(kl + (int64_t)cur_g * N + tp_s[buf][p], x);
           }
       }
       // dk^I of these keys += dzI^T q^I (k = the 16 positions)
@@ -680,7 +706,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int p = g8 + 8 * half;
-        const int32_t t = tp_s[p];
+        const int32_t t = tp_s[buf][p];
         if (t >= 0) {
           float* pp = dq_idx + ((int64_t)t * G + cur_g) * DI + warp * 16 + 2 * c4;
           red_add2(pp, sI * acc[0][2 * half], sI * acc[0][2 * half + 1]);
@@ -700,6 +726,7 @@ struct BwdScratch {
   TileRecord* rec;
   float *Dr, *lseI;
   float2* partI;
+  float* pbar;  // [tile][16 positions][Bk keys]: the teacher, written by the main kernel
   int64_t max_tiles, nb;
 };
 
@@ -727,6 +754,7 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
   s.Dr = (float*)take((size_t)H_q * N * 4);
   s.lseI = (float*)take((size_t)G * N * 4);
   s.partI = (float2*)take((size_t)G * N * k * 8);
+  s.pbar = (float*)take((size_t)s.max_tiles * kPosT * Bk * 4);
   if (out) *out = s;
   return off;
 }
@@ -750,16 +778,16 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
   e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, MainSmem<D, BK>::BYTES);
   if (e != cudaSuccess) return e;
   km<<<grid, kThreadsB, MainSmem<D, BK>::BYTES, s>>>((const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v,
-                                                    (const uint16_t*)dout, lse, sc.Dr, block_idx, sc.rec,
-                                                    sc.tile_off, n_gb, N, H_q, H_kv, gs, k, scale, dq, dk, dv);
+                                                    (const uint16_t*)dout, lse, sc.Dr, sc.rec, sc.tile_off, n_gb, N,
+                                                    H_q, H_kv, gs, scale, dq, dk, dv, sc.pbar);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto ki = bwd_index_kernel<D, BK, DI>;
-  e = cudaFuncSetAttribute(ki, cudaFuncAttributeMaxDynamicSharedMemorySize, IndexSmem<D, BK, DI>::BYTES);
+  auto ki = bwd_index_kernel<BK, DI>;
+  e = cudaFuncSetAttribute(ki, cudaFuncAttributeMaxDynamicSharedMemorySize, IndexSmem<BK, DI>::BYTES);
   if (e != cudaSuccess) return e;
-  ki<<<grid, kThreadsB, IndexSmem<D, BK, DI>::BYTES, s>>>(
-      (const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)q_idx, (const uint16_t*)k_idx, lse, sc.lseI,
-      block_idx, sc.rec, sc.tile_off, n_gb, N, H_q, H_kv, gs, k, scale, sI, kl_weight, dq_idx, dk_idx, kl);
+  ki<<<grid, kThreadsB, IndexSmem<BK, DI>::BYTES, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.lseI,
+                                                      sc.pbar, sc.rec, sc.tile_off, n_gb, N, G, sI, kl_weight, dq_idx,
+                                                      dk_idx, kl);
   return cudaGetLastError();
 }
 
@@ -805,6 +833,9 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   if ((e = launch_tile_schedule(sc.row_ptr, sc.entries, N, G, kb, sc.nb, 0, N, sc.max_tiles, sc.lo, sc.cnt, sc.tiles,
                                 sc.tile_off, sc.rec, s)) != cudaSuccess)
     return e;
+  mark_repeats_kernel<<<(unsigned)ceil_div(sc.max_tiles * kPosT, 256), 256, 0, s>>>(sc.rec, sc.tile_off,
+                                                                                   (int64_t)G * sc.nb, block_idx, N,
+                                                                                   kb);
   bwd_rowdot_kernel<<<(unsigned)ceil_div(N * H_q * 32, 256), 256, 0, s>>>((const uint16_t*)dout,
                                                                         (const uint16_t*)out, N, H_q, d, sc.Dr);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
