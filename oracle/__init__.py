@@ -43,6 +43,10 @@ def _load():
         P, I64, I, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
         lib.msa_ref_block_scores.argtypes = [P, P, P, I64, I64, I, I, I, P, I]
         lib.msa_ref_select_blocks.argtypes = [P, P, P, I64, I64, I, I, I, I, P, P, I]
+        lib.msa_ref_e4m3_decode.argtypes = [P, I64, P]
+        lib.msa_ref_e4m3_quantize.argtypes = [P, I64, ctypes.c_float, P]
+        lib.msa_ref_block_scores_e4m3.argtypes = [P, P, P, I64, I64, I, I, I, P, I]
+        lib.msa_ref_select_blocks_e4m3.argtypes = [P, P, P, I64, I64, I, I, I, I, P, P, I]
         lib.msa_ref_invert_blocks.argtypes = [P, I64, I, I, I, P, P, P]
         lib.msa_ref_sparse_attn.argtypes = [P, P, P, P, P, I64, I64, I, I, I, I, I, D, P, P, I]
         lib.msa_ref_dense_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, D, P, P, I]
@@ -105,6 +109,46 @@ def select_blocks(q_idx_rows, k_idx, rows, N, Bk, k, n_threads=None):
     kth = np.empty((G, n_rows, 2), np.float64)
     _check(_load().msa_ref_select_blocks(_p(q_idx_rows), _p(k_idx), _p(rows), n_rows, N, G, d_I, Bk, k, _p(blk),
                                          _p(kth), n_threads or threads()), "msa_ref_select_blocks")
+    return blk, kth
+
+
+def e4m3_decode(codes):
+    """Values (fp64) of FP8 E4M3 codes (OCP 8-bit floating point specification, E4M3)."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _check(_load().msa_ref_e4m3_decode(_p(codes), codes.size, _p(out)), "msa_ref_e4m3_decode")
+    return out
+
+
+def e4m3_quantize(x_bf16, scale=1.0):
+    """E4M3 codes of the fp32 products (bf16 x) * scale: nearest, ties to even, saturated at 448."""
+    x = _u16(x_bf16)
+    codes = np.empty(x.shape, np.uint8)
+    _check(_load().msa_ref_e4m3_quantize(_p(x), x.size, float(scale), _p(codes)), "msa_ref_e4m3_quantize")
+    return codes
+
+
+def block_scores_e4m3(q_idx_rows, k_idx, rows, N, Bk, n_threads=None):
+    """block_scores on FP8 E4M3 index inputs (chipsbuilder "Co-Design Del Kernel": FP8 precision)."""
+    q_idx_rows, k_idx = np.ascontiguousarray(q_idx_rows, np.uint8), np.ascontiguousarray(k_idx, np.uint8)
+    rows = _i64(rows)
+    n_rows, G, d_I = q_idx_rows.shape
+    nb = (N + Bk - 1) // Bk
+    S = np.empty((n_rows, G, nb), np.float64)
+    _check(_load().msa_ref_block_scores_e4m3(_p(q_idx_rows), _p(k_idx), _p(rows), n_rows, N, G, d_I, Bk, _p(S),
+                                             n_threads or threads()), "msa_ref_block_scores_e4m3")
+    return S
+
+
+def select_blocks_e4m3(q_idx_rows, k_idx, rows, N, Bk, k, n_threads=None):
+    """select_blocks on FP8 E4M3 index inputs: the same rule on the exactly decoded scores."""
+    q_idx_rows, k_idx = np.ascontiguousarray(q_idx_rows, np.uint8), np.ascontiguousarray(k_idx, np.uint8)
+    rows = _i64(rows)
+    n_rows, G, d_I = q_idx_rows.shape
+    blk = np.empty((G, n_rows, k), np.int32)
+    kth = np.empty((G, n_rows, 2), np.float64)
+    _check(_load().msa_ref_select_blocks_e4m3(_p(q_idx_rows), _p(k_idx), _p(rows), n_rows, N, G, d_I, Bk, k,
+                                              _p(blk), _p(kth), n_threads or threads()), "msa_ref_select_blocks_e4m3")
     return blk, kth
 
 

@@ -52,8 +52,8 @@
  *   logits q^I.k^I / sqrt(d_I); the loss is kl_weight * sum over (t, g) of
  *   KL(teacher || index); the main branch receives dO only.
  *
- * Arithmetic: bf16 inputs widened exactly to double; every dot product,
- * maximum, exponential and sum in double.
+ * Arithmetic: bf16 (or FP8 E4M3) inputs widened exactly to double; every
+ * dot product, maximum, exponential and sum in double.
  */
 #include <math.h>
 #include <pthread.h>
@@ -237,6 +237,153 @@ int msa_ref_select_blocks(const uint16_t* q_idx_rows, const uint16_t* k_idx, con
     if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
   select_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, k, NULL, block_idx, kth, 0};
   parallel_for(n_rows * G, n_threads, select_item, &c);
+  return c.status;
+}
+
+/* ------------------------------------------- FP8 (E4M3) index inputs */
+/*
+ * [P2] "Co-Design Del Kernel" lists FP8 among the precisions of the pages'
+ * kernel, and [P1] 6 "Limitations" 1 notes that the index branch scores the
+ * whole context, so the index inputs are the ones worth narrowing.  Reading:
+ * q^I and k^I are stored as FP8 E4M3 codes, every product and sum of the
+ * scores is exact arithmetic on the decoded values (fp64 here), and the
+ * selection rule is unchanged.  A positive factor applied to all of q^I or
+ * all of k^I before the cast leaves every row's ordering unchanged, so the
+ * selection needs no scale.
+ *
+ * The encoding is the E4M3 format of the OCP 8-bit floating point
+ * specification: sign bit, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent field 0 holds the subnormals (m/8) 2^-6; S.1111.111 is NaN; there
+ * is no infinity, and the largest finite magnitude is 1.75 * 2^8 = 448.
+ */
+static double e4m3_to_double(uint8_t c) {
+  int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/*
+ * Nearest E4M3 code of the float value v, ties to the even code (round to
+ * nearest even), magnitudes past 448 saturated to 448 (there is no
+ * infinity to overflow to); NaN gives the positive NaN code 0x7F.
+ */
+static uint8_t e4m3_from_float(float v) {
+  if (isnan(v)) return 0x7F;
+  uint8_t s = signbit(v) ? 0x80 : 0x00;
+  double a = fabs((double)v);
+  if (a >= 448.0) return (uint8_t)(s | 0x7E);
+  /* spacing of the codes around a: 2^(e-3) in binade [2^e, 2^(e+1)) for
+   * e >= -6, and the subnormal spacing 2^-9 below 2^-6 */
+  int E;
+  frexp(a, &E); /* a = f 2^E with f in [0.5, 1): a lies in binade E-1 */
+  int e = E - 1;
+  if (a == 0.0 || e < -6) e = -6;
+  double q = ldexp(1.0, e - 3);
+  double r = rint(a / q) * q; /* a / q is exact; rint rounds half to even */
+  if (r == 0.0) return s;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(s | (int)(r / ldexp(1.0, -9)));
+  frexp(r, &E);
+  e = E - 1;
+  int m = (int)((r / ldexp(1.0, e) - 1.0) * 8.0);
+  return (uint8_t)(s | ((e + 7) << 3) | m);
+}
+
+/* Decoded values of n E4M3 codes. */
+int msa_ref_e4m3_decode(const uint8_t* codes, int64_t n, double* out) {
+  if ((!codes || !out) && n > 0) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(codes[i]);
+  return ORACLE_OK;
+}
+
+/* codes[i] = E4M3 code of the float product (bf16 x[i]) * scale. */
+int msa_ref_e4m3_quantize(const uint16_t* x, int64_t n, float scale, uint8_t* codes) {
+  if ((!x || !codes) && n > 0) return ORACLE_BAD_ARG;
+  for (int64_t i = 0; i < n; ++i) {
+    float xf = (float)bf16_to_double(x[i]);
+    float p = xf * scale;
+    codes[i] = e4m3_from_float(p);
+  }
+  return ORACLE_OK;
+}
+
+/* Step 1 on E4M3 inputs: the same block maxima of the decoded scores. */
+static void block_scores_row_e4m3(const uint8_t* qrow, const uint8_t* k_idx, int64_t t, int d_I, int Bk,
+                                  int64_t nb, double* S) {
+  double inv = 1.0 / sqrt((double)d_I);
+  double q[512];
+  for (int c = 0; c < d_I; ++c) q[c] = e4m3_to_double(qrow[c]);
+  for (int64_t b = 0; b < nb; ++b) S[b] = -INFINITY;
+  for (int64_t j = 0; j <= t; ++j) {
+    const uint8_t* kr = k_idx + j * d_I;
+    double s = 0.0;
+    for (int c = 0; c < d_I; ++c) s += q[c] * e4m3_to_double(kr[c]);
+    s *= inv;
+    int64_t b = j / Bk;
+    if (s > S[b]) S[b] = s;
+  }
+}
+
+typedef struct {
+  const uint8_t* q_idx_rows; /* [n_rows, G, d_I] E4M3 */
+  const uint8_t* k_idx;      /* [N, d_I] E4M3 */
+  const int64_t* rows;
+  int64_t n_rows, N, nb;
+  int G, d_I, Bk, k;
+  double* S;
+  int32_t* blk;
+  double* kth;
+  int status;
+} select8_ctx;
+
+static void select8_item(int64_t it, void* p) {
+  select8_ctx* c = (select8_ctx*)p;
+  int64_t r = it / c->G;
+  int g = (int)(it % c->G);
+  int64_t t = c->rows[r];
+  double* S = c->S ? c->S + (r * c->G + g) * c->nb : (double*)malloc(sizeof(double) * (size_t)c->nb);
+  unsigned char* taken = (unsigned char*)malloc((size_t)c->nb + 1);
+  if (!S || !taken) {
+    c->status = ORACLE_NO_MEM;
+    if (!c->S) free(S);
+    free(taken);
+    return;
+  }
+  block_scores_row_e4m3(c->q_idx_rows + (r * c->G + g) * c->d_I, c->k_idx, t, c->d_I, c->Bk, c->nb, S);
+  if (c->blk)
+    topk_row(S, t, c->Bk, c->k, c->blk + ((int64_t)g * c->n_rows + r) * c->k,
+             c->kth ? c->kth + ((int64_t)g * c->n_rows + r) * 2 : NULL, taken);
+  if (!c->S) free(S);
+  free(taken);
+}
+
+/* msa_ref_block_scores on E4M3 codes. */
+int msa_ref_block_scores_e4m3(const uint8_t* q_idx_rows, const uint8_t* k_idx, const int64_t* rows,
+                              int64_t n_rows, int64_t N, int G, int d_I, int Bk, double* S, int n_threads) {
+  if (!q_idx_rows || !k_idx || !rows || !S || N <= 0 || G <= 0 || d_I <= 0 || d_I > 512 || Bk <= 0)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  select8_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, 0, S, NULL, NULL, 0};
+  parallel_for(n_rows * G, n_threads, select8_item, &c);
+  return c.status;
+}
+
+/* msa_ref_select_blocks on E4M3 codes. */
+int msa_ref_select_blocks_e4m3(const uint8_t* q_idx_rows, const uint8_t* k_idx, const int64_t* rows,
+                               int64_t n_rows, int64_t N, int G, int d_I, int Bk, int k, int32_t* block_idx,
+                               double* kth, int n_threads) {
+  if (!q_idx_rows || !k_idx || !rows || !block_idx || N <= 0 || G <= 0 || d_I <= 0 || d_I > 512 || Bk <= 0 ||
+      k < 1)
+    return ORACLE_BAD_ARG;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  select8_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, k, NULL, block_idx, kth, 0};
+  parallel_for(n_rows * G, n_threads, select8_item, &c);
   return c.status;
 }
 
