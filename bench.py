@@ -42,8 +42,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) index-input variants")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
-    ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode"],
+    ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode", "select_fp8",
+                                                       "decode_fp8"],
                     help="time one stage alone on --config (small-memory cases for profiler captures)")
     return ap.parse_args()
 
@@ -258,6 +260,35 @@ def bench_prefill(args, dist, torch, peaks):
         res["bwd_ms"] = a.elapsed_time(b) / K
         del dout, grads, wsb
 
+    # ---- the same step on FP8 (E4M3) index inputs: msa_prefill_fp8 (q, k, v stay bf16)
+    if not args.no_fp8:
+        from block_sparse_long_index_gb300 import msa
+        q8 = torch.empty(qi.shape, dtype=torch.uint8, device="cuda")
+        k8 = torch.empty(ki.shape, dtype=torch.uint8, device="cuda")
+        quant = lambda: (msa.msa_quantize_e4m3(qi, qi.numel(), 1.0, q8),  # noqa: E731
+                         msa.msa_quantize_e4m3(ki, ki.numel(), 1.0, k8))
+        scale = 1.0 / math.sqrt(cfg.d)
+        step8 = lambda: msa.msa_prefill_fp8(q, k, v, q8, k8, run.shape, scale, run.block_idx, run.out,  # noqa
+                                            run.lse, run.workspace)
+        sel8 = lambda: msa.msa_select_blocks_fp8(q8, k8, cfg.N, cfg.G, cfg.d_I, cfg.Bk, cfg.k,  # noqa: E731
+                                                 run.block_idx, run.workspace)
+        quant()
+        for _ in range(args.warmup):
+            step8()
+        torch.cuda.synchronize()
+        tm = {}
+        for name, fn in (("quant", quant), ("step", step8), ("select", sel8)):
+            a, b = E(), E()
+            a.record(stream)
+            for _ in range(K):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            tm[name] = a.elapsed_time(b) / K
+        assert run.device_status() == 0
+        res["fp8"] = dict(step_ms=tm["step"], sel_ms=tm["select"], quant_ms=tm["quant"])
+        del q8, k8
+
     # ---- end to end through host buffers (pinned), copies inside the timed region: every step copies
     # its five inputs in and out, lse back; PrefillHostPipeline overlaps those copies with compute
     if not args.no_e2e:
@@ -351,6 +382,29 @@ def bench_decode(args, dist, torch):
     assert run.device_status() == 0
     tp = sorted(a.elapsed_time(b) for a, b in evp)
     res["paged"] = dict(mean_ms=sum(tp) / K, median_ms=tp[K // 2], page=page)
+    # the same step with an FP8 (E4M3) index-key cache and index query (msa_decode_fp8)
+    if not args.no_fp8:
+        ki8 = torch.empty(inp["k_idx_cache"].shape, dtype=torch.uint8, device="cuda")
+        qi8 = torch.empty(inp["q_idx_t"].shape, dtype=torch.uint8, device="cuda")
+        msa.msa_quantize_e4m3(inp["k_idx_cache"], ki8.numel(), 1.0, ki8)
+        msa.msa_quantize_e4m3(inp["q_idx_t"], qi8.numel(), 1.0, qi8)
+        dec8 = lambda: msa.msa_decode_fp8(inp["q_t"], qi8, ki8, inp["k_cache"], inp["v_cache"],  # noqa: E731
+                                          inp["ctx_len"], cfg.B, run.shape, scale, run.out, run.lse, run.block_idx,
+                                          run.workspace)
+        for _ in range(args.warmup):
+            dec8()
+        torch.cuda.synchronize()
+        ev8 = [(E(), E()) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev8[i][0].record(stream)
+            dec8()
+            ev8[i][1].record(stream)
+        torch.cuda.synchronize()
+        assert run.device_status() == 0
+        t8 = sorted(a.elapsed_time(b) for a, b in ev8)
+        res["fp8"] = dict(mean_ms=sum(t8) / K, median_ms=t8[K // 2])
+        del ki8, qi8
     del inp, run, flush
     torch.cuda.empty_cache()
     return res
@@ -418,21 +472,37 @@ def run_stage(args):
     from block_sparse_long_index_gb300 import msa
     cfg = datagen.CONFIGS[args.config]
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    if args.stage == "decode":
+    if args.stage in ("decode", "decode_fp8"):
         from block_sparse_long_index_gb300 import MsaDecode
         inp = datagen.decode_device(cfg)
         run = MsaDecode(cfg.B, cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
         call = lambda: run(inp["q_t"], inp["q_idx_t"], inp["k_idx_cache"], inp["k_cache"], inp["v_cache"],  # noqa
                            inp["ctx_len"])
+        if args.stage == "decode_fp8":
+            ki8 = torch.empty(inp["k_idx_cache"].shape, dtype=torch.uint8, device="cuda")
+            qi8 = torch.empty(inp["q_idx_t"].shape, dtype=torch.uint8, device="cuda")
+            msa.msa_quantize_e4m3(inp["k_idx_cache"], ki8.numel(), 1.0, ki8)
+            msa.msa_quantize_e4m3(inp["q_idx_t"], qi8.numel(), 1.0, qi8)
+            del inp["k_idx_cache"]
+            call = lambda: msa.msa_decode_fp8(inp["q_t"], qi8, ki8, inp["k_cache"], inp["v_cache"],  # noqa
+                                              inp["ctx_len"], cfg.B, run.shape, 1.0 / math.sqrt(cfg.d), run.out,
+                                              run.lse, run.block_idx, run.workspace)
     else:
-        want = ("q_idx", "k_idx") if args.stage == "select" else ("q", "k", "v", "q_idx", "k_idx")
+        want = ("q_idx", "k_idx") if args.stage.startswith("select") else ("q", "k", "v", "q_idx", "k_idx")
         inp = datagen.prefill_device(cfg, want=want)
         blk = torch.empty((cfg.G, cfg.N, cfg.k), dtype=torch.int32, device="cuda")
         ws_sel = torch.empty(msa.msa_select_blocks_workspace(cfg.N, cfg.G, cfg.d_I, cfg.Bk, cfg.k),
                              dtype=torch.uint8, device="cuda")
         select = lambda: msa.msa_select_blocks(inp["q_idx"], inp["k_idx"], cfg.N, cfg.G, cfg.d_I, cfg.Bk,  # noqa
                                                cfg.k, blk, ws_sel)
-        if args.stage == "select":
+        if args.stage == "select_fp8":
+            q8 = torch.empty(inp["q_idx"].shape, dtype=torch.uint8, device="cuda")
+            k8 = torch.empty(inp["k_idx"].shape, dtype=torch.uint8, device="cuda")
+            msa.msa_quantize_e4m3(inp["q_idx"], q8.numel(), 1.0, q8)
+            msa.msa_quantize_e4m3(inp["k_idx"], k8.numel(), 1.0, k8)
+            call = lambda: msa.msa_select_blocks_fp8(q8, k8, cfg.N, cfg.G, cfg.d_I, cfg.Bk, cfg.k, blk,  # noqa
+                                                     ws_sel)
+        elif args.stage == "select":
             call = select
         else:
             select()
@@ -542,6 +612,23 @@ def main():
                        "how": "PrefillHostPipeline: per step pinned host -> device copies of q, k, v, q_idx, k_idx, "
                               "select + attention, device -> pinned host copies of out and lse; copies of one "
                               "step overlap the compute of its neighbours"}
+    if "fp8" in pre:
+        f8 = pre["fp8"]
+        f8_ms = dist.max(f8["step_ms"])
+        peak8 = 2.0 * peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        sel8_tf = flops_index / (f8["sel_ms"] / 1000.0) / 1e12
+        line["prefill_fp8"] = {
+            "metric": "prefill tokens/s at 128K with FP8 (E4M3) index inputs (msa_prefill_fp8)",
+            "value": ws * cfg.N / (f8_ms / 1000.0), "unit": "tokens/s", "ms_per_step": f8_ms,
+            "stages_ms": {"select_fp8": f8["sel_ms"], "quantize_q_idx_k_idx": f8["quant_ms"]},
+            "note": "the step takes q_idx and k_idx already in E4M3 (as an index projection emitting FP8 would); "
+                    "msa_quantize_e4m3 of both from bf16 is timed apart",
+            "roofline_select": {"bound": "tensor", "achieved": sel8_tf, "peak": peak8, "unit": "TFLOP/s",
+                                "frac": sel8_tf / peak8, "traffic": None,
+                                "algorithmic": "(N^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index,
+                                "peak_source": "%s bf16_tflops_sustained x 2 (nominal fp8/bf16 dense ratio "
+                                               "4.5/2.25)" % peak_src},
+            "gpu_launches": (prefill_launches(cfg)) * K}
     if not args.no_decode:
         dec = bench_decode(args, dist, torch)
         dcfg = dec["cfg"]
@@ -570,6 +657,21 @@ def main():
                                              "frac": pbw / hbm, "traffic": None,
                                              "peak_source": "%s hbm_gbs" % peak_src},
                                 "gpu_launches": 2 * dec["steps"]}
+        if "fp8" in dec:
+            f8 = dec["fp8"]
+            f8_ms = dist.max(f8["mean_ms"])
+            bytes8 = dcfg.B * (dcfg.ctx * dcfg.d_I * 1 + dcfg.k * dcfg.Bk * 2 * dcfg.H_kv * dcfg.d * 2)
+            bw8 = bytes8 / (f8_ms / 1000.0) / 1e9
+            line["decode_fp8"] = {"metric": "decode tokens/s at 1M ctx with an FP8 (E4M3) index-key cache "
+                                            "(msa_decode_fp8)",
+                                  "value": ws * dcfg.B / (f8_ms / 1000.0), "unit": "tokens/s", "ms_per_step": f8_ms,
+                                  "median_ms": f8["median_ms"],
+                                  "roofline": {"bound": "hbm", "achieved": bw8, "peak": hbm, "unit": "GB/s",
+                                               "frac": bw8 / hbm, "traffic": None,
+                                               "algorithmic": "B*(ctx*d_I*1 + k*Bk*2*H_kv*d*2) = %d bytes per step"
+                                                              % bytes8,
+                                               "peak_source": "%s hbm_gbs" % peak_src},
+                                  "gpu_launches": 2 * dec["steps"]}
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         dt, n, th = oracle_prefill_sample(cfg, args.cpu_rows)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": th, "kind": "oracle",

@@ -46,14 +46,15 @@ static CUtensorMapSwizzle swizzle_of(int swizzle_bytes) {
 }
 
 bool encode_tmap_2d(void* tmap, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
-                    uint32_t box_inner, uint32_t box_rows, int swizzle_bytes) {
+                    uint32_t box_inner, uint32_t box_rows, int swizzle_bytes, int elem_bytes) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
   if (!encode) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = encode(reinterpret_cast<CUtensorMap*>(tmap), dt, 2,
                       const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                       swizzle_of(swizzle_bytes), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -144,16 +145,35 @@ size_t msa_select_blocks_workspace(int64_t N, int G, int d_I, int Bk, int k) {
   return kHeader;
 }
 
-msa_status_t msa_select_blocks(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
-                               int32_t* block_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+static msa_status_t select_impl(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
+                                int32_t* block_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream,
+                                bool f8) {
   if (!q_idx || !k_idx || !block_idx) return MSA_ERR_INVALID_ARGUMENT;
   msa_status_t st = check_common(N, G, d_I, Bk, k);
   if (st != MSA_OK) return st;
+  if (f8 && d_I == 32) return MSA_ERR_UNSUPPORTED;
   if (!aligned16(q_idx) || !aligned16(k_idx) || ((uintptr_t)block_idx & 3u)) return MSA_ERR_INVALID_ARGUMENT;
   cudaStream_t s = (cudaStream_t)stream;
   st = begin(workspace, workspace_bytes, msa_select_blocks_workspace(N, G, d_I, Bk, k), s);
   if (st != MSA_OK) return st;
-  return finish(msa::launch_select(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, (msa::DeviceStatus*)workspace, s));
+  return finish(
+      msa::launch_select(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, (msa::DeviceStatus*)workspace, s, f8));
+}
+
+msa_status_t msa_select_blocks(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
+                               int32_t* block_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return select_impl(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, workspace, workspace_bytes, stream, false);
+}
+
+msa_status_t msa_select_blocks_fp8(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
+                                   int32_t* block_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return select_impl(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, workspace, workspace_bytes, stream, true);
+}
+
+msa_status_t msa_quantize_e4m3(const void* x, int64_t n, float scale, void* y, msa_stream_t stream) {
+  if (n < 0 || ((!x || !y) && n > 0)) return MSA_ERR_INVALID_ARGUMENT;
+  if (((uintptr_t)x & 1u) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  return finish(msa::launch_quantize_e4m3(x, n, scale, y, (cudaStream_t)stream));
 }
 
 size_t msa_invert_blocks_workspace(int64_t N, int G, int Bk, int k) {
@@ -207,12 +227,13 @@ size_t msa_prefill_workspace(const msa_shape_t* shape) {
   return kHeader + msa::attn_scratch_bytes(p);
 }
 
-msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
-                         const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
-                         void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+static msa_status_t prefill_impl(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                 const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, msa_stream_t stream, bool f8) {
   if (!q || !k || !v || !q_idx || !k_idx || !block_idx || !out || !lse) return MSA_ERR_INVALID_ARGUMENT;
   msa_status_t st = check_shape(shape);
   if (st != MSA_OK) return st;
+  if (f8 && shape->d_I == 32) return MSA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_idx) || !aligned16(k_idx) ||
       !aligned16(out) || ((uintptr_t)block_idx & 3u) || ((uintptr_t)lse & 3u))
@@ -222,7 +243,21 @@ msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void
   if (st != MSA_OK) return st;
   msa::AttnPlan p = msa::attn_plan(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
   return finish(msa::launch_prefill(q, k, v, q_idx, k_idx, shape->d_I, p, scale, block_idx, out, lse,
-                                    (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
+                                    (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s, f8));
+}
+
+msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                         const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return prefill_impl(q, k, v, q_idx, k_idx, shape, scale, block_idx, out, lse, workspace, workspace_bytes, stream,
+                      false);
+}
+
+msa_status_t msa_prefill_fp8(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                             const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return prefill_impl(q, k, v, q_idx, k_idx, shape, scale, block_idx, out, lse, workspace, workspace_bytes, stream,
+                      true);
 }
 
 size_t msa_sparse_attn_bwd_workspace(const msa_shape_t* shape) {
@@ -260,14 +295,15 @@ size_t msa_decode_workspace(int B, const msa_shape_t* shape) {
   return kHeader + msa::decode_scratch_bytes(p);
 }
 
-msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
-                        const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
-                        void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
-                        msa_stream_t stream) {
+static msa_status_t decode_impl(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                                const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape,
+                                float scale, void* out, float* lse, int32_t* block_idx, void* workspace,
+                                size_t workspace_bytes, msa_stream_t stream, bool f8) {
   if (!q_t || !q_idx_t || !k_idx_cache || !k_cache || !v_cache || !ctx_len || !out) return MSA_ERR_INVALID_ARGUMENT;
   if (B < 1) return MSA_ERR_INVALID_ARGUMENT;
   msa_status_t st = check_shape(shape);
   if (st != MSA_OK) return st;
+  if (f8 && shape->d_I == 32) return MSA_ERR_UNSUPPORTED;
   if (shape->H_kv > 8) return MSA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
   if (!aligned16(q_t) || !aligned16(q_idx_t) || !aligned16(k_idx_cache) || !aligned16(k_cache) ||
@@ -277,23 +313,42 @@ msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_
   cudaStream_t s = (cudaStream_t)stream;
   msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,
                                        shape->k);
+  p.f8 = f8;
   st = begin(workspace, workspace_bytes, msa_decode_workspace(B, shape), s, kHeader + msa::decode_clear_bytes(p));
   if (st != MSA_OK) return st;
   return finish(msa::launch_decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, p, scale, out, lse,
                                    block_idx, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
 }
 
-msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* k_idx_pool, const void* k_pool,
-                              const void* v_pool, const int32_t* page_table, int64_t max_pages, int64_t n_pages,
-                              int page_size, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
-                              void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
-                              msa_stream_t stream) {
+msa_status_t msa_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                        const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                        void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                        msa_stream_t stream) {
+  return decode_impl(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shape, scale, out, lse, block_idx,
+                     workspace, workspace_bytes, stream, false);
+}
+
+msa_status_t msa_decode_fp8(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                            const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                            void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                            msa_stream_t stream) {
+  return decode_impl(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shape, scale, out, lse, block_idx,
+                     workspace, workspace_bytes, stream, true);
+}
+
+static msa_status_t decode_paged_impl(const void* q_t, const void* q_idx_t, const void* k_idx_pool,
+                                      const void* k_pool, const void* v_pool, const int32_t* page_table,
+                                      int64_t max_pages, int64_t n_pages, int page_size, const int32_t* ctx_len, int B,
+                                      const msa_shape_t* shape, float scale, void* out, float* lse,
+                                      int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                                      msa_stream_t stream, bool f8) {
   if (!q_t || !q_idx_t || !k_idx_pool || !k_pool || !v_pool || !page_table || !ctx_len || !out)
     return MSA_ERR_INVALID_ARGUMENT;
   if (B < 1 || max_pages < 1 || n_pages < 1 || page_size < 16 || page_size % 16 != 0) return MSA_ERR_INVALID_ARGUMENT;
   msa_status_t st = check_shape(shape);
   if (st != MSA_OK) return st;
   if (shape->N != max_pages * (int64_t)page_size) return MSA_ERR_INVALID_ARGUMENT;  // capacity of a sequence
+  if (f8 && shape->d_I == 32) return MSA_ERR_UNSUPPORTED;
   if (shape->H_kv > 8) return MSA_ERR_UNSUPPORTED;
   if (n_pages > (int64_t)1 << 31) return MSA_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
@@ -306,6 +361,7 @@ msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* 
                                        shape->k);
   st = begin(workspace, workspace_bytes, msa_decode_workspace(B, shape), s, kHeader + msa::decode_clear_bytes(p));
   if (st != MSA_OK) return st;
+  p.f8 = f8;
   msa::CacheMap map;
   map.table = page_table;
   map.max_pages = max_pages;
@@ -313,6 +369,24 @@ msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* 
   map.page = page_size;
   return finish(msa::launch_decode(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, ctx_len, p, scale, out, lse, block_idx,
                                    (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s, &map));
+}
+
+msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* k_idx_pool, const void* k_pool,
+                              const void* v_pool, const int32_t* page_table, int64_t max_pages, int64_t n_pages,
+                              int page_size, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                              void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                              msa_stream_t stream) {
+  return decode_paged_impl(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, page_table, max_pages, n_pages, page_size,
+                           ctx_len, B, shape, scale, out, lse, block_idx, workspace, workspace_bytes, stream, false);
+}
+
+msa_status_t msa_decode_paged_fp8(const void* q_t, const void* q_idx_t, const void* k_idx_pool, const void* k_pool,
+                                  const void* v_pool, const int32_t* page_table, int64_t max_pages, int64_t n_pages,
+                                  int page_size, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                                  void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                                  msa_stream_t stream) {
+  return decode_paged_impl(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, page_table, max_pages, n_pages, page_size,
+                           ctx_len, B, shape, scale, out, lse, block_idx, workspace, workspace_bytes, stream, true);
 }
 
 // The decode step without a caller workspace: its scratch is the library's

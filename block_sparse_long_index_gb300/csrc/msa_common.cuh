@@ -87,6 +87,16 @@ __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, cons
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// D = A(16x32 e4m3, row) * B(32x8 e4m3, col) + D, fp32 accumulate.  Each
+// fragment register holds four consecutive k of one row (A) or column (B).
+__device__ __forceinline__ void mma_e4m3_16832(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 // Programmatic dependent launch: a primary grid lets its dependent grid be
 // scheduled; the dependent waits for the primary's completion and memory.
 __device__ __forceinline__ void griddep_launch_dependents() {

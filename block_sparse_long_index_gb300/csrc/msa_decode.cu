@@ -37,11 +37,17 @@ constexpr int kGroupsPerMma = 8;    // mma n = 8 groups
 constexpr int kMergeListsPerLane = 16;  // last-CTA merge: splits <= 32 * 16
 constexpr int kMaxCtaBlocks = 2048;     // block maxima kept in shared memory per scan CTA
 
-// dims of fragment column kf (0..15) in k-step ks: see the load pattern below
+// dims of fragment column kf (0..15) in k-step ks of the bf16 scan: see the load pattern below
 __device__ __forceinline__ int frag_dim(int ks, int kf) {
   int p = ks >> 1, half = ks & 1;
   int c = (kf & 7) >> 1, e = kf & 1, hi = kf >> 3;
   return 32 * p + 8 * c + 4 * half + 2 * hi + e;
+}
+// the same for the E4M3 scan (m16n8k32: fragment column kf in 0..31, four codes per register)
+__device__ __forceinline__ int frag_dim8(int ks, int kf) {
+  int p = ks >> 1, half = ks & 1;
+  int c = (kf & 15) >> 2, e = kf & 3, hi = kf >> 4;
+  return 64 * p + 16 * c + 8 * half + 4 * hi + e;
 }
 
 // fp32 -> unsigned with the same order (-0 folded to +0); 0 is below every value
@@ -50,12 +56,13 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int DI>
-__device__ __forceinline__ void load_keys16(uint4 (&v)[DI / 32][2], const uint16_t* p) {
+// 16-byte pieces 64q + 16c of key rows `row` and `row + 8` of a 16-key chunk (RB bytes per row)
+template <int RB>
+__device__ __forceinline__ void load_keys16(uint4 (&v)[RB / 64][2], const uint8_t* p) {
 #pragma unroll
-  for (int q = 0; q < DI / 32; ++q) {
-    v[q][0] = ldg_stream_16(p + 32 * q);
-    v[q][1] = ldg_stream_16(p + 8 * DI + 32 * q);
+  for (int q = 0; q < RB / 64; ++q) {
+    v[q][0] = ldg_stream_16(p + 64 * q);
+    v[q][1] = ldg_stream_16(p + 8 * RB + 64 * q);
   }
 }
 
@@ -63,13 +70,19 @@ __device__ __forceinline__ void load_keys16(uint4 (&v)[DI / 32][2], const uint16
 // the candidates are the blocks before the query's local block.  The CTA's
 // 16-key chunks are divided evenly among its warps; a block whose chunks fall
 // to two warps gets its maximum from both through the shared-memory atomic.
-template <int DI, int BK, bool PAGED>
+// F8: the index query and cache hold E4M3 codes; the same 16-byte pieces feed
+// m16n8k32 E4M3 MMAs (32 dims per k-step instead of 16), so a key row is half
+// the bytes and the scan reads half the cache traffic.
+template <int DI, int BK, bool PAGED, bool F8>
 __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
-    const uint16_t* __restrict__ q_idx_t, const uint16_t* __restrict__ k_idx_cache,
+    const uint8_t* __restrict__ q_idx_t, const uint8_t* __restrict__ k_idx_cache,
     const int32_t* __restrict__ ctx_len, int64_t ctx_max, CacheMap map, int G, int k, int splits,
     uint64_t* __restrict__ cand, unsigned int* __restrict__ tickets, int32_t* __restrict__ block_idx,
     DeviceStatus* st) {
-  constexpr int KS = DI / 16;
+  constexpr int RB = DI * (F8 ? 1 : 2);  // bytes per index row
+  constexpr int NQ = RB / 64;            // 16-byte pieces per lane and row
+  constexpr int KS = 2 * NQ;             // MMA k-steps per 16-key chunk
+  static_assert(NQ >= 1, "index rows of at least 64 bytes");
   constexpr int CPB = BK / 16;  // chunks per block
   extern __shared__ uint32_t bmax_s[];  // [blocks of this CTA][8 groups], ordered_bits of the block maxima
   __shared__ int s_last;
@@ -97,9 +110,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
       for (int r = 0; r < 2; ++r) {
         uint32_t w = 0;
         if (n < G) {
-          const uint16_t* qp = q_idx_t + ((int64_t)seq * G + n) * DI;
-          int d0 = frag_dim(ks, 2 * c + 8 * r), d1 = frag_dim(ks, 2 * c + 1 + 8 * r);
-          w = (uint32_t)qp[d0] | ((uint32_t)qp[d1] << 16);
+          const uint8_t* qrow = q_idx_t + ((int64_t)seq * G + n) * RB;
+          if (F8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w |= (uint32_t)qrow[frag_dim8(ks, 16 * r + 4 * c + e)] << (8 * e);
+          } else {
+            const uint16_t* qp = reinterpret_cast<const uint16_t*>(qrow);
+            int d0 = frag_dim(ks, 2 * c + 8 * r), d1 = frag_dim(ks, 2 * c + 1 + 8 * r);
+            w = (uint32_t)qp[d0] | ((uint32_t)qp[d1] << 16);
+          }
         }
         qf[ks][r] = w;
       }
@@ -109,23 +128,29 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   // this warp's chunks [c0, c1) of the CTA's nblk * CPB
   const int64_t nch = (int64_t)nblk * CPB;
   const int64_t c0 = nch * warp / kScanWarps, c1 = nch * (warp + 1) / kScanWarps;
-  const uint16_t* base = k_idx_cache + ((int64_t)seq * ctx_max + b_lo * BK + row) * DI + 8 * c;
+  const uint8_t* base = k_idx_cache + ((int64_t)seq * ctx_max + b_lo * BK + row) * RB + 16 * c;
   // first key row of chunk cc (+ row): contiguous, or through the page table (a page holds whole chunks)
-  auto chunk_ptr = [&](int64_t cc) -> const uint16_t* {
-    if (!PAGED) return base + cc * 16 * DI;
+  auto chunk_ptr = [&](int64_t cc) -> const uint8_t* {
+    if (!PAGED) return base + cc * 16 * RB;
     const int64_t key = b_lo * BK + cc * 16;
     const int64_t r = map.row(seq, key, st);
-    return k_idx_cache + (r + row) * DI + 8 * c;
+    return k_idx_cache + (r + row) * RB + 16 * c;
   };
   float bm0 = __int_as_float(0xff800000), bm1 = bm0;
-  auto score = [&](const uint4 (&v)[DI / 32][2], int64_t cc) {
+  auto score = [&](const uint4 (&v)[NQ][2], int64_t cc) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < DI / 32; ++q) {
-      const uint32_t a0[4] = {v[q][0].x, v[q][1].x, v[q][0].y, v[q][1].y};  // k-step 2q: dims +0..3 of each 8
-      const uint32_t a1[4] = {v[q][0].z, v[q][1].z, v[q][0].w, v[q][1].w};  // k-step 2q+1: dims +4..7
-      mma_bf16_16816(acc, a0, qf[2 * q]);
-      mma_bf16_16816(acc, a1, qf[2 * q + 1]);
+    for (int q = 0; q < NQ; ++q) {
+      // k-step 2q: bytes 0..7 of each lane's piece; k-step 2q+1: bytes 8..15
+      const uint32_t a0[4] = {v[q][0].x, v[q][1].x, v[q][0].y, v[q][1].y};
+      const uint32_t a1[4] = {v[q][0].z, v[q][1].z, v[q][0].w, v[q][1].w};
+      if (F8) {
+        mma_e4m3_16832(acc, a0, qf[2 * q]);
+        mma_e4m3_16832(acc, a1, qf[2 * q + 1]);
+      } else {
+        mma_bf16_16816(acc, a0, qf[2 * q]);
+        mma_bf16_16816(acc, a1, qf[2 * q + 1]);
+      }
     }
     bm0 = fmaxf(bm0, fmaxf(acc[0], acc[2]));  // group 2c, keys row and row+8
     bm1 = fmaxf(bm1, fmaxf(acc[1], acc[3]));  // group 2c+1
@@ -142,13 +167,13 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
       bm0 = bm1 = __int_as_float(0xff800000);
     }
   };
-  uint4 va[DI / 32][2], vb[DI / 32][2];
-  if (c0 < c1) load_keys16<DI>(va, chunk_ptr(c0));
+  uint4 va[NQ][2], vb[NQ][2];
+  if (c0 < c1) load_keys16<RB>(va, chunk_ptr(c0));
   for (int64_t ci = c0; ci < c1; ci += 2) {  // one chunk in flight ahead of the one being scored
-    if (ci + 1 < c1) load_keys16<DI>(vb, chunk_ptr(ci + 1));
+    if (ci + 1 < c1) load_keys16<RB>(vb, chunk_ptr(ci + 1));
     score(va, ci);
     if (ci + 1 < c1) {
-      if (ci + 2 < c1) load_keys16<DI>(va, chunk_ptr(ci + 2));
+      if (ci + 2 < c1) load_keys16<RB>(va, chunk_ptr(ci + 2));
       score(vb, ci + 1);
     }
   }
@@ -488,16 +513,16 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   return off;
 }
 
-template <int DI, int BK, bool PAGED>
+template <int DI, int BK, bool PAGED, bool F8>
 cudaError_t launch_scan_t(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
                           const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
                           cudaStream_t s) {
   const size_t smem = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
-  auto kern = decode_scan_kernel<DI, BK, PAGED>;
+  auto kern = decode_scan_kernel<DI, BK, PAGED, F8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
-      (const uint16_t*)q_idx_t, (const uint16_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits,
+      (const uint8_t*)q_idx_t, (const uint8_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits,
       sc.cand, sc.tickets, blk, st);
   return cudaGetLastError();
 }
@@ -505,8 +530,15 @@ cudaError_t launch_scan_t(const void* q_idx_t, const void* k_idx_cache, const in
 template <int DI, int BK>
 cudaError_t launch_scan(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
                         const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st, cudaStream_t s) {
-  return map.table ? launch_scan_t<DI, BK, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                   : launch_scan_t<DI, BK, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+  if constexpr (DI >= 64) {  // E4M3 rows of 64 or 128 bytes
+    if (p.f8)
+      return map.table ? launch_scan_t<DI, BK, true, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                       : launch_scan_t<DI, BK, false, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+  } else {
+    if (p.f8) return cudaErrorInvalidValue;
+  }
+  return map.table ? launch_scan_t<DI, BK, true, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                   : launch_scan_t<DI, BK, false, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
 }
 
 // The attention grid as a programmatic dependent of the scan: its CTAs may be

@@ -15,11 +15,13 @@ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 int num_sms();  // cached cudaDevAttrMultiProcessorCount of the current device
 
-// 2-D tiled TMA descriptor over a row-major bf16 matrix [rows, inner] with the
-// given row stride, box {box_inner, box_rows} and swizzle (0, 32, 64 or 128
-// bytes); out-of-bounds elements read as zero.  False if the driver refuses.
+// 2-D tiled TMA descriptor over a row-major matrix [rows, inner] of bf16
+// (elem_bytes 2) or bytes (elem_bytes 1, e.g. FP8 codes) with the given row
+// stride, box {box_inner, box_rows} and swizzle (0, 32, 64 or 128 bytes);
+// out-of-bounds elements read as zero.  False if the driver refuses.
 bool encode_tmap_2d(void* tmap /* CUtensorMap */, const void* base, uint64_t inner, uint64_t rows,
-                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes,
+                    int elem_bytes = 2);
 // 3-D variant: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1 and 2, box {b0, b1, b2}.
 bool encode_tmap_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
                     uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes);
@@ -28,8 +30,11 @@ bool encode_tmap_4d(void* tmap, const void* base, const uint64_t dims[4], const 
                     const uint32_t box[4], int swizzle_bytes);
 
 // ---- select (msa_select.cu)
+// f8: q_idx and k_idx hold FP8 E4M3 codes (d_I of 64 or 128) instead of bf16.
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
-                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s);
+                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s, bool f8 = false);
+// y[i] = E4M3 code of (bf16 x[i]) * scale (round to nearest even, saturated at 448).
+cudaError_t launch_quantize_e4m3(const void* x, int64_t n, float scale, void* y, cudaStream_t s);
 
 // ---- invert (msa_invert.cu)
 struct InvertScratch {
@@ -83,7 +88,7 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
 // The select kernel followed by the attention call, on one stream.
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
                            int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
-                           void* scratch, DeviceStatus* st, cudaStream_t s);
+                           void* scratch, DeviceStatus* st, cudaStream_t s, bool f8 = false);
 
 // ---- backward (msa_bwd.cu)
 size_t bwd_scratch_bytes(int64_t N, int H_q, int H_kv, int d, int Bk, int k);
@@ -114,6 +119,7 @@ struct DecodePlan {
   int H_q, H_kv, d, d_I, Bk, k, gs;
   int splits;          // CTAs per sequence in the index-key scan
   int max_cta_blocks;  // candidate blocks of one scan CTA, at most
+  bool f8 = false;     // index query and index-key cache hold FP8 E4M3 codes
 };
 DecodePlan decode_plan(int B, int64_t ctx_max, int H_q, int H_kv, int d, int d_I, int Bk, int k);
 size_t decode_scratch_bytes(const DecodePlan& p);

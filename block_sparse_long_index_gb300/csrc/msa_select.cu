@@ -22,6 +22,12 @@
 //               3-input max into block maxima (one per Bk-block of the tile)
 //               and offers (max, block) to its register top-(k-1) list.
 //               Scores never leave the SM.
+// The same kernel runs on FP8 E4M3 index inputs (chipsbuilder "Co-Design Del
+// Kernel": FP8 among the kernel's precisions): tcgen05.mma kind::f8f6f4 takes
+// 32 bytes of K per instruction as kind::f16 does, so the shared-memory tiles,
+// descriptors and K steps are the same in bytes and a tile of d_I = 128 is one
+// 128-byte swizzle atom per row; the tensor core runs twice the multiply-adds
+// per instruction.
 // Only blocks b < local(t) are candidates: every token of such a block is
 // visible (j <= t), so no causal mask is applied; the local block is written
 // directly as slot 0.  Items are visited longest-first in a snake order over
@@ -42,18 +48,21 @@ constexpr int kMaxGpc = 2;     // groups per work item
 constexpr int kEpiWarps = 4 * kMaxGpc;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
 
-template <int DI>
+template <int DI, bool F8>
 struct SelectLayout {
-  static constexpr int CH_E = DI >= 64 ? 64 : DI;  // elements per swizzled row chunk
-  static constexpr int CH_B = CH_E * 2;             // 128 or 64 bytes
-  static constexpr int NCH = DI / CH_E;
+  static constexpr int ESZ = F8 ? 1 : 2;              // bytes per element
+  static constexpr int RB = DI * ESZ;                 // bytes per row
+  static constexpr int CH_B = RB >= 128 ? 128 : RB;   // bytes per swizzled row chunk
+  static constexpr int CH_E = CH_B / ESZ;             // elements per chunk
+  static constexpr int NCH = RB / CH_B;
+  static_assert(CH_B == 64 || CH_B == 128, "rows of 64 or 128 bytes per swizzle atom");
   static constexpr int A_CHUNK = kRows * CH_B;
   static constexpr int B_CHUNK = kKeys * CH_B;
   static constexpr int A_BYTES = kMaxGpc * NCH * A_CHUNK;
   static constexpr int STAGE_BYTES = NCH * B_CHUNK;
   static constexpr int STAGES_FIT = (200 * 1024 - A_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;  // k^I ring depth
-  static constexpr int KSTEPS = CH_E / 16;
+  static constexpr int KSTEPS = CH_B / 32;  // 32 bytes of K per MMA
   static constexpr int BAR_BYTES = 256;
   static constexpr int SMEM = 1024 + A_BYTES + STAGES * STAGE_BYTES + BAR_BYTES;
   static_assert(STAGES >= 2, "k^I ring needs two stages");
@@ -80,11 +89,11 @@ __device__ __forceinline__ int64_t key_tiles(int64_t qb, int Bk) {
   return (key_limit + kKeys - 1) / kKeys;
 }
 
-template <int DI, int CAP>
+template <int DI, int CAP, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      int64_t N, int G, int gpc, int Bk, int k, int32_t* __restrict__ block_idx, DeviceStatus* st) {
-  using L = SelectLayout<DI>;
+  using L = SelectLayout<DI, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -180,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(kRows, kKeys);
+      constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(kRows, kKeys) : idesc_bf16_f32(kRows, kKeys);
       uint32_t kt_glob = 0, a_glob = 0;
       uint32_t uses0 = 0, uses1 = 0;  // fills of accumulator buffers 0 and 1 so far
       int64_t r = 0, j;
@@ -207,7 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t ad = umma_desc_kmajor(smem_u32(sA + (gi * L::NCH + c) * L::A_CHUNK + kk * 32), L::CH_B);
                 const uint64_t bd =
                     umma_desc_kmajor(smem_u32(sB + s * L::STAGE_BYTES + c * L::B_CHUNK + kk * 32), L::CH_B);
-                mma_bf16_ss(d, ad, bd, IDESC, (c | kk) != 0);
+                if constexpr (F8)
+                  mma_e4m3_ss(d, ad, bd, IDESC, (c | kk) != 0);
+                else
+                  mma_bf16_ss(d, ad, bd, IDESC, (c | kk) != 0);
               }
             umma_commit(acc_full(buf));
             if (buf) ++uses1; else ++uses0;
@@ -248,25 +260,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(acc_full(buf), use & 1, abort, st, 0x301))) break;
         if (buf) ++uses1; else ++uses0;
         tc_fence_after();
-        // the tile's four 64-key quarters in turn; a block's maximum is offered
-        // as soon as its quarters are done (Bk = 128: two, Bk = 64: one)
+        // the tile's four 64-key quarters in turn, the next quarter's TMEM
+        // loads in flight while this one is reduced; a block's maximum is
+        // offered as soon as its quarters are done (Bk = 128: two, Bk = 64:
+        // one).  Four independent max chains keep the reduction short.
         const uint32_t col = tmem + lane_base + (uint32_t)(buf * kKeys);
         float mb = __int_as_float(0xff800000);
-#pragma unroll 1
+        uint32_t xq[2][2][32];
+        tmem_ld_x32(col, xq[0][0]);
+        tmem_ld_x32(col + 32, xq[0][1]);
+#pragma unroll
         for (int h = 0; h < 4; ++h) {
-          uint32_t x[32], y[32];
-          tmem_ld_x32(col + 64 * h, x);
-          tmem_ld_x32(col + 64 * h + 32, y);
+          uint32_t (&x)[32] = xq[h & 1][0];
+          uint32_t (&y)[32] = xq[h & 1][1];
           tmem_ld_wait();
+          reg_fence32(x);
+          reg_fence32(y);
           if (h == 3) {  // the whole tile is in registers or reduced: release TMEM
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty(buf));
+          } else {
+            tmem_ld_x32(col + 64 * (h + 1), xq[(h + 1) & 1][0]);
+            tmem_ld_x32(col + 64 * (h + 1) + 32, xq[(h + 1) & 1][1]);
           }
+          float m4[4];
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) mb = max3(mb, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+          for (int c = 0; c < 4; ++c) m4[c] = max3(__uint_as_float(x[2 * c]), __uint_as_float(x[2 * c + 1]), mb);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) mb = max3(mb, __uint_as_float(y[i]), __uint_as_float(y[i + 1]));
+          for (int i = 8; i < 32; i += 8)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              m4[c] = max3(m4[c], __uint_as_float(x[i + 2 * c]), __uint_as_float(x[i + 2 * c + 1]));
+#pragma unroll
+          for (int i = 0; i < 32; i += 8)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              m4[c] = max3(m4[c], __uint_as_float(y[i + 2 * c]), __uint_as_float(y[i + 2 * c + 1]));
+          mb = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
           if (Bk == 64 || (h & 1)) {
             const int b = Bk == 128 ? (int)(2 * kt) + (h >> 1) : (int)(4 * kt) + h;
             if (b < local) top.insert(mb, b);
@@ -290,16 +321,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DI, int CAP>
+template <int DI, int CAP, bool F8>
 cudaError_t launch_t(const void* q_idx, const void* k_idx, int64_t N, int G, int gpc, int Bk, int k,
                      int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
-  using L = SelectLayout<DI>;
+  using L = SelectLayout<DI, F8>;
   CUtensorMap tq, tk;
-  if (!encode_tmap_2d(&tq, q_idx, (uint64_t)G * DI, (uint64_t)N, (uint64_t)G * DI * 2, L::CH_E, kRows, L::CH_B))
+  if (!encode_tmap_2d(&tq, q_idx, (uint64_t)G * DI, (uint64_t)N, (uint64_t)G * L::RB, L::CH_E, kRows, L::CH_B,
+                      L::ESZ))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tk, k_idx, (uint64_t)DI, (uint64_t)N, (uint64_t)DI * 2, L::CH_E, kKeys, L::CH_B))
+  if (!encode_tmap_2d(&tk, k_idx, (uint64_t)DI, (uint64_t)N, (uint64_t)L::RB, L::CH_E, kKeys, L::CH_B, L::ESZ))
     return cudaErrorInvalidValue;
-  auto kern = select_tc_kernel<DI, CAP>;
+  auto kern = select_tc_kernel<DI, CAP, F8>;
   // more than half of an SM's shared memory: one CTA per SM, so the 512 TMEM columns are always free
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -310,24 +342,71 @@ cudaError_t launch_t(const void* q_idx, const void* k_idx, int64_t N, int G, int
   return cudaGetLastError();
 }
 
-template <int DI>
+template <int DI, bool F8>
 cudaError_t launch_cap(const void* q_idx, const void* k_idx, int64_t N, int G, int gpc, int Bk, int k,
                        int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
   const int km1 = k - 1;
-  if (km1 <= 4) return launch_t<DI, 4>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  if (km1 <= 8) return launch_t<DI, 8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  if (km1 <= 16) return launch_t<DI, 16>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  return launch_t<DI, 32>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (km1 <= 4) return launch_t<DI, 4, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (km1 <= 8) return launch_t<DI, 8, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (km1 <= 16) return launch_t<DI, 16, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  return launch_t<DI, 32, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+}
+
+// y = E4M3 code of (bf16 x) * scale, nearest with ties to even, saturated at
+// +-448 (cvt.rn.satfinite); eight elements (16 bytes in, 8 out) per step when
+// both pointers allow it.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__global__ void __launch_bounds__(256) quantize_e4m3_kernel(const uint16_t* __restrict__ x, int64_t n, float scale,
+                                                            uint8_t* __restrict__ y, int vec) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t done = 0;
+  if (vec) {
+    const int64_t n8 = n / 8;
+    for (int64_t i = i0; i < n8; i += stride) {
+      const uint4 v = ldg_stream_16(x + 8 * i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) p[j] = cvt_e4m3x2(__fmul_rn(bf16_hi(w[j]), scale), __fmul_rn(bf16_lo(w[j]), scale));
+      *reinterpret_cast<uint2*>(y + 8 * i) = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+    }
+    done = n8 * 8;
+  }
+  for (int64_t i = done + i0; i < n; i += stride)
+    y[i] = (uint8_t)(cvt_e4m3x2(0.f, __fmul_rn(__uint_as_float((uint32_t)x[i] << 16), scale)) & 0xFFu);
 }
 
 }  // namespace
 
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
-                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
+                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s, bool f8) {
   const int gpc = (G % 2 == 0) ? 2 : 1;
-  if (d_I == 32) return launch_cap<32>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  if (d_I == 64) return launch_cap<64>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  return launch_cap<128>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (f8) {  // d_I of 64 or 128 (64- or 128-byte rows)
+    if (d_I == 64) return launch_cap<64, true>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+    if (d_I == 128) return launch_cap<128, true>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+    return cudaErrorInvalidValue;
+  }
+  if (d_I == 32) return launch_cap<32, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (d_I == 64) return launch_cap<64, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  return launch_cap<128, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+}
+
+cudaError_t launch_quantize_e4m3(const void* x, int64_t n, float scale, void* y, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int vec = ((reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(y) & 7u) == 0) ? 1 : 0;
+  const int64_t per_thread = vec ? 8 : 1;
+  int64_t blocks = (n / per_thread + 255) / 256;
+  const int64_t cap = (int64_t)num_sms() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  quantize_e4m3_kernel<<<(unsigned)blocks, 256, 0, s>>>((const uint16_t*)x, n, scale, (uint8_t*)y, vec);
+  return cudaGetLastError();
 }
 
 }  // namespace msa

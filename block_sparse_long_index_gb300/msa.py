@@ -52,6 +52,11 @@ _SIGS = {
     "msa_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P]),
+    "msa_quantize_e4m3": (_I, [_P, _I64, _F, _P, _P]),
+    "msa_select_blocks_fp8": (_I, [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "msa_prefill_fp8": (_I, [_P, _P, _P, _P, _P, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
+    "msa_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
+    "msa_decode_paged_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_check_device_error": (_I, [_P, _P]),
     "msa_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -185,6 +190,43 @@ def msa_decode_noalloc(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, 
     return _check(_lib.msa_decode_noalloc(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_cache), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(ctx_len), B, ctypes.byref(shp), float(scale), _ptr(out), _ptr(lse),
                                           _ptr(block_idx), _stream(stream)), "msa_decode_noalloc")
+
+
+def msa_quantize_e4m3(x, n, scale, y, stream=None):
+    return _check(_lib.msa_quantize_e4m3(_ptr(x), int(n), float(scale), _ptr(y), _stream(stream)),
+                  "msa_quantize_e4m3")
+
+
+def msa_select_blocks_fp8(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_select_blocks_fp8(_ptr(q_idx), _ptr(k_idx), N, G, d_I, Bk, k, _ptr(block_idx),
+                                             _ptr(workspace), wb, _stream(stream)), "msa_select_blocks_fp8")
+
+
+def msa_prefill_fp8(q, k, v, q_idx, k_idx, shp, scale, block_idx, out, lse, workspace, workspace_bytes=None,
+                    stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_prefill_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), ctypes.byref(shp),
+                                       float(scale), _ptr(block_idx), _ptr(out), _ptr(lse), _ptr(workspace), wb,
+                                       _stream(stream)), "msa_prefill_fp8")
+
+
+def msa_decode_fp8(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, B, shp, scale, out, lse, block_idx,
+                   workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_decode_fp8(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_cache), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(ctx_len), B, ctypes.byref(shp), float(scale), _ptr(out), _ptr(lse),
+                                      _ptr(block_idx), _ptr(workspace), wb, _stream(stream)), "msa_decode_fp8")
+
+
+def msa_decode_paged_fp8(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, page_table, max_pages, n_pages, page_size,
+                         ctx_len, B, shp, scale, out, lse, block_idx, workspace, workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_decode_paged_fp8(_ptr(q_t), _ptr(q_idx_t), _ptr(k_idx_pool), _ptr(k_pool),
+                                            _ptr(v_pool), _ptr(page_table), int(max_pages), int(n_pages),
+                                            int(page_size), _ptr(ctx_len), B, ctypes.byref(shp), float(scale),
+                                            _ptr(out), _ptr(lse), _ptr(block_idx), _ptr(workspace), wb,
+                                            _stream(stream)), "msa_decode_paged_fp8")
 
 
 def msa_check_device_error(workspace, stream=None):

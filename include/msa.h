@@ -243,6 +243,51 @@ msa_status_t msa_decode_paged(const void* q_t, const void* q_idx_t, const void* 
                               void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
                               msa_stream_t stream);
 
+/* ---------------------------------------------------------------- FP8 index inputs
+ * The index branch on FP8 inputs.  Pages: the chipsbuilder.com article, "Co-
+ * Design Del Kernel" (FP8 is among the precisions of the method's kernel),
+ * and the "MSA" study note, 6 "Limitations" item 1 (the index branch scores
+ * the whole context, so its inputs carry the cost that grows with it).
+ *
+ * FP8 here is E4M3 of the OCP 8-bit floating point specification: one byte
+ * per element, 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+ * infinity, largest finite magnitude 448.  The selection rule is exactly that
+ * of msa_select_blocks, applied to the decoded values: every product of two
+ * E4M3 values is exact and the tensor cores sum them in fp32.  Multiplying all
+ * of q^I, or all of k^I, by one positive factor before quantizing changes no
+ * ranking, so the selection calls take no scale.  Supported d_I: 64 or 128
+ * (MSA_ERR_UNSUPPORTED otherwise).
+ *
+ * msa_quantize_e4m3: y[i] = the E4M3 code nearest to the fp32 product
+ *   (bf16 x[i]) * scale, ties to the even code, magnitudes beyond 448
+ *   saturated to 448, NaN kept NaN.  x [n] bf16 (2-byte aligned), y [n] bytes
+ *   out; no workspace.
+ * msa_select_blocks_fp8: msa_select_blocks with q_idx [N, G, d_I] and
+ *   k_idx [N, d_I] as E4M3 codes; workspace msa_select_blocks_workspace().
+ * msa_prefill_fp8: msa_prefill with E4M3 q_idx and k_idx (q, k, v stay bf16);
+ *   workspace msa_prefill_workspace().
+ * msa_decode_fp8: msa_decode with q_idx_t [B, G, d_I] and k_idx_cache
+ *   [B, N, d_I] as E4M3 codes, so the scan reads d_I bytes per cached token
+ *   instead of 2 d_I; workspace msa_decode_workspace().
+ * msa_decode_paged_fp8: msa_decode_paged with E4M3 q_idx_t and k_idx_pool
+ *   [n_pages, page_size, d_I].
+ */
+msa_status_t msa_quantize_e4m3(const void* x, int64_t n, float scale, void* y, msa_stream_t stream);
+msa_status_t msa_select_blocks_fp8(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
+                                   int32_t* block_idx, void* workspace, size_t workspace_bytes, msa_stream_t stream);
+msa_status_t msa_prefill_fp8(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                             const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
+                             void* workspace, size_t workspace_bytes, msa_stream_t stream);
+msa_status_t msa_decode_fp8(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
+                            const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                            void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                            msa_stream_t stream);
+msa_status_t msa_decode_paged_fp8(const void* q_t, const void* q_idx_t, const void* k_idx_pool, const void* k_pool,
+                                  const void* v_pool, const int32_t* page_table, int64_t max_pages, int64_t n_pages,
+                                  int page_size, const int32_t* ctx_len, int B, const msa_shape_t* shape, float scale,
+                                  void* out, float* lse, int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                                  msa_stream_t stream);
+
 /* ---------------------------------------------------------------- decode without allocation
  * The same decode step as msa_decode, for callers that cannot allocate device
  * memory: for instance a plugin whose host application owns every byte of the

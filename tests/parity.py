@@ -138,3 +138,17 @@ def compare_attn(out_gpu, lse_gpu, out_ref, lse_ref, mask=None):
     assert ok_lse, ("lse outside 2e-2 abs + 1e-2 rel", rep)
     assert cos >= COS_MIN, ("cosine below 0.9999", rep)
     return rep
+
+
+def e4m3_codes(x_bf16_bits):
+    """E4M3 codes (uint8) of bf16 values (uint16 bit patterns), cast by torch's float8_e4m3fn on the CPU:
+    the FP8 index inputs of the tests, made independently of both the oracle and the CUDA path."""
+    import torch
+    x = torch.from_numpy(np.ascontiguousarray(x_bf16_bits, np.uint16).view(np.int16)).view(torch.bfloat16)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def gamma_rows_e4m3(q_codes, k_codes, rows, d_I):
+    """gamma_rows on the decoded values of E4M3 inputs."""
+    import oracle
+    return gamma_rows(oracle.e4m3_decode(q_codes), oracle.e4m3_decode(k_codes), rows, d_I)

@@ -21,7 +21,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "msa.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -116,3 +116,31 @@ def test_prefill_and_paged_decode_validation(lib):
     big = lib.shape(64 * 128, 64, 16, 128, 128, 128, 8)  # more than 8 groups
     assert raw.msa_decode_paged(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 200, 128, FAKE, 2, ctypes.byref(big), 0.1,
                                 FAKE, None, None, FAKE, 1 << 40, None) == lib.MSA_ERR_UNSUPPORTED
+
+
+def test_fp8_entry_points_validation(lib):
+    raw = lib.raw()
+    # FP8 index inputs take d_I of 64 or 128 only
+    ws = lib.msa_select_blocks_workspace(4096, 2, 32, 128, 16)
+    assert raw.msa_select_blocks_fp8(FAKE, FAKE, 4096, 2, 32, 128, 16, FAKE, FAKE, ws, None) == lib.MSA_ERR_UNSUPPORTED
+    assert raw.msa_select_blocks_fp8(None, FAKE, 4096, 2, 128, 128, 16, FAKE, FAKE, ws,
+                                     None) == lib.MSA_ERR_INVALID_ARGUMENT
+    s32 = lib.shape(4096, 16, 2, 128, 32, 128, 16)
+    need = lib.msa_prefill_workspace(s32)
+    assert raw.msa_prefill_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s32), 0.1, FAKE, FAKE, FAKE, FAKE, need,
+                               None) == lib.MSA_ERR_UNSUPPORTED
+    d32 = lib.shape(8192, 16, 2, 128, 32, 128, 8)
+    assert raw.msa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, ctypes.byref(d32), 0.1, FAKE, None, None, FAKE,
+                              1 << 40, None) == lib.MSA_ERR_UNSUPPORTED
+    assert raw.msa_decode_paged_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 64, 200, 128, FAKE, 2, ctypes.byref(d32), 0.1,
+                                    FAKE, None, None, FAKE, 1 << 40, None) == lib.MSA_ERR_UNSUPPORTED
+    d = lib.shape(8192, 16, 2, 128, 128, 128, 8)
+    wsd = lib.msa_decode_workspace(2, d)
+    assert raw.msa_decode_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, ctypes.byref(d), 0.1, FAKE, None, None, FAKE,
+                              wsd - 256, None) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    # quantize: negative size, null pointers with work to do, odd bf16 address, NaN scale
+    assert raw.msa_quantize_e4m3(FAKE, -1, 1.0, FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_quantize_e4m3(None, 8, 1.0, FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_quantize_e4m3(ctypes.c_void_p((1 << 20) + 1), 8, 1.0, FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_quantize_e4m3(FAKE, 8, float("nan"), FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_quantize_e4m3(None, 0, 1.0, None, None) == lib.MSA_OK  # nothing to do
