@@ -167,14 +167,20 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
       bm0 = bm1 = __int_as_float(0xff800000);
     }
   };
-  uint4 va[NQ][2], vb[NQ][2];
-  if (c0 < c1) load_keys16<RB>(va, chunk_ptr(c0));
-  for (int64_t ci = c0; ci < c1; ci += 2) {  // one chunk in flight ahead of the one being scored
-    if (ci + 1 < c1) load_keys16<RB>(vb, chunk_ptr(ci + 1));
-    score(va, ci);
-    if (ci + 1 < c1) {
-      if (ci + 2 < c1) load_keys16<RB>(va, chunk_ptr(ci + 2));
-      score(vb, ci + 1);
+  // a ring of PD chunks: PD - 1 in flight ahead of the one being scored (about 4-6 KB per warp either way)
+  constexpr int PD = F8 ? 4 : 2;
+  uint4 vr[PD][NQ][2];
+#pragma unroll
+  for (int p = 0; p < PD - 1; ++p)
+    if (c0 + p < c1) load_keys16<RB>(vr[p], chunk_ptr(c0 + p));
+  for (int64_t ci = c0; ci < c1; ci += PD) {
+#pragma unroll
+    for (int p = 0; p < PD; ++p) {
+      const int64_t cc = ci + p;
+      if (cc < c1) {
+        if (cc + PD - 1 < c1) load_keys16<RB>(vr[(p + PD - 1) % PD], chunk_ptr(cc + PD - 1));
+        score(vr[p], cc);
+      }
     }
   }
   __syncthreads();

@@ -47,6 +47,7 @@ constexpr int kKeys = 256;     // keys per tile = MMA N
 constexpr int kMaxGpc = 2;     // groups per work item
 constexpr int kEpiWarps = 4 * kMaxGpc;
 constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr uint32_t kHint = 20000;  // ns: waiting warps sleep in try_wait instead of spinning
 
 template <int DI, bool F8>
 struct SelectLayout {
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int gq = (int)(j % n_gq);
         const int64_t nkt = key_tiles(qb, Bk);
         if (nkt == 0) continue;
-        if (!(ok = mbar_wait(a_empty, (a_glob & 1) ^ 1, abort, st, 0x101))) break;
+        if (!(ok = mbar_wait(a_empty, (a_glob & 1) ^ 1, abort, st, 0x101, kHint))) break;
         mbar_arrive_expect_tx(a_full, (uint32_t)(gpc * L::NCH * L::A_CHUNK));
         for (int gi = 0; gi < gpc; ++gi)
           for (int c = 0; c < L::NCH; ++c)
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
           const int s = kt_glob % kStages;
           const uint32_t ph = (kt_glob / kStages) & 1;
-          if (!(ok = mbar_wait(empty_bar(s), ph ^ 1, abort, st, 0x102))) break;
+          if (!(ok = mbar_wait(empty_bar(s), ph ^ 1, abort, st, 0x102, kHint))) break;
           mbar_arrive_expect_tx(full_bar(s), (uint32_t)L::STAGE_BYTES);
           for (int c = 0; c < L::NCH; ++c)
             tma_load_2d(smem_u32(sB + s * L::STAGE_BYTES + c * L::B_CHUNK), &tmap_k, c * L::CH_E,
@@ -198,15 +199,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t qb = n_qt - 1 - j / n_gq;
         const int64_t nkt = key_tiles(qb, Bk);
         if (nkt == 0) continue;
-        if (!(ok = mbar_wait(a_full, a_glob & 1, abort, st, 0x201))) break;
+        if (!(ok = mbar_wait(a_full, a_glob & 1, abort, st, 0x201, kHint))) break;
         tc_fence_after();
         for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
           const int s = kt_glob % kStages;
-          if (!(ok = mbar_wait(full_bar(s), (kt_glob / kStages) & 1, abort, st, 0x202))) break;
+          if (!(ok = mbar_wait(full_bar(s), (kt_glob / kStages) & 1, abort, st, 0x202, kHint))) break;
           for (int gi = 0; gi < gpc && ok; ++gi) {
             const int buf = gpc == 2 ? gi : (int)(kt_glob & 1);
             const uint32_t use = buf ? uses1 : uses0;
-            if (!(ok = mbar_wait(acc_empty(buf), (use & 1) ^ 1, abort, st, 0x203))) break;
+            if (!(ok = mbar_wait(acc_empty(buf), (use & 1) ^ 1, abort, st, 0x203, kHint))) break;
             tc_fence_after();
             const uint32_t d = tmem + (uint32_t)(buf * kKeys);
 #pragma unroll
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
         const int buf = gpc == 2 ? gi : (int)(kt_glob & 1);
         const uint32_t use = buf ? uses1 : uses0;
-        if (!(ok = mbar_wait(acc_full(buf), use & 1, abort, st, 0x301))) break;
+        if (!(ok = mbar_wait(acc_full(buf), use & 1, abort, st, 0x301, kHint))) break;
         if (buf) ++uses1; else ++uses0;
         tc_fence_after();
         // the tile's four 64-key quarters in turn, the next quarter's TMEM

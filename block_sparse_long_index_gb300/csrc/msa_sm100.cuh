@@ -36,6 +36,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread may sleep up to ~hint_ns
+// nanoseconds inside the instruction unless the phase completes first.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -47,12 +59,14 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // to ignore that, e.g. while draining): then it raises the timeout flag in the
 // status word, sets *abort and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// hint_ns > 0: the retries sleep in the hardware (try_wait's suspend-time
+// hint) rather than spin, which leaves issue slots to the working warps.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, DeviceStatus* st,
-                                          unsigned code) {
+                                          unsigned code, uint32_t hint_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (hint_ns ? mbar_try_wait_hint(bar, parity, hint_ns) : mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (abort && *abort) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {

@@ -311,17 +311,24 @@ int msa_ref_e4m3_quantize(const uint16_t* x, int64_t n, float scale, uint8_t* co
   return ORACLE_OK;
 }
 
+/* The 256 decoded values, filled by the exported entry points before any
+ * worker thread runs (the same e4m3_to_double values, looked up). */
+static double e4m3_value[256];
+static void e4m3_fill_values(void) {
+  for (int c = 0; c < 256; ++c) e4m3_value[c] = e4m3_to_double((uint8_t)c);
+}
+
 /* Step 1 on E4M3 inputs: the same block maxima of the decoded scores. */
 static void block_scores_row_e4m3(const uint8_t* qrow, const uint8_t* k_idx, int64_t t, int d_I, int Bk,
                                   int64_t nb, double* S) {
   double inv = 1.0 / sqrt((double)d_I);
   double q[512];
-  for (int c = 0; c < d_I; ++c) q[c] = e4m3_to_double(qrow[c]);
+  for (int c = 0; c < d_I; ++c) q[c] = e4m3_value[qrow[c]];
   for (int64_t b = 0; b < nb; ++b) S[b] = -INFINITY;
   for (int64_t j = 0; j <= t; ++j) {
     const uint8_t* kr = k_idx + j * d_I;
     double s = 0.0;
-    for (int c = 0; c < d_I; ++c) s += q[c] * e4m3_to_double(kr[c]);
+    for (int c = 0; c < d_I; ++c) s += q[c] * e4m3_value[kr[c]];
     s *= inv;
     int64_t b = j / Bk;
     if (s > S[b]) S[b] = s;
@@ -369,6 +376,7 @@ int msa_ref_block_scores_e4m3(const uint8_t* q_idx_rows, const uint8_t* k_idx, c
   for (int64_t r = 0; r < n_rows; ++r)
     if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
   select8_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, 0, S, NULL, NULL, 0};
+  e4m3_fill_values();
   parallel_for(n_rows * G, n_threads, select8_item, &c);
   return c.status;
 }
@@ -383,6 +391,7 @@ int msa_ref_select_blocks_e4m3(const uint8_t* q_idx_rows, const uint8_t* k_idx, 
   for (int64_t r = 0; r < n_rows; ++r)
     if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
   select8_ctx c = {q_idx_rows, k_idx, rows, n_rows, N, (N + Bk - 1) / Bk, G, d_I, Bk, k, NULL, block_idx, kth, 0};
+  e4m3_fill_values();
   parallel_for(n_rows * G, n_threads, select8_item, &c);
   return c.status;
 }

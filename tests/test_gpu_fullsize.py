@@ -188,3 +188,105 @@ def test_bwd_32k_sampled():
 
 def test_bwd_128k_sampled():
     _bwd_sampled("prefill_128k", 64)
+
+
+def _device_e4m3(msa, x):
+    y = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    msa.msa_quantize_e4m3(x, x.numel(), 1.0, y)
+    return y
+
+
+def test_select_fp8_128k_sampled():
+    """msa_select_blocks_fp8 at 128K on inputs cast by msa_quantize_e4m3 on the device; the oracle gets the
+    torch CPU cast of the host inputs, and the two casts must agree byte for byte where they are compared."""
+    from parity import e4m3_codes, gamma_rows_e4m3
+    from block_sparse_long_index_gb300 import msa
+    cfg = datagen.CONFIGS["prefill_128k"]
+    N, G = cfg.N, cfg.G
+    dev = datagen.prefill_device(cfg, want=("q_idx", "k_idx"))
+    q8, k8 = _device_e4m3(msa, dev["q_idx"]), _device_e4m3(msa, dev["k_idx"])
+    del dev
+    blk = torch.empty((G, N, cfg.k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(msa.msa_select_blocks_workspace(N, G, cfg.d_I, cfg.Bk, cfg.k), dtype=torch.uint8, device="cuda")
+    msa.msa_select_blocks_fp8(q8, k8, N, G, cfg.d_I, cfg.Bk, cfg.k, blk, ws)
+    assert msa.msa_check_device_error(ws) == 0
+    rows = datagen.sample_rows(N, 512, cfg.seed, must=(0, cfg.Bk - 1, cfg.Bk, N - 1))
+    rows_d = torch.from_numpy(rows).cuda()
+    gpu_blk = blk[:, rows_d].cpu().numpy()
+    host = datagen.prefill_host(cfg, rows=rows, want=("q_idx", "k_idx"))
+    hq8, hk8 = e4m3_codes(host["q_idx"]), e4m3_codes(host["k_idx"])
+    assert np.array_equal(q8[rows_d].cpu().numpy(), hq8)
+    assert np.array_equal(k8.cpu().numpy(), hk8)
+    check_set_invariants(gpu_blk, rows, cfg.Bk, cfg.k)
+    ora, kth = oracle.select_blocks_e4m3(hq8, hk8, rows, N, cfg.Bk, cfg.k)
+    mism = np.nonzero(np.any(np.any(np.sort(gpu_blk, 2) != np.sort(ora, 2), axis=2), axis=0))[0]
+    rep = compare_sets(gpu_blk, ora, kth)
+    if len(mism):
+        S = oracle.block_scores_e4m3(hq8[mism], hk8, rows[mism], N, cfg.Bk)
+        sub = compare_sets(gpu_blk[:, mism], ora[:, mism], kth[:, mism], S=S,
+                           gamma=gamma_rows_e4m3(hq8[mism], hk8, rows[mism], cfg.d_I), rows=rows[mism], Bk=cfg.Bk)
+        rep["strict_invalid"] = sub["strict_invalid"]
+    print("prefill_128k fp8 sets", rep)
+    nd = host["needles"]
+    masks = datagen.pick_masks(cfg, nd, rows, rows, datagen.TID["pick"])
+    for i in range(len(rows)):
+        for g in range(G):
+            for n in range(nd.m):
+                if masks[i, g] >> n & 1:
+                    assert int(nd.blocks[0, g, n]) in set(gpu_blk[g, i].tolist())
+
+
+def test_decode_fp8_1m_full():
+    """msa_decode_fp8 on the 1M-context decode workload: every sequence's sets against the oracle on the torch
+    CPU cast of the host caches (equal, byte for byte, to the device cast), and the outputs against the oracle's
+    attention on the GPU's sets."""
+    from parity import e4m3_codes
+    from block_sparse_long_index_gb300 import msa
+    cfg = datagen.CONFIGS["decode_1m"]
+    dev = datagen.decode_device(cfg)
+    qi8, ki8 = _device_e4m3(msa, dev["q_idx_t"]), _device_e4m3(msa, dev["k_idx_cache"])
+    del dev["k_idx_cache"]
+    shp = msa.shape(cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    ws = torch.empty(msa.msa_decode_workspace(cfg.B, shp), dtype=torch.uint8, device="cuda")
+    out = torch.empty((cfg.B, cfg.H_q, cfg.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((cfg.B, cfg.H_q), dtype=torch.float32, device="cuda")
+    blk = torch.empty((cfg.B, cfg.H_kv, cfg.k), dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(cfg.d)
+    msa.msa_decode_fp8(dev["q_t"], qi8, ki8, dev["k_cache"], dev["v_cache"], dev["ctx_len"], cfg.B, shp, scale, out,
+                       lse, blk, ws)
+    assert msa.msa_check_device_error(ws) == 0
+    gpu_blk = blk.cpu().numpy()
+    ctx_len = dev["ctx_len_host"]
+    host = datagen.decode_host(cfg, ctx_len, want=("q_t", "q_idx_t", "k_idx_cache"))
+    hq8, hk8 = e4m3_codes(host["q_idx_t"]), e4m3_codes(host["k_idx_cache"])
+    assert np.array_equal(qi8.cpu().numpy(), hq8)
+    assert np.array_equal(ki8.cpu().numpy(), hk8)
+    check_set_invariants(gpu_blk.transpose(1, 0, 2), ctx_len - 1, cfg.Bk, cfg.k)
+    o, l = bf16_tensor_to_f64(out), lse.cpu().numpy().astype(np.float64)
+    ora_blk = np.empty_like(gpu_blk)
+    kth = np.empty((cfg.B, cfg.G, 2))
+    for b in range(cfg.B):
+        t = int(ctx_len[b]) - 1
+        ob, kb = oracle.select_blocks_e4m3(hq8[b:b + 1], hk8[b, :t + 1], [t], t + 1, cfg.Bk, cfg.k)
+        ora_blk[b], kth[b] = ob[:, 0], kb[:, 0]
+        # K/V rows of the GPU's blocks only (the rest of the arrays is never read)
+        kc = np.zeros((cfg.ctx, cfg.H_kv, cfg.d), np.uint16)
+        vc = np.zeros((cfg.ctx, cfg.H_kv, cfg.d), np.uint16)
+        toks = np.concatenate([np.arange(x * cfg.Bk, min((x + 1) * cfg.Bk, cfg.ctx))
+                               for x in sorted(set(gpu_blk[b].reshape(-1).tolist())) if x >= 0])
+        ids = b * cfg.ctx + toks
+        kc[toks] = datagen.host_normal_rows(ids, cfg.H_kv * cfg.d, cfg.seed, datagen.TID["k_cache"]).reshape(
+            -1, cfg.H_kv, cfg.d)
+        vc[toks] = datagen.host_normal_rows(ids, cfg.H_kv * cfg.d, cfg.seed, datagen.TID["v_cache"]).reshape(
+            -1, cfg.H_kv, cfg.d)
+        ref, ref_lse = oracle.sparse_attn(host["q_t"][b:b + 1], kc, vc, gpu_blk[b][:, None, :], [t], cfg.Bk, scale)
+        compare_attn(o[b:b + 1], l[b:b + 1], ref, ref_lse)
+    rep = compare_sets(gpu_blk.transpose(1, 0, 2), ora_blk.transpose(1, 0, 2), kth.transpose(1, 0, 2))
+    print("decode_1m fp8 sets", rep)
+    nd = host["needles"]
+    for b in range(cfg.B):
+        mk = datagen.pick_masks(cfg, nd, [b], [ctx_len[b] - 1], datagen.TID["pick_t"], s=b)[0]
+        for g in range(cfg.G):
+            for n in range(nd.m):
+                if mk[g] >> n & 1:
+                    assert int(nd.blocks[b, g, n]) in set(gpu_blk[b, g].tolist())
