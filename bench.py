@@ -624,7 +624,9 @@ def main():
             "note": "the step takes q_idx and k_idx already in E4M3 (as an index projection emitting FP8 would); "
                     "msa_quantize_e4m3 of both from bf16 is timed apart",
             "roofline_select": {"bound": "tensor", "achieved": sel8_tf, "peak": peak8, "unit": "TFLOP/s",
-                                "frac": sel8_tf / peak8, "traffic": None,
+                                "frac": sel8_tf / peak8,
+                                "traffic": traffic_for("select_fp8_prefill_128k",
+                                                       "block_sparse_long_index_gb300/csrc/msa_select.cu"),
                                 "algorithmic": "(N^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index,
                                 "peak_source": "%s bf16_tflops_sustained x 2 (nominal fp8/bf16 dense ratio "
                                                "4.5/2.25)" % peak_src},
