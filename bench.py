@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) index-input variants")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the varlen (packed sequences) prefill")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
     ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode", "select_fp8",
                                                        "decode_fp8"],
@@ -185,6 +186,15 @@ def prefill_launches(cfg):
     return 1 + 4 + 5 * prefill_slabs(cfg)
 
 
+def varlen_mix(N, Bk):
+    """A fixed mix of sequence lengths (block multiples) filling N cells: 1/4, 3/16, 1/8, 1/8, 3/32, 3/32,
+    1/16, 1/16 of N."""
+    parts = [8, 6, 4, 4, 3, 3, 2, 2]  # in 32nds
+    lengths = [N * p // 32 // Bk * Bk for p in parts]
+    lengths[-1] += N - sum(lengths)
+    return lengths
+
+
 def bench_prefill(args, dist, torch, peaks):
     import datagen
     from block_sparse_long_index_gb300 import MsaPrefill
@@ -288,6 +298,36 @@ def bench_prefill(args, dist, torch, peaks):
         assert run.device_status() == 0
         res["fp8"] = dict(step_ms=tm["step"], sel_ms=tm["select"], quant_ms=tm["quant"])
         del q8, k8
+
+    # ---- the same cells as several sequences (msa_prefill_varlen): a fixed mix of lengths filling N
+    if not args.no_varlen:
+        from block_sparse_long_index_gb300 import msa
+        lengths = varlen_mix(cfg.N, cfg.Bk)
+        cu = [0]
+        for n in lengths:
+            cu.append(cu[-1] + n)
+        cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+        wsv = torch.empty(msa.msa_prefill_varlen_workspace(run.shape), dtype=torch.uint8, device="cuda")
+        scale = 1.0 / math.sqrt(cfg.d)
+        stepv = lambda: msa.msa_prefill_varlen(q, k, v, qi, ki, cu_d, len(lengths), run.shape, scale,  # noqa: E731
+                                               run.block_idx, run.out, run.lse, wsv)
+        selv = lambda: msa.msa_select_blocks_varlen(qi, ki, cu_d, len(lengths), cfg.N, cfg.G, cfg.d_I,  # noqa
+                                                    cfg.Bk, cfg.k, run.block_idx, wsv)
+        for _ in range(args.warmup):
+            stepv()
+        torch.cuda.synchronize()
+        tv = {}
+        for name, fn in (("step", stepv), ("select", selv)):
+            a, b = E(), E()
+            a.record(stream)
+            for _ in range(K):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            tv[name] = a.elapsed_time(b) / K
+        assert msa.msa_check_device_error(wsv) == 0
+        res["varlen"] = dict(step_ms=tv["step"], sel_ms=tv["select"], lengths=lengths)
+        del wsv
 
     # ---- end to end through host buffers (pinned), copies inside the timed region: every step copies
     # its five inputs in and out, lse back; PrefillHostPipeline overlaps those copies with compute
@@ -631,6 +671,20 @@ def main():
                                 "peak_source": "%s bf16_tflops_sustained x 2 (nominal fp8/bf16 dense ratio "
                                                "4.5/2.25)" % peak_src},
             "gpu_launches": (prefill_launches(cfg)) * K}
+    if "varlen" in pre:
+        vl = pre["varlen"]
+        v_ms = dist.max(vl["step_ms"])
+        flops_index_v = sum(n * n / 2.0 for n in vl["lengths"]) * cfg.G * cfg.d_I * 2.0
+        selv_tf = flops_index_v / (vl["sel_ms"] / 1000.0) / 1e12
+        line["prefill_varlen"] = {
+            "metric": "prefill tokens/s at 128K cells holding %d sequences (msa_prefill_varlen)" % len(vl["lengths"]),
+            "value": ws * cfg.N / (v_ms / 1000.0), "unit": "tokens/s", "ms_per_step": v_ms,
+            "lengths": vl["lengths"], "stages_ms": {"select_varlen": vl["sel_ms"]},
+            "roofline_select": {"bound": "tensor", "achieved": selv_tf, "peak": peak_t, "unit": "TFLOP/s",
+                                "frac": selv_tf / peak_t, "traffic": None,
+                                "algorithmic": "sum_s(len_s^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index_v,
+                                "peak_source": "%s bf16_tflops_sustained" % peak_src},
+            "gpu_launches": (prefill_launches(cfg) + 1) * K}
     if not args.no_decode:
         dec = bench_decode(args, dist, torch)
         dcfg = dec["cfg"]

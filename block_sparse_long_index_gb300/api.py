@@ -103,6 +103,16 @@ def decode(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, Bk=128, k_block
     return run(q_t, q_idx_t, k_idx_cache, k_cache, v_cache, ctx_len, scale)
 
 
+def varlen_cells(lengths, Bk):
+    """Block-aligned cell offsets for sequences of the given lengths: cu_seqlens [S+1] (a list of ints)
+    for msa_select_blocks_varlen / msa_prefill_varlen, sequence s starting at the first block boundary
+    after sequence s-1's last token; N = cu_seqlens[-1] cells hold them all."""
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + (int(n) + Bk - 1) // Bk * Bk)
+    return cu
+
+
 def prefill_from_host(run: MsaPrefill, host_inputs, dev_inputs, host_out, stream=None):
     """End-to-end step through the public API with host buffers: pinned host -> device copies,
     the prefill step, device -> pinned host copies of out and lse, all on one stream."""

@@ -360,8 +360,8 @@ cudaError_t launch_tile_schedule(const int32_t* row_ptr, const int32_t* entries,
 
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
                            int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
-                           void* scratch, DeviceStatus* st, cudaStream_t s, bool f8) {
-  cudaError_t e = launch_select(q_idx, k_idx, p.N, p.H_kv, d_I, p.Bk, p.k, block_idx, st, s, f8);
+                           void* scratch, DeviceStatus* st, cudaStream_t s, bool f8, const int32_t* blk_lo) {
+  cudaError_t e = launch_select(q_idx, k_idx, p.N, p.H_kv, d_I, p.Bk, p.k, block_idx, st, s, f8, blk_lo);
   if (e != cudaSuccess) return e;
   return launch_attn(q, k, v, block_idx, p, scale, out, lse, scratch, st, s);
 }

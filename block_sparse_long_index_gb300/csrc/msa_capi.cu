@@ -170,6 +170,32 @@ msa_status_t msa_select_blocks_fp8(const void* q_idx, const void* k_idx, int64_t
   return select_impl(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, workspace, workspace_bytes, stream, true);
 }
 
+size_t msa_select_blocks_varlen_workspace(int64_t N, int G, int d_I, int Bk, int k) {
+  (void)G;
+  (void)d_I;
+  (void)k;
+  if (N < 1 || Bk < 1) return kHeader;
+  return kHeader + msa::align_up((size_t)((N + Bk - 1) / Bk) * 4, 256);
+}
+
+msa_status_t msa_select_blocks_varlen(const void* q_idx, const void* k_idx, const int32_t* cu_seqlens, int S,
+                                      int64_t N, int G, int d_I, int Bk, int k, int32_t* block_idx, void* workspace,
+                                      size_t workspace_bytes, msa_stream_t stream) {
+  if (!q_idx || !k_idx || !block_idx || !cu_seqlens || S < 1) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_common(N, G, d_I, Bk, k);
+  if (st != MSA_OK) return st;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || ((uintptr_t)block_idx & 3u) || ((uintptr_t)cu_seqlens & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_select_blocks_varlen_workspace(N, G, d_I, Bk, k), s);
+  if (st != MSA_OK) return st;
+  int32_t* blk_lo = (int32_t*)((char*)workspace + kHeader);
+  msa::DeviceStatus* dst = (msa::DeviceStatus*)workspace;
+  cudaError_t e = msa::launch_varlen_blocks(cu_seqlens, S, N, Bk, blk_lo, dst, s);
+  if (e != cudaSuccess) return MSA_ERR_CUDA;
+  return finish(msa::launch_select(q_idx, k_idx, N, G, d_I, Bk, k, block_idx, dst, s, false, blk_lo));
+}
+
 msa_status_t msa_quantize_e4m3(const void* x, int64_t n, float scale, void* y, msa_stream_t stream) {
   if (n < 0 || ((!x || !y) && n > 0)) return MSA_ERR_INVALID_ARGUMENT;
   if (((uintptr_t)x & 1u) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
@@ -251,6 +277,38 @@ msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void
                          void* workspace, size_t workspace_bytes, msa_stream_t stream) {
   return prefill_impl(q, k, v, q_idx, k_idx, shape, scale, block_idx, out, lse, workspace, workspace_bytes, stream,
                       false);
+}
+
+size_t msa_prefill_varlen_workspace(const msa_shape_t* shape) {
+  if (check_shape(shape) != MSA_OK) return kHeader;
+  const size_t lo_bytes = msa::align_up((size_t)((shape->N + shape->Bk - 1) / shape->Bk) * 4, 256);
+  const size_t attn = msa_prefill_workspace(shape) - kHeader;
+  return kHeader + (lo_bytes > attn ? lo_bytes : attn);
+}
+
+msa_status_t msa_prefill_varlen(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                const int32_t* cu_seqlens, int S, const msa_shape_t* shape, float scale,
+                                int32_t* block_idx, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                msa_stream_t stream) {
+  if (!q || !k || !v || !q_idx || !k_idx || !block_idx || !out || !lse || !cu_seqlens || S < 1)
+    return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_idx) || !aligned16(k_idx) ||
+      !aligned16(out) || ((uintptr_t)block_idx & 3u) || ((uintptr_t)lse & 3u) || ((uintptr_t)cu_seqlens & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = (cudaStream_t)stream;
+  st = begin(workspace, workspace_bytes, msa_prefill_varlen_workspace(shape), s);
+  if (st != MSA_OK) return st;
+  // the block map lives where the attention scratch goes later: the select has read it by then
+  int32_t* blk_lo = (int32_t*)((char*)workspace + kHeader);
+  msa::DeviceStatus* dst = (msa::DeviceStatus*)workspace;
+  if (msa::launch_varlen_blocks(cu_seqlens, S, shape->N, shape->Bk, blk_lo, dst, s) != cudaSuccess)
+    return MSA_ERR_CUDA;
+  msa::AttnPlan p = msa::attn_plan(shape->N, shape->H_q, shape->H_kv, shape->d, shape->Bk, shape->k);
+  return finish(msa::launch_prefill(q, k, v, q_idx, k_idx, shape->d_I, p, scale, block_idx, out, lse,
+                                    (char*)workspace + kHeader, dst, s, false, blk_lo));
 }
 
 msa_status_t msa_prefill_fp8(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,

@@ -31,8 +31,14 @@ bool encode_tmap_4d(void* tmap, const void* base, const uint64_t dims[4], const 
 
 // ---- select (msa_select.cu)
 // f8: q_idx and k_idx hold FP8 E4M3 codes (d_I of 64 or 128) instead of bf16.
+// blk_lo (nullable): first block of each block's sequence when several
+// sequences share the cells; candidates of row t are then [blk_lo[t/Bk], t/Bk).
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
-                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s, bool f8 = false);
+                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s, bool f8 = false,
+                          const int32_t* blk_lo = nullptr);
+// blk_lo[nb] from the block-aligned sequence offsets cu_seqlens[S+1] (device).
+cudaError_t launch_varlen_blocks(const int32_t* cu_seqlens, int S, int64_t N, int Bk, int32_t* blk_lo,
+                                 DeviceStatus* st, cudaStream_t s);
 // y[i] = E4M3 code of (bf16 x[i]) * scale (round to nearest even, saturated at 448).
 cudaError_t launch_quantize_e4m3(const void* x, int64_t n, float scale, void* y, cudaStream_t s);
 
@@ -88,7 +94,8 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
 // The select kernel followed by the attention call, on one stream.
 cudaError_t launch_prefill(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
                            int d_I, const AttnPlan& p, float scale, int32_t* block_idx, void* out, float* lse,
-                           void* scratch, DeviceStatus* st, cudaStream_t s, bool f8 = false);
+                           void* scratch, DeviceStatus* st, cudaStream_t s, bool f8 = false,
+                           const int32_t* blk_lo = nullptr);
 
 // ---- backward (msa_bwd.cu)
 size_t bwd_scratch_bytes(int64_t N, int H_q, int H_kv, int d, int Bk, int k);

@@ -90,10 +90,18 @@ __device__ __forceinline__ int64_t key_tiles(int64_t qb, int Bk) {
   return (key_limit + kKeys - 1) / kKeys;
 }
 
+// First key tile a query tile needs when several sequences share the cells
+// (blk_lo[b] = first block of block b's sequence): the tile holding the first
+// block of its first row's sequence; 0 for one sequence.
+__device__ __forceinline__ int64_t first_key_tile(const int32_t* blk_lo, int64_t qb, int Bk) {
+  return blk_lo ? (int64_t)__ldg(blk_lo + qb * kRows / Bk) * Bk / kKeys : 0;
+}
+
 template <int DI, int CAP, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     select_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     int64_t N, int G, int gpc, int Bk, int k, int32_t* __restrict__ block_idx, DeviceStatus* st) {
+                     int64_t N, int G, int gpc, int Bk, int k, int32_t* __restrict__ block_idx,
+                     const int32_t* __restrict__ blk_lo, DeviceStatus* st) {
   using L = SelectLayout<DI, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -160,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && next_item(r, n_items, j)) {
         const int64_t qb = n_qt - 1 - j / n_gq;
         const int gq = (int)(j % n_gq);
-        const int64_t nkt = key_tiles(qb, Bk);
-        if (nkt == 0) continue;
+        const int64_t nkt = key_tiles(qb, Bk), kt0 = first_key_tile(blk_lo, qb, Bk);
+        if (nkt <= kt0) continue;
         if (!(ok = mbar_wait(a_empty, (a_glob & 1) ^ 1, abort, st, 0x101, kHint))) break;
         mbar_arrive_expect_tx(a_full, (uint32_t)(gpc * L::NCH * L::A_CHUNK));
         for (int gi = 0; gi < gpc; ++gi)
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (gq * gpc + gi) * DI + c * L::CH_E, (int32_t)(qb * kRows), a_full);
         a_last = a_glob & 1;
         ++a_glob;
-        for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
+        for (int64_t kt = kt0; kt < nkt; ++kt, ++kt_glob) {
           const int s = kt_glob % kStages;
           const uint32_t ph = (kt_glob / kStages) & 1;
           if (!(ok = mbar_wait(empty_bar(s), ph ^ 1, abort, st, 0x102, kHint))) break;
@@ -197,11 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       while (ok && next_item(r, n_items, j)) {
         const int64_t qb = n_qt - 1 - j / n_gq;
-        const int64_t nkt = key_tiles(qb, Bk);
-        if (nkt == 0) continue;
+        const int64_t nkt = key_tiles(qb, Bk), kt0 = first_key_tile(blk_lo, qb, Bk);
+        if (nkt <= kt0) continue;
         if (!(ok = mbar_wait(a_full, a_glob & 1, abort, st, 0x201, kHint))) break;
         tc_fence_after();
-        for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
+        for (int64_t kt = kt0; kt < nkt; ++kt, ++kt_glob) {
           const int s = kt_glob % kStages;
           if (!(ok = mbar_wait(full_bar(s), (kt_glob / kStages) & 1, abort, st, 0x202, kHint))) break;
           for (int gi = 0; gi < gpc && ok; ++gi) {
@@ -251,11 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && next_item(r, n_items, j)) {
       const int64_t qb = n_qt - 1 - j / n_gq;
       const int gq = (int)(j % n_gq);
-      const int64_t nkt = key_tiles(qb, Bk);
+      const int64_t nkt = key_tiles(qb, Bk), kt0 = first_key_tile(blk_lo, qb, Bk);
       const int64_t t = qb * kRows + row;
       const int64_t local = t / Bk;
+      // candidates: blocks [lo, local) of the row's own sequence
+      const int64_t lo = (blk_lo && t < N) ? (int64_t)__ldg(blk_lo + local) : 0;
       top.init(k - 1);
-      for (int64_t kt = 0; kt < nkt; ++kt, ++kt_glob) {
+      for (int64_t kt = kt0; kt < nkt; ++kt, ++kt_glob) {
         const int buf = gpc == 2 ? gi : (int)(kt_glob & 1);
         const uint32_t use = buf ? uses1 : uses0;
         if (!(ok = mbar_wait(acc_full(buf), use & 1, abort, st, 0x301, kHint))) break;
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mb = max3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
           if (Bk == 64 || (h & 1)) {
             const int b = Bk == 128 ? (int)(2 * kt) + (h >> 1) : (int)(4 * kt) + h;
-            if (b < local) top.insert(mb, b);
+            if (b < local && b >= lo) top.insert(mb, b);
             mb = __int_as_float(0xff800000);
           }
         }
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DI, int CAP, bool F8>
 cudaError_t launch_t(const void* q_idx, const void* k_idx, int64_t N, int G, int gpc, int Bk, int k,
-                     int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
+                     int32_t* block_idx, const int32_t* blk_lo, DeviceStatus* st, cudaStream_t s) {
   using L = SelectLayout<DI, F8>;
   CUtensorMap tq, tk;
   if (!encode_tmap_2d(&tq, q_idx, (uint64_t)G * DI, (uint64_t)N, (uint64_t)G * L::RB, L::CH_E, kRows, L::CH_B,
@@ -339,18 +349,49 @@ cudaError_t launch_t(const void* q_idx, const void* k_idx, int64_t N, int G, int
   if (e != cudaSuccess) return e;
   const int64_t n_items = ((N + kRows - 1) / kRows) * (G / gpc);
   const int grid = (int)(n_items < num_sms() ? n_items : num_sms());
-  kern<<<grid, kThreads, smem, s>>>(tq, tk, N, G, gpc, Bk, k, block_idx, st);
+  kern<<<grid, kThreads, smem, s>>>(tq, tk, N, G, gpc, Bk, k, block_idx, blk_lo, st);
   return cudaGetLastError();
 }
 
 template <int DI, bool F8>
 cudaError_t launch_cap(const void* q_idx, const void* k_idx, int64_t N, int G, int gpc, int Bk, int k,
-                       int32_t* block_idx, DeviceStatus* st, cudaStream_t s) {
+                       int32_t* block_idx, const int32_t* blk_lo, DeviceStatus* st, cudaStream_t s) {
   const int km1 = k - 1;
-  if (km1 <= 4) return launch_t<DI, 4, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  if (km1 <= 8) return launch_t<DI, 8, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  if (km1 <= 16) return launch_t<DI, 16, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  return launch_t<DI, 32, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (km1 <= 4) return launch_t<DI, 4, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+  if (km1 <= 8) return launch_t<DI, 8, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+  if (km1 <= 16) return launch_t<DI, 16, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+  return launch_t<DI, 32, F8>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+}
+
+// blk_lo[b] = first block of the sequence whose cells hold block b.  Sequence
+// s holds cells [cu[s], cu[s+1]); every cu[s] must be a multiple of Bk with
+// cu[0] = 0, non-decreasing, cu[S] <= N.  Blocks past cu[S] belong to no
+// sequence (blk_lo[b] = b: the local block only).  A cu that breaks those
+// rules sets the device error word; every block then keeps only its local
+// block.
+__global__ void varlen_blocks_kernel(const int32_t* __restrict__ cu, int S, int64_t N, int Bk, int64_t nb,
+                                     int32_t* __restrict__ blk_lo, DeviceStatus* st) {
+  __shared__ int bad;
+  if (threadIdx.x == 0) {
+    int b_ = cu[0] != 0;
+    for (int i = 0; i < S && !b_; ++i) b_ = cu[i + 1] < cu[i] || (cu[i + 1] % Bk) != 0;
+    b_ = b_ || (int64_t)cu[S] > N;
+    bad = b_;
+    if (b_ && blockIdx.x == 0) raise_error(st, kErrBadIndex, 4u);
+  }
+  __syncthreads();
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nb; b += (int64_t)gridDim.x * blockDim.x) {
+    int32_t lo = (int32_t)b;
+    if (!bad && b * Bk < (int64_t)cu[S]) {
+      int a = 0, z = S;  // the last s with cu[s] <= b * Bk (cu[0] = 0 <= b * Bk)
+      while (z - a > 1) {
+        const int m = (a + z) >> 1;
+        if ((int64_t)cu[m] <= b * Bk) a = m; else z = m;
+      }
+      lo = cu[a] / Bk;
+    }
+    blk_lo[b] = lo;
+  }
 }
 
 // y = E4M3 code of (bf16 x) * scale, nearest with ties to even, saturated at
@@ -386,16 +427,25 @@ __global__ void __launch_bounds__(256) quantize_e4m3_kernel(const uint16_t* __re
 }  // namespace
 
 cudaError_t launch_select(const void* q_idx, const void* k_idx, int64_t N, int G, int d_I, int Bk, int k,
-                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s, bool f8) {
+                          int32_t* block_idx, DeviceStatus* st, cudaStream_t s, bool f8, const int32_t* blk_lo) {
   const int gpc = (G % 2 == 0) ? 2 : 1;
   if (f8) {  // d_I of 64 or 128 (64- or 128-byte rows)
-    if (d_I == 64) return launch_cap<64, true>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-    if (d_I == 128) return launch_cap<128, true>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+    if (d_I == 64) return launch_cap<64, true>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+    if (d_I == 128) return launch_cap<128, true>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
     return cudaErrorInvalidValue;
   }
-  if (d_I == 32) return launch_cap<32, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  if (d_I == 64) return launch_cap<64, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
-  return launch_cap<128, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, st, s);
+  if (d_I == 32) return launch_cap<32, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+  if (d_I == 64) return launch_cap<64, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+  return launch_cap<128, false>(q_idx, k_idx, N, G, gpc, Bk, k, block_idx, blk_lo, st, s);
+}
+
+cudaError_t launch_varlen_blocks(const int32_t* cu_seqlens, int S, int64_t N, int Bk, int32_t* blk_lo,
+                                 DeviceStatus* st, cudaStream_t s) {
+  const int64_t nb = (N + Bk - 1) / Bk;
+  int64_t blocks = (nb + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  varlen_blocks_kernel<<<(unsigned)blocks, 256, 0, s>>>(cu_seqlens, S, N, Bk, nb, blk_lo, st);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_e4m3(const void* x, int64_t n, float scale, void* y, cudaStream_t s) {

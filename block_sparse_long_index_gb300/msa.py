@@ -53,6 +53,10 @@ _SIGS = {
     "msa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P]),
     "msa_quantize_e4m3": (_I, [_P, _I64, _F, _P, _P]),
+    "msa_select_blocks_varlen_workspace": (_SZ, [_I64, _I, _I, _I, _I]),
+    "msa_select_blocks_varlen": (_I, [_P, _P, _P, _I, _I64, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "msa_prefill_varlen_workspace": (_SZ, [_SP]),
+    "msa_prefill_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_select_blocks_fp8": (_I, [_P, _P, _I64, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "msa_prefill_fp8": (_I, [_P, _P, _P, _P, _P, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_fp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
@@ -227,6 +231,30 @@ def msa_decode_paged_fp8(q_t, q_idx_t, k_idx_pool, k_pool, v_pool, page_table, m
                                             int(page_size), _ptr(ctx_len), B, ctypes.byref(shp), float(scale),
                                             _ptr(out), _ptr(lse), _ptr(block_idx), _ptr(workspace), wb,
                                             _stream(stream)), "msa_decode_paged_fp8")
+
+
+def msa_select_blocks_varlen_workspace(N, G, d_I, Bk, k):
+    return int(_lib.msa_select_blocks_varlen_workspace(N, G, d_I, Bk, k))
+
+
+def msa_select_blocks_varlen(q_idx, k_idx, cu_seqlens, S, N, G, d_I, Bk, k, block_idx, workspace,
+                             workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_select_blocks_varlen(_ptr(q_idx), _ptr(k_idx), _ptr(cu_seqlens), int(S), N, G, d_I, Bk,
+                                                k, _ptr(block_idx), _ptr(workspace), wb, _stream(stream)),
+                  "msa_select_blocks_varlen")
+
+
+def msa_prefill_varlen_workspace(shp):
+    return int(_lib.msa_prefill_varlen_workspace(ctypes.byref(shp)))
+
+
+def msa_prefill_varlen(q, k, v, q_idx, k_idx, cu_seqlens, S, shp, scale, block_idx, out, lse, workspace,
+                       workspace_bytes=None, stream=None):
+    wb = workspace.numel() if workspace_bytes is None else workspace_bytes
+    return _check(_lib.msa_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(cu_seqlens),
+                                          int(S), ctypes.byref(shp), float(scale), _ptr(block_idx), _ptr(out),
+                                          _ptr(lse), _ptr(workspace), wb, _stream(stream)), "msa_prefill_varlen")
 
 
 def msa_check_device_error(workspace, stream=None):

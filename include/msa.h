@@ -189,6 +189,48 @@ msa_status_t msa_prefill(const void* q, const void* k, const void* v, const void
                          const msa_shape_t* shape, float scale, int32_t* block_idx, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/* ---------------------------------------------------------------- varlen prefill
+ * Several sequences in one prefill, each in its own run of cells.  Pages:
+ * velog llama.cpp analysis, section 4 (with sequences mixed in one shared
+ * cache the condition "block of the sequence = run of consecutive cache
+ * cells" breaks and the port falls back to dense attention) and section 5
+ * (the fix named there: an explicit per-sequence position -> cell -> block
+ * map).
+ *
+ * Layout: sequence s holds cells [cu_seqlens[s], cu_seqlens[s+1]) of the
+ * N-cell tensors (q, k, v, q_idx, k_idx, out, lse, block_idx: the msa_prefill
+ * layouts with N cells); its position p is cell cu_seqlens[s] + p.  Every
+ * cu_seqlens[s] is a multiple of Bk, cu_seqlens[0] = 0, the values do not
+ * decrease and cu_seqlens[S] <= N.  A sequence's blocks are therefore whole
+ * runs of cells and never shared.  Cells of a sequence past its last token
+ * (padding up to the next block boundary) and cells past cu_seqlens[S] are
+ * computed like tokens; no real token selects or attends to them (they lie
+ * after every token of their block, and blocks of other sequences are never
+ * candidates).
+ *
+ * Per cell t of sequence s the set is msa_select_blocks' rule with the
+ * candidates restricted to the sequence: {local(t)} plus the k-1 best blocks b
+ * with cu_seqlens[s]/Bk <= b < local(t).  Block ids are cell block ids.  The
+ * attention is msa_sparse_attn_fwd on those sets, so out and lse of every
+ * real token equal msa_prefill run on that sequence alone (block ids offset
+ * by cu_seqlens[s]/Bk).
+ *
+ *   cu_seqlens [S+1] int32 (device), S >= 1.  A cu_seqlens that breaks the
+ *              rules above sets the device error word (MSA_ERR_BAD_INDEX from
+ *              msa_check_device_error); every cell then keeps only its local
+ *              block.
+ *   workspace  msa_select_blocks_varlen_workspace() / msa_prefill_varlen_workspace() bytes
+ */
+size_t msa_select_blocks_varlen_workspace(int64_t N, int G, int d_I, int Bk, int k);
+msa_status_t msa_select_blocks_varlen(const void* q_idx, const void* k_idx, const int32_t* cu_seqlens, int S,
+                                      int64_t N, int G, int d_I, int Bk, int k, int32_t* block_idx, void* workspace,
+                                      size_t workspace_bytes, msa_stream_t stream);
+size_t msa_prefill_varlen_workspace(const msa_shape_t* shape);
+msa_status_t msa_prefill_varlen(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                const int32_t* cu_seqlens, int S, const msa_shape_t* shape, float scale,
+                                int32_t* block_idx, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                msa_stream_t stream);
+
 /* ---------------------------------------------------------------- decode
  * One decode step for B sequences.  The query of sequence s sits at position
  * t = ctx_len[s] - 1 and its k, v and k^I are already in the caches.  The

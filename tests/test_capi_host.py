@@ -144,3 +144,31 @@ def test_fp8_entry_points_validation(lib):
     assert raw.msa_quantize_e4m3(ctypes.c_void_p((1 << 20) + 1), 8, 1.0, FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
     assert raw.msa_quantize_e4m3(FAKE, 8, float("nan"), FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
     assert raw.msa_quantize_e4m3(None, 0, 1.0, None, None) == lib.MSA_OK  # nothing to do
+
+
+def test_varlen_validation(lib):
+    raw = lib.raw()
+    N, G, d_I, Bk, k = 4096, 2, 128, 128, 8
+    ws = lib.msa_select_blocks_varlen_workspace(N, G, d_I, Bk, k)
+    assert ws >= lib.msa_select_blocks_workspace(N, G, d_I, Bk, k) + (N // Bk) * 4
+    assert raw.msa_select_blocks_varlen(FAKE, FAKE, None, 2, N, G, d_I, Bk, k, FAKE, FAKE, ws,
+                                        None) == lib.MSA_ERR_INVALID_ARGUMENT  # no cu_seqlens
+    assert raw.msa_select_blocks_varlen(FAKE, FAKE, FAKE, 0, N, G, d_I, Bk, k, FAKE, FAKE, ws,
+                                        None) == lib.MSA_ERR_INVALID_ARGUMENT  # S = 0
+    assert raw.msa_select_blocks_varlen(FAKE, FAKE, ctypes.c_void_p((1 << 20) + 2), 2, N, G, d_I, Bk, k, FAKE, FAKE,
+                                        ws, None) == lib.MSA_ERR_INVALID_ARGUMENT  # misaligned int32
+    assert raw.msa_select_blocks_varlen(FAKE, FAKE, FAKE, 2, N, G, d_I, Bk, k, FAKE, FAKE, ws - 256,
+                                        None) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    s = lib.shape(N, 16, G, 128, d_I, Bk, k)
+    need = lib.msa_prefill_varlen_workspace(s)
+    assert need >= lib.msa_prefill_workspace(s)
+    assert raw.msa_prefill_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, ctypes.byref(s), 0.1, FAKE, FAKE, FAKE, FAKE,
+                                  need - 256, None) == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    assert raw.msa_prefill_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, ctypes.byref(s), -1.0, FAKE, FAKE, FAKE, FAKE,
+                                  need, None) == lib.MSA_ERR_INVALID_ARGUMENT
+
+
+def test_varlen_cells_helper():
+    from block_sparse_long_index_gb300.api import varlen_cells
+    assert varlen_cells([1, 128, 129, 0, 300], 128) == [0, 128, 256, 512, 512, 896]
+    assert varlen_cells([64], 64) == [0, 64]
