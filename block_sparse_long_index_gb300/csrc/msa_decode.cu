@@ -34,7 +34,7 @@ namespace {
 constexpr int kScanThreads = 256;  // 8 warps, two CTAs per SM
 constexpr int kScanWarps = kScanThreads / 32;
 constexpr int kGroupsPerMma = 8;    // mma n = 8 groups
-constexpr int kMergeListsPerLane = 16;  // last-CTA merge: splits <= 32 * 16
+constexpr int kMergeListsPerLane = 8;  // last-CTA merge: splits <= 32 * 8
 constexpr int kMaxCtaBlocks = 2048;     // block maxima kept in shared memory per scan CTA
 
 // dims of fragment column kf (0..15) in k-step ks of the bf16 scan: see the load pattern below
@@ -56,6 +56,25 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Completion ticket of the last-CTA pattern: every thread's writes are made
+// visible (__threadfence) and gathered by __syncthreads before thread 0 takes a
+// ticket with acquire-release semantics; the CTA that takes the last ticket
+// then reads the others' results after a __syncthreads (L2 loads only).
+__device__ __forceinline__ unsigned int ticket_acq_rel(unsigned int* t) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(t) : "memory");
+  return old;
+}
+
+// The largest 64-bit key across the warp: two single-instruction reductions,
+// the high words first, then the low words of the lanes that hold that high word.
+__device__ __forceinline__ uint64_t warp_max_key(uint64_t x) {
+  const uint32_t hi = (uint32_t)(x >> 32), lo = (uint32_t)x;
+  const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? lo : 0u);
+  return ((uint64_t)mh << 32) | ml;
+}
+
 // 16-byte pieces 64q + 16c of key rows `row` and `row + 8` of a 16-key chunk (RB bytes per row)
 template <int RB>
 __device__ __forceinline__ void load_keys16(uint4 (&v)[RB / 64][2], const uint8_t* p) {
@@ -73,10 +92,10 @@ __device__ __forceinline__ void load_keys16(uint4 (&v)[RB / 64][2], const uint8_
 // F8: the index query and cache hold E4M3 codes; the same 16-byte pieces feed
 // m16n8k32 E4M3 MMAs (32 dims per k-step instead of 16), so a key row is half
 // the bytes and the scan reads half the cache traffic.
-template <int DI, int BK, bool PAGED, bool F8>
+template <int DI, int BK, bool PAGED, bool F8, int CAP>
 __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     const uint8_t* __restrict__ q_idx_t, const uint8_t* __restrict__ k_idx_cache,
-    const int32_t* __restrict__ ctx_len, int64_t ctx_max, CacheMap map, int G, int k, int splits,
+    const int32_t* __restrict__ ctx_len, int64_t ctx_max, CacheMap map, int G, int k, int splits, bool staged,
     uint64_t* __restrict__ cand, unsigned int* __restrict__ tickets, int32_t* __restrict__ block_idx,
     DeviceStatus* st) {
   constexpr int RB = DI * (F8 ? 1 : 2);  // bytes per index row
@@ -84,7 +103,8 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   constexpr int KS = 2 * NQ;             // MMA k-steps per 16-key chunk
   static_assert(NQ >= 1, "index rows of at least 64 bytes");
   constexpr int CPB = BK / 16;  // chunks per block
-  extern __shared__ uint32_t bmax_s[];  // [blocks of this CTA][8 groups], ordered_bits of the block maxima
+  // [blocks of this CTA][8 groups], ordered_bits of the block maxima; in the last CTA, later the staged lists
+  extern __shared__ __align__(16) uint32_t bmax_s[];
   __shared__ int s_last;
   griddep_launch_dependents();  // the attention grid may be scheduled once every scan CTA is resident
   const int seq = blockIdx.y, split = blockIdx.x;
@@ -185,28 +205,27 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   }
   __syncthreads();
 
-  // this CTA's top-(k-1) blocks of group g (warp g): k-1 rounds of a warp-wide
-  // maximum over (score, lower block id first) keys; the winner is cleared
+  // this CTA's top-(k-1) blocks of group g (warp g): lane l ranks blocks l,
+  // l + 32, ... of the CTA's range into its register list of the best CAP (one
+  // insertion site in a rolled loop), then k-1 rounds of a warp-wide maximum
+  // over the lists' heads pop the CTA's list, best first
+  const int kp = km1 + (km1 & 1);  // list stride: an even count of keys (16-byte rows)
   if (warp < G) {
     const int g = warp;
-    uint64_t* out = cand + (((int64_t)seq * splits + split) * G + g) * km1;
+    TopK<CAP> top;
+    top.init(CAP);
+#pragma unroll 1
+    for (int b = lane; b < nblk; b += 32) {
+      const uint32_t o = bmax_s[b * kGroupsPerMma + g];
+      if (o) top.insert_key(((uint64_t)o << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(b_lo + b)));
+    }
+    uint64_t* out = cand + (((int64_t)seq * G + g) * splits + split) * kp;
     for (int r = 0; r < km1; ++r) {
-      uint64_t best = 0;
-      for (int b = lane; b < nblk; b += 32) {
-        const uint32_t o = bmax_s[b * kGroupsPerMma + g];
-        const uint64_t key = o ? (((uint64_t)o << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(b_lo + b))) : 0ull;
-        best = key > best ? key : best;
-      }
+      const uint64_t best = warp_max_key(top.key[CAP - 1]);
+      const bool pop = best != 0ull && top.key[CAP - 1] == best;  // keys are unique: one lane pops
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
-      }
-      if (best != 0) {
-        const int b = (int)((0xFFFFFFFFu - (uint32_t)best) - (uint32_t)b_lo);
-        if ((b & 31) == lane) bmax_s[b * kGroupsPerMma + g] = 0u;
-      }
-      __syncwarp();
+      for (int i = CAP - 1; i > 0; --i) top.key[i] = pop ? top.key[i - 1] : top.key[i];
+      top.key[0] = pop ? 0ull : top.key[0];
       if (lane == 0) out[r] = best;  // 0 = no candidate
     }
   }
@@ -214,41 +233,64 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   // the last CTA of this sequence to get here merges every CTA's lists
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&tickets[seq], 1u) == (unsigned)(splits - 1);
+  if (tid == 0) s_last = ticket_acq_rel(&tickets[seq]) == (unsigned)(splits - 1);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
+  // with room in shared memory, each group's lists (contiguous in cand) are
+  // first copied there with 16-byte cp.async (L2 only), so the rounds below read
+  // the next head of a list from shared memory rather than from L2
+  uint64_t* stage = reinterpret_cast<uint64_t*>(bmax_s);
+  if (staged) {
+    const int n16 = splits * kp / 2;  // 16-byte pieces per group
+    for (int i = tid; i < G * n16; i += kScanThreads) {
+      const int gg = i / n16, j = i % n16;
+      cp_async_16(stage + ((int64_t)gg * splits * kp) + 2 * j,
+                  cand + (((int64_t)seq * G + gg) * splits) * kp + 2 * j, 16);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+  }
   if (warp < G) {
     // a tournament: lane l holds the heads of lists l, l + 32, ... (each sorted best-first)
     const int g = warp;
-    auto list = [&](int sp) { return cand + (((int64_t)seq * splits + sp) * G + g) * km1; };
+    const uint64_t* gl = cand + (((int64_t)seq * G + g) * splits) * kp;
+    const uint64_t* sl = stage + (int64_t)g * splits * kp;
+    auto entry = [&](int sp, int r) -> uint64_t {
+      return staged ? sl[sp * kp + r] : __ldcg(gl + (int64_t)sp * kp + r);
+    };
     int pos[kMergeListsPerLane];
     uint64_t head[kMergeListsPerLane];
 #pragma unroll
     for (int i = 0; i < kMergeListsPerLane; ++i) {
       const int sp = lane + 32 * i;
       pos[i] = 0;
-      head[i] = (sp < splits && km1 > 0) ? __ldcg(list(sp)) : 0ull;
+      head[i] = (sp < splits && km1 > 0) ? entry(sp, 0) : 0ull;
     }
     int32_t* outb = block_idx + ((int64_t)seq * G + g) * k;
     if (lane == 0) outb[0] = ok ? (int32_t)local : -1;
     for (int r = 0; r < km1; ++r) {
-      uint64_t best = 0;
+      uint64_t m2[kMergeListsPerLane / 2];  // the lane's best head, as a tree
 #pragma unroll
-      for (int i = 0; i < kMergeListsPerLane; ++i) best = head[i] > best ? head[i] : best;
+      for (int i = 0; i < kMergeListsPerLane / 2; ++i)
+        m2[i] = head[2 * i] > head[2 * i + 1] ? head[2 * i] : head[2 * i + 1];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, best, o);
-        best = other > best ? other : best;
-      }
+      for (int w = kMergeListsPerLane / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m2[i] = m2[i] > m2[i + w] ? m2[i] : m2[i + w];
+      const uint64_t best = warp_max_key(m2[0]);
       if (lane == 0) outb[1 + r] = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
       if (best == 0) continue;
+      // the list holding best (keys are unique: block ids differ across lists) moves to its next entry;
+      // branch-free, so the warp never splits over the lane that owns it
 #pragma unroll
-      for (int i = 0; i < kMergeListsPerLane; ++i)
-        if (head[i] == best) {  // keys are unique: block ids differ across lists
-          ++pos[i];
-          head[i] = pos[i] < km1 ? __ldcg(list(lane + 32 * i) + pos[i]) : 0ull;
-        }
+      for (int i = 0; i < kMergeListsPerLane; ++i) {
+        const bool hit = head[i] == best;
+        pos[i] += hit ? 1 : 0;
+        uint64_t nv = 0ull;
+        if (hit && pos[i] < km1) nv = entry(lane + 32 * i, pos[i]);
+        head[i] = hit ? nv : head[i];
+      }
     }
   }
   if (tid == 0) tickets[seq] = 0u;  // ready for the next call
@@ -288,8 +330,7 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   constexpr int C8 = D / 8;     // 16-byte chunks per row
   constexpr int KPW = BK / 4;   // keys per warp
   constexpr int NT = KPW / 8;   // 8-key n-tiles per warp
-  constexpr int KS = D / 16;    // k-steps over d
-  constexpr int NP = D / 32;    // 16-byte pieces of a row per lane
+  constexpr int NP = D / 32;    // 16-byte pieces of a row per lane (two k-steps over d each)
   static_assert(NT % 2 == 0, "P V k-steps take two n-tiles");
   static_assert(4 * 8 * D * 4 <= BK * D * 2, "partial O sums fit over V");
   const int slot = blockIdx.x, g = blockIdx.y, seq = blockIdx.z;
@@ -433,10 +474,9 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   // the last of the group's k CTAs merges the partials
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&tickets[(int64_t)seq * G + g], 1u) == (unsigned)(k - 1);
+  if (tid == 0) s_last = ticket_acq_rel(&tickets[(int64_t)seq * G + g]) == (unsigned)(k - 1);
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   const float* gl = part_lse + ((int64_t)seq * H_q + g * gs) * k;  // [gs][k]
   for (int i = tid; i < gs * k; i += blockDim.x) w_s[i / k][i % k] = __ldcg(gl + i);
   __syncthreads();
@@ -493,13 +533,16 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
 
 struct DecodeScratch {
   unsigned int* tickets;  // [B] scan + [B * G] attention; cleared before every call
-  uint64_t* cand;         // [B, splits, G, k-1] per-CTA candidate keys
+  uint64_t* cand;         // [B, G, splits, kp] per-CTA candidate keys (kp = k-1 rounded up to even)
   int32_t* blk;
   float* part_o;
   float* part_lse;
 };
 
 static size_t ticket_bytes(const DecodePlan& p) { return align_up((size_t)p.B * (1 + p.H_kv) * 4, 256); }
+static int list_stride(const DecodePlan& p) { return p.k > 1 ? (p.k - 1) + ((p.k - 1) & 1) : 2; }
+constexpr size_t kStageMaxBytes = 96 * 1024;  // the last CTA stages the lists in shared memory up to this size
+static size_t stage_bytes(const DecodePlan& p) { return (size_t)p.H_kv * p.splits * list_stride(p) * 8; }
 
 static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   char* c = (char*)base;
@@ -511,7 +554,7 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   };
   DecodeScratch s;
   s.tickets = (unsigned int*)take(ticket_bytes(p));
-  s.cand = (uint64_t*)take((size_t)p.B * p.splits * p.H_kv * (p.k > 1 ? p.k - 1 : 1) * 8);
+  s.cand = (uint64_t*)take((size_t)p.B * p.splits * p.H_kv * list_stride(p) * 8);
   s.blk = (int32_t*)take((size_t)p.B * p.H_kv * p.k * 4);
   s.part_o = (float*)take((size_t)p.B * p.H_q * p.k * p.d * 4);
   s.part_lse = (float*)take((size_t)p.B * p.H_q * p.k * 4);
@@ -519,18 +562,28 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   return off;
 }
 
+template <int DI, int BK, bool PAGED, bool F8, int CAP>
+cudaError_t launch_scan_c(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
+                          const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
+                          cudaStream_t s) {
+  const size_t bm = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
+  const bool staged = stage_bytes(p) <= kStageMaxBytes;
+  const size_t smem = staged && stage_bytes(p) > bm ? stage_bytes(p) : bm;
+  auto kern = decode_scan_kernel<DI, BK, PAGED, F8, CAP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
+      (const uint8_t*)q_idx_t, (const uint8_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits, staged,
+      sc.cand, sc.tickets, blk, st);
+  return cudaGetLastError();
+}
+
 template <int DI, int BK, bool PAGED, bool F8>
 cudaError_t launch_scan_t(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
                           const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
                           cudaStream_t s) {
-  const size_t smem = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
-  auto kern = decode_scan_kernel<DI, BK, PAGED, F8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  kern<<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
-      (const uint8_t*)q_idx_t, (const uint8_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits,
-      sc.cand, sc.tickets, blk, st);
-  return cudaGetLastError();
+  return p.k - 1 <= 16 ? launch_scan_c<DI, BK, PAGED, F8, 16>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
+                       : launch_scan_c<DI, BK, PAGED, F8, 32>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
 }
 
 template <int DI, int BK>
