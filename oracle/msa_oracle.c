@@ -855,3 +855,126 @@ int msa_ref_sparse_attn_bwd_rows(const uint16_t* q, const uint16_t* K, const uin
   free(dq), free(dqI), free(kl);
   return c.status;
 }
+
+
+/* -------------------------------------------------------------- warmup mode */
+/*
+ * [P1] 4-4 "Indexer warmup": before top-k routing is switched on, the main
+ * branch runs full (dense causal) attention and the index branch learns the KL
+ * alignment against the full-context teacher.  Per row (t, g), over every
+ * j <= t:
+ *   z_{h,j} = scale q_{t,h}.k_{j,g}, P_{h,j} = exp(z_{h,j} - lse_h) for the
+ *   group's heads h ([P1] 1-1, dense causal GQA); teacher pbar_j = mean_h P_{h,j}
+ *   ([P1] 4-2, detached); index logits zI_j = q^I.k^I_j / sqrt(d_I);
+ *   KL = sum_j pbar_j (log pbar_j - log pI_j) with pI = softmax_j(zI);
+ *   dL/dzI_j = w (pI_j - pbar_j) ([P4] KL section);
+ *   dq^I_{t,g} = sum_j dL/dzI_j k^I_j / sqrt(d_I),
+ *   dk^I_j += dL/dzI_j q^I_{t,g} / sqrt(d_I).
+ * The main branch's own output is msa_ref_dense_attn.
+ */
+typedef struct {
+  const uint16_t *q, *K, *q_idx, *k_idx;
+  const int64_t* rows; /* NULL: every position */
+  int64_t n_rows, N;
+  int H_q, H_kv, d, d_I, chunks;
+  double scale, kl_weight;
+  double *kl, *dq_idx; /* [G, n_rows], [n_rows, G, d_I] */
+  double* dkI_acc;     /* [items][N][d_I] or NULL */
+  int status;
+} warm_ctx;
+
+static void warm_item(int64_t it, void* p) {
+  warm_ctx* c = (warm_ctx*)p;
+  const int g = (int)(it / c->chunks), ch = (int)(it % c->chunks);
+  const int gs = c->H_q / c->H_kv, d = c->d, dI = c->d_I;
+  const int64_t r0 = c->n_rows * ch / c->chunks, r1 = c->n_rows * (ch + 1) / c->chunks;
+  const int64_t kv_stride = (int64_t)c->H_kv * d;
+  double* dkI_acc = c->dkI_acc ? c->dkI_acc + it * c->N * dI : NULL;
+  double* z = (double*)malloc(sizeof(double) * (size_t)c->N);
+  double* pbar = (double*)malloc(sizeof(double) * (size_t)c->N);
+  if (!z || !pbar) {
+    c->status = ORACLE_NO_MEM;
+    free(z), free(pbar);
+    return;
+  }
+  const double sI = 1.0 / sqrt((double)dI);
+  for (int64_t ri = r0; ri < r1; ++ri) {
+    const int64_t t = c->rows ? c->rows[ri] : ri;
+    const int64_t n = t + 1; /* keys 0..t */
+    for (int64_t j = 0; j < n; ++j) pbar[j] = 0.0;
+    for (int hh = 0; hh < gs; ++hh) {
+      const uint16_t* qr = c->q + (t * c->H_q + g * gs + hh) * d;
+      double m = -INFINITY;
+      for (int64_t j = 0; j < n; ++j) {
+        z[j] = c->scale * dot_bf16(qr, c->K + j * kv_stride + (int64_t)g * d, d);
+        if (z[j] > m) m = z[j];
+      }
+      double l = 0.0;
+      for (int64_t j = 0; j < n; ++j) l += exp(z[j] - m);
+      const double lse = m + log(l);
+      for (int64_t j = 0; j < n; ++j) pbar[j] += exp(z[j] - lse) / gs;
+    }
+    const uint16_t* qIr = c->q_idx + (t * c->H_kv + g) * dI;
+    double mI = -INFINITY;
+    for (int64_t j = 0; j < n; ++j) {
+      z[j] = sI * dot_bf16(qIr, c->k_idx + j * dI, dI);
+      if (z[j] > mI) mI = z[j];
+    }
+    double lI = 0.0;
+    for (int64_t j = 0; j < n; ++j) lI += exp(z[j] - mI);
+    const double lseI = mI + log(lI);
+    double* dqI = c->dq_idx + (ri * c->H_kv + g) * dI;
+    for (int x = 0; x < dI; ++x) dqI[x] = 0.0;
+    double kl = 0.0;
+    for (int64_t j = 0; j < n; ++j) {
+      const double logpI = z[j] - lseI;
+      if (pbar[j] > 0.0) kl += pbar[j] * (log(pbar[j]) - logpI);
+      const double dz = c->kl_weight * (exp(logpI) - pbar[j]);
+      const uint16_t* kIr = c->k_idx + j * dI;
+      for (int x = 0; x < dI; ++x) dqI[x] += sI * dz * bf16_to_double(kIr[x]);
+      if (dkI_acc) {
+        double* dkIr = dkI_acc + j * dI;
+        for (int x = 0; x < dI; ++x) dkIr[x] += sI * dz * bf16_to_double(qIr[x]);
+      }
+    }
+    c->kl[(int64_t)g * c->n_rows + ri] = kl;
+  }
+  free(z), free(pbar);
+}
+
+/*
+ * Warmup mode's index-branch loss and gradients.  rows == NULL: every
+ * position (n_rows = N), and dk_idx [N, d_I] is written; otherwise only the
+ * listed positions' kl [G, n_rows] and dq_idx [n_rows, G, d_I] (dk_idx may be
+ * NULL).  q [N, H_q, d], K [N, H_kv, d], q_idx [N, G, d_I], k_idx [N, d_I].
+ */
+int msa_ref_warmup_index(const uint16_t* q, const uint16_t* K, const uint16_t* q_idx, const uint16_t* k_idx,
+                         const int64_t* rows, int64_t n_rows, int64_t N, int H_q, int H_kv, int d, int d_I,
+                         double scale, double kl_weight, double* kl, double* dq_idx, double* dk_idx, int n_threads) {
+  if (!q || !K || !q_idx || !k_idx || !kl || !dq_idx || N <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 ||
+      d_I <= 0 || (!rows && (n_rows != N || !dk_idx)))
+    return ORACLE_BAD_ARG;
+  if (rows)
+    for (int64_t r = 0; r < n_rows; ++r)
+      if (rows[r] < 0 || rows[r] >= N) return ORACLE_BAD_ARG;
+  int chunks = n_threads / H_kv;
+  if (chunks < 1) chunks = 1;
+  const int want_dk = rows == NULL;
+  while (want_dk && chunks > 1 && (double)N * d_I * 8.0 * chunks * H_kv > 2.0e9) --chunks;
+  const int64_t items = (int64_t)H_kv * chunks;
+  double* dkI_acc = want_dk ? (double*)calloc((size_t)(items * N * d_I), sizeof(double)) : NULL;
+  if (want_dk && !dkI_acc) return ORACLE_NO_MEM;
+  warm_ctx c = {q, K, q_idx, k_idx, rows, n_rows, N, H_q, H_kv, d, d_I, chunks, scale, kl_weight, kl, dq_idx,
+                dkI_acc, 0};
+  parallel_for(items, n_threads, warm_item, &c);
+  if (want_dk) {
+    for (int64_t j = 0; j < N; ++j)
+      for (int x = 0; x < d_I; ++x) {
+        double a = 0.0;
+        for (int64_t itm = 0; itm < items; ++itm) a += dkI_acc[(itm * N + j) * d_I + x];
+        dk_idx[j * d_I + x] = a;
+      }
+    free(dkI_acc);
+  }
+  return c.status;
+}
