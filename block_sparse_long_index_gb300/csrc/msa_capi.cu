@@ -346,6 +346,43 @@ msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, co
                                 dk_idx, kl, (char*)workspace + kHeader, (msa::DeviceStatus*)workspace, s));
 }
 
+static msa_status_t check_warmup(const msa_shape_t* shape, float scale) {
+  msa_status_t st = check_shape(shape);
+  if (st != MSA_OK) return st;
+  if (!(scale > 0.f) || scale != scale) return MSA_ERR_INVALID_ARGUMENT;
+  if (shape->N > ((int64_t)1 << 31) / 16 * 16) return MSA_ERR_UNSUPPORTED;
+  return MSA_OK;
+}
+
+msa_status_t msa_warmup_fwd(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                            const msa_shape_t* shape, float scale, void* out, float* lse, float* lse_idx,
+                            msa_stream_t stream) {
+  if (!q || !k || !v || !q_idx || !k_idx || !out || !lse || !lse_idx) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_warmup(shape, scale);
+  if (st != MSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_idx) || !aligned16(k_idx) || !aligned16(out) ||
+      ((uintptr_t)lse & 3u) || ((uintptr_t)lse_idx & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  return finish(msa::launch_warmup(q, k, v, q_idx, k_idx, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I,
+                                   scale, 0.f, true, false, out, lse, lse_idx, nullptr, nullptr, nullptr,
+                                   (cudaStream_t)stream));
+}
+
+msa_status_t msa_warmup_index_grad(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                                   const float* lse, const float* lse_idx, const msa_shape_t* shape, float scale,
+                                   float kl_weight, float* dq_idx, float* dk_idx, float* kl, msa_stream_t stream) {
+  if (!q || !k || !q_idx || !k_idx || !lse || !lse_idx || !dq_idx || !dk_idx || !kl) return MSA_ERR_INVALID_ARGUMENT;
+  msa_status_t st = check_warmup(shape, scale);
+  if (st != MSA_OK) return st;
+  if (kl_weight != kl_weight) return MSA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_idx) || !aligned16(k_idx) || !aligned16(dq_idx) ||
+      !aligned16(dk_idx) || ((uintptr_t)lse & 3u) || ((uintptr_t)lse_idx & 3u) || ((uintptr_t)kl & 3u))
+    return MSA_ERR_INVALID_ARGUMENT;
+  return finish(msa::launch_warmup(q, k, nullptr, q_idx, k_idx, shape->N, shape->H_q, shape->H_kv, shape->d,
+                                   shape->d_I, scale, kl_weight, false, true, nullptr, const_cast<float*>(lse),
+                                   const_cast<float*>(lse_idx), dq_idx, dk_idx, kl, (cudaStream_t)stream));
+}
+
 size_t msa_decode_workspace(int B, const msa_shape_t* shape) {
   if (B < 1 || check_shape(shape) != MSA_OK) return kHeader;
   msa::DecodePlan p = msa::decode_plan(B, shape->N, shape->H_q, shape->H_kv, shape->d, shape->d_I, shape->Bk,

@@ -106,6 +106,14 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
                        float* dk, float* dv, float* dq_idx, float* dk_idx, float* kl, void* scratch, DeviceStatus* st,
                        cudaStream_t s);
 
+// ---- warmup mode (msa_warmup.cu)
+// fwd: out, lse (dense causal attention) and lseI [G, N] (the index branch's
+// lse over every key j <= t); grad: kl [G, N], dq_idx [N, G, d_I] and dk_idx
+// [N, d_I] (cleared here, then accumulated) from lse and lseI.
+cudaError_t launch_warmup(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx, int64_t N,
+                          int H_q, int H_kv, int d, int d_I, float scale, float kl_weight, bool fwd, bool grad,
+                          void* out, float* lse, float* lseI, float* dq_idx, float* dk_idx, float* kl, cudaStream_t s);
+
 // ---- decode (msa_decode.cu)
 // Where token `key` of sequence `seq` sits in a decode cache: contiguous (no
 // table: row seq * ctx_max + key) or paged (row table[seq][key / page] * page +

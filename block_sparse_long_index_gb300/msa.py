@@ -53,6 +53,8 @@ _SIGS = {
     "msa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I, _P, _I, _SP, _F, _P, _P, _P, _P, _SZ, _P]),
     "msa_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _SP, _F, _P, _P, _P, _P]),
     "msa_quantize_e4m3": (_I, [_P, _I64, _F, _P, _P]),
+    "msa_warmup_fwd": (_I, [_P, _P, _P, _P, _P, _SP, _F, _P, _P, _P, _P]),
+    "msa_warmup_index_grad": (_I, [_P, _P, _P, _P, _P, _P, _SP, _F, _F, _P, _P, _P, _P]),
     "msa_select_blocks_varlen_workspace": (_SZ, [_I64, _I, _I, _I, _I]),
     "msa_select_blocks_varlen": (_I, [_P, _P, _P, _I, _I64, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "msa_prefill_varlen_workspace": (_SZ, [_SP]),
@@ -255,6 +257,18 @@ def msa_prefill_varlen(q, k, v, q_idx, k_idx, cu_seqlens, S, shp, scale, block_i
     return _check(_lib.msa_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(cu_seqlens),
                                           int(S), ctypes.byref(shp), float(scale), _ptr(block_idx), _ptr(out),
                                           _ptr(lse), _ptr(workspace), wb, _stream(stream)), "msa_prefill_varlen")
+
+
+def msa_warmup_fwd(q, k, v, q_idx, k_idx, shp, scale, out, lse, lse_idx, stream=None):
+    return _check(_lib.msa_warmup_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), ctypes.byref(shp),
+                                      float(scale), _ptr(out), _ptr(lse), _ptr(lse_idx), _stream(stream)),
+                  "msa_warmup_fwd")
+
+
+def msa_warmup_index_grad(q, k, q_idx, k_idx, lse, lse_idx, shp, scale, kl_weight, dq_idx, dk_idx, kl, stream=None):
+    return _check(_lib.msa_warmup_index_grad(_ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(lse), _ptr(lse_idx),
+                                             ctypes.byref(shp), float(scale), float(kl_weight), _ptr(dq_idx),
+                                             _ptr(dk_idx), _ptr(kl), _stream(stream)), "msa_warmup_index_grad")
 
 
 def msa_check_device_error(workspace, stream=None):

@@ -171,6 +171,35 @@ msa_status_t msa_sparse_attn_bwd(const void* q, const void* k, const void* v, co
                                  float* dv, float* dq_idx, float* dk_idx, float* kl, void* workspace,
                                  size_t workspace_bytes, msa_stream_t stream);
 
+/* ---------------------------------------------------------------- warmup mode
+ * The training-time variant that comes before sparse routing.  Pages: the
+ * "MSA" study note, 4-4 "Indexer warmup" (the main branch runs full attention
+ * while the index branch learns the KL alignment against the full-context
+ * teacher; top-k routing is switched on afterwards), 4-2 and 4-3 (the teacher
+ * is the mean of the group's main-branch probabilities, detached, and the KL
+ * reaches only q^I and k^I), 1-1 (dense causal GQA attention).  Same
+ * definitions as msa_sparse_attn_bwd's index branch, with J(t, g) = every key
+ * j <= t.  shape->Bk and shape->k must be valid values but are not used.  No
+ * workspace and no device-side error paths.
+ *
+ * msa_warmup_fwd: dense causal attention and the index branch's normaliser.
+ *   q, k, v, q_idx, k_idx: as msa_prefill
+ *   out      [N, H_q, d] bf16 out: softmax(scale q.k_j, j <= t) V
+ *   lse      [H_q, N] fp32 out: natural-log log-sum-exp of the scaled scores
+ *   lse_idx  [G, N] fp32 out: log-sum-exp over j <= t of q^I.k^I_j / sqrt(d_I)
+ * msa_warmup_index_grad: the KL loss of every row and its gradients, from the
+ *   forward's lse and lse_idx.
+ *   kl       [G, N] fp32 out: KL(teacher || index) of each row (not weighted)
+ *   dq_idx   [N, G, d_I] fp32 out: kl_weight * d(sum KL)/d q^I
+ *   dk_idx   [N, d_I] fp32 out: kl_weight * d(sum KL)/d k^I (overwritten)
+ */
+msa_status_t msa_warmup_fwd(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                            const msa_shape_t* shape, float scale, void* out, float* lse, float* lse_idx,
+                            msa_stream_t stream);
+msa_status_t msa_warmup_index_grad(const void* q, const void* k, const void* q_idx, const void* k_idx,
+                                   const float* lse, const float* lse_idx, const msa_shape_t* shape, float scale,
+                                   float kl_weight, float* dq_idx, float* dk_idx, float* kl, msa_stream_t stream);
+
 /* ---------------------------------------------------------------- prefill
  * The whole forward pass in one call: msa_select_blocks followed by
  * msa_sparse_attn_fwd on the same shapes and stream, with the same results.

@@ -47,7 +47,7 @@ def _load():
         lib.msa_ref_e4m3_quantize.argtypes = [P, I64, ctypes.c_float, P]
         lib.msa_ref_block_scores_e4m3.argtypes = [P, P, P, I64, I64, I, I, I, P, I]
         lib.msa_ref_select_blocks_e4m3.argtypes = [P, P, P, I64, I64, I, I, I, I, P, P, I]
-        lib.msa_ref_warmup_index.argtypes = [P, P, P, P, P, I64, I64, I, I, I, I, D, D, P, P, P, I]
+        lib.msa_ref_warmup_index.argtypes = [P, P, P, P, P, I64, I64, I, I, I, I, D, D, P, P, P, P, I]
         lib.msa_ref_invert_blocks.argtypes = [P, I64, I, I, I, P, P, P]
         lib.msa_ref_sparse_attn.argtypes = [P, P, P, P, P, I64, I64, I, I, I, I, I, D, P, P, I]
         lib.msa_ref_dense_attn.argtypes = [P, P, P, P, I64, I64, I, I, I, D, P, P, I]
@@ -262,7 +262,7 @@ def sparse_attn_bwd_rows(q, k, v, q_idx, k_idx, block_idx, dout, rows, Bk, scale
 def warmup_index(q, k, q_idx, k_idx, scale, kl_weight=1.0, rows=None, n_threads=None):
     """Warmup mode's index branch ("MSA" study note 4-4 "Indexer warmup"): the full-context teacher (mean over
     the group's heads of dense causal attention probabilities), the KL of each row and its gradients on q^I
-    and k^I.  Returns dict(kl [G, R], dq_idx [R, G, d_I], dk_idx [N, d_I] or None with rows)."""
+    and k^I.  Returns dict(kl [G, R], dq_idx [R, G, d_I], dk_idx [N, d_I] or None with rows, lse_idx [G, R])."""
     q, k, q_idx, k_idx = _u16(q), _u16(k), _u16(q_idx), _u16(k_idx)
     N, H_q, d = q.shape
     H_kv = k.shape[1]
@@ -272,7 +272,8 @@ def warmup_index(q, k, q_idx, k_idx, scale, kl_weight=1.0, rows=None, n_threads=
     kl = np.empty((G, R), np.float64)
     dq_idx = np.empty((R, G, d_I), np.float64)
     dk_idx = np.empty((N, d_I), np.float64) if rr is None else None
+    lse_idx = np.empty((G, R), np.float64)
     _check(_load().msa_ref_warmup_index(_p(q), _p(k), _p(q_idx), _p(k_idx), _p(rr), R, N, H_q, H_kv, d, d_I,
-                                        float(scale), float(kl_weight), _p(kl), _p(dq_idx), _p(dk_idx),
+                                        float(scale), float(kl_weight), _p(kl), _p(dq_idx), _p(dk_idx), _p(lse_idx),
                                         n_threads or threads()), "msa_ref_warmup_index")
-    return dict(kl=kl, dq_idx=dq_idx, dk_idx=dk_idx)
+    return dict(kl=kl, dq_idx=dq_idx, dk_idx=dk_idx, lse_idx=lse_idx)

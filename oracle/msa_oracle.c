@@ -879,6 +879,7 @@ typedef struct {
   int H_q, H_kv, d, d_I, chunks;
   double scale, kl_weight;
   double *kl, *dq_idx; /* [G, n_rows], [n_rows, G, d_I] */
+  double* lse_idx;     /* [G, n_rows] or NULL: the index branch's lse per row */
   double* dkI_acc;     /* [items][N][d_I] or NULL */
   int status;
 } warm_ctx;
@@ -923,6 +924,7 @@ static void warm_item(int64_t it, void* p) {
     double lI = 0.0;
     for (int64_t j = 0; j < n; ++j) lI += exp(z[j] - mI);
     const double lseI = mI + log(lI);
+    if (c->lse_idx) c->lse_idx[(int64_t)g * c->n_rows + ri] = lseI;
     double* dqI = c->dq_idx + (ri * c->H_kv + g) * dI;
     for (int x = 0; x < dI; ++x) dqI[x] = 0.0;
     double kl = 0.0;
@@ -946,11 +948,13 @@ static void warm_item(int64_t it, void* p) {
  * Warmup mode's index-branch loss and gradients.  rows == NULL: every
  * position (n_rows = N), and dk_idx [N, d_I] is written; otherwise only the
  * listed positions' kl [G, n_rows] and dq_idx [n_rows, G, d_I] (dk_idx may be
- * NULL).  q [N, H_q, d], K [N, H_kv, d], q_idx [N, G, d_I], k_idx [N, d_I].
+ * NULL).  lse_idx [G, n_rows] (nullable): each row's index log-sum-exp.
+ * q [N, H_q, d], K [N, H_kv, d], q_idx [N, G, d_I], k_idx [N, d_I].
  */
 int msa_ref_warmup_index(const uint16_t* q, const uint16_t* K, const uint16_t* q_idx, const uint16_t* k_idx,
                          const int64_t* rows, int64_t n_rows, int64_t N, int H_q, int H_kv, int d, int d_I,
-                         double scale, double kl_weight, double* kl, double* dq_idx, double* dk_idx, int n_threads) {
+                         double scale, double kl_weight, double* kl, double* dq_idx, double* dk_idx,
+                         double* lse_idx, int n_threads) {
   if (!q || !K || !q_idx || !k_idx || !kl || !dq_idx || N <= 0 || H_kv <= 0 || H_q % H_kv != 0 || d <= 0 ||
       d_I <= 0 || (!rows && (n_rows != N || !dk_idx)))
     return ORACLE_BAD_ARG;
@@ -965,7 +969,7 @@ int msa_ref_warmup_index(const uint16_t* q, const uint16_t* K, const uint16_t* q
   double* dkI_acc = want_dk ? (double*)calloc((size_t)(items * N * d_I), sizeof(double)) : NULL;
   if (want_dk && !dkI_acc) return ORACLE_NO_MEM;
   warm_ctx c = {q, K, q_idx, k_idx, rows, n_rows, N, H_q, H_kv, d, d_I, chunks, scale, kl_weight, kl, dq_idx,
-                dkI_acc, 0};
+                lse_idx, dkI_acc, 0};
   parallel_for(items, n_threads, warm_item, &c);
   if (want_dk) {
     for (int64_t j = 0; j < N; ++j)

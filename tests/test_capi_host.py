@@ -172,3 +172,18 @@ def test_varlen_cells_helper():
     from block_sparse_long_index_gb300.api import varlen_cells
     assert varlen_cells([1, 128, 129, 0, 300], 128) == [0, 128, 256, 512, 512, 896]
     assert varlen_cells([64], 64) == [0, 64]
+
+
+def test_warmup_validation(lib):
+    raw = lib.raw()
+    s = lib.shape(1000, 16, 2, 128, 128, 128, 16)
+    args = lambda scale: (FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), scale, FAKE, FAKE, FAKE, None)  # noqa: E731
+    assert raw.msa_warmup_fwd(*args(0.0)) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_warmup_fwd(None, *args(0.1)[1:]) == lib.MSA_ERR_INVALID_ARGUMENT
+    bad = lib.shape(1000, 24, 2, 128, 128, 128, 16)  # gs = 12
+    assert raw.msa_warmup_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(bad), 0.1, FAKE, FAKE, FAKE,
+                              None) == lib.MSA_ERR_UNSUPPORTED
+    assert raw.msa_warmup_index_grad(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, float("nan"), FAKE,
+                                     FAKE, FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
+    assert raw.msa_warmup_index_grad(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 1.0, FAKE,
+                                     ctypes.c_void_p((1 << 20) + 8), FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT

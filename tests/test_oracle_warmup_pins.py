@@ -98,3 +98,12 @@ def test_warmup_identities_and_rows():
     assert np.array_equal(part["dq_idx"], full["dq_idx"][rows])
     # row 0 sees only itself: both distributions are one-hot, KL = 0 and no gradient
     assert full["kl"][:, 0].max() == 0.0 and np.abs(full["dq_idx"][0]).max() == 0.0
+
+
+def test_warmup_lse_idx_is_the_index_logsumexp():
+    N, H_q, H_kv, d, d_I = 90, 4, 2, 8, 16
+    q, kk, q_idx, k_idx = make_case(N, H_q, H_kv, d, d_I, seed=5)
+    got = oracle.warmup_index(q, kk, q_idx, k_idx, 0.3, 1.0)["lse_idx"]
+    zI = torch.einsum("tgc,jc->gtj", torch.from_numpy(bf16_to_f64(q_idx)), torch.from_numpy(bf16_to_f64(k_idx)))
+    zI = (zI / math.sqrt(d_I)).masked_fill(~torch.ones(N, N, dtype=torch.bool).tril(), float("-inf"))
+    assert close(got, torch.logsumexp(zI, dim=-1).numpy(), 1e-12)
