@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 (E4M3) index-input variants")
     ap.add_argument("--no-varlen", action="store_true", help="skip the varlen (packed sequences) prefill")
+    ap.add_argument("--no-warmup", action="store_true", help="skip warmup mode (dense attention + index KL)")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
     ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode", "select_fp8",
                                                        "decode_fp8"],
@@ -450,6 +451,47 @@ def bench_decode(args, dist, torch):
     return res
 
 
+WARMUP_CFG = dict(N=32768, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16, needles=0, index=7)
+
+
+def bench_warmup(args, dist, torch):
+    """Warmup mode on the 128K prefill's head shapes at N = 32K: msa_warmup_fwd, then msa_warmup_index_grad."""
+    import datagen
+    from block_sparse_long_index_gb300 import msa
+    cfg = datagen.make_config("warmup_32k", **WARMUP_CFG)
+    inp = datagen.prefill_device(cfg)
+    N, G = cfg.N, cfg.G
+    shp = msa.shape(N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    f32 = lambda *s_: torch.empty(s_, dtype=torch.float32, device="cuda")  # noqa: E731
+    out = torch.empty((N, cfg.H_q, cfg.d), dtype=torch.bfloat16, device="cuda")
+    lse, lse_idx = f32(cfg.H_q, N), f32(G, N)
+    dq_idx, dk_idx, kl = f32(N, G, cfg.d_I), f32(N, cfg.d_I), f32(G, N)
+    scale = 1.0 / math.sqrt(cfg.d)
+    fwd = lambda: msa.msa_warmup_fwd(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], shp, scale, out,  # noqa
+                                     lse, lse_idx)
+    grad = lambda: msa.msa_warmup_index_grad(inp["q"], inp["k"], inp["q_idx"], inp["k_idx"], lse, lse_idx, shp,  # noqa
+                                             scale, 1.0, dq_idx, dk_idx, kl)
+    for _ in range(max(1, args.warmup)):
+        fwd()
+        grad()
+    torch.cuda.synchronize()
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    stream = torch.cuda.current_stream()
+    K = max(1, min(args.steps, 5))
+    tm = {}
+    for name, fn in (("fwd", fwd), ("grad", grad)):
+        a, b = E(), E()
+        a.record(stream)
+        for _ in range(K):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        tm[name] = a.elapsed_time(b) / K
+    del inp, out, lse, lse_idx, dq_idx, dk_idx, kl
+    torch.cuda.empty_cache()
+    return dict(cfg=cfg, fwd_ms=tm["fwd"], grad_ms=tm["grad"], steps=K)
+
+
 # --------------------------------------------------------------------------- the oracle (CPU) leg
 def oracle_prefill_sample(cfg, n_rows, seed=7):
     """Times the fp64 oracle (select + attention over every head) on n_rows sampled positions.
@@ -685,6 +727,27 @@ def main():
                                 "algorithmic": "sum_s(len_s^2/2)*G*d_I*2 = %.4g FLOP per launch" % flops_index_v,
                                 "peak_source": "%s bf16_tflops_sustained" % peak_src},
             "gpu_launches": (prefill_launches(cfg) + 1) * K}
+    if not args.no_warmup:
+        wu = bench_warmup(args, dist, torch)
+        wc = wu["cfg"]
+        f_ms, g_ms = dist.max(wu["fwd_ms"]), dist.max(wu["grad_ms"])
+        tri = wc.N * wc.N / 2.0
+        f_fl = tri * (4.0 * wc.H_q * wc.d + 2.0 * wc.G * wc.d_I)
+        g_fl = tri * (2.0 * wc.H_q * wc.d + 6.0 * wc.G * wc.d_I)
+        line["warmup"] = {
+            "metric": "warmup-mode tokens/s (dense main attention + index KL and its gradients, msa_warmup_fwd + "
+                      "msa_warmup_index_grad)",
+            "value": ws * wc.N / ((f_ms + g_ms) / 1000.0), "unit": "tokens/s", "ms_per_step": f_ms + g_ms,
+            "stages_ms": {"fwd": f_ms, "index_grad": g_ms}, "steps": wu["steps"],
+            "workload": workload_name(wc),
+            "roofline": {"bound": "tensor", "achieved": (f_fl + g_fl) / ((f_ms + g_ms) / 1000.0) / 1e12,
+                         "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": (f_fl + g_fl) / ((f_ms + g_ms) / 1000.0) / 1e12 / peak_t, "traffic": None,
+                         "algorithmic": "N^2/2 * (4 H_q d + 2 G d_I) forward + N^2/2 * (2 H_q d + 6 G d_I) index "
+                                        "gradient (teacher scores, index logits, dq^I, dk^I) = %.4g FLOP per step"
+                                        % (f_fl + g_fl),
+                         "peak_source": "%s bf16_tflops_sustained" % peak_src},
+            "gpu_launches": 3 * wu["steps"]}
     if not args.no_decode:
         dec = bench_decode(args, dist, torch)
         dcfg = dec["cfg"]

@@ -25,7 +25,8 @@
 //           and dk^I += dz^T Q^I, flushed once with fp32 reductions over the
 //           groups.
 // The dz tile: S recomputed for the 128 rows, P = exp(scale S - lse), the
-// teacher summed over each position's 8 rows by shuffles, the index logits
+// teacher summed over each position's 8 rows by a shuffle reduce-scatter (each
+// lane ends with 4 of the warp's 32 x 2 teacher entries), the index logits
 // through shared memory, dz (bf16) into shared memory.  K/V (or Q) tiles are
 // double-buffered with cp.async.
 #include <math.h>
@@ -69,7 +70,7 @@ __device__ __forceinline__ const uint16_t* q_row(const uint16_t* q, int64_t t0, 
 // [j0, j0+64) (Ks, kIs), for the warp's rows; lse_r[2]: the main lse of its
 // rows gq, gq+8 (-inf for padding rows); lseI_p[2]: lse^I of its positions
 // 2w, 2w+1.  Writes dz (bf16) of the 16 positions x 64 keys into dz_s and, with
-// KL, adds the KL terms of its positions to kl_acc (lanes with gq = 0).
+// KL, adds the KL terms of its positions to kl_acc (spread over the warp's lanes).
 template <int D, int DI, bool KL>
 __device__ __forceinline__ void dz_tile(uint32_t Qs, uint32_t qIs, uint32_t Ks, uint32_t kIs, float* zI_s,
                                         uint16_t* dz_s, int64_t t0, int64_t j0, int64_t N, float scale, float sI,
@@ -109,10 +110,9 @@ __device__ __forceinline__ void dz_tile(uint32_t Qs, uint32_t qIs, uint32_t Ks, 
       mma2(s[2 * np], s[2 * np + 1], a, b);
     }
   }
-  // P and the teacher: rows gq (position 2w) and gq + 8 (position 2w + 1), slot gq
+  // P for the warp's rows: gq (position 2w) and gq + 8 (position 2w + 1), slot gq
   const int64_t tp[2] = {t0 + 2 * warp, t0 + 2 * warp + 1};
-  const float inv_gs = 1.f / (float)gs;
-  float pb[8][4];
+  float v[32];  // v[4n + e]: n-tile n, accumulator element e
 #pragma unroll
   for (int n = 0; n < 8; ++n)
 #pragma unroll
@@ -120,30 +120,45 @@ __device__ __forceinline__ void dz_tile(uint32_t Qs, uint32_t qIs, uint32_t Ks, 
       const int ri = e >> 1;
       const int64_t j = j0 + 8 * n + 2 * tq + (e & 1);
       const bool ok = tp[ri] < N && j <= tp[ri] && gq < gs;
-      float v = ok ? __expf(fmaf(s[n][e], scale, -lse_r[ri])) : 0.f;
-      v += __shfl_xor_sync(0xffffffffu, v, 4);
-      v += __shfl_xor_sync(0xffffffffu, v, 8);
-      v += __shfl_xor_sync(0xffffffffu, v, 16);
-      pb[n][e] = v * inv_gs;
+      v[4 * n + e] = ok ? __expf(fmaf(s[n][e], scale, -lse_r[ri])) : 0.f;
     }
+  // The teacher sums each position's 8 slot rows, which sit in the 8 lanes of a
+  // tq column (lane bits 2-4).  A reduce-scatter over those bits (exchange half,
+  // keep half, three times) leaves lane gq with the full sums of n-tile
+  // nf = 4 (gq & 1) + 2 ((gq >> 1) & 1) + (gq >> 2), elements 0..3.
+  const int b0 = gq & 1, b1 = (gq >> 1) & 1, b2 = gq >> 2;
+  float r1[16], r2[8], pb[4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float keep = b0 ? v[16 + i] : v[i], send = b0 ? v[i] : v[16 + i];
+    r1[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float keep = b1 ? r1[8 + i] : r1[i], send = b1 ? r1[i] : r1[8 + i];
+    r2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const float inv_gs = 1.f / (float)gs;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b2 ? r2[4 + i] : r2[i], send = b2 ? r2[i] : r2[4 + i];
+    pb[i] = (keep + __shfl_xor_sync(0xffffffffu, send, 16)) * inv_gs;
+  }
+  const int nf = 4 * b0 + 2 * b1 + b2;
   __syncthreads();  // zI_s complete
-  // dz and KL on the lanes of slot 0 (every slot lane holds the same teacher)
-  if (gq == 0) {
+  // dz and KL of the lane's 4 teacher entries
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int ri = e >> 1, p = 2 * warp + ri, col = 8 * n + 2 * tq + (e & 1);
-        const int64_t j = j0 + col;
-        const bool ok = tp[ri] < N && j <= tp[ri];
-        float dz = 0.f;
-        if (ok) {
-          const float lp = zI_s[p * kWKeys + col] - lseI_p[ri];  // log pI
-          dz = w_kl * (__expf(lp) - pb[n][e]);
-          if (KL && pb[n][e] > 0.f) kl_acc[ri] += pb[n][e] * (__logf(pb[n][e]) - lp);
-        }
-        st_bf16(dz_s, p, col, kWKeys, dz);
-      }
+  for (int e = 0; e < 4; ++e) {
+    const int ri = e >> 1, p = 2 * warp + ri, col = 8 * nf + 2 * tq + (e & 1);
+    const int64_t j = j0 + col;
+    const bool ok = tp[ri] < N && j <= tp[ri];
+    float dz = 0.f;
+    if (ok) {
+      const float lp = zI_s[p * kWKeys + col] - lseI_p[ri];  // log pI
+      dz = w_kl * (__expf(lp) - pb[e]);
+      if (KL && pb[e] > 0.f) kl_acc[ri] += pb[e] * (__logf(pb[e]) - lp);
+    }
+    st_bf16(dz_s, p, col, kWKeys, dz);
   }
   __syncthreads();  // dz_s complete
 }
@@ -439,16 +454,14 @@ __global__ void __launch_bounds__(kWThreads, 1)
     }
     __syncthreads();
   }
-  // KL of positions 2w, 2w+1 (lanes of slot 0, reduced over tq)
-  if (gq == 0) {
+  // KL of positions 2w, 2w+1 (terms spread over all lanes of the warp)
 #pragma unroll
-    for (int ri = 0; ri < 2; ++ri) {
-      float x = kl_acc[ri];
-      x += __shfl_xor_sync(0x0000000fu, x, 1);
-      x += __shfl_xor_sync(0x0000000fu, x, 2);
-      const int64_t t = t0 + 2 * warp + ri;
-      if (tq == 0 && t < N) kl[(int64_t)g * N + t] = x;
-    }
+  for (int ri = 0; ri < 2; ++ri) {
+    float x = kl_acc[ri];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    const int64_t t = t0 + 2 * warp + ri;
+    if (lane == 0 && t < N) kl[(int64_t)g * N + t] = x;
   }
   if (16 * warp < DI) {
 #pragma unroll

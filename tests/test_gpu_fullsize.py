@@ -290,3 +290,41 @@ def test_decode_fp8_1m_full():
             for n in range(nd.m):
                 if mk[g] >> n & 1:
                     assert int(nd.blocks[b, g, n]) in set(gpu_blk[b, g].tolist())
+
+
+def test_warmup_32k_sampled():
+    """Warmup mode at N = 32K with the 128K prefill's head shapes: sampled rows of out, lse, lse^I, KL and dq^I
+    against the oracle's row mode, and over every key the identity sum_j dk^I_j = 0."""
+    from test_gpu_bwd import rel_report
+    from block_sparse_long_index_gb300 import msa
+    cfg = datagen.make_config("warmup_32k", N=32768, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16, needles=0,
+                              index=7)
+    N, G = cfg.N, cfg.G
+    dev = datagen.prefill_device(cfg)
+    shp = msa.shape(N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+    f32 = lambda *s_: torch.empty(s_, dtype=torch.float32, device="cuda")  # noqa: E731
+    out = torch.empty((N, cfg.H_q, cfg.d), dtype=torch.bfloat16, device="cuda")
+    lse, lse_idx = f32(cfg.H_q, N), f32(G, N)
+    dq_idx, dk_idx, kl = f32(N, G, cfg.d_I), f32(N, cfg.d_I), f32(G, N)
+    scale, w = 1.0 / math.sqrt(cfg.d), 1.0
+    msa.msa_warmup_fwd(dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"], shp, scale, out, lse, lse_idx)
+    msa.msa_warmup_index_grad(dev["q"], dev["k"], dev["q_idx"], dev["k_idx"], lse, lse_idx, shp, scale, w, dq_idx,
+                              dk_idx, kl)
+    torch.cuda.synchronize()
+    x = dk_idx.double()
+    assert float((x.sum(dim=0).abs() / x.pow(2).sum(dim=0).sqrt()).max()) < 2e-2
+    rows = datagen.sample_rows(N, 96, cfg.seed, must=(0, 1, 63, 64, N - 1))
+    rows_d = torch.from_numpy(rows).cuda()
+    host = datagen.prefill_host(cfg, rows=rows)
+    ref_o, ref_l = oracle.dense_attn(host["q"], host["k"], host["v"], rows, scale)
+    compare_attn(bf16_tensor_to_f64(out[rows_d]), lse[:, rows_d].T.cpu().numpy().astype(np.float64), ref_o, ref_l)
+    q_full = _scatter_rows(host["q"], rows, (N, cfg.H_q, cfg.d))
+    qi_full = _scatter_rows(host["q_idx"], rows, (N, G, cfg.d_I))
+    ref = oracle.warmup_index(q_full, host["k"], qi_full, host["k_idx"], scale, w, rows=rows)
+    lerr = np.abs(lse_idx[:, rows_d].cpu().numpy() - ref["lse_idx"])
+    assert float(lerr.max()) <= 2e-2 + 1e-2 * float(np.abs(ref["lse_idx"]).max())
+    reps = {nm: rel_report(g.cpu().numpy().astype(np.float64), ref[nm])
+            for nm, g in (("kl", kl[:, rows_d]), ("dq_idx", dq_idx[rows_d]))}
+    print("warmup_32k", reps)
+    for nm, r in reps.items():
+        assert r["ok"], (nm, r)
