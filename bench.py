@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--no-warmup", action="store_true", help="skip warmup mode (dense attention + index KL)")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
     ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode", "select_fp8",
-                                                       "decode_fp8"],
+                                                       "decode_fp8", "warmup"],
                     help="time one stage alone on --config (small-memory cases for profiler captures)")
     return ap.parse_args()
 
@@ -554,7 +554,21 @@ def run_stage(args):
     from block_sparse_long_index_gb300 import msa
     cfg = datagen.CONFIGS[args.config]
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    if args.stage in ("decode", "decode_fp8"):
+    if args.stage == "warmup":  # msa_warmup_fwd + msa_warmup_index_grad on the prefill config's shapes
+        inp = datagen.prefill_device(cfg)
+        N, G = cfg.N, cfg.G
+        shp = msa.shape(N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
+        f32 = lambda *s_: torch.empty(s_, dtype=torch.float32, device="cuda")  # noqa: E731
+        out = torch.empty((N, cfg.H_q, cfg.d), dtype=torch.bfloat16, device="cuda")
+        lse, lse_idx = f32(cfg.H_q, N), f32(G, N)
+        dq_idx, dk_idx, kl = f32(N, G, cfg.d_I), f32(N, cfg.d_I), f32(G, N)
+        sc = 1.0 / math.sqrt(cfg.d)
+
+        def call():
+            msa.msa_warmup_fwd(inp["q"], inp["k"], inp["v"], inp["q_idx"], inp["k_idx"], shp, sc, out, lse, lse_idx)
+            msa.msa_warmup_index_grad(inp["q"], inp["k"], inp["q_idx"], inp["k_idx"], lse, lse_idx, shp, sc, 1.0,
+                                      dq_idx, dk_idx, kl)
+    elif args.stage in ("decode", "decode_fp8"):
         from block_sparse_long_index_gb300 import MsaDecode
         inp = datagen.decode_device(cfg)
         run = MsaDecode(cfg.B, cfg.ctx, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)
