@@ -42,11 +42,14 @@ class MsaPrefill:
                              self.workspace, stream=stream)
         return self.block_idx
 
-    def attend(self, q, k, v, block_idx=None, scale=None, stream=None):
+    def attend(self, q, k, v, block_idx=None, scale=None, stream=None, out=None, lse=None):
+        """The attention stage; out / lse default to the object's own buffers."""
         scale = 1.0 / math.sqrt(self.d) if scale is None else scale
+        out = self.out if out is None else out
+        lse = self.lse if lse is None else lse
         _c.msa_sparse_attn_fwd(q, k, v, self.block_idx if block_idx is None else block_idx, self.shape, scale,
-                               self.out, self.lse, self.workspace, stream=stream)
-        return self.out, self.lse
+                               out, lse, self.workspace, stream=stream)
+        return out, lse
 
     def __call__(self, q, k, v, q_idx, k_idx, scale=None, stream=None):
         N, G = self.N, self.G
@@ -131,9 +134,11 @@ class PrefillHostPipeline:
     Three streams: host->device copies, compute, device->host copies.  Step i's
     inputs land in one of two device input sets while step i-1 computes on the
     other; its index inputs (q_idx, k_idx) are copied first so that the select
-    can start while q, k and v are still in flight; out and lse of step i are
-    copied back while step i+1 runs.  Every step still copies all of its inputs
-    in and all of its outputs (out, lse) out."""
+    can start while q, k and v are still in flight.  Step i's out and lse go to
+    one of two device output sets and are copied back while step i+1 computes
+    into the other, so the compute stream never waits for a device->host copy
+    of the step before.  Every step still copies all of its inputs in and all of
+    its outputs (out, lse) out."""
 
     NAMES = ("q_idx", "k_idx", "q", "k", "v")
 
@@ -141,6 +146,7 @@ class PrefillHostPipeline:
         self.run = run
         self.dev = [{n: torch.empty(_input_shape(run, n), dtype=torch.bfloat16, device=device) for n in self.NAMES}
                     for _ in range(2)]
+        self.outs = [(run.out, run.lse), (torch.empty_like(run.out), torch.empty_like(run.lse))]
         self.h2d, self.d2h = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
 
     def __call__(self, host_inputs, host_outputs, stream=None):
@@ -167,15 +173,16 @@ class PrefillHostPipeline:
             comp.wait_event(idx_in)
             self.run.select(dev["q_idx"], dev["k_idx"], stream=comp)
             comp.wait_event(qkv_in)
-            if i - 1 in d2h_done:  # out and lse of step i-1 are on the host before they are rewritten
-                comp.wait_event(d2h_done[i - 1])
-            self.run.attend(dev["q"], dev["k"], dev["v"], stream=comp)
+            if i - 2 in d2h_done:  # out and lse of step i-2 (this output set) are on the host
+                comp.wait_event(d2h_done[i - 2])
+            out, lse = self.outs[i % 2]
+            self.run.attend(dev["q"], dev["k"], dev["v"], stream=comp, out=out, lse=lse)
             attn_done[i] = E()
             attn_done[i].record(comp)
             with torch.cuda.stream(self.d2h):
                 self.d2h.wait_event(attn_done[i])
-                hout["out"].copy_(self.run.out, non_blocking=True)
-                hout["lse"].copy_(self.run.lse, non_blocking=True)
+                hout["out"].copy_(out, non_blocking=True)
+                hout["lse"].copy_(lse, non_blocking=True)
                 d2h_done[i] = E()
                 d2h_done[i].record(self.d2h)
         comp.wait_stream(self.h2d)
