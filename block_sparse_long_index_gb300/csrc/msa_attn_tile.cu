@@ -155,22 +155,6 @@ __device__ __forceinline__ bool soft_bar_and(bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-
-// Descriptor of an MN-major operand: 64-element (128 B) rows along N, 8-row
-// groups along K at 1024 B, successive 64-element N chunks `lbo` bytes apart.
-__device__ __forceinline__ uint64_t umma_desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1u << 46;
-  d |= (uint64_t)2u << 61;
-  return d;
-}
-
 // D (TMEM) += A (TMEM, 128 lanes x 16 bf16 packed in 8 columns) * B (shared memory).
 __device__ __forceinline__ void mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
                                             uint32_t accumulate) {

@@ -38,6 +38,7 @@
 #include <math.h>
 
 #include "msa_common.cuh"
+#include "msa_sm100.cuh"
 #include "msa_tiles.cuh"
 
 namespace msa {
@@ -693,11 +694,285 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
   return off;
 }
 
+
+// ------------------------------------------------------------------ main, on tcgen05 (d = Bk = 128)
+// The same tile work as bwd_main_kernel with every product on the 5th
+// generation tensor cores.  Shared-memory tiles (128 rows x 128 bf16 each)
+// are in the canonical 128B-swizzled K-major layout (two 64-column chunks of
+// 16 KB, 8-row groups 1 KB apart), so one tile serves as a K-major operand of
+// one product and an MN-major operand of another.  Per tile:
+//   S^T = K Q^T and dP^T = V dO^T (M = keys, N = rows, K = d) into TMEM
+//   columns 0-127 and 128-255;
+//   warps 0-3 (thread = key = TMEM lane) read both rows, form P^T and dZ^T
+//   = P^T (dP^T - D), write them (bf16) to shared memory as K-major tiles
+//   over the rows, and write the teacher (mean P over each position's slots);
+//   dV += P^T dO and dK += dZ^T Q (K = rows; dO, Q as MN-major B) accumulate
+//   in TMEM columns 256-383 and 384-511 over the tiles of a (group, block)
+//   run; dQ = dZ K (M = rows: dZ^T read as an MN-major A; K as MN-major B)
+//   into columns 0-127;
+//   warps 0-3 (thread = row) add dQ to dq, and at a run's end (thread = key)
+//   dK and dV to dk and dv, with fp32 vector reductions.
+// Warp 4 owns TMEM and its lane 0 issues the MMAs; all 8 warps load rows with
+// cp.async.  Phases are separated by CTA barriers and MMA completion
+// mbarriers; every wait is bounded.
+namespace tcb {
+constexpr int kChunk = 128 * 128;  // one 64-column chunk of a 128-row tile, bytes
+constexpr int kK = 0, kV = 2 * kChunk, kQ = 4 * kChunk, kDO = 6 * kChunk, kPT = 8 * kChunk, kZT = 10 * kChunk;
+constexpr int kBar = 12 * kChunk;
+constexpr int kBytes = 1024 + kBar + 64;
+constexpr uint32_t kIdescSS = sm100::idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescMnB = kIdescSS | (1u << 16);             // B MN-major
+constexpr uint32_t kIdescMnAB = kIdescSS | (1u << 15) | (1u << 16);  // A and B MN-major
+// byte offset of element (row r, column c) of a 128 x 128 bf16 tile
+__device__ __forceinline__ uint32_t off(int r, int c) {
+  return (uint32_t)((c >> 6) * kChunk + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
+                    ((c & 7) << 1));
+}
+// rows [0, 128) of a tile from src(r) (nullptr: zeros), 16-byte cp.async copies
+template <typename F>
+__device__ __forceinline__ void load_tile(uint8_t* base, const uint16_t* any, F src) {
+  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
+    const int r = i >> 4, c = (i & 15) * 8;
+    const uint16_t* gp = src(r);
+    cp_async_16(base + off(r, c), gp ? gp + c : any, gp ? 16 : 0);
+  }
+}
+__device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+}  // namespace tcb
+
+__global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
+    const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
+    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int H_q,
+    int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+    float* __restrict__ pbar_g, DeviceStatus* st) {
+  using namespace tcb;
+  constexpr int D = 128, BK = 128;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ float lse2_s[kRowsT], D_s[kRowsT];  // lse in log2 units, D
+  __shared__ int32_t trow_s[kRowsT];              // position of each tile row, -1 if none
+  __shared__ __align__(16) TileRecord rc_s;
+  const uint32_t bar_s = sb + kBar, bar_q = sb + kBar + 8, bar_drain = sb + kBar + 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
+  if (tid == 0) {
+    sm100::mbar_init(bar_s, 1);
+    sm100::mbar_init(bar_q, 1);
+    sm100::mbar_init(bar_drain, 1);
+    sm100::fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == 4) {
+    sm100::tmem_alloc(smem_u32(&tmem_slot), 512);
+    sm100::tc_fence_before();
+  }
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+  const float inv_gs = 1.f / (float)gs;
+  const int64_t kv_row = (int64_t)H_kv * D;
+  int64_t lo, hi;
+  tile_range(tile_off, n_gb, lo, hi);
+  int32_t cur_gb = -1, cur_g = 0, cur_b = 0;
+  uint32_t nt = 0;  // tiles done: the parity of both completion barriers
+  bool issued = false;
+  for (int64_t ti = lo; ti < hi; ++ti) {
+    copy_record(&rc_s, rec + ti);
+    __syncthreads();
+    const bool new_run = rc_s.gb != cur_gb;
+    const bool run_ends = ti + 1 >= hi || __ldg(&rec[ti + 1].gb) != rc_s.gb;
+    if (new_run) {
+      cur_gb = rc_s.gb;
+      cur_g = rc_s.g;
+      cur_b = rc_s.b;
+      load_tile(sm + kK, kc, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)cur_b * BK + r;
+        return j < N ? kc + j * kv_row + (int64_t)cur_g * D : nullptr;
+      });
+      load_tile(sm + kV, vc, [&](int r) -> const uint16_t* {
+        const int64_t j = (int64_t)cur_b * BK + r;
+        return j < N ? vc + j * kv_row + (int64_t)cur_g * D : nullptr;
+      });
+    }
+    const int g = rc_s.g;
+    load_tile(sm + kQ, q, [&](int r) -> const uint16_t* {
+      const int32_t t = row_t(rc_s, r, gs);
+      return t >= 0 ? q + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
+    });
+    load_tile(sm + kDO, dout, [&](int r) -> const uint16_t* {
+      const int32_t t = row_t(rc_s, r, gs);
+      return t >= 0 ? dout + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
+    });
+    if (tid < kRowsT) {
+      const int32_t t = row_t(rc_s, tid, gs);
+      const int64_t h = g * gs + (tid & 7);
+      trow_s[tid] = t;
+      lse2_s[tid] = t >= 0 ? lse[h * N + t] * 1.4426950408889634f : 0.f;
+      D_s[tid] = t >= 0 ? Dr[h * N + t] : 0.f;
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    sm100::fence_proxy_async_smem();
+    __syncthreads();
+    // ---- S^T and dP^T
+    if (warp == 4 && lane == 0) {
+      sm100::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int c = ks >> 2, kk = ks & 3;
+        sm100::mma_bf16_ss(tmem, sm100::umma_desc_kmajor(sb + kK + c * kChunk + kk * 32, 128),
+                           sm100::umma_desc_kmajor(sb + kQ + c * kChunk + kk * 32, 128), kIdescSS, ks > 0);
+        sm100::mma_bf16_ss(tmem + 128, sm100::umma_desc_kmajor(sb + kV + c * kChunk + kk * 32, 128),
+                           sm100::umma_desc_kmajor(sb + kDO + c * kChunk + kk * 32, 128), kIdescSS, ks > 0);
+      }
+      sm100::umma_commit(bar_s);
+      issued = true;
+    }
+    // ---- P^T, dZ^T and the teacher: thread = key; warpgroup `half` takes tile rows 64 half .. + 63
+    {
+      if (sm100::mbar_wait(bar_s, nt & 1, abort, st, 0x801)) {
+        sm100::tc_fence_after();
+        const int key = quad * 32 + lane;
+        const int64_t j = (int64_t)cur_b * BK + key;
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const float sl2 = scale * 1.4426950408889634f;  // exp(x) = 2^(x log2 e)
+        uint32_t sx[2][32], px[2][32];
+        sm100::tmem_ld_x32(tmem + lane_base + half * 64, sx[0]);
+        sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64, px[0]);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {  // 32 rows at a time, the next 32 in flight
+          const int cc = 2 * half + h2;
+          sm100::tmem_ld_wait();
+          sm100::reg_fence32(sx[h2]);
+          sm100::reg_fence32(px[h2]);
+          if (h2 == 0) {
+            sm100::tmem_ld_x32(tmem + lane_base + half * 64 + 32, sx[1]);
+            sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64 + 32, px[1]);
+          }
+          uint32_t pk[16], zk[16];
+          float tsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], zv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int r = cc * 32 + e + u;
+              const bool ok = j <= (int64_t)trow_s[r];  // -1 for rows without a position
+              const float p = ok ? sm100::ex2_approx(fmaf(__uint_as_float(sx[h2][e + u]), sl2, -lse2_s[r])) : 0.f;
+              pv[u] = p;
+              zv[u] = p * (__uint_as_float(px[h2][e + u]) - D_s[r]);
+            }
+            tsum[e >> 3] += pv[0] + pv[1];
+            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+            zk[e >> 1] = pack_bf16x2(zv[0], zv[1]);
+          }
+          if (pbar_g) {
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) pbar_g[(ti * kPosT + cc * 4 + pp) * BK + key] = tsum[pp] * inv_gs;
+          }
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte units: tile rows 32 cc + 8 q8 .. + 7
+            const uint32_t o = off(key, cc * 32 + q8 * 8);
+            *reinterpret_cast<uint4*>(sm + kPT + o) = make_uint4(pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
+            *reinterpret_cast<uint4*>(sm + kZT + o) = make_uint4(zk[4 * q8], zk[4 * q8 + 1], zk[4 * q8 + 2], zk[4 * q8 + 3]);
+          }
+        }
+        sm100::fence_proxy_async_smem();
+        sm100::tc_fence_before();
+      }
+    }
+    __syncthreads();
+    if (*abort) break;
+    // ---- dV, dK (accumulated over the run) and dQ
+    if (warp == 4 && lane == 0) {
+      sm100::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < kRowsT / 16; ++ks) {
+        const int c = ks >> 2, kk = ks & 3;
+        const uint32_t acc = (new_run && ks == 0) ? 0u : 1u;
+        sm100::mma_bf16_ss(tmem + 256, sm100::umma_desc_kmajor(sb + kPT + c * kChunk + kk * 32, 128),
+                           sm100::umma_desc_mnmajor_sw128(sb + kDO + ks * 16 * 128, kChunk), kIdescMnB, acc);
+        sm100::mma_bf16_ss(tmem + 384, sm100::umma_desc_kmajor(sb + kZT + c * kChunk + kk * 32, 128),
+                           sm100::umma_desc_mnmajor_sw128(sb + kQ + ks * 16 * 128, kChunk), kIdescMnB, acc);
+      }
+#pragma unroll
+      for (int ks = 0; ks < BK / 16; ++ks)
+        sm100::mma_bf16_ss(tmem, sm100::umma_desc_mnmajor_sw128(sb + kZT + ks * 16 * 128, kChunk),
+                           sm100::umma_desc_mnmajor_sw128(sb + kK + ks * 16 * 128, kChunk), kIdescMnAB, ks > 0);
+      sm100::umma_commit(bar_q);
+    }
+    {
+      if (sm100::mbar_wait(bar_q, nt & 1, abort, st, 0x802)) {
+        sm100::tc_fence_after();
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int r = quad * 32 + lane;  // dQ: thread = tile row, warpgroup `half` = d columns 64 half ..
+        const int32_t t = trow_s[r];
+#pragma unroll 1
+        for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
+          uint32_t x[32];
+          sm100::tmem_ld_x32(tmem + lane_base + cc * 32, x);
+          sm100::tmem_ld_wait();
+          if (t >= 0) {
+            float* p = dq + ((int64_t)t * H_q + g * gs + (r & 7)) * D + cc * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add4(p + e, scale * __uint_as_float(x[e]), scale * __uint_as_float(x[e + 1]),
+                       scale * __uint_as_float(x[e + 2]), scale * __uint_as_float(x[e + 3]));
+          }
+        }
+        if (run_ends) {  // thread = key: the run's dV and dK
+          const int64_t j = (int64_t)cur_b * BK + r;
+#pragma unroll 1
+          for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
+            uint32_t xv[32], xk[32];
+            sm100::tmem_ld_x32(tmem + lane_base + 256 + cc * 32, xv);
+            sm100::tmem_ld_x32(tmem + lane_base + 384 + cc * 32, xk);
+            sm100::tmem_ld_wait();
+            if (j < N) {
+              float* pv = dv + (j * H_kv + cur_g) * D + cc * 32;
+              float* pk2 = dk + (j * H_kv + cur_g) * D + cc * 32;
+#pragma unroll
+              for (int e = 0; e < 32; e += 4) {
+                red_add4(pv + e, __uint_as_float(xv[e]), __uint_as_float(xv[e + 1]), __uint_as_float(xv[e + 2]),
+                         __uint_as_float(xv[e + 3]));
+                red_add4(pk2 + e, scale * __uint_as_float(xk[e]), scale * __uint_as_float(xk[e + 1]),
+                         scale * __uint_as_float(xk[e + 2]), scale * __uint_as_float(xk[e + 3]));
+              }
+            }
+          }
+        }
+        sm100::tc_fence_before();
+      }
+    }
+    __syncthreads();
+    if (*abort) break;
+    ++nt;
+  }
+  __syncthreads();
+  if (warp == 4) {
+    if (lane == 0 && *abort && issued) {  // let the MMAs in flight finish before TMEM is released
+      sm100::umma_commit(bar_drain);
+      sm100::mbar_wait(bar_drain, 0, nullptr, st, 0x8F1);
+    }
+    __syncwarp();
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem, 512);
+  }
+}
+
 template <int D, int BK, int DI>
 cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
                          const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc,
                          int64_t N, int H_q, int H_kv, int k, float scale, float kl_weight, float* dq, float* dk,
-                         float* dv, float* dq_idx, float* dk_idx, float* kl, cudaStream_t s) {
+                         float* dv, float* dq_idx, float* dk_idx, float* kl, DeviceStatus* st, cudaStream_t s) {
   const int G = H_kv, gs = H_q / H_kv;
   const int64_t n_gb = (int64_t)G * sc.nb;
   const float sI = 1.f / sqrtf((float)DI);
@@ -708,12 +983,21 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
                                                                                       sc.nb, sc.lseI);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto km = bwd_main_kernel<D, BK>;
-  e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, MainSmem<D, BK>::BYTES);
-  if (e != cudaSuccess) return e;
-  km<<<grid, kThreadsB, MainSmem<D, BK>::BYTES, s>>>((const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v,
-                                                    (const uint16_t*)dout, lse, sc.Dr, sc.rec, sc.tile_off, n_gb, N,
-                                                    H_q, H_kv, gs, scale, dq, dk, dv, sc.pbar);
+  if constexpr (D == 128 && BK == 128) {
+    e = cudaFuncSetAttribute(bwd_main_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcb::kBytes);
+    if (e != cudaSuccess) return e;
+    bwd_main_tc_kernel<<<grid, kThreadsB, tcb::kBytes, s>>>((const uint16_t*)q, (const uint16_t*)kk,
+                                                            (const uint16_t*)v, (const uint16_t*)dout, lse, sc.Dr,
+                                                            sc.rec, sc.tile_off, n_gb, N, H_q, H_kv, gs, scale, dq,
+                                                            dk, dv, sc.pbar, st);
+  } else {
+    auto km = bwd_main_kernel<D, BK>;
+    e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, MainSmem<D, BK>::BYTES);
+    if (e != cudaSuccess) return e;
+    km<<<grid, kThreadsB, MainSmem<D, BK>::BYTES, s>>>((const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v,
+                                                      (const uint16_t*)dout, lse, sc.Dr, sc.rec, sc.tile_off, n_gb, N,
+                                                      H_q, H_kv, gs, scale, dq, dk, dv, sc.pbar);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto ki = bwd_index_kernel<BK, DI>;
@@ -729,15 +1013,15 @@ template <int D, int BK>
 cudaError_t launch_di(int d_I, const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
                       const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc, int64_t N,
                       int H_q, int H_kv, int k, float scale, float w, float* dq, float* dk, float* dv, float* dq_idx,
-                      float* dk_idx, float* kl, cudaStream_t s) {
+                      float* dk_idx, float* kl, DeviceStatus* st, cudaStream_t s) {
   if (d_I == 32)
     return launch_tiles<D, BK, 32>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
-                                   dk, dv, dq_idx, dk_idx, kl, s);
+                                   dk, dv, dq_idx, dk_idx, kl, st, s);
   if (d_I == 64)
     return launch_tiles<D, BK, 64>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
-                                   dk, dv, dq_idx, dk_idx, kl, s);
+                                   dk, dv, dq_idx, dk_idx, kl, st, s);
   return launch_tiles<D, BK, 128>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
-                                  dk, dv, dq_idx, dk_idx, kl, s);
+                                  dk, dv, dq_idx, dk_idx, kl, st, s);
 }
 
 }  // namespace
@@ -775,13 +1059,13 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (d == 64)
     return Bk == 64 ? launch_di<64, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
-                                        kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s)
+                                        kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s)
                     : launch_di<64, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
-                                         scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s);
+                                         scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s);
   return Bk == 64 ? launch_di<128, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
-                                       kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s)
+                                       kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s)
                   : launch_di<128, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
-                                        scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, s);
+                                        scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s);
 }
 
 }  // namespace msa
