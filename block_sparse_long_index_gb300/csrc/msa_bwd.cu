@@ -703,22 +703,27 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
 // one product and an MN-major operand of another.  Per tile:
 //   S^T = K Q^T and dP^T = V dO^T (M = keys, N = rows, K = d) into TMEM
 //   columns 0-127 and 128-255;
-//   warps 0-3 (thread = key = TMEM lane) read both rows, form P^T and dZ^T
-//   = P^T (dP^T - D), write them (bf16) to shared memory as K-major tiles
-//   over the rows, and write the teacher (mean P over each position's slots);
-//   dV += P^T dO and dK += dZ^T Q (K = rows; dO, Q as MN-major B) accumulate
-//   in TMEM columns 256-383 and 384-511 over the tiles of a (group, block)
-//   run; dQ = dZ K (M = rows: dZ^T read as an MN-major A; K as MN-major B)
-//   into columns 0-127;
-//   warps 0-3 (thread = row) add dQ to dq, and at a run's end (thread = key)
-//   dK and dV to dk and dv, with fp32 vector reductions.
-// Warp 4 owns TMEM and its lane 0 issues the MMAs; all 8 warps load rows with
-// cp.async.  Phases are separated by CTA barriers and MMA completion
-// mbarriers; every wait is bounded.
+//   both warpgroups (thread = key = TMEM lane; warpgroup h takes tile rows
+//   64h..64h+63) form P^T and dZ^T = P^T (dP^T - D), write P^T (bf16) back
+//   over the first half of their own S^T columns and dZ^T (bf16) to shared
+//   memory as a K-major tile over the rows, and write the teacher (mean P
+//   over each position's slots);
+//   dV += P^T dO (P^T read from TMEM) and dK += dZ^T Q (dO, Q as MN-major B)
+//   accumulate in TMEM columns 256-383 and 384-511 over the tiles of a
+//   (group, block) run; dQ = dZ K (M = rows: dZ^T read as an MN-major A; K
+//   as MN-major B) into columns 128-255 (dP^T is consumed by then; P^T in
+//   columns 0-127 stays untouched until the next tile's S^T);
+//   each thread adds 64 columns of its dQ row to dq, and at a run's end 64
+//   columns of its key's dK and dV to dk and dv, with fp32 vector reductions.
+// Q and dO rows are double-buffered: tile i+1's rows arrive by cp.async (and
+// its per-row position, lse and D into registers) while tile i computes.
+// Warp 4 owns TMEM and its lane 0 issues the MMAs.  Phases are separated by
+// CTA barriers and MMA completion mbarriers; every wait is bounded.
 namespace tcb {
 constexpr int kChunk = 128 * 128;  // one 64-column chunk of a 128-row tile, bytes
-constexpr int kK = 0, kV = 2 * kChunk, kQ = 4 * kChunk, kDO = 6 * kChunk, kPT = 8 * kChunk, kZT = 10 * kChunk;
-constexpr int kBar = 12 * kChunk;
+constexpr int kTile = 2 * kChunk;  // one 128 x 128 bf16 tile
+constexpr int kK = 0, kV = kTile, kQ = 2 * kTile, kDO = 4 * kTile, kZT = 6 * kTile;  // Q, dO: two buffers each
+constexpr int kBar = 7 * kTile;
 constexpr int kBytes = 1024 + kBar + 64;
 constexpr uint32_t kIdescSS = sm100::idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescMnB = kIdescSS | (1u << 16);             // B MN-major
@@ -741,6 +746,12 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// Position of row r of tile ti (16 positions x 8 head slots), or -1: no position, a slot past gs, or a
+// repeated block (marked in the record).
+__device__ __forceinline__ int32_t rec_row_t(const TileRecord* rec, int64_t ti, int r, int gs) {
+  const int p = r >> 3;
+  return ((r & 7) < gs && p < __ldg(&rec[ti].count)) ? __ldg(&rec[ti].t[p]) : -1;
+}
 }  // namespace tcb
 
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
@@ -758,7 +769,6 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   __shared__ int abort_flag;
   __shared__ float lse2_s[kRowsT], D_s[kRowsT];  // lse in log2 units, D
   __shared__ int32_t trow_s[kRowsT];              // position of each tile row, -1 if none
-  __shared__ __align__(16) TileRecord rc_s;
   const uint32_t bar_s = sb + kBar, bar_q = sb + kBar + 8, bar_drain = sb + kBar + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant, column half
@@ -778,21 +788,48 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
   const float inv_gs = 1.f / (float)gs;
+  const float kLog2e = 1.4426950408889634f;
   const int64_t kv_row = (int64_t)H_kv * D;
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
+  // rows of tile ti into Q/dO buffer b; row info (thread tid < 128 = row tid) into registers
+  int32_t nt_t = -1;
+  float nt_lse2 = 0.f, nt_D = 0.f;
+  auto issue_rows = [&](int64_t ti, int b) {
+    const int g = __ldg(&rec[ti].g);
+    load_tile(sm + kQ + b * kTile, q, [&](int r) -> const uint16_t* {
+      const int32_t t = rec_row_t(rec, ti, r, gs);
+      return t >= 0 ? q + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
+    });
+    load_tile(sm + kDO + b * kTile, dout, [&](int r) -> const uint16_t* {
+      const int32_t t = rec_row_t(rec, ti, r, gs);
+      return t >= 0 ? dout + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
+    });
+    if (tid < kRowsT) {
+      nt_t = rec_row_t(rec, ti, tid, gs);
+      const int64_t h = g * gs + (tid & 7);
+      nt_lse2 = nt_t >= 0 ? lse[h * N + nt_t] * kLog2e : 0.f;
+      nt_D = nt_t >= 0 ? Dr[h * N + nt_t] : 0.f;
+    }
+  };
+  if (lo < hi) issue_rows(lo, 0);
   int32_t cur_gb = -1, cur_g = 0, cur_b = 0;
   uint32_t nt = 0;  // tiles done: the parity of both completion barriers
   bool issued = false;
   for (int64_t ti = lo; ti < hi; ++ti) {
-    copy_record(&rc_s, rec + ti);
-    __syncthreads();
-    const bool new_run = rc_s.gb != cur_gb;
-    const bool run_ends = ti + 1 >= hi || __ldg(&rec[ti + 1].gb) != rc_s.gb;
+    const int buf = (int)((ti - lo) & 1);
+    const int32_t gb = __ldg(&rec[ti].gb);
+    const bool new_run = gb != cur_gb;
+    const bool run_ends = ti + 1 >= hi || __ldg(&rec[ti + 1].gb) != gb;
+    if (tid < kRowsT) {  // this tile's row info, fetched with its rows
+      trow_s[tid] = nt_t;
+      lse2_s[tid] = nt_lse2;
+      D_s[tid] = nt_D;
+    }
     if (new_run) {
-      cur_gb = rc_s.gb;
-      cur_g = rc_s.g;
-      cur_b = rc_s.b;
+      cur_gb = gb;
+      cur_g = __ldg(&rec[ti].g);
+      cur_b = __ldg(&rec[ti].b);
       load_tile(sm + kK, kc, [&](int r) -> const uint16_t* {
         const int64_t j = (int64_t)cur_b * BK + r;
         return j < N ? kc + j * kv_row + (int64_t)cur_g * D : nullptr;
@@ -802,26 +839,15 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
         return j < N ? vc + j * kv_row + (int64_t)cur_g * D : nullptr;
       });
     }
-    const int g = rc_s.g;
-    load_tile(sm + kQ, q, [&](int r) -> const uint16_t* {
-      const int32_t t = row_t(rc_s, r, gs);
-      return t >= 0 ? q + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
-    });
-    load_tile(sm + kDO, dout, [&](int r) -> const uint16_t* {
-      const int32_t t = row_t(rc_s, r, gs);
-      return t >= 0 ? dout + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
-    });
-    if (tid < kRowsT) {
-      const int32_t t = row_t(rc_s, tid, gs);
-      const int64_t h = g * gs + (tid & 7);
-      trow_s[tid] = t;
-      lse2_s[tid] = t >= 0 ? lse[h * N + t] * 1.4426950408889634f : 0.f;
-      D_s[tid] = t >= 0 ? Dr[h * N + t] : 0.f;
-    }
     cp_async_commit();
-    cp_async_wait<0>();
+    cp_async_wait<0>();  // this tile's rows (issued during the previous tile) and a new run's K/V
     sm100::fence_proxy_async_smem();
     __syncthreads();
+    // the next tile's rows stream in while this one computes (its buffer's last readers, the
+    // previous tile's MMAs, have completed)
+    if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
+    cp_async_commit();
+    const uint32_t qb = sb + kQ + buf * kTile, dob = sb + kDO + buf * kTile;
     // ---- S^T and dP^T
     if (warp == 4 && lane == 0) {
       sm100::tc_fence_after();
@@ -829,65 +855,66 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
       for (int ks = 0; ks < D / 16; ++ks) {
         const int c = ks >> 2, kk = ks & 3;
         sm100::mma_bf16_ss(tmem, sm100::umma_desc_kmajor(sb + kK + c * kChunk + kk * 32, 128),
-                           sm100::umma_desc_kmajor(sb + kQ + c * kChunk + kk * 32, 128), kIdescSS, ks > 0);
+                           sm100::umma_desc_kmajor(qb + c * kChunk + kk * 32, 128), kIdescSS, ks > 0);
         sm100::mma_bf16_ss(tmem + 128, sm100::umma_desc_kmajor(sb + kV + c * kChunk + kk * 32, 128),
-                           sm100::umma_desc_kmajor(sb + kDO + c * kChunk + kk * 32, 128), kIdescSS, ks > 0);
+                           sm100::umma_desc_kmajor(dob + c * kChunk + kk * 32, 128), kIdescSS, ks > 0);
       }
       sm100::umma_commit(bar_s);
       issued = true;
     }
-    // ---- P^T, dZ^T and the teacher: thread = key; warpgroup `half` takes tile rows 64 half .. + 63
-    {
-      if (sm100::mbar_wait(bar_s, nt & 1, abort, st, 0x801)) {
-        sm100::tc_fence_after();
-        const int key = quad * 32 + lane;
-        const int64_t j = (int64_t)cur_b * BK + key;
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const float sl2 = scale * 1.4426950408889634f;  // exp(x) = 2^(x log2 e)
-        uint32_t sx[2][32], px[2][32];
-        sm100::tmem_ld_x32(tmem + lane_base + half * 64, sx[0]);
-        sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64, px[0]);
+    // ---- P^T (to TMEM), dZ^T (to shared memory) and the teacher: thread = key
+    if (sm100::mbar_wait(bar_s, nt & 1, abort, st, 0x801)) {
+      sm100::tc_fence_after();
+      const int key = quad * 32 + lane;
+      const int64_t j = (int64_t)cur_b * BK + key;
+      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+      const float sl2 = scale * kLog2e;  // exp(x) = 2^(x log2 e)
+      uint32_t sx[2][32], px[2][32];
+      sm100::tmem_ld_x32(tmem + lane_base + half * 64, sx[0]);
+      sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64, px[0]);
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {  // 32 rows at a time, the next 32 in flight
-          const int cc = 2 * half + h2;
-          sm100::tmem_ld_wait();
-          sm100::reg_fence32(sx[h2]);
-          sm100::reg_fence32(px[h2]);
-          if (h2 == 0) {
-            sm100::tmem_ld_x32(tmem + lane_base + half * 64 + 32, sx[1]);
-            sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64 + 32, px[1]);
-          }
-          uint32_t pk[16], zk[16];
-          float tsum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], zv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int r = cc * 32 + e + u;
-              const bool ok = j <= (int64_t)trow_s[r];  // -1 for rows without a position
-              const float p = ok ? sm100::ex2_approx(fmaf(__uint_as_float(sx[h2][e + u]), sl2, -lse2_s[r])) : 0.f;
-              pv[u] = p;
-              zv[u] = p * (__uint_as_float(px[h2][e + u]) - D_s[r]);
-            }
-            tsum[e >> 3] += pv[0] + pv[1];
-            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-            zk[e >> 1] = pack_bf16x2(zv[0], zv[1]);
-          }
-          if (pbar_g) {
-#pragma unroll
-            for (int pp = 0; pp < 4; ++pp) pbar_g[(ti * kPosT + cc * 4 + pp) * BK + key] = tsum[pp] * inv_gs;
-          }
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte units: tile rows 32 cc + 8 q8 .. + 7
-            const uint32_t o = off(key, cc * 32 + q8 * 8);
-            *reinterpret_cast<uint4*>(sm + kPT + o) = make_uint4(pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
-            *reinterpret_cast<uint4*>(sm + kZT + o) = make_uint4(zk[4 * q8], zk[4 * q8 + 1], zk[4 * q8 + 2], zk[4 * q8 + 3]);
-          }
+      for (int h2 = 0; h2 < 2; ++h2) {  // 32 rows at a time, the next 32 in flight
+        const int cc = 2 * half + h2;
+        sm100::tmem_ld_wait();
+        sm100::reg_fence32(sx[h2]);
+        sm100::reg_fence32(px[h2]);
+        if (h2 == 0) {
+          sm100::tmem_ld_x32(tmem + lane_base + half * 64 + 32, sx[1]);
+          sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64 + 32, px[1]);
         }
-        sm100::fence_proxy_async_smem();
-        sm100::tc_fence_before();
+        uint32_t pk[16], zk[16];
+        float tsum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2], zv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int r = cc * 32 + e + u;
+            const bool ok = j <= (int64_t)trow_s[r];  // -1 for rows without a position
+            const float p = ok ? sm100::ex2_approx(fmaf(__uint_as_float(sx[h2][e + u]), sl2, -lse2_s[r])) : 0.f;
+            pv[u] = p;
+            zv[u] = p * (__uint_as_float(px[h2][e + u]) - D_s[r]);
+          }
+          tsum[e >> 3] += pv[0] + pv[1];
+          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+          zk[e >> 1] = pack_bf16x2(zv[0], zv[1]);
+        }
+        if (pbar_g) {
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) pbar_g[(ti * kPosT + cc * 4 + pp) * BK + key] = tsum[pp] * inv_gs;
+        }
+        // P^T rows 32 cc .. +31 -> packed columns 64 half + 16 h2 .. + 15 (within this warpgroup's S^T
+        // columns, all already read)
+        sm100::tmem_st_x16(tmem + lane_base + half * 64 + h2 * 16, pk);
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {  // 16-byte units: tile rows 32 cc + 8 q8 .. + 7
+          const uint32_t o = off(key, cc * 32 + q8 * 8);
+          *reinterpret_cast<uint4*>(sm + kZT + o) = make_uint4(zk[4 * q8], zk[4 * q8 + 1], zk[4 * q8 + 2], zk[4 * q8 + 3]);
+        }
       }
+      sm100::tmem_st_wait();
+      sm100::fence_proxy_async_smem();
+      sm100::tc_fence_before();
     }
     __syncthreads();
     if (*abort) break;
@@ -898,64 +925,64 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
       for (int ks = 0; ks < kRowsT / 16; ++ks) {
         const int c = ks >> 2, kk = ks & 3;
         const uint32_t acc = (new_run && ks == 0) ? 0u : 1u;
-        sm100::mma_bf16_ss(tmem + 256, sm100::umma_desc_kmajor(sb + kPT + c * kChunk + kk * 32, 128),
-                           sm100::umma_desc_mnmajor_sw128(sb + kDO + ks * 16 * 128, kChunk), kIdescMnB, acc);
+        // P^T rows 16 ks .. : half h = ks / 4 holds them packed at columns 64 h + 8 (ks % 4)
+        sm100::mma_bf16_ts(tmem + 256, tmem + (uint32_t)(64 * c + 8 * kk),
+                           sm100::umma_desc_mnmajor_sw128(dob + ks * 16 * 128, kChunk), kIdescMnB, acc);
         sm100::mma_bf16_ss(tmem + 384, sm100::umma_desc_kmajor(sb + kZT + c * kChunk + kk * 32, 128),
-                           sm100::umma_desc_mnmajor_sw128(sb + kQ + ks * 16 * 128, kChunk), kIdescMnB, acc);
+                           sm100::umma_desc_mnmajor_sw128(qb + ks * 16 * 128, kChunk), kIdescMnB, acc);
       }
 #pragma unroll
       for (int ks = 0; ks < BK / 16; ++ks)
-        sm100::mma_bf16_ss(tmem, sm100::umma_desc_mnmajor_sw128(sb + kZT + ks * 16 * 128, kChunk),
+        sm100::mma_bf16_ss(tmem + 128, sm100::umma_desc_mnmajor_sw128(sb + kZT + ks * 16 * 128, kChunk),
                            sm100::umma_desc_mnmajor_sw128(sb + kK + ks * 16 * 128, kChunk), kIdescMnAB, ks > 0);
       sm100::umma_commit(bar_q);
     }
-    {
-      if (sm100::mbar_wait(bar_q, nt & 1, abort, st, 0x802)) {
-        sm100::tc_fence_after();
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int r = quad * 32 + lane;  // dQ: thread = tile row, warpgroup `half` = d columns 64 half ..
-        const int32_t t = trow_s[r];
+    if (sm100::mbar_wait(bar_q, nt & 1, abort, st, 0x802)) {
+      sm100::tc_fence_after();
+      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+      const int r = quad * 32 + lane;  // dQ: thread = tile row, warpgroup `half` = d columns 64 half ..
+      const int32_t t = trow_s[r];
+#pragma unroll 1
+      for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
+        uint32_t x[32];
+        sm100::tmem_ld_x32(tmem + lane_base + 128 + cc * 32, x);
+        sm100::tmem_ld_wait();
+        if (t >= 0) {
+          float* p = dq + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D + cc * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            red_add4(p + e, scale * __uint_as_float(x[e]), scale * __uint_as_float(x[e + 1]),
+                     scale * __uint_as_float(x[e + 2]), scale * __uint_as_float(x[e + 3]));
+        }
+      }
+      if (run_ends) {  // thread = key: the run's dV and dK
+        const int64_t j = (int64_t)cur_b * BK + r;
 #pragma unroll 1
         for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
-          uint32_t x[32];
-          sm100::tmem_ld_x32(tmem + lane_base + cc * 32, x);
+          uint32_t xv[32], xk[32];
+          sm100::tmem_ld_x32(tmem + lane_base + 256 + cc * 32, xv);
+          sm100::tmem_ld_x32(tmem + lane_base + 384 + cc * 32, xk);
           sm100::tmem_ld_wait();
-          if (t >= 0) {
-            float* p = dq + ((int64_t)t * H_q + g * gs + (r & 7)) * D + cc * 32;
+          if (j < N) {
+            float* pv = dv + (j * H_kv + cur_g) * D + cc * 32;
+            float* pk2 = dk + (j * H_kv + cur_g) * D + cc * 32;
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add4(p + e, scale * __uint_as_float(x[e]), scale * __uint_as_float(x[e + 1]),
-                       scale * __uint_as_float(x[e + 2]), scale * __uint_as_float(x[e + 3]));
-          }
-        }
-        if (run_ends) {  // thread = key: the run's dV and dK
-          const int64_t j = (int64_t)cur_b * BK + r;
-#pragma unroll 1
-          for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
-            uint32_t xv[32], xk[32];
-            sm100::tmem_ld_x32(tmem + lane_base + 256 + cc * 32, xv);
-            sm100::tmem_ld_x32(tmem + lane_base + 384 + cc * 32, xk);
-            sm100::tmem_ld_wait();
-            if (j < N) {
-              float* pv = dv + (j * H_kv + cur_g) * D + cc * 32;
-              float* pk2 = dk + (j * H_kv + cur_g) * D + cc * 32;
-#pragma unroll
-              for (int e = 0; e < 32; e += 4) {
-                red_add4(pv + e, __uint_as_float(xv[e]), __uint_as_float(xv[e + 1]), __uint_as_float(xv[e + 2]),
-                         __uint_as_float(xv[e + 3]));
-                red_add4(pk2 + e, scale * __uint_as_float(xk[e]), scale * __uint_as_float(xk[e + 1]),
-                         scale * __uint_as_float(xk[e + 2]), scale * __uint_as_float(xk[e + 3]));
-              }
+            for (int e = 0; e < 32; e += 4) {
+              red_add4(pv + e, __uint_as_float(xv[e]), __uint_as_float(xv[e + 1]), __uint_as_float(xv[e + 2]),
+                       __uint_as_float(xv[e + 3]));
+              red_add4(pk2 + e, scale * __uint_as_float(xk[e]), scale * __uint_as_float(xk[e + 1]),
+                       scale * __uint_as_float(xk[e + 2]), scale * __uint_as_float(xk[e + 3]));
             }
           }
         }
-        sm100::tc_fence_before();
       }
+      sm100::tc_fence_before();
     }
     __syncthreads();
     if (*abort) break;
     ++nt;
   }
+  cp_async_wait<0>();  // no copy of ours is left in flight when the CTA exits
   __syncthreads();
   if (warp == 4) {
     if (lane == 0 && *abort && issued) {  // let the MMAs in flight finish before TMEM is released
@@ -968,6 +995,335 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   }
 }
 
+// ------------------------------------------------------------------ index branch, on tcgen05 (Bk = d_I = 128)
+// Both index-branch passes over chunks of up to 8 consecutive tiles of one
+// (group, block) run: 128 positions, one per thread and TMEM lane (row r =
+// 16 i + p is position p of the chunk's tile i; rows past the chunk are
+// zero).  The index queries and the block's index keys are 128 x 128 bf16
+// tiles in the 128B-swizzled K-major layout of the main kernel.
+//   lse pass:  Z = Q^I K^I^T (M = positions, N = keys) into TMEM; each thread
+//              reduces its row to one (max, sum of exp) per (t, slot);
+//   gradient:  the same Z; each thread forms dzI = w (pI - pbar) of its row
+//              and the row's KL terms, writes dzI (bf16) to shared memory;
+//              dq^I = dzI K^I (K^I as MN-major B) over the Z columns, and
+//              dk^I += dzI^T Q^I (dzI and Q^I read MN-major) accumulated in
+//              TMEM columns 128-255 over the run's chunks, flushed with fp32
+//              reductions at the run's end.
+// The lse pass needs 128 TMEM columns and 64 KB of shared memory (three CTAs
+// per SM), the gradient pass 256 columns and 96 KB (two CTAs per SM); the
+// CTAs of an SM overlap one another's loads and arithmetic.
+namespace tci {
+constexpr int kThreads = 128;
+constexpr int kChunkTiles = 8;
+constexpr int kKI = 0, kQI = tcb::kTile, kDZ = 2 * tcb::kTile;
+constexpr int kLseBar = 2 * tcb::kTile, kLseBytes = 1024 + kLseBar + 64;
+constexpr int kGradBar = 3 * tcb::kTile, kGradBytes = 1024 + kGradBar + 64;
+constexpr uint32_t kIdescSS = tcb::kIdescSS, kIdescMnB = tcb::kIdescMnB, kIdescMnAB = tcb::kIdescMnAB;
+
+// The chunk starting at tile ti0 (< hi): its tile count and whether its run ends with it (in this range).
+__device__ __forceinline__ int chunk_tiles(const TileRecord* rec, int64_t ti0, int64_t hi, int32_t gb,
+                                           bool& run_ends) {
+  int n = 1;
+  while (n < kChunkTiles && ti0 + n < hi && __ldg(&rec[ti0 + n].gb) == gb) ++n;
+  run_ends = ti0 + n >= hi || __ldg(&rec[ti0 + n].gb) != gb;
+  return n;
+}
+// Position of row r of a chunk of n tiles from ti0, or -1 (no position, or a repeated block).
+__device__ __forceinline__ int32_t chunk_row_t(const TileRecord* rec, int64_t ti0, int n, int r) {
+  const int i = r >> 4, p = r & 15;
+  return (i < n && p < __ldg(&rec[ti0 + i].count)) ? __ldg(&rec[ti0 + i].t[p]) : -1;
+}
+// Z = Q^I K^I^T: 8 steps over d_I.
+__device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t sb) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const int c = ks >> 2, kk = ks & 3;
+    sm100::mma_bf16_ss(tmem, sm100::umma_desc_kmajor(sb + kQI + c * tcb::kChunk + kk * 32, 128),
+                       sm100::umma_desc_kmajor(sb + kKI + c * tcb::kChunk + kk * 32, 128), kIdescSS, ks > 0);
+  }
+}
+// The run's index keys (new run) and the chunk's index queries into shared memory.
+__device__ __forceinline__ void load_chunk(uint8_t* sm, const uint16_t* q_idx, const uint16_t* k_idx,
+                                           const TileRecord* rec, int64_t ti0, int n, bool new_run, int g, int b,
+                                           int G, int64_t N) {
+  if (new_run)
+    tcb::load_tile(sm + kKI, k_idx, [&](int r) -> const uint16_t* {
+      const int64_t j = (int64_t)b * 128 + r;
+      return j < N ? k_idx + j * 128 : nullptr;
+    });
+  tcb::load_tile(sm + kQI, q_idx, [&](int r) -> const uint16_t* {
+    const int32_t t = chunk_row_t(rec, ti0, n, r);
+    return t >= 0 ? q_idx + ((int64_t)t * G + g) * 128 : nullptr;
+  });
+  cp_async_commit();
+  cp_async_wait<0>();
+  sm100::fence_proxy_async_smem();
+}
+}  // namespace tci
+
+__global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
+    const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const TileRecord* __restrict__ rec,
+    const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int G, int k, float sI,
+    float2* __restrict__ part, DeviceStatus* st) {
+  using namespace tci;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const uint32_t bar = sb + kLseBar, bar_drain = sb + kLseBar + 8;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    sm100::mbar_init(bar, 1);
+    sm100::mbar_init(bar_drain, 1);
+    sm100::fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    sm100::tmem_alloc(smem_u32(&tmem_slot), 128);
+    sm100::tc_fence_before();
+  }
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+  const float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+  const float s2 = sI * kLog2e;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  int64_t lo, hi;
+  tile_range(tile_off, n_gb, lo, hi);
+  int32_t cur_gb = -1;
+  uint32_t phase = 0;
+  bool issued = false;
+  for (int64_t ti0 = lo; ti0 < hi;) {
+    const int32_t gb = __ldg(&rec[ti0].gb);
+    bool run_ends;
+    const int n = chunk_tiles(rec, ti0, hi, gb, run_ends);
+    const int g = __ldg(&rec[ti0].g), b = __ldg(&rec[ti0].b);
+    load_chunk(sm, q_idx, k_idx, rec, ti0, n, gb != cur_gb, g, b, G, N);
+    cur_gb = gb;
+    const int32_t t = chunk_row_t(rec, ti0, n, tid);
+    const int slot = (t >= 0) ? (int)__ldg(&rec[ti0 + (tid >> 4)].slot[tid & 15]) : 0;
+    __syncthreads();
+    if (tid == 0) {
+      sm100::tc_fence_after();
+      issue_logits(tmem, sb);
+      sm100::umma_commit(bar);
+      issued = true;
+    }
+    if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x803)) {
+      sm100::tc_fence_after();
+      const int64_t lim = (int64_t)t - (int64_t)b * 128;  // keys c <= lim are visible to this row
+      float m = -INFINITY, l = 0.f;  // base-2 units
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        uint32_t x[32];
+        sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x);
+        sm100::tmem_ld_wait();
+        float cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float y = (c32 * 32 + e <= lim) ? __uint_as_float(x[e]) * s2 : -INFINITY;
+          x[e] = __float_as_uint(y);
+          cm = fmaxf(cm, y);
+        }
+        if (cm > -INFINITY) {
+          const float mn = fmaxf(m, cm);
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) acc += sm100::ex2_approx(__uint_as_float(x[e]) - mn);
+          l = l * sm100::ex2_approx(m - mn) + acc;
+          m = mn;
+        }
+      }
+      if (t >= 0) part[((int64_t)g * N + t) * k + slot] = make_float2(m > -INFINITY ? m * kLn2 : -INFINITY, l);
+      sm100::tc_fence_before();
+    }
+    ++phase;
+    __syncthreads();
+    if (*abort) break;
+    ti0 += n;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (warp == 0) {
+    if ((tid & 31) == 0 && *abort && issued) {
+      sm100::umma_commit(bar_drain);
+      sm100::mbar_wait(bar_drain, 0, nullptr, st, 0x8F2);
+    }
+    __syncwarp();
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem, 128);
+  }
+}
+
+__global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
+    const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const float* __restrict__ lseI,
+    const float* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
+    int64_t n_gb, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
+    float* __restrict__ kl, DeviceStatus* st) {
+  using namespace tci;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const uint32_t bar = sb + kGradBar, bar_drain = sb + kGradBar + 8;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    sm100::mbar_init(bar, 1);
+    sm100::mbar_init(bar_drain, 1);
+    sm100::fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    sm100::tmem_alloc(smem_u32(&tmem_slot), 256);
+    sm100::tc_fence_before();
+  }
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+  const float kLog2e = 1.4426950408889634f;
+  const float s2 = sI * kLog2e;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  int64_t lo, hi;
+  tile_range(tile_off, n_gb, lo, hi);
+  int32_t cur_gb = -1;
+  uint32_t phase = 0;
+  bool issued = false;
+  for (int64_t ti0 = lo; ti0 < hi;) {
+    const int32_t gb = __ldg(&rec[ti0].gb);
+    bool run_ends;
+    const int n = chunk_tiles(rec, ti0, hi, gb, run_ends);
+    const int g = __ldg(&rec[ti0].g), b = __ldg(&rec[ti0].b);
+    const bool new_run = gb != cur_gb;
+    load_chunk(sm, q_idx, k_idx, rec, ti0, n, new_run, g, b, G, N);
+    cur_gb = gb;
+    const int32_t t = chunk_row_t(rec, ti0, n, tid);
+    const float l2 = t >= 0 ? __ldg(&lseI[(int64_t)g * N + t]) * kLog2e : INFINITY;
+    // this row's teacher: the main kernel's row (tile ti0 + i, position p), 128 keys
+    const float4* pb4 = reinterpret_cast<const float4*>(pbar_g + ((ti0 + (tid >> 4)) * kPosT + (tid & 15)) * 128);
+    __syncthreads();
+    if (tid == 0) {
+      sm100::tc_fence_after();
+      issue_logits(tmem, sb);
+      sm100::umma_commit(bar);
+      issued = true;
+    }
+    if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x804)) {
+      sm100::tc_fence_after();
+      const int64_t lim = (int64_t)t - (int64_t)b * 128;  // keys c <= lim are visible (none when t < 0)
+      float klsum = 0.f;
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {
+        uint32_t x[32];
+        float pb[32];
+        sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x);
+        if (t >= 0) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float4 v = __ldg(pb4 + c32 * 8 + e);
+            pb[4 * e] = v.x, pb[4 * e + 1] = v.y, pb[4 * e + 2] = v.z, pb[4 * e + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) pb[e] = 0.f;
+        }
+        sm100::tmem_ld_wait();
+        uint32_t zk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float dz[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const bool ok = c32 * 32 + e + u <= lim;
+            const float y = fmaf(__uint_as_float(x[e + u]), s2, -l2);  // log2 pI
+            const float p = pb[e + u];
+            dz[u] = ok ? w * (sm100::ex2_approx(y) - p) : 0.f;
+            if (ok && p > 0.f) klsum += p * (__logf(p) - y * 0.6931471805599453f);
+          }
+          zk[e >> 1] = pack_bf16x2(dz[0], dz[1]);
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {
+          const uint32_t o = tcb::off(tid, c32 * 32 + q8 * 8);
+          *reinterpret_cast<uint4*>(sm + kDZ + o) = make_uint4(zk[4 * q8], zk[4 * q8 + 1], zk[4 * q8 + 2], zk[4 * q8 + 3]);
+        }
+      }
+      if (kl && t >= 0) atomicAdd(kl + (int64_t)g * N + t, klsum);
+      sm100::fence_proxy_async_smem();
+      sm100::tc_fence_before();
+    }
+    ++phase;
+    __syncthreads();
+    if (*abort) break;
+    if (tid == 0) {
+      sm100::tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {  // dq^I = dzI K^I over the keys
+        const int c = ks >> 2, kk = ks & 3;
+        sm100::mma_bf16_ss(tmem, sm100::umma_desc_kmajor(sb + kDZ + c * tcb::kChunk + kk * 32, 128),
+                           sm100::umma_desc_mnmajor_sw128(sb + kKI + ks * 16 * 128, tcb::kChunk), kIdescMnB, ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)  // dk^I += dzI^T Q^I over the positions
+        sm100::mma_bf16_ss(tmem + 128, sm100::umma_desc_mnmajor_sw128(sb + kDZ + ks * 16 * 128, tcb::kChunk),
+                           sm100::umma_desc_mnmajor_sw128(sb + kQI + ks * 16 * 128, tcb::kChunk), kIdescMnAB,
+                           (new_run && ks == 0) ? 0u : 1u);
+      sm100::umma_commit(bar);
+    }
+    if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x805)) {
+      sm100::tc_fence_after();
+#pragma unroll 1
+      for (int c32 = 0; c32 < 4; ++c32) {  // thread = position: its dq^I row
+        uint32_t x[32];
+        sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x);
+        sm100::tmem_ld_wait();
+        if (t >= 0) {
+          float* pq = dq_idx + ((int64_t)t * G + g) * 128 + c32 * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            tcb::red_add4(pq + e, sI * __uint_as_float(x[e]), sI * __uint_as_float(x[e + 1]),
+                          sI * __uint_as_float(x[e + 2]), sI * __uint_as_float(x[e + 3]));
+        }
+      }
+      if (run_ends) {  // thread = key: the run's dk^I
+        const int64_t j = (int64_t)b * 128 + tid;
+#pragma unroll 1
+        for (int c32 = 0; c32 < 4; ++c32) {
+          uint32_t x[32];
+          sm100::tmem_ld_x32(tmem + lane_base + 128 + c32 * 32, x);
+          sm100::tmem_ld_wait();
+          if (j < N) {
+            float* pk = dk_idx + j * 128 + c32 * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              tcb::red_add4(pk + e, sI * __uint_as_float(x[e]), sI * __uint_as_float(x[e + 1]),
+                            sI * __uint_as_float(x[e + 2]), sI * __uint_as_float(x[e + 3]));
+          }
+        }
+      }
+      sm100::tc_fence_before();
+    }
+    ++phase;
+    __syncthreads();
+    if (*abort) break;
+    ti0 += n;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (warp == 0) {
+    if ((tid & 31) == 0 && *abort && issued) {
+      sm100::umma_commit(bar_drain);
+      sm100::mbar_wait(bar_drain, 0, nullptr, st, 0x8F3);
+    }
+    __syncwarp();
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem, 256);
+  }
+}
+
 template <int D, int BK, int DI>
 cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
                          const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc,
@@ -977,8 +1333,17 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
   const int64_t n_gb = (int64_t)G * sc.nb;
   const float sI = 1.f / sqrtf((float)DI);
   const int grid = num_sms();
-  bwd_index_lse_kernel<BK, DI><<<grid, kThreadsB, 0, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec,
-                                                          sc.tile_off, n_gb, N, G, k, sI, sc.partI);
+  constexpr bool kIndexTc = BK == 128 && DI == 128;
+  if constexpr (kIndexTc) {
+    cudaError_t e0 = cudaFuncSetAttribute(bwd_index_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          tci::kLseBytes);
+    if (e0 != cudaSuccess) return e0;
+    bwd_index_lse_tc_kernel<<<3 * grid, tci::kThreads, tci::kLseBytes, s>>>(
+        (const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec, sc.tile_off, n_gb, N, G, k, sI, sc.partI, st);
+  } else {
+    bwd_index_lse_kernel<BK, DI><<<grid, kThreadsB, 0, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec,
+                                                            sc.tile_off, n_gb, N, G, k, sI, sc.partI);
+  }
   bwd_index_lse_combine_kernel<<<(unsigned)ceil_div((int64_t)G * N, 256), 256, 0, s>>>(sc.partI, block_idx, N, G, k,
                                                                                       sc.nb, sc.lseI);
   cudaError_t e = cudaGetLastError();
@@ -1000,6 +1365,14 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if constexpr (kIndexTc) {
+    e = cudaFuncSetAttribute(bwd_index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tci::kGradBytes);
+    if (e != cudaSuccess) return e;
+    bwd_index_tc_kernel<<<2 * grid, tci::kThreads, tci::kGradBytes, s>>>(
+        (const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.lseI, sc.pbar, sc.rec, sc.tile_off, n_gb, N, G, sI,
+        kl_weight, dq_idx, dk_idx, kl, st);
+    return cudaGetLastError();
+  }
   auto ki = bwd_index_kernel<BK, DI>;
   e = cudaFuncSetAttribute(ki, cudaFuncAttributeMaxDynamicSharedMemorySize, IndexSmem<BK, DI>::BYTES);
   if (e != cudaSuccess) return e;

@@ -31,6 +31,8 @@ CASES = [
     ("gs1_bk128", 1536, 4, 4, 128, 64, 128, 6, 2),
     ("k1_local_only", 777, 4, 2, 128, 32, 128, 1, 0),
     ("gs2_k8", 3000, 8, 4, 64, 128, 64, 8, 2),
+    ("d64_bk128_dI128", 2500, 8, 2, 64, 128, 128, 6, 2),   # tensor-core index passes, mma.sync main pass
+    ("gs1_long_runs", 4000, 2, 2, 128, 128, 128, 3, 0),    # runs of many 8-tile chunks, split between CTAs
 ]
 
 
