@@ -746,12 +746,6 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
-// Position of row r of tile ti (16 positions x 8 head slots), or -1: no position, a slot past gs, or a
-// repeated block (marked in the record).
-__device__ __forceinline__ int32_t rec_row_t(const TileRecord* rec, int64_t ti, int r, int gs) {
-  const int p = r >> 3;
-  return ((r & 7) < gs && p < __ldg(&rec[ti].count)) ? __ldg(&rec[ti].t[p]) : -1;
-}
 }  // namespace tcb
 
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
@@ -792,44 +786,70 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   const int64_t kv_row = (int64_t)H_kv * D;
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
-  // rows of tile ti into Q/dO buffer b; row info (thread tid < 128 = row tid) into registers
-  int32_t nt_t = -1;
-  float nt_lse2 = 0.f, nt_D = 0.f;
+  // Rows of tile ti into Q/dO buffer b.  Thread tid copies 16-byte unit (tid & 15) of rows (tid >> 4) +
+  // 16 m, m < 8: positions (tid >> 7) + 2 m, head slot (tid >> 4) & 7; the record fields it needs are
+  // loaded together before any copy is issued.  The tile's (group, block) and the next tile's run key
+  // are kept in registers for the loop.
+  int32_t nx_gb = -1, nx_g = 0, nx_b = 0, nx2_gb = -1;
   auto issue_rows = [&](int64_t ti, int b) {
-    const int g = __ldg(&rec[ti].g);
-    load_tile(sm + kQ + b * kTile, q, [&](int r) -> const uint16_t* {
-      const int32_t t = rec_row_t(rec, ti, r, gs);
-      return t >= 0 ? q + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
-    });
-    load_tile(sm + kDO + b * kTile, dout, [&](int r) -> const uint16_t* {
-      const int32_t t = rec_row_t(rec, ti, r, gs);
-      return t >= 0 ? dout + ((int64_t)t * H_q + g * gs + (r & 7)) * D : nullptr;
-    });
-    if (tid < kRowsT) {
-      nt_t = rec_row_t(rec, ti, tid, gs);
-      const int64_t h = g * gs + (tid & 7);
-      nt_lse2 = nt_t >= 0 ? lse[h * N + nt_t] * kLog2e : 0.f;
-      nt_D = nt_t >= 0 ? Dr[h * N + nt_t] : 0.f;
+    const TileRecord* R = rec + ti;
+    const int g = __ldg(&R->g), cnt = __ldg(&R->count);
+    const int hs = (tid >> 4) & 7, p0 = tid >> 7, c = (tid & 15) * 8;
+    int32_t tt[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) tt[m] = __ldg(&R->t[p0 + 2 * m]);
+    nx_gb = __ldg(&R->gb);
+    nx_b = __ldg(&R->b);
+    nx2_gb = ti + 1 < hi ? __ldg(&rec[ti + 1].gb) : -1;
+    nx_g = g;
+    const bool slot_ok = hs < gs;
+    const int64_t hrow = (int64_t)g * gs + hs;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int r = (tid >> 4) + 16 * m;
+      const int32_t t = (slot_ok && p0 + 2 * m < cnt) ? tt[m] : -1;
+      const uint32_t o = off(r, c);
+      const bool ok = t >= 0;
+      cp_async_16(sm + kQ + b * kTile + o, ok ? q + ((int64_t)t * H_q + hrow) * D + c : q, ok ? 16 : 0);
+      cp_async_16(sm + kDO + b * kTile + o, ok ? dout + ((int64_t)t * H_q + hrow) * D + c : dout, ok ? 16 : 0);
     }
   };
-  if (lo < hi) issue_rows(lo, 0);
+  // Row info of tile ti (thread tid < 128 = row tid): position, lse, D; loaded while the previous tile's
+  // second MMA batch runs, stored to shared memory at the tile's start.
+  int32_t nt_t = -1;
+  float nt_lse = 0.f, nt_D = 0.f;
+  auto load_row_info = [&](int64_t ti) {
+    if (tid < kRowsT) {
+      const TileRecord* R = rec + ti;
+      const int g = __ldg(&R->g), cnt = __ldg(&R->count);
+      const int32_t tr = __ldg(&R->t[tid >> 3]);
+      nt_t = ((tid & 7) < gs && (tid >> 3) < cnt) ? tr : -1;
+      const int64_t h = (int64_t)g * gs + (tid & 7);
+      nt_lse = nt_t >= 0 ? __ldg(&lse[h * N + nt_t]) : 0.f;
+      nt_D = nt_t >= 0 ? __ldg(&Dr[h * N + nt_t]) : 0.f;
+    }
+  };
+  if (lo < hi) {
+    issue_rows(lo, 0);
+    load_row_info(lo);
+  }
   int32_t cur_gb = -1, cur_g = 0, cur_b = 0;
   uint32_t nt = 0;  // tiles done: the parity of both completion barriers
   bool issued = false;
   for (int64_t ti = lo; ti < hi; ++ti) {
     const int buf = (int)((ti - lo) & 1);
-    const int32_t gb = __ldg(&rec[ti].gb);
+    const int32_t gb = nx_gb;
     const bool new_run = gb != cur_gb;
-    const bool run_ends = ti + 1 >= hi || __ldg(&rec[ti + 1].gb) != gb;
-    if (tid < kRowsT) {  // this tile's row info, fetched with its rows
+    const bool run_ends = ti + 1 >= hi || nx2_gb != gb;
+    if (tid < kRowsT) {  // this tile's row info
       trow_s[tid] = nt_t;
-      lse2_s[tid] = nt_lse2;
+      lse2_s[tid] = nt_lse * kLog2e;
       D_s[tid] = nt_D;
     }
     if (new_run) {
       cur_gb = gb;
-      cur_g = __ldg(&rec[ti].g);
-      cur_b = __ldg(&rec[ti].b);
+      cur_g = nx_g;
+      cur_b = nx_b;
       load_tile(sm + kK, kc, [&](int r) -> const uint16_t* {
         const int64_t j = (int64_t)cur_b * BK + r;
         return j < N ? kc + j * kv_row + (int64_t)cur_g * D : nullptr;
@@ -843,10 +863,6 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     cp_async_wait<0>();  // this tile's rows (issued during the previous tile) and a new run's K/V
     sm100::fence_proxy_async_smem();
     __syncthreads();
-    // the next tile's rows stream in while this one computes (its buffer's last readers, the
-    // previous tile's MMAs, have completed)
-    if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
-    cp_async_commit();
     const uint32_t qb = sb + kQ + buf * kTile, dob = sb + kDO + buf * kTile;
     // ---- S^T and dP^T
     if (warp == 4 && lane == 0) {
@@ -862,6 +878,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
       sm100::umma_commit(bar_s);
       issued = true;
     }
+    // the next tile's rows stream in while this one computes (its buffer's last readers, the
+    // previous tile's MMAs, have completed)
+    if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
+    cp_async_commit();
     // ---- P^T (to TMEM), dZ^T (to shared memory) and the teacher: thread = key
     if (sm100::mbar_wait(bar_s, nt & 1, abort, st, 0x801)) {
       sm100::tc_fence_after();
@@ -937,22 +957,37 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
                            sm100::umma_desc_mnmajor_sw128(sb + kK + ks * 16 * 128, kChunk), kIdescMnAB, ks > 0);
       sm100::umma_commit(bar_q);
     }
+    if (ti + 1 < hi) load_row_info(ti + 1);
     if (sm100::mbar_wait(bar_q, nt & 1, abort, st, 0x802)) {
       sm100::tc_fence_after();
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-      const int r = quad * 32 + lane;  // dQ: thread = tile row, warpgroup `half` = d columns 64 half ..
-      const int32_t t = trow_s[r];
-#pragma unroll 1
-      for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
-        uint32_t x[32];
-        sm100::tmem_ld_x32(tmem + lane_base + 128 + cc * 32, x);
+      const int r = quad * 32 + lane;
+      {  // dQ: thread = tile row r, warpgroup `half` = d columns 64 half .. + 63
+        // The scaled rows are staged in this tile's Q (half 0) or dO (half 1) buffer, free now: 256 bytes
+        // per row, 16-byte unit u at u ^ (row % 16), so that the row-wise writes and the unit-wise reads
+        // below are both conflict-free.  Each warp then adds back the 32 rows it wrote, two rows (512
+        // contiguous bytes of dq each) per instruction, instead of 32 scattered rows.
+        uint32_t x[2][32];
+        sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64, x[0]);
+        sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64 + 32, x[1]);
         sm100::tmem_ld_wait();
-        if (t >= 0) {
-          float* p = dq + ((int64_t)t * H_q + cur_g * gs + (r & 7)) * D + cc * 32;
+        uint8_t* stg = sm + (half ? kDO : kQ) + buf * kTile;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add4(p + e, scale * __uint_as_float(x[e]), scale * __uint_as_float(x[e + 1]),
-                     scale * __uint_as_float(x[e + 2]), scale * __uint_as_float(x[e + 3]));
+        for (int u = 0; u < 16; ++u) {
+          const uint32_t* xs = &x[u >> 3][(u & 7) * 4];
+          *reinterpret_cast<float4*>(stg + r * 256 + ((u ^ (r & 15)) << 4)) =
+              make_float4(scale * __uint_as_float(xs[0]), scale * __uint_as_float(xs[1]),
+                          scale * __uint_as_float(xs[2]), scale * __uint_as_float(xs[3]));
+        }
+        __syncwarp();
+        const int u = lane & 15;
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+          const int rr = quad * 32 + 2 * it + (lane >> 4);
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 256 + ((u ^ (rr & 15)) << 4));
+          const int32_t t = trow_s[rr];
+          if (t >= 0)
+            red_add4(dq + ((int64_t)t * H_q + cur_g * gs + (rr & 7)) * D + half * 64 + u * 4, v.x, v.y, v.z, v.w);
         }
       }
       if (run_ends) {  // thread = key: the run's dV and dK
@@ -1015,23 +1050,41 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
 namespace tci {
 constexpr int kThreads = 128;
 constexpr int kChunkTiles = 8;
+constexpr int kRecs = kChunkTiles + 1;  // a chunk's records and the record after them (its run key)
 constexpr int kKI = 0, kQI = tcb::kTile, kDZ = 2 * tcb::kTile;
 constexpr int kLseBar = 2 * tcb::kTile, kLseBytes = 1024 + kLseBar + 64;
 constexpr int kGradBar = 3 * tcb::kTile, kGradBytes = 1024 + kGradBar + 64;
 constexpr uint32_t kIdescSS = tcb::kIdescSS, kIdescMnB = tcb::kIdescMnB, kIdescMnAB = tcb::kIdescMnAB;
 
-// The chunk starting at tile ti0 (< hi): its tile count and whether its run ends with it (in this range).
-__device__ __forceinline__ int chunk_tiles(const TileRecord* rec, int64_t ti0, int64_t hi, int32_t gb,
-                                           bool& run_ends) {
-  int n = 1;
-  while (n < kChunkTiles && ti0 + n < hi && __ldg(&rec[ti0 + n].gb) == gb) ++n;
-  run_ends = ti0 + n >= hi || __ldg(&rec[ti0 + n].gb) != gb;
-  return n;
+// Records [ti0, ti0 + kRecs) that lie below hi into dst: 16-byte cp.async pieces, threads 0 .. 8 kRecs - 1.
+__device__ __forceinline__ void fetch_records(TileRecord* dst, const TileRecord* rec, int64_t ti0, int64_t hi) {
+  const int i = threadIdx.x >> 3;
+  if (threadIdx.x < kRecs * 8 && ti0 + i < hi)
+    cp_async_16(reinterpret_cast<char*>(dst) + 16 * threadIdx.x,
+                reinterpret_cast<const char*>(rec + ti0) + 16 * threadIdx.x, 16);
 }
-// Position of row r of a chunk of n tiles from ti0, or -1 (no position, or a repeated block).
-__device__ __forceinline__ int32_t chunk_row_t(const TileRecord* rec, int64_t ti0, int n, int r) {
+struct Chunk {
+  int n;          // tiles in the chunk
+  bool run_ends;  // its (group, block) run ends with it, in this CTA's range
+  int32_t gb;
+  int g, b;
+};
+// The chunk starting at ti0 from its staged records: up to 8 tiles of one run.
+__device__ __forceinline__ Chunk chunk_of(const TileRecord* RS, int64_t ti0, int64_t hi) {
+  Chunk c;
+  c.gb = RS[0].gb;
+  c.g = RS[0].g;
+  c.b = RS[0].b;
+  int n = 1;
+  while (n < kChunkTiles && ti0 + n < hi && RS[n].gb == c.gb) ++n;
+  c.n = n;
+  c.run_ends = ti0 + n >= hi || RS[n].gb != c.gb;
+  return c;
+}
+// Position of chunk row r (tile r / 16, position r % 16), or -1 (no position, or a repeated block).
+__device__ __forceinline__ int32_t row_t(const TileRecord* RS, int n, int r) {
   const int i = r >> 4, p = r & 15;
-  return (i < n && p < __ldg(&rec[ti0 + i].count)) ? __ldg(&rec[ti0 + i].t[p]) : -1;
+  return (i < n && p < RS[i].count) ? RS[i].t[p] : -1;
 }
 // Z = Q^I K^I^T: 8 steps over d_I.
 __device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t sb) {
@@ -1042,21 +1095,25 @@ __device__ __forceinline__ void issue_logits(uint32_t tmem, uint32_t sb) {
                        sm100::umma_desc_kmajor(sb + kKI + c * tcb::kChunk + kk * 32, 128), kIdescSS, ks > 0);
   }
 }
-// The run's index keys (new run) and the chunk's index queries into shared memory.
+// Copies of the run's index keys (new run) and the chunk's index queries into shared memory, and of the
+// next chunk's records into the other record slot (a separate cp.async group, waited for at the next
+// chunk).  Returns once the keys and queries have landed.
 __device__ __forceinline__ void load_chunk(uint8_t* sm, const uint16_t* q_idx, const uint16_t* k_idx,
-                                           const TileRecord* rec, int64_t ti0, int n, bool new_run, int g, int b,
-                                           int G, int64_t N) {
+                                           const TileRecord* RS, const Chunk& ch, bool new_run, int G, int64_t N,
+                                           TileRecord* next_slot, const TileRecord* rec, int64_t ti0, int64_t hi) {
   if (new_run)
     tcb::load_tile(sm + kKI, k_idx, [&](int r) -> const uint16_t* {
-      const int64_t j = (int64_t)b * 128 + r;
+      const int64_t j = (int64_t)ch.b * 128 + r;
       return j < N ? k_idx + j * 128 : nullptr;
     });
   tcb::load_tile(sm + kQI, q_idx, [&](int r) -> const uint16_t* {
-    const int32_t t = chunk_row_t(rec, ti0, n, r);
-    return t >= 0 ? q_idx + ((int64_t)t * G + g) * 128 : nullptr;
+    const int32_t t = row_t(RS, ch.n, r);
+    return t >= 0 ? q_idx + ((int64_t)t * G + ch.g) * 128 : nullptr;
   });
   cp_async_commit();
-  cp_async_wait<0>();
+  if (ti0 + ch.n < hi) fetch_records(next_slot, rec, ti0 + ch.n, hi);
+  cp_async_commit();
+  cp_async_wait<1>();
   sm100::fence_proxy_async_smem();
 }
 }  // namespace tci
@@ -1071,6 +1128,7 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
   const uint32_t sb = smem_u32(sm);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ __align__(16) TileRecord recs_s[2][kRecs];
   const uint32_t bar = sb + kLseBar, bar_drain = sb + kLseBar + 8;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
@@ -1092,18 +1150,21 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
+  if (lo < hi) fetch_records(recs_s[0], rec, lo, hi);
+  cp_async_commit();
   int32_t cur_gb = -1;
   uint32_t phase = 0;
+  int slot = 0;
   bool issued = false;
   for (int64_t ti0 = lo; ti0 < hi;) {
-    const int32_t gb = __ldg(&rec[ti0].gb);
-    bool run_ends;
-    const int n = chunk_tiles(rec, ti0, hi, gb, run_ends);
-    const int g = __ldg(&rec[ti0].g), b = __ldg(&rec[ti0].b);
-    load_chunk(sm, q_idx, k_idx, rec, ti0, n, gb != cur_gb, g, b, G, N);
-    cur_gb = gb;
-    const int32_t t = chunk_row_t(rec, ti0, n, tid);
-    const int slot = (t >= 0) ? (int)__ldg(&rec[ti0 + (tid >> 4)].slot[tid & 15]) : 0;
+    cp_async_wait<0>();  // this chunk's records
+    __syncthreads();
+    const TileRecord* RS = recs_s[slot];
+    const Chunk ch = chunk_of(RS, ti0, hi);
+    const int32_t t = row_t(RS, ch.n, tid);
+    const int slot_k = t >= 0 ? (int)RS[tid >> 4].slot[tid & 15] : 0;
+    load_chunk(sm, q_idx, k_idx, RS, ch, ch.gb != cur_gb, G, N, recs_s[slot ^ 1], rec, ti0, hi);
+    cur_gb = ch.gb;
     __syncthreads();
     if (tid == 0) {
       sm100::tc_fence_after();
@@ -1113,36 +1174,31 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
     }
     if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x803)) {
       sm100::tc_fence_after();
-      const int64_t lim = (int64_t)t - (int64_t)b * 128;  // keys c <= lim are visible to this row
-      float m = -INFINITY, l = 0.f;  // base-2 units
-#pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
-        uint32_t x[32];
-        sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x);
-        sm100::tmem_ld_wait();
-        float cm = -INFINITY;
+      const int64_t lim = (int64_t)t - (int64_t)ch.b * 128;  // keys c <= lim are visible to this row
+      uint32_t x[4][32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float y = (c32 * 32 + e <= lim) ? __uint_as_float(x[e]) * s2 : -INFINITY;
-          x[e] = __float_as_uint(y);
-          cm = fmaxf(cm, y);
-        }
-        if (cm > -INFINITY) {
-          const float mn = fmaxf(m, cm);
-          float acc = 0.f;
+      for (int c32 = 0; c32 < 4; ++c32) sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x[c32]);
+      sm100::tmem_ld_wait();
+      float m = -INFINITY;  // base-2 units
 #pragma unroll
-          for (int e = 0; e < 32; ++e) acc += sm100::ex2_approx(__uint_as_float(x[e]) - mn);
-          l = l * sm100::ex2_approx(m - mn) + acc;
-          m = mn;
-        }
+      for (int c = 0; c < 128; ++c) {
+        const float y = (c <= lim) ? __uint_as_float(x[c >> 5][c & 31]) * s2 : -INFINITY;
+        x[c >> 5][c & 31] = __float_as_uint(y);
+        m = fmaxf(m, y);
       }
-      if (t >= 0) part[((int64_t)g * N + t) * k + slot] = make_float2(m > -INFINITY ? m * kLn2 : -INFINITY, l);
+      float l = 0.f;
+      if (m > -INFINITY) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) l += sm100::ex2_approx(__uint_as_float(x[c >> 5][c & 31]) - m);
+      }
+      if (t >= 0) part[((int64_t)ch.g * N + t) * k + slot_k] = make_float2(m > -INFINITY ? m * kLn2 : -INFINITY, l);
       sm100::tc_fence_before();
     }
     ++phase;
     __syncthreads();
     if (*abort) break;
-    ti0 += n;
+    ti0 += ch.n;
+    slot ^= 1;
   }
   cp_async_wait<0>();
   __syncthreads();
@@ -1168,6 +1224,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
   const uint32_t sb = smem_u32(sm);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ __align__(16) TileRecord recs_s[2][kRecs];
   const uint32_t bar = sb + kGradBar, bar_drain = sb + kGradBar + 8;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
@@ -1189,21 +1246,31 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
+  if (lo < hi) fetch_records(recs_s[0], rec, lo, hi);
+  cp_async_commit();
   int32_t cur_gb = -1;
   uint32_t phase = 0;
+  int slot = 0;
   bool issued = false;
   for (int64_t ti0 = lo; ti0 < hi;) {
-    const int32_t gb = __ldg(&rec[ti0].gb);
-    bool run_ends;
-    const int n = chunk_tiles(rec, ti0, hi, gb, run_ends);
-    const int g = __ldg(&rec[ti0].g), b = __ldg(&rec[ti0].b);
-    const bool new_run = gb != cur_gb;
-    load_chunk(sm, q_idx, k_idx, rec, ti0, n, new_run, g, b, G, N);
-    cur_gb = gb;
-    const int32_t t = chunk_row_t(rec, ti0, n, tid);
-    const float l2 = t >= 0 ? __ldg(&lseI[(int64_t)g * N + t]) * kLog2e : INFINITY;
-    // this row's teacher: the main kernel's row (tile ti0 + i, position p), 128 keys
+    cp_async_wait<0>();  // this chunk's records
+    __syncthreads();
+    const TileRecord* RS = recs_s[slot];
+    const Chunk ch = chunk_of(RS, ti0, hi);
+    const bool new_run = ch.gb != cur_gb;
+    const int32_t t = row_t(RS, ch.n, tid);
+    // this row's lse^I and teacher (the main kernel's row: tile ti0 + tid / 16, position tid % 16, 128
+    // keys), requested before the copies so that all the latencies overlap
+    const float lse_r = t >= 0 ? __ldg(&lseI[(int64_t)ch.g * N + t]) : INFINITY;
+    const bool have_pb = t >= 0;
     const float4* pb4 = reinterpret_cast<const float4*>(pbar_g + ((ti0 + (tid >> 4)) * kPosT + (tid & 15)) * 128);
+    float4 pb[2][8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pb[h][e] = have_pb ? __ldg(pb4 + h * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    load_chunk(sm, q_idx, k_idx, RS, ch, new_run, G, N, recs_s[slot ^ 1], rec, ti0, hi);
+    cur_gb = ch.gb;
     __syncthreads();
     if (tid == 0) {
       sm100::tc_fence_after();
@@ -1213,37 +1280,37 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     }
     if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x804)) {
       sm100::tc_fence_after();
-      const int64_t lim = (int64_t)t - (int64_t)b * 128;  // keys c <= lim are visible (none when t < 0)
+      const int64_t lim = (int64_t)t - (int64_t)ch.b * 128;  // keys c <= lim are visible (none when t < 0)
+      const float l2 = lse_r * kLog2e;
       float klsum = 0.f;
-#pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {
-        uint32_t x[32];
-        float pb[32];
-        sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x);
-        if (t >= 0) {
+      uint32_t x[2][32];
+      sm100::tmem_ld_x32(tmem + lane_base, x[0]);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 v = __ldg(pb4 + c32 * 8 + e);
-            pb[4 * e] = v.x, pb[4 * e + 1] = v.y, pb[4 * e + 2] = v.z, pb[4 * e + 3] = v.w;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) pb[e] = 0.f;
-        }
+      for (int c32 = 0; c32 < 4; ++c32) {  // 32 keys at a time; the next 32 logits and teacher values in flight
         sm100::tmem_ld_wait();
+        sm100::reg_fence32(x[c32 & 1]);
+        if (c32 < 3) sm100::tmem_ld_x32(tmem + lane_base + (c32 + 1) * 32, x[(c32 + 1) & 1]);
         uint32_t zk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float dz[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const bool ok = c32 * 32 + e + u <= lim;
-            const float y = fmaf(__uint_as_float(x[e + u]), s2, -l2);  // log2 pI
-            const float p = pb[e + u];
+            const int c = c32 * 32 + e + u;
+            const bool ok = c <= lim;
+            const float y = fmaf(__uint_as_float(x[c32 & 1][e + u]), s2, -l2);  // log2 pI
+            const float4& q4 = pb[c32 & 1][(e + u) >> 2];
+            const int cc = (e + u) & 3;
+            const float p = cc == 0 ? q4.x : cc == 1 ? q4.y : cc == 2 ? q4.z : q4.w;
             dz[u] = ok ? w * (sm100::ex2_approx(y) - p) : 0.f;
             if (ok && p > 0.f) klsum += p * (__logf(p) - y * 0.6931471805599453f);
           }
           zk[e >> 1] = pack_bf16x2(dz[0], dz[1]);
+        }
+        if (c32 < 2) {  // teacher values of keys 32 (c32 + 2) .. into the registers just used
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            pb[c32 & 1][e] = have_pb ? __ldg(pb4 + (c32 + 2) * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
@@ -1251,7 +1318,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
           *reinterpret_cast<uint4*>(sm + kDZ + o) = make_uint4(zk[4 * q8], zk[4 * q8 + 1], zk[4 * q8 + 2], zk[4 * q8 + 3]);
         }
       }
-      if (kl && t >= 0) atomicAdd(kl + (int64_t)g * N + t, klsum);
+      if (kl && t >= 0) atomicAdd(kl + (int64_t)ch.g * N + t, klsum);
       sm100::fence_proxy_async_smem();
       sm100::tc_fence_before();
     }
@@ -1275,21 +1342,32 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     }
     if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x805)) {
       sm100::tc_fence_after();
-#pragma unroll 1
-      for (int c32 = 0; c32 < 4; ++c32) {  // thread = position: its dq^I row
-        uint32_t x[32];
-        sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x);
-        sm100::tmem_ld_wait();
-        if (t >= 0) {
-          float* pq = dq_idx + ((int64_t)t * G + g) * 128 + c32 * 32;
+      {  // thread = position: its dq^I row, staged through the (now free) query tile so that each warp adds
+         // two rows (1 KB of dq^I) per instruction; 16-byte unit u of row r sits at u ^ (r % 32)
+        uint32_t x[4][32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            tcb::red_add4(pq + e, sI * __uint_as_float(x[e]), sI * __uint_as_float(x[e + 1]),
-                          sI * __uint_as_float(x[e + 2]), sI * __uint_as_float(x[e + 3]));
+        for (int c32 = 0; c32 < 4; ++c32) sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x[c32]);
+        sm100::tmem_ld_wait();
+        uint8_t* stg = sm + kQI;  // 128 rows x 512 bytes = the query tile and the dzI tile after it
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const uint32_t* xs = &x[u >> 3][(u & 7) * 4];
+          *reinterpret_cast<float4*>(stg + tid * 512 + ((u ^ (tid & 31)) << 4)) =
+              make_float4(sI * __uint_as_float(xs[0]), sI * __uint_as_float(xs[1]), sI * __uint_as_float(xs[2]),
+                          sI * __uint_as_float(xs[3]));
+        }
+        __syncwarp();
+        const int lane = tid & 31;
+#pragma unroll 4
+        for (int rr0 = 0; rr0 < 32; ++rr0) {  // row warp * 32 + rr0: lane = unit
+          const int rr = warp * 32 + rr0;
+          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 512 + ((lane ^ (rr & 31)) << 4));
+          const int32_t tr = row_t(RS, ch.n, rr);
+          if (tr >= 0) tcb::red_add4(dq_idx + ((int64_t)tr * G + ch.g) * 128 + lane * 4, v.x, v.y, v.z, v.w);
         }
       }
-      if (run_ends) {  // thread = key: the run's dk^I
-        const int64_t j = (int64_t)b * 128 + tid;
+      if (ch.run_ends) {  // thread = key: the run's dk^I
+        const int64_t j = (int64_t)ch.b * 128 + tid;
 #pragma unroll 1
         for (int c32 = 0; c32 < 4; ++c32) {
           uint32_t x[32];
@@ -1309,7 +1387,8 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     ++phase;
     __syncthreads();
     if (*abort) break;
-    ti0 += n;
+    ti0 += ch.n;
+    slot ^= 1;
   }
   cp_async_wait<0>();
   __syncthreads();
