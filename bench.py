@@ -748,7 +748,7 @@ def main():
         tri = wc.N * wc.N / 2.0
         f_fl = tri * (4.0 * wc.H_q * wc.d + 2.0 * wc.G * wc.d_I)
         g_fl = tri * (2.0 * wc.H_q * wc.d + 6.0 * wc.G * wc.d_I)
-        line["warmup"] = {
+        line["warmup_mode"] = {
             "metric": "warmup-mode tokens/s (dense main attention + index KL and its gradients, msa_warmup_fwd + "
                       "msa_warmup_index_grad)",
             "value": ws * wc.N / ((f_ms + g_ms) / 1000.0), "unit": "tokens/s", "ms_per_step": f_ms + g_ms,

@@ -59,6 +59,10 @@ __device__ __forceinline__ void tile_range(const int32_t* tile_off, int64_t n_gb
   hi = min(total, lo + per);
 }
 
+// The teacher rows pass between kernels as bf16 (round to nearest even).
+__device__ __forceinline__ uint16_t teacher_bf16(float x) { return (uint16_t)(pack_bf16x2(x, 0.f) & 0xffffu); }
+__device__ __forceinline__ float teacher_f32(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
@@ -228,9 +232,11 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
 // lse^I[g, t] from the (max, sum) of the row's slots; a slot counts iff its id
 // is in [0, nb) and first of its kind in the row.
 __global__ void bwd_index_lse_combine_kernel(const float2* __restrict__ part, const int32_t* __restrict__ block_idx,
-                                             int64_t N, int G, int k, int64_t nb, float* __restrict__ lseI) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // g * N + t
-  if (i >= (int64_t)G * N) return;
+                                             int64_t N, int G, int k, int64_t nb, int64_t T0, int64_t S,
+                                             float* __restrict__ lseI) {
+  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // g * S + (t - T0)
+  if (w >= (int64_t)G * S) return;
+  const int64_t i = (w / S) * N + T0 + w % S;  // g * N + t
   const int32_t* sel = block_idx + i * k;
   const float2* pp = part + i * k;
   float M = __int_as_float(0xff800000);
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
     const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
     const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int H_q,
     int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
-    float* __restrict__ pbar_g) {
+    uint16_t* __restrict__ pbar_g) {
   using L = MainSmem<D, BK>;
   extern __shared__ __align__(128) uint8_t smb[];
   uint16_t* Ks = reinterpret_cast<uint16_t*>(smb + L::K);
@@ -422,9 +428,9 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
             tsum[half] += __shfl_xor_sync(0xffffffffu, tsum[half], 2);
           }
           if (c4 == 0) {
-            float* pb = pbar_g + (ti * kPosT + row0 / 8 + nt) * BK + key0 + g8;
-            pb[0] = tsum[0] * inv_gs;
-            pb[8] = tsum[1] * inv_gs;
+            uint16_t* pb = pbar_g + (ti * kPosT + row0 / 8 + nt) * BK + key0 + g8;
+            pb[0] = teacher_bf16(tsum[0] * inv_gs);
+            pb[8] = teacher_bf16(tsum[1] * inv_gs);
           }
         }
       }
@@ -480,14 +486,14 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
 // and teacher rows (from the main kernel); dzI.
 template <int BK, int DI>
 struct IndexSmem {
-  static constexpr int KI = 0, QI = BK * DI * 2, PB = QI + 2 * kPosT * DI * 2, DZ = PB + 2 * kPosT * BK * 4;
+  static constexpr int KI = 0, QI = BK * DI * 2, PB = QI + 2 * kPosT * DI * 2, DZ = PB + 2 * kPosT * BK * 2;
   static constexpr int BYTES = DZ + kPosT * BK * 2;
 };
 
 template <int BK, int DI>
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const float* __restrict__ lseI,
-    const float* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
+    const uint16_t* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
     int64_t n_gb, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
     float* __restrict__ kl) {
   using L = IndexSmem<BK, DI>;
@@ -501,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
   const uint32_t kIs_a = smem_u32(kIs), dzs_a = smem_u32(dzs);
   auto qIs = [&](int b) { return reinterpret_cast<uint16_t*>(smb + L::QI + b * kPosT * DI * 2); };
-  auto pbs = [&](int b) { return reinterpret_cast<float*>(smb + L::PB + b * kPosT * BK * 4); };
+  auto pbs = [&](int b) { return reinterpret_cast<uint16_t*>(smb + L::PB + b * kPosT * BK * 2); };
   float accI[DI / 8][4];
 #pragma unroll
   for (int i = 0; i < DI / 8; ++i) accI[i][0] = accI[i][1] = accI[i][2] = accI[i][3] = 0.f;
@@ -532,9 +538,9 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
       const int32_t t = p < rc.count ? rc.t[p] : -1;
       return t >= 0 ? q_idx + ((int64_t)t * G + rc.g) * DI : nullptr;
     });
-    const float* src = pbar_g + ti * kPosT * BK;  // the teacher rows the main kernel wrote for this tile
-    float* dst = pbs(b);
-    for (int i = tid; i < kPosT * BK / 4; i += blockDim.x) cp_async_16(dst + 4 * i, src + 4 * i, 16);
+    const uint16_t* src = pbar_g + ti * kPosT * BK;  // the teacher rows the main kernel wrote for this tile
+    uint16_t* dst = pbs(b);
+    for (int i = tid; i < kPosT * BK / 8; i += blockDim.x) cp_async_16(dst + 8 * i, src + 8 * i, 16);
   };
   int64_t lo, hi;
   tile_range(tile_off, n_gb, lo, hi);
@@ -569,7 +575,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
     if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
     cp_async_commit();
     const uint32_t qIs_a = smem_u32(qIs(buf));
-    const float* pb_s = pbs(buf);
+    const uint16_t* pb_s = pbs(buf);
 
     // ---- index logits of this warp's 16 keys for the 16 positions, dzI and the KL terms
     if (warp < KSL) {
@@ -596,7 +602,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
             float dz = 0.f;
             if (t >= 0 && j <= t) {
               const float logp = zi[nt][2 * half + e] * sI - lseI_s[buf][p];
-              const float pb = pb_s[p * BK + key];
+              const float pb = teacher_f32(pb_s[p * BK + key]);
               dz = w * (__expf(logp) - pb);
               if (pb > 0.f) klp[nt][e] += pb * (__logf(pb) - logp);
             }
@@ -661,8 +667,8 @@ struct BwdScratch {
   TileRecord* rec;
   float *Dr, *lseI;
   float2* partI;
-  float* pbar;  // [tile][16 positions][Bk keys]: the teacher, written by the main kernel
-  int64_t max_tiles, nb;
+  uint16_t* pbar;  // [slab tile][16 positions][Bk keys] bf16: the teacher, written by the main kernel
+  int64_t max_tiles, nb, slab;
 };
 
 size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* out) {
@@ -675,7 +681,13 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
   };
   BwdScratch s;
   s.nb = ceil_div(N, Bk);
-  s.max_tiles = (int64_t)G * ceil_div(N * k, kPosT) + (int64_t)G * s.nb;
+  // the per-slab buffer: the teacher rows, G k Bk 2 bytes a position
+  const double per_pos = (double)G * k * Bk * 2.0;
+  int64_t cap = (int64_t)(32.0e9 / per_pos);
+  if (cap > 131072) cap = 131072;
+  if (cap < 1024) cap = 1024;
+  s.slab = N < cap ? N : cap;
+  s.max_tiles = (int64_t)G * ceil_div(s.slab * k, kPosT) + (int64_t)G * s.nb;
   s.row_ptr = (int32_t*)take((size_t)G * (s.nb + 1) * 4);
   s.entries = (int32_t*)take((size_t)G * N * k * 4);
   s.n_entries = (int32_t*)take((size_t)G * 4);
@@ -689,7 +701,7 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
   s.Dr = (float*)take((size_t)H_q * N * 4);
   s.lseI = (float*)take((size_t)G * N * 4);
   s.partI = (float2*)take((size_t)G * N * k * 8);
-  s.pbar = (float*)take((size_t)s.max_tiles * kPosT * Bk * 4);
+  s.pbar = (uint16_t*)take((size_t)s.max_tiles * kPosT * Bk * 2);
   if (out) *out = s;
   return off;
 }
@@ -753,7 +765,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
     const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int H_q,
     int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
-    float* __restrict__ pbar_g, DeviceStatus* st) {
+    uint16_t* __restrict__ pbar_g, DeviceStatus* st) {
   using namespace tcb;
   constexpr int D = 128, BK = 128;
   extern __shared__ uint8_t smraw[];
@@ -921,7 +933,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
         }
         if (pbar_g) {
 #pragma unroll
-          for (int pp = 0; pp < 4; ++pp) pbar_g[(ti * kPosT + cc * 4 + pp) * BK + key] = tsum[pp] * inv_gs;
+          for (int pp = 0; pp < 4; ++pp) pbar_g[(ti * kPosT + cc * 4 + pp) * BK + key] = teacher_bf16(tsum[pp] * inv_gs);
         }
         // P^T rows 32 cc .. +31 -> packed columns 64 half + 16 h2 .. + 15 (within this warpgroup's S^T
         // columns, all already read)
@@ -1215,7 +1227,7 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
 
 __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const float* __restrict__ lseI,
-    const float* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
+    const uint16_t* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
     int64_t n_gb, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
     float* __restrict__ kl, DeviceStatus* st) {
   using namespace tci;
@@ -1260,15 +1272,12 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     const bool new_run = ch.gb != cur_gb;
     const int32_t t = row_t(RS, ch.n, tid);
     // this row's lse^I and teacher (the main kernel's row: tile ti0 + tid / 16, position tid % 16, 128
-    // keys), requested before the copies so that all the latencies overlap
+    // keys in bf16), requested before the copies so that all the latencies overlap
     const float lse_r = t >= 0 ? __ldg(&lseI[(int64_t)ch.g * N + t]) : INFINITY;
-    const bool have_pb = t >= 0;
-    const float4* pb4 = reinterpret_cast<const float4*>(pbar_g + ((ti0 + (tid >> 4)) * kPosT + (tid & 15)) * 128);
-    float4 pb[2][8];
+    const uint4* pb8 = reinterpret_cast<const uint4*>(pbar_g + ((ti0 + (tid >> 4)) * kPosT + (tid & 15)) * 128);
+    uint4 pb[16];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) pb[h][e] = have_pb ? __ldg(pb4 + h * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = 0; e < 16; ++e) pb[e] = t >= 0 ? __ldg(pb8 + e) : make_uint4(0u, 0u, 0u, 0u);
     load_chunk(sm, q_idx, k_idx, RS, ch, new_run, G, N, recs_s[slot ^ 1], rec, ti0, hi);
     cur_gb = ch.gb;
     __syncthreads();
@@ -1286,7 +1295,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
       uint32_t x[2][32];
       sm100::tmem_ld_x32(tmem + lane_base, x[0]);
 #pragma unroll
-      for (int c32 = 0; c32 < 4; ++c32) {  // 32 keys at a time; the next 32 logits and teacher values in flight
+      for (int c32 = 0; c32 < 4; ++c32) {  // 32 keys at a time; the next 32 logits in flight
         sm100::tmem_ld_wait();
         sm100::reg_fence32(x[c32 & 1]);
         if (c32 < 3) sm100::tmem_ld_x32(tmem + lane_base + (c32 + 1) * 32, x[(c32 + 1) & 1]);
@@ -1299,18 +1308,14 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
             const int c = c32 * 32 + e + u;
             const bool ok = c <= lim;
             const float y = fmaf(__uint_as_float(x[c32 & 1][e + u]), s2, -l2);  // log2 pI
-            const float4& q4 = pb[c32 & 1][(e + u) >> 2];
-            const int cc = (e + u) & 3;
-            const float p = cc == 0 ? q4.x : cc == 1 ? q4.y : cc == 2 ? q4.z : q4.w;
+            const uint4& q8 = pb[c32 * 4 + ((e + u) >> 3)];
+            const int cc = (e + u) & 7;
+            const uint32_t wd = (cc >> 1) == 0 ? q8.x : (cc >> 1) == 1 ? q8.y : (cc >> 1) == 2 ? q8.z : q8.w;
+            const float p = __uint_as_float((cc & 1) ? (wd & 0xffff0000u) : (wd << 16));
             dz[u] = ok ? w * (sm100::ex2_approx(y) - p) : 0.f;
             if (ok && p > 0.f) klsum += p * (__logf(p) - y * 0.6931471805599453f);
           }
           zk[e >> 1] = pack_bf16x2(dz[0], dz[1]);
-        }
-        if (c32 < 2) {  // teacher values of keys 32 (c32 + 2) .. into the registers just used
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            pb[c32 & 1][e] = have_pb ? __ldg(pb4 + (c32 + 2) * 8 + e) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
@@ -1407,7 +1412,8 @@ template <int D, int BK, int DI>
 cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
                          const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc,
                          int64_t N, int H_q, int H_kv, int k, float scale, float kl_weight, float* dq, float* dk,
-                         float* dv, float* dq_idx, float* dk_idx, float* kl, DeviceStatus* st, cudaStream_t s) {
+                         float* dv, float* dq_idx, float* dk_idx, float* kl, int64_t T0, int64_t T1, DeviceStatus* st,
+                         cudaStream_t s) {
   const int G = H_kv, gs = H_q / H_kv;
   const int64_t n_gb = (int64_t)G * sc.nb;
   const float sI = 1.f / sqrtf((float)DI);
@@ -1423,8 +1429,8 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
     bwd_index_lse_kernel<BK, DI><<<grid, kThreadsB, 0, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec,
                                                             sc.tile_off, n_gb, N, G, k, sI, sc.partI);
   }
-  bwd_index_lse_combine_kernel<<<(unsigned)ceil_div((int64_t)G * N, 256), 256, 0, s>>>(sc.partI, block_idx, N, G, k,
-                                                                                      sc.nb, sc.lseI);
+  bwd_index_lse_combine_kernel<<<(unsigned)ceil_div((int64_t)G * (T1 - T0), 256), 256, 0, s>>>(
+      sc.partI, block_idx, N, G, k, sc.nb, T0, T1 - T0, sc.lseI);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (D == 128 && BK == 128) {
@@ -1465,15 +1471,15 @@ template <int D, int BK>
 cudaError_t launch_di(int d_I, const void* q, const void* kk, const void* v, const void* q_idx, const void* k_idx,
                       const int32_t* block_idx, const void* dout, const float* lse, const BwdScratch& sc, int64_t N,
                       int H_q, int H_kv, int k, float scale, float w, float* dq, float* dk, float* dv, float* dq_idx,
-                      float* dk_idx, float* kl, DeviceStatus* st, cudaStream_t s) {
+                      float* dk_idx, float* kl, int64_t T0, int64_t T1, DeviceStatus* st, cudaStream_t s) {
   if (d_I == 32)
     return launch_tiles<D, BK, 32>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
-                                   dk, dv, dq_idx, dk_idx, kl, st, s);
+                                   dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s);
   if (d_I == 64)
     return launch_tiles<D, BK, 64>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
-                                   dk, dv, dq_idx, dk_idx, kl, st, s);
+                                   dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s);
   return launch_tiles<D, BK, 128>(q, kk, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, k, scale, w, dq,
-                                  dk, dv, dq_idx, dk_idx, kl, st, s);
+                                  dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s);
 }
 
 }  // namespace
@@ -1500,24 +1506,33 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   if (kl && (e = cudaMemsetAsync(kl, 0, (size_t)G * N * 4, s)) != cudaSuccess) return e;
   if ((e = launch_invert(block_idx, N, G, Bk, kb, sc.row_ptr, sc.entries, sc.n_entries, sc.inv, st, s)) != cudaSuccess)
     return e;
-  if ((e = launch_tile_schedule(sc.row_ptr, sc.entries, N, G, kb, sc.nb, 0, N, sc.max_tiles, sc.lo, sc.cnt, sc.tiles,
-                                sc.tile_off, sc.rec, s)) != cudaSuccess)
-    return e;
-  mark_repeats_kernel<<<(unsigned)ceil_div(sc.max_tiles * kPosT, 256), 256, 0, s>>>(sc.rec, sc.tile_off,
-                                                                                   (int64_t)G * sc.nb, block_idx, N,
-                                                                                   kb);
   bwd_rowdot_kernel<<<(unsigned)ceil_div(N * H_q * 32, 256), 256, 0, s>>>((const uint16_t*)dout,
                                                                         (const uint16_t*)out, N, H_q, d, sc.Dr);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (d == 64)
-    return Bk == 64 ? launch_di<64, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
-                                        kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s)
-                    : launch_di<64, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
-                                         scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s);
-  return Bk == 64 ? launch_di<128, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
-                                       kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s)
-                  : launch_di<128, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
-                                        scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, st, s);
+  // Query slabs [T0, T1) bound the teacher buffer; the gradients accumulate across slabs, and a slab's
+  // positions have all their blocks in its tile list.
+  for (int64_t T0 = 0; T0 < N; T0 += sc.slab) {
+    const int64_t T1 = T0 + sc.slab < N ? T0 + sc.slab : N;
+    if ((e = launch_tile_schedule(sc.row_ptr, sc.entries, N, G, kb, sc.nb, T0, T1, sc.max_tiles, sc.lo, sc.cnt,
+                                  sc.tiles, sc.tile_off, sc.rec, s)) != cudaSuccess)
+      return e;
+    mark_repeats_kernel<<<(unsigned)ceil_div(sc.max_tiles * kPosT, 256), 256, 0, s>>>(sc.rec, sc.tile_off,
+                                                                                     (int64_t)G * sc.nb, block_idx, N,
+                                                                                     kb);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (d == 64)
+      e = Bk == 64 ? launch_di<64, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb, scale,
+                                       kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s)
+                   : launch_di<64, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
+                                        scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s);
+    else
+      e = Bk == 64 ? launch_di<128, 64>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
+                                        scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s)
+                   : launch_di<128, 128>(d_I, q, k, v, q_idx, k_idx, block_idx, dout, lse, sc, N, H_q, H_kv, kb,
+                                         scale, kl_weight, dq, dk, dv, dq_idx, dk_idx, kl, T0, T1, st, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace msa

@@ -129,7 +129,7 @@ def _bwd_sampled(name, n_rows):
     sum_j dv_{j,g} = the sum of the group's dout rows (each row's probabilities sum to 1)."""
     from test_gpu_bwd import rel_report
     from block_sparse_long_index_gb300 import msa
-    cfg = datagen.CONFIGS[name]
+    cfg = datagen.CONFIGS[name] if isinstance(name, str) else name
     N, G, d, d_I = cfg.N, cfg.G, cfg.d, cfg.d_I
     dev = datagen.prefill_device(cfg)
     dout = datagen.device_normal_(torch.empty((N, cfg.H_q, d), dtype=torch.bfloat16, device="cuda"), cfg.seed,
@@ -188,6 +188,12 @@ def test_bwd_32k_sampled():
 
 def test_bwd_128k_sampled():
     _bwd_sampled("prefill_128k", 64)
+
+
+def test_bwd_two_query_slabs_sampled():
+    """N above the backward's query-slab cap (131072 positions): two slabs, sampled rows from both."""
+    cfg = datagen.make_config("bwd_two_slabs", N=180000, H_q=8, H_kv=2, d=128, d_I=128, Bk=128, k=8, needles=4)
+    _bwd_sampled(cfg, 96)
 
 
 def _device_e4m3(msa, x):
