@@ -19,21 +19,27 @@
 //   dk^I_j += dzI_j q^I / sqrt(d_I).
 //
 // Kernels, all over the forward's KV-outer tile list (B -> B*, tiles of 16
-// positions x 8 head slots = 128 rows, one (group, block) per tile):
+// positions x 8 head slots = 128 rows, one (group, block) per tile), built per
+// query slab of at most 131072 positions (the slab bounds the teacher buffer;
+// every gradient accumulates across slabs):
 //   rowdot:     D[h, t] = dO.O;
-//   index lse:  per tile the masked index logits of its 16 positions -> one
-//               (max, sum) per (t, slot); a combine per (t, g) -> lse^I;
-//   main:       warps own 16-key slices: S^T, P^T, dP^T, dZ^T for their keys
-//               and the tile's rows, dV and dK accumulated in registers over
-//               the tiles of a (group, block) and flushed with fp32 reductions;
-//               dZ staged in shared memory, then warps own rows for dQ, added
-//               to dq with fp32 reductions;
-//   index:      the same shape for the index branch, with the teacher rows
-//               the main kernel wrote per tile: the index logits, dzI, dk^I
-//               per key slice in registers, dq^I through shared memory; KL
-//               per row.
-// The tile kernels prefetch: while one tile computes, the next tile's rows
-// (and the record after it) arrive by cp.async into a second set of buffers.
+//   index lse:  the masked index logits of each position over the tile's
+//               block -> one (max, sum) per (t, slot); a combine per (t, g)
+//               -> lse^I;
+//   main:       S^T, P^T, dP^T, dZ^T of the tile's keys and rows; dV and dK
+//               accumulated over the tiles of a (group, block) and flushed
+//               with fp32 reductions; dQ added to dq with fp32 reductions;
+//               the teacher rows (mean P over each position's heads, bf16)
+//               written per tile;
+//   index:      the index logits again, dzI and the KL terms against the
+//               teacher rows, dq^I added to dq_idx, dk^I accumulated over the
+//               run.
+// For d = Bk = d_I = 128 the three tile kernels run on tcgen05 (the *_tc
+// kernels below: operands in 128B-swizzled shared memory, accumulators in
+// TMEM, dK/dV and dk^I accumulated in TMEM across a run); other shapes use
+// mma.sync kernels in which warps own 16-key slices and keep dK/dV in
+// registers.  The tile kernels fetch the next tile's (or chunk's) rows and
+// records while the current one computes.
 // A block id repeated in a row's set contributes once (its first slot).
 #include <math.h>
 

@@ -161,7 +161,10 @@ msa_status_t msa_sparse_attn_fwd(const void* q, const void* k, const void* v, co
  *   dq        [N, H_q, d] fp32 out;  dk, dv [N, H_kv, d] fp32 out
  *   dq_idx    [N, G, d_I] fp32 out;  dk_idx [N, d_I] fp32 out
  *   kl        [G, N] fp32 out (nullable): each row's KL
- *   workspace msa_sparse_attn_bwd_workspace(shape) bytes, 256-byte aligned
+ *   workspace msa_sparse_attn_bwd_workspace(shape) bytes, 256-byte aligned;
+ *             it grows with N * G * k (the B* entries and per-slot partials)
+ *             plus a teacher buffer bounded by query slabs of at most 131072
+ *             positions (G * k * Bk * 2 bytes a position of one slab)
  * The gradient outputs are cleared and then accumulated in place on `stream`.
  */
 size_t msa_sparse_attn_bwd_workspace(const msa_shape_t* shape);

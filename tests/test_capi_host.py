@@ -187,3 +187,18 @@ def test_warmup_validation(lib):
                                      FAKE, FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
     assert raw.msa_warmup_index_grad(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(s), 0.1, 1.0, FAKE,
                                      ctypes.c_void_p((1 << 20) + 8), FAKE, None) == lib.MSA_ERR_INVALID_ARGUMENT
+
+
+def test_bwd_workspace_teacher_is_slab_bounded(lib):
+    """The backward's teacher buffer (G k Bk 2 bytes a position) is sized for one query slab of at most
+    131072 positions: past one slab the workspace grows linearly, by the per-entry and per-row buffers
+    only (B* entries, index partials, D, lse^I: a few KB a position, against 32 KB for the teacher)."""
+    def ws(N):
+        return lib.msa_sparse_attn_bwd_workspace(lib.shape(N, 64, 8, 128, 128, 128, 16))
+    a, b, c = ws(131072), ws(262144), ws(524288)
+    per_pos = (b - a) / 131072
+    assert 0 < per_pos < 8192, per_pos
+    assert abs((c - b) - 2 * (b - a)) < (1 << 16)  # linear past the slab, up to alignment
+    # below one slab the teacher grows with N as well
+    small = (ws(65536) - ws(32768)) / 32768
+    assert small > per_pos + 8 * 16 * 128 * 2 * 0.9
