@@ -187,6 +187,15 @@ def prefill_launches(cfg):
     return 1 + 4 + 5 * prefill_slabs(cfg)
 
 
+def bwd_launches(cfg):
+    """Kernels libmsa launches for one msa_sparse_attn_bwd call: B* inversion 4, rowdot 1, then per query slab
+    (at most 131072 positions, fewer when the G k Bk 2-byte teacher rows of a slab would pass 32 GB) the
+    schedule 3, mark_repeats 1, index lse 1 and its combine 1, main 1, index gradient 1."""
+    cap = int(32.0e9 / (cfg.G * cfg.k * cfg.Bk * 2.0))
+    slab = min(cfg.N, max(1024, min(131072, cap)))
+    return 5 + 8 * ((cfg.N + slab - 1) // slab)
+
+
 def varlen_mix(N, Bk):
     """A fixed mix of sequence lengths (block multiples) filling N cells: 1/4, 3/16, 1/8, 1/8, 3/32, 3/32,
     1/16, 1/16 of N."""
@@ -699,7 +708,7 @@ def main():
                                          "algorithmic": "N*H_q*k*Bk*d*10 (S, dP, dV, dK, dQ) + N*G*k*Bk*d_I*6 "
                                                         "(index logits, dk_idx, dq_idx) = %.4g FLOP per call" % bflops,
                                          "peak_source": "%s bf16_tflops_sustained" % peak_src},
-                            "gpu_launches": 10 * K}
+                            "gpu_launches": bwd_launches(cfg) * K}
     if "e2e" in pre:
         e = pre["e2e"]
         e_ms = dist.max(e["ms"])
