@@ -23,6 +23,7 @@
 //      overlaps the scan's tail.
 #include <math.h>
 
+#include <cudaTypedefs.h>
 #include <mutex>
 
 #include "msa_sm100.cuh"
@@ -701,10 +702,41 @@ cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_id
 // up below with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// Unique id of the calling thread's current context (cuCtxGetId), 0 when none is
+// current.  The driver calls come through the runtime's entry-point table, so
+// the library links no libcuda.
+static cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  *id = 0;
+  if (!get_current || !get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || !f1)
+      return cudaErrorNotSupported;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess || !f2)
+      return cudaErrorNotSupported;
+    get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+    get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+  if (!ctx) return cudaSuccess;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorUnknown;
+}
+
+// The array's device address is looked up once per device and context, with
+// that device current: after cudaDeviceReset, or with another context made
+// current, the module is loaded again and the address is looked up again
+// (context ids are never reused within a process).
 cudaError_t noalloc_scratch(size_t need, void** out) {
   constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   *out = nullptr;
   if (need > kNoAllocScratchBytes) return cudaErrorInvalidValue;
   int dev = 0;
@@ -712,11 +744,18 @@ cudaError_t noalloc_scratch(size_t need, void** out) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {  // once per device, with that device current
+  unsigned long long id = 0;
+  e = current_context_id(&id);
+  if (e != cudaSuccess) return e;
+  if (!addr[dev] || id == 0 || ctx_of[dev] != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current if none was
     if (e != cudaSuccess) return e;
+    e = current_context_id(&id);
+    if (e != cudaSuccess) return e;
+    if (id == 0) return cudaErrorInvalidResourceHandle;
     addr[dev] = p;
+    ctx_of[dev] = id;
   }
   *out = addr[dev];
   return cudaSuccess;

@@ -376,7 +376,9 @@ msa_status_t msa_decode_paged_fp8(const void* q_t, const void* q_idx_t, const vo
  * msa_decode.
  *   - The first call on a device looks up the array's device address for that
  *     device (cudaGetSymbolAddress, with the device current); make that first
- *     call before any stream capture.
+ *     call before any stream capture.  The address is kept per device and
+ *     context: a call made after cudaDeviceReset, or under another context of
+ *     the same device, looks it up again, so it is never stale.
  *   - Shapes whose scratch (what msa_decode_workspace() reports for them)
  *     exceeds 8 MiB are rejected with MSA_ERR_WORKSPACE_TOO_SMALL before any
  *     launch.  B = 4, H_q = 64, H_kv = 8, d = 128, k = 16 needs about 2.4 MiB.
@@ -385,8 +387,11 @@ msa_status_t msa_decode_paged_fp8(const void* q_t, const void* q_idx_t, const vo
  *     that can overlap on the GPU (different streams, or different host
  *     threads) race on it: order them on one stream.
  *   - Device-side bad data (ctx_len outside [1, N]) still zeroes that
- *     sequence's outputs, but the error word lives in the shared array and is
- *     not reported by this call.
+ *     sequence's outputs, and a bounded device wait that gives up still ends
+ *     its kernel cleanly, but both flags live in the shared array's status
+ *     word: this call returns MSA_OK for them and cannot report
+ *     MSA_ERR_BAD_INDEX or MSA_ERR_TIMEOUT.  Callers that need those statuses
+ *     use msa_decode with a workspace and msa_check_device_error.
  */
 msa_status_t msa_decode_noalloc(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
                                 const void* v_cache, const int32_t* ctx_len, int B, const msa_shape_t* shape,

@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -23,3 +24,24 @@ def _built_host_libs():
     if not os.path.exists(os.path.join(ROOT, "oracle", "libmsa_oracle.so")):
         oracle.build()
     yield
+
+
+_PARITY_LOG = []
+
+
+@pytest.fixture
+def parity_log(request):
+    """Records a parity report (set counts: rows, mismatches, near-tie rows, strict-invalid rows; attention:
+    max abs / rel error and cosine).  The reports are printed, and written as JSON at the end of the session
+    to the path in MSA_PARITY_REPORT when that variable is set."""
+    def log(case, **reports):
+        _PARITY_LOG.append(dict(test=request.node.nodeid, case=case, **reports))
+        print(case, reports)
+    return log
+
+
+def pytest_sessionfinish(session, exitstatus):
+    path = os.environ.get("MSA_PARITY_REPORT")
+    if path and _PARITY_LOG:
+        with open(path, "w") as f:
+            json.dump(_PARITY_LOG, f, indent=1)

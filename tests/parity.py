@@ -105,7 +105,9 @@ def compare_sets_lazy(gpu_blk, ora_blk, kth, q_idx_rows, k_idx, rows, N, Bk):
     G, R, k = ora_blk.shape
     mism_rows = np.nonzero(np.any(np.any(np.sort(gpu_blk, 2) != np.sort(ora_blk, 2), axis=2), axis=0))[0]
     if len(mism_rows) == 0:
-        return compare_sets(gpu_blk, ora_blk, kth)
+        rep = compare_sets(gpu_blk, ora_blk, kth)
+        rep["strict_invalid"] = 0  # no row differs, so none can be invalid
+        return rep
     sub_rows = np.asarray(rows)[mism_rows]
     S = oracle.block_scores(q_idx_rows[mism_rows], k_idx, sub_rows, N, Bk)
     gam = gamma_rows(bf16_to_f64(q_idx_rows[mism_rows]), bf16_to_f64(k_idx), sub_rows, q_idx_rows.shape[2])
@@ -152,3 +154,56 @@ def gamma_rows_e4m3(q_codes, k_codes, rows, d_I):
     """gamma_rows on the decoded values of E4M3 inputs."""
     import oracle
     return gamma_rows(oracle.e4m3_decode(q_codes), oracle.e4m3_decode(k_codes), rows, d_I)
+
+
+def _sum_reports(reps):
+    keys = ("rows", "mismatch", "near_tie", "mismatch_outside_near_tie", "strict_invalid")
+    return {k_: int(sum(r.get(k_, 0) for r in reps)) for k_ in keys}
+
+
+def decode_sets_check(gpu_blk, q_idx_t, k_idx_cache, ctx_len, Bk, k, fp8=False):
+    """The selection contract on a decode step, sequence by sequence: set equality outside near-tie rows and,
+    on every row whose set differs from the oracle's, the strict validity check against the oracle's fp64
+    block scores (the same rules as prefill rows).
+
+    gpu_blk [B, G, k]; q_idx_t [B, G, d_I] and k_idx_cache [B, ctx, d_I] as bf16 bit patterns (E4M3 codes
+    with fp8=True).  Returns (summed report, oracle sets [B, G, k])."""
+    import oracle
+    from datagen import bf16_to_f64
+    B, G, _ = gpu_blk.shape
+    d_I = q_idx_t.shape[2]
+    sel = oracle.select_blocks_e4m3 if fp8 else oracle.select_blocks
+    scores = oracle.block_scores_e4m3 if fp8 else oracle.block_scores
+    ora_all = np.empty_like(gpu_blk)
+    reps = []
+    for b in range(B):
+        t = int(ctx_len[b]) - 1
+        qb, kb = q_idx_t[b:b + 1], k_idx_cache[b, :t + 1]
+        ora, kth = sel(qb, kb, [t], t + 1, Bk, k)
+        ora_all[b] = ora[:, 0]
+        g_b = gpu_blk[b][:, None, :]
+        if np.array_equal(np.sort(g_b, 2), np.sort(ora, 2)):
+            rep = compare_sets(g_b, ora, kth)
+            rep["strict_invalid"] = 0
+        else:
+            S = scores(qb, kb, [t], t + 1, Bk)
+            gam = gamma_rows_e4m3(qb, kb, [t], d_I) if fp8 else gamma_rows(bf16_to_f64(qb), bf16_to_f64(kb), [t], d_I)
+            rep = compare_sets(g_b, ora, kth, S=S, gamma=gam, rows=[t], Bk=Bk)
+        reps.append(rep)
+    return _sum_reports(reps), ora_all
+
+
+def decode_attn_check(out_gpu, lse_gpu, gpu_blk, q_t, kv_rows, ctx_len, Bk, scale):
+    """out [B, H_q, d] and lse [B, H_q] (float64) of a decode step against the oracle's attention on the GPU's
+    own block sets, for every (sequence, head).  kv_rows(b) gives sequence b's (k_cache, v_cache) rows
+    [ctx, H_kv, d] as bf16 bit patterns; only the rows of the GPU's blocks are read."""
+    import oracle
+    B = gpu_blk.shape[0]
+    refs, lrefs = [], []
+    for b in range(B):
+        t = int(ctx_len[b]) - 1
+        kc, vc = kv_rows(b)
+        ref, ref_lse = oracle.sparse_attn(q_t[b:b + 1], kc, vc, gpu_blk[b][:, None, :], [t], Bk, scale)
+        refs.append(ref)
+        lrefs.append(ref_lse)
+    return compare_attn(out_gpu, lse_gpu, np.concatenate(refs), np.concatenate(lrefs))

@@ -202,3 +202,21 @@ def test_bwd_workspace_teacher_is_slab_bounded(lib):
     # below one slab the teacher grows with N as well
     small = (ws(65536) - ws(32768)) / 32768
     assert small > per_pos + 8 * 16 * 128 * 2 * 0.9
+
+
+def test_decode_noalloc_size_edge(lib):
+    """msa_decode_noalloc takes its scratch from a fixed 8 MiB array.  Its size check is msa_decode_workspace:
+    the first batch past the edge is rejected before any launch (the batch at the edge runs on the GPU in
+    tests/test_zz_no_alloc.py), and the sizes cross the edge between those two batches."""
+    raw = lib.raw()
+    limit = 8 << 20
+    s = lib.shape(1024, 64, 8, 128, 128, 128, 32)
+    sizes = {B: lib.msa_decode_workspace(B, s) for B in range(1, 33)}
+    b_max = max(B for B, n in sizes.items() if n <= limit)
+    assert all(sizes[B] <= limit for B in range(1, b_max + 1))
+    assert sizes[b_max] <= limit < sizes[b_max + 1]
+    status = raw.msa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, b_max + 1, ctypes.byref(s), 0.1, FAKE, None,
+                                    None, None)
+    assert status == lib.MSA_ERR_WORKSPACE_TOO_SMALL
+    assert raw.msa_decode_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, ctypes.byref(s), 0.1, FAKE, None, None,
+                                  None) == lib.MSA_ERR_INVALID_ARGUMENT

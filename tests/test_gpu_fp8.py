@@ -8,8 +8,8 @@ import torch
 
 import datagen
 import oracle
-from parity import (bf16_tensor_to_f64, check_set_invariants, compare_attn, compare_sets, e4m3_codes,
-                    gamma_rows_e4m3)
+from parity import (bf16_tensor_to_f64, check_set_invariants, compare_attn, compare_sets, decode_attn_check,
+                    decode_sets_check, e4m3_codes, gamma_rows_e4m3)
 
 pytestmark = pytest.mark.gpu
 
@@ -71,7 +71,7 @@ def _select_fp8(msa, q8, k8, N, G, d_I, Bk, k):
 
 
 @pytest.mark.parametrize("case", SELECT_CASES, ids=[c[0] for c in SELECT_CASES])
-def test_select_fp8_parity(msa, case):
+def test_select_fp8_parity(msa, case, parity_log):
     name, N, H_q, H_kv, d, d_I, Bk, k, m = case
     cfg = datagen.make_config(name, N=N, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k, needles=m)
     inp = datagen.prefill_host(cfg, want=("q_idx", "k_idx"))
@@ -82,7 +82,7 @@ def test_select_fp8_parity(msa, case):
     ora, kth = oracle.select_blocks_e4m3(q8, k8, rows, N, Bk, k)
     S = oracle.block_scores_e4m3(q8, k8, rows, N, Bk)
     rep = compare_sets(gpu, ora, kth, S=S, gamma=gamma_rows_e4m3(q8, k8, rows, d_I), rows=rows, Bk=Bk)
-    print(name, rep)
+    parity_log(name, sets=rep)
     nd = inp["needles"]
     if nd.m:
         masks = datagen.pick_masks(cfg, nd, rows, rows, datagen.TID["pick"])
@@ -140,7 +140,7 @@ def _decode_oracle_sets(q8, k8, ctx_len, Bk, k):
 
 
 @pytest.mark.parametrize("case", DECODE_CASES, ids=[c[0] for c in DECODE_CASES])
-def test_decode_fp8_parity(msa, case):
+def test_decode_fp8_parity(msa, case, parity_log):
     name, B, C, H_q, H_kv, d, d_I, Bk, k, m, ctx_len = case
     cfg = datagen.make_config(name, kind="decode", B=B, ctx=C, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k,
                               needles=m)
@@ -158,16 +158,11 @@ def test_decode_fp8_parity(msa, case):
     assert msa.msa_check_device_error(ws) == 0
     gpu_blk = blk.cpu().numpy()
     check_set_invariants(gpu_blk.transpose(1, 0, 2), ctx_len - 1, Bk, k)
-    ora_blk, kth = _decode_oracle_sets(q8, k8, ctx_len, Bk, k)
-    rep = compare_sets(gpu_blk.transpose(1, 0, 2), ora_blk.transpose(1, 0, 2), kth.transpose(1, 0, 2))
-    print(name, rep)
-    # attention on the GPU's sets, row by row
-    o, l = bf16_tensor_to_f64(out), lse.cpu().numpy().astype(np.float64)
-    for b in range(B):
-        t = int(ctx_len[b]) - 1
-        ref, ref_lse = oracle.sparse_attn(inp["q_t"][b:b + 1], inp["k_cache"][b], inp["v_cache"][b],
-                                          gpu_blk[b][:, None, :], [t], Bk, scale)
-        compare_attn(o[b:b + 1], l[b:b + 1], ref, ref_lse)
+    rep, ora_blk = decode_sets_check(gpu_blk, q8, k8, ctx_len, Bk, k, fp8=True)
+    np.testing.assert_array_equal(ora_blk, _decode_oracle_sets(q8, k8, ctx_len, Bk, k)[0])
+    rep_a = decode_attn_check(bf16_tensor_to_f64(out), lse.cpu().numpy().astype(np.float64), gpu_blk, inp["q_t"],
+                              lambda b: (inp["k_cache"][b], inp["v_cache"][b]), ctx_len, Bk, scale)
+    parity_log(name, sets=rep, attn=rep_a)
     nd = inp["needles"]
     for b in range(B):
         mk = datagen.pick_masks(cfg, nd, [b], [ctx_len[b] - 1], datagen.TID["pick_t"], s=b)[0]
@@ -178,7 +173,10 @@ def test_decode_fp8_parity(msa, case):
 
 
 @pytest.mark.parametrize("page", [16, 128])
-def test_decode_paged_fp8_equals_contiguous(msa, page):
+def test_decode_paged_fp8_equals_contiguous(msa, page, parity_log):
+    """msa_decode_paged_fp8 on randomly paged pools equals msa_decode_fp8 on the contiguous caches bit for bit,
+    and its results meet the oracle on the logical caches (sets under the set contract, out/lse on the GPU's
+    own sets)."""
     B, C, H_q, H_kv, d, d_I, Bk, k = 3, 4096, 16, 4, 128, 128, 128, 8
     cfg = datagen.make_config("f8_paged", kind="decode", B=B, ctx=C, H_q=H_q, H_kv=H_kv, d=d, d_I=d_I, Bk=Bk, k=k,
                               needles=2)
@@ -217,3 +215,10 @@ def test_decode_paged_fp8_equals_contiguous(msa, page):
         res.append((out.view(torch.int16).cpu(), lse.cpu(), blk.cpu()))
     for a, b in zip(*res):
         assert torch.equal(a, b)
+    p_out, p_lse, p_blk = res[1]
+    gpu_blk = p_blk.numpy()
+    check_set_invariants(gpu_blk.transpose(1, 0, 2), ctx_len - 1, Bk, k)
+    rep, _ = decode_sets_check(gpu_blk, q8, k8, ctx_len, Bk, k, fp8=True)
+    rep_a = decode_attn_check(p_out.view(torch.bfloat16).double().numpy(), p_lse.double().numpy(), gpu_blk,
+                              inp["q_t"], lambda b: (inp["k_cache"][b], inp["v_cache"][b]), ctx_len, Bk, scale)
+    parity_log("f8_paged_%d" % page, sets=rep, attn=rep_a)
