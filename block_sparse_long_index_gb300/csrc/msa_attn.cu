@@ -102,43 +102,101 @@ __global__ void __launch_bounds__(1024) sched_scan_kernel(const int32_t* __restr
   if (tid == blockDim.x - 1) off[n] = run;
 }
 
-// Record of every tile: 16 threads per tile, thread pp fills position pp.
-__global__ void __launch_bounds__(256) tile_records_kernel(const int32_t* __restrict__ tile_off,
-                                                           const int32_t* __restrict__ lo,
-                                                           const int32_t* __restrict__ cnt,
-                                                           const int32_t* __restrict__ entries, int64_t N, int k,
-                                                           int64_t nb, int64_t n_gb, int64_t max_tiles,
-                                                           TileRecord* __restrict__ rec) {
-  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t tile = gt / kTilePos;
-  const int pp = (int)(gt % kTilePos);
-  const int32_t total = tile_off[n_gb];
-  if (tile >= total || tile >= max_tiles) return;
-  // the last (g, b) whose first tile is <= tile: its list is not empty
-  int64_t l = 0, h = n_gb;
-  while (h - l > 1) {
-    const int64_t m = (l + h) >> 1;
-    if (tile_off[m] <= tile) l = m; else h = m;
+// The last index i in [0, n) with a[i] <= x, for a non-decreasing a with
+// a[0] <= x: a 32-ary search by one warp (each step samples 32 points and
+// narrows the range 32-fold), so 8192 lists take three dependent loads.
+__device__ __forceinline__ int64_t warp_last_le(const int32_t* __restrict__ a, int64_t n, int64_t x, int lane) {
+  int64_t lo = 0, hi = n;  // a[lo] <= x; the answer lies in [lo, hi)
+  while (hi - lo > 1) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t i = lo + (int64_t)lane * step;
+    const unsigned m = __ballot_sync(0xffffffffu, i < hi && (int64_t)a[i] <= x);
+    const int64_t nlo = lo + (int64_t)(31 - __clz(m)) * step;  // bit 0 is set: a[lo] <= x
+    hi = min(hi, nlo + step);
+    lo = nlo;
   }
-  const int64_t gb = l;
-  const int g = (int)(gb / nb);
-  const int32_t first = lo[gb] + (int32_t)(tile - tile_off[gb]) * kTilePos;
-  const int count = min(kTilePos, lo[gb] + cnt[gb] - first);
-  TileRecord& r = rec[tile];
-  if (pp == 0) {
-    r.gb = (int32_t)gb;
-    r.g = g;
-    r.b = (int32_t)(gb % nb);
-    r.count = count;
+  return lo;
+}
+
+// Records of the tiles: persistent CTAs, each over a contiguous range [a, z)
+// of the tile list.  Warp 0 finds the (g, b) lists that hold the range's first
+// and last tile; the warps then note, in shared memory, the (g, b) of every
+// tile of the range (a warp per list, lanes over its tiles); finally every
+// thread fills (tile, position) items, 16 PPR per tile, four items at a time
+// with all their loads issued before any store.
+constexpr int kRecThreads = 256;
+constexpr int kRecUnroll = 4;
+template <int PPR>
+__global__ void __launch_bounds__(kRecThreads) tile_records_kernel(const int32_t* __restrict__ tile_off,
+                                                                  const int32_t* __restrict__ lo,
+                                                                  const int32_t* __restrict__ cnt,
+                                                                  const int32_t* __restrict__ entries, int64_t N,
+                                                                  int k, int64_t nb, int64_t n_gb, int64_t max_tiles,
+                                                                  TileRecord* __restrict__ rec) {
+  constexpr int P = kTilePositions * PPR;
+  extern __shared__ int32_t tab[];  // (g, b) of each tile of this CTA's range
+  __shared__ int64_t range_gb[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t total = min((int64_t)tile_off[n_gb], max_tiles);
+  const int64_t a = total * blockIdx.x / gridDim.x, z = total * (blockIdx.x + 1) / gridDim.x;
+  if (a >= z) return;
+  if (warp == 0) {
+    const int64_t g0 = warp_last_le(tile_off, n_gb, a, lane);
+    const int64_t g1 = warp_last_le(tile_off, n_gb, z - 1, lane);
+    if (lane == 0) {
+      range_gb[0] = g0;
+      range_gb[1] = g1;
+    }
   }
-  int32_t t = -1, slot = 0;
-  if (pp < count) {
-    const int32_t e = entries[(int64_t)g * N * k + first + pp];
-    t = e / k;
-    slot = e - t * k;
+  __syncthreads();
+  const int64_t g0 = range_gb[0], g1 = range_gb[1];
+  for (int64_t gb = g0 + warp; gb <= g1; gb += kRecThreads / 32) {
+    const int64_t f = max((int64_t)tile_off[gb], a), l = min((int64_t)tile_off[gb + 1], z);
+    for (int64_t t = f + lane; t < l; t += 32) tab[t - a] = (int32_t)gb;
   }
-  r.t[pp] = t;
-  r.slot[pp] = (uint8_t)slot;
+  __syncthreads();
+  const int items = (int)(z - a) * P;  // at most 8192 tiles of 128 positions per CTA
+  for (int it0 = tid; it0 < items; it0 += kRecThreads * kRecUnroll) {
+    int32_t gbv[kRecUnroll], first[kRecUnroll], ctot[kRecUnroll], e[kRecUnroll];
+#pragma unroll
+    for (int u = 0; u < kRecUnroll; ++u) {
+      const int it = it0 + u * kRecThreads;
+      const int tl = it / P, q = it % P;
+      gbv[u] = it < items ? tab[tl] : 0;
+      const int64_t gb = gbv[u];
+      first[u] = lo[gb] + (int32_t)(a + tl - tile_off[gb]) * P;
+      ctot[u] = min(P, lo[gb] + cnt[gb] - first[u]);
+      e[u] = (it < items && q < ctot[u]) ? entries[(gb / nb) * N * k + first[u] + q] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kRecUnroll; ++u) {
+      const int it = it0 + u * kRecThreads;
+      if (it >= items) break;
+      const int tl = it / P, q = it % P;
+      const int sub = q / kTilePositions, pp = q % kTilePositions;
+      TileRecord& r = rec[(a + tl) * PPR + sub];
+      if (pp == 0) {
+        r.gb = gbv[u];
+        r.g = (int32_t)(gbv[u] / nb);
+        r.b = (int32_t)(gbv[u] % nb);
+        r.count = max(0, min(kTilePositions, ctot[u] - sub * kTilePositions));
+      }
+      const int32_t t = e[u] >= 0 ? e[u] / k : -1;
+      r.t[pp] = t;
+      r.slot[pp] = (uint8_t)(e[u] >= 0 ? e[u] - t * k : 0);
+    }
+  }
+}
+
+// Grid of the record kernel: enough CTAs that one CTA's table of tiles stays
+// within 32 KB of shared memory.
+static int64_t records_grid(int64_t max_tiles, int64_t& tab_bytes) {
+  int64_t grid = (int64_t)num_sms() * 4;
+  const int64_t need = ceil_div(max_tiles, 8192);
+  if (grid < need) grid = need;
+  if (grid < 1) grid = 1;
+  tab_bytes = (ceil_div(max_tiles, grid) + 1) * 4;
+  return grid;
 }
 
 // ---------------------------------------------------------------- combine
@@ -314,7 +372,7 @@ static size_t carve(const AttnPlan& p, void* base, AttnScratch* out) {
   s.cnt = (int32_t*)take((size_t)G * p.nb * 4);
   s.tiles = (int32_t*)take((size_t)G * p.nb * 4);
   s.tile_off = (int32_t*)take(((size_t)G * p.nb + 1) * 4);
-  s.rec = (TileRecord*)take((size_t)p.max_tiles * sizeof(TileRecord));
+  s.rec = (TileRecord*)take((size_t)p.max_tiles * p.ppr * sizeof(TileRecord));
   s.part_o = (uint16_t*)take((size_t)p.slab * p.k * p.H_q * p.d * 2);
   s.part_ml = (float2*)take((size_t)p.slab * p.k * p.H_q * 8);
   if (out) *out = s;
@@ -339,22 +397,27 @@ AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k) {
   if (cap > 131072) cap = 131072;
   if (cap < 1024) cap = 1024;
   p.slab = N < cap ? N : cap;
-  // sum over (g, b) of ceil(cnt / 16) <= entries / 16 + lists
-  p.max_tiles = (int64_t)H_kv * ceil_div(p.slab * k, kTilePos) + (int64_t)H_kv * p.nb;
+  p.ppr = 8 / p.gs;  // gs in {1, 2, 4, 8}
+  // sum over (g, b) of ceil(cnt / P) <= entries / P + lists, P = 16 ppr positions per tile
+  p.max_tiles = (int64_t)H_kv * ceil_div(p.slab * k, (int64_t)kTilePos * p.ppr) + (int64_t)H_kv * p.nb;
   return p;
 }
 
 size_t attn_scratch_bytes(const AttnPlan& p) { return carve(p, nullptr, nullptr); }
 
 cudaError_t launch_tile_schedule(const int32_t* row_ptr, const int32_t* entries, int64_t N, int G, int k, int64_t nb,
-                                 int64_t T0, int64_t T1, int64_t max_tiles, int32_t* lo, int32_t* cnt,
+                                 int64_t T0, int64_t T1, int64_t max_tiles, int ppr, int32_t* lo, int32_t* cnt,
                                  int32_t* tiles, int32_t* tile_off, TileRecord* rec, cudaStream_t s) {
   const int64_t n_gb = (int64_t)G * nb;
-  sched_count_kernel<<<(unsigned)((n_gb + 255) / 256), 256, 0, s>>>(row_ptr, entries, N, G, k, nb, T0, T1, kTilePos,
-                                                                    lo, cnt, tiles);
+  sched_count_kernel<<<(unsigned)((n_gb + 255) / 256), 256, 0, s>>>(row_ptr, entries, N, G, k, nb, T0, T1,
+                                                                    kTilePos * ppr, lo, cnt, tiles);
   sched_scan_kernel<<<1, 1024, 0, s>>>(tiles, n_gb, tile_off);
-  tile_records_kernel<<<(unsigned)ceil_div(max_tiles * kTilePos, 256), 256, 0, s>>>(tile_off, lo, cnt, entries, N, k,
-                                                                                    nb, n_gb, max_tiles, rec);
+  int64_t tab_bytes = 0;
+  const int64_t grid = records_grid(max_tiles, tab_bytes);
+  auto rk = ppr == 1 ? tile_records_kernel<1> : ppr == 2 ? tile_records_kernel<2>
+            : ppr == 4 ? tile_records_kernel<4> : tile_records_kernel<8>;
+  rk<<<(unsigned)grid, kRecThreads, (size_t)tab_bytes, s>>>(tile_off, lo, cnt, entries, N, k, nb, n_gb, max_tiles,
+                                                            rec);
   return cudaGetLastError();
 }
 
@@ -373,15 +436,12 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
   const int G = p.H_kv;
   cudaError_t e = launch_invert(block_idx, p.N, G, p.Bk, p.k, sc.row_ptr, sc.entries, sc.n_entries, sc.inv, st, s);
   if (e != cudaSuccess) return e;
-  const int64_t n_gb = (int64_t)G * p.nb;
   for (int64_t T0 = 0; T0 < p.N; T0 += p.slab) {
     const int64_t T1 = T0 + p.slab < p.N ? T0 + p.slab : p.N;
-    sched_count_kernel<<<(unsigned)((n_gb + 255) / 256), 256, 0, s>>>(sc.row_ptr, sc.entries, p.N, G, p.k, p.nb, T0,
-                                                                      T1, kTilePos, sc.lo, sc.cnt, sc.tiles);
-    sched_scan_kernel<<<1, 1024, 0, s>>>(sc.tiles, n_gb, sc.tile_off);
-    tile_records_kernel<<<(unsigned)ceil_div(p.max_tiles * kTilePos, 256), 256, 0, s>>>(
-        sc.tile_off, sc.lo, sc.cnt, sc.entries, p.N, p.k, p.nb, n_gb, p.max_tiles, sc.rec);
-    e = launch_attn_tiles(q, k, v, sc.rec, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb, p.gs, T0,
+    e = launch_tile_schedule(sc.row_ptr, sc.entries, p.N, G, p.k, p.nb, T0, T1, p.max_tiles, p.ppr, sc.lo, sc.cnt,
+                             sc.tiles, sc.tile_off, sc.rec, s);
+    if (e != cudaSuccess) return e;
+    e = launch_attn_tiles(q, k, v, sc.rec, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb, p.gs, p.ppr, T0,
                           p.slab * p.k, p.max_tiles, scale, sc.part_o, sc.part_ml, st, s);
     if (e != cudaSuccess) return e;
     const CombineSmem lay = combine_smem(p.k, p.H_q, G);

@@ -5,9 +5,10 @@
 // queries that chose a KV block are concatenated into one large MMA that
 // reuses the block from on-chip memory; hot blocks pre-chunked into tiles).
 //
-// A tile is (group g, block b, up to 16 query positions that chose b).  Its
-// 128 MMA rows are (position pp, head slot hh) -> row 8 pp + hh; head slots
-// hh >= gs are padding (never loaded, never stored).  Per tile:
+// A tile is (group g, block b, up to P = 16 ppr query positions that chose
+// b), ppr = 8 / gs: its 128 MMA rows are (position pp, head hh < gs) -> row
+// gs pp + hh, so every row is a real (position, head) whatever the group
+// size, and one 8-row swizzle atom holds ppr positions.  Per tile:
 //   S = Q K_b^T (128 x Bk fp32 in TMEM), causal mask j <= t, row max m and
 //   P = 2^(s log2e / sqrt(d) - m) (bf16, each half of the keys written back
 //   over the first columns of that half of S),
@@ -15,11 +16,12 @@
 //   row's un-normalised O goes out in bf16 and its (m, l = sum P) in fp32, so
 //   the combine divides once per (t, h) by the merged sum.
 // Roles (512 threads):
-//   warp 3        copies each tile's 128-byte record (query positions, slots)
-//                 from the schedule into an 8-slot shared ring;
-//   warp 0        Q loader: gathers a tile's Q rows with one TMA box per
-//                 position (8 heads x d, as d/64 swizzled 1 KB atoms) into one
-//                 of three position-major, 128B-swizzled K-major Q buffers;
+//   warp 3        copies each tile's ppr 128-byte records (query positions,
+//                 slots) from the schedule into an 8-slot shared ring;
+//   warp 0        Q loader: gathers a tile's Q rows with TMA boxes per
+//                 position (gs heads x 64 dims, or all 8 heads x d in one box
+//                 when gs = 8) into one of three position-major,
+//                 128B-swizzled K-major Q buffers;
 //   warp 1        TMEM owner; lane 0 issues tcgen05.mma.  S/P and O have two
 //                 TMEM buffers each, so S runs one tile ahead of P V and the
 //                 epilogue drains O(i-1) while PV(i) runs: per tile i it issues
@@ -31,6 +33,9 @@
 //   warps 12..15  epilogue warpgroup: O -> bf16 in a swizzled shared tile of
 //                 the same layout, written out by TMA stores (one box per
 //                 position when gs = 8, one per 64 dims otherwise).
+// A position's gs rows of an atom sit at byte (pp % ppr) gs 128 of atom
+// pp / ppr; TMA applies the 128-byte swizzle by shared-memory address, so a
+// box of gs rows written there lands exactly where the 8-row atom has them.
 // Buffer reuse needs no extra waits: S(j) is issued after PV(j-2) (tensor
 // core operations run in issue order), and each barrier phase a role waits
 // for cannot be overtaken by the next one (the next use of a buffer depends,
@@ -67,9 +72,9 @@ constexpr int kEpiWarps = 4;
 constexpr int kMetaReaders = 1 + 1 + 1 + 2 * kSoftWarps + 1;
 static_assert(kPosT == kTilePositions, "tile records hold 16 positions");
 
-// Q and O tiles in shared memory are position-major: position pp holds its
-// d/64 chunks of 8 rows x 128 bytes (one 128B-swizzle atom each) in
-// POS_BYTES, so rows 8pp..8pp+7 of K-chunk c sit at pp * POS_BYTES + c * 1024.
+// Q and O tiles in shared memory are atom-major: 8-row group a (ppr positions)
+// holds its d/64 chunks of 8 rows x 128 bytes (one 128B-swizzle atom each) in
+// POS_BYTES, so rows 8a..8a+7 of K-chunk c sit at a * POS_BYTES + c * 1024.
 template <int D, int BK>
 struct AttnLayout {
   static constexpr int NCD = D / 64;                // 64-column chunks of d
@@ -185,19 +190,25 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   return d;
 }
 
-template <int D, int BK>
+// PPR = 8 / gs records (of 16 positions) per tile, a compile-time constant so
+// that each group size gets its own straight-line code.
+template <int D, int BK, int PPR>
 __global__ void __launch_bounds__(kThreadsT, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_po,
                    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t max_tiles,
-                   int H_q, int H_kv, int k, int64_t nb, int gs, int q_box_heads, int64_t T0, float scale_log2,
+                   int H_q, int H_kv, int k, int64_t nb, int64_t T0, float scale_log2,
                    float2* __restrict__ part_ml, DeviceStatus* st) {
   using L = AttnLayout<D, BK>;
+  constexpr int GS = 8 / PPR;                  // heads per group = rows per position
+  constexpr int P = kTilePositions * PPR;      // positions per tile
+  constexpr int GS_SHIFT = GS == 8 ? 3 : GS == 4 ? 2 : GS == 2 ? 1 : 0;
+  constexpr int LANE_POS = (P + 31) / 32;      // positions per lane in the Q loader
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ TileRecord meta[kMeta];
+  __shared__ TileRecord meta[kMeta * PPR];  // slot i: records [i PPR, (i + 1) PPR)
   __shared__ float ex_m[2][kRowsT], ex_l[2][kRowsT];  // softmax halves: row maxima and partial sums
 
   const uint32_t sbase = smem_u32(smem);
@@ -215,8 +226,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   auto meta_empty = [&](int i) { return bar0 + 8u * (19 + kMeta + i); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Head slots >= gs of the Q buffers are never loaded: zero them (and the
-  // rest) once so that the padding rows of S stay finite.
+  // Rows of positions past a tile's count keep whatever an earlier tile left
+  // there: zero the Q buffers once so that those rows of S stay finite.
   for (int i = tid; i < kQBufs * L::Q_BYTES / 16; i += kThreadsT)
     reinterpret_cast<uint4*>(smem + L::OFF_Q)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
@@ -273,8 +284,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       for (int i = 0; i < n && ok; ++i) {
         const int ms_ = i % kMeta;
         if (!(ok = mbar_wait(meta_empty(ms_), ((i / kMeta) & 1) ^ 1, abort, st, 0x300))) break;
-        mbar_arrive_expect_tx(meta_full(ms_), (uint32_t)sizeof(TileRecord));
-        bulk_load(smem_u32(&meta[ms_]), rec + t_begin + i, (uint32_t)sizeof(TileRecord), meta_full(ms_));
+        mbar_arrive_expect_tx(meta_full(ms_), (uint32_t)(PPR * sizeof(TileRecord)));
+        bulk_load(smem_u32(&meta[ms_ * PPR]), rec + (t_begin + i) * PPR, (uint32_t)(PPR * sizeof(TileRecord)),
+                  meta_full(ms_));
         issued = i + 1;
       }
       // after an abort: wait for the copies still in flight before the CTA exits
@@ -289,24 +301,38 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     for (int i = 0; i < n && ok; ++i) {
       const int ms_ = i % kMeta;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x400)))) break;
-      const int count = meta[ms_].count, g = meta[ms_].g;
-      const int32_t t = lane < count ? meta[ms_].t[lane] : -1;
+      const TileRecord* mt = &meta[ms_ * PPR];
+      const int g = mt[0].g;
+      int count = 0;
+#pragma unroll
+      for (int r = 0; r < PPR; ++r) count += mt[r].count;
+      int32_t tl[LANE_POS];  // this lane's positions pp = lane + 32 j
+#pragma unroll
+      for (int j = 0; j < LANE_POS; ++j) {
+        const int pp = lane + 32 * j;
+        tl[j] = -1;
+        if (pp < P && (pp & 15) < mt[pp >> 4].count) tl[j] = mt[pp >> 4].t[pp & 15];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(meta_empty(ms_));
       const int qb = i % kQBufs;
       int w = 1;
       if (lane == 0) {
         w = mbar_wait(q_empty(qb), ((i / kQBufs) & 1) ^ 1, abort, st, 0x401) ? 1 : 0;
-        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(count * L::NCD * q_box_heads * 128));
+        if (w) mbar_arrive_expect_tx(q_full(qb), (uint32_t)(count * L::NCD * GS * 128));
       }
       if (!(ok = __shfl_sync(0xffffffffu, w, 0) != 0)) break;
-      if (t >= 0) {  // heads g*gs .. g*gs + q_box_heads - 1 (past H_q: zero fill)
-        const uint32_t dst = sbase + L::OFF_Q + qb * L::Q_BYTES + lane * L::POS_BYTES;
-        if (q_box_heads == 8) {  // all d/64 atoms in one box
-          tma_load_4d(dst, &tmap_q, 0, g * gs, 0, t, q_full(qb));
-        } else {                 // fewer than 8 heads: one box per atom
 #pragma unroll
-          for (int c = 0; c < L::NCD; ++c) tma_load_4d(dst + c * 1024, &tmap_q, 0, g * gs, c, t, q_full(qb));
+      for (int j = 0; j < LANE_POS; ++j) {
+        const int pp = lane + 32 * j;
+        if (tl[j] < 0) continue;
+        // heads g*GS .. g*GS + GS - 1 of position tl[j] -> rows GS pp .. GS pp + GS - 1
+        const uint32_t dst = sbase + L::OFF_Q + qb * L::Q_BYTES + (pp / PPR) * L::POS_BYTES + (pp % PPR) * GS * 128;
+        if (GS == 8) {  // all d/64 atoms in one box
+          tma_load_4d(dst, &tmap_q, 0, g * GS, 0, tl[j], q_full(qb));
+        } else {        // one box of GS rows per atom
+#pragma unroll
+          for (int c = 0; c < L::NCD; ++c) tma_load_4d(dst + c * 1024, &tmap_q, 0, g * GS, c, tl[j], q_full(qb));
         }
       }
       issued = i + 1;
@@ -325,9 +351,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       for (int i = 0; i < n && ok; ++i) {
         const int ms_ = i % kMeta;
         if (!(ok = mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x403))) break;
-        const int64_t gb = meta[ms_].gb;
-        const int g = meta[ms_].g;
-        const int32_t b = meta[ms_].b;
+        const int64_t gb = meta[ms_ * PPR].gb;
+        const int g = meta[ms_ * PPR].g;
+        const int32_t b = meta[ms_ * PPR].b;
         mbar_arrive(meta_empty(ms_));
         if (gb == prev) continue;
         prev = gb;
@@ -356,7 +382,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       auto gb_of = [&](int j, int32_t& out) -> bool {
         for (; fetched <= j; ++fetched)
           if (!mbar_wait(meta_full(fetched % kMeta), (fetched / kMeta) & 1, abort, st, 0x500)) return false;
-        out = meta[j % kMeta].gb;
+        out = meta[(j % kMeta) * PPR].gb;
         return true;
       };
       int s_next = 0;  // next tile whose S is not issued
@@ -433,15 +459,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const int pos = row >> 3, hh = row & 7;
+    const int pos = row >> GS_SHIFT, hh = row & (GS - 1);
     const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
     for (int j = 0; j < n; ++j) {
       const int ms_ = j % kMeta;
       const bool w1 = mbar_wait(meta_full(ms_), (j / kMeta) & 1, abort, st, 0x600);
-      const int64_t t = (w1 && hh < gs && pos < meta[ms_].count) ? meta[ms_].t[pos] : -1;
-      const int slot = meta[ms_].slot[pos];
-      const int tg = meta[ms_].g;
-      const int64_t tb = meta[ms_].b;
+      const TileRecord& sr = meta[ms_ * PPR + (pos >> 4)];
+      const int64_t t = (w1 && (pos & 15) < sr.count) ? sr.t[pos & 15] : -1;
+      const int slot = sr.slot[pos & 15];
+      const int tg = meta[ms_ * PPR].g;
+      const int64_t tb = meta[ms_ * PPR].b;
       __syncwarp();
       if (lane == 0 && w1) mbar_arrive(meta_empty(ms_));
       const int sb = j % kSBufs;
@@ -451,7 +478,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       // (rows without output count as unmasked so that a warp takes the
       // masked path only where a real row needs it; TMEM loads are
       // warp-collective).
-      const int64_t prow = t >= 0 ? ((t - T0) * k + slot) * H_q + (int64_t)tg * gs + hh : 0;
+      const int64_t prow = t >= 0 ? ((t - T0) * k + slot) * H_q + (int64_t)tg * GS + hh : 0;
       const int64_t key0 = tb * BK + half * HW;
       const int lim = t < 0 ? HW - 1 : (int)max((int64_t)-1, min((int64_t)HW - 1, t - key0));
       const bool full = __all_sync(0xffffffffu, lim == HW - 1);
@@ -599,17 +626,26 @@ __global__ void __launch_bounds__(kThreadsT, 1)
         int w = 1;
         if (lane == 0) w = mbar_wait(meta_full(ms_), (i / kMeta) & 1, abort, st, 0x702) ? 1 : 0;
         lead_ok = __shfl_sync(0xffffffffu, w, 0) != 0;
-        const TileRecord& mt = meta[ms_];
-        if (lead_ok && lane < mt.count) {
-          const int32_t z = (int32_t)((mt.t[lane] - T0) * k + mt.slot[lane]);
-          const uint32_t src = stg + lane * L::POS_BYTES;
-          if (gs == 8) {  // the position's 8 heads x d in one box
-            tma_store_4d(&tmap_po, src, 0, mt.g * 8, 0, z);
-          } else {        // gs heads of each 64-dim chunk
+        const TileRecord* mt = &meta[ms_ * PPR];
+        if (lead_ok) {
+          const int g = mt[0].g;
+          bool any = false;
 #pragma unroll
-            for (int c = 0; c < L::NCD; ++c) tma_store_4d(&tmap_po, src + c * 1024, 0, mt.g * gs, c, z);
+          for (int j = 0; j < LANE_POS; ++j) {
+            const int pp = lane + 32 * j;
+            if (pp >= P || (pp & 15) >= mt[pp >> 4].count) continue;
+            const TileRecord& sr = mt[pp >> 4];
+            const int32_t z = (int32_t)((sr.t[pp & 15] - T0) * k + sr.slot[pp & 15]);
+            const uint32_t src = stg + (pp / PPR) * L::POS_BYTES + (pp % PPR) * GS * 128;
+            if (GS == 8) {  // the position's 8 heads x d in one box
+              tma_store_4d(&tmap_po, src, 0, g * 8, 0, z);
+            } else {        // GS heads of each 64-dim chunk
+#pragma unroll
+              for (int c = 0; c < L::NCD; ++c) tma_store_4d(&tmap_po, src + c * 1024, 0, g * GS, c, z);
+            }
+            any = true;
           }
-          bulk_commit();
+          if (any) bulk_commit();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(meta_empty(ms_));
@@ -625,9 +661,9 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
 }
 
-template <int D, int BK>
+template <int D, int BK, int PPR>
 cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRecord* rec, const int32_t* tile_off,
-                     int64_t N, int H_q, int H_kv, int k, int64_t nb, int gs, int64_t T0, int64_t rows,
+                     int64_t N, int H_q, int H_kv, int k, int64_t nb, int gs, int ppr, int64_t T0, int64_t rows,
                      int64_t max_tiles, float scale, uint16_t* part_o, float2* part_ml, DeviceStatus* st,
                      cudaStream_t s) {
   using L = AttnLayout<D, BK>;
@@ -635,11 +671,10 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
   const uint64_t row_bytes = (uint64_t)D * 2;
   // Q and partial O as [rows][H_q][d/64][64] viewed in the order {64, H_q, d/64, rows}: a box
   // {64, heads, d/64, 1} lands as d/64 atoms of `heads` x 128 bytes, i.e. the tiles' layout.
-  const int q_box_heads = H_q < 8 ? H_q : 8;
   const uint64_t q_dims[4] = {64, (uint64_t)H_q, (uint64_t)L::NCD, (uint64_t)N};
   const uint64_t po_dims[4] = {64, (uint64_t)H_q, (uint64_t)L::NCD, (uint64_t)rows};
   const uint64_t qo_strides[3] = {row_bytes, 128, (uint64_t)H_q * row_bytes};
-  const uint32_t q_box[4] = {64, (uint32_t)q_box_heads, q_box_heads == 8 ? (uint32_t)L::NCD : 1u, 1};
+  const uint32_t q_box[4] = {64, (uint32_t)gs, gs == 8 ? (uint32_t)L::NCD : 1u, 1};
   const uint32_t po_box[4] = {64, (uint32_t)gs, gs == 8 ? (uint32_t)L::NCD : 1u, 1};
   if (!encode_tmap_4d(tq, q, q_dims, qo_strides, q_box, 128) ||
       !encode_tmap_3d(tk, kk, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, row_bytes, (uint64_t)H_kv * row_bytes, 64,
@@ -648,14 +683,14 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
                       1, BK, 128) ||
       !encode_tmap_4d(tpo, part_o, po_dims, qo_strides, po_box, 128))
     return cudaErrorInvalidValue;
-  auto kern = attn_tc_kernel<D, BK>;
+  auto kern = attn_tc_kernel<D, BK, PPR>;
   const int smem = L::SMEM > 120 * 1024 ? L::SMEM : 120 * 1024;  // one CTA per SM: TMEM is never contended
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms(), kThreadsT, smem, s>>>(
       *reinterpret_cast<const CUtensorMap*>(tq), *reinterpret_cast<const CUtensorMap*>(tk),
       *reinterpret_cast<const CUtensorMap*>(tv), *reinterpret_cast<const CUtensorMap*>(tpo), rec, tile_off,
-      max_tiles, H_q, H_kv, k, nb, gs, q_box_heads, T0, scale * 1.4426950408889634f, part_ml, st);
+      max_tiles, H_q, H_kv, k, nb, T0, scale * 1.4426950408889634f, part_ml, st);
   return cudaGetLastError();
 }
 
@@ -663,12 +698,21 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
 
 cudaError_t launch_attn_tiles(const void* q, const void* kk, const void* vv, const TileRecord* rec,
                               const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k, int64_t nb,
-                              int gs, int64_t T0, int64_t rows, int64_t max_tiles, float scale, uint16_t* part_o,
-                              float2* part_ml, DeviceStatus* st, cudaStream_t s) {
-  auto launch = d == 64 ? (Bk == 64 ? launch_t<64, 64> : launch_t<64, 128>)
-                        : (Bk == 64 ? launch_t<128, 64> : launch_t<128, 128>);
-  return launch(q, kk, vv, rec, tile_off, N, H_q, H_kv, k, nb, gs, T0, rows, max_tiles, scale, part_o, part_ml, st,
-                s);
+                              int gs, int ppr, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
+                              uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s) {
+  using Fn = cudaError_t (*)(const void*, const void*, const void*, const TileRecord*, const int32_t*, int64_t, int,
+                            int, int, int64_t, int, int, int64_t, int64_t, int64_t, float, uint16_t*, float2*,
+                            DeviceStatus*, cudaStream_t);
+  // [d == 128][Bk == 128][log2 ppr]
+  static const Fn table[2][2][4] = {
+      {{launch_t<64, 64, 1>, launch_t<64, 64, 2>, launch_t<64, 64, 4>, launch_t<64, 64, 8>},
+       {launch_t<64, 128, 1>, launch_t<64, 128, 2>, launch_t<64, 128, 4>, launch_t<64, 128, 8>}},
+      {{launch_t<128, 64, 1>, launch_t<128, 64, 2>, launch_t<128, 64, 4>, launch_t<128, 64, 8>},
+       {launch_t<128, 128, 1>, launch_t<128, 128, 2>, launch_t<128, 128, 4>, launch_t<128, 128, 8>}}};
+  const int lp = ppr == 1 ? 0 : ppr == 2 ? 1 : ppr == 4 ? 2 : 3;
+  const Fn launch = table[d == 128][Bk == 128][lp];
+  return launch(q, kk, vv, rec, tile_off, N, H_q, H_kv, k, nb, gs, ppr, T0, rows, max_tiles, scale, part_o, part_ml,
+                st, s);
 }
 
 }  // namespace msa

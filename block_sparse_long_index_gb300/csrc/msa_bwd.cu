@@ -1519,7 +1519,7 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   // positions have all their blocks in its tile list.
   for (int64_t T0 = 0; T0 < N; T0 += sc.slab) {
     const int64_t T1 = T0 + sc.slab < N ? T0 + sc.slab : N;
-    if ((e = launch_tile_schedule(sc.row_ptr, sc.entries, N, G, kb, sc.nb, T0, T1, sc.max_tiles, sc.lo, sc.cnt,
+    if ((e = launch_tile_schedule(sc.row_ptr, sc.entries, N, G, kb, sc.nb, T0, T1, sc.max_tiles, 1, sc.lo, sc.cnt,
                                   sc.tiles, sc.tile_off, sc.rec, s)) != cudaSuccess)
       return e;
     mark_repeats_kernel<<<(unsigned)ceil_div(sc.max_tiles * kPosT, 256), 256, 0, s>>>(sc.rec, sc.tile_off,

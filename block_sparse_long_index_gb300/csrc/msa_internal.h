@@ -55,10 +55,13 @@ cudaError_t launch_invert(const int32_t* block_idx, int64_t N, int G, int Bk, in
                           cudaStream_t s);
 
 // ---- attention (msa_attn.cu)
-// One attention tile of a slab's flat work list: (group g, block b) and up to
+// One record of a slab's flat work list: (group g, block b) and up to
 // kTilePositions query positions that chose b, with each position's slot in
 // its block set.  Written by the schedule, copied whole into shared memory by
-// the tile kernel (128 bytes, 16-byte aligned).
+// the tile kernels (128 bytes, 16-byte aligned).  A tile of the forward
+// attention is ppr consecutive records of one (g, b) (16 ppr positions x gs
+// heads = 128 MMA rows, ppr = 8 / gs); a record past the tile's last position
+// has count 0 and every t = -1.
 constexpr int kTilePositions = 16;
 struct alignas(16) TileRecord {
   int32_t gb;     // g * nb + b
@@ -73,21 +76,23 @@ static_assert(sizeof(TileRecord) == 128, "tile record is one 128-byte line");
 struct AttnPlan {
   int64_t N;
   int H_q, H_kv, d, Bk, k, gs;
+  int ppr;            // records (of 16 positions) per tile: 8 / gs
   int64_t nb;
   int64_t slab;       // query positions per slab
-  int64_t max_tiles;  // bound on the tiles of one slab
+  int64_t max_tiles;  // bound on the tiles of one slab (each ppr records)
 };
 AttnPlan attn_plan(int64_t N, int H_q, int H_kv, int d, int Bk, int k);
 size_t attn_scratch_bytes(const AttnPlan& p);
 // The tcgen05 tile kernel of one query slab (msa_attn_tile.cu).
 cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const TileRecord* rec,
                               const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k_blocks,
-                              int64_t nb, int gs, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
+                              int64_t nb, int gs, int ppr, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
                               uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s);
 // The flat tile list of positions [T0, T1) from the CSR (row_ptr, entries): per (g, b)
-// the list's positions cut into tiles of kTilePositions, tile_off[G*nb] = total.
+// the list's positions cut into tiles of 16 ppr positions, tile_off[G*nb] = total
+// tiles; tile i is records [i ppr, (i + 1) ppr) of rec.
 cudaError_t launch_tile_schedule(const int32_t* row_ptr, const int32_t* entries, int64_t N, int G, int k, int64_t nb,
-                                 int64_t T0, int64_t T1, int64_t max_tiles, int32_t* lo, int32_t* cnt,
+                                 int64_t T0, int64_t T1, int64_t max_tiles, int ppr, int32_t* lo, int32_t* cnt,
                                  int32_t* tiles, int32_t* tile_off, TileRecord* rec, cudaStream_t s);
 cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32_t* block_idx, const AttnPlan& p,
                         float scale, void* out, float* lse, void* scratch, DeviceStatus* st, cudaStream_t s);

@@ -8,15 +8,18 @@
 //   1. count:   per (group, chunk of positions) a shared-memory histogram;
 //   2. prefix:  per (group, block) the running sum over chunks (in place);
 //   3. scan:    per group the exclusive scan over blocks -> row_ptr;
-//   4. scatter: one warp per chunk walks its entries in order; lanes holding
-//               the same block are ranked by lane (= entry order) with
-//               __match_any_sync, so every list comes out in ascending t and
-//               the result does not depend on scheduling.
+//   4. scatter: one warp per chunk walks its block ids in order, staged in
+//               shared memory ahead of use; lanes holding the same block are
+//               ranked by lane (= entry order) with __match_any_sync, so every
+//               list comes out in ascending t and the result does not depend
+//               on scheduling.
 #include "msa_common.cuh"
 
 namespace msa {
 
 namespace {
+
+__host__ __device__ inline int64_t align_up_i(int64_t n) { return (n + 3) & ~(int64_t)3; }
 
 __global__ void inv_count_kernel(const int32_t* __restrict__ B, int64_t N, int k, int64_t nb, int chunk,
                                  int n_chunks, int32_t* __restrict__ counts, DeviceStatus* st) {
@@ -41,20 +44,35 @@ __global__ void inv_count_kernel(const int32_t* __restrict__ B, int64_t N, int k
   for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) out[b] = hist[b];
 }
 
-// counts[g][c][b] <- sum over c' < c; totals into row_ptr[g][b].
-__global__ void inv_prefix_kernel(int32_t* __restrict__ counts, int64_t nb, int n_chunks,
-                                  int32_t* __restrict__ row_ptr) {
-  const int g = blockIdx.y;
-  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (b >= nb) return;
-  int32_t run = 0;
+// counts[g][c][b] <- sum over c' < c; totals into row_ptr[g][b].  A CTA takes
+// 32 consecutive blocks of one group (lane = block, so every row of 32 counts
+// is one coalesced 128-byte access); its 8 warps split the chunk axis into
+// contiguous ranges, sum them, exchange the range totals through shared
+// memory and write the running prefix in a second pass over their range.
+constexpr int kPrefixWarps = 8;
+__global__ void __launch_bounds__(kPrefixWarps * 32) inv_prefix_kernel(int32_t* __restrict__ counts, int64_t nb,
+                                                                       int n_chunks, int32_t* __restrict__ row_ptr) {
+  __shared__ int32_t wsum[kPrefixWarps][32];
+  const int g = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t b = (int64_t)blockIdx.x * 32 + lane;
+  const int per = (n_chunks + kPrefixWarps - 1) / kPrefixWarps;
+  const int c0 = min(warp * per, n_chunks), c1 = min(c0 + per, n_chunks);
   int32_t* col = counts + (int64_t)g * n_chunks * nb + b;
-  for (int c = 0; c < n_chunks; ++c) {
-    int32_t x = col[(int64_t)c * nb];
-    col[(int64_t)c * nb] = run;
-    run += x;
+  int32_t sum = 0;
+  if (b < nb)
+    for (int c = c0; c < c1; ++c) sum += col[(int64_t)c * nb];
+  wsum[warp][lane] = sum;
+  __syncthreads();
+  int32_t run = 0;
+  for (int w = 0; w < warp; ++w) run += wsum[w][lane];
+  if (b < nb) {
+    for (int c = c0; c < c1; ++c) {
+      const int32_t x = col[(int64_t)c * nb];
+      col[(int64_t)c * nb] = run;
+      run += x;
+    }
+    if (warp == kPrefixWarps - 1) row_ptr[(int64_t)g * (nb + 1) + b] = run;
   }
-  row_ptr[(int64_t)g * (nb + 1) + b] = run;
 }
 
 // In-place exclusive scan of row_ptr[g][0..nb), row_ptr[g][nb] = total.
@@ -100,37 +118,63 @@ __global__ void __launch_bounds__(1024) inv_scan_kernel(int32_t* __restrict__ ro
   }
 }
 
+// One warp per (chunk, group), so that every chunk's warp is resident at
+// once.  The chunk's block ids are staged in shared memory kScatterSub at a
+// time, double-buffered with cp.async (the next part lands while this one is
+// ranked), so the serial ranking rounds read no global memory.
+constexpr int kScatterSub = 1024;  // entries per staging buffer
+__device__ __forceinline__ void cp_async_4(int32_t* smem_dst, const int32_t* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
 __global__ void __launch_bounds__(32) inv_scatter_kernel(const int32_t* __restrict__ B, int64_t N, int k, int64_t nb,
-                                                         int chunk, int n_chunks,
-                                                         const int32_t* __restrict__ counts,
+                                                         int chunk, int n_chunks, const int32_t* __restrict__ counts,
                                                          const int32_t* __restrict__ row_ptr,
                                                          int32_t* __restrict__ entries) {
-  extern __shared__ int32_t cursor[];
+  extern __shared__ int32_t sc_smem[];
+  int32_t* cursor = sc_smem;               // [nb]
+  int32_t* sb = sc_smem + align_up_i(nb);  // [2][kScatterSub]
   const int c = blockIdx.x, g = blockIdx.y, lane = threadIdx.x;
   const int32_t* rp = row_ptr + (int64_t)g * (nb + 1);
   const int32_t* cc = counts + ((int64_t)g * n_chunks + c) * nb;
   for (int64_t b = lane; b < nb; b += 32) cursor[b] = rp[b] + cc[b];
-  __syncwarp();
   const int64_t e0 = (int64_t)c * chunk * k;
   const int64_t e1 = min((int64_t)(c + 1) * chunk, N) * k;
   const int32_t* Bg = B + (int64_t)g * N * k;
   int32_t* Eg = entries + (int64_t)g * N * k;
   const unsigned lt_mask = (1u << lane) - 1u;
-  for (int64_t base = e0; base < e1; base += 32) {
-    int64_t e = base + lane;
-    int32_t b = (e < e1) ? Bg[e] : -1;
-    bool valid = b >= 0 && (int64_t)b < nb;
-    int key = valid ? b : -2 - lane;  // invalid lanes match nobody
-    unsigned peers = __match_any_sync(0xffffffffu, key);
-    int leader = __ffs(peers) - 1;
-    int32_t pos = 0;
-    if (valid && lane == leader) {
-      pos = cursor[b];
-      cursor[b] = pos + __popc(peers);
+  auto stage = [&](int64_t s0, int buf) {
+    const int n = (int)min((int64_t)kScatterSub, e1 - s0);
+    for (int i = lane; i < n; i += 32) cp_async_4(sb + buf * kScatterSub + i, Bg + s0 + i);
+    cp_async_commit();
+  };
+  if (e0 < e1) stage(e0, 0);
+  int buf = 0;
+  for (int64_t s0 = e0; s0 < e1; s0 += kScatterSub, buf ^= 1) {
+    if (s0 + kScatterSub < e1) {
+      stage(s0 + kScatterSub, buf ^ 1);  // that buffer's previous part was ranked last round
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    pos = __shfl_sync(0xffffffffu, pos, leader);
-    if (valid) Eg[pos + __popc(peers & lt_mask)] = (int32_t)e;
     __syncwarp();
+    const int n = (int)min((int64_t)kScatterSub, e1 - s0);
+    const int32_t* ids = sb + buf * kScatterSub;
+    for (int base = 0; base < n; base += 32) {
+      const int i = base + lane;
+      const int32_t b = i < n ? ids[i] : -1;
+      const bool valid = b >= 0 && (int64_t)b < nb;
+      const int key = valid ? b : -2 - lane;  // invalid lanes match nobody
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      const int leader = __ffs(peers) - 1;
+      int32_t pos = 0;
+      if (valid && lane == leader) {
+        pos = cursor[b];
+        cursor[b] = pos + __popc(peers);
+      }
+      pos = __shfl_sync(0xffffffffu, pos, leader);
+      if (valid) Eg[pos + __popc(peers & lt_mask)] = (int32_t)(s0 + i);
+      __syncwarp();
+    }
   }
 }
 
@@ -170,15 +214,16 @@ cudaError_t launch_invert(const int32_t* block_idx, int64_t N, int G, int Bk, in
   cudaError_t e;
   e = cudaFuncSetAttribute(inv_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(inv_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hist_bytes);
+  const size_t scatter_bytes = (size_t)(align_up_i(nb) + 2 * kScatterSub) * sizeof(int32_t);
+  e = cudaFuncSetAttribute(inv_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scatter_bytes);
   if (e != cudaSuccess) return e;
   dim3 grid_c((unsigned)sc.n_chunks, (unsigned)G);
   inv_count_kernel<<<grid_c, 256, hist_bytes, s>>>(block_idx, N, k, nb, sc.chunk, sc.n_chunks, sc.counts, st);
-  dim3 grid_p((unsigned)((nb + 255) / 256), (unsigned)G);
-  inv_prefix_kernel<<<grid_p, 256, 0, s>>>(sc.counts, nb, sc.n_chunks, row_ptr);
+  dim3 grid_p((unsigned)((nb + 31) / 32), (unsigned)G);
+  inv_prefix_kernel<<<grid_p, kPrefixWarps * 32, 0, s>>>(sc.counts, nb, sc.n_chunks, row_ptr);
   inv_scan_kernel<<<G, 1024, 0, s>>>(row_ptr, nb, n_entries);
-  inv_scatter_kernel<<<grid_c, 32, hist_bytes, s>>>(block_idx, N, k, nb, sc.chunk, sc.n_chunks, sc.counts, row_ptr,
-                                                    entries);
+  inv_scatter_kernel<<<grid_c, 32, scatter_bytes, s>>>(block_idx, N, k, nb, sc.chunk, sc.n_chunks, sc.counts, row_ptr,
+                                                       entries);
   return cudaGetLastError();
 }
 
