@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--no-other-prefill", action="store_true", help="skip the 32K and 1M prefill lines")
     ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle rows timed for cpu_baseline (about 10 s)")
     ap.add_argument("--stage", default="all", choices=["all", "select", "attend", "decode", "select_fp8",
-                                                       "decode_fp8", "warmup"],
+                                                       "decode_fp8", "warmup", "select_varlen"],
                     help="time one stage alone on --config (small-memory cases for profiler captures)")
     return ap.parse_args()
 
@@ -666,6 +666,15 @@ def run_stage(args):
                                                      ws_sel)
         elif args.stage == "select":
             call = select
+        elif args.stage == "select_varlen":  # the bench's packed sequence mix over the config's N cells
+            cu = [0]
+            for n in varlen_mix(cfg.N, cfg.Bk):
+                cu.append(cu[-1] + n)
+            cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+            wsv = torch.empty(msa.msa_select_blocks_varlen_workspace(cfg.N, cfg.G, cfg.d_I, cfg.Bk, cfg.k),
+                              dtype=torch.uint8, device="cuda")
+            call = lambda: msa.msa_select_blocks_varlen(inp["q_idx"], inp["k_idx"], cu_d, len(cu) - 1, cfg.N,  # noqa
+                                                        cfg.G, cfg.d_I, cfg.Bk, cfg.k, blk, wsv)
         else:
             select()
             shp = msa.shape(cfg.N, cfg.H_q, cfg.H_kv, cfg.d, cfg.d_I, cfg.Bk, cfg.k)

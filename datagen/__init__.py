@@ -94,6 +94,10 @@ CONFIGS = {
     # a smaller prefill case (same shapes, N = 8K) for profiler captures of a few GB
     "prefill_8k": Config("prefill_8k", "prefill", N=8192, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
                          needles=4, index=6),
+    # the 128K shapes at N = 16K: q (268 MB) is larger than L2 while the attention call holds ~5 GB, so a
+    # profiler capture of it sees DRAM traffic that scales with N to the 128K workload
+    "prefill_16k": Config("prefill_16k", "prefill", N=16384, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
+                          needles=4, index=8),
     "prefill_1m": Config("prefill_1m", "prefill", N=1 << 20, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
                          needles=16, index=4),
 }
