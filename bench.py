@@ -155,17 +155,20 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- traffic from a committed ncu summary
-def traffic_for(kernel_key, src_file):
-    """Per-launch DRAM bytes recorded in profiles/traffic.json for the given kernel source hash, else None."""
+def traffic_for(kernel_key, *src_files):
+    """Per-launch DRAM bytes recorded in profiles/traffic.json for the given kernel sources' hash, else None
+    (None as soon as any of those sources changed since the counters were taken)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         with open(p) as f:
             d = json.load(f).get(kernel_key)
-        with open(os.path.join(ROOT, src_file), "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-        if d and d.get("source_sha") == h:
+        h = hashlib.sha256()
+        for src in src_files:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if d and d.get("source_sha") == h.hexdigest()[:16]:
             return d.get("bytes_per_launch")
     except (OSError, ValueError):
         return None
@@ -748,7 +751,11 @@ def main():
     att_bw = attn_bytes / att_s / 1e9
     roofline = {"kernel": "msa_sparse_attn_fwd (B->B*, schedule, KV-outer tcgen05 tiles, LSE combine)",
                 "bound": "hbm", "achieved": att_bw, "peak": hbm, "unit": "GB/s", "frac": att_bw / hbm,
-                "traffic": None,
+                "traffic": traffic_for("attn_call_prefill_128k", "block_sparse_long_index_gb300/csrc/msa_attn.cu",
+                                       "block_sparse_long_index_gb300/csrc/msa_attn_tile.cu",
+                                       "block_sparse_long_index_gb300/csrc/msa_invert.cu"),
+                "traffic_note": "DRAM bytes of every kernel of one call captured at prefill_16k (q larger than L2) "
+                                "and scaled by 8 to 128K (all terms scale with N); null once a source changes",
                 "algorithmic": "N*G*k*gs*d*2*3 + N*G*k*gs*16 + G*nb*Bk*d*4 + G*N*k*12 + N*H_q*(2d+4)"
                                " = %d bytes per call" % attn_bytes,
                 "peak_source": "%s hbm_gbs" % peak_src}
