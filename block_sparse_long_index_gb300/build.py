@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmsa.so")
 SOURCES = ["msa_capi.cu", "msa_select.cu", "msa_invert.cu", "msa_attn.cu", "msa_attn_tile.cu", "msa_decode.cu",
-           "msa_bwd.cu", "msa_warmup.cu"]
+           "msa_bwd.cu", "msa_warmup.cu", "msa_warmup_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"] + ARCH
 

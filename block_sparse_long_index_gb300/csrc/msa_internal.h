@@ -119,6 +119,13 @@ cudaError_t launch_warmup(const void* q, const void* k, const void* v, const voi
                           int H_q, int H_kv, int d, int d_I, float scale, float kl_weight, bool fwd, bool grad,
                           void* out, float* lse, float* lseI, float* dq_idx, float* dk_idx, float* kl, cudaStream_t s);
 
+// ---- warmup mode on tcgen05 (msa_warmup_tc.cu): d = d_I = 128 and gs = 8
+bool warmup_tc_supported(int d, int d_I, int H_q, int H_kv);
+// kl, dq_idx and dk_idx are cleared here, then accumulated; st may be null.
+cudaError_t launch_warmup_grad_tc(const void* q, const void* k, const void* q_idx, const void* k_idx, int64_t N,
+                                  int H_q, int H_kv, float scale, float kl_weight, const float* lse, const float* lseI,
+                                  float* dq_idx, float* dk_idx, float* kl, DeviceStatus* st, cudaStream_t s);
+
 // ---- decode (msa_decode.cu)
 // Where token `key` of sequence `seq` sits in a decode cache: contiguous (no
 // table: row seq * ctx_max + key) or paged (row table[seq][key / page] * page +

@@ -592,6 +592,9 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* q_
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (!grad) return cudaSuccess;
+  if (warmup_tc_supported(D, DI, H_q, H_kv))  // one key-outer pass on the tensor cores
+    return launch_warmup_grad_tc(q, k, q_idx, k_idx, N, H_q, H_kv, scale, kl_weight, lse, lseI, dq_idx, dk_idx, kl,
+                                 nullptr, s);
   if ((e = cudaFuncSetAttribute(warmup_dq_kernel<D, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem)) !=
       cudaSuccess)
     return e;

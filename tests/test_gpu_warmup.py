@@ -21,6 +21,10 @@ CASES = [
     ("gs8_d128", 1000, 16, 2, 128, 128),
     ("gs1_dI64", 777, 4, 4, 128, 64),
     ("gs2_long", 2100, 8, 4, 128, 128),
+    # the tensor-core path (d = d_I = 128, gs = 8): one key tile exactly, a partial tile, ragged with 3 groups
+    ("tc_one_key_tile", 128, 8, 1, 128, 128),
+    ("tc_partial_tile", 17, 8, 1, 128, 128),
+    ("tc_ragged_g3", 3001, 24, 3, 128, 128),
 ]
 
 
