@@ -121,6 +121,10 @@ cudaError_t launch_warmup(const void* q, const void* k, const void* v, const voi
 
 // ---- warmup mode on tcgen05 (msa_warmup_tc.cu): d = d_I = 128 and gs = 8
 bool warmup_tc_supported(int d, int d_I, int H_q, int H_kv);
+// out, lse (dense causal attention) and lseI; st may be null.
+cudaError_t launch_warmup_fwd_tc(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                 int64_t N, int H_q, int H_kv, float scale, void* out, float* lse, float* lseI,
+                                 DeviceStatus* st, cudaStream_t s);
 // kl, dq_idx and dk_idx are cleared here, then accumulated; st may be null.
 cudaError_t launch_warmup_grad_tc(const void* q, const void* k, const void* q_idx, const void* k_idx, int64_t N,
                                   int H_q, int H_kv, float scale, float kl_weight, const float* lse, const float* lseI,

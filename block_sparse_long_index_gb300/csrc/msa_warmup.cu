@@ -582,7 +582,11 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* q_
   const int dq_smem = L::Q + L::QI + 2 * L::K + 2 * L::KI + L::ZI + L::DZ;
   const int dk_smem = 2 * L::Q + 2 * L::QI + L::K + L::KI + L::ZI + L::DZ;
   cudaError_t e;
-  if (fwd) {
+  if (fwd && warmup_tc_supported(D, DI, H_q, H_kv)) {  // dense attention and the index lse on the tensor cores
+    if ((e = launch_warmup_fwd_tc(q, k, v, q_idx, k_idx, N, H_q, H_kv, scale, out, lse, lseI, nullptr, s)) !=
+        cudaSuccess)
+      return e;
+  } else if (fwd) {
     if ((e = cudaFuncSetAttribute(warmup_fwd_kernel<D, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   fwd_smem)) != cudaSuccess)
       return e;

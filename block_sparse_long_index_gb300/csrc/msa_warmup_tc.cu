@@ -29,6 +29,20 @@
 // The next query tile's rows arrive by cp.async while this one computes.  The
 // main scores are computed once per (key, query) pair here; the forward pass
 // keeps its own.
+//
+// Forward, query-outer: one CTA per (query tile of 16 positions x 8 heads,
+// group), two CTAs per SM (256 TMEM columns and 96 KB each, so one CTA's MMAs
+// run while the other's softmax does), heaviest tiles first.  Per 128-key
+// tile: S = Q K^T into TMEM; both warpgroups take half of the key columns of
+// every row (row maxima and sums exchanged through shared memory) and write P
+// (bf16) back over their half of S; O += P V with P read from TMEM and V as
+// an MN-major operand.  The running maximum is lazy: O and the row sum are
+// rescaled only when a row's maximum grows by more than 2^8, so P stays below
+// 256 and the rescale of O in TMEM is rare.  The next tile's K lands while
+// the softmax runs, its V while the next S is computed.
+// Index lse: one CTA per (128 positions, group), Z = Q^I K^I^T per 128-key
+// tile into TMEM (two buffers), each thread keeps an exact online log-sum-exp
+// of its row.
 #include <math.h>
 
 #include "msa_sm100.cuh"
@@ -111,8 +125,8 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
   const uint32_t bar_s = sb + kBar, bar_q = sb + kBar + 8, bar_drain = sb + kBar + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant; positions 8 half .. 8 half + 7
-  const int g = blockIdx.x;
-  const int64_t j0 = (int64_t)blockIdx.y * kKeys;  // key tiles in launch order: the heaviest first
+  const int g = (int)(blockIdx.x % (unsigned)G);
+  const int64_t j0 = (int64_t)(blockIdx.x / (unsigned)G) * kKeys;  // launch order: the heaviest key tiles first
   if (tid == 0) {
     mbar_init(bar_s, 1);
     mbar_init(bar_q, 1);
@@ -214,7 +228,9 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
     if (qt + 1 < n_qt) issue_q(qt + 1, buf ^ 1);
     cp_async_commit();
     // ---- teacher, index probabilities, dzI and KL: thread = key, its warpgroup's 8 positions
-    if (mbar_wait(bar_s, nt & 1, abort, st, 0xA01)) {
+    // every thread takes the same branch (the TMEM loads and shuffles below are warp-collective)
+    if (!__syncthreads_and(mbar_wait(bar_s, nt & 1, abort, st, 0xA01))) break;
+    {
       tc_fence_after();
       const int key = quad * 32 + lane;
       const int64_t j = j0 + key;
@@ -285,7 +301,8 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
       if (t >= 0 && v != 0.f) red_add(kl + (int64_t)g * N + t, v);
     }
     if (qt + 1 < n_qt) load_row_info(qt + 1);
-    if (mbar_wait(bar_q, nt & 1, abort, st, 0xA02)) {
+    if (!__syncthreads_and(mbar_wait(bar_q, nt & 1, abort, st, 0xA02))) break;
+    {
       tc_fence_after();
       // dq^I: thread = dim (TMEM lane), its warpgroup's 8 positions
       const int dim = quad * 32 + lane;
@@ -334,9 +351,373 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
   }
 }
 
+namespace wtf {
+constexpr int kThreads = 256;
+constexpr int kQ = 0, kK = wtc::kTile128, kV = 2 * wtc::kTile128;  // one 128 x 128 tile each
+constexpr int kBar = 3 * wtc::kTile128;
+constexpr int kBytes = 1024 + kBar + 64;
+constexpr uint32_t kTS = 0, kTO = 128, kCols = 256;
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128) | (1u << 16);  // V as MN-major B
+constexpr float kLazy = 8.0f;  // log2 units a row maximum may grow before O is rescaled
+__device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+}  // namespace wtf
+
+__global__ void __launch_bounds__(wtf::kThreads, 2) warmup_fwd_tc_kernel(
+    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc, int64_t N,
+    int H_q, int G, float scale, uint16_t* __restrict__ out, float* __restrict__ lse, DeviceStatus* st) {
+  using namespace wtf;
+  using wtc::kChunk128;
+  using wtc::off;
+  constexpr int D = 128;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ float ex_m[2][128], ex_l[2][128];  // the two halves' row maxima and sums
+  const uint32_t bar_s = sb + kBar, bar_o = sb + kBar + 8, bar_drain = sb + kBar + 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant; key columns 64 half .. + 63
+  const int g = (int)(blockIdx.x % (unsigned)G);
+  const int64_t n_qt = (N + wtc::kPos - 1) / wtc::kPos;
+  const int64_t t0 = (n_qt - 1 - (int64_t)(blockIdx.x / (unsigned)G)) * wtc::kPos;  // the longest rows first
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_drain, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), kCols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+  const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
+  const int64_t kv_row = (int64_t)G * D;
+  // Q rows r = 8 p + h: position t0 + p, head g*8 + h
+#pragma unroll
+  for (int m = 0; m < wtc::kRows * 16 / kThreads; ++m) {
+    const int i = tid + m * kThreads;
+    const int r = i >> 4, c = (i & 15) * 8;
+    const int64_t t = t0 + (r >> 3);
+    const bool ok = t < N;
+    cp_async_16(sm + kQ + off(r, c, kChunk128), ok ? q + (t * H_q + (int64_t)g * 8 + (r & 7)) * D + c : q,
+                ok ? 16 : 0);
+  }
+  // keys [128 i, 128 i + 128) of group g into the K or V tile
+  auto load_kv = [&](int base, const uint16_t* src, int64_t i) {
+#pragma unroll
+    for (int m = 0; m < 128 * 16 / kThreads; ++m) {
+      const int e = tid + m * kThreads;
+      const int r = e >> 4, c = (e & 15) * 8;
+      const int64_t j = i * 128 + r;
+      const bool ok = j < N;
+      cp_async_16(sm + base + off(r, c, kChunk128), ok ? src + j * kv_row + (int64_t)g * D + c : src, ok ? 16 : 0);
+    }
+  };
+  const int64_t t_last = min(t0 + wtc::kPos, N) - 1;  // keys [0, t_last] are visible to some row
+  const int64_t n_kv = t_last / 128 + 1;
+  load_kv(kK, kc, 0);
+  load_kv(kV, vc, 0);
+  cp_async_commit();
+  const int row = quad * 32 + lane;
+  const int64_t t = t0 + (row >> 3);  // this thread's row
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  const uint32_t scol = tmem + lane_base + kTS + half * 64;
+  const uint32_t ocol = tmem + lane_base + kTO + half * 64;
+  float m_used = __int_as_float(0xff800000);  // the row's maximum in use (log2 units)
+  float l_run = 0.f;
+  bool issued = false;
+  for (int64_t i = 0; i < n_kv; ++i) {
+    cp_async_wait<0>();  // K(i) and V(i) (and, at i = 0, Q)
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const int c = ks >> 2, kk = ks & 3;
+        mma_bf16_ss(tmem + kTS, umma_desc_kmajor(sb + kQ + c * kChunk128 + kk * 32, 128),
+                    umma_desc_kmajor(sb + kK + c * kChunk128 + kk * 32, 128), kIdescS, ks > 0);
+      }
+      umma_commit(bar_s);
+      issued = true;
+    }
+    // every thread takes the same branch (the TMEM loads below are warp-collective)
+    const bool ok_s = __syncthreads_and(mbar_wait(bar_s, (uint32_t)(i & 1), abort, st, 0xB01));
+    // S(i) is done, and so is P V(i - 1) (issued before it): K is free for the next tile
+    if (i + 1 < n_kv) load_kv(kK, kc, i + 1);
+    cp_async_commit();
+    if (ok_s) {
+      tc_fence_after();
+      const int64_t key0 = i * 128 + half * 64;
+      // last visible column of this half for this row (-1: none); rows past N see nothing
+      const int lim = t < N ? (int)max((int64_t)-1, min((int64_t)63, t - key0)) : -1;
+      uint32_t x[2][32];
+      tmem_ld_x32(scol, x[0]);
+      tmem_ld_x32(scol + 32, x[1]);
+      tmem_ld_wait();
+      reg_fence32(x[0]);
+      reg_fence32(x[1]);
+      float mx = __int_as_float(0xff800000);
+#pragma unroll
+      for (int e = 0; e < 64; ++e)
+        if (e <= lim) mx = fmaxf(mx, __uint_as_float(x[e >> 5][e & 31]));
+      ex_m[half][row] = mx;
+      __syncthreads();
+      const float mt = fmaxf(ex_m[0][row], ex_m[1][row]);
+      const float mt2 = mt == __int_as_float(0xff800000) ? mt : mt * sl2;
+      // both halves take the same decision for the row: the maximum in use moves only past 2^8 of growth
+      const bool rescale = mt2 > m_used + kLazy;
+      const float alpha = !rescale || m_used == __int_as_float(0xff800000) ? 0.f : ex2_approx(m_used - mt2);
+      if (rescale) {
+        l_run *= alpha;
+        m_used = mt2;
+      }
+      float ls = 0.f;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {  // 32 keys at a time -> 16 packed columns
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int c0 = cc * 32 + e;
+          const float p0 = c0 <= lim ? ex2_approx(fmaf(__uint_as_float(x[cc][e]), sl2, -m_used)) : 0.f;
+          const float p1 = c0 + 1 <= lim ? ex2_approx(fmaf(__uint_as_float(x[cc][e + 1]), sl2, -m_used)) : 0.f;
+          ls += p0 + p1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(scol + cc * 16, pk);  // keys of this half -> its first 32 columns, packed
+      }
+      if (rescale && i > 0) {  // O holds P V of earlier tiles (complete: see above); rescale this half's columns
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(ocol + cc * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          wtf::tmem_st_x32(ocol + cc * 32, o);
+        }
+      }
+      ex_l[half][row] = ls;
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    __syncthreads();
+    if (*abort) break;
+    l_run += ex_l[0][row] + ex_l[1][row];
+    if (warp == 0 && lane == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {  // keys 16 ks ..: half ks / 4, packed at column 64 half + 8 (ks % 4)
+        const uint32_t acol = tmem + kTS + (uint32_t)(64 * (ks >> 2) + 8 * (ks & 3));
+        mma_bf16_ts(tmem + kTO, acol, umma_desc_mnmajor_sw128(sb + kV + ks * 16 * 128, kChunk128), kIdescPV,
+                    (i > 0 || ks > 0) ? 1u : 0u);
+      }
+      umma_commit(bar_o);
+    }
+    if (!__syncthreads_and(mbar_wait(bar_o, (uint32_t)(i & 1), abort, st, 0xB02))) break;
+    // P V(i) is done: V is free for the next tile (its S runs while V lands)
+    if (i + 1 < n_kv) load_kv(kV, vc, i + 1);
+    cp_async_commit();
+  }
+  // ---- out = O / l and lse: thread = row, its half's 64 columns
+  if (!*abort) {
+    tc_fence_after();
+    uint32_t o[2][32];
+    tmem_ld_x32(ocol, o[0]);
+    tmem_ld_x32(ocol + 32, o[1]);
+    tmem_ld_wait();
+    if (t < N) {
+      const float il = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint16_t* orow = out + (t * H_q + (int64_t)g * 8 + (row & 7)) * D + half * 64;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(o[u >> 2][(u & 3) * 8 + 0]) * il, __uint_as_float(o[u >> 2][(u & 3) * 8 + 1]) * il);
+        v.y = pack_bf16x2(__uint_as_float(o[u >> 2][(u & 3) * 8 + 2]) * il, __uint_as_float(o[u >> 2][(u & 3) * 8 + 3]) * il);
+        v.z = pack_bf16x2(__uint_as_float(o[u >> 2][(u & 3) * 8 + 4]) * il, __uint_as_float(o[u >> 2][(u & 3) * 8 + 5]) * il);
+        v.w = pack_bf16x2(__uint_as_float(o[u >> 2][(u & 3) * 8 + 6]) * il, __uint_as_float(o[u >> 2][(u & 3) * 8 + 7]) * il);
+        *reinterpret_cast<uint4*>(orow + u * 8) = v;
+      }
+      if (half == 0)
+        lse[((int64_t)g * 8 + (row & 7)) * N + t] =
+            l_run > 0.f ? (m_used + __log2f(l_run)) * 0.69314718055994530942f : __int_as_float(0xff800000);
+    }
+    tc_fence_before();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0 && *abort && issued) {
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0, nullptr, st, 0xBF1);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// ---- the index branch's log-sum-exp over j <= t: thread = position
+namespace wti {
+constexpr int kThreads = 128;
+constexpr int kQI = 0, kKI = wtc::kTile128;  // K^I: two buffers
+constexpr int kBar = 3 * wtc::kTile128;
+constexpr int kBytes = 1024 + kBar + 64;
+constexpr uint32_t kCols = 256;
+constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
+}  // namespace wti
+
+__global__ void __launch_bounds__(wti::kThreads, 2) warmup_index_lse_tc_kernel(
+    const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, int64_t N, int G,
+    float* __restrict__ lseI, DeviceStatus* st) {
+  using namespace wti;
+  using wtc::kChunk128;
+  using wtc::off;
+  constexpr int DI = 128;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(sm);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const uint32_t bar0 = sb + kBar, bar_drain = sb + kBar + 16;  // bar0 + 8 b: Z buffer b complete
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = (int)(blockIdx.x % (unsigned)G);
+  const int64_t n_pt = (N + 127) / 128;
+  const int64_t p0 = (n_pt - 1 - (int64_t)(blockIdx.x / (unsigned)G)) * 128;  // the longest rows first
+  if (tid == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar0 + 8, 1);
+    mbar_init(bar_drain, 1);
+    fence_mbar_init();
+    abort_flag = 0;
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), kCols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  volatile int* abort = &abort_flag;
+  const float sI2 = 1.4426950408889634f / sqrtf((float)DI);
+  for (int e = tid; e < 128 * 16; e += kThreads) {
+    const int r = e >> 4, c = (e & 15) * 8;
+    const int64_t t = p0 + r;
+    const bool ok = t < N;
+    cp_async_16(sm + kQI + off(r, c, kChunk128), ok ? q_idx + (t * G + g) * DI + c : q_idx, ok ? 16 : 0);
+  }
+  auto load_k = [&](int b, int64_t i) {
+    for (int e = tid; e < 128 * 16; e += kThreads) {
+      const int r = e >> 4, c = (e & 15) * 8;
+      const int64_t j = i * 128 + r;
+      const bool ok = j < N;
+      cp_async_16(sm + kKI + b * wtc::kTile128 + off(r, c, kChunk128), ok ? k_idx + j * DI + c : k_idx,
+                  ok ? 16 : 0);
+    }
+  };
+  const int64_t t_last = min(p0 + 128, N) - 1;
+  const int64_t n_kt = t_last / 128 + 1;
+  load_k(0, 0);
+  cp_async_commit();
+  const int64_t t = p0 + warp * 32 + lane;  // this thread's position (TMEM lane)
+  float m = __int_as_float(0xff800000), l = 0.f;
+  bool issued = false;
+  for (int64_t i = 0; i < n_kt; ++i) {
+    const int b = (int)(i & 1);
+    if (i + 1 < n_kt) load_k(b ^ 1, i + 1);  // that buffer's last MMA (tile i - 1) completed
+    cp_async_commit();
+    cp_async_wait<1>();  // tile i's keys (and Q^I)
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (warp == 0 && lane == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < DI / 16; ++ks) {
+        const int c = ks >> 2, kk = ks & 3;
+        mma_bf16_ss(tmem + (uint32_t)(b * 128), umma_desc_kmajor(sb + kQI + c * kChunk128 + kk * 32, 128),
+                    umma_desc_kmajor(sb + kKI + b * wtc::kTile128 + c * kChunk128 + kk * 32, 128), kIdesc, ks > 0);
+      }
+      umma_commit(bar0 + 8 * b);
+      issued = true;
+    }
+    if (!__syncthreads_and(mbar_wait(bar0 + 8 * b, (uint32_t)((i >> 1) & 1), abort, st, 0xC01))) break;
+    tc_fence_after();
+    const int lim = t < N ? (int)max((int64_t)-1, min((int64_t)127, t - i * 128)) : -1;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t x[32];
+      tmem_ld_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * 128 + cc * 32), x);
+      tmem_ld_wait();
+      float mx = __int_as_float(0xff800000);
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (cc * 32 + e <= lim) mx = fmaxf(mx, __uint_as_float(x[e]) * sI2);
+      if (mx == __int_as_float(0xff800000)) continue;
+      const float mn = fmaxf(m, mx);
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        if (cc * 32 + e <= lim) s += ex2_approx(fmaf(__uint_as_float(x[e]), sI2, -mn));
+      l = l * ex2_approx(m - mn) + s;  // 2^(-inf) = 0 at the first key
+      m = mn;
+    }
+    tc_fence_before();
+    __syncthreads();  // buffer b is read: the tile after next may overwrite it
+  }
+  if (!*abort && t < N)
+    lseI[(int64_t)g * N + t] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994530942f : __int_as_float(0xff800000);
+  cp_async_wait<0>();
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0 && *abort && issued) {
+      umma_commit(bar_drain);
+      mbar_wait(bar_drain, 0, nullptr, st, 0xCF1);
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
 }  // namespace
 
 bool warmup_tc_supported(int d, int d_I, int H_q, int H_kv) { return d == 128 && d_I == 128 && H_q == 8 * H_kv; }
+
+cudaError_t launch_warmup_fwd_tc(const void* q, const void* k, const void* v, const void* q_idx, const void* k_idx,
+                                 int64_t N, int H_q, int H_kv, float scale, void* out, float* lse, float* lseI,
+                                 DeviceStatus* st, cudaStream_t s) {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(warmup_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, wtf::kBytes)) !=
+      cudaSuccess)
+    return e;
+  const int64_t n_qt = (N + wtc::kPos - 1) / wtc::kPos;
+  warmup_fwd_tc_kernel<<<(unsigned)(n_qt * H_kv), wtf::kThreads, wtf::kBytes, s>>>(
+      (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, N, H_q, H_kv, scale, (uint16_t*)out, lse, st);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(warmup_index_lse_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                wti::kBytes)) != cudaSuccess)
+    return e;
+  const int64_t n_pt = (N + 127) / 128;
+  warmup_index_lse_tc_kernel<<<(unsigned)(n_pt * H_kv), wti::kThreads, wti::kBytes, s>>>(
+      (const uint16_t*)q_idx, (const uint16_t*)k_idx, N, H_kv, lseI, st);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_warmup_grad_tc(const void* q, const void* k, const void* q_idx, const void* k_idx, int64_t N,
                                   int H_q, int H_kv, float scale, float kl_weight, const float* lse, const float* lseI,
@@ -349,7 +730,7 @@ cudaError_t launch_warmup_grad_tc(const void* q, const void* k, const void* q_id
                                 wtc::kBytes)) != cudaSuccess)
     return e;
   const int64_t n_kt = (N + wtc::kKeys - 1) / wtc::kKeys;
-  warmup_grad_tc_kernel<<<dim3((unsigned)H_kv, (unsigned)n_kt), wtc::kThreads, wtc::kBytes, s>>>(
+  warmup_grad_tc_kernel<<<(unsigned)(n_kt * H_kv), wtc::kThreads, wtc::kBytes, s>>>(
       (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)q_idx, (const uint16_t*)k_idx, lse, lseI, N, H_q,
       H_kv, scale, kl_weight, dq_idx, dk_idx, kl, st);
   return cudaGetLastError();
