@@ -26,9 +26,10 @@
 //   dq^I^T = K^I^T dzI^T (K^I as MN-major A, M = d_I, N = 16 positions),
 //                         added to dq^I with fp32 reductions (32 consecutive
 //                         dims per warp instruction).
-// The next query tile's rows arrive by cp.async while this one computes.  The
-// main scores are computed once per (key, query) pair here; the forward pass
-// keeps its own.
+// S^T and Z^T have two TMEM buffers: the next query tile's products are
+// issued before this tile's softmax, so the tensor cores and the exponentials
+// overlap; its rows arrive by cp.async two tiles ahead.  The main scores are
+// computed once per (key, query) pair here; the forward pass keeps its own.
 //
 // Forward, query-outer: one CTA per (query tile of 16 positions x 8 heads,
 // group), two CTAs per SM (256 TMEM columns and 96 KB each, so one CTA's MMAs
@@ -57,18 +58,18 @@ namespace wtc {
 constexpr int kKeys = 128;   // keys of a CTA
 constexpr int kPos = 16;     // positions of a query tile
 constexpr int kRows = 128;   // 16 positions x 8 heads
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;      // gradient kernel: four warpgroups, 4 positions each
 constexpr int kChunk128 = 128 * 128;  // one 64-column chunk of a 128-row bf16 tile, bytes
 constexpr int kTile128 = 2 * kChunk128;
 constexpr int kChunk16 = 16 * 128;    // one 64-column chunk of a 16-row bf16 tile
 constexpr int kTile16 = 2 * kChunk16;
 constexpr int kK = 0, kKI = kTile128, kQ = 2 * kTile128;  // Q: two buffers
-constexpr int kQI = 4 * kTile128;                           // Q^I: two buffers
-constexpr int kDZ = kQI + 2 * kTile16;                      // dzI [16 positions][128 keys], K-major
+constexpr int kQI = 4 * kTile128;                           // Q^I: three buffers
+constexpr int kDZ = kQI + 3 * kTile16;                      // dzI [16 positions][128 keys], K-major
 constexpr int kBar = kDZ + kTile16;
 constexpr int kBytes = 1024 + kBar + 64;
-// TMEM columns: S^T, Z^T, dq^I^T, dzI^T (A operand, bf16 packed), dk^I
-constexpr uint32_t kTS = 0, kTZ = 128, kTDQ = 160, kTDZ = 192, kTDK = 256;
+// TMEM columns: S^T (two buffers), Z^T (two buffers), dq^I^T, dzI^T (A operand, bf16 packed), dk^I
+constexpr uint32_t kTS = 0, kTZ = 256, kTDQ = 288, kTDZ = 304, kTDK = 384;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescZ = idesc_bf16_f32(128, 16);
 constexpr uint32_t kIdescDK = idesc_bf16_f32(128, 128) | (1u << 16);  // B MN-major
@@ -94,9 +95,16 @@ __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
 __device__ __forceinline__ void reg_fence8(uint32_t (&r)[8]) {
   asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]));
 }
-__device__ __forceinline__ void tmem_st_x4(uint32_t taddr, const uint32_t (&r)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3])
+__device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void reg_fence4(uint32_t (&r)[4]) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
+}
+__device__ __forceinline__ void tmem_st_x2(uint32_t taddr, const uint32_t (&r)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1])
                : "memory");
 }
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -118,17 +126,18 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
   const uint32_t sb = smem_u32(sm);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float lse2_s[kRows];   // main lse of each tile row, log2 units
-  __shared__ float lseI2_s[kPos];   // lse^I of each position, log2 units
-  __shared__ int32_t tpos_s[kPos];  // position of each tile position, -1 past N
-  __shared__ float kl_s[8][8];      // per warp, the KL sums of its warpgroup's 8 positions
-  const uint32_t bar_s = sb + kBar, bar_q = sb + kBar + 8, bar_drain = sb + kBar + 16;
+  __shared__ float lse2_s[2][kRows];   // main lse of each tile row, log2 units (two tiles in flight)
+  __shared__ float lseI2_s[2][kPos];   // lse^I of each position, log2 units
+  __shared__ int32_t tpos_s[2][kPos];  // position of each tile position, -1 past N
+  __shared__ float kl_s[16][4];        // per warp, the KL sums of its warpgroup's 4 positions
+  const uint32_t bar_s0 = sb + kBar, bar_q = sb + kBar + 16, bar_drain = sb + kBar + 24;  // bar_s0 + 8 b
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, half = warp >> 2;  // TMEM lane quadrant; positions 8 half .. 8 half + 7
+  const int quad = warp & 3, quarter = warp >> 2;  // TMEM lane quadrant; positions 4 quarter .. 4 quarter + 3
   const int g = (int)(blockIdx.x % (unsigned)G);
   const int64_t j0 = (int64_t)(blockIdx.x / (unsigned)G) * kKeys;  // launch order: the heaviest key tiles first
   if (tid == 0) {
-    mbar_init(bar_s, 1);
+    mbar_init(bar_s0, 1);
+    mbar_init(bar_s0 + 8, 1);
     mbar_init(bar_q, 1);
     mbar_init(bar_drain, 1);
     fence_mbar_init();
@@ -156,31 +165,36 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
     cp_async_16(sm + kK + off(r, c, kChunk128), ok ? kc + (j * G + g) * D + c : kc, ok ? 16 : 0);
     cp_async_16(sm + kKI + off(r, c, kChunk128), ok ? k_idx + j * DI + c : k_idx, ok ? 16 : 0);
   }
-  // rows of query tile qt into buffer b: Q rows r = 8 p + h (position p, head g*8 + h), Q^I rows p
-  auto issue_q = [&](int64_t qt, int b) {
-    const int64_t t0 = qt * kPos;
+  const int64_t n_qt = (N + kPos - 1) / kPos;
+  const int64_t qt0 = j0 / kPos;  // the first query tile with a position >= j0
+  const int64_t n_tiles = n_qt - qt0;
+  // rows of query tile n (qt0 + n): Q rows r = 8 p + h (position p, head g*8 + h) into Q buffer n % 2,
+  // Q^I rows p into Q^I buffer n % 3 (Q^I is read until that tile's dk^I product, one tile later than Q)
+  auto issue_q = [&](int64_t n) {
+    const int64_t t0 = (qt0 + n) * kPos;
+    const int bq = (int)(n & 1), bi = (int)(n % 3);
 #pragma unroll
     for (int m = 0; m < kRows * 16 / kThreads; ++m) {
       const int i = tid + m * kThreads;
       const int r = i >> 4, c = (i & 15) * 8;
       const int64_t t = t0 + (r >> 3);
       const bool ok = t < N;
-      cp_async_16(sm + kQ + b * kTile128 + off(r, c, kChunk128),
+      cp_async_16(sm + kQ + bq * kTile128 + off(r, c, kChunk128),
                   ok ? q + (t * H_q + (int64_t)g * 8 + (r & 7)) * D + c : q, ok ? 16 : 0);
     }
-    {
-      const int r = tid >> 4, c = (tid & 15) * 8;  // 16 rows x 16 units = 256 threads
+    if (tid < kPos * 16) {
+      const int r = tid >> 4, c = (tid & 15) * 8;  // 16 rows x 16 units
       const int64_t t = t0 + r;
       const bool ok = t < N;
-      cp_async_16(sm + kQI + b * kTile16 + off(r, c, kChunk16), ok ? q_idx + (t * G + g) * DI + c : q_idx,
+      cp_async_16(sm + kQI + bi * kTile16 + off(r, c, kChunk16), ok ? q_idx + (t * G + g) * DI + c : q_idx,
                   ok ? 16 : 0);
     }
   };
-  // row info of query tile qt into registers (stored to shared memory when the tile starts)
+  // row info of tile n into registers, then into shared-memory slot n % 2
   float nt_lse = 0.f, nt_lseI = 0.f;
   int32_t nt_t = -1;
-  auto load_row_info = [&](int64_t qt) {
-    const int64_t t0 = qt * kPos;
+  auto load_row_info = [&](int64_t n) {
+    const int64_t t0 = (qt0 + n) * kPos;
     if (tid < kRows) {
       const int64_t t = t0 + (tid >> 3);
       nt_lse = t < N ? __ldg(lse + ((int64_t)g * 8 + (tid & 7)) * N + t) : 0.f;
@@ -190,87 +204,100 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
       nt_lseI = t < N ? __ldg(lseI + (int64_t)g * N + t) : 0.f;
     }
   };
-  const int64_t n_qt = (N + kPos - 1) / kPos;
-  const int64_t qt0 = j0 / kPos;  // the first query tile with a position >= j0
-  issue_q(qt0, 0);
-  cp_async_commit();
-  load_row_info(qt0);
-  bool issued = false;
-  uint32_t nt = 0;
-  for (int64_t qt = qt0; qt < n_qt; ++qt, ++nt) {
-    const int buf = (int)(nt & 1);
+  auto store_row_info = [&](int slot) {
     if (tid < kRows) {
-      lse2_s[tid] = nt_lse * kLog2e;
+      lse2_s[slot][tid] = nt_lse * kLog2e;
     } else if (tid < kRows + kPos) {
-      tpos_s[tid - kRows] = nt_t;
-      lseI2_s[tid - kRows] = nt_lseI * kLog2e;
+      tpos_s[slot][tid - kRows] = nt_t;
+      lseI2_s[slot][tid - kRows] = nt_lseI * kLog2e;
     }
-    cp_async_wait<0>();  // this tile's rows (and, at the first tile, the CTA's keys)
-    fence_proxy_async_smem();
-    __syncthreads();
-    const uint32_t qb = sb + kQ + buf * kTile128, qib = sb + kQI + buf * kTile16;
-    // ---- S^T and Z^T
-    if (warp == 0 && lane == 0) {
-      tc_fence_after();
+  };
+  // S^T and Z^T of tile n into TMEM buffer n % 2
+  auto issue_sz = [&](int64_t n) {
+    const int b = (int)(n & 1);
+    const uint32_t qb = sb + kQ + b * kTile128, qib = sb + kQI + (int)(n % 3) * kTile16;
+    tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int c = ks >> 2, kk = ks & 3;
-        mma_bf16_ss(tmem + kTS, umma_desc_kmajor(sb + kK + c * kChunk128 + kk * 32, 128),
-                    umma_desc_kmajor(qb + c * kChunk128 + kk * 32, 128), kIdescS, ks > 0);
-        mma_bf16_ss(tmem + kTZ, umma_desc_kmajor(sb + kKI + c * kChunk128 + kk * 32, 128),
-                    umma_desc_kmajor(qib + c * kChunk16 + kk * 32, 128), kIdescZ, ks > 0);
-      }
-      umma_commit(bar_s);
-      issued = true;
+    for (int ks = 0; ks < D / 16; ++ks) {
+      const int c = ks >> 2, kk = ks & 3;
+      mma_bf16_ss(tmem + kTS + b * 128, umma_desc_kmajor(sb + kK + c * kChunk128 + kk * 32, 128),
+                  umma_desc_kmajor(qb + c * kChunk128 + kk * 32, 128), kIdescS, ks > 0);
+      mma_bf16_ss(tmem + kTZ + b * 16, umma_desc_kmajor(sb + kKI + c * kChunk128 + kk * 32, 128),
+                  umma_desc_kmajor(qib + c * kChunk16 + kk * 32, 128), kIdescZ, ks > 0);
     }
-    // the next tile's rows stream in while this one computes (their buffer's last readers, the
-    // MMAs of the previous tile, have completed)
-    if (qt + 1 < n_qt) issue_q(qt + 1, buf ^ 1);
-    cp_async_commit();
-    // ---- teacher, index probabilities, dzI and KL: thread = key, its warpgroup's 8 positions
+    umma_commit(bar_s0 + 8 * b);
+  };
+  issue_q(0);
+  cp_async_commit();
+  if (n_tiles > 1) issue_q(1);
+  cp_async_commit();
+  load_row_info(0);
+  store_row_info(0);
+  if (n_tiles > 1) load_row_info(1);
+  cp_async_wait<1>();  // the keys and tile 0's rows
+  fence_proxy_async_smem();
+  __syncthreads();
+  bool issued = false;
+  if (warp == 0 && lane == 0) {
+    issue_sz(0);
+    issued = true;
+  }
+  for (int64_t n = 0; n < n_tiles; ++n) {
+    const int b = (int)(n & 1);
+    // ---- the next tile's S^T and Z^T go to the tensor cores before this tile's softmax
+    if (n + 1 < n_tiles) {
+      store_row_info(b ^ 1);
+      cp_async_wait<0>();  // tile n+1's rows
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (warp == 0 && lane == 0) issue_sz(n + 1);
+    }
     // every thread takes the same branch (the TMEM loads and shuffles below are warp-collective)
-    if (!__syncthreads_and(mbar_wait(bar_s, nt & 1, abort, st, 0xA01))) break;
+    if (!__syncthreads_and(mbar_wait(bar_s0 + 8 * b, (uint32_t)((n >> 1) & 1), abort, st, 0xA01))) break;
+    // S^T(n) is done, so its Q buffer is free: tile n+2's rows stream in now
+    if (n + 2 < n_tiles) {
+      issue_q(n + 2);
+      load_row_info(n + 2);
+    }
+    cp_async_commit();
+    // ---- teacher, index probabilities, dzI and KL: thread = key, its warpgroup's 4 positions
     {
       tc_fence_after();
       const int key = quad * 32 + lane;
       const int64_t j = j0 + key;
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-      uint32_t sx[2][32], zx[8];
-      tmem_ld_x32(tmem + lane_base + kTS + half * 64, sx[0]);
-      tmem_ld_x32(tmem + lane_base + kTS + half * 64 + 32, sx[1]);
-      tmem_ld_x8(tmem + lane_base + kTZ + half * 8, zx);
+      uint32_t sx[32], zx[4];
+      tmem_ld_x32(tmem + lane_base + kTS + b * 128 + quarter * 32, sx);
+      wtc::tmem_ld_x4(tmem + lane_base + kTZ + b * 16 + quarter * 4, zx);
       tmem_ld_wait();
-      reg_fence32(sx[0]);
-      reg_fence32(sx[1]);
-      reg_fence8(zx);
-      float dz[8], klv[8];
+      reg_fence32(sx);
+      wtc::reg_fence4(zx);
+      float dz[4], klv[4];
 #pragma unroll
-      for (int pl = 0; pl < 8; ++pl) {
-        const int p = half * 8 + pl;
-        const int32_t t = tpos_s[p];
+      for (int pl = 0; pl < 4; ++pl) {
+        const int p = quarter * 4 + pl;
+        const int32_t t = tpos_s[b][p];
         const bool valid = t >= 0 && j <= (int64_t)t;
         float ps = 0.f;
 #pragma unroll
         for (int hd = 0; hd < 8; ++hd) {
-          const int r = pl * 8 + hd;  // column within this warpgroup's 64
-          ps += ex2_approx(fmaf(__uint_as_float(sx[r >> 5][r & 31]), sl2, -lse2_s[half * 64 + r]));
+          const int r = pl * 8 + hd;  // column within this warpgroup's 32
+          ps += ex2_approx(fmaf(__uint_as_float(sx[r]), sl2, -lse2_s[b][quarter * 32 + r]));
         }
         const float pbar = valid ? ps * 0.125f : 0.f;
-        const float zl2 = fmaf(__uint_as_float(zx[pl]), sI2, -lseI2_s[p]);  // log2 pI
+        const float zl2 = fmaf(__uint_as_float(zx[pl]), sI2, -lseI2_s[b][p]);  // log2 pI
         const float pI = valid ? ex2_approx(zl2) : 0.f;
         dz[pl] = w_kl * (pI - pbar);
         klv[pl] = pbar > 0.f ? pbar * (wtc::lg2_approx(pbar) - zl2) * kLn2 : 0.f;
       }
-      uint32_t pk[4];
+      const uint32_t pk[2] = {pack_bf16x2(dz[0], dz[1]), pack_bf16x2(dz[2], dz[3])};
+      wtc::tmem_st_x2(tmem + lane_base + kTDZ + quarter * 2, pk);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) pk[u] = pack_bf16x2(dz[2 * u], dz[2 * u + 1]);
-      wtc::tmem_st_x4(tmem + lane_base + kTDZ + half * 4, pk);
-#pragma unroll
-      for (int pl = 0; pl < 8; ++pl)
-        *reinterpret_cast<uint16_t*>(sm + kDZ + off(half * 8 + pl, key, kChunk16)) =
+      for (int pl = 0; pl < 4; ++pl)
+        *reinterpret_cast<uint16_t*>(sm + kDZ + off(quarter * 4 + pl, key, kChunk16)) =
             (uint16_t)(pack_bf16x2(dz[pl], 0.f) & 0xFFFFu);
 #pragma unroll
-      for (int pl = 0; pl < 8; ++pl) {
+      for (int pl = 0; pl < 4; ++pl) {
         float v = klv[pl];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -281,11 +308,11 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
       tc_fence_before();
     }
     __syncthreads();
-    if (*abort) break;
     // ---- dk^I += dzI^T Q^I and dq^I^T = K^I^T dzI^T
     if (warp == 0 && lane == 0) {
       tc_fence_after();
-      mma_bf16_ts(tmem + kTDK, tmem + kTDZ, umma_desc_mnmajor_sw128(qib, kChunk16), kIdescDK, nt > 0 ? 1u : 0u);
+      mma_bf16_ts(tmem + kTDK, tmem + kTDZ, umma_desc_mnmajor_sw128(sb + kQI + (int)(n % 3) * kTile16, kChunk16),
+                  kIdescDK, n > 0 ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < kKeys / 16; ++ks) {
         const int c = ks >> 2, kk = ks & 3;
@@ -295,38 +322,37 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
       umma_commit(bar_q);
     }
     if (tid < kPos) {  // the tile's KL sums: the four warps of the position's warpgroup
-      const int h2 = tid >> 3, pl = tid & 7;
-      const float v = kl_s[4 * h2][pl] + kl_s[4 * h2 + 1][pl] + kl_s[4 * h2 + 2][pl] + kl_s[4 * h2 + 3][pl];
-      const int32_t t = tpos_s[tid];
+      const int qg = tid >> 2, pl = tid & 3;
+      const float v = kl_s[4 * qg][pl] + kl_s[4 * qg + 1][pl] + kl_s[4 * qg + 2][pl] + kl_s[4 * qg + 3][pl];
+      const int32_t t = tpos_s[b][tid];
       if (t >= 0 && v != 0.f) red_add(kl + (int64_t)g * N + t, v);
     }
-    if (qt + 1 < n_qt) load_row_info(qt + 1);
-    if (!__syncthreads_and(mbar_wait(bar_q, nt & 1, abort, st, 0xA02))) break;
+    if (!__syncthreads_and(mbar_wait(bar_q, (uint32_t)(n & 1), abort, st, 0xA02))) break;
     {
       tc_fence_after();
-      // dq^I: thread = dim (TMEM lane), its warpgroup's 8 positions
+      // dq^I: thread = dim (TMEM lane), its warpgroup's 4 positions
       const int dim = quad * 32 + lane;
-      uint32_t x[8];
-      tmem_ld_x8(tmem + ((uint32_t)(quad * 32) << 16) + kTDQ + half * 8, x);
+      uint32_t x[4];
+      wtc::tmem_ld_x4(tmem + ((uint32_t)(quad * 32) << 16) + kTDQ + quarter * 4, x);
       tmem_ld_wait();
-      reg_fence8(x);
+      wtc::reg_fence4(x);
 #pragma unroll
-      for (int pl = 0; pl < 8; ++pl) {
-        const int32_t t = tpos_s[half * 8 + pl];
-        if (t >= (int32_t)j0) red_add(dq_idx + ((int64_t)t * G + g) * DI + dim, sI * __uint_as_float(x[pl]));
+      for (int pl = 0; pl < 4; ++pl) {
+        const int32_t t = tpos_s[b][quarter * 4 + pl];
+        if (t >= 0) red_add(dq_idx + ((int64_t)t * G + g) * DI + dim, sI * __uint_as_float(x[pl]));
       }
       tc_fence_before();
     }
     __syncthreads();
     if (*abort) break;
   }
-  // ---- dk^I of the CTA's keys: thread = key, its warpgroup's 64 dims; the groups add up in dk_idx
+  // ---- dk^I of the CTA's keys: thread = key, its warpgroup's 32 dims; the groups add up in dk_idx
   if (!*abort) {
     tc_fence_after();
     const int key = quad * 32 + lane;
     const int64_t j = j0 + key;
-#pragma unroll 1
-    for (int cc = 2 * half; cc < 2 * half + 2; ++cc) {
+    {
+      const int cc = quarter;
       uint32_t x[32];
       tmem_ld_x32(tmem + ((uint32_t)(quad * 32) << 16) + kTDK + cc * 32, x);
       tmem_ld_wait();
@@ -360,6 +386,20 @@ constexpr uint32_t kTS = 0, kTO = 128, kCols = 256;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128) | (1u << 16);  // V as MN-major B
 constexpr float kLazy = 8.0f;  // log2 units a row maximum may grow before O is rescaled
+// Packed pairs of fp32 (one 64-bit register): two lanes of arithmetic per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -473,10 +513,23 @@ __global__ void __launch_bounds__(wtf::kThreads, 2) warmup_fwd_tc_kernel(
       tmem_ld_wait();
       reg_fence32(x[0]);
       reg_fence32(x[1]);
+      // tiles below the diagonal for every row of the warp take the unmasked path
+      const bool full = __all_sync(0xffffffffu, lim == 63);
       float mx = __int_as_float(0xff800000);
+      if (full) {
+        float m2[2];
 #pragma unroll
-      for (int e = 0; e < 64; ++e)
-        if (e <= lim) mx = fmaxf(mx, __uint_as_float(x[e >> 5][e & 31]));
+        for (int cc = 0; cc < 2; ++cc) {
+          m2[cc] = __int_as_float(0xff800000);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) m2[cc] = max3(m2[cc], __uint_as_float(x[cc][e]), __uint_as_float(x[cc][e + 1]));
+        }
+        mx = fmaxf(m2[0], m2[1]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e <= lim) mx = fmaxf(mx, __uint_as_float(x[e >> 5][e & 31]));
+      }
       ex_m[half][row] = mx;
       __syncthreads();
       const float mt = fmaxf(ex_m[0][row], ex_m[1][row]);
@@ -489,18 +542,38 @@ __global__ void __launch_bounds__(wtf::kThreads, 2) warmup_fwd_tc_kernel(
         m_used = mt2;
       }
       float ls = 0.f;
+      if (full) {
+        const uint64_t sl2x2 = wtf::f2_pack(sl2, sl2), nm2 = wtf::f2_pack(-m_used, -m_used);
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {  // 32 keys at a time -> 16 packed columns
-        uint32_t pk[16];
+        for (int cc = 0; cc < 2; ++cc) {  // 32 keys at a time -> 16 packed columns
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int c0 = cc * 32 + e;
-          const float p0 = c0 <= lim ? ex2_approx(fmaf(__uint_as_float(x[cc][e]), sl2, -m_used)) : 0.f;
-          const float p1 = c0 + 1 <= lim ? ex2_approx(fmaf(__uint_as_float(x[cc][e + 1]), sl2, -m_used)) : 0.f;
-          ls += p0 + p1;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 32; e += 2) {
+            float a0, a1;
+            wtf::f2_unpack(wtf::f2_fma(wtf::f2_pack(__uint_as_float(x[cc][e]), __uint_as_float(x[cc][e + 1])), sl2x2,
+                                       nm2),
+                           a0, a1);
+            a0 = ex2_approx(a0);
+            a1 = ex2_approx(a1);
+            ls += a0 + a1;
+            pk[e >> 1] = pack_bf16x2(a0, a1);
+          }
+          tmem_st_x16(scol + cc * 16, pk);  // keys of this half -> its first 32 columns, packed
         }
-        tmem_st_x16(scol + cc * 16, pk);  // keys of this half -> its first 32 columns, packed
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int c0 = cc * 32 + e;
+            const float p0 = c0 <= lim ? ex2_approx(fmaf(__uint_as_float(x[cc][e]), sl2, -m_used)) : 0.f;
+            const float p1 = c0 + 1 <= lim ? ex2_approx(fmaf(__uint_as_float(x[cc][e + 1]), sl2, -m_used)) : 0.f;
+            ls += p0 + p1;
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_x16(scol + cc * 16, pk);
+        }
       }
       if (rescale && i > 0) {  // O holds P V of earlier tiles (complete: see above); rescale this half's columns
 #pragma unroll 1
