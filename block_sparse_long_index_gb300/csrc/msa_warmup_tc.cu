@@ -18,7 +18,7 @@
 // into TMEM; each thread owns one key (TMEM lane), so a position's 8 head
 // probabilities are 8 consecutive columns of its own row and the teacher is
 // a sum of 8 registers, with no exchange between threads.  It forms dzI for
-// the 16 positions, writes it (bf16) to TMEM (the A operand of dk^I) and to a
+// its positions, writes it (bf16) to TMEM (the A operand of dk^I) and to a
 // K-major shared tile (the B operand of dq^I), and adds its KL terms;
 //   dk^I  += dzI^T Q^I   (A from TMEM, Q^I as MN-major B), accumulated in
 //                         TMEM over every query tile of the CTA and written
@@ -26,10 +26,16 @@
 //   dq^I^T = K^I^T dzI^T (K^I as MN-major A, M = d_I, N = 16 positions),
 //                         added to dq^I with fp32 reductions (32 consecutive
 //                         dims per warp instruction).
-// S^T and Z^T have two TMEM buffers: the next query tile's products are
-// issued before this tile's softmax, so the tensor cores and the exponentials
-// overlap; its rows arrive by cp.async two tiles ahead.  The main scores are
-// computed once per (key, query) pair here; the forward pass keeps its own.
+// Roles: a producer warp (TMA boxes of the query tiles' Q and Q^I into three
+// slots, and each tile's lse row info), an MMA warp (one thread issues), and
+// 16 softmax warps, 4 positions each.  They hand over through mbarriers:
+// S^T, Z^T, dzI and dq^I^T have two TMEM buffers each, so S^T of tile n + 1
+// runs on the tensor cores while tile n's exponentials do, and tile n's dk^I
+// and dq^I products run while tile n + 1's do; a warp reads tile n's dq^I
+// after its softmax of tile n + 1.  Barriers that a warp could reach again
+// before the others leave them come in pairs (one per tile parity).  The main
+// scores are computed once per (key, query) pair here; the forward pass keeps
+// its own.
 //
 // Forward, query-outer: one CTA per (query tile of 16 positions x 8 heads,
 // group), two CTAs per SM (256 TMEM columns and 96 KB each, so one CTA's MMAs
@@ -58,24 +64,31 @@ namespace wtc {
 constexpr int kKeys = 128;   // keys of a CTA
 constexpr int kPos = 16;     // positions of a query tile
 constexpr int kRows = 128;   // 16 positions x 8 heads
-constexpr int kThreads = 512;      // gradient kernel: four warpgroups, 4 positions each
+constexpr int kSoftWarps = 16;                  // four warpgroups, 4 positions each
+constexpr int kWarpLoad = 16, kWarpMma = 17;    // producer (TMA, row info) and MMA issuer
+constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kSlots = 3;                       // query tiles in flight (Q, Q^I, row info)
 constexpr int kChunk128 = 128 * 128;  // one 64-column chunk of a 128-row bf16 tile, bytes
 constexpr int kTile128 = 2 * kChunk128;
 constexpr int kChunk16 = 16 * 128;    // one 64-column chunk of a 16-row bf16 tile
 constexpr int kTile16 = 2 * kChunk16;
-constexpr int kK = 0, kKI = kTile128, kQ = 2 * kTile128;  // Q: two buffers
-constexpr int kQI = 4 * kTile128;                           // Q^I: three buffers
-constexpr int kDZ = kQI + 3 * kTile16;                      // dzI [16 positions][128 keys], K-major
-constexpr int kBar = kDZ + kTile16;
-constexpr int kBytes = 1024 + kBar + 64;
-// TMEM columns: S^T (two buffers), Z^T (two buffers), dq^I^T, dzI^T (A operand, bf16 packed), dk^I
-constexpr uint32_t kTS = 0, kTZ = 256, kTDQ = 288, kTDZ = 304, kTDK = 384;
+constexpr int kK = 0, kKI = kTile128, kQ = 2 * kTile128;  // Q: kSlots buffers
+constexpr int kQI = kQ + kSlots * kTile128;                 // Q^I: kSlots buffers
+constexpr int kDZ = kQI + kSlots * kTile16;                 // dzI [16 positions][128 keys], K-major: two buffers
+constexpr int kBar = kDZ + 2 * kTile16;
+constexpr int kNumBars = 18;
+constexpr int kBytes = 1024 + kBar + 8 * kNumBars;
+constexpr uint32_t kTileTx = kTile128 + kTile16;  // bytes of one query tile's Q and Q^I
+// TMEM columns: S^T, Z^T, dq^I^T and dzI^T (A operand, bf16 packed) with two buffers each, dk^I.
+// Softmax warp w (TMEM lanes 32 (w % 4) ..) owns positions 4 (w / 4) .. + 3 of a query tile.
+constexpr uint32_t kTS = 0, kTZ = 256, kTDQ = 288, kTDZ = 320, kTDK = 384;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescZ = idesc_bf16_f32(128, 16);
 constexpr uint32_t kIdescDK = idesc_bf16_f32(128, 128) | (1u << 16);  // B MN-major
 constexpr uint32_t kIdescDQ = idesc_bf16_f32(128, 16) | (1u << 15);   // A MN-major
 // Byte offset of element (row r, column c) of a 128B-swizzled K-major bf16
-// tile whose 64-column chunks are `chunk` bytes apart (8-row groups 1 KB apart).
+// tile whose 64-column chunks are `chunk` bytes apart (8-row groups 1 KB apart):
+// the layout a TMA box of 64 columns lands in, one box per chunk.
 __device__ __forceinline__ uint32_t off(int r, int c, int chunk) {
   return (uint32_t)((c >> 6) * chunk + (r >> 3) * 1024 + (r & 7) * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) +
                     ((c & 7) << 1));
@@ -86,6 +99,14 @@ __device__ __forceinline__ void red_add(float* p, float a) {
 __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
@@ -107,43 +128,84 @@ __device__ __forceinline__ void tmem_st_x2(uint32_t taddr, const uint32_t (&r)[2
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1])
                : "memory");
 }
+// Packed pairs of fp32 (one 64-bit register): two lanes of arithmetic per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 __device__ __forceinline__ float lg2_approx(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// A bounded wait whose result every lane of the warp shares (warp-collective work follows it).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, DeviceStatus* st,
+                                          unsigned code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, st, code, 64));
+}
 }  // namespace wtc
 
 __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
-    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ q_idx,
-    const uint16_t* __restrict__ k_idx, const float* __restrict__ lse, const float* __restrict__ lseI, int64_t N,
-    int H_q, int G, float scale, float w_kl, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
-    float* __restrict__ kl, DeviceStatus* st) {
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qi,
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_ki,
+    const float* __restrict__ lse, const float* __restrict__ lseI, int64_t N, int G, float scale, float w_kl,
+    float* __restrict__ dq_idx, float* __restrict__ dk_idx, float* __restrict__ kl, DeviceStatus* st) {
   using namespace wtc;
-  constexpr int D = 128, DI = 128;
+  constexpr int DI = 128;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float lse2_s[2][kRows];   // main lse of each tile row, log2 units (two tiles in flight)
-  __shared__ float lseI2_s[2][kPos];   // lse^I of each position, log2 units
-  __shared__ int32_t tpos_s[2][kPos];  // position of each tile position, -1 past N
-  __shared__ float kl_s[16][4];        // per warp, the KL sums of its warpgroup's 4 positions
-  const uint32_t bar_s0 = sb + kBar, bar_q = sb + kBar + 16, bar_drain = sb + kBar + 24;  // bar_s0 + 8 b
+  __shared__ __align__(16) float lse2_s[kSlots][kRows];   // main lse of each tile row, log2 units
+  __shared__ float lseI2_s[kSlots][kPos];   // lse^I of each position, log2 units
+  __shared__ int32_t tpos_s[kSlots][kPos];  // position of each tile position, -1 past N
+  const uint32_t bar = sb + kBar;
+  const uint32_t kv_full = bar;
+  auto full = [&](int i) { return bar + 8u * (1 + i); };     // producer -> MMA, softmax (count 32 + tx)
+  auto empty = [&](int i) { return bar + 8u * (4 + i); };    // softmax -> producer (count 8)
+  auto s_full = [&](int i) { return bar + 8u * (7 + i); };   // MMA -> softmax (commit)
+  auto s_empty = [&](int i) { return bar + 8u * (9 + i); };  // softmax -> MMA (count 8)
+  // Per buffer parity, so that no warp can reach a barrier's next use before every arrival of this one:
+  auto dz_full = [&](int i) { return bar + 8u * (11 + i); };  // softmax -> MMA (count 8): dzI of tile written
+  auto q_done = [&](int i) { return bar + 8u * (13 + i); };   // MMA -> softmax (commit): dk^I, dq^I done
+  auto dq_read = [&](int i) { return bar + 8u * (15 + i); };  // softmax -> MMA (count 8): dq buffer i read
+  const uint32_t drain = bar + 8u * 17;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, quarter = warp >> 2;  // TMEM lane quadrant; positions 4 quarter .. 4 quarter + 3
   const int g = (int)(blockIdx.x % (unsigned)G);
   const int64_t j0 = (int64_t)(blockIdx.x / (unsigned)G) * kKeys;  // launch order: the heaviest key tiles first
+  const int64_t n_qt = (N + kPos - 1) / kPos;
+  const int64_t qt0 = j0 / kPos;  // the first query tile with a position >= j0
+  const int n_tiles = (int)(n_qt - qt0);
   if (tid == 0) {
-    mbar_init(bar_s0, 1);
-    mbar_init(bar_s0 + 8, 1);
-    mbar_init(bar_q, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(full(i), 32);
+      mbar_init(empty(i), kSoftWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(s_full(i), 1);
+      mbar_init(s_empty(i), kSoftWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(dz_full(i), kSoftWarps);
+      mbar_init(q_done(i), 1);
+      mbar_init(dq_read(i), kSoftWarps);
+    }
+    mbar_init(drain, 1);
     fence_mbar_init();
     abort_flag = 0;
   }
-  if (warp == 0) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&tmem_slot), 512);
     tc_fence_before();
   }
@@ -152,226 +214,206 @@ __global__ void __launch_bounds__(wtc::kThreads, 1) warmup_grad_tc_kernel(
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
   const float kLog2e = 1.4426950408889634f;
-  const float sl2 = scale * kLog2e;             // main scores -> log2 units
-  const float sI = 1.0f / sqrtf((float)DI);
-  const float sI2 = sI * kLog2e;                // index logits -> log2 units
-  const float kLn2 = 0.69314718055994530942f;
 
-  // the CTA's keys: K (group g) and K^I, 128 x 128 each
-  for (int i = tid; i < kKeys * 16; i += kThreads) {
-    const int r = i >> 4, c = (i & 15) * 8;
-    const int64_t j = j0 + r;
-    const bool ok = j < N;
-    cp_async_16(sm + kK + off(r, c, kChunk128), ok ? kc + (j * G + g) * D + c : kc, ok ? 16 : 0);
-    cp_async_16(sm + kKI + off(r, c, kChunk128), ok ? k_idx + j * DI + c : k_idx, ok ? 16 : 0);
-  }
-  const int64_t n_qt = (N + kPos - 1) / kPos;
-  const int64_t qt0 = j0 / kPos;  // the first query tile with a position >= j0
-  const int64_t n_tiles = n_qt - qt0;
-  // rows of query tile n (qt0 + n): Q rows r = 8 p + h (position p, head g*8 + h) into Q buffer n % 2,
-  // Q^I rows p into Q^I buffer n % 3 (Q^I is read until that tile's dk^I product, one tile later than Q)
-  auto issue_q = [&](int64_t n) {
-    const int64_t t0 = (qt0 + n) * kPos;
-    const int bq = (int)(n & 1), bi = (int)(n % 3);
+  if (warp == kWarpLoad) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_qi);
+      mbar_arrive_expect_tx(kv_full, (uint32_t)(2 * kTile128));
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(sb + kK + c * kChunk128, &tm_k, c * 64, g, (int32_t)j0, kv_full);
+        tma_load_3d(sb + kKI + c * kChunk128, &tm_ki, c * 64, 0, (int32_t)j0, kv_full);
+      }
+    }
+    int issued = 0;
+    for (int n = 0; n < n_tiles; ++n) {
+      const int slot = n % kSlots;
+      if (n >= kSlots && !warp_wait(empty(slot), (uint32_t)((n / kSlots - 1) & 1), abort, st, 0xA10)) break;
+      const int64_t t0 = (qt0 + n) * kPos;
+      // row info: lse of rows 8 p + h (coalesced along p), and lse^I and the position of each p
 #pragma unroll
-    for (int m = 0; m < kRows * 16 / kThreads; ++m) {
-      const int i = tid + m * kThreads;
-      const int r = i >> 4, c = (i & 15) * 8;
-      const int64_t t = t0 + (r >> 3);
-      const bool ok = t < N;
-      cp_async_16(sm + kQ + bq * kTile128 + off(r, c, kChunk128),
-                  ok ? q + (t * H_q + (int64_t)g * 8 + (r & 7)) * D + c : q, ok ? 16 : 0);
-    }
-    if (tid < kPos * 16) {
-      const int r = tid >> 4, c = (tid & 15) * 8;  // 16 rows x 16 units
-      const int64_t t = t0 + r;
-      const bool ok = t < N;
-      cp_async_16(sm + kQI + bi * kTile16 + off(r, c, kChunk16), ok ? q_idx + (t * G + g) * DI + c : q_idx,
-                  ok ? 16 : 0);
-    }
-  };
-  // row info of tile n into registers, then into shared-memory slot n % 2
-  float nt_lse = 0.f, nt_lseI = 0.f;
-  int32_t nt_t = -1;
-  auto load_row_info = [&](int64_t n) {
-    const int64_t t0 = (qt0 + n) * kPos;
-    if (tid < kRows) {
-      const int64_t t = t0 + (tid >> 3);
-      nt_lse = t < N ? __ldg(lse + ((int64_t)g * 8 + (tid & 7)) * N + t) : 0.f;
-    } else if (tid < kRows + kPos) {
-      const int64_t t = t0 + (tid - kRows);
-      nt_t = t < N ? (int32_t)t : -1;
-      nt_lseI = t < N ? __ldg(lseI + (int64_t)g * N + t) : 0.f;
-    }
-  };
-  auto store_row_info = [&](int slot) {
-    if (tid < kRows) {
-      lse2_s[slot][tid] = nt_lse * kLog2e;
-    } else if (tid < kRows + kPos) {
-      tpos_s[slot][tid - kRows] = nt_t;
-      lseI2_s[slot][tid - kRows] = nt_lseI * kLog2e;
-    }
-  };
-  // S^T and Z^T of tile n into TMEM buffer n % 2
-  auto issue_sz = [&](int64_t n) {
-    const int b = (int)(n & 1);
-    const uint32_t qb = sb + kQ + b * kTile128, qib = sb + kQI + (int)(n % 3) * kTile16;
-    tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-      const int c = ks >> 2, kk = ks & 3;
-      mma_bf16_ss(tmem + kTS + b * 128, umma_desc_kmajor(sb + kK + c * kChunk128 + kk * 32, 128),
-                  umma_desc_kmajor(qb + c * kChunk128 + kk * 32, 128), kIdescS, ks > 0);
-      mma_bf16_ss(tmem + kTZ + b * 16, umma_desc_kmajor(sb + kKI + c * kChunk128 + kk * 32, 128),
-                  umma_desc_kmajor(qib + c * kChunk16 + kk * 32, 128), kIdescZ, ks > 0);
-    }
-    umma_commit(bar_s0 + 8 * b);
-  };
-  issue_q(0);
-  cp_async_commit();
-  if (n_tiles > 1) issue_q(1);
-  cp_async_commit();
-  load_row_info(0);
-  store_row_info(0);
-  if (n_tiles > 1) load_row_info(1);
-  cp_async_wait<1>();  // the keys and tile 0's rows
-  fence_proxy_async_smem();
-  __syncthreads();
-  bool issued = false;
-  if (warp == 0 && lane == 0) {
-    issue_sz(0);
-    issued = true;
-  }
-  for (int64_t n = 0; n < n_tiles; ++n) {
-    const int b = (int)(n & 1);
-    // ---- the next tile's S^T and Z^T go to the tensor cores before this tile's softmax
-    if (n + 1 < n_tiles) {
-      store_row_info(b ^ 1);
-      cp_async_wait<0>();  // tile n+1's rows
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (warp == 0 && lane == 0) issue_sz(n + 1);
-    }
-    // every thread takes the same branch (the TMEM loads and shuffles below are warp-collective)
-    if (!__syncthreads_and(mbar_wait(bar_s0 + 8 * b, (uint32_t)((n >> 1) & 1), abort, st, 0xA01))) break;
-    // S^T(n) is done, so its Q buffer is free: tile n+2's rows stream in now
-    if (n + 2 < n_tiles) {
-      issue_q(n + 2);
-      load_row_info(n + 2);
-    }
-    cp_async_commit();
-    // ---- teacher, index probabilities, dzI and KL: thread = key, its warpgroup's 4 positions
-    {
-      tc_fence_after();
-      const int key = quad * 32 + lane;
-      const int64_t j = j0 + key;
-      const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-      uint32_t sx[32], zx[4];
-      tmem_ld_x32(tmem + lane_base + kTS + b * 128 + quarter * 32, sx);
-      wtc::tmem_ld_x4(tmem + lane_base + kTZ + b * 16 + quarter * 4, zx);
-      tmem_ld_wait();
-      reg_fence32(sx);
-      wtc::reg_fence4(zx);
-      float dz[4], klv[4];
-#pragma unroll
-      for (int pl = 0; pl < 4; ++pl) {
-        const int p = quarter * 4 + pl;
-        const int32_t t = tpos_s[b][p];
-        const bool valid = t >= 0 && j <= (int64_t)t;
-        float ps = 0.f;
-#pragma unroll
-        for (int hd = 0; hd < 8; ++hd) {
-          const int r = pl * 8 + hd;  // column within this warpgroup's 32
-          ps += ex2_approx(fmaf(__uint_as_float(sx[r]), sl2, -lse2_s[b][quarter * 32 + r]));
+      for (int m = 0; m < kRows / 32; ++m) {
+        const int idx = lane + 32 * m, h = idx >> 4, p = idx & 15;
+        const int64_t t = t0 + p;
+        lse2_s[slot][p * 8 + h] = t < N ? __ldg(lse + ((int64_t)g * 8 + h) * N + t) * kLog2e : 0.f;
+      }
+      if (lane < kPos) {
+        const int64_t t = t0 + lane;
+        tpos_s[slot][lane] = t < N ? (int32_t)t : -1;
+        lseI2_s[slot][lane] = t < N ? __ldg(lseI + (int64_t)g * N + t) * kLog2e : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full(slot), kTileTx);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(sb + kQ + slot * kTile128 + c * kChunk128, &tm_q, c * 64, g * 8, (int32_t)t0, full(slot));
+          tma_load_3d(sb + kQI + slot * kTile16 + c * kChunk16, &tm_qi, c * 64, g, (int32_t)t0, full(slot));
         }
-        const float pbar = valid ? ps * 0.125f : 0.f;
-        const float zl2 = fmaf(__uint_as_float(zx[pl]), sI2, -lseI2_s[b][p]);  // log2 pI
-        const float pI = valid ? ex2_approx(zl2) : 0.f;
-        dz[pl] = w_kl * (pI - pbar);
-        klv[pl] = pbar > 0.f ? pbar * (wtc::lg2_approx(pbar) - zl2) * kLn2 : 0.f;
+      } else {
+        mbar_arrive(full(slot));
       }
-      const uint32_t pk[2] = {pack_bf16x2(dz[0], dz[1]), pack_bf16x2(dz[2], dz[3])};
-      wtc::tmem_st_x2(tmem + lane_base + kTDZ + quarter * 2, pk);
+      issued = n + 1;
+    }
+    // after an abort: the copies still in flight land before the CTA exits
+    if (*abort && lane == 0)
+      for (int n = max(0, issued - kSlots); n < issued; ++n)
+        mbar_wait(full(n % kSlots), (uint32_t)((n / kSlots) & 1), nullptr, st, 0xAF2);
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    bool ok = warp_wait(kv_full, 0, abort, st, 0xA20);
+    bool issued = false;
+    for (int n = 0; ok && n <= n_tiles; ++n) {
+      if (n < n_tiles) {  // S^T(n), Z^T(n) into TMEM buffer n % 2
+        const int slot = n % kSlots, b = n & 1;
+        if (!(ok = warp_wait(full(slot), (uint32_t)((n / kSlots) & 1), abort, st, 0xA21))) break;
+        if (n >= 2 && !(ok = warp_wait(s_empty(b), (uint32_t)((n / 2 - 1) & 1), abort, st, 0xA22))) break;
+        if (lane == 0) {
+          tc_fence_after();
 #pragma unroll
-      for (int pl = 0; pl < 4; ++pl)
-        *reinterpret_cast<uint16_t*>(sm + kDZ + off(quarter * 4 + pl, key, kChunk16)) =
-            (uint16_t)(pack_bf16x2(dz[pl], 0.f) & 0xFFFFu);
-#pragma unroll
-      for (int pl = 0; pl < 4; ++pl) {
-        float v = klv[pl];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) kl_s[warp][pl] = v;
+          for (int ks = 0; ks < 8; ++ks) {
+            const int c = ks >> 2, kk = ks & 3;
+            mma_bf16_ss(tmem + kTS + b * 128, umma_desc_kmajor(sb + kK + c * kChunk128 + kk * 32, 128),
+                        umma_desc_kmajor(sb + kQ + slot * kTile128 + c * kChunk128 + kk * 32, 128), kIdescS, ks > 0);
+            mma_bf16_ss(tmem + kTZ + b * 16, umma_desc_kmajor(sb + kKI + c * kChunk128 + kk * 32, 128),
+                        umma_desc_kmajor(sb + kQI + slot * kTile16 + c * kChunk16 + kk * 32, 128), kIdescZ, ks > 0);
+          }
+          umma_commit(s_full(b));
+        }
+        issued = true;
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-    }
-    __syncthreads();
-    // ---- dk^I += dzI^T Q^I and dq^I^T = K^I^T dzI^T
-    if (warp == 0 && lane == 0) {
-      tc_fence_after();
-      mma_bf16_ts(tmem + kTDK, tmem + kTDZ, umma_desc_mnmajor_sw128(sb + kQI + (int)(n % 3) * kTile16, kChunk16),
-                  kIdescDK, n > 0 ? 1u : 0u);
+      if (n >= 1) {  // dk^I += dzI^T Q^I and dq^I^T = K^I^T dzI^T of tile m = n - 1 (buffers m % 2)
+        const int m = n - 1, slot = m % kSlots, bm = m & 1;
+        if (!(ok = warp_wait(dz_full(bm), (uint32_t)((m / 2) & 1), abort, st, 0xA23))) break;
+        if (m >= 2 && !(ok = warp_wait(dq_read(bm), (uint32_t)((m / 2 - 1) & 1), abort, st, 0xA24))) break;
+        if (lane == 0) {
+          tc_fence_after();
+          mma_bf16_ts(tmem + kTDK, tmem + kTDZ + bm * 8,
+                      umma_desc_mnmajor_sw128(sb + kQI + slot * kTile16, kChunk16), kIdescDK, m > 0 ? 1u : 0u);
 #pragma unroll
-      for (int ks = 0; ks < kKeys / 16; ++ks) {
-        const int c = ks >> 2, kk = ks & 3;
-        mma_bf16_ss(tmem + kTDQ, umma_desc_mnmajor_sw128(sb + kKI + ks * 16 * 128, kChunk128),
-                    umma_desc_kmajor(sb + kDZ + c * kChunk16 + kk * 32, 128), kIdescDQ, ks > 0);
+          for (int ks = 0; ks < kKeys / 16; ++ks) {
+            const int c = ks >> 2, kk = ks & 3;
+            mma_bf16_ss(tmem + kTDQ + bm * 16, umma_desc_mnmajor_sw128(sb + kKI + ks * 16 * 128, kChunk128),
+                        umma_desc_kmajor(sb + kDZ + bm * kTile16 + c * kChunk16 + kk * 32, 128), kIdescDQ, ks > 0);
+          }
+          umma_commit(q_done(bm));
+        }
       }
-      umma_commit(bar_q);
     }
-    if (tid < kPos) {  // the tile's KL sums: the four warps of the position's warpgroup
-      const int qg = tid >> 2, pl = tid & 3;
-      const float v = kl_s[4 * qg][pl] + kl_s[4 * qg + 1][pl] + kl_s[4 * qg + 2][pl] + kl_s[4 * qg + 3][pl];
-      const int32_t t = tpos_s[b][tid];
-      if (t >= 0 && v != 0.f) red_add(kl + (int64_t)g * N + t, v);
+    if (!ok && issued && lane == 0) {  // let the MMAs in flight finish before TMEM is released
+      umma_commit(drain);
+      mbar_wait(drain, 0, nullptr, st, 0xAF1);
     }
-    if (!__syncthreads_and(mbar_wait(bar_q, (uint32_t)(n & 1), abort, st, 0xA02))) break;
-    {
-      tc_fence_after();
-      // dq^I: thread = dim (TMEM lane), its warpgroup's 4 positions
-      const int dim = quad * 32 + lane;
-      uint32_t x[4];
-      wtc::tmem_ld_x4(tmem + ((uint32_t)(quad * 32) << 16) + kTDQ + quarter * 4, x);
-      tmem_ld_wait();
-      wtc::reg_fence4(x);
-#pragma unroll
-      for (int pl = 0; pl < 4; ++pl) {
-        const int32_t t = tpos_s[b][quarter * 4 + pl];
-        if (t >= 0) red_add(dq_idx + ((int64_t)t * G + g) * DI + dim, sI * __uint_as_float(x[pl]));
-      }
-      tc_fence_before();
-    }
-    __syncthreads();
-    if (*abort) break;
-  }
-  // ---- dk^I of the CTA's keys: thread = key, its warpgroup's 32 dims; the groups add up in dk_idx
-  if (!*abort) {
-    tc_fence_after();
+  } else {
+    // ---------------------------------------------------------------- softmax warps: thread = key
+    const int quad = warp & 3, qtr = warp >> 2;  // TMEM lane quadrant; positions 4 qtr .. 4 qtr + 3
     const int key = quad * 32 + lane;
     const int64_t j = j0 + key;
-    {
-      const int cc = quarter;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const float sl2 = scale * kLog2e;  // main scores -> log2 units
+    const float sI = 1.0f / sqrtf((float)DI);
+    const float sI2 = sI * kLog2e;     // index logits -> log2 units
+    const float kLn2 = 0.69314718055994530942f;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    bool ok = true;
+    // iteration n: the softmax of tile n, then the dq^I of tile n - 1 (whose products ran meanwhile)
+    for (int n = 0; n <= n_tiles; ++n) {
+      if (n < n_tiles) {
+        const int b = n & 1, slot = n % kSlots;
+        if (!(ok = warp_wait(s_full(b), (uint32_t)((n / 2) & 1), abort, st, 0xA30))) break;
+        if (!(ok = warp_wait(full(slot), (uint32_t)((n / kSlots) & 1), abort, st, 0xA31))) break;
+        tc_fence_after();
+        uint32_t sx[32], zx[4];
+        tmem_ld_x32(tmem + lane_base + kTS + b * 128 + qtr * 32, sx);
+        tmem_ld_x4(tmem + lane_base + kTZ + b * 16 + qtr * 4, zx);
+        tmem_ld_wait();
+        reg_fence32(sx);
+        reg_fence4(zx);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty(b));  // the MMA may overwrite this S^T / Z^T buffer
+        float dz[4], klv[4];
+        const float2* lse2p = reinterpret_cast<const float2*>(&lse2_s[slot][qtr * 32]);
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl) {
+          const int p = qtr * 4 + pl;
+          const int32_t t = tpos_s[slot][p];
+          const bool valid = t >= 0 && j <= (int64_t)t;
+          float ps = 0.f;
+#pragma unroll
+          for (int hd = 0; hd < 8; hd += 2) {
+            const int r = pl * 8 + hd;  // column within this warpgroup's 32
+            const float2 l2 = lse2p[r >> 1];
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sx[r]), __uint_as_float(sx[r + 1])), sl2x2, f2_pack(-l2.x, -l2.y)),
+                      a0, a1);
+            ps += ex2_approx(a0) + ex2_approx(a1);
+          }
+          const float pbar = valid ? ps * 0.125f : 0.f;
+          const float zl2 = fmaf(__uint_as_float(zx[pl]), sI2, -lseI2_s[slot][p]);  // log2 pI
+          const float pI = valid ? ex2_approx(zl2) : 0.f;
+          dz[pl] = w_kl * (pI - pbar);
+          klv[pl] = pbar > 0.f ? pbar * (lg2_approx(pbar) - zl2) * kLn2 : 0.f;
+        }
+        // dzI to TMEM (A of dk^I) and to the K-major shared tile (B of dq^I), buffer n % 2; their last
+        // readers, the products of tile n - 2, completed before this warp read that tile's dq^I
+        const uint32_t pk[2] = {pack_bf16x2(dz[0], dz[1]), pack_bf16x2(dz[2], dz[3])};
+        tmem_st_x2(tmem + lane_base + kTDZ + b * 8 + qtr * 2, pk);
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl)
+          *reinterpret_cast<uint16_t*>(sm + kDZ + b * kTile16 + off(qtr * 4 + pl, key, kChunk16)) =
+              (uint16_t)(pack_bf16x2(dz[pl], 0.f) & 0xFFFFu);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dz_full(b));
+        // this warp's KL sums over its 32 keys, one reduction per position
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl) {
+          float v = klv[pl];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          const int32_t t = tpos_s[slot][qtr * 4 + pl];
+          if (lane == 0 && t >= 0 && v != 0.f) red_add(kl + (int64_t)g * N + t, v);
+        }
+      }
+      if (n >= 1) {  // dq^I of tile m = n - 1: thread = dim (TMEM lane), its warpgroup's 4 positions
+        const int m = n - 1, bm = m & 1, slot = m % kSlots;
+        if (!(ok = warp_wait(q_done(bm), (uint32_t)((m / 2) & 1), abort, st, 0xA32))) break;
+        tc_fence_after();
+        uint32_t x[4];
+        tmem_ld_x4(tmem + lane_base + kTDQ + bm * 16 + qtr * 4, x);
+        tmem_ld_wait();
+        reg_fence4(x);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_read(bm));  // the product of tile m + 2 may overwrite these columns
+#pragma unroll
+        for (int pl = 0; pl < 4; ++pl) {
+          const int32_t t = tpos_s[slot][qtr * 4 + pl];
+          if (t >= 0) red_add(dq_idx + ((int64_t)t * G + g) * DI + key, sI * __uint_as_float(x[pl]));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(slot));  // tile m's Q, Q^I and row info are no longer read
+      }
+    }
+    // dk^I of the CTA's keys: thread = key, its warpgroup's 32 dims; the groups add up in dk_idx
+    if (ok && n_tiles > 0) {
+      tc_fence_after();
       uint32_t x[32];
-      tmem_ld_x32(tmem + ((uint32_t)(quad * 32) << 16) + kTDK + cc * 32, x);
+      tmem_ld_x32(tmem + lane_base + kTDK + qtr * 32, x);
       tmem_ld_wait();
       if (j < N)
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
-          wtc::red_add4(dk_idx + j * DI + cc * 32 + e, sI * __uint_as_float(x[e]), sI * __uint_as_float(x[e + 1]),
-                        sI * __uint_as_float(x[e + 2]), sI * __uint_as_float(x[e + 3]));
+          red_add4(dk_idx + j * DI + qtr * 32 + e, sI * __uint_as_float(x[e]), sI * __uint_as_float(x[e + 1]),
+                   sI * __uint_as_float(x[e + 2]), sI * __uint_as_float(x[e + 3]));
+      tc_fence_before();
     }
-    tc_fence_before();
   }
-  cp_async_wait<0>();  // no copy of ours is left in flight when the CTA exits
   __syncthreads();
-  if (warp == 0) {
-    if (lane == 0 && *abort && issued) {  // let the MMAs in flight finish before TMEM is released
-      umma_commit(bar_drain);
-      mbar_wait(bar_drain, 0, nullptr, st, 0xAF1);
-    }
-    __syncwarp();
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -795,17 +837,29 @@ cudaError_t launch_warmup_fwd_tc(const void* q, const void* k, const void* v, co
 cudaError_t launch_warmup_grad_tc(const void* q, const void* k, const void* q_idx, const void* k_idx, int64_t N,
                                   int H_q, int H_kv, float scale, float kl_weight, const float* lse, const float* lseI,
                                   float* dq_idx, float* dk_idx, float* kl, DeviceStatus* st, cudaStream_t s) {
+  constexpr int D = 128, DI = 128;
+  alignas(64) unsigned char tq[128], tqi[128], tk[128], tki[128];
+  // q [N][H_q][d] as boxes {64 dims, 8 heads, 16 positions}; q^I [N][G][d_I] as {64, 1, 16};
+  // k [N][H_kv][d] as {64, 1, 128 keys}; k^I [N][d_I] as {64, 1, 128}: each box lands as one 64-column chunk
+  // of the kernels' 128B-swizzled K-major tiles
+  if (!encode_tmap_3d(tq, q, D, (uint64_t)H_q, (uint64_t)N, D * 2, (uint64_t)H_q * D * 2, 64, 8, 16, 128) ||
+      !encode_tmap_3d(tqi, q_idx, DI, (uint64_t)H_kv, (uint64_t)N, DI * 2, (uint64_t)H_kv * DI * 2, 64, 1, 16, 128) ||
+      !encode_tmap_3d(tk, k, D, (uint64_t)H_kv, (uint64_t)N, D * 2, (uint64_t)H_kv * D * 2, 64, 1, 128, 128) ||
+      !encode_tmap_3d(tki, k_idx, DI, 1, (uint64_t)N, DI * 2, DI * 2, 64, 1, 128, 128))
+    return cudaErrorInvalidValue;
   cudaError_t e;
-  if ((e = cudaMemsetAsync(dq_idx, 0, (size_t)N * H_kv * 128 * 4, s)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(dk_idx, 0, (size_t)N * 128 * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dq_idx, 0, (size_t)N * H_kv * DI * 4, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(dk_idx, 0, (size_t)N * DI * 4, s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(kl, 0, (size_t)H_kv * N * 4, s)) != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(warmup_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 wtc::kBytes)) != cudaSuccess)
     return e;
+  (void)H_q;
   const int64_t n_kt = (N + wtc::kKeys - 1) / wtc::kKeys;
   warmup_grad_tc_kernel<<<(unsigned)(n_kt * H_kv), wtc::kThreads, wtc::kBytes, s>>>(
-      (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)q_idx, (const uint16_t*)k_idx, lse, lseI, N, H_q,
-      H_kv, scale, kl_weight, dq_idx, dk_idx, kl, st);
+      *reinterpret_cast<const CUtensorMap*>(tq), *reinterpret_cast<const CUtensorMap*>(tqi),
+      *reinterpret_cast<const CUtensorMap*>(tk), *reinterpret_cast<const CUtensorMap*>(tki), lse, lseI, N, H_kv,
+      scale, kl_weight, dq_idx, dk_idx, kl, st);
   return cudaGetLastError();
 }
 
