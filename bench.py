@@ -836,15 +836,19 @@ def main():
             fi = (oc.N ** 2 / 2.0) * oc.G * oc.d_I * 2.0
             fm = oc.N * oc.H_q * oc.k * oc.Bk * oc.d * 4.0
             tf = (fi + fm) / (o_ms / 1000.0) / 1e12
+            # a timed region of a second or more runs under the power cap: the sustained peak applies there
+            long_region = o_ms * o["steps"] > 1000.0
+            pk, pk_src = (peak_sus, "%s bf16_tflops_sustained (the timed region lasts over a second)" % peak_src) \
+                if long_region else (peak_t, burst_src)
             line[nm] = {"metric": "prefill tokens/s (msa_prefill: select, invert, schedule, tiles, combine)",
                         "value": ws * oc.N / (o_ms / 1000.0), "unit": "tokens/s", "ms_per_step": o_ms,
                         "steps": o["steps"], "workload": workload_name(oc),
                         "stages_ms": {"select": o["sel_ms"], "attend": o["att_ms"]},
-                        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak_t, "unit": "TFLOP/s",
-                                     "frac": tf / peak_t, "traffic": None,
+                        "roofline": {"bound": "tensor", "achieved": tf, "peak": pk, "unit": "TFLOP/s",
+                                     "frac": tf / pk, "frac_of_burst": tf / peak_t, "traffic": None,
                                      "algorithmic": "(N^2/2)*G*d_I*2 + N*H_q*k*Bk*d*4 = %.4g + %.4g FLOP per step"
                                                     % (fi, fm),
-                                     "peak_source": burst_src},
+                                     "peak_source": pk_src},
                         "gpu_launches": prefill_launches(oc) * o["steps"]}
     if not args.no_warmup:
         wu = bench_warmup(args, dist, torch)

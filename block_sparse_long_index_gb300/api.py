@@ -131,14 +131,17 @@ def prefill_from_host(run: MsaPrefill, host_inputs, dev_inputs, host_out, stream
 class PrefillHostPipeline:
     """Prefill steps from pinned host buffers to pinned host buffers, with the copies overlapped.
 
-    Three streams: host->device copies, compute, device->host copies.  Step i's
-    inputs land in one of two device input sets while step i-1 computes on the
-    other; its index inputs (q_idx, k_idx) are copied first so that the select
-    can start while q, k and v are still in flight.  Step i's out and lse go to
-    one of two device output sets and are copied back while step i+1 computes
-    into the other, so the compute stream never waits for a device->host copy
-    of the step before.  Every step still copies all of its inputs in and all of
-    its outputs (out, lse) out."""
+    Copies run on two host->device and two device->host streams (each direction
+    then keeps two copy engines busy, which on this GPU's host link roughly
+    doubles what one stream moves while the other direction is busy too), and
+    the prefill on the compute stream.  Step i's inputs land in one of two
+    device input sets while step i-1 computes on the other; its index inputs
+    (q_idx, k_idx) are copied first so that the select can start while q, k and
+    v are still in flight.  Step i's out and lse go to one of two device output
+    sets and are copied back while step i+1 computes into the other, so the
+    compute stream never waits for a device->host copy of the step before.
+    Every step still copies all of its inputs in and all of its outputs (out,
+    lse) out."""
 
     NAMES = ("q_idx", "k_idx", "q", "k", "v")
 
@@ -147,7 +150,8 @@ class PrefillHostPipeline:
         self.dev = [{n: torch.empty(_input_shape(run, n), dtype=torch.bfloat16, device=device) for n in self.NAMES}
                     for _ in range(2)]
         self.outs = [(run.out, run.lse), (torch.empty_like(run.out), torch.empty_like(run.lse))]
-        self.h2d, self.d2h = torch.cuda.Stream(device=device), torch.cuda.Stream(device=device)
+        self.h2d = [torch.cuda.Stream(device=device) for _ in range(2)]
+        self.d2h = [torch.cuda.Stream(device=device) for _ in range(2)]
 
     def __call__(self, host_inputs, host_outputs, stream=None):
         """host_inputs: list of dicts of pinned bf16 tensors (q, k, v, q_idx, k_idx), one per step;
@@ -155,38 +159,51 @@ class PrefillHostPipeline:
         work is queued; it is ordered before later work on `stream` (default: the current stream)."""
         comp = torch.cuda.current_stream() if stream is None else stream
         E = torch.cuda.Event
-        self.h2d.wait_stream(comp)
-        self.d2h.wait_stream(comp)
+        for st in self.h2d + self.d2h:
+            st.wait_stream(comp)
+        half = self.run.N // 2
         attn_done, d2h_done = {}, {}
         for i, (hin, hout) in enumerate(zip(host_inputs, host_outputs)):
             dev = self.dev[i % 2]
-            idx_in, qkv_in = E(), E()
-            with torch.cuda.stream(self.h2d):
-                if i - 2 in attn_done:  # the attention of step i-2 has finished reading this input set
-                    self.h2d.wait_event(attn_done[i - 2])
-                for n in ("q_idx", "k_idx"):
-                    dev[n].copy_(hin[n], non_blocking=True)
-                idx_in.record(self.h2d)
-                for n in ("q", "k", "v"):
-                    dev[n].copy_(hin[n], non_blocking=True)
-                qkv_in.record(self.h2d)
+            idx_in, qkv_in = E(), [E(), E()]
+            for j, st in enumerate(self.h2d):
+                with torch.cuda.stream(st):
+                    if i - 2 in attn_done:  # the attention of step i-2 has finished reading this input set
+                        st.wait_event(attn_done[i - 2])
+                    if j == 0:
+                        for n in ("q_idx", "k_idx"):
+                            dev[n].copy_(hin[n], non_blocking=True)
+                        idx_in.record(st)
+                        dev["q"][:half].copy_(hin["q"][:half], non_blocking=True)
+                        dev["k"].copy_(hin["k"], non_blocking=True)
+                    else:
+                        dev["q"][half:].copy_(hin["q"][half:], non_blocking=True)
+                        dev["v"].copy_(hin["v"], non_blocking=True)
+                    qkv_in[j].record(st)
             comp.wait_event(idx_in)
             self.run.select(dev["q_idx"], dev["k_idx"], stream=comp)
-            comp.wait_event(qkv_in)
-            if i - 2 in d2h_done:  # out and lse of step i-2 (this output set) are on the host
-                comp.wait_event(d2h_done[i - 2])
+            for ev in qkv_in:
+                comp.wait_event(ev)
+            for ev in d2h_done.get(i - 2, ()):  # out and lse of step i-2 (this output set) are on the host
+                comp.wait_event(ev)
             out, lse = self.outs[i % 2]
             self.run.attend(dev["q"], dev["k"], dev["v"], stream=comp, out=out, lse=lse)
             attn_done[i] = E()
             attn_done[i].record(comp)
-            with torch.cuda.stream(self.d2h):
-                self.d2h.wait_event(attn_done[i])
-                hout["out"].copy_(out, non_blocking=True)
-                hout["lse"].copy_(lse, non_blocking=True)
-                d2h_done[i] = E()
-                d2h_done[i].record(self.d2h)
-        comp.wait_stream(self.h2d)
-        comp.wait_stream(self.d2h)
+            d2h_done[i] = []
+            for j, st in enumerate(self.d2h):
+                with torch.cuda.stream(st):
+                    st.wait_event(attn_done[i])
+                    if j == 0:
+                        hout["out"][:half].copy_(out[:half], non_blocking=True)
+                        hout["lse"].copy_(lse, non_blocking=True)
+                    else:
+                        hout["out"][half:].copy_(out[half:], non_blocking=True)
+                    ev = E()
+                    ev.record(st)
+                    d2h_done[i].append(ev)
+        for st in self.h2d + self.d2h:
+            comp.wait_stream(st)
         return host_outputs
 
 
