@@ -30,9 +30,9 @@
 //                 the same block, released after the run's last P V;
 //   warps 4..11   two softmax warpgroups, both on every tile: each takes one
 //                 half of the key columns and writes its P over that half;
-//   warps 12..15  epilogue warpgroup: O -> bf16 in a swizzled shared tile of
-//                 the same layout, written out by TMA stores (one box per
-//                 position when gs = 8, one per 64 dims otherwise).
+//   warps 12..15  epilogue warpgroup: O -> bf16 in a position-major, swizzled
+//                 shared tile, written out by one TMA store box per position
+//                 (its gs heads x d).
 // A position's gs rows of an atom sit at byte (pp % ppr) gs 128 of atom
 // pp / ppr; TMA applies the 128-byte swizzle by shared-memory address, so a
 // box of gs rows written there lands exactly where the 8-row atom has them.
@@ -582,7 +582,16 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     const uint32_t ocol = tmem + ((uint32_t)(quarter * 32) << 16) + L::TMEM_O;
     const bool leader = warp == kWarpEpi0;
     const uint32_t stg = sbase + L::OFF_STG;
-    const uint32_t my_row = stg + (row >> 3) * L::POS_BYTES + (row & 7) * 128;
+    // The staging tile is position-major: position p's block of SPB bytes holds
+    // chunk c of head h in its row c * GS + h, so one TMA box {64, GS, d/64, 1}
+    // stores the whole position.  Unit u of a row sits at u ^ (row address bits
+    // 7..9) (the 128B swizzle).  With two chunks and GS < 8, lanes 4 apart would
+    // share banks; those with lane bit 2 set walk their units in an order with
+    // bit GS_SHIFT flipped, which keeps every quarter-warp's stores conflict-free.
+    constexpr int SPB = L::NCD * GS * 128;
+    constexpr uint32_t FLIP = (L::NCD == 2 && GS < 8) ? (1u << GS_SHIFT) : 0u;
+    const bool flip = FLIP != 0 && ((lane >> 2) & 1);
+    const uint32_t my_blk = stg + (uint32_t)((row >> GS_SHIFT) * SPB) + (uint32_t)(row & (GS - 1)) * 128;
     bool lead_ok = true;  // the store issuer's own waits
     for (int i = 0; i < n; ++i) {
       const int ob = i % kOBufs;
@@ -609,16 +618,21 @@ __global__ void __launch_bounds__(kThreadsT, 1)
       // the staging tile is free once the previous tile's stores have read it
       if (leader) bulk_wait_read_all();
       epi_bar_sync();
-      // 16-byte unit jj of 64-column chunk c -> its 128B-swizzled place in the row
+      // 16-byte unit u of 64-column chunk c -> its 128B-swizzled place in the row
 #pragma unroll
-      for (int c = 0; c < L::NCD; ++c)
+      for (int c = 0; c < L::NCD; ++c) {
+        const uint32_t ra = my_blk + (uint32_t)(c * GS * 128);
+        const uint32_t xm = ((ra >> 7) & 7) ^ (flip ? FLIP : 0u);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          const uint32_t a = my_row + c * 1024 + ((jj ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(pk[c * 32 + jj * 4]),
-                       "r"(pk[c * 32 + jj * 4 + 1]), "r"(pk[c * 32 + jj * 4 + 2]), "r"(pk[c * 32 + jj * 4 + 3])
+          const int u0 = c * 32 + jj * 4, u1 = c * 32 + (jj ^ (int)FLIP) * 4;  // unit jj, or jj ^ FLIP
+          const uint32_t a = ra + ((jj ^ xm) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(flip ? pk[u1] : pk[u0]),
+                       "r"(flip ? pk[u1 + 1] : pk[u0 + 1]), "r"(flip ? pk[u1 + 2] : pk[u0 + 2]),
+                       "r"(flip ? pk[u1 + 3] : pk[u0 + 3])
                        : "memory");
         }
+      }
       fence_proxy_async_smem();
       epi_bar_sync();
       if (leader) {
@@ -636,13 +650,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
             if (pp >= P || (pp & 15) >= mt[pp >> 4].count) continue;
             const TileRecord& sr = mt[pp >> 4];
             const int32_t z = (int32_t)((sr.t[pp & 15] - T0) * k + sr.slot[pp & 15]);
-            const uint32_t src = stg + (pp / PPR) * L::POS_BYTES + (pp % PPR) * GS * 128;
-            if (GS == 8) {  // the position's 8 heads x d in one box
-              tma_store_4d(&tmap_po, src, 0, g * 8, 0, z);
-            } else {        // GS heads of each 64-dim chunk
-#pragma unroll
-              for (int c = 0; c < L::NCD; ++c) tma_store_4d(&tmap_po, src + c * 1024, 0, g * GS, c, z);
-            }
+            tma_store_4d(&tmap_po, stg + (uint32_t)(pp * SPB), 0, g * GS, 0, z);  // GS heads x d in one box
             any = true;
           }
           if (any) bulk_commit();
@@ -675,7 +683,7 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
   const uint64_t po_dims[4] = {64, (uint64_t)H_q, (uint64_t)L::NCD, (uint64_t)rows};
   const uint64_t qo_strides[3] = {row_bytes, 128, (uint64_t)H_q * row_bytes};
   const uint32_t q_box[4] = {64, (uint32_t)gs, gs == 8 ? (uint32_t)L::NCD : 1u, 1};
-  const uint32_t po_box[4] = {64, (uint32_t)gs, gs == 8 ? (uint32_t)L::NCD : 1u, 1};
+  const uint32_t po_box[4] = {64, (uint32_t)gs, (uint32_t)L::NCD, 1};
   if (!encode_tmap_4d(tq, q, q_dims, qo_strides, q_box, 128) ||
       !encode_tmap_3d(tk, kk, (uint64_t)D, (uint64_t)H_kv, (uint64_t)N, row_bytes, (uint64_t)H_kv * row_bytes, 64,
                       1, BK, 128) ||

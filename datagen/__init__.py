@@ -98,6 +98,9 @@ CONFIGS = {
     # profiler capture of it sees DRAM traffic that scales with N to the 128K workload
     "prefill_16k": Config("prefill_16k", "prefill", N=16384, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
                           needles=4, index=8),
+    # the 32K head layout (gs = 4) at N = 16K: q (134 MB) is larger than L2 and the call holds ~2.5 GB
+    "prefill_16k_gs4": Config("prefill_16k_gs4", "prefill", N=16384, H_q=32, H_kv=8, d=128, d_I=128, Bk=128,
+                              k=16, needles=4, index=9),
     "prefill_1m": Config("prefill_1m", "prefill", N=1 << 20, H_q=64, H_kv=8, d=128, d_I=128, Bk=128, k=16,
                          needles=16, index=4),
 }
