@@ -13,12 +13,13 @@
 //      no shared-memory staging is needed) and scores all groups at once
 //      (16 keys x 8 groups x d_I per mma chain).  Block maxima meet in shared
 //      memory (an atomic max on order-preserving integers joins the two parts
-//      of a block split between warps); each CTA then keeps its top-(k-1)
-//      blocks per group, and the last CTA of a sequence to finish merges the
-//      CTAs' lists into that sequence's block sets.
-//   2. attend (+ combine): per (sequence, group, slot) one CTA reads that
-//      block's K/V rows and produces each group head's partial (O, lse); the
-//      last CTA of a (sequence, group) merges the k partials by their lse.
+//      of a block split between warps); each CTA then writes its top-(k-1)
+//      blocks per group as a list sorted best first.
+//   2. select + attend (+ combine): per (sequence, group, slot) one CTA merges
+//      the group's lists up to its slot (every CTA of the group does the same
+//      merge, from shared memory, so no single CTA holds the others up), reads
+//      that block's K/V rows and produces each group head's partial (O, lse);
+//      the last CTA of a (sequence, group) merges the k partials by their lse.
 //      It is launched as a programmatic dependent of the scan, so its launch
 //      overlaps the scan's tail.
 #include <math.h>
@@ -35,7 +36,7 @@ namespace {
 constexpr int kScanThreads = 256;  // 8 warps, two CTAs per SM
 constexpr int kScanWarps = kScanThreads / 32;
 constexpr int kGroupsPerMma = 8;    // mma n = 8 groups
-constexpr int kMergeListsPerLane = 8;  // last-CTA merge: splits <= 32 * 8
+constexpr int kMergeListsPerLane = 8;  // list merge: splits <= 32 * 8
 constexpr int kMaxCtaBlocks = 2048;     // block maxima kept in shared memory per scan CTA
 
 // dims of fragment column kf (0..15) in k-step ks of the bf16 scan: see the load pattern below
@@ -96,17 +97,15 @@ __device__ __forceinline__ void load_keys16(uint4 (&v)[RB / 64][2], const uint8_
 template <int DI, int BK, bool PAGED, bool F8, int CAP>
 __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     const uint8_t* __restrict__ q_idx_t, const uint8_t* __restrict__ k_idx_cache,
-    const int32_t* __restrict__ ctx_len, int64_t ctx_max, CacheMap map, int G, int k, int splits, bool staged,
-    uint64_t* __restrict__ cand, unsigned int* __restrict__ tickets, int32_t* __restrict__ block_idx,
-    DeviceStatus* st) {
+    const int32_t* __restrict__ ctx_len, int64_t ctx_max, CacheMap map, int G, int k, int splits,
+    uint64_t* __restrict__ cand, DeviceStatus* st) {
   constexpr int RB = DI * (F8 ? 1 : 2);  // bytes per index row
   constexpr int NQ = RB / 64;            // 16-byte pieces per lane and row
   constexpr int KS = 2 * NQ;             // MMA k-steps per 16-key chunk
   static_assert(NQ >= 1, "index rows of at least 64 bytes");
   constexpr int CPB = BK / 16;  // chunks per block
-  // [blocks of this CTA][8 groups], ordered_bits of the block maxima; in the last CTA, later the staged lists
+  // [blocks of this CTA][8 groups], ordered_bits of the block maxima
   extern __shared__ __align__(16) uint32_t bmax_s[];
-  __shared__ int s_last;
   griddep_launch_dependents();  // the attention grid may be scheduled once every scan CTA is resident
   const int seq = blockIdx.y, split = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -231,75 +230,15 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     }
   }
 
-  // the last CTA of this sequence to get here merges every CTA's lists
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = ticket_acq_rel(&tickets[seq]) == (unsigned)(splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  // with room in shared memory, each group's lists (contiguous in cand) are
-  // first copied there with 16-byte cp.async (L2 only), so the rounds below read
-  // the next head of a list from shared memory rather than from L2
-  uint64_t* stage = reinterpret_cast<uint64_t*>(bmax_s);
-  if (staged) {
-    const int n16 = splits * kp / 2;  // 16-byte pieces per group
-    for (int i = tid; i < G * n16; i += kScanThreads) {
-      const int gg = i / n16, j = i % n16;
-      cp_async_16(stage + ((int64_t)gg * splits * kp) + 2 * j,
-                  cand + (((int64_t)seq * G + gg) * splits) * kp + 2 * j, 16);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-  }
-  if (warp < G) {
-    // a tournament: lane l holds the heads of lists l, l + 32, ... (each sorted best-first)
-    const int g = warp;
-    const uint64_t* gl = cand + (((int64_t)seq * G + g) * splits) * kp;
-    const uint64_t* sl = stage + (int64_t)g * splits * kp;
-    auto entry = [&](int sp, int r) -> uint64_t {
-      return staged ? sl[sp * kp + r] : __ldcg(gl + (int64_t)sp * kp + r);
-    };
-    int pos[kMergeListsPerLane];
-    uint64_t head[kMergeListsPerLane];
-#pragma unroll
-    for (int i = 0; i < kMergeListsPerLane; ++i) {
-      const int sp = lane + 32 * i;
-      pos[i] = 0;
-      head[i] = (sp < splits && km1 > 0) ? entry(sp, 0) : 0ull;
-    }
-    int32_t* outb = block_idx + ((int64_t)seq * G + g) * k;
-    if (lane == 0) outb[0] = ok ? (int32_t)local : -1;
-    for (int r = 0; r < km1; ++r) {
-      uint64_t m2[kMergeListsPerLane / 2];  // the lane's best head, as a tree
-#pragma unroll
-      for (int i = 0; i < kMergeListsPerLane / 2; ++i)
-        m2[i] = head[2 * i] > head[2 * i + 1] ? head[2 * i] : head[2 * i + 1];
-#pragma unroll
-      for (int w = kMergeListsPerLane / 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) m2[i] = m2[i] > m2[i + w] ? m2[i] : m2[i + w];
-      const uint64_t best = warp_max_key(m2[0]);
-      if (lane == 0) outb[1 + r] = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
-      if (best == 0) continue;
-      // the list holding best (keys are unique: block ids differ across lists) moves to its next entry;
-      // branch-free, so the warp never splits over the lane that owns it
-#pragma unroll
-      for (int i = 0; i < kMergeListsPerLane; ++i) {
-        const bool hit = head[i] == best;
-        pos[i] += hit ? 1 : 0;
-        uint64_t nv = 0ull;
-        if (hit && pos[i] < km1) nv = entry(lane + 32 * i, pos[i]);
-        head[i] = hit ? nv : head[i];
-      }
-    }
-  }
-  if (tid == 0) tickets[seq] = 0u;  // ready for the next call
 }
 
-// One CTA (4 warps) per (slot, group, sequence).  The group's heads are the
-// rows of m16n8k16 tensor-core tiles (rows >= gs are zero) and warp w takes
-// keys [w BK/4, (w+1) BK/4):
+// One CTA (4 warps) per (slot, group, sequence).  Its block: slot 0 is the
+// local block; slot r + 1 is the r-th best candidate over the scan CTAs'
+// lists of the group, found by r rounds of a tournament (lane l holds the heads
+// of lists l, l + 32, ...; each round takes the warp's best head and advances
+// that list) over the lists staged in shared memory.  The CTA writes its slot
+// of block_idx.  The group's heads are the rows of m16n8k16 tensor-core tiles
+// (rows >= gs are zero) and warp w takes keys [w BK/4, (w+1) BK/4):
 //   - K rows go straight from HBM into B fragments (16-byte loads; the head
 //     dims are permuted the same way in the query's A fragments, as in the
 //     scan), so only V is staged in shared memory (16-byte chunk c of row j
@@ -317,16 +256,19 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
                                                           const uint16_t* __restrict__ k_cache,
                                                           const uint16_t* __restrict__ v_cache,
                                                           const int32_t* __restrict__ ctx_len,
-                                                          const int32_t* __restrict__ block_idx, int64_t ctx_max,
+                                                          const uint64_t* __restrict__ cand, int splits,
+                                                          int32_t* __restrict__ block_idx, int64_t ctx_max,
                                                           CacheMap map, int H_q, int G, int k, float scale,
                                                           float* __restrict__ part_o, float* __restrict__ part_lse,
                                                           unsigned int* __restrict__ tickets,
                                                           uint16_t* __restrict__ out, float* __restrict__ lse,
                                                           DeviceStatus* st) {
-  extern __shared__ __align__(16) uint16_t v_s[];  // V rows [BK][D]; later the warps' partial O
+  // the group's candidate lists first; then V rows [BK][D]; later the warps' partial O
+  extern __shared__ __align__(16) uint16_t v_s[];
   __shared__ float red_m[4][8], red_l[4][8];
   __shared__ float w_s[8][32];  // combine weights [head][slot]
   __shared__ int s_last;
+  __shared__ int32_t s_blk;
   __shared__ int64_t krow_s[PAGED ? BK : 1];  // cache row of each key of the block (paged caches)
   constexpr int C8 = D / 8;     // 16-byte chunks per row
   constexpr int KPW = BK / 4;   // keys per warp
@@ -347,10 +289,58 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
 #pragma unroll
     for (int p = 0; p < NP; ++p) qv[p] = gq < gs ? ldg_stream_16(qrow + 32 * p) : make_uint4(0u, 0u, 0u, 0u);
   }
-  griddep_wait();  // block_idx comes from the scan grid
-  const int32_t b = block_idx[((int64_t)seq * G + g) * k + slot];
+  const bool ok = len >= 1 && len <= ctx_max;
+  griddep_wait();  // the candidate lists come from the scan grid
+  if (slot == 0) {
+    if (tid == 0) s_blk = ok ? (int32_t)((len - 1) / BK) : -1;
+  } else {
+    const int kp = (k - 1) + ((k - 1) & 1);  // list stride (an even count of keys)
+    const uint64_t* gl = cand + (((int64_t)seq * G + g) * splits) * kp;
+    uint64_t* sl = reinterpret_cast<uint64_t*>(v_s);
+    const int n16 = splits * kp / 2;  // 16-byte pieces
+    for (int i = tid; i < n16; i += blockDim.x) cp_async_16(sl + 2 * i, gl + 2 * i, 16);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    if (warp == 0) {
+      int pos[kMergeListsPerLane];
+      uint64_t head[kMergeListsPerLane];
+#pragma unroll
+      for (int i = 0; i < kMergeListsPerLane; ++i) {
+        const int sp = lane + 32 * i;
+        pos[i] = 0;
+        head[i] = sp < splits ? sl[sp * kp] : 0ull;
+      }
+      uint64_t best = 0ull;
+      for (int r = 0; r < slot; ++r) {
+        uint64_t m2[kMergeListsPerLane / 2];  // the lane's best head, as a tree
+#pragma unroll
+        for (int i = 0; i < kMergeListsPerLane / 2; ++i)
+          m2[i] = head[2 * i] > head[2 * i + 1] ? head[2 * i] : head[2 * i + 1];
+#pragma unroll
+        for (int w = kMergeListsPerLane / 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) m2[i] = m2[i] > m2[i + w] ? m2[i] : m2[i + w];
+        best = warp_max_key(m2[0]);
+        if (best == 0ull) break;  // fewer candidates than slots
+        // the list holding best (keys are unique: block ids differ across lists) moves to its next entry;
+        // branch-free, so the warp never splits over the lane that owns it
+#pragma unroll
+        for (int i = 0; i < kMergeListsPerLane; ++i) {
+          const bool hit = head[i] == best;
+          pos[i] += hit ? 1 : 0;
+          const uint64_t nv = hit && pos[i] < k - 1 ? sl[(lane + 32 * i) * kp + pos[i]] : 0ull;
+          head[i] = hit ? nv : head[i];
+        }
+      }
+      if (lane == 0) s_blk = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
+    }
+  }
+  __syncthreads();  // s_blk, and the lists are no longer read: v_s takes the V rows
+  const int32_t b = s_blk;
+  if (tid == 0) block_idx[((int64_t)seq * G + g) * k + slot] = b;
   const int64_t nb = (ctx_max + BK - 1) / BK;
-  const bool valid = len >= 1 && len <= ctx_max && b >= 0 && (int64_t)b < nb;
+  const bool valid = ok && b >= 0 && (int64_t)b < nb;
   const int64_t t = len - 1;
   const int64_t key0 = (int64_t)b * BK;
   const int nvis = valid ? (int)max((int64_t)0, min((int64_t)BK, t - key0 + 1)) : 0;
@@ -533,17 +523,17 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
 
 
 struct DecodeScratch {
-  unsigned int* tickets;  // [B] scan + [B * G] attention; cleared before every call
+  unsigned int* tickets;  // [B * G] attention; cleared before every call
   uint64_t* cand;         // [B, G, splits, kp] per-CTA candidate keys (kp = k-1 rounded up to even)
   int32_t* blk;
   float* part_o;
   float* part_lse;
 };
 
-static size_t ticket_bytes(const DecodePlan& p) { return align_up((size_t)p.B * (1 + p.H_kv) * 4, 256); }
+static size_t ticket_bytes(const DecodePlan& p) { return align_up((size_t)p.B * p.H_kv * 4, 256); }
 static int list_stride(const DecodePlan& p) { return p.k > 1 ? (p.k - 1) + ((p.k - 1) & 1) : 2; }
-constexpr size_t kStageMaxBytes = 96 * 1024;  // the last CTA stages the lists in shared memory up to this size
-static size_t stage_bytes(const DecodePlan& p) { return (size_t)p.H_kv * p.splits * list_stride(p) * 8; }
+// one group's lists, staged in shared memory by each attention CTA (at most 256 splits x 32 keys = 64 KB)
+static size_t group_lists_bytes(const DecodePlan& p) { return (size_t)p.splits * list_stride(p) * 8; }
 
 static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
   char* c = (char*)base;
@@ -565,49 +555,48 @@ static size_t carve(const DecodePlan& p, void* base, DecodeScratch* out) {
 
 template <int DI, int BK, bool PAGED, bool F8, int CAP>
 cudaError_t launch_scan_c(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
-                          const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
+                          const DecodePlan& p, const DecodeScratch& sc, DeviceStatus* st,
                           cudaStream_t s) {
-  const size_t bm = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
-  const bool staged = stage_bytes(p) <= kStageMaxBytes;
-  const size_t smem = staged && stage_bytes(p) > bm ? stage_bytes(p) : bm;
+  const size_t smem = (size_t)p.max_cta_blocks * kGroupsPerMma * 4;
   auto kern = decode_scan_kernel<DI, BK, PAGED, F8, CAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<dim3((unsigned)p.splits, (unsigned)p.B), kScanThreads, smem, s>>>(
-      (const uint8_t*)q_idx_t, (const uint8_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits, staged,
-      sc.cand, sc.tickets, blk, st);
+      (const uint8_t*)q_idx_t, (const uint8_t*)k_idx_cache, ctx_len, p.ctx_max, map, p.H_kv, p.k, p.splits, sc.cand,
+      st);
   return cudaGetLastError();
 }
 
 template <int DI, int BK, bool PAGED, bool F8>
 cudaError_t launch_scan_t(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
-                          const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st,
+                          const DecodePlan& p, const DecodeScratch& sc, DeviceStatus* st,
                           cudaStream_t s) {
-  return p.k - 1 <= 16 ? launch_scan_c<DI, BK, PAGED, F8, 16>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                       : launch_scan_c<DI, BK, PAGED, F8, 32>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+  return p.k - 1 <= 16 ? launch_scan_c<DI, BK, PAGED, F8, 16>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s)
+                       : launch_scan_c<DI, BK, PAGED, F8, 32>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s);
 }
 
 template <int DI, int BK>
 cudaError_t launch_scan(const void* q_idx_t, const void* k_idx_cache, const int32_t* ctx_len, const CacheMap& map,
-                        const DecodePlan& p, const DecodeScratch& sc, int32_t* blk, DeviceStatus* st, cudaStream_t s) {
+                        const DecodePlan& p, const DecodeScratch& sc, DeviceStatus* st, cudaStream_t s) {
   if constexpr (DI >= 64) {  // E4M3 rows of 64 or 128 bytes
     if (p.f8)
-      return map.table ? launch_scan_t<DI, BK, true, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                       : launch_scan_t<DI, BK, false, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+      return map.table ? launch_scan_t<DI, BK, true, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s)
+                       : launch_scan_t<DI, BK, false, true>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s);
   } else {
     if (p.f8) return cudaErrorInvalidValue;
   }
-  return map.table ? launch_scan_t<DI, BK, true, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                   : launch_scan_t<DI, BK, false, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+  return map.table ? launch_scan_t<DI, BK, true, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s)
+                   : launch_scan_t<DI, BK, false, false>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s);
 }
 
 // The attention grid as a programmatic dependent of the scan: its CTAs may be
 // scheduled while the scan drains and wait (griddepcontrol.wait) for its results.
 template <int D, int BK, bool PAGED>
 cudaError_t launch_attn_dep_t(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
-                              const int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
+                              int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
                               const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
-  const int smem = BK * D * 2;  // V rows of one block
+  const size_t vb = (size_t)BK * D * 2, lb = group_lists_bytes(p);
+  const int smem = (int)(vb > lb ? vb : lb);  // V rows of one block, or first the group's candidate lists
   auto kern = decode_attn_kernel<D, BK, PAGED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -622,13 +611,13 @@ cudaError_t launch_attn_dep_t(const void* q_t, const void* k_cache, const void* 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, (const uint16_t*)q_t, (const uint16_t*)k_cache, (const uint16_t*)v_cache,
-                            ctx_len, (const int32_t*)blk, p.ctx_max, map, p.H_q, p.H_kv, p.k, scale, sc.part_o,
-                            sc.part_lse, sc.tickets + p.B, (uint16_t*)out, lse, st);
+                            ctx_len, (const uint64_t*)sc.cand, p.splits, blk, p.ctx_max, map, p.H_q, p.H_kv, p.k,
+                            scale, sc.part_o, sc.part_lse, sc.tickets, (uint16_t*)out, lse, st);
 }
 
 template <int D, int BK>
 cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
-                            const int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
+                            int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
                             const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
   return map.table ? launch_attn_dep_t<D, BK, true>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse,
                                                      st, s)
@@ -677,14 +666,14 @@ cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_id
   int32_t* blk = block_idx ? block_idx : sc.blk;
   cudaError_t e;
   if (p.d_I == 32) {
-    e = p.Bk == 64 ? launch_scan<32, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                   : launch_scan<32, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<32, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s)
+                   : launch_scan<32, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s);
   } else if (p.d_I == 64) {
-    e = p.Bk == 64 ? launch_scan<64, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                   : launch_scan<64, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<64, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s)
+                   : launch_scan<64, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s);
   } else {
-    e = p.Bk == 64 ? launch_scan<128, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s)
-                   : launch_scan<128, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, blk, st, s);
+    e = p.Bk == 64 ? launch_scan<128, 64>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s)
+                   : launch_scan<128, 128>(q_idx_t, k_idx_cache, ctx_len, map, p, sc, st, s);
   }
   if (e != cudaSuccess) return e;
   if (p.d == 64)

@@ -155,7 +155,7 @@ struct DecodePlan {
 DecodePlan decode_plan(int B, int64_t ctx_max, int H_q, int H_kv, int d, int d_I, int Bk, int k);
 size_t decode_scratch_bytes(const DecodePlan& p);
 // Bytes at the start of the decode scratch that must be zero when a call starts
-// (the completion tickets of the scan and attention CTAs).
+// (the completion tickets of the attention CTAs).
 size_t decode_clear_bytes(const DecodePlan& p);
 cudaError_t launch_decode(const void* q_t, const void* q_idx_t, const void* k_idx_cache, const void* k_cache,
                           const void* v_cache, const int32_t* ctx_len, const DecodePlan& p, float scale, void* out,
