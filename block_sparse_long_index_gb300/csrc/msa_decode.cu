@@ -229,15 +229,53 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
       if (lane == 0) out[r] = best;  // 0 = no candidate
     }
   }
+}
 
+// The r-th best key (r >= 1) over `splits` lists of km1 keys (stride kp),
+// each sorted best first, staged in shared memory; one warp, lane l holding
+// lists l, l + 32, ... (LPL of them).  Each round takes the warp's best head
+// and advances that list.  The list's next key sits in a register, loaded one
+// round ahead, so a round waits on no shared-memory load; the advance is
+// branch-free, so the warp never splits over the lane that owns the winner.
+template <int LPL>
+__device__ __forceinline__ uint64_t merged_key(const uint64_t* sl, int splits, int kp, int km1, int r, int lane) {
+  uint64_t head[LPL], nxt[LPL];
+  int pos[LPL];
+#pragma unroll
+  for (int i = 0; i < LPL; ++i) {
+    const int sp = lane + 32 * i;
+    const bool in = sp < splits;
+    pos[i] = 0;
+    head[i] = in && km1 > 0 ? sl[sp * kp] : 0ull;
+    nxt[i] = in && km1 > 1 ? sl[sp * kp + 1] : 0ull;
+  }
+  uint64_t best = 0ull;
+  for (int j = 0; j < r; ++j) {
+    uint64_t m[LPL];  // the lane's best head, as a tree
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) m[i] = head[i];
+#pragma unroll
+    for (int w = LPL / 2; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) m[i] = m[i] > m[i + w] ? m[i] : m[i + w];
+    best = warp_max_key(m[0]);
+    if (best == 0ull) break;  // fewer candidates than r (uniform: the reduction's result)
+#pragma unroll
+    for (int i = 0; i < LPL; ++i) {
+      const bool hit = head[i] == best;  // keys are unique: block ids differ across lists
+      pos[i] += hit ? 1 : 0;
+      const uint64_t nn = hit && pos[i] + 1 < km1 ? sl[(lane + 32 * i) * kp + pos[i] + 1] : 0ull;
+      head[i] = hit ? nxt[i] : head[i];
+      nxt[i] = hit ? nn : nxt[i];
+    }
+  }
+  return best;
 }
 
 // One CTA (4 warps) per (slot, group, sequence).  Its block: slot 0 is the
 // local block; slot r + 1 is the r-th best candidate over the scan CTAs'
-// lists of the group, found by r rounds of a tournament (lane l holds the heads
-// of lists l, l + 32, ...; each round takes the warp's best head and advances
-// that list) over the lists staged in shared memory.  The CTA writes its slot
-// of block_idx.  The group's heads are the rows of m16n8k16 tensor-core tiles
+// lists of the group (merged_key over the lists staged in shared memory).  The
+// CTA writes its slot of block_idx.  The group's heads are the rows of m16n8k16 tensor-core tiles
 // (rows >= gs are zero) and warp w takes keys [w BK/4, (w+1) BK/4):
 //   - K rows go straight from HBM into B fragments (16-byte loads; the head
 //     dims are permuted the same way in the query's A fragments, as in the
@@ -251,7 +289,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
 // The last CTA of a (sequence, group) to finish merges the group's k partials
 // per head: M = max lse_s, w_s = e^(lse_s - M) / sum e^(lse_s - M),
 // out = sum w_s O_s, lse = M + ln sum e^(lse_s - M).
-template <int D, int BK, bool PAGED>
+template <int D, int BK, bool PAGED, int LPL>
 __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __restrict__ q_t,
                                                           const uint16_t* __restrict__ k_cache,
                                                           const uint16_t* __restrict__ v_cache,
@@ -303,36 +341,7 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
     cp_async_wait<0>();
     __syncthreads();
     if (warp == 0) {
-      int pos[kMergeListsPerLane];
-      uint64_t head[kMergeListsPerLane];
-#pragma unroll
-      for (int i = 0; i < kMergeListsPerLane; ++i) {
-        const int sp = lane + 32 * i;
-        pos[i] = 0;
-        head[i] = sp < splits ? sl[sp * kp] : 0ull;
-      }
-      uint64_t best = 0ull;
-      for (int r = 0; r < slot; ++r) {
-        uint64_t m2[kMergeListsPerLane / 2];  // the lane's best head, as a tree
-#pragma unroll
-        for (int i = 0; i < kMergeListsPerLane / 2; ++i)
-          m2[i] = head[2 * i] > head[2 * i + 1] ? head[2 * i] : head[2 * i + 1];
-#pragma unroll
-        for (int w = kMergeListsPerLane / 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) m2[i] = m2[i] > m2[i + w] ? m2[i] : m2[i + w];
-        best = warp_max_key(m2[0]);
-        if (best == 0ull) break;  // fewer candidates than slots
-        // the list holding best (keys are unique: block ids differ across lists) moves to its next entry;
-        // branch-free, so the warp never splits over the lane that owns it
-#pragma unroll
-        for (int i = 0; i < kMergeListsPerLane; ++i) {
-          const bool hit = head[i] == best;
-          pos[i] += hit ? 1 : 0;
-          const uint64_t nv = hit && pos[i] < k - 1 ? sl[(lane + 32 * i) * kp + pos[i]] : 0ull;
-          head[i] = hit ? nv : head[i];
-        }
-      }
+      const uint64_t best = merged_key<LPL>(sl, splits, kp, k - 1, slot, lane);
       if (lane == 0) s_blk = best ? (int32_t)(0xFFFFFFFFu - (uint32_t)best) : -1;
     }
   }
@@ -591,13 +600,13 @@ cudaError_t launch_scan(const void* q_idx_t, const void* k_idx_cache, const int3
 
 // The attention grid as a programmatic dependent of the scan: its CTAs may be
 // scheduled while the scan drains and wait (griddepcontrol.wait) for its results.
-template <int D, int BK, bool PAGED>
+template <int D, int BK, bool PAGED, int LPL>
 cudaError_t launch_attn_dep_t(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
                               int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
                               const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
   const size_t vb = (size_t)BK * D * 2, lb = group_lists_bytes(p);
   const int smem = (int)(vb > lb ? vb : lb);  // V rows of one block, or first the group's candidate lists
-  auto kern = decode_attn_kernel<D, BK, PAGED>;
+  auto kern = decode_attn_kernel<D, BK, PAGED, LPL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -615,13 +624,25 @@ cudaError_t launch_attn_dep_t(const void* q_t, const void* k_cache, const void* 
                             scale, sc.part_o, sc.part_lse, sc.tickets, (uint16_t*)out, lse, st);
 }
 
+template <int D, int BK, bool PAGED>
+cudaError_t launch_attn_dep_p(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
+                              int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
+                              const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
+  // lists per lane of the merge: splits <= 64, 128, 256
+  if (p.splits <= 64)
+    return launch_attn_dep_t<D, BK, PAGED, 2>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s);
+  if (p.splits <= 128)
+    return launch_attn_dep_t<D, BK, PAGED, 4>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s);
+  return launch_attn_dep_t<D, BK, PAGED, 8>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse, st, s);
+}
+
 template <int D, int BK>
 cudaError_t launch_attn_dep(const void* q_t, const void* k_cache, const void* v_cache, const int32_t* ctx_len,
                             int32_t* blk, const CacheMap& map, const DecodePlan& p, float scale,
                             const DecodeScratch& sc, void* out, float* lse, DeviceStatus* st, cudaStream_t s) {
-  return map.table ? launch_attn_dep_t<D, BK, true>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse,
+  return map.table ? launch_attn_dep_p<D, BK, true>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out, lse,
                                                      st, s)
-                   : launch_attn_dep_t<D, BK, false>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out,
+                   : launch_attn_dep_p<D, BK, false>(q_t, k_cache, v_cache, ctx_len, blk, map, p, scale, sc, out,
                                                       lse, st, s);
 }
 

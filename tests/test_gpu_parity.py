@@ -276,6 +276,8 @@ DECODE_CASES = [
     ("dec_small", 3, 5000, 8, 4, 128, 64, 64, 5, 2, [5000, 4097, 70]),
     ("dec_bk128", 2, 20000, 16, 8, 128, 128, 128, 16, 4, [20000, 13000]),
     ("dec_tiny_ctx", 2, 300, 4, 1, 64, 32, 64, 4, 1, [1, 300]),
+    # k - 1 = 19 candidates: the scan CTAs keep 32-entry lists
+    ("dec_k20", 2, 9000, 8, 2, 64, 64, 64, 20, 2, [9000, 6100]),
 ]
 
 
