@@ -58,10 +58,11 @@ __device__ __forceinline__ uint32_t ordered_bits(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Completion ticket of the last-CTA pattern: every thread's writes are made
-// visible (__threadfence) and gathered by __syncthreads before thread 0 takes a
-// ticket with acquire-release semantics; the CTA that takes the last ticket
-// then reads the others' results after a __syncthreads (L2 loads only).
+// Completion ticket of the last-CTA pattern: __syncthreads gathers every
+// thread's writes before thread 0 takes a ticket with acquire-release semantics
+// at GPU scope (the release covers what the barrier ordered before it); the CTA
+// that takes the last ticket reads the others' results after a __syncthreads
+// (L2 loads only), which orders its reads after that acquire.
 __device__ __forceinline__ unsigned int ticket_acq_rel(unsigned int* t) {
   unsigned int old;
   asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(t) : "memory");
@@ -472,28 +473,25 @@ __global__ void __launch_bounds__(128) decode_attn_kernel(const uint16_t* __rest
   }  // nvis > 0
 
   // the last of the group's k CTAs merges the partials
-  __threadfence();
   __syncthreads();
   if (tid == 0) s_last = ticket_acq_rel(&tickets[(int64_t)seq * G + g]) == (unsigned)(k - 1);
   __syncthreads();
   if (!s_last) return;
   const float* gl = part_lse + ((int64_t)seq * H_q + g * gs) * k;  // [gs][k]
-  for (int i = tid; i < gs * k; i += blockDim.x) w_s[i / k][i % k] = __ldcg(gl + i);
-  __syncthreads();
-  if (tid < gs) {
-    float M = __int_as_float(0xff800000);
-    for (int s = 0; s < k; ++s) M = fmaxf(M, w_s[tid][s]);
-    float L = 0.f;
-    for (int s = 0; s < k; ++s) {
-      const float w = M == __int_as_float(0xff800000) || w_s[tid][s] == __int_as_float(0xff800000)
-                          ? 0.f
-                          : __expf(w_s[tid][s] - M);
-      w_s[tid][s] = w;
-      L += w;
-    }
+  // one warp per head, lane = slot (k <= 32): M, the weights and L by warp reductions
+  for (int hh = warp; hh < gs; hh += blockDim.x / 32) {
+    const float v = lane < k ? __ldcg(gl + hh * k + lane) : __int_as_float(0xff800000);
+    float M = v;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = M == __int_as_float(0xff800000) || v == __int_as_float(0xff800000) ? 0.f : __expf(v - M);
+    float L = w;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    for (int s = 0; s < k; ++s) w_s[tid][s] *= inv;
-    if (lse) lse[(int64_t)seq * H_q + g * gs + tid] = L > 0.f ? M + logf(L) : __int_as_float(0xff800000);
+    w_s[hh][lane] = w * inv;
+    if (lane == 0 && lse)
+      lse[(int64_t)seq * H_q + g * gs + hh] = L > 0.f ? M + logf(L) : __int_as_float(0xff800000);
   }
   __syncthreads();
   // thread -> (head, 4 columns); the partial loads of 16 slots are all in flight before the sums
