@@ -356,7 +356,9 @@ def bench_prefill(args, dist, torch, peaks):
         houts = [{"out": torch.empty(run.out.shape, dtype=run.out.dtype, pin_memory=True),
                   "lse": torch.empty(run.lse.shape, dtype=run.lse.dtype, pin_memory=True)} for _ in range(2)]
         pipe = PrefillHostPipeline(run)
-        Ke = max(3, K)
+        # at least 30 pipelined steps (about a second): on some hosts the copies of a run's first ~0.2 s go slower,
+        # and a ten-step run would report that start rather than the pipeline's throughput
+        Ke = max(30, K)
         pipe([host] * 2, houts)  # warm-up
         torch.cuda.synchronize()
         dist.barrier()
@@ -792,7 +794,7 @@ def main():
         e = pre["e2e"]
         e_ms = dist.max(e["ms"])
         line["e2e"] = {"value": ws * cfg.N / (e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": e["h2d"],
-                       "d2h_bytes_per_step": e["d2h"], "steps": e["steps"],
+                       "d2h_bytes_per_step": e["d2h"], "steps": e["steps"], "ms_per_step": e_ms,
                        "how": "PrefillHostPipeline: per step pinned host -> device copies of q, k, v, q_idx, k_idx, "
                               "select + attention, device -> pinned host copies of out and lse; copies of one "
                               "step overlap the compute of its neighbours"}
