@@ -88,6 +88,7 @@ __device__ __forceinline__ void issue_record(TileRecord* slot, const TileRecord*
 
 // A block id repeated in a row's set counts once: its later slots are marked
 // t = -1 in the tile records, so the backward kernels skip them.
+// With k a multiple of 4 a row's earlier slots are read as 16-byte pieces, all in flight before the compares.
 __global__ void mark_repeats_kernel(TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb,
                                     const int32_t* __restrict__ block_idx, int64_t N, int k) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -97,11 +98,21 @@ __global__ void mark_repeats_kernel(TileRecord* __restrict__ rec, const int32_t*
   TileRecord& r = rec[tile];
   if (p >= r.count) return;
   const int32_t* sel = block_idx + ((int64_t)r.g * N + r.t[p]) * k;
-  for (int s2 = 0; s2 < r.slot[p]; ++s2)
-    if (sel[s2] == r.b) {
-      r.t[p] = -1;
-      return;
-    }
+  const int slot = r.slot[p];
+  const int32_t b = r.b;
+  bool rep = false;
+  if ((k & 3) == 0) {
+    int4 v[8];  // k <= 32
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 4 * j < slot ? __ldg(reinterpret_cast<const int4*>(sel) + j) : make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      rep |= (4 * j < slot && v[j].x == b) || (4 * j + 1 < slot && v[j].y == b) || (4 * j + 2 < slot && v[j].z == b) ||
+             (4 * j + 3 < slot && v[j].w == b);
+  } else {
+    for (int s2 = 0; s2 < slot && !rep; ++s2) rep = sel[s2] == b;
+  }
+  if (rep) r.t[p] = -1;
 }
 
 __device__ __forceinline__ void copy_record(TileRecord* dst, const TileRecord* src) {
@@ -110,25 +121,40 @@ __device__ __forceinline__ void copy_record(TileRecord* dst, const TileRecord* s
 }
 
 // ------------------------------------------------------------------ D = dO . O
-__global__ void bwd_rowdot_kernel(const uint16_t* __restrict__ dout, const uint16_t* __restrict__ out, int64_t N,
-                                  int H_q, int D, float* __restrict__ Dr) {
-  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // t * H_q + h
-  const int lane = threadIdx.x & 31;
-  if (row >= N * H_q) return;
-  const uint16_t* a = dout + row * D;
-  const uint16_t* b = out + row * D;
-  float s = 0.f;
-  for (int c = 2 * lane; c < D; c += 64) {
-    const uint32_t x = *reinterpret_cast<const uint32_t*>(a + c), y = *reinterpret_cast<const uint32_t*>(b + c);
-    s = fmaf(bf16_lo(x), bf16_lo(y), s);
-    s = fmaf(bf16_hi(x), bf16_hi(y), s);
+// A row (t, h) is D/8 16-byte pieces, one per lane of a group of D/8 lanes;
+// a warp takes 32 / (D/8) rows a step and kRowdotSteps steps, with every
+// step's loads in flight before the sums.
+constexpr int kRowdotSteps = 4;
+template <int D>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restrict__ dout,
+                                                         const uint16_t* __restrict__ out, int64_t N, int H_q,
+                                                         float* __restrict__ Dr) {
+  constexpr int U = D / 8, RPS = 32 / U;  // lanes per row, rows per step
+  const int lane = threadIdx.x & 31, u = lane % U;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t rows = N * H_q;
+  const int64_t r0 = warp * (RPS * kRowdotSteps) + lane / U;  // t * H_q + h
+  uint4 a[kRowdotSteps], b[kRowdotSteps];
+#pragma unroll
+  for (int j = 0; j < kRowdotSteps; ++j) {
+    const int64_t row = r0 + (int64_t)j * RPS;
+    const bool in = row < rows;
+    a[j] = in ? ldg_stream_16(dout + row * D + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
+    b[j] = in ? ldg_stream_16(out + row * D + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) {
-    const int64_t t = row / H_q;
-    const int h = (int)(row % H_q);
-    Dr[(int64_t)h * N + t] = s;
+  for (int j = 0; j < kRowdotSteps; ++j) {
+    const uint32_t x[4] = {a[j].x, a[j].y, a[j].z, a[j].w}, y[4] = {b[j].x, b[j].y, b[j].z, b[j].w};
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s = fmaf(bf16_lo(x[e]), bf16_lo(y[e]), s);
+      s = fmaf(bf16_hi(x[e]), bf16_hi(y[e]), s);
+    }
+#pragma unroll
+    for (int o = U / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const int64_t row = r0 + (int64_t)j * RPS;
+    if (u == 0 && row < rows) Dr[(row % H_q) * N + row / H_q] = s;
   }
 }
 
@@ -236,29 +262,32 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
 }
 
 // lse^I[g, t] from the (max, sum) of the row's slots; a slot counts iff its id
-// is in [0, nb) and first of its kind in the row.
+// is in [0, nb) and first of its kind in the row.  A row is kp lanes (k
+// rounded up to a power of two, k <= 32), lane s holding slot s: the first of
+// a kind is the lowest lane of its match group, and the max and the sum are
+// shuffle reductions within the kp lanes, so a warp takes 32 / kp rows with
+// coalesced loads.
 __global__ void bwd_index_lse_combine_kernel(const float2* __restrict__ part, const int32_t* __restrict__ block_idx,
                                              int64_t N, int G, int k, int64_t nb, int64_t T0, int64_t S,
                                              float* __restrict__ lseI) {
-  const int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // g * S + (t - T0)
-  if (w >= (int64_t)G * S) return;
-  const int64_t i = (w / S) * N + T0 + w % S;  // g * N + t
-  const int32_t* sel = block_idx + i * k;
-  const float2* pp = part + i * k;
-  float M = __int_as_float(0xff800000);
-  for (int s = 0; s < k; ++s) {
-    bool ok = sel[s] >= 0 && (int64_t)sel[s] < nb;
-    for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != sel[s];
-    if (ok) M = fmaxf(M, pp[s].x);
-  }
-  float L = 0.f;
-  if (M != __int_as_float(0xff800000))
-    for (int s = 0; s < k; ++s) {
-      bool ok = sel[s] >= 0 && (int64_t)sel[s] < nb;
-      for (int s2 = 0; s2 < s && ok; ++s2) ok = sel[s2] != sel[s];
-      if (ok && pp[s].x != __int_as_float(0xff800000)) L += pp[s].y * __expf(pp[s].x - M);
-    }
-  lseI[i] = L > 0.f ? M + logf(L) : __int_as_float(0x7f800000);  // +inf: no index logit (no gradient)
+  int kp = 1;
+  while (kp < k) kp <<= 1;
+  const int lane = threadIdx.x & 31, sub = lane / kp, s = lane % kp;
+  const int64_t w = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * (32 / kp) + sub;  // g * S + (t - T0)
+  const bool row_in = w < (int64_t)G * S;
+  const int64_t i = row_in ? (w / S) * N + T0 + w % S : 0;  // g * N + t
+  const bool in = row_in && s < k;
+  const int32_t id = in ? __ldg(block_idx + i * k + s) : -1;
+  const float2 pm = in ? __ldg(part + i * k + s) : make_float2(__int_as_float(0xff800000), 0.f);
+  const unsigned long long key = ((unsigned long long)(unsigned)sub << 32) | (unsigned)id;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  const bool ok = in && id >= 0 && (int64_t)id < nb && __ffs(peers) - 1 == lane;
+  float M = ok ? pm.x : __int_as_float(0xff800000);
+  for (int o = kp / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = ok && M != __int_as_float(0xff800000) && pm.x != __int_as_float(0xff800000) ? pm.y * __expf(pm.x - M)
+                                                                                        : 0.f;
+  for (int o = kp / 2; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  if (row_in && s == 0) lseI[i] = L > 0.f ? M + logf(L) : __int_as_float(0x7f800000);  // +inf: no index logit
 }
 
 // ------------------------------------------------------------------ main branch
@@ -1435,8 +1464,13 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
     bwd_index_lse_kernel<BK, DI><<<grid, kThreadsB, 0, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec,
                                                             sc.tile_off, n_gb, N, G, k, sI, sc.partI);
   }
-  bwd_index_lse_combine_kernel<<<(unsigned)ceil_div((int64_t)G * (T1 - T0), 256), 256, 0, s>>>(
-      sc.partI, block_idx, N, G, k, sc.nb, T0, T1 - T0, sc.lseI);
+  {
+    int kp = 1;
+    while (kp < k) kp <<= 1;
+    const int64_t rows_per_cta = 8 * (32 / kp);  // 8 warps
+    bwd_index_lse_combine_kernel<<<(unsigned)ceil_div((int64_t)G * (T1 - T0), rows_per_cta), 256, 0, s>>>(
+        sc.partI, block_idx, N, G, k, sc.nb, T0, T1 - T0, sc.lseI);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if constexpr (D == 128 && BK == 128) {
@@ -1512,8 +1546,14 @@ cudaError_t launch_bwd(const void* q, const void* k, const void* v, const void* 
   if (kl && (e = cudaMemsetAsync(kl, 0, (size_t)G * N * 4, s)) != cudaSuccess) return e;
   if ((e = launch_invert(block_idx, N, G, Bk, kb, sc.row_ptr, sc.entries, sc.n_entries, sc.inv, st, s)) != cudaSuccess)
     return e;
-  bwd_rowdot_kernel<<<(unsigned)ceil_div(N * H_q * 32, 256), 256, 0, s>>>((const uint16_t*)dout,
-                                                                        (const uint16_t*)out, N, H_q, d, sc.Dr);
+  {
+    const int64_t rows_per_cta = 8 * (32 / (d / 8)) * kRowdotSteps;  // 8 warps
+    const unsigned grid = (unsigned)ceil_div(N * H_q, rows_per_cta);
+    if (d == 64)
+      bwd_rowdot_kernel<64><<<grid, 256, 0, s>>>((const uint16_t*)dout, (const uint16_t*)out, N, H_q, sc.Dr);
+    else
+      bwd_rowdot_kernel<128><<<grid, 256, 0, s>>>((const uint16_t*)dout, (const uint16_t*)out, N, H_q, sc.Dr);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // Query slabs [T0, T1) bound the teacher buffer; the gradients accumulate across slabs, and a slab's
   // positions have all their blocks in its tile list.
