@@ -1103,6 +1103,36 @@ constexpr int kLseBar = 2 * tcb::kTile, kLseBytes = 1024 + kLseBar + 64;
 constexpr int kGradBar = 3 * tcb::kTile, kGradBytes = 1024 + kGradBar + 64;
 constexpr uint32_t kIdescSS = tcb::kIdescSS, kIdescMnB = tcb::kIdescMnB, kIdescMnAB = tcb::kIdescMnAB;
 
+// Packed pairs of fp32 (one 64-bit register): two lanes per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Records [ti0, ti0 + kRecs) that lie below hi into dst: 16-byte cp.async pieces, threads 0 .. 8 kRecs - 1.
 __device__ __forceinline__ void fetch_records(TileRecord* dst, const TileRecord* rec, int64_t ti0, int64_t hi) {
   const int i = threadIdx.x >> 3;
@@ -1227,16 +1257,44 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
       for (int c32 = 0; c32 < 4; ++c32) sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x[c32]);
       sm100::tmem_ld_wait();
       float m = -INFINITY;  // base-2 units
-#pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float y = (c <= lim) ? __uint_as_float(x[c >> 5][c & 31]) * s2 : -INFINITY;
-        x[c >> 5][c & 31] = __float_as_uint(y);
-        m = fmaxf(m, y);
-      }
       float l = 0.f;
-      if (m > -INFINITY) {
+      if (lim >= 127) {
+        // every key visible (rows below the diagonal block): the maximum of the raw logits times s2 > 0 (the
+        // rounding is monotonic, so it is the maximum of the scaled ones), then 2^(z s2 - m) by packed FMAs
+        float mr[4];
 #pragma unroll
-        for (int c = 0; c < 128; ++c) l += sm100::ex2_approx(__uint_as_float(x[c >> 5][c & 31]) - m);
+        for (int c32 = 0; c32 < 4; ++c32) {
+          mr[c32] = __uint_as_float(x[c32][0]);
+#pragma unroll
+          for (int e = 1; e < 31; e += 2)
+            mr[c32] = sm100::max3(mr[c32], __uint_as_float(x[c32][e]), __uint_as_float(x[c32][e + 1]));
+          mr[c32] = fmaxf(mr[c32], __uint_as_float(x[c32][31]));
+        }
+        m = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * s2;
+        const uint64_t s2x2 = f2_pack(s2, s2), nm2 = f2_pack(-m, -m);
+        uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          float a, b;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(x[c >> 5][c & 31]), __uint_as_float(x[c >> 5][(c & 31) + 1])),
+                           s2x2, nm2),
+                    a, b);
+          acc = f2_add(acc, f2_pack(sm100::ex2_approx(a), sm100::ex2_approx(b)));
+        }
+        float l0, l1;
+        f2_unpack(acc, l0, l1);
+        l = l0 + l1;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float y = (c <= lim) ? __uint_as_float(x[c >> 5][c & 31]) * s2 : -INFINITY;
+          x[c >> 5][c & 31] = __float_as_uint(y);
+          m = fmaxf(m, y);
+        }
+        if (m > -INFINITY) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) l += sm100::ex2_approx(__uint_as_float(x[c >> 5][c & 31]) - m);
+        }
       }
       if (t >= 0) part[((int64_t)ch.g * N + t) * k + slot_k] = make_float2(m > -INFINITY ? m * kLn2 : -INFINITY, l);
       sm100::tc_fence_before();
@@ -1327,6 +1385,9 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
       const int64_t lim = (int64_t)t - (int64_t)ch.b * 128;  // keys c <= lim are visible (none when t < 0)
       const float l2 = lse_r * kLog2e;
       float klsum = 0.f;
+      const bool full = lim >= 127;  // rows below the diagonal block: every key visible
+      const uint64_t s2x2 = f2_pack(s2, s2), nl2x2 = f2_pack(-l2, -l2), w2 = f2_pack(w, w), neg1 = f2_pack(-1.f, -1.f);
+      uint64_t kl2 = f2_pack(0.f, 0.f);
       uint32_t x[2][32];
       sm100::tmem_ld_x32(tmem + lane_base, x[0]);
 #pragma unroll
@@ -1335,28 +1396,57 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
         sm100::reg_fence32(x[c32 & 1]);
         if (c32 < 3) sm100::tmem_ld_x32(tmem + lane_base + (c32 + 1) * 32, x[(c32 + 1) & 1]);
         uint32_t zk[16];
+        if (full) {
+          // every key visible: a pair of keys per packed instruction; the KL term of a key is
+          // ln 2 * p (log2 p - log2 pI), with p = 0 contributing 0 (p times a finite log)
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float dz[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = c32 * 32 + e + u;
-            const bool ok = c <= lim;
-            const float y = fmaf(__uint_as_float(x[c32 & 1][e + u]), s2, -l2);  // log2 pI
-            const uint4& q8 = pb[c32 * 4 + ((e + u) >> 3)];
-            const int cc = (e + u) & 7;
-            const uint32_t wd = (cc >> 1) == 0 ? q8.x : (cc >> 1) == 1 ? q8.y : (cc >> 1) == 2 ? q8.z : q8.w;
-            const float p = __uint_as_float((cc & 1) ? (wd & 0xffff0000u) : (wd << 16));
-            dz[u] = ok ? w * (sm100::ex2_approx(y) - p) : 0.f;
-            if (ok && p > 0.f) klsum += p * (__logf(p) - y * 0.6931471805599453f);
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t y2 = f2_fma(f2_pack(__uint_as_float(x[c32 & 1][e]), __uint_as_float(x[c32 & 1][e + 1])),
+                                       s2x2, nl2x2);  // log2 pI
+            float y0, y1;
+            f2_unpack(y2, y0, y1);
+            const uint4& q8 = pb[c32 * 4 + (e >> 3)];
+            const int cw = (e & 7) >> 1;
+            const uint32_t wd = cw == 0 ? q8.x : cw == 1 ? q8.y : cw == 2 ? q8.z : q8.w;
+            const float p0 = __uint_as_float(wd << 16), p1 = __uint_as_float(wd & 0xffff0000u);
+            const uint64_t p2 = f2_pack(p0, p1);
+            const uint64_t dz2 =
+                f2_mul(w2, f2_add(f2_pack(sm100::ex2_approx(y0), sm100::ex2_approx(y1)), f2_mul(p2, neg1)));
+            const uint64_t lp2 = f2_pack(lg2_approx(fmaxf(p0, 1e-30f)), lg2_approx(fmaxf(p1, 1e-30f)));
+            kl2 = f2_fma(p2, f2_add(lp2, f2_mul(y2, neg1)), kl2);
+            float d0, d1;
+            f2_unpack(dz2, d0, d1);
+            zk[e >> 1] = pack_bf16x2(d0, d1);
           }
-          zk[e >> 1] = pack_bf16x2(dz[0], dz[1]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float dz[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int c = c32 * 32 + e + u;
+              const bool ok = c <= lim;
+              const float y = fmaf(__uint_as_float(x[c32 & 1][e + u]), s2, -l2);  // log2 pI
+              const uint4& q8 = pb[c32 * 4 + ((e + u) >> 3)];
+              const int cc = (e + u) & 7;
+              const uint32_t wd = (cc >> 1) == 0 ? q8.x : (cc >> 1) == 1 ? q8.y : (cc >> 1) == 2 ? q8.z : q8.w;
+              const float p = __uint_as_float((cc & 1) ? (wd & 0xffff0000u) : (wd << 16));
+              dz[u] = ok ? w * (sm100::ex2_approx(y) - p) : 0.f;
+              if (ok && p > 0.f) klsum += p * (__logf(p) - y * 0.6931471805599453f);
+            }
+            zk[e >> 1] = pack_bf16x2(dz[0], dz[1]);
+          }
         }
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           const uint32_t o = tcb::off(tid, c32 * 32 + q8 * 8);
           *reinterpret_cast<uint4*>(sm + kDZ + o) = make_uint4(zk[4 * q8], zk[4 * q8 + 1], zk[4 * q8 + 2], zk[4 * q8 + 3]);
         }
+      }
+      {
+        float k0, k1;
+        f2_unpack(kl2, k0, k1);
+        klsum += 0.6931471805599453f * (k0 + k1);  // the full path's sum, in natural-log units
       }
       if (kl && t >= 0) atomicAdd(kl + (int64_t)ch.g * N + t, klsum);
       sm100::fence_proxy_async_smem();
