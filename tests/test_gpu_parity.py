@@ -278,6 +278,8 @@ DECODE_CASES = [
     ("dec_tiny_ctx", 2, 300, 4, 1, 64, 32, 64, 4, 1, [1, 300]),
     # k - 1 = 19 candidates: the scan CTAs keep 32-entry lists
     ("dec_k20", 2, 9000, 8, 2, 64, 64, 64, 20, 2, [9000, 6100]),
+    # k = 1: the local block only (no candidate lists)
+    ("dec_k1", 2, 3000, 8, 2, 64, 64, 64, 1, 0, [3000, 1500]),
 ]
 
 
