@@ -123,6 +123,30 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t sr
                "r"(src), "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
 }
+// The CTAs split the tile list by weight, not by count: a (group, block) run
+// weighs its tiles plus kRunWeight more for its start (the K/V load and the
+// run's leading diagonal tiles, whose masked softmax is slower).  Timed per
+// CTA at 128K, an equal count of tiles left the CTAs that hold the short runs
+// of the late blocks 1.2-1.5 ms behind the median (the per-CTA end time fits
+// 4.7 us per run on top of the tiles).  Run r starts at weight
+// W(r) = tile_off[r] + w r; a CTA's first tile is the one at weight
+// W_total c / grid, found by a 32-ary search of one warp.
+__device__ __forceinline__ int64_t tile_at_weight(const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t w,
+                                                  int64_t rw, int lane) {
+  int64_t lo = 0, hi = n_gb + 1;  // W(lo) <= w; the run holding weight w lies in [lo, hi)
+  while (hi - lo > 1) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t i = lo + (int64_t)lane * step;
+    const unsigned m = __ballot_sync(0xffffffffu, i < hi && (int64_t)tile_off[i] + rw * i <= w);
+    const int64_t nlo = lo + (int64_t)(31 - __clz(m)) * step;  // bit 0 is set: W(lo) <= w
+    hi = min(hi, nlo + step);
+    lo = nlo;
+  }
+  if (lo >= n_gb) return tile_off[n_gb];
+  const int64_t t0 = tile_off[lo], tr = (int64_t)tile_off[lo + 1] - t0;
+  return t0 + max((int64_t)0, min(tr, w - (t0 + rw * lo) - rw));  // the start weight goes with the run's first tile
+}
+
 // K-major, 128B-swizzled operand whose 8-row atoms are `sbo` bytes apart.
 __device__ __forceinline__ uint64_t umma_desc_kmajor_sbo(uint32_t saddr, uint32_t sbo) {
   uint64_t d = 0;
@@ -210,6 +234,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   __shared__ int abort_flag;
   __shared__ TileRecord meta[kMeta * PPR];  // slot i: records [i PPR, (i + 1) PPR)
   __shared__ float ex_m[2][kRowsT], ex_l[2][kRowsT];  // softmax halves: row maxima and partial sums
+  __shared__ int64_t range_s[2];                       // this CTA's tiles [range_s[0], range_s[1])
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar0 = sbase + L::OFF_BAR;
@@ -254,6 +279,19 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     fence_mbar_init();
     abort_flag = 0;
   }
+  if (warp == kWarpLoad) {
+    // extra weight of a run start, in tiles (swept at 128K: 2 / 3 / 4 / 5 -> 16.82 / 16.53 / 16.57 / 16.62 ms
+    // per attention call); with ppr > 1 a tile's own time dominates and an equal count splits best
+    constexpr int64_t kRunWeight = PPR == 1 ? 3 : 0;
+    const int64_t n_gb = (int64_t)H_kv * nb;
+    const int64_t w_total = (int64_t)tile_off[n_gb] + kRunWeight * n_gb;
+    const int64_t a = tile_at_weight(tile_off, n_gb, w_total * blockIdx.x / gridDim.x, kRunWeight, lane);
+    const int64_t z = tile_at_weight(tile_off, n_gb, w_total * (blockIdx.x + 1) / gridDim.x, kRunWeight, lane);
+    if (lane == 0) {
+      range_s[0] = min(a, max_tiles);
+      range_s[1] = min(z, max_tiles);
+    }
+  }
   if (warp == kWarpLoad && lane == 0) {
     prefetch_tmap(&tmap_q);
     prefetch_tmap(&tmap_k);
@@ -269,10 +307,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   const uint32_t tmem = tmem_slot;
   volatile int* abort = &abort_flag;
 
-  const int64_t n_gb = (int64_t)H_kv * nb;
-  const int64_t total = min((int64_t)tile_off[n_gb], max_tiles);
-  const int64_t t_begin = total * blockIdx.x / gridDim.x;
-  const int n = (int)(total * (blockIdx.x + 1) / gridDim.x - t_begin);
+  const int64_t t_begin = range_s[0];
+  const int n = (int)(range_s[1] - range_s[0]);
 
   if (warp < kWarpSoft0) {
   regs_dec<kRegsProducers>();  // warps 0..3: the producers' warpgroup
