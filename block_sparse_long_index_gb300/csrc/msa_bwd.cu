@@ -58,11 +58,38 @@ constexpr int kPosT = kTilePositions;  // 16
 constexpr int kThreadsB = 256;
 
 // The contiguous range of the flat tile list this CTA walks.
-__device__ __forceinline__ void tile_range(const int32_t* tile_off, int64_t n_gb, int64_t& lo, int64_t& hi) {
-  const int64_t total = tile_off[n_gb];
-  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
-  lo = min(total, per * (int64_t)blockIdx.x);
-  hi = min(total, lo + per);
+// The CTAs split the tile list by weight, not by count: a (group, block) run
+// weighs its tiles plus `rw` more for what its start costs (the K/V or K^I
+// load, the dK/dV or dk^I flush at its end, its leading diagonal tiles, and in
+// the index passes a partial chunk of 8 tiles).  With an equal count, per-CTA
+// timers at 128K left the CTAs holding the late blocks' short runs 2 ms (main)
+// and 3 ms (index gradient) behind the median.  The weights were swept at
+// 128K (0/0/0: 49.4 ms per call; 3/4/4: 46.6; 6/8/8: 46.2; 3/8/12: 45.2;
+// 3/8/20: 45.4; 4/12/16: 45.4, flat around the chosen one).  Run r starts at weight
+// W(r) = tile_off[r] + rw r; each warp finds its CTA's first and last tiles by
+// a 32-ary search (every thread of the CTA calls this, warp-uniformly).
+constexpr int64_t kRunWeightMain = 3, kRunWeightLse = 8, kRunWeightGrad = 12;
+__device__ __forceinline__ int64_t tile_at_weight(const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t w,
+                                                  int64_t rw) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = 0, hi = n_gb + 1;  // W(lo) <= w; the run holding weight w lies in [lo, hi)
+  while (hi - lo > 1) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t i = lo + (int64_t)lane * step;
+    const unsigned m = __ballot_sync(0xffffffffu, i < hi && (int64_t)tile_off[i] + rw * i <= w);
+    const int64_t nlo = lo + (int64_t)(31 - __clz(m)) * step;  // bit 0 is set: W(lo) <= w
+    hi = min(hi, nlo + step);
+    lo = nlo;
+  }
+  if (lo >= n_gb) return tile_off[n_gb];
+  const int64_t t0 = tile_off[lo], tr = (int64_t)tile_off[lo + 1] - t0;
+  return t0 + max((int64_t)0, min(tr, w - (t0 + rw * lo) - rw));  // the start weight goes with the run's first tile
+}
+__device__ __forceinline__ void tile_range(const int32_t* tile_off, int64_t n_gb, int64_t rw, int64_t& lo,
+                                           int64_t& hi) {
+  const int64_t wt = (int64_t)tile_off[n_gb] + rw * n_gb;
+  lo = tile_at_weight(tile_off, n_gb, wt * blockIdx.x / gridDim.x, rw);
+  hi = tile_at_weight(tile_off, n_gb, wt * (blockIdx.x + 1) / gridDim.x, rw);
 }
 
 // The teacher rows pass between kernels as bf16 (round to nearest even).
@@ -174,7 +201,7 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
   const uint32_t kIs_a = smem_u32(kIs), qIs_a = smem_u32(qIs);
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, lo, hi);
+  tile_range(tile_off, n_gb, kRunWeightLse, lo, hi);
   int cur_gb = -1;
   for (int64_t ti = lo; ti < hi; ++ti) {
     __syncthreads();
@@ -377,7 +404,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
     });
   };
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, lo, hi);
+  tile_range(tile_off, n_gb, kRunWeightMain, lo, hi);
   if (lo < hi) {
     issue_record(&rc_s[lo % 3], rec, lo);
     if (lo + 1 < hi) issue_record(&rc_s[(lo + 1) % 3], rec, lo + 1);
@@ -578,7 +605,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
     for (int i = tid; i < kPosT * BK / 8; i += blockDim.x) cp_async_16(dst + 8 * i, src + 8 * i, 16);
   };
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, lo, hi);
+  tile_range(tile_off, n_gb, kRunWeightGrad, lo, hi);
   if (lo < hi) {
     issue_record(&rc_s[lo % 3], rec, lo);
     if (lo + 1 < hi) issue_record(&rc_s[(lo + 1) % 3], rec, lo + 1);
@@ -832,7 +859,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   const float kLog2e = 1.4426950408889634f;
   const int64_t kv_row = (int64_t)H_kv * D;
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, lo, hi);
+  tile_range(tile_off, n_gb, kRunWeightMain, lo, hi);
   // Rows of tile ti into Q/dO buffer b.  Thread tid copies 16-byte unit (tid & 15) of rows (tid >> 4) +
   // 16 m, m < 8: positions (tid >> 7) + 2 m, head slot (tid >> 4) & 7; the record fields it needs are
   // loaded together before any copy is issued.  The tile's (group, block) and the next tile's run key
@@ -1226,7 +1253,7 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
   const float s2 = sI * kLog2e;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, lo, hi);
+  tile_range(tile_off, n_gb, kRunWeightLse, lo, hi);
   if (lo < hi) fetch_records(recs_s[0], rec, lo, hi);
   cp_async_commit();
   int32_t cur_gb = -1;
@@ -1350,7 +1377,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
   const float s2 = sI * kLog2e;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, lo, hi);
+  tile_range(tile_off, n_gb, kRunWeightGrad, lo, hi);
   if (lo < hi) fetch_records(recs_s[0], rec, lo, hi);
   cp_async_commit();
   int32_t cur_gb = -1;
