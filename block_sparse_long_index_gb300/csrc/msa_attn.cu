@@ -442,7 +442,7 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, const int32
                              sc.tiles, sc.tile_off, sc.rec, s);
     if (e != cudaSuccess) return e;
     e = launch_attn_tiles(q, k, v, sc.rec, sc.tile_off, p.N, p.H_q, p.H_kv, p.d, p.Bk, p.k, p.nb, p.gs, p.ppr, T0,
-                          p.slab * p.k, p.max_tiles, scale, sc.part_o, sc.part_ml, st, s);
+                          T1, p.slab * p.k, p.max_tiles, scale, sc.part_o, sc.part_ml, st, s);
     if (e != cudaSuccess) return e;
     const CombineSmem lay = combine_smem(p.k, p.H_q, G);
     auto ck = p.d == 64 ? combine_kernel<64> : combine_kernel<128>;

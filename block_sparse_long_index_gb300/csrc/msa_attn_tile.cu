@@ -128,23 +128,42 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t sr
 // run's leading diagonal tiles, whose masked softmax is slower).  Timed per
 // CTA at 128K, an equal count of tiles left the CTAs that hold the short runs
 // of the late blocks 1.2-1.5 ms behind the median (the per-CTA end time fits
-// 4.7 us per run on top of the tiles).  Run r starts at weight
-// W(r) = tile_off[r] + w r; a CTA's first tile is the one at weight
-// W_total c / grid, found by a 32-ary search of one warp.
+// 4.7 us per run on top of the tiles).  A block inside the query slab
+// [T0, T1) has the diagonal tiles of its own positions; a block before the
+// slab (later slabs of a long prefill) has none and weighs less; a block past
+// the slab has no tiles at all and weighs nothing.  With runs in (group,
+// block) order, r = g nb + b, and b0 = T0 / Bk, b1 = ceil(T1 / Bk), the runs
+// before r number F(r) = g b0 + min(b, b0) before the slab and
+// I(r) = g (b1 - b0) + clamp(b - b0, 0, b1 - b0) inside it, so run r starts at
+// weight W(r) = tile_off[r] + rf F(r) + rd I(r).  A CTA's first tile is the
+// one at weight W_total c / grid, found by a 32-ary search of one warp.
+struct RunWeights {
+  int64_t nb, b0, b1, rd, rf;  // blocks per group, the slab's blocks [b0, b1), start weight in / before it
+  __device__ __forceinline__ int64_t start(const int32_t* tile_off, int64_t r) const {
+    const int64_t g = r / nb, b = r % nb;
+    const int64_t before = g * b0 + min(b, b0);
+    const int64_t in = g * (b1 - b0) + min(max(b - b0, (int64_t)0), b1 - b0);
+    return (int64_t)tile_off[r] + rf * before + rd * in;
+  }
+  __device__ __forceinline__ int64_t own(int64_t r) const {
+    const int64_t b = r % nb;
+    return b < b0 ? rf : b < b1 ? rd : 0;
+  }
+};
 __device__ __forceinline__ int64_t tile_at_weight(const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t w,
-                                                  int64_t rw, int lane) {
+                                                  const RunWeights& rw, int lane) {
   int64_t lo = 0, hi = n_gb + 1;  // W(lo) <= w; the run holding weight w lies in [lo, hi)
   while (hi - lo > 1) {
     const int64_t step = (hi - lo + 31) / 32;
     const int64_t i = lo + (int64_t)lane * step;
-    const unsigned m = __ballot_sync(0xffffffffu, i < hi && (int64_t)tile_off[i] + rw * i <= w);
+    const unsigned m = __ballot_sync(0xffffffffu, i < hi && rw.start(tile_off, i) <= w);
     const int64_t nlo = lo + (int64_t)(31 - __clz(m)) * step;  // bit 0 is set: W(lo) <= w
     hi = min(hi, nlo + step);
     lo = nlo;
   }
   if (lo >= n_gb) return tile_off[n_gb];
   const int64_t t0 = tile_off[lo], tr = (int64_t)tile_off[lo + 1] - t0;
-  return t0 + max((int64_t)0, min(tr, w - (t0 + rw * lo) - rw));  // the start weight goes with the run's first tile
+  return t0 + max((int64_t)0, min(tr, w - rw.start(tile_off, lo) - rw.own(lo)));  // with the run's first tile
 }
 
 // K-major, 128B-swizzled operand whose 8-row atoms are `sbo` bytes apart.
@@ -221,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_po,
                    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t max_tiles,
-                   int H_q, int H_kv, int k, int64_t nb, int64_t T0, float scale_log2,
+                   int H_q, int H_kv, int k, int64_t nb, int64_t T0, int64_t T1, float scale_log2,
                    float2* __restrict__ part_ml, DeviceStatus* st) {
   using L = AttnLayout<D, BK>;
   constexpr int GS = 8 / PPR;                  // heads per group = rows per position
@@ -281,12 +300,13 @@ __global__ void __launch_bounds__(kThreadsT, 1)
   }
   if (warp == kWarpLoad) {
     // extra weight of a run start, in tiles (swept at 128K: 2 / 3 / 4 / 5 -> 16.82 / 16.53 / 16.57 / 16.62 ms
-    // per attention call); with ppr > 1 a tile's own time dominates and an equal count splits best
-    constexpr int64_t kRunWeight = PPR == 1 ? 3 : 0;
+    // per attention call; a run before the slab: its K/V load only); with ppr > 1 a tile's own time dominates
+    // and an equal count splits best
+    const RunWeights rw{nb, min(nb, T0 / BK), min(nb, (T1 + BK - 1) / BK), PPR == 1 ? 3 : 0, PPR == 1 ? 1 : 0};
     const int64_t n_gb = (int64_t)H_kv * nb;
-    const int64_t w_total = (int64_t)tile_off[n_gb] + kRunWeight * n_gb;
-    const int64_t a = tile_at_weight(tile_off, n_gb, w_total * blockIdx.x / gridDim.x, kRunWeight, lane);
-    const int64_t z = tile_at_weight(tile_off, n_gb, w_total * (blockIdx.x + 1) / gridDim.x, kRunWeight, lane);
+    const int64_t w_total = rw.start(tile_off, n_gb);
+    const int64_t a = tile_at_weight(tile_off, n_gb, w_total * blockIdx.x / gridDim.x, rw, lane);
+    const int64_t z = tile_at_weight(tile_off, n_gb, w_total * (blockIdx.x + 1) / gridDim.x, rw, lane);
     if (lane == 0) {
       range_s[0] = min(a, max_tiles);
       range_s[1] = min(z, max_tiles);
@@ -707,7 +727,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 
 template <int D, int BK, int PPR>
 cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRecord* rec, const int32_t* tile_off,
-                     int64_t N, int H_q, int H_kv, int k, int64_t nb, int gs, int ppr, int64_t T0, int64_t rows,
+                     int64_t N, int H_q, int H_kv, int k, int64_t nb, int gs, int ppr, int64_t T0, int64_t T1,
+                     int64_t rows,
                      int64_t max_tiles, float scale, uint16_t* part_o, float2* part_ml, DeviceStatus* st,
                      cudaStream_t s) {
   using L = AttnLayout<D, BK>;
@@ -734,7 +755,7 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
   kern<<<num_sms(), kThreadsT, smem, s>>>(
       *reinterpret_cast<const CUtensorMap*>(tq), *reinterpret_cast<const CUtensorMap*>(tk),
       *reinterpret_cast<const CUtensorMap*>(tv), *reinterpret_cast<const CUtensorMap*>(tpo), rec, tile_off,
-      max_tiles, H_q, H_kv, k, nb, T0, scale * 1.4426950408889634f, part_ml, st);
+      max_tiles, H_q, H_kv, k, nb, T0, T1, scale * 1.4426950408889634f, part_ml, st);
   return cudaGetLastError();
 }
 
@@ -742,11 +763,11 @@ cudaError_t launch_t(const void* q, const void* kk, const void* vv, const TileRe
 
 cudaError_t launch_attn_tiles(const void* q, const void* kk, const void* vv, const TileRecord* rec,
                               const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k, int64_t nb,
-                              int gs, int ppr, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
+                              int gs, int ppr, int64_t T0, int64_t T1, int64_t rows, int64_t max_tiles, float scale,
                               uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s) {
   using Fn = cudaError_t (*)(const void*, const void*, const void*, const TileRecord*, const int32_t*, int64_t, int,
-                            int, int, int64_t, int, int, int64_t, int64_t, int64_t, float, uint16_t*, float2*,
-                            DeviceStatus*, cudaStream_t);
+                            int, int, int64_t, int, int, int64_t, int64_t, int64_t, int64_t, float, uint16_t*,
+                            float2*, DeviceStatus*, cudaStream_t);
   // [d == 128][Bk == 128][log2 ppr]
   static const Fn table[2][2][4] = {
       {{launch_t<64, 64, 1>, launch_t<64, 64, 2>, launch_t<64, 64, 4>, launch_t<64, 64, 8>},
@@ -755,7 +776,7 @@ cudaError_t launch_attn_tiles(const void* q, const void* kk, const void* vv, con
        {launch_t<128, 128, 1>, launch_t<128, 128, 2>, launch_t<128, 128, 4>, launch_t<128, 128, 8>}}};
   const int lp = ppr == 1 ? 0 : ppr == 2 ? 1 : ppr == 4 ? 2 : 3;
   const Fn launch = table[d == 128][Bk == 128][lp];
-  return launch(q, kk, vv, rec, tile_off, N, H_q, H_kv, k, nb, gs, ppr, T0, rows, max_tiles, scale, part_o, part_ml,
+  return launch(q, kk, vv, rec, tile_off, N, H_q, H_kv, k, nb, gs, ppr, T0, T1, rows, max_tiles, scale, part_o, part_ml,
                 st, s);
 }
 

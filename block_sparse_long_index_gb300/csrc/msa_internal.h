@@ -86,7 +86,8 @@ size_t attn_scratch_bytes(const AttnPlan& p);
 // The tcgen05 tile kernel of one query slab (msa_attn_tile.cu).
 cudaError_t launch_attn_tiles(const void* q, const void* k, const void* v, const TileRecord* rec,
                               const int32_t* tile_off, int64_t N, int H_q, int H_kv, int d, int Bk, int k_blocks,
-                              int64_t nb, int gs, int ppr, int64_t T0, int64_t rows, int64_t max_tiles, float scale,
+                              int64_t nb, int gs, int ppr, int64_t T0, int64_t T1, int64_t rows, int64_t max_tiles,
+                              float scale,
                               uint16_t* part_o, float2* part_ml, DeviceStatus* st, cudaStream_t s);
 // The flat tile list of positions [T0, T1) from the CSR (row_ptr, entries): per (g, b)
 // the list's positions cut into tiles of 16 ppr positions, tile_off[G*nb] = total
