@@ -63,33 +63,53 @@ constexpr int kThreadsB = 256;
 // load, the dK/dV or dk^I flush at its end, its leading diagonal tiles, and in
 // the index passes a partial chunk of 8 tiles).  With an equal count, per-CTA
 // timers at 128K left the CTAs holding the late blocks' short runs 2 ms (main)
-// and 3 ms (index gradient) behind the median.  The weights were swept at
-// 128K (0/0/0: 49.4 ms per call; 3/4/4: 46.6; 6/8/8: 46.2; 3/8/12: 45.2;
-// 3/8/20: 45.4; 4/12/16: 45.4, flat around the chosen one).  Run r starts at weight
-// W(r) = tile_off[r] + rw r; each warp finds its CTA's first and last tiles by
-// a 32-ary search (every thread of the CTA calls this, warp-uniformly).
-constexpr int64_t kRunWeightMain = 3, kRunWeightLse = 8, kRunWeightGrad = 12;
-__device__ __forceinline__ int64_t tile_at_weight(const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t w,
-                                                  int64_t rw) {
+// and 3 ms (index gradient) behind the median.  The in-slab weights were swept
+// at 128K (main/lse/gradient 0/0/0: 49.4 ms per call; 3/4/4: 46.6; 6/8/8: 46.2;
+// 3/8/12: 45.2; 3/8/20: 45.4; 4/12/16: 45.4, flat around the chosen one).
+// A slab's runs: n_gb = G nb runs in (group, block) order, r = g nb + b; the
+// slab's own blocks are [b0, b1).  A run weighs its tiles plus `in` for its
+// start when its block lies in the slab, `before` when the block precedes the
+// slab (no diagonal tiles: later slabs of a long sequence), and 0 past the slab
+// (no tiles).  The runs before r number g b0 + min(b, b0) before the slab and
+// g (b1 - b0) + clamp(b - b0, 0, b1 - b0) inside it, so the prefix weight has a
+// closed form and each warp finds its CTA's first and last tiles by a 32-ary
+// search (every thread of the CTA calls tile_range, warp-uniformly).
+struct RunSpan {
+  int64_t n_gb, nb, b0, b1;
+};
+struct RunWeight {
+  int64_t in, before;
+};
+constexpr RunWeight kRunWeightMain{3, 2}, kRunWeightLse{8, 7}, kRunWeightGrad{12, 11};
+__device__ __forceinline__ int64_t run_start(const int32_t* __restrict__ tile_off, const RunSpan& rs, RunWeight rw,
+                                             int64_t r) {
+  const int64_t g = r / rs.nb, b = r % rs.nb;
+  const int64_t before = g * rs.b0 + min(b, rs.b0);
+  const int64_t in = g * (rs.b1 - rs.b0) + min(max(b - rs.b0, (int64_t)0), rs.b1 - rs.b0);
+  return (int64_t)tile_off[r] + rw.before * before + rw.in * in;
+}
+__device__ __forceinline__ int64_t tile_at_weight(const int32_t* __restrict__ tile_off, const RunSpan& rs,
+                                                  RunWeight rw, int64_t w) {
   const int lane = threadIdx.x & 31;
-  int64_t lo = 0, hi = n_gb + 1;  // W(lo) <= w; the run holding weight w lies in [lo, hi)
+  int64_t lo = 0, hi = rs.n_gb + 1;  // W(lo) <= w; the run holding weight w lies in [lo, hi)
   while (hi - lo > 1) {
     const int64_t step = (hi - lo + 31) / 32;
     const int64_t i = lo + (int64_t)lane * step;
-    const unsigned m = __ballot_sync(0xffffffffu, i < hi && (int64_t)tile_off[i] + rw * i <= w);
+    const unsigned m = __ballot_sync(0xffffffffu, i < hi && run_start(tile_off, rs, rw, i) <= w);
     const int64_t nlo = lo + (int64_t)(31 - __clz(m)) * step;  // bit 0 is set: W(lo) <= w
     hi = min(hi, nlo + step);
     lo = nlo;
   }
-  if (lo >= n_gb) return tile_off[n_gb];
+  if (lo >= rs.n_gb) return tile_off[rs.n_gb];
+  const int64_t b = lo % rs.nb, own = b < rs.b0 ? rw.before : b < rs.b1 ? rw.in : 0;
   const int64_t t0 = tile_off[lo], tr = (int64_t)tile_off[lo + 1] - t0;
-  return t0 + max((int64_t)0, min(tr, w - (t0 + rw * lo) - rw));  // the start weight goes with the run's first tile
+  return t0 + max((int64_t)0, min(tr, w - run_start(tile_off, rs, rw, lo) - own));  // with the run's first tile
 }
-__device__ __forceinline__ void tile_range(const int32_t* tile_off, int64_t n_gb, int64_t rw, int64_t& lo,
+__device__ __forceinline__ void tile_range(const int32_t* tile_off, const RunSpan& rs, RunWeight rw, int64_t& lo,
                                            int64_t& hi) {
-  const int64_t wt = (int64_t)tile_off[n_gb] + rw * n_gb;
-  lo = tile_at_weight(tile_off, n_gb, wt * blockIdx.x / gridDim.x, rw);
-  hi = tile_at_weight(tile_off, n_gb, wt * (blockIdx.x + 1) / gridDim.x, rw);
+  const int64_t wt = run_start(tile_off, rs, rw, rs.n_gb);
+  lo = tile_at_weight(tile_off, rs, rw, wt * blockIdx.x / gridDim.x);
+  hi = tile_at_weight(tile_off, rs, rw, wt * (blockIdx.x + 1) / gridDim.x);
 }
 
 // The teacher rows pass between kernels as bf16 (round to nearest even).
@@ -191,7 +211,7 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const uint16_t* __restr
 template <int BK, int DI>
 __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const TileRecord* __restrict__ rec,
-    const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int G, int k, float sI,
+    const int32_t* __restrict__ tile_off, RunSpan rs, int64_t N, int G, int k, float sI,
     float2* __restrict__ part) {
   __shared__ __align__(128) uint16_t kIs[BK * DI];
   __shared__ __align__(128) uint16_t qIs[kPosT * DI];
@@ -201,7 +221,7 @@ __global__ void __launch_bounds__(kThreadsB) bwd_index_lse_kernel(
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g8 = lane >> 2, c4 = lane & 3;
   const uint32_t kIs_a = smem_u32(kIs), qIs_a = smem_u32(qIs);
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, kRunWeightLse, lo, hi);
+  tile_range(tile_off, rs, kRunWeightLse, lo, hi);
   int cur_gb = -1;
   for (int64_t ti = lo; ti < hi; ++ti) {
     __syncthreads();
@@ -331,7 +351,7 @@ template <int D, int BK>
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
     const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
-    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int H_q,
+    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, RunSpan rs, int64_t N, int H_q,
     int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
     uint16_t* __restrict__ pbar_g) {
   using L = MainSmem<D, BK>;
@@ -404,7 +424,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_kernel(
     });
   };
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, kRunWeightMain, lo, hi);
+  tile_range(tile_off, rs, kRunWeightMain, lo, hi);
   if (lo < hi) {
     issue_record(&rc_s[lo % 3], rec, lo);
     if (lo + 1 < hi) issue_record(&rc_s[(lo + 1) % 3], rec, lo + 1);
@@ -556,7 +576,7 @@ template <int BK, int DI>
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const float* __restrict__ lseI,
     const uint16_t* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
-    int64_t n_gb, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
+    RunSpan rs, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
     float* __restrict__ kl) {
   using L = IndexSmem<BK, DI>;
   extern __shared__ __align__(128) uint8_t smb[];
@@ -605,7 +625,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_index_kernel(
     for (int i = tid; i < kPosT * BK / 8; i += blockDim.x) cp_async_16(dst + 8 * i, src + 8 * i, 16);
   };
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, kRunWeightGrad, lo, hi);
+  tile_range(tile_off, rs, kRunWeightGrad, lo, hi);
   if (lo < hi) {
     issue_record(&rc_s[lo % 3], rec, lo);
     if (lo + 1 < hi) issue_record(&rc_s[(lo + 1) % 3], rec, lo + 1);
@@ -825,7 +845,7 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
     const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
-    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int H_q,
+    const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, RunSpan rs, int64_t N, int H_q,
     int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
     uint16_t* __restrict__ pbar_g, DeviceStatus* st) {
   using namespace tcb;
@@ -859,7 +879,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   const float kLog2e = 1.4426950408889634f;
   const int64_t kv_row = (int64_t)H_kv * D;
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, kRunWeightMain, lo, hi);
+  tile_range(tile_off, rs, kRunWeightMain, lo, hi);
   // Rows of tile ti into Q/dO buffer b.  Thread tid copies 16-byte unit (tid & 15) of rows (tid >> 4) +
   // 16 m, m < 8: positions (tid >> 7) + 2 m, head slot (tid >> 4) & 7; the record fields it needs are
   // loaded together before any copy is issued.  The tile's (group, block) and the next tile's run key
@@ -1224,7 +1244,7 @@ __device__ __forceinline__ void load_chunk(uint8_t* sm, const uint16_t* q_idx, c
 
 __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const TileRecord* __restrict__ rec,
-    const int32_t* __restrict__ tile_off, int64_t n_gb, int64_t N, int G, int k, float sI,
+    const int32_t* __restrict__ tile_off, RunSpan rs, int64_t N, int G, int k, float sI,
     float2* __restrict__ part, DeviceStatus* st) {
   using namespace tci;
   extern __shared__ uint8_t smraw[];
@@ -1253,7 +1273,7 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
   const float s2 = sI * kLog2e;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, kRunWeightLse, lo, hi);
+  tile_range(tile_off, rs, kRunWeightLse, lo, hi);
   if (lo < hi) fetch_records(recs_s[0], rec, lo, hi);
   cp_async_commit();
   int32_t cur_gb = -1;
@@ -1348,7 +1368,7 @@ __global__ void __launch_bounds__(tci::kThreads, 3) bwd_index_lse_tc_kernel(
 __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     const uint16_t* __restrict__ q_idx, const uint16_t* __restrict__ k_idx, const float* __restrict__ lseI,
     const uint16_t* __restrict__ pbar_g, const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off,
-    int64_t n_gb, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
+    RunSpan rs, int64_t N, int G, float sI, float w, float* __restrict__ dq_idx, float* __restrict__ dk_idx,
     float* __restrict__ kl, DeviceStatus* st) {
   using namespace tci;
   extern __shared__ uint8_t smraw[];
@@ -1377,7 +1397,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
   const float s2 = sI * kLog2e;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   int64_t lo, hi;
-  tile_range(tile_off, n_gb, kRunWeightGrad, lo, hi);
+  tile_range(tile_off, rs, kRunWeightGrad, lo, hi);
   if (lo < hi) fetch_records(recs_s[0], rec, lo, hi);
   cp_async_commit();
   int32_t cur_gb = -1;
@@ -1568,6 +1588,7 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
                          cudaStream_t s) {
   const int G = H_kv, gs = H_q / H_kv;
   const int64_t n_gb = (int64_t)G * sc.nb;
+  const RunSpan rs{n_gb, sc.nb, T0 / BK, (T1 + BK - 1) / BK};
   const float sI = 1.f / sqrtf((float)DI);
   const int grid = num_sms();
   constexpr bool kIndexTc = BK == 128 && DI == 128;
@@ -1576,10 +1597,10 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
                                           tci::kLseBytes);
     if (e0 != cudaSuccess) return e0;
     bwd_index_lse_tc_kernel<<<3 * grid, tci::kThreads, tci::kLseBytes, s>>>(
-        (const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec, sc.tile_off, n_gb, N, G, k, sI, sc.partI, st);
+        (const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec, sc.tile_off, rs, N, G, k, sI, sc.partI, st);
   } else {
     bwd_index_lse_kernel<BK, DI><<<grid, kThreadsB, 0, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.rec,
-                                                            sc.tile_off, n_gb, N, G, k, sI, sc.partI);
+                                                            sc.tile_off, rs, N, G, k, sI, sc.partI);
   }
   {
     int kp = 1;
@@ -1595,14 +1616,14 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
     if (e != cudaSuccess) return e;
     bwd_main_tc_kernel<<<grid, kThreadsB, tcb::kBytes, s>>>((const uint16_t*)q, (const uint16_t*)kk,
                                                             (const uint16_t*)v, (const uint16_t*)dout, lse, sc.Dr,
-                                                            sc.rec, sc.tile_off, n_gb, N, H_q, H_kv, gs, scale, dq,
+                                                            sc.rec, sc.tile_off, rs, N, H_q, H_kv, gs, scale, dq,
                                                             dk, dv, sc.pbar, st);
   } else {
     auto km = bwd_main_kernel<D, BK>;
     e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, MainSmem<D, BK>::BYTES);
     if (e != cudaSuccess) return e;
     km<<<grid, kThreadsB, MainSmem<D, BK>::BYTES, s>>>((const uint16_t*)q, (const uint16_t*)kk, (const uint16_t*)v,
-                                                      (const uint16_t*)dout, lse, sc.Dr, sc.rec, sc.tile_off, n_gb, N,
+                                                      (const uint16_t*)dout, lse, sc.Dr, sc.rec, sc.tile_off, rs, N,
                                                       H_q, H_kv, gs, scale, dq, dk, dv, sc.pbar);
   }
   e = cudaGetLastError();
@@ -1611,7 +1632,7 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
     e = cudaFuncSetAttribute(bwd_index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tci::kGradBytes);
     if (e != cudaSuccess) return e;
     bwd_index_tc_kernel<<<2 * grid, tci::kThreads, tci::kGradBytes, s>>>(
-        (const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.lseI, sc.pbar, sc.rec, sc.tile_off, n_gb, N, G, sI,
+        (const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.lseI, sc.pbar, sc.rec, sc.tile_off, rs, N, G, sI,
         kl_weight, dq_idx, dk_idx, kl, st);
     return cudaGetLastError();
   }
@@ -1619,7 +1640,7 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
   e = cudaFuncSetAttribute(ki, cudaFuncAttributeMaxDynamicSharedMemorySize, IndexSmem<BK, DI>::BYTES);
   if (e != cudaSuccess) return e;
   ki<<<grid, kThreadsB, IndexSmem<BK, DI>::BYTES, s>>>((const uint16_t*)q_idx, (const uint16_t*)k_idx, sc.lseI,
-                                                      sc.pbar, sc.rec, sc.tile_off, n_gb, N, G, sI, kl_weight, dq_idx,
+                                                      sc.pbar, sc.rec, sc.tile_off, rs, N, G, sI, kl_weight, dq_idx,
                                                       dk_idx, kl);
   return cudaGetLastError();
 }
