@@ -146,19 +146,24 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   }
   __syncthreads();
 
-  // this warp's chunks [c0, c1) of the CTA's nblk * CPB
-  const int64_t nch = (int64_t)nblk * CPB;
-  const int64_t c0 = nch * warp / kScanWarps, c1 = nch * (warp + 1) / kScanWarps;
+  // this warp's chunks [c0, c1) of the CTA's nblk * CPB.  Chunk indices and
+  // offsets within the CTA's range are 32-bit (nblk <= kMaxCtaBlocks, so an
+  // offset stays below 2^26 bytes): the per-chunk loop carries no 64-bit
+  // integer arithmetic, which at E4M3's 2 KB chunks was most of its ALU work.
+  constexpr int CPB_SHIFT = CPB == 8 ? 3 : CPB == 4 ? 2 : CPB == 2 ? 1 : 0;
+  static_assert((1 << CPB_SHIFT) == CPB, "chunks per block is a power of two");
+  const int nch = nblk * CPB;
+  const int c0 = nch * warp / kScanWarps, c1 = nch * (warp + 1) / kScanWarps;
   const uint8_t* base = k_idx_cache + ((int64_t)seq * ctx_max + b_lo * BK + row) * RB + 16 * c;
   // first key row of chunk cc (+ row): contiguous, or through the page table (a page holds whole chunks)
-  auto chunk_ptr = [&](int64_t cc) -> const uint8_t* {
-    if (!PAGED) return base + cc * 16 * RB;
-    const int64_t key = b_lo * BK + cc * 16;
+  auto chunk_ptr = [&](int cc) -> const uint8_t* {
+    if (!PAGED) return base + (uint32_t)cc * (uint32_t)(16 * RB);
+    const int64_t key = b_lo * BK + (int64_t)cc * 16;
     const int64_t r = map.row(seq, key, st);
     return k_idx_cache + (r + row) * RB + 16 * c;
   };
   float bm0 = __int_as_float(0xff800000), bm1 = bm0;
-  auto score = [&](const uint4 (&v)[NQ][2], int64_t cc) {
+  auto score = [&](const uint4 (&v)[NQ][2], int cc) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
     }
     bm0 = fmaxf(bm0, fmaxf(acc[0], acc[2]));  // group 2c, keys row and row+8
     bm1 = fmaxf(bm1, fmaxf(acc[1], acc[3]));  // group 2c+1
-    if ((cc % CPB) == CPB - 1 || cc == c1 - 1) {  // end of this warp's part of a block
+    if ((cc & (CPB - 1)) == CPB - 1 || cc == c1 - 1) {  // end of this warp's part of a block
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
         bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o));
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
       // group g's maximum sits in lane g/2 (value g&1)
       const float x0 = __shfl_sync(0xffffffffu, bm0, (lane & 7) >> 1);
       const float x1 = __shfl_sync(0xffffffffu, bm1, (lane & 7) >> 1);
-      if (lane < G) atomicMax(&bmax_s[(int)(cc / CPB) * kGroupsPerMma + lane], ordered_bits((lane & 1) ? x1 : x0));
+      if (lane < G) atomicMax(&bmax_s[(cc >> CPB_SHIFT) * kGroupsPerMma + lane], ordered_bits((lane & 1) ? x1 : x0));
       bm0 = bm1 = __int_as_float(0xff800000);
     }
   };
@@ -194,10 +199,10 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
 #pragma unroll
   for (int p = 0; p < PD - 1; ++p)
     if (c0 + p < c1) load_keys16<RB>(vr[p], chunk_ptr(c0 + p));
-  for (int64_t ci = c0; ci < c1; ci += PD) {
+  for (int ci = c0; ci < c1; ci += PD) {
 #pragma unroll
     for (int p = 0; p < PD; ++p) {
-      const int64_t cc = ci + p;
+      const int cc = ci + p;
       if (cc < c1) {
         if (cc + PD - 1 < c1) load_keys16<RB>(vr[(p + PD - 1) % PD], chunk_ptr(cc + PD - 1));
         score(vr[p], cc);
