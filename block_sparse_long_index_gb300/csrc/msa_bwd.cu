@@ -840,10 +840,23 @@ __device__ __forceinline__ void red_add4(float* p, float a, float b, float c, fl
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// fp32 add of a shared-memory box into the tensor behind `map` at {x, y, z}, by the TMA unit (bulk group)
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y,
+                                                  int32_t z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::
+                   "l"(reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// this thread's bulk operations have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// ... and have completed
+__device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 }  // namespace tcb
 
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
-    const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
+    const __grid_constant__ CUtensorMap tmap_dq, const uint16_t* __restrict__ q, const uint16_t* __restrict__ kc, const uint16_t* __restrict__ vc,
     const uint16_t* __restrict__ dout, const float* __restrict__ lse, const float* __restrict__ Dr,
     const TileRecord* __restrict__ rec, const int32_t* __restrict__ tile_off, RunSpan rs, int64_t N, int H_q,
     int H_kv, int gs, float scale, float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
@@ -956,6 +969,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     cp_async_commit();
     cp_async_wait<0>();  // this tile's rows (issued during the previous tile) and a new run's K/V
     sm100::fence_proxy_async_smem();
+    bulk_wait_read();  // the previous tile's dQ reductions have read their staging (buffer buf ^ 1)
     __syncthreads();
     const uint32_t qb = sb + kQ + buf * kTile, dob = sb + kDO + buf * kTile;
     // ---- S^T and dP^T
@@ -1057,31 +1071,33 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
       const int r = quad * 32 + lane;
       {  // dQ: thread = tile row r, warpgroup `half` = d columns 64 half .. + 63
-        // The scaled rows are staged in this tile's Q (half 0) or dO (half 1) buffer, free now: 256 bytes
-        // per row, 16-byte unit u at u ^ (row % 16), so that the row-wise writes and the unit-wise reads
-        // below are both conflict-free.  Each warp then adds back the 32 rows it wrote, two rows (512
-        // contiguous bytes of dq each) per instruction, instead of 32 scattered rows.
+        // The scaled rows are staged in this tile's Q (half 0) or dO (half 1) buffer, free now, as two
+        // 32-column fp32 chunks of 128 rows x 128 bytes in the 128B-swizzled layout of the dq tensor map
+        // (16-byte unit u of row r at u ^ (r % 8): conflict-free row-wise writes).  A position's gs rows are
+        // one box {32 columns, gs heads, 1 position}; lanes 0-7 of each warp hand the warp's 4 positions x 2
+        // chunks to the TMA unit as fp32 add-reductions into dq, which drain while the next tile computes.
         uint32_t x[2][32];
         sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64, x[0]);
         sm100::tmem_ld_x32(tmem + lane_base + 128 + half * 64 + 32, x[1]);
         sm100::tmem_ld_wait();
-        uint8_t* stg = sm + (half ? kDO : kQ) + buf * kTile;
+        const uint32_t stg = (half ? kDO : kQ) + buf * kTile;  // chunk j at stg + j kChunk
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const uint32_t* xs = &x[u >> 3][(u & 7) * 4];
-          *reinterpret_cast<float4*>(stg + r * 256 + ((u ^ (r & 15)) << 4)) =
-              make_float4(scale * __uint_as_float(xs[0]), scale * __uint_as_float(xs[1]),
-                          scale * __uint_as_float(xs[2]), scale * __uint_as_float(xs[3]));
-        }
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint32_t* xs = &x[j][u * 4];
+            *reinterpret_cast<float4*>(sm + stg + j * kChunk + r * 128 + ((u ^ (r & 7)) << 4)) =
+                make_float4(scale * __uint_as_float(xs[0]), scale * __uint_as_float(xs[1]),
+                            scale * __uint_as_float(xs[2]), scale * __uint_as_float(xs[3]));
+          }
+        sm100::fence_proxy_async_smem();
         __syncwarp();
-        const int u = lane & 15;
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-          const int rr = quad * 32 + 2 * it + (lane >> 4);
-          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 256 + ((u ^ (rr & 15)) << 4));
-          const int32_t t = trow_s[rr];
+        if (lane < 8) {
+          const int p = quad * 4 + (lane >> 1), j = lane & 1;  // position of the tile, chunk of this half
+          const int32_t t = trow_s[p * 8];
           if (t >= 0)
-            red_add4(dq + ((int64_t)t * H_q + cur_g * gs + (rr & 7)) * D + half * 64 + u * 4, v.x, v.y, v.z, v.w);
+            tma_reduce_add_3d(&tmap_dq, sb + stg + j * kChunk + p * 1024, (2 * half + j) * 32, cur_g * gs, t);
+          bulk_commit();
         }
       }
       if (run_ends) {  // thread = key: the run's dV and dK
@@ -1112,6 +1128,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     ++nt;
   }
   cp_async_wait<0>();  // no copy of ours is left in flight when the CTA exits
+  bulk_wait();
   __syncthreads();
   if (warp == 4) {
     if (lane == 0 && *abort && issued) {  // let the MMAs in flight finish before TMEM is released
@@ -1614,7 +1631,13 @@ cudaError_t launch_tiles(const void* q, const void* kk, const void* v, const voi
   if constexpr (D == 128 && BK == 128) {
     e = cudaFuncSetAttribute(bwd_main_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tcb::kBytes);
     if (e != cudaSuccess) return e;
-    bwd_main_tc_kernel<<<grid, kThreadsB, tcb::kBytes, s>>>((const uint16_t*)q, (const uint16_t*)kk,
+    // dq as {d, H_q, N} fp32 with 32-column, gs-head boxes, 128B-swizzled: the main kernel's reductions
+    alignas(64) unsigned char tdq[128];
+    if (!encode_tmap_3d(tdq, dq, (uint64_t)D, (uint64_t)H_q, (uint64_t)N, (uint64_t)D * 4, (uint64_t)H_q * D * 4, 32,
+                        (uint32_t)gs, 1, 128, 4))
+      return cudaErrorInvalidValue;
+    bwd_main_tc_kernel<<<grid, kThreadsB, tcb::kBytes, s>>>(*reinterpret_cast<const CUtensorMap*>(tdq),
+                                                            (const uint16_t*)q, (const uint16_t*)kk,
                                                             (const uint16_t*)v, (const uint16_t*)dout, lse, sc.Dr,
                                                             sc.rec, sc.tile_off, rs, N, H_q, H_kv, gs, scale, dq,
                                                             dk, dv, sc.pbar, st);

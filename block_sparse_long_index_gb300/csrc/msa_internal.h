@@ -22,9 +22,11 @@ int num_sms();  // cached cudaDevAttrMultiProcessorCount of the current device
 bool encode_tmap_2d(void* tmap /* CUtensorMap */, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, int swizzle_bytes,
                     int elem_bytes = 2);
-// 3-D variant: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1 and 2, box {b0, b1, b2}.
+// 3-D variant: dims {d0, d1, d2} (d0 contiguous), byte strides of dims 1 and 2, box {b0, b1, b2}; elements
+// are bf16 (elem_bytes 2) or fp32 (elem_bytes 4).
 bool encode_tmap_3d(void* tmap, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
-                    uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes);
+                    uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2, int swizzle_bytes,
+                    int elem_bytes = 2);
 // 4-D variant: byte strides of dims 1..3 in any order (a permuted view is allowed).
 bool encode_tmap_4d(void* tmap, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
                     const uint32_t box[4], int swizzle_bytes);
