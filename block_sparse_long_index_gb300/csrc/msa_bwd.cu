@@ -813,6 +813,36 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
 // its per-row position, lse and D into registers) while tile i computes.
 // Warp 4 owns TMEM and its lane 0 issues the MMAs.  Phases are separated by
 // CTA barriers and MMA completion mbarriers; every wait is bounded.
+// Packed pairs of fp32 (one 64-bit register): two lanes per instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 namespace tcb {
 constexpr int kChunk = 128 * 128;  // one 64-column chunk of a 128-row tile, bytes
 constexpr int kTile = 2 * kChunk;  // one 128 x 128 bf16 tile
@@ -868,7 +898,7 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
   const uint32_t sb = smem_u32(sm);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ float lse2_s[kRowsT], D_s[kRowsT];  // lse in log2 units, D
+  __shared__ __align__(16) float nlse2_s[kRowsT], nD_s[kRowsT];  // -lse in log2 units (-inf: no position), -D
   __shared__ int32_t trow_s[kRowsT];              // position of each tile row, -1 if none
   const uint32_t bar_s = sb + kBar, bar_q = sb + kBar + 8, bar_drain = sb + kBar + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -921,8 +951,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
       cp_async_16(sm + kDO + b * kTile + o, ok ? dout + ((int64_t)t * H_q + hrow) * D + c : dout, ok ? 16 : 0);
     }
   };
-  // Row info of tile ti (thread tid < 128 = row tid): position, lse, D; loaded while the previous tile's
-  // second MMA batch runs, stored to shared memory at the tile's start.
+  // Row info of tile ti (thread tid < 128 = row tid): position, lse, D; loaded with the tile's rows (during
+  // the previous tile), stored to shared memory at the tile's start.
   int32_t nt_t = -1;
   float nt_lse = 0.f, nt_D = 0.f;
   auto load_row_info = [&](int64_t ti) {
@@ -950,8 +980,8 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     const bool run_ends = ti + 1 >= hi || nx2_gb != gb;
     if (tid < kRowsT) {  // this tile's row info
       trow_s[tid] = nt_t;
-      lse2_s[tid] = nt_lse * kLog2e;
-      D_s[tid] = nt_D;
+      nlse2_s[tid] = nt_t >= 0 ? -nt_lse * kLog2e : -INFINITY;
+      nD_s[tid] = -nt_D;
     }
     if (new_run) {
       cur_gb = gb;
@@ -970,7 +1000,9 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
     cp_async_wait<0>();  // this tile's rows (issued during the previous tile) and a new run's K/V
     sm100::fence_proxy_async_smem();
     bulk_wait_read();  // the previous tile's dQ reductions have read their staging (buffer buf ^ 1)
-    __syncthreads();
+    // full: every row either has no position or sees the whole block (t >= last key), so no key is masked
+    const bool full =
+        __syncthreads_and(tid >= kRowsT || nt_t < 0 || (int64_t)nt_t >= (int64_t)cur_b * BK + BK - 1) != 0;
     const uint32_t qb = sb + kQ + buf * kTile, dob = sb + kDO + buf * kTile;
     // ---- S^T and dP^T
     if (warp == 4 && lane == 0) {
@@ -986,9 +1018,12 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
       sm100::umma_commit(bar_s);
       issued = true;
     }
-    // the next tile's rows stream in while this one computes (its buffer's last readers, the
-    // previous tile's MMAs, have completed)
-    if (ti + 1 < hi) issue_rows(ti + 1, buf ^ 1);
+    // the next tile's rows and row info stream in while this one computes (its buffer's last readers,
+    // the previous tile's MMAs, have completed)
+    if (ti + 1 < hi) {
+      issue_rows(ti + 1, buf ^ 1);
+      load_row_info(ti + 1);
+    }
     cp_async_commit();
     // ---- P^T (to TMEM), dZ^T (to shared memory) and the teacher: thread = key
     if (sm100::mbar_wait(bar_s, nt & 1, abort, st, 0x801)) {
@@ -1012,20 +1047,53 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
         }
         uint32_t pk[16], zk[16];
         float tsum[4] = {0.f, 0.f, 0.f, 0.f};
+        if (full) {  // two rows per instruction; rows without a position get 2^-inf = 0
+          const uint64_t sl2x2 = f2_pack(sl2, sl2);
+          uint64_t tacc[4];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], zv[2];
+          for (int pp = 0; pp < 4; ++pp) tacc[pp] = f2_pack(0.f, 0.f);
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = cc * 32 + e + u;
-            const bool ok = j <= (int64_t)trow_s[r];  // -1 for rows without a position
-            const float p = ok ? sm100::ex2_approx(fmaf(__uint_as_float(sx[h2][e + u]), sl2, -lse2_s[r])) : 0.f;
-            pv[u] = p;
-            zv[u] = p * (__uint_as_float(px[h2][e + u]) - D_s[r]);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 nl = *reinterpret_cast<const float4*>(&nlse2_s[cc * 32 + e]);
+            const float4 nd = *reinterpret_cast<const float4*>(&nD_s[cc * 32 + e]);
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              float a0, a1, z0, z1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sx[h2][e + u]), __uint_as_float(sx[h2][e + u + 1])), sl2x2,
+                               u ? f2_pack(nl.z, nl.w) : f2_pack(nl.x, nl.y)),
+                        a0, a1);
+              const float p0 = sm100::ex2_approx(a0), p1 = sm100::ex2_approx(a1);
+              const uint64_t p2 = f2_pack(p0, p1);
+              f2_unpack(f2_mul(p2, f2_add(f2_pack(__uint_as_float(px[h2][e + u]), __uint_as_float(px[h2][e + u + 1])),
+                                          u ? f2_pack(nd.z, nd.w) : f2_pack(nd.x, nd.y))),
+                        z0, z1);
+              tacc[e >> 3] = f2_add(tacc[e >> 3], p2);
+              pk[(e + u) >> 1] = pack_bf16x2(p0, p1);
+              zk[(e + u) >> 1] = pack_bf16x2(z0, z1);
+            }
           }
-          tsum[e >> 3] += pv[0] + pv[1];
-          pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-          zk[e >> 1] = pack_bf16x2(zv[0], zv[1]);
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            float t0, t1;
+            f2_unpack(tacc[pp], t0, t1);
+            tsum[pp] = t0 + t1;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], zv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int r = cc * 32 + e + u;
+              const bool ok = j <= (int64_t)trow_s[r];  // -1 for rows without a position
+              const float p = ok ? sm100::ex2_approx(fmaf(__uint_as_float(sx[h2][e + u]), sl2, nlse2_s[r])) : 0.f;
+              pv[u] = p;
+              zv[u] = p * (__uint_as_float(px[h2][e + u]) + nD_s[r]);
+            }
+            tsum[e >> 3] += pv[0] + pv[1];
+            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+            zk[e >> 1] = pack_bf16x2(zv[0], zv[1]);
+          }
         }
         if (pbar_g) {
 #pragma unroll
@@ -1065,7 +1133,6 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
                            sm100::umma_desc_mnmajor_sw128(sb + kK + ks * 16 * 128, kChunk), kIdescMnAB, ks > 0);
       sm100::umma_commit(bar_q);
     }
-    if (ti + 1 < hi) load_row_info(ti + 1);
     if (sm100::mbar_wait(bar_q, nt & 1, abort, st, 0x802)) {
       sm100::tc_fence_after();
       const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -1166,36 +1233,6 @@ constexpr int kKI = 0, kQI = tcb::kTile, kDZ = 2 * tcb::kTile;
 constexpr int kLseBar = 2 * tcb::kTile, kLseBytes = 1024 + kLseBar + 64;
 constexpr int kGradBar = 3 * tcb::kTile, kGradBytes = 1024 + kGradBar + 64;
 constexpr uint32_t kIdescSS = tcb::kIdescSS, kIdescMnB = tcb::kIdescMnB, kIdescMnAB = tcb::kIdescMnAB;
-
-// Packed pairs of fp32 (one 64-bit register): two lanes per instruction.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ float lg2_approx(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 // Records [ti0, ti0 + kRecs) that lie below hi into dst: 16-byte cp.async pieces, threads 0 .. 8 kRecs - 1.
 __device__ __forceinline__ void fetch_records(TileRecord* dst, const TileRecord* rec, int64_t ti0, int64_t hi) {
