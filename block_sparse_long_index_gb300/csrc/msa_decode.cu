@@ -78,6 +78,37 @@ __device__ __forceinline__ uint64_t warp_max_key(uint64_t x) {
   return ((uint64_t)mh << 32) | ml;
 }
 
+// Descending sort of the 32 R keys x[j] (element e = 32 j + lane) across a warp: a bitonic network whose
+// partner at distance d is a shuffle for d < 32 and another register of the same lane for d >= 32.  In each
+// compare-exchange the element with the lower index keeps the larger key exactly when its block of kk
+// elements is to end up in descending order; the last merge (kk = 32 R) orders the whole warp.
+template <int R>
+__device__ __forceinline__ void warp_sort_desc(uint64_t (&x)[R], int lane) {
+#pragma unroll
+  for (int kk = 2; kk <= 32 * R; kk <<= 1) {
+#pragma unroll
+    for (int d = kk >> 1; d > 0; d >>= 1) {
+      uint64_t y[R];
+#pragma unroll
+      for (int j = 0; j < R; ++j) {
+        const int e = 32 * j + lane;
+        uint64_t o;
+        if (d >= 32) {
+          o = x[j ^ (d >> 5)];
+        } else {
+          const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(x[j] >> 32), d);
+          const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)x[j], d);
+          o = ((uint64_t)hi << 32) | lo;
+        }
+        const bool keep_max = ((e & d) == 0) == ((e & kk) == 0);
+        y[j] = keep_max == (x[j] > o) ? x[j] : o;
+      }
+#pragma unroll
+      for (int j = 0; j < R; ++j) x[j] = y[j];
+    }
+  }
+}
+
 // 16-byte pieces 64q + 16c of key rows `row` and `row + 8` of a 16-key chunk (RB bytes per row)
 template <int RB>
 __device__ __forceinline__ void load_keys16(uint4 (&v)[RB / 64][2], const uint8_t* p) {
@@ -211,12 +242,24 @@ __global__ void __launch_bounds__(kScanThreads, 2) decode_scan_kernel(
   }
   __syncthreads();
 
-  // this CTA's top-(k-1) blocks of group g (warp g): lane l ranks blocks l,
-  // l + 32, ... of the CTA's range into its register list of the best CAP (one
-  // insertion site in a rolled loop), then k-1 rounds of a warp-wide maximum
-  // over the lists' heads pop the CTA's list, best first
+  // this CTA's top-(k-1) blocks of group g (warp g), best first (0 where the CTA has fewer candidates).
+  // Up to 128 blocks: one warp-wide sort of their (maximum, ~id) keys.  More: lane l ranks blocks l,
+  // l + 32, ... into its register list of the best CAP (one insertion site in a rolled loop), then k-1
+  // rounds of a warp-wide maximum over the lists' heads pop the CTA's list.
   const int kp = km1 + (km1 & 1);  // list stride: an even count of keys (16-byte rows)
-  if (warp < G) {
+  if (warp < G && nblk <= 128) {
+    const int g = warp;
+    uint64_t x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int b = 32 * j + lane;
+      const uint32_t o = b < nblk ? bmax_s[b * kGroupsPerMma + g] : 0u;
+      x[j] = o ? ((uint64_t)o << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)(b_lo + b)) : 0ull;
+    }
+    warp_sort_desc<4>(x, lane);
+    uint64_t* out = cand + (((int64_t)seq * G + g) * splits + split) * kp;
+    if (lane < km1) out[lane] = x[0];  // k - 1 <= 32
+  } else if (warp < G) {
     const int g = warp;
     TopK<CAP> top;
     top.init(CAP);

@@ -280,6 +280,9 @@ DECODE_CASES = [
     ("dec_k20", 2, 9000, 8, 2, 64, 64, 64, 20, 2, [9000, 6100]),
     # k = 1: the local block only (no candidate lists)
     ("dec_k1", 2, 3000, 8, 2, 64, 64, 64, 1, 0, [3000, 1500]),
+    # about 133 candidate blocks per scan CTA in the first sequence (the register lists; up to 128 a CTA
+    # sorts its blocks across the warp) and about 112 in the second (the sort)
+    ("dec_cta_lists", 2, 1300000, 1, 1, 64, 32, 64, 4, 1, [1300000, 1100000]),
 ]
 
 
