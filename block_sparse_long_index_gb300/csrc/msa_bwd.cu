@@ -883,6 +883,13 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 // ... and have completed
 __device__ __forceinline__ void bulk_wait() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// fp32 add of `bytes` contiguous bytes of shared memory into global memory, by the TMA unit (bulk group);
+// both addresses 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
 }  // namespace tcb
 
 __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
@@ -1231,7 +1238,9 @@ constexpr int kChunkTiles = 8;
 constexpr int kRecs = kChunkTiles + 1;  // a chunk's records and the record after them (its run key)
 constexpr int kKI = 0, kQI = tcb::kTile, kDZ = 2 * tcb::kTile;
 constexpr int kLseBar = 2 * tcb::kTile, kLseBytes = 1024 + kLseBar + 64;
-constexpr int kGradBar = 3 * tcb::kTile, kGradBytes = 1024 + kGradBar + 64;
+// the gradient pass stages its dq^I rows over the query and dzI tiles at a 528-byte row stride
+constexpr int kStgRow = 528;
+constexpr int kGradBar = kQI + 128 * kStgRow, kGradBytes = 1024 + kGradBar + 64;
 constexpr uint32_t kIdescSS = tcb::kIdescSS, kIdescMnB = tcb::kIdescMnB, kIdescMnAB = tcb::kIdescMnAB;
 
 // Records [ti0, ti0 + kRecs) that lie below hi into dst: 16-byte cp.async pieces, threads 0 .. 8 kRecs - 1.
@@ -1460,6 +1469,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
   bool issued = false;
   for (int64_t ti0 = lo; ti0 < hi;) {
     cp_async_wait<0>();  // this chunk's records
+    tcb::bulk_wait_read();  // the previous chunk's dq^I reductions have read their staging
     __syncthreads();
     const TileRecord* RS = recs_s[slot];
     const Chunk ch = chunk_of(RS, ti0, hi);
@@ -1573,29 +1583,25 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     }
     if (sm100::mbar_wait(bar, phase & 1, abort, st, 0x805)) {
       sm100::tc_fence_after();
-      {  // thread = position: its dq^I row, staged through the (now free) query tile so that each warp adds
-         // two rows (1 KB of dq^I) per instruction; 16-byte unit u of row r sits at u ^ (r % 32)
+      {  // thread = position: its dq^I row, staged over the (now free) query and dzI tiles at a 528-byte
+         // stride (row-wise writes fall in distinct banks), then added to dq^I by one 512-byte bulk fp32
+         // add-reduction, which drains while the next chunk loads and computes
         uint32_t x[4][32];
 #pragma unroll
         for (int c32 = 0; c32 < 4; ++c32) sm100::tmem_ld_x32(tmem + lane_base + c32 * 32, x[c32]);
         sm100::tmem_ld_wait();
-        uint8_t* stg = sm + kQI;  // 128 rows x 512 bytes = the query tile and the dzI tile after it
+        uint8_t* row = sm + kQI + tid * kStgRow;
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
           const uint32_t* xs = &x[u >> 3][(u & 7) * 4];
-          *reinterpret_cast<float4*>(stg + tid * 512 + ((u ^ (tid & 31)) << 4)) =
+          *reinterpret_cast<float4*>(row + u * 16) =
               make_float4(sI * __uint_as_float(xs[0]), sI * __uint_as_float(xs[1]), sI * __uint_as_float(xs[2]),
                           sI * __uint_as_float(xs[3]));
         }
-        __syncwarp();
-        const int lane = tid & 31;
-#pragma unroll 4
-        for (int rr0 = 0; rr0 < 32; ++rr0) {  // row warp * 32 + rr0: lane = unit
-          const int rr = warp * 32 + rr0;
-          const float4 v = *reinterpret_cast<const float4*>(stg + rr * 512 + ((lane ^ (rr & 31)) << 4));
-          const int32_t tr = row_t(RS, ch.n, rr);
-          if (tr >= 0) tcb::red_add4(dq_idx + ((int64_t)tr * G + ch.g) * 128 + lane * 4, v.x, v.y, v.z, v.w);
-        }
+        sm100::fence_proxy_async_smem();
+        const int32_t tr = row_t(RS, ch.n, tid);
+        if (tr >= 0) tcb::bulk_reduce_add_f32(dq_idx + ((int64_t)tr * G + ch.g) * 128, smem_u32(row), 512);
+        tcb::bulk_commit();
       }
       if (ch.run_ends) {  // thread = key: the run's dk^I
         const int64_t j = (int64_t)ch.b * 128 + tid;
@@ -1622,6 +1628,7 @@ __global__ void __launch_bounds__(tci::kThreads, 2) bwd_index_tc_kernel(
     slot ^= 1;
   }
   cp_async_wait<0>();
+  tcb::bulk_wait();
   __syncthreads();
   if (warp == 0) {
     if ((tid & 31) == 0 && *abort && issued) {
