@@ -213,25 +213,6 @@ constexpr uint32_t kRegsProducers = 64, kRegsSoftmax = 168, kRegsEpilogue = 112;
 static_assert(4 * 32 * kRegsProducers + 8 * 32 * kRegsSoftmax + 4 * 32 * kRegsEpilogue == 512 * 128,
               "register split must add up to the launch's registers");
 
-// Packed pairs of fp32 (one 64-bit register): two lanes per instruction.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 
 // PPR = 8 / gs records (of 16 positions) per tile, a compile-time constant so
 // that each group size gets its own straight-line code.

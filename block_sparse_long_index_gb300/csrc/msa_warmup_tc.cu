@@ -128,25 +128,6 @@ __device__ __forceinline__ void tmem_st_x2(uint32_t taddr, const uint32_t (&r)[2
   asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1,%2};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1])
                : "memory");
 }
-// Packed pairs of fp32 (one 64-bit register): two lanes of arithmetic per instruction.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ float lg2_approx(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 // A bounded wait whose result every lane of the warp shares (warp-collective work follows it).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, DeviceStatus* st,
                                           unsigned code) {
@@ -428,20 +409,6 @@ constexpr uint32_t kTS = 0, kTO = 128, kCols = 256;
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128) | (1u << 16);  // V as MN-major B
 constexpr float kLazy = 8.0f;  // log2 units a row maximum may grow before O is rescaled
-// Packed pairs of fp32 (one 64-bit register): two lanes of arithmetic per instruction.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
 __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -585,14 +552,14 @@ __global__ void __launch_bounds__(wtf::kThreads, 2) warmup_fwd_tc_kernel(
       }
       float ls = 0.f;
       if (full) {
-        const uint64_t sl2x2 = wtf::f2_pack(sl2, sl2), nm2 = wtf::f2_pack(-m_used, -m_used);
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_used, -m_used);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {  // 32 keys at a time -> 16 packed columns
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             float a0, a1;
-            wtf::f2_unpack(wtf::f2_fma(wtf::f2_pack(__uint_as_float(x[cc][e]), __uint_as_float(x[cc][e + 1])), sl2x2,
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(x[cc][e]), __uint_as_float(x[cc][e + 1])), sl2x2,
                                        nm2),
                            a0, a1);
             a0 = ex2_approx(a0);
