@@ -28,7 +28,8 @@
 //               -> lse^I;
 //   main:       S^T, P^T, dP^T, dZ^T of the tile's keys and rows; dV and dK
 //               accumulated over the tiles of a (group, block) and flushed
-//               with fp32 reductions; dQ added to dq with fp32 reductions;
+//               with fp32 reductions; dQ added to dq with fp32 reductions
+//               (TMA add-reductions from shared memory on tcgen05);
 //               the teacher rows (mean P over each position's heads, bf16)
 //               written per tile;
 //   index:      the index logits again, dzI and the KL terms against the
@@ -807,8 +808,10 @@ size_t carve(int64_t N, int H_q, int G, int Bk, int k, void* base, BwdScratch* o
 //   (group, block) run; dQ = dZ K (M = rows: dZ^T read as an MN-major A; K
 //   as MN-major B) into columns 128-255 (dP^T is consumed by then; P^T in
 //   columns 0-127 stays untouched until the next tile's S^T);
-//   each thread adds 64 columns of its dQ row to dq, and at a run's end 64
-//   columns of its key's dK and dV to dk and dv, with fp32 vector reductions.
+//   each thread stages 64 columns of its dQ row in shared memory, which the
+//   TMA unit adds to dq (fp32 add-reductions of gs-head boxes, one per
+//   position and 32 columns); at a run's end each thread adds 64 columns of
+//   its key's dK and dV to dk and dv with fp32 vector reductions.
 // Q and dO rows are double-buffered: tile i+1's rows arrive by cp.async (and
 // its per-row position, lse and D into registers) while tile i computes.
 // Warp 4 owns TMEM and its lane 0 issues the MMAs.  Phases are separated by
@@ -1200,8 +1203,10 @@ __global__ void __launch_bounds__(kThreadsB, 1) bwd_main_tc_kernel(
 //              dk^I += dzI^T Q^I (dzI and Q^I read MN-major) accumulated in
 //              TMEM columns 128-255 over the run's chunks, flushed with fp32
 //              reductions at the run's end.
+//              Each thread adds its dq^I row to dq_idx with one 512-byte bulk
+//              fp32 add-reduction from shared memory.
 // The lse pass needs 128 TMEM columns and 64 KB of shared memory (three CTAs
-// per SM), the gradient pass 256 columns and 96 KB (two CTAs per SM); the
+// per SM), the gradient pass 256 columns and 98 KB (two CTAs per SM); the
 // CTAs of an SM overlap one another's loads and arithmetic.
 namespace tci {
 constexpr int kThreads = 128;
