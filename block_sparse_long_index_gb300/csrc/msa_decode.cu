@@ -8,13 +8,15 @@
 // Two launches per step:
 //   1. scan (+ merge): split-K over the cache, two 8-warp CTAs per SM.  Each
 //      warp streams an equal share of 16-key chunks straight from HBM into
-//      mma.sync A fragments (16-byte loads, one chunk in flight ahead of the
-//      one being scored; dims permuted consistently in the query fragments, so
+//      mma.sync A fragments (16-byte loads, one chunk (bf16) or three (E4M3)
+//      in flight ahead of the one being scored; dims permuted consistently in the query fragments, so
 //      no shared-memory staging is needed) and scores all groups at once
 //      (16 keys x 8 groups x d_I per mma chain).  Block maxima meet in shared
 //      memory (an atomic max on order-preserving integers joins the two parts
 //      of a block split between warps); each CTA then writes its top-(k-1)
-//      blocks per group as a list sorted best first.
+//      blocks per group as a list sorted best first (one warp-wide sort of
+//      its blocks when it holds at most 128, else register lists popped in
+//      k-1 rounds).
 //   2. select + attend (+ combine): per (sequence, group, slot) one CTA merges
 //      the group's lists up to its slot (every CTA of the group does the same
 //      merge, from shared memory, so no single CTA holds the others up), reads
